@@ -1,0 +1,396 @@
+"""Plain CPU oracle for indexer-routed sparse GQA attention.
+
+TEST INFRASTRUCTURE. Only the tests, the smoke check of ``__graft_entry__`` and
+the CPU-baseline / reference leg of ``bench.py`` may import or run this module.
+The CUDA library never calls it and it never calls the CUDA library: the two
+share no code. It is slow on purpose: every step is the plain definition,
+evaluated in float64 (except where the method itself fixes FP32), one query row
+at a time.
+
+Sources (NVIDIA NeMo AutoModel API reference pages):
+
+* "nemo_automodel.components.models.qwen3_8_flash_next.qsa" (the QSA page):
+  - ``Qwen3_8_FlashNextQSAIndexer`` class description: raw index keys
+    [B,S,1,D_index]; complete consecutive groups of ``compress_ratio`` keys are
+    averaged in FP32 into [B, floor(S/c), 1, D_index]; the route tensor is
+    [B, S, budget + c - 1].
+  - ``select_qsa_token_ids`` description: a query at position t sees
+    floor((t+1)/c) complete blocks; each block is scored by a sum over index
+    heads of ReLU(q_h . k_block); the best budget/c blocks are expanded to token
+    IDs and the 0..c-1 tokens of the current incomplete block are appended;
+    invalid slots are -1.
+  - ``_forward_packed`` description: with packed documents, compression groups
+    restart at each document start, visibility is bounded by the document, and
+    per-document IDs are offset by the document start (global flattened IDs).
+  - ``gathered_qsa_gqa_attention`` / ``_gathered_qsa_gqa_attention_chunk``:
+    grouped queries [B,Q,Hkv,G,D] attend K/V [B,S,Hkv,D] at the listed global
+    IDs; -1 marks invalid slots; the default scale is 1/sqrt(D).
+* "nemo_automodel.components.models.step5.sparse" (the Step-5 sparse page):
+  ``indexer_score_tile`` fuses weighted-ReLU scoring with FP32 per-head weights
+  into an FP32 score tile; ``pack_region_bitmap`` packs selected region IDs into
+  32-bit words.
+* "nemo_automodel.components.models.step5.fa4" (``heads_per_group``):
+  consecutive query heads share one KV group.
+* "nemo_automodel.components.models.common.cudnn_sparse_attention":
+  latent attention, q [Tq,H,576], kv_latent [Tk,1,576], values are the first
+  512 latent dims, int32 indices with -1 invalid.
+
+Readings where the pages are silent or loose (each one is listed in the design
+notes of the repository):
+
+* R1  The FP32 block mean is rounded once to bf16 (round to nearest even)
+      before it is used as a scoring operand (the scores are tensor-core dot
+      products of bf16 operands).
+* R2  The block score is sum_h w[t,h] * ReLU(q[t,h] . k~[b]) with no extra
+      1/sqrt(D) factor: a caller who wants one folds it into w.
+* R3  Top-k ties go to the lower block index; -0.0 equals +0.0.
+* R4  A route row has fixed sections: slots [0, budget) hold the selected blocks
+      in ascending block order, c tokens each, then -1; slots
+      [budget, budget+c-1) hold the incomplete-block tail tokens, then -1.
+* R5  When (tau+1) % c == 0 the query's own block is complete and competes in
+      the top-k like any other block; the tail is then empty.
+* R6  Unstated softmax scales are 1/sqrt(D_qk).
+* R7  A row with no valid route entry produces out = 0 and lse = -inf.
+* The FP32 mean is a sequential FP32 sum over the c rows of the block in
+  ascending token order, followed by one IEEE division by c.
+* Route entries outside [0, Tk) are padding.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+# --------------------------------------------------------------------------------------
+# bf16 helpers (bit patterns are numpy uint16)
+# --------------------------------------------------------------------------------------
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact value of bf16 bit patterns, as float64."""
+    u = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    u = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32)
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Nearest bf16 value of each float32 in `x`, ties to even mantissa (reading R1).
+
+    Written from the definition: the two bf16 neighbours of x are the float32
+    patterns with the low 16 bits cleared (toward zero) and that plus one bf16
+    ulp (away from zero); pick the nearer one in exact float64 arithmetic, and
+    on a tie the one whose last kept mantissa bit is 0. Returns float32 values.
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    bits = x.view(np.uint32)
+    lo_bits = bits & np.uint32(0xFFFF0000)
+    hi_bits = lo_bits + np.uint32(0x10000)
+    lo = lo_bits.view(np.float32).astype(np.float64)
+    hi = hi_bits.view(np.float32).astype(np.float64)
+    xv = x.astype(np.float64)
+    d_lo = np.abs(xv - lo)
+    d_hi = np.abs(hi - xv)
+    lo_even = ((lo_bits >> np.uint32(16)) & np.uint32(1)) == 0
+    pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & lo_even)
+    return np.where(pick_lo, lo_bits, hi_bits).view(np.float32)
+
+
+# --------------------------------------------------------------------------------------
+# a1: document layout (QSA page, `_forward_packed`: cu_seqlens strictly increasing,
+# starting at zero and ending at T)
+# --------------------------------------------------------------------------------------
+
+
+def doc_bounds(cu_seqlens: np.ndarray, T: int) -> tuple[np.ndarray, np.ndarray]:
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    if cu.ndim != 1 or cu.shape[0] < 2:
+        raise ValueError("cu_seqlens must be 1-D with at least two entries")
+    if cu[0] != 0 or cu[-1] != T or np.any(cu[1:] <= cu[:-1]):
+        raise ValueError("cu_seqlens must be strictly increasing from 0 to T")
+    return cu[:-1].copy(), cu[1:].copy()
+
+
+def doc_of_token(cu_seqlens: np.ndarray, t: int) -> int:
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    return int(np.searchsorted(cu, t, side="right") - 1)
+
+
+# --------------------------------------------------------------------------------------
+# a2: block mean-pool (QSA page, indexer class description)
+# --------------------------------------------------------------------------------------
+
+
+def pool_doc(kI_doc_f32: np.ndarray, c: int) -> np.ndarray:
+    """FP32 means of the complete consecutive groups of `c` rows of one document.
+
+    Each block is summed row by row in ascending token order in float32, then
+    divided once by c in float32. Returns float32 [floor(L/c), Di].
+    """
+    L, Di = kI_doc_f32.shape
+    nb = L // c
+    x = np.asarray(kI_doc_f32, dtype=np.float32)
+    acc = np.zeros((nb, Di), dtype=np.float32)
+    for j in range(c):                               # row j of every block, in token order
+        acc = (acc + x[j: nb * c: c]).astype(np.float32)
+    return (acc / np.float32(c)).astype(np.float32)
+
+
+def pool_keys(kI_bits: np.ndarray, cu_seqlens: np.ndarray, c: int) -> tuple[np.ndarray, np.ndarray]:
+    """Pooled keys of every document, concatenated; and the per-document block offsets."""
+    T = kI_bits.shape[0]
+    starts, ends = doc_bounds(cu_seqlens, T)
+    kI = bf16_to_f32(kI_bits)
+    blocks = []
+    blk_off = [0]
+    for s, e in zip(starts, ends):
+        p = pool_doc(kI[s:e], c)
+        blocks.append(p)
+        blk_off.append(blk_off[-1] + p.shape[0])
+    Di = kI_bits.shape[1]
+    kbar = np.concatenate(blocks, axis=0) if blocks else np.zeros((0, Di), np.float32)
+    return kbar, np.asarray(blk_off, dtype=np.int64)
+
+
+# --------------------------------------------------------------------------------------
+# a3: visibility and block scores (QSA page `select_qsa_token_ids`; Step-5 sparse page
+# `indexer_score_tile` for the per-head FP32 weights)
+# --------------------------------------------------------------------------------------
+
+
+def visible_blocks(tau: int, c: int) -> int:
+    """Complete blocks visible to a query at document-local position tau."""
+    return (tau + 1) // c
+
+
+def block_scores(qI_t: np.ndarray, w_t: np.ndarray, ktilde: np.ndarray) -> np.ndarray:
+    """score[b] = sum_h w[h] * ReLU(sum_d qI[h,d] * k~[b,d]), float64, rounded once to float32.
+
+    qI_t: float64 [Hi, Di]; w_t: float64 [Hi]; ktilde: float64 [n, Di] (bf16 values).
+    """
+    dots = qI_t @ ktilde.T                      # [Hi, n]
+    relu = np.maximum(dots, 0.0)
+    s = w_t @ relu                              # [n]
+    return s.astype(np.float32)
+
+
+# --------------------------------------------------------------------------------------
+# a4: top-k (reading R3) and a5: bitmap + expansion (reading R4)
+# --------------------------------------------------------------------------------------
+
+
+def select_top(scores_f32: np.ndarray, kb: int) -> np.ndarray:
+    """Indices of the kb largest scores, ties to the lower index, in ascending order."""
+    s = np.asarray(scores_f32, dtype=np.float32).astype(np.float64)
+    n = s.shape[0]
+    if n <= kb:
+        return np.arange(n, dtype=np.int64)
+    order = np.lexsort((np.arange(n), -s))     # primary: score descending; then index ascending
+    return np.sort(order[:kb])
+
+
+def pack_bitmap(selected: np.ndarray, nblocks: int) -> np.ndarray:
+    """32-bit words, bit (b % 32) of word b // 32 set for each selected block b."""
+    words = np.zeros((nblocks + 31) // 32, dtype=np.uint32)
+    for b in selected:
+        words[b // 32] |= np.uint32(1) << np.uint32(b % 32)
+    return words
+
+
+def unpack_bitmap(words: np.ndarray, nblocks: int) -> np.ndarray:
+    out = []
+    for b in range(nblocks):
+        if (int(words[b // 32]) >> (b % 32)) & 1:
+            out.append(b)
+    return np.asarray(out, dtype=np.int64)
+
+
+def expand_route(doc_start: int, tau: int, c: int, budget: int, selected: np.ndarray) -> np.ndarray:
+    """One route row [budget + c - 1] in global token IDs (reading R4)."""
+    W = budget + c - 1
+    row = np.full(W, -1, dtype=np.int32)
+    slot = 0
+    for b in selected:
+        for j in range(c):
+            row[slot] = doc_start + int(b) * c + j
+            slot += 1
+    nv = visible_blocks(tau, c)
+    tail = (tau + 1) % c
+    for j in range(tail):
+        row[budget + j] = doc_start + nv * c + j
+    return row
+
+
+def route_row(doc_start: int, tau: int, c: int, budget: int, scores_f32) -> np.ndarray:
+    """Route of one query from its block scores (None when every visible block is taken)."""
+    kb = budget // c
+    nv = visible_blocks(tau, c)
+    if nv <= kb:
+        selected = np.arange(nv, dtype=np.int64)
+    else:
+        selected = select_top(scores_f32, kb)
+        selected = unpack_bitmap(pack_bitmap(selected, nv), nv)
+    return expand_route(doc_start, tau, c, budget, selected)
+
+
+def index_routes(qI_bits, kI_bits, w, cu_seqlens, c: int, budget: int, rows=None,
+                 want_scores: bool = False, ldS: int | None = None):
+    """Indexer routes (and optionally FP32 block scores) for the requested rows.
+
+    qI_bits [T, Hi, Di] bf16 bits, kI_bits [T, Di] bf16 bits, w [T, Hi] float32,
+    cu_seqlens int [ndocs+1]. Returns int32 routes [len(rows), budget + c - 1];
+    with want_scores also float32 scores [len(rows), ldS] (NaN where not scored:
+    a row is scored only when more than budget/c blocks are visible).
+    """
+    if budget % c != 0 or budget <= 0 or c <= 0:
+        raise ValueError("budget must be a positive multiple of c")
+    T = qI_bits.shape[0]
+    starts, ends = doc_bounds(cu_seqlens, T)
+    rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
+    kb = budget // c
+    W = budget + c - 1
+    kbar, blk_off = pool_keys(kI_bits, cu_seqlens, c)
+    ktilde = round_to_bf16(kbar).astype(np.float64)
+    if ldS is None:
+        ldS = int(np.max(ends - starts)) // c
+    routes = np.full((rows.shape[0], W), -1, dtype=np.int32)
+    scores = np.full((rows.shape[0], max(ldS, 1)), np.nan, dtype=np.float32) if want_scores else None
+    for i, t in enumerate(rows):
+        d = doc_of_token(cu_seqlens, int(t))
+        s = int(starts[d])
+        tau = int(t) - s
+        nv = visible_blocks(tau, c)
+        sc = None
+        if nv > kb:
+            kt = ktilde[blk_off[d]: blk_off[d] + nv]
+            sc = block_scores(bf16_to_f64(qI_bits[t]), np.asarray(w[t], dtype=np.float64), kt)
+            if want_scores:
+                scores[i, :nv] = sc
+        routes[i] = route_row(s, tau, c, budget, sc)
+    return (routes, scores) if want_scores else routes
+
+
+def routes_from_scores(scores: np.ndarray, cu_seqlens, T: int, c: int, budget: int, rows=None) -> np.ndarray:
+    """Routes from given float32 scores [T, ldS] (entries [0, nvis) of sparse rows are read)."""
+    starts, _ = doc_bounds(cu_seqlens, T)
+    rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
+    kb = budget // c
+    out = np.full((rows.shape[0], budget + c - 1), -1, dtype=np.int32)
+    for i, t in enumerate(rows):
+        d = doc_of_token(cu_seqlens, int(t))
+        s = int(starts[d])
+        tau = int(t) - s
+        nv = visible_blocks(tau, c)
+        sc = scores[t, :nv] if nv > kb else None
+        out[i] = route_row(s, tau, c, budget, sc)
+    return out
+
+
+# --------------------------------------------------------------------------------------
+# a5': sliding window in front of the indexer route (Step-5 layers page: attention is
+# windowed or CSA-selected; the windowed workload uses both)
+# --------------------------------------------------------------------------------------
+
+
+def compose_window(routes: np.ndarray, cu_seqlens, T: int, window: int, rows=None) -> np.ndarray:
+    """[window causal tokens t-window+1..t (-1 before the document start)] ++ the
+    indexer route with every ID already inside the window replaced by -1.
+
+    `routes` is the full indexer route tensor [T, W]; `rows` selects output rows.
+    """
+    starts, _ = doc_bounds(cu_seqlens, T)
+    rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
+    W = routes.shape[1]
+    out = np.full((rows.shape[0], window + W), -1, dtype=np.int32)
+    for i, t in enumerate(rows):
+        d = doc_of_token(cu_seqlens, int(t))
+        s = int(starts[d])
+        lo = int(t) - window + 1
+        for j in range(window):
+            tok = lo + j
+            out[i, j] = tok if tok >= s else -1
+        r = routes[t]
+        for j in range(W):
+            out[i, window + j] = r[j] if r[j] < lo else -1
+    return out
+
+
+# --------------------------------------------------------------------------------------
+# a6: gathered sparse GQA attention (QSA page `gathered_qsa_gqa_attention`; latent
+# attention page for the MLA case)
+# --------------------------------------------------------------------------------------
+
+
+def kv_group(h: int, Hq: int, Hkv: int) -> int:
+    """KV head of query head h: consecutive query heads share one KV group."""
+    return h // (Hq // Hkv)
+
+
+def attend_row(q_t: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float, Hkv: int):
+    """One query row over its gathered keys.
+
+    q_t float64 [Hq, Dqk]; K float64 [n, Hkv, Dqk]; V float64 [n, Hkv, Dv].
+    Returns out float64 [Hq, Dv], lse float64 [Hq] (natural log).
+    """
+    Hq = q_t.shape[0]
+    Dv = V.shape[2]
+    n = K.shape[0]
+    out = np.zeros((Hq, Dv), dtype=np.float64)
+    lse = np.full(Hq, -np.inf, dtype=np.float64)
+    if n == 0:
+        return out, lse                          # reading R7
+    for h in range(Hq):
+        g = kv_group(h, Hq, Hkv)
+        s = scale * (K[:, g, :] @ q_t[h])        # [n]
+        m = np.max(s)
+        p = np.exp(s - m)
+        l = np.sum(p)
+        out[h] = (p @ V[:, g, :]) / l
+        lse[h] = m + math.log(l)
+    return out, lse
+
+
+def attention(q_bits, k_bits, v_bits, routes, scale: float, rows=None):
+    """Sparse attention of the requested rows.
+
+    q_bits [T, Hq, Dqk], k_bits [Tk, Hkv, Dqk], v_bits [Tk, Hkv, Dv] (bf16 bits),
+    routes int32 [T, W] global key IDs (anything outside [0, Tk) is padding).
+    Returns out float32 [len(rows), Hq, Dv] and lse float32 [len(rows), Hq].
+    """
+    T, Hq, _ = q_bits.shape
+    Tk, Hkv, _ = k_bits.shape
+    Dv = v_bits.shape[2]
+    if Hq % Hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    if not scale > 0:
+        raise ValueError("scale must be positive")
+    rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
+    out = np.zeros((rows.shape[0], Hq, Dv), dtype=np.float32)
+    lse = np.zeros((rows.shape[0], Hq), dtype=np.float32)
+    for i, t in enumerate(rows):
+        ids = np.asarray(routes[t], dtype=np.int64)
+        ids = ids[(ids >= 0) & (ids < Tk)]
+        K = bf16_to_f64(k_bits[ids])
+        V = bf16_to_f64(v_bits[ids])
+        o, l = attend_row(bf16_to_f64(q_bits[t]), K, V, scale, Hkv)
+        out[i] = o.astype(np.float32)
+        lse[i] = l.astype(np.float32)
+    return out, lse
+
+
+def latent_attention(q_bits, kv_bits, routes, scale: float, Dv: int = 512, rows=None):
+    """Latent (MLA) attention: keys are the full latent rows, values their first Dv dims."""
+    return attention(q_bits, kv_bits, kv_bits[:, :, :Dv], routes, scale, rows=rows)
+
+
+# --------------------------------------------------------------------------------------
+# counts used by the benchmark's roofline (algorithmic, from the definitions above)
+# --------------------------------------------------------------------------------------
+
+
+def valid_pairs(routes: np.ndarray, Tk: int) -> int:
+    r = np.asarray(routes)
+    return int(np.count_nonzero((r >= 0) & (r < Tk)))

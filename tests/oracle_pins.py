@@ -1,0 +1,505 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each ``pin_*`` takes the oracle module ``O`` and raises ``AssertionError`` when
+the oracle disagrees with what the reference pages or mathematics fix:
+hand-worked examples from the pages' rules (tests/golden), brute-force
+enumeration, closed forms, library routines (torch SDPA, torch's bf16 cast,
+numpy's bit packing) and invariants. ``test_oracle_pins`` runs them on the real
+oracle; ``test_oracle_mutations`` plants mistakes in the oracle and checks that
+some pin fails.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------------------
+# helpers (no method arithmetic beyond what each pin states)
+# --------------------------------------------------------------------------------------
+
+
+def exact_bf16_bits(values) -> np.ndarray:
+    """bf16 bits of values that are exactly representable (fixtures)."""
+    x = np.asarray(values, dtype=np.float32)
+    bits = x.view(np.uint32)
+    assert np.all(bits & np.uint32(0xFFFF) == 0), "fixture value not exact in bf16"
+    return (bits >> np.uint32(16)).astype(np.uint16)
+
+
+def torch_bf16_bits(x_f32: np.ndarray) -> np.ndarray:
+    """Library rounding: torch's float32 -> bfloat16 cast (round to nearest even)."""
+    t = torch.from_numpy(np.ascontiguousarray(x_f32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_to_f64(bits) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16)).view(
+        torch.bfloat16).to(torch.float64).numpy()
+
+
+def parse_fixture(name: str) -> list[tuple[str, list[str]]]:
+    out = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            out.append((key, vals))
+    return out
+
+
+def doc_start_of(cu, t):
+    cu = list(int(x) for x in cu)
+    for d in range(len(cu) - 1):
+        if cu[d] <= t < cu[d + 1]:
+            return cu[d], cu[d + 1]
+    raise AssertionError("token outside documents")
+
+
+def small_case(seed: int, T: int, Hq: int, Hkv: int, Dqk: int, Dv: int, Hi: int, Di: int,
+               doc_lens, w_kind="uniform"):
+    import irs_synth
+
+    return irs_synth.custom(T, Hq, Hkv, Dqk, Dv, Hi, Di, c=4, budget=8, doc_lens=doc_lens, seed=seed,
+                            w_kind=w_kind)
+
+
+# --------------------------------------------------------------------------------------
+# golden, hand-worked examples
+# --------------------------------------------------------------------------------------
+
+
+def pin_golden_two_docs(O):
+    recs = parse_fixture("route_two_docs.txt")
+    d = {}
+    routes_by_budget = {}
+    budget = None
+    for key, vals in recs:
+        if key == "budget":
+            budget = int(vals[0])
+            routes_by_budget[budget] = {}
+        elif key == "route":
+            routes_by_budget[budget][int(vals[0])] = [int(v) for v in vals[1:]]
+        else:
+            d[key] = vals
+    c = int(d["c"][0])
+    cu = np.asarray([int(v) for v in d["cu_seqlens"]], dtype=np.int32)
+    k0 = [float(v) for v in d["kI0"]]
+    k1 = [float(v) for v in d["kI1"]]
+    T = len(k0)
+    kI = exact_bf16_bits(np.stack([k0, k1], axis=1))
+    qI = exact_bf16_bits(np.tile(np.asarray([[[1.0, 0.0]]], np.float32), (T, 1, 1)))
+    w = np.ones((T, 1), dtype=np.float32)
+    for b, expect in routes_by_budget.items():
+        got = O.index_routes(qI, kI, w, cu, c, b)
+        for t, row in expect.items():
+            assert got[t].tolist() == row, f"budget {b} t {t}: {got[t].tolist()} != {row}"
+        assert got.shape == (T, b + c - 1)
+
+
+def pin_golden_head_weights(O):
+    recs = dict((k, v) for k, v in parse_fixture("route_head_weights.txt") if k != "route")
+    routes = {int(v[0]): [int(x) for x in v[1:]] for k, v in parse_fixture("route_head_weights.txt")
+              if k == "route"}
+    c = int(recs["c"][0])
+    budget = int(recs["budget"][0])
+    cu = np.asarray([int(v) for v in recs["cu_seqlens"]], dtype=np.int32)
+    kI = exact_bf16_bits(np.asarray([float(v) for v in recs["kI_rows"]], np.float32).reshape(-1, 2))
+    T = kI.shape[0]
+    w = np.tile(np.asarray([[float(v) for v in recs["w"]]], np.float32), (T, 1))
+    qI = exact_bf16_bits(np.tile(np.asarray([[[1.0, 0.0], [0.0, 1.0]]], np.float32), (T, 1, 1)))
+    got, scores = O.index_routes(qI, kI, w, cu, c, budget, want_scores=True)
+    for t, row in routes.items():
+        assert got[t].tolist() == row, f"t {t}: {got[t].tolist()} != {row}"
+    t_s = int(recs["scores_at"][0])
+    expect = [float(v) for v in recs["scores_at"][1:]]
+    assert scores[t_s, :len(expect)].tolist() == expect
+
+
+# --------------------------------------------------------------------------------------
+# top-k: brute force over all subsets
+# --------------------------------------------------------------------------------------
+
+
+def brute_force_topk(scores, kb):
+    """Max-sum subset of size kb; among equal sums the lexicographically smallest sorted tuple."""
+    n = len(scores)
+    if n <= kb:
+        return tuple(range(n))
+    best, best_sum = None, None
+    for sub in itertools.combinations(range(n), kb):
+        s = math.fsum(float(scores[i]) for i in sub)   # exact: few float32 terms
+        if best is None or s > best_sum or (s == best_sum and sub < best):
+            best, best_sum = sub, s
+    return best
+
+
+def pin_topk_bruteforce(O):
+    rng = np.random.default_rng(123)
+    for trial in range(200):
+        n = int(rng.integers(1, 13))
+        kb = int(rng.integers(1, 5))
+        if trial % 3 == 0:
+            s = rng.choice(np.asarray([0.0, -0.0, 0.5, 1.0, 2.0], np.float32), size=n).astype(np.float32)
+        else:
+            s = rng.standard_normal(n).astype(np.float32)
+        got = tuple(int(x) for x in O.select_top(s, kb))
+        assert got == brute_force_topk(s, kb), (s, kb, got)
+
+
+def pin_routes_from_scores_bruteforce(O):
+    """Whole route rows from given scores: blocks = brute-force argmax set, tail per the page."""
+    rng = np.random.default_rng(7)
+    c, budget = 2, 6          # kb = 3
+    cu = np.asarray([0, 13, 24], np.int32)
+    T = 24
+    ldS = 6
+    scores = rng.choice(np.asarray([0.0, 1.0, 2.0, 3.0], np.float32), size=(T, ldS)).astype(np.float32)
+    got = O.routes_from_scores(scores, cu, T, c, budget)
+    kb = budget // c
+    for t in range(T):
+        s, _ = doc_start_of(cu, t)
+        tau = t - s
+        nv = (tau + 1) // c
+        blocks = brute_force_topk(scores[t, :nv], kb) if nv > kb else tuple(range(nv))
+        expect_ids = sorted(s + b * c + j for b in blocks for j in range(c))
+        row = got[t]
+        assert row[:len(expect_ids)].tolist() == expect_ids, (t, row)
+        assert np.all(row[len(expect_ids):budget] == -1)
+        tail = [s + nv * c + j for j in range((tau + 1) % c)]
+        assert row[budget:budget + len(tail)].tolist() == tail
+        assert np.all(row[budget + len(tail):] == -1)
+
+
+# --------------------------------------------------------------------------------------
+# route invariants on random multi-document inputs
+# --------------------------------------------------------------------------------------
+
+
+def check_route_invariants(routes, cu, c, budget, rows=None):
+    T = routes.shape[0] if rows is None else None
+    rows = range(routes.shape[0]) if rows is None else rows
+    kb = budget // c
+    assert routes.shape[1] == budget + c - 1
+    for i, t in enumerate(rows):
+        row = routes[i]
+        s, e = doc_start_of(cu, t)
+        tau = t - s
+        nv = (tau + 1) // c
+        valid = row[row >= 0]
+        assert np.all((valid >= s) & (valid <= t)), f"t {t}: route leaves [doc start, t]"
+        assert len(set(valid.tolist())) == valid.shape[0], "duplicate IDs"
+        assert valid.shape[0] == min(nv, kb) * c + (tau + 1) % c, f"t {t}: valid count"
+        blk = row[:budget]
+        bv = blk[blk >= 0]
+        assert bv.shape[0] == min(nv, kb) * c
+        assert np.all(blk[bv.shape[0]:] == -1), "block section not a valid prefix"
+        starts = bv[::c]
+        assert np.all((starts - s) % c == 0), "block not c-aligned to the document start"
+        assert np.all(np.diff(starts) > 0), "blocks not ascending"
+        for j in range(c):
+            assert np.all(bv[j::c] == starts + j), "block not expanded to c consecutive tokens"
+        assert np.all(starts + c - 1 < s + nv * c), "block not complete or not visible"
+        tail = row[budget:]
+        ntail = (tau + 1) % c
+        assert tail[:ntail].tolist() == list(range(s + nv * c, t + 1)), "tail tokens"
+        assert np.all(tail[ntail:] == -1)
+    return T
+
+
+def pin_route_invariants(O):
+    for seed, lens in ((1, [37, 5, 64, 22]), (2, [128]), (3, [1, 2, 3, 4, 50, 3])):
+        T = sum(lens)
+        for c, budget in ((4, 8), (4, 16), (1, 3), (3, 9)):
+            wl = small_case(seed, T, 2, 1, 8, 8, 3, 8, lens)
+            r = O.index_routes(wl.arrays["qI"], wl.arrays["kI"], wl.arrays["w"], wl.cu_seqlens, c, budget)
+            check_route_invariants(r, wl.cu_seqlens, c, budget)
+
+
+def pin_dense_budget_routes(O):
+    """budget >= document length: every causal token of the document is routed."""
+    lens = [19, 33, 12]
+    T = sum(lens)
+    wl = small_case(5, T, 2, 1, 8, 8, 2, 8, lens)
+    for c in (1, 2, 4):
+        budget = 36 if c != 1 else 34
+        budget -= budget % c
+        r = O.index_routes(wl.arrays["qI"], wl.arrays["kI"], wl.arrays["w"], wl.cu_seqlens, c, budget)
+        for t in range(T):
+            s, _ = doc_start_of(wl.cu_seqlens, t)
+            v = np.sort(r[t][r[t] >= 0])
+            assert v.tolist() == list(range(s, t + 1)), (c, t)
+
+
+# --------------------------------------------------------------------------------------
+# block scores: closed forms and symmetries
+# --------------------------------------------------------------------------------------
+
+
+def pin_score_closed_form(O):
+    """One-hot index query and weight: score_b = w * ReLU(bf16(mean of block column d0))."""
+    rng = np.random.default_rng(11)
+    T, Hi, Di, c = 40, 3, 8, 4
+    kI_vals = (rng.integers(-64, 64, size=(T, Di)) / 8.0).astype(np.float32)   # block sums exact
+    kI = exact_bf16_bits(kI_vals)
+    cu = np.asarray([0, 17, 40], np.int32)
+    for h0, d0 in ((0, 3), (2, 7), (1, 0)):
+        qI_vals = np.zeros((T, Hi, Di), np.float32)
+        qI_vals[:, h0, d0] = 1.0
+        qI_vals[:, (h0 + 1) % Hi, :] = 0.0
+        w = np.zeros((T, Hi), np.float32)
+        w[:, h0] = 0.75
+        _, sc = O.index_routes(exact_bf16_bits(qI_vals), kI, w, cu, c, 4, want_scores=True)
+        for t in range(T):
+            s, _ = doc_start_of(cu, t)
+            nv = (t - s + 1) // c
+            if nv <= 1:
+                continue
+            for b in range(nv):
+                m = sum(Fraction(float(kI_vals[s + b * c + j, d0])) for j in range(c)) / c
+                mb = bits_to_f64(torch_bf16_bits(np.asarray([float(m)], np.float32)))[0]
+                assert sc[t, b] == np.float32(0.75 * max(mb, 0.0)), (t, b, sc[t, b], mb)
+
+
+def pin_score_symmetries(O):
+    wl = small_case(9, 48, 2, 1, 8, 8, 4, 16, [48])
+    qI, kI, w, cu = wl.arrays["qI"], wl.arrays["kI"], wl.arrays["w"], wl.cu_seqlens
+    c, budget = 4, 4
+    _, s0 = O.index_routes(qI, kI, w, cu, c, budget, want_scores=True)
+    # permuting index heads together with their weights leaves scores unchanged
+    perm_h = np.asarray([2, 0, 3, 1])
+    _, s1 = O.index_routes(qI[:, perm_h], kI, w[:, perm_h], cu, c, budget, want_scores=True)
+    np.testing.assert_allclose(s1, s0, rtol=1e-6, atol=0)
+    # permuting feature dims of queries and keys together leaves scores unchanged
+    perm_d = np.random.default_rng(0).permutation(16)
+    _, s2 = O.index_routes(qI[:, :, perm_d], kI[:, perm_d], w, cu, c, budget, want_scores=True)
+    np.testing.assert_allclose(s2, s0, rtol=1e-6, atol=0)
+    # doubling the weights doubles the scores exactly
+    _, s3 = O.index_routes(qI, kI, (w * np.float32(2)).astype(np.float32), cu, c, budget, want_scores=True)
+    np.testing.assert_array_equal(s3, s0 * np.float32(2))
+
+
+def pin_bf16_rounding(O):
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(20000).astype(np.float32) * np.float32(10.0)
+    # exact ties: low 16 bits == 0x8000, both parities of the last kept bit, both signs
+    base = rng.standard_normal(4000).astype(np.float32).view(np.uint32) & np.uint32(0xFFFF0000)
+    ties = (base | np.uint32(0x8000)).view(np.float32)
+    ties_odd = ((base | np.uint32(0x10000)) | np.uint32(0x8000)).view(np.float32)
+    x = np.concatenate([x, ties, ties_odd, -ties])
+    got = O.round_to_bf16(x).view(np.uint32) >> np.uint32(16)
+    ref = torch_bf16_bits(x).astype(np.uint32)
+    np.testing.assert_array_equal(got, ref)
+
+
+def pin_pool_mean(O):
+    rng = np.random.default_rng(5)
+    lens = [7, 13, 9]
+    T, Di = sum(lens), 6
+    cu = np.asarray([0, 7, 20, 29], np.int32)
+    vals = rng.standard_normal((T, Di)).astype(np.float32)
+    kI = torch_bf16_bits(vals)
+    kf = bits_to_f64(kI)
+    for c in (1, 2, 3, 4):
+        kbar, blk_off = O.pool_keys(kI, cu, c)
+        assert blk_off.tolist() == [0] + list(np.cumsum([L // c for L in lens]))
+        for d, L in enumerate(lens):
+            s = int(cu[d])
+            for b in range(L // c):
+                got = kbar[blk_off[d] + b]
+                exact = [sum(Fraction(float(kf[s + b * c + j, i])) for j in range(c)) / c for i in range(Di)]
+                for i in range(Di):
+                    e = float(exact[i])
+                    mag = float(sum(abs(Fraction(float(kf[s + b * c + j, i]))) for j in range(c)) / c)
+                    assert abs(float(got[i]) - e) <= (c + 1) * 2.0 ** -24 * c * mag + 1e-38, (c, d, b, i)
+    # a constant group pools exactly to the constant
+    kc = exact_bf16_bits(np.full((8, 2), 1.5, np.float32))
+    kbar, _ = O.pool_keys(kc, np.asarray([0, 8], np.int32), 4)
+    assert np.all(kbar == np.float32(1.5))
+
+
+def pin_bitmap(O):
+    rng = np.random.default_rng(2)
+    for n in (1, 31, 32, 33, 100):
+        sel = np.sort(rng.choice(n, size=min(n, 7), replace=False))
+        words = O.pack_bitmap(sel, n)
+        flags = np.zeros(((n + 31) // 32) * 32, np.uint8)
+        flags[sel] = 1
+        ref = np.packbits(flags, bitorder="little").view(np.uint8)
+        ref_words = np.frombuffer(ref.tobytes(), dtype="<u4")
+        np.testing.assert_array_equal(words, ref_words)
+        np.testing.assert_array_equal(O.unpack_bitmap(words, n), sel)
+
+
+# --------------------------------------------------------------------------------------
+# attention: library routine (torch SDPA) on the same gathered sets, and invariants
+# --------------------------------------------------------------------------------------
+
+
+def sdpa_masked(q_bits, k_bits, v_bits, routes, scale):
+    """Reference: dense SDPA over all keys with a boolean mask built from the routes."""
+    q = torch.from_numpy(bits_to_f64(q_bits))           # [T, Hq, D]
+    k = torch.from_numpy(bits_to_f64(k_bits))           # [Tk, Hkv, D]
+    v = torch.from_numpy(bits_to_f64(v_bits))
+    T, Hq, _ = q.shape
+    Tk, Hkv, _ = k.shape
+    G = Hq // Hkv
+    allowed = torch.zeros(T, Tk, dtype=torch.bool)
+    for t in range(T):
+        ids = [int(x) for x in routes[t] if 0 <= int(x) < Tk]
+        allowed[t, ids] = True
+    kk = k.repeat_interleave(G, dim=1).permute(1, 0, 2)    # [Hq, Tk, D]
+    vv = v.repeat_interleave(G, dim=1).permute(1, 0, 2)
+    qq = q.permute(1, 0, 2)                                 # [Hq, T, D]
+    out = torch.nn.functional.scaled_dot_product_attention(
+        qq, kk, vv, attn_mask=allowed.unsqueeze(0), scale=scale)
+    scores = (qq @ kk.transpose(1, 2)) * scale
+    scores = scores.masked_fill(~allowed.unsqueeze(0), float("-inf"))
+    lse = torch.logsumexp(scores, dim=-1)                   # [Hq, T]
+    return out.permute(1, 0, 2).numpy(), lse.T.numpy()
+
+
+def pin_attention_vs_sdpa(O):
+    import irs_synth
+
+    for seed, (Hq, Hkv, Dqk, Dv), lens in ((1, (4, 2, 16, 8), [40]), (2, (6, 3, 8, 16), [10, 25, 15]),
+                                            (3, (4, 1, 24, 24), [3, 47])):
+        T = sum(lens)
+        wl = irs_synth.custom(T, Hq, Hkv, Dqk, Dv, 2, 8, 4, 8, doc_lens=lens, seed=seed)
+        rng = np.random.default_rng(seed)
+        routes = irs_synth.random_routes(rng, T, T, 12, wl.cu_seqlens)
+        scale = 0.3
+        out, lse = O.attention(wl.arrays["q"], wl.arrays["k"], wl.arrays["v"], routes, scale)
+        ref_o, ref_l = sdpa_masked(wl.arrays["q"], wl.arrays["k"], wl.arrays["v"], routes, scale)
+        np.testing.assert_allclose(out, ref_o, rtol=1e-5, atol=1e-6)
+        np.testing.assert_allclose(lse, ref_l, rtol=1e-5, atol=1e-6)
+
+
+def pin_dense_causal_attention(O):
+    """budget >= document length: indexer routes + attention == dense causal varlen GQA."""
+    import irs_synth
+
+    lens = [24, 9, 31]
+    T = sum(lens)
+    wl = irs_synth.custom(T, 4, 2, 16, 16, 2, 8, 4, 32, doc_lens=lens, seed=4)
+    r = O.index_routes(wl.arrays["qI"], wl.arrays["kI"], wl.arrays["w"], wl.cu_seqlens, 4, 32)
+    out, lse = O.attention(wl.arrays["q"], wl.arrays["k"], wl.arrays["v"], r, 0.25)
+    q = torch.from_numpy(bits_to_f64(wl.arrays["q"]))
+    k = torch.from_numpy(bits_to_f64(wl.arrays["k"])).repeat_interleave(2, dim=1)
+    v = torch.from_numpy(bits_to_f64(wl.arrays["v"])).repeat_interleave(2, dim=1)
+    cu = wl.cu_seqlens
+    for d in range(len(lens)):
+        s, e = int(cu[d]), int(cu[d + 1])
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q[s:e].permute(1, 0, 2), k[s:e].permute(1, 0, 2), v[s:e].permute(1, 0, 2),
+            is_causal=True, scale=0.25).permute(1, 0, 2).numpy()
+        np.testing.assert_allclose(out[s:e], ref, rtol=1e-5, atol=1e-6)
+
+
+def pin_attention_invariants(O):
+    import irs_synth
+
+    T, Hq, Hkv, D = 24, 4, 2, 16
+    wl = irs_synth.custom(T, Hq, Hkv, D, D, 2, 8, 4, 8, seed=8)
+    rng = np.random.default_rng(8)
+    routes = irs_synth.random_routes(rng, T, T, 10, wl.cu_seqlens)
+    q, k, v = wl.arrays["q"], wl.arrays["k"], wl.arrays["v"]
+    scale = 1.0 / math.sqrt(D)
+    out, lse = O.attention(q, k, v, routes, scale)
+    # softmax weights sum to one: all-ones values give all-ones output
+    ones = exact_bf16_bits(np.ones_like(bits_to_f64(v), dtype=np.float32))
+    o1, _ = O.attention(q, k, ones, routes, scale)
+    np.testing.assert_allclose(o1, 1.0, rtol=0, atol=1e-6)
+    # moving, adding or removing -1 slots changes nothing
+    r2 = np.full((T, 17), -1, np.int32)
+    for t in range(T):
+        vals = routes[t][routes[t] >= 0]
+        slots = np.sort(rng.choice(17, size=vals.shape[0], replace=False))
+        r2[t, slots] = vals
+    o2, l2 = O.attention(q, k, v, r2, scale)
+    np.testing.assert_allclose(o2, out, rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(l2, lse, rtol=1e-6, atol=1e-7)
+    # permuting the valid IDs changes nothing
+    r3 = routes[:, rng.permutation(routes.shape[1])]
+    o3, _ = O.attention(q, k, v, r3, scale)
+    np.testing.assert_allclose(o3, out, rtol=1e-6, atol=1e-7)
+    # a single valid ID: out is that value row, lse = scale * q . k
+    r4 = np.full((T, 5), -1, np.int32)
+    r4[:, 3] = np.arange(T) // 2
+    o4, l4 = O.attention(q, k, v, r4, scale)
+    qf, kf, vf = bits_to_f64(q), bits_to_f64(k), bits_to_f64(v)
+    G = Hq // Hkv
+    for t in range(T):
+        j = t // 2
+        for h in range(Hq):
+            g = h // G
+            np.testing.assert_allclose(o4[t, h], vf[j, g], rtol=0, atol=1e-7)
+            np.testing.assert_allclose(l4[t, h], scale * qf[t, h] @ kf[j, g], rtol=1e-6, atol=1e-6)
+    # no valid ID at all: zeros and -inf (reading R7)
+    r5 = np.full((T, 4), -1, np.int32)
+    o5, l5 = O.attention(q, k, v, r5, scale)
+    assert np.all(o5 == 0) and np.all(np.isneginf(l5))
+
+
+def pin_latent_attention(O):
+    import irs_synth
+
+    rng = np.random.default_rng(6)
+    q = torch_bf16_bits(rng.standard_normal((6, 4, 64)).astype(np.float32))
+    kv = torch_bf16_bits(rng.standard_normal((200, 1, 64)).astype(np.float32))
+    r = irs_synth.latent_routes(rng, 6, 200, 16)
+    out, lse = O.latent_attention(q, kv, r, 0.125, Dv=48)
+    ref_o, ref_l = sdpa_masked(q, kv, kv[:, :, :48], r, 0.125)
+    np.testing.assert_allclose(out, ref_o, rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(lse, ref_l, rtol=1e-5, atol=1e-6)
+
+
+def pin_window_compose(O):
+    rng = np.random.default_rng(4)
+    cu = np.asarray([0, 30, 100], np.int32)
+    T, c, budget, window = 100, 4, 16, 8
+    import irs_synth
+
+    wl = irs_synth.custom(T, 2, 1, 8, 8, 2, 8, c, budget, doc_lens=[30, 70], seed=4)
+    r = O.index_routes(wl.arrays["qI"], wl.arrays["kI"], wl.arrays["w"], cu, c, budget)
+    comp = O.compose_window(r, cu, T, window)
+    assert comp.shape == (T, window + budget + c - 1)
+    for t in range(T):
+        s, _ = doc_start_of(cu, t)
+        win = comp[t, :window]
+        expect = [x if x >= s else -1 for x in range(t - window + 1, t + 1)]
+        assert win.tolist() == expect
+        allv = comp[t][comp[t] >= 0]
+        assert len(set(allv.tolist())) == allv.shape[0], "duplicate after composition"
+        assert set(allv.tolist()) == set(x for x in range(max(s, t - window + 1), t + 1)) | set(
+            x for x in r[t].tolist() if x >= 0), "union of window and route"
+    del rng
+
+
+ALL_PINS = [
+    pin_golden_two_docs,
+    pin_golden_head_weights,
+    pin_topk_bruteforce,
+    pin_routes_from_scores_bruteforce,
+    pin_route_invariants,
+    pin_dense_budget_routes,
+    pin_score_closed_form,
+    pin_score_symmetries,
+    pin_bf16_rounding,
+    pin_pool_mean,
+    pin_bitmap,
+    pin_attention_vs_sdpa,
+    pin_dense_causal_attention,
+    pin_attention_invariants,
+    pin_latent_attention,
+    pin_window_compose,
+]

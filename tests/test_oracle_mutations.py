@@ -1,0 +1,164 @@
+"""Plant plausible mistakes in the CPU oracle and check that some pin catches each.
+
+Every mutation replaces one oracle function for the duration of a test
+(monkeypatch on the oracle module; the oracle looks its helpers up at call time).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle_pins
+from oracle import irs_oracle as O
+
+
+def _select_top_high_ties(scores_f32, kb):
+    s = np.asarray(scores_f32, dtype=np.float32).astype(np.float64)
+    n = s.shape[0]
+    if n <= kb:
+        return np.arange(n)
+    order = np.lexsort((-np.arange(n), -s))
+    return np.sort(order[:kb])
+
+
+def _select_top_smallest(scores_f32, kb):
+    s = np.asarray(scores_f32, dtype=np.float32).astype(np.float64)
+    n = s.shape[0]
+    if n <= kb:
+        return np.arange(n)
+    return np.sort(np.lexsort((np.arange(n), s))[:kb])
+
+
+def _scores_no_relu(qI_t, w_t, kt):
+    return (w_t @ (qI_t @ kt.T)).astype(np.float32)
+
+
+def _scores_no_weight(qI_t, w_t, kt):
+    return np.maximum(qI_t @ kt.T, 0.0).sum(axis=0).astype(np.float32)
+
+
+def _scores_max_heads(qI_t, w_t, kt):
+    return (w_t[:, None] * np.maximum(qI_t @ kt.T, 0.0)).max(axis=0).astype(np.float32)
+
+
+def _expand_no_tail(doc_start, tau, c, budget, selected):
+    row = np.full(budget + c - 1, -1, dtype=np.int32)
+    slot = 0
+    for b in selected:
+        for j in range(c):
+            row[slot] = doc_start + int(b) * c + j
+            slot += 1
+    return row
+
+
+def _expand_tail_shift(doc_start, tau, c, budget, selected):
+    row = _expand_no_tail(doc_start, tau, c, budget, selected)
+    nv = O.visible_blocks(tau, c)
+    for j in range((tau + 1) % c):
+        row[budget + j] = doc_start + nv * c + j + 1
+    return row
+
+
+def _expand_global_ids_missing_offset(doc_start, tau, c, budget, selected):
+    row = np.full(budget + c - 1, -1, dtype=np.int32)
+    slot = 0
+    for b in selected:
+        for j in range(c):
+            row[slot] = int(b) * c + j
+            slot += 1
+    nv = O.visible_blocks(tau, c)
+    for j in range((tau + 1) % c):
+        row[budget + j] = nv * c + j
+    return row
+
+
+def _pool_no_div(x, c):
+    L, Di = x.shape
+    nb = L // c
+    acc = np.zeros((nb, Di), np.float32)
+    for j in range(c):
+        acc = (acc + x[j: nb * c: c]).astype(np.float32)
+    return acc
+
+
+def _pool_strided(x, c):
+    L, Di = x.shape
+    nb = L // c
+    acc = np.zeros((nb, Di), np.float32)
+    for j in range(c):
+        acc = (acc + x[j * nb:(j + 1) * nb]).astype(np.float32)
+    return (acc / np.float32(c)).astype(np.float32)
+
+
+def _pool_ignores_docs(kI_bits, cu_seqlens, c):
+    T = kI_bits.shape[0]
+    kbar = O.pool_doc(O.bf16_to_f32(kI_bits), c)
+    offs = [0]
+    cu = np.asarray(cu_seqlens, np.int64)
+    for d in range(cu.shape[0] - 1):
+        offs.append(int(cu[d + 1]) // c)
+    return kbar, np.asarray(offs, np.int64)
+
+
+def _round_truncate(x):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return (x.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32)
+
+
+def _attend_no_scale(q_t, K, V, scale, Hkv):
+    return _REAL_ATTEND(q_t, K, V, 1.0, Hkv)
+
+
+def _attend_lse_no_max(q_t, K, V, scale, Hkv):
+    out, lse = _REAL_ATTEND(q_t, K, V, scale, Hkv)
+    if K.shape[0] == 0:
+        return out, lse
+    Hq = q_t.shape[0]
+    G = Hq // Hkv
+    for h in range(Hq):
+        s = scale * (K[:, h // G, :] @ q_t[h])
+        lse[h] = math.log(np.sum(np.exp(s - np.max(s))))
+    return out, lse
+
+
+def _compose_shifted(routes, cu_seqlens, T, window, rows=None):
+    out = _REAL_COMPOSE(routes, cu_seqlens, T, window, rows)
+    out[:, :window] = np.where(out[:, :window] >= 0, out[:, :window] - 1, -1)
+    return out
+
+
+_REAL_ATTEND = O.attend_row
+_REAL_COMPOSE = O.compose_window
+
+MUTATIONS = {
+    "visibility_off_by_one": ("visible_blocks", lambda tau, c: tau // c),
+    "visibility_one_extra": ("visible_blocks", lambda tau, c: (tau + 1) // c + 1 if tau > 0 else 0),
+    "ties_to_higher_index": ("select_top", _select_top_high_ties),
+    "smallest_instead_of_largest": ("select_top", _select_top_smallest),
+    "missing_relu": ("block_scores", _scores_no_relu),
+    "missing_head_weights": ("block_scores", _scores_no_weight),
+    "max_over_heads": ("block_scores", _scores_max_heads),
+    "missing_tail": ("expand_route", _expand_no_tail),
+    "tail_shifted": ("expand_route", _expand_tail_shift),
+    "local_ids_not_global": ("expand_route", _expand_global_ids_missing_offset),
+    "pool_without_division": ("pool_doc", _pool_no_div),
+    "pool_wrong_grouping": ("pool_doc", _pool_strided),
+    "pool_ignores_documents": ("pool_keys", _pool_ignores_docs),
+    "bf16_truncation": ("round_to_bf16", _round_truncate),
+    "kv_group_modulo": ("kv_group", lambda h, Hq, Hkv: h % Hkv),
+    "scale_ignored": ("attend_row", _attend_no_scale),
+    "lse_missing_max": ("attend_row", _attend_lse_no_max),
+    "window_shifted": ("compose_window", _compose_shifted),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(name, monkeypatch):
+    attr, fn = MUTATIONS[name]
+    monkeypatch.setattr(O, attr, fn)
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(O)
+        except Exception:
+            return
+    pytest.fail(f"no pin caught the planted mistake {name!r}")
