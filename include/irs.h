@@ -1,0 +1,175 @@
+/*
+ * irs.h — C ABI of the indexer-routed sparse attention library (libirs.so, sm_103a).
+ *
+ * The library computes, on one GPU, the hot path of indexer-routed sparse GQA
+ * attention as described by the NVIDIA NeMo AutoModel API reference pages
+ *   "nemo_automodel.components.models.qwen3_8_flash_next.qsa"       (QSA page),
+ *   "nemo_automodel.components.models.step5.sparse"                 (Step-5 sparse page),
+ *   "nemo_automodel.components.models.step5.layers" / "...step5.fa4" (windowed GQA),
+ *   "nemo_automodel.components.models.common.cudnn_sparse_attention" (latent attention page):
+ *
+ *   1. a compressed-block indexer: FP32 mean of every c consecutive index keys of a
+ *      document, a weighted-ReLU score per (query, visible block) on tensor cores,
+ *      and a per-query top-k over blocks;
+ *   2. expansion of the chosen blocks into an int32 route row of global token IDs;
+ *   3. attention forward over exactly the routed keys and values.
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers unless stated otherwise, owned by the
+ *     caller. The library allocates no memory: scratch space is passed in.
+ *   - "bf16" pointers point to IEEE bfloat16 data; they are typed `const void*`.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *     and is asynchronous: a return value of IRS_OK means the arguments were valid
+ *     and the kernels were launched, not that they have finished.
+ *   - Host-side validation raises by category, like the pages' error taxonomy
+ *     (TypeError / ValueError / RuntimeError): see irs_status. Nothing falls back to
+ *     another implementation.
+ *   - Conditions only the device can see (route IDs out of range, malformed
+ *     cu_seqlens, a bounded wait that gave up) are OR-ed into *err_flag
+ *     (IRS_DEVERR_* bits) when err_flag is not NULL. The caller reads it after the
+ *     stream has synchronised. No kernel traps.
+ *   - irs_last_error() returns a thread-local message for the last non-OK status.
+ */
+#ifndef IRS_H_
+#define IRS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* irs_stream_t;
+
+typedef enum {
+  IRS_OK = 0,
+  IRS_ERR_TYPE = 1,    /* unsupported element type or layout class (pages: TypeError)   */
+  IRS_ERR_VALUE = 2,   /* bad size, shape, stride, alignment, width, scale, NULL, buffer
+                          too small (pages: ValueError)                                   */
+  IRS_ERR_RUNTIME = 3  /* no usable sm_103 device, or a CUDA launch error (RuntimeError)  */
+} irs_status;
+
+/* Bits OR-ed into *err_flag by the kernels. */
+#define IRS_DEVERR_ROUTE_ID 0x1   /* a route entry outside [-1, Tk); it was treated as padding */
+#define IRS_DEVERR_CU_SEQLENS 0x2 /* cu_seqlens not strictly increasing from 0 to T, or a
+                                     document longer than max_doc_len; no route was written  */
+#define IRS_DEVERR_TIMEOUT 0x4    /* a bounded on-device wait gave up; outputs are undefined */
+
+/* Version of this ABI (incremented on incompatible change). */
+int irs_abi_version(void);
+
+/* Message describing the last non-OK status returned on this host thread. */
+const char* irs_last_error(void);
+
+/*
+ * Scratch bytes irs_sparse_index_score_topk needs for these sizes (0 on invalid sizes).
+ * The scratch holds the per-document layout, the pooled bf16 block keys
+ * [floor(T/c), Di] and, when the caller passes no score buffer, the FP32 score rows
+ * [T, max_doc_len / c].
+ */
+size_t irs_index_workspace_bytes(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len,
+                                 int with_score_buffer);
+
+/*
+ * sparse_index_score_topk(qI, kI, w, cu_seqlens, c, budget) -> route_ids
+ *
+ * QSA page, `select_qsa_token_ids` and `Qwen3_8_FlashNextQSAIndexer`; Step-5 sparse
+ * page, `indexer_score_tile` (per-head FP32 weights) and `pack_region_bitmap`.
+ *
+ * For a query at document-local position tau (document d = [s_d, e_d) of cu_seqlens):
+ *   nvis = floor((tau+1)/c) complete blocks are visible; block b is the FP32 mean of
+ *   index keys s_d + b*c .. s_d + b*c + c-1 (sequential FP32 sum, one division by c),
+ *   rounded once to bf16;
+ *   score[b] = sum_h w[t,h] * ReLU(sum_d qI[t,h,d] * kbar[b,d])   (FP32 accumulation);
+ *   if nvis > budget/c the budget/c highest scores are kept (ties: lower block index),
+ *   otherwise every visible block is kept.
+ * Route row t (width W = budget + c - 1, int32, global token IDs):
+ *   slots [0, budget): the kept blocks in ascending block order, c tokens each, then -1;
+ *   slots [budget, W): the (tau+1) % c tokens s_d + nvis*c .. t of the incomplete block,
+ *   then -1. Routes never leave the query's document.
+ *
+ * qI          bf16 [T, Hi, Di] contiguous (row t*Hi + h has Di elements), 16-byte aligned
+ * kI          bf16 [T, Di] contiguous, 16-byte aligned
+ * w           fp32 [T, Hi] contiguous
+ * cu_seqlens  int32 [ndocs + 1] DEVICE, strictly increasing, 0 .. T
+ * ndocs, max_doc_len  host values: number of documents and the longest document
+ * T, Hi, Di, c, budget  sizes; 1 <= Hi <= 256, Di in {64, 128}, c >= 1, budget % c == 0
+ * route_ids   int32 [T, budget + c - 1] output
+ * scores_dbg  NULL, or fp32 [T, ld_scores] output: for rows with nvis > budget/c the
+ *             entries [0, nvis) receive the block scores; other entries are untouched.
+ *             ld_scores >= max_doc_len / c. When not NULL it also serves as the score
+ *             scratch, so the workspace may be sized with with_score_buffer = 0.
+ * workspace   scratch of at least irs_index_workspace_bytes(...) bytes, 256-byte aligned
+ * err_flag    NULL or one device int32 (IRS_DEVERR_* bits are OR-ed in)
+ */
+irs_status irs_sparse_index_score_topk(const void* qI, const void* kI, const float* w, const int32_t* cu_seqlens,
+                                       int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
+                                       int32_t* route_ids, float* scores_dbg, int64_t ld_scores, void* workspace,
+                                       size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream);
+
+/*
+ * Top-k, bitmap packing and expansion from given FP32 scores (the second half of
+ * irs_sparse_index_score_topk), so that routes can be compared bit for bit with an
+ * independent implementation that selects from the same scores.
+ *
+ * scores      fp32 [T, ld_scores]; for row t with nvis > budget/c, entries [0, nvis)
+ *             are read (NaN is outside the contract); other rows are not read.
+ * Other arguments as in irs_sparse_index_score_topk.
+ */
+irs_status irs_topk_from_scores(const float* scores, int64_t ld_scores, const int32_t* cu_seqlens, int ndocs,
+                                int max_doc_len, int T, int c, int budget, int32_t* route_ids, int32_t* err_flag,
+                                irs_stream_t stream);
+
+/*
+ * Sliding window in front of an indexer route (Step-5 layers page: GQA with windowed
+ * or CSA-selected keys; the windowed workload combines both).
+ *   out[t, j]          = t - window + 1 + j if that token is in t's document, else -1
+ *   out[t, window + j] = route_ids[t, j] if it is < t - window + 1, else -1
+ * so the composed row never repeats an ID.
+ * route_ids int32 [T, W]; out int32 [T, window + W]; window >= 1.
+ */
+irs_status irs_compose_window_routes(const int32_t* route_ids, int W, const int32_t* cu_seqlens, int ndocs,
+                                     int T, int window, int32_t* out, int32_t* err_flag, irs_stream_t stream);
+
+/*
+ * sparse_gqa_attn_fwd(q, k, v, route_ids, scale) -> out, lse
+ *
+ * QSA page, `gathered_qsa_gqa_attention`; latent attention page,
+ * `cudnn_sparse_attention` (keys = full latent rows, values = their first Dv dims,
+ * passed as v = k with Dv < Dqk).
+ *
+ * For query t and query head h, with KV head g = h / (Hq/Hkv) (consecutive query
+ * heads share a KV head) and R_t = { r = route_ids[t, i] : 0 <= r < Tk }:
+ *   s_r   = scale * q[t,h,:] . k[r,g,:]
+ *   out   = sum_r exp(s_r - m) v[r,g,:] / sum_r exp(s_r - m),   m = max_r s_r
+ *   lse   = m + ln sum_r exp(s_r - m)                (natural log)
+ * A row with no valid entry gives out = 0 and lse = -inf. Entries equal to -1 are
+ * padding; other entries outside [0, Tk) are also padding and set IRS_DEVERR_ROUTE_ID.
+ * IDs within a row must be distinct (a repeated ID is counted twice).
+ *
+ * q     bf16, element (t,h,d) at q + t*q_stride_t + h*q_stride_h + d
+ * k     bf16, element (r,g,d) at k + r*k_stride_t + g*k_stride_h + d
+ * v     bf16, element (r,g,d) at v + r*v_stride_t + g*v_stride_h + d (may alias k)
+ *       strides are in elements; rows must be 16-byte aligned (strides multiple of 8)
+ * route_ids  int32, entry (t,i) at route_ids + t*route_stride + i, 0 <= i < W
+ * sizes: Hq % Hkv == 0, Dqk % 64 == 0 and Dqk <= 576, Dv % 128 == 0 and Dv <= 512,
+ *        one chunk of 128 gathered key rows (plus value rows unless v aliases k) and
+ *        the query tile must fit in 227 KB of shared memory (IRS_ERR_VALUE otherwise;
+ *        about Dqk + Dv <= 704 without aliasing),
+ *        1 <= W <= 4096
+ * scale > 0 (finite)
+ * out   bf16 [T, Hq, Dv] contiguous;  lse  fp32 [T, Hq] contiguous (may be NULL)
+ */
+irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k,
+                                   int64_t k_stride_t, int64_t k_stride_h, const void* v, int64_t v_stride_t,
+                                   int64_t v_stride_h, const int32_t* route_ids, int64_t route_stride, int T,
+                                   int Tk, int Hq, int Hkv, int Dqk, int Dv, int W, float scale, void* out,
+                                   float* lse, int32_t* err_flag, irs_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IRS_H_ */

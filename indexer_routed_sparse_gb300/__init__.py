@@ -1,0 +1,26 @@
+"""Indexer-routed sparse GQA attention for GB300 (sm_103a).
+
+The compute lives in libirs.so (CUDA kernels behind the C ABI of include/irs.h);
+this package is its thin Python binding. Names follow the C entry points:
+
+* ``sparse_index_score_topk(qI, kI, w, cu_seqlens, c, budget) -> route_ids``
+* ``sparse_gqa_attn_fwd(q, k, v, route_ids, scale) -> (out, lse)``
+* ``topk_from_scores(scores, cu_seqlens, c, budget) -> route_ids``
+* ``compose_window_routes(route_ids, cu_seqlens, window) -> route_ids``
+"""
+from ._binding import (  # noqa: F401
+    DEVERR_CU_SEQLENS,
+    DEVERR_ROUTE_ID,
+    DEVERR_TIMEOUT,
+    LIB_PATH,
+    check_device_errors,
+    compose_window_routes,
+    device_error_flag,
+    exported_symbols,
+    index_workspace_bytes,
+    lib,
+    read_device_errors,
+    sparse_gqa_attn_fwd,
+    sparse_index_score_topk,
+    topk_from_scores,
+)

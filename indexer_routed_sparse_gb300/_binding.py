@@ -1,0 +1,263 @@
+"""ctypes binding of libirs.so (include/irs.h).
+
+Argument marshalling only: tensors are checked, outputs and scratch are allocated
+with torch on the tensors' device, and the C entry points are called with raw
+device pointers and the current torch stream. There is no other code path: if the
+library is missing or the device is not an sm_103 GPU, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libirs.so")
+
+IRS_OK, IRS_ERR_TYPE, IRS_ERR_VALUE, IRS_ERR_RUNTIME = 0, 1, 2, 3
+DEVERR_ROUTE_ID, DEVERR_CU_SEQLENS, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+
+_lib = None
+_lock = threading.Lock()
+_err_flags: dict[int, torch.Tensor] = {}
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_F = ctypes.c_float
+
+_SIGNATURES = {
+    "irs_abi_version": (_I, []),
+    "irs_last_error": (ctypes.c_char_p, []),
+    "irs_index_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
+    "irs_sparse_index_score_topk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I64, _P, _SZ, _P, _P]),
+    "irs_topk_from_scores": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "irs_compose_window_routes": (_I, [_P, _I, _P, _I, _I, _I, _P, _P, _P]),
+    "irs_sparse_gqa_attn_fwd": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I, _I, _I, _I, _I, _I,
+                                     _I, _F, _P, _P, _P, _P]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                                   f"g.build()\"` (nvcc, sm_103a)")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def exported_symbols() -> list[str]:
+    return list(_SIGNATURES)
+
+
+def _check(status: int, what: str) -> None:
+    if status == IRS_OK:
+        return
+    msg = f"{what}: {lib().irs_last_error().decode(errors='replace')}"
+    if status == IRS_ERR_TYPE:
+        raise TypeError(msg)
+    if status == IRS_ERR_VALUE:
+        raise ValueError(msg)
+    raise RuntimeError(msg)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(dev: torch.device) -> int:
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int | None = None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+
+
+def device_error_flag(device=None) -> torch.Tensor:
+    """The per-device int32 word the kernels OR IRS_DEVERR_* bits into."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index)
+    if dev.index not in _err_flags:
+        _err_flags[dev.index] = torch.zeros(1, dtype=torch.int32, device=dev)
+    return _err_flags[dev.index]
+
+
+def read_device_errors(device=None, reset: bool = True) -> int:
+    """Synchronise and return (then clear) the device error bits."""
+    f = device_error_flag(device)
+    torch.cuda.synchronize(f.device)
+    v = int(f.item())
+    if reset:
+        f.zero_()
+    return v
+
+
+def check_device_errors(device=None) -> None:
+    v = read_device_errors(device)
+    if v:
+        names = [n for b, n in ((DEVERR_ROUTE_ID, "route id out of range"),
+                                (DEVERR_CU_SEQLENS, "malformed cu_seqlens"),
+                                (DEVERR_TIMEOUT, "on-device wait timed out")) if v & b]
+        raise RuntimeError("device reported: " + ", ".join(names))
+
+
+def index_workspace_bytes(T, Hi, Di, c, budget, ndocs, max_doc_len, with_score_buffer=True) -> int:
+    return int(lib().irs_index_workspace_bytes(T, Hi, Di, c, budget, ndocs, max_doc_len, int(bool(with_score_buffer))))
+
+
+def _doc_stats(cu_seqlens: torch.Tensor, ndocs, max_doc_len):
+    if ndocs is None:
+        ndocs = cu_seqlens.numel() - 1
+    if max_doc_len is None:
+        max_doc_len = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item())
+    return int(ndocs), int(max_doc_len)
+
+
+def sparse_index_score_topk(qI: torch.Tensor, kI: torch.Tensor, w: torch.Tensor, cu_seqlens: torch.Tensor,
+                            c: int, budget: int, *, ndocs: int | None = None, max_doc_len: int | None = None,
+                            scores_out: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                            workspace: torch.Tensor | None = None, err: torch.Tensor | None = None) -> torch.Tensor:
+    """Route IDs int32 [T, budget + c - 1] from the compressed-block indexer.
+
+    qI bf16 [T, Hi, Di], kI bf16 [T, Di] (or [T, 1, Di]), w fp32 [T, Hi], cu_seqlens int32
+    [ndocs + 1] on the same device. `scores_out` (fp32 [T, ld >= max_doc_len // c]) receives
+    the block scores of every row with more than budget // c visible blocks.
+    """
+    _need(qI, "qI", torch.bfloat16, 3)
+    _need(kI, "kI", torch.bfloat16)
+    _need(w, "w", torch.float32, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, Hi, Di = qI.shape
+    if kI.dim() == 3:
+        kI = kI.reshape(kI.shape[0], kI.shape[2])
+    if tuple(kI.shape) != (T, Di) or tuple(w.shape) != (T, Hi):
+        raise ValueError(f"shape mismatch: qI {tuple(qI.shape)}, kI {tuple(kI.shape)}, w {tuple(w.shape)}")
+    if not (qI.is_contiguous() and kI.is_contiguous() and w.is_contiguous() and cu_seqlens.is_contiguous()):
+        raise ValueError("qI, kI, w and cu_seqlens must be contiguous")
+    ndocs, max_doc_len = _doc_stats(cu_seqlens, ndocs, max_doc_len)
+    W = budget + c - 1
+    dev = qI.device
+    if out is None:
+        out = torch.empty((T, W), dtype=torch.int32, device=dev)
+    ld = 0
+    if scores_out is not None:
+        _need(scores_out, "scores_out", torch.float32, 2)
+        if scores_out.shape[0] != T or scores_out.stride(1) != 1:
+            raise ValueError("scores_out must be [T, ld] with unit inner stride")
+        ld = scores_out.stride(0)
+    nbytes = index_workspace_bytes(T, Hi, Di, c, budget, ndocs, max_doc_len, scores_out is None)
+    if nbytes == 0:
+        _check(IRS_ERR_VALUE, "sparse_index_score_topk")
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    if err is None:
+        err = device_error_flag(dev)
+    st = lib().irs_sparse_index_score_topk(
+        _ptr(qI), _ptr(kI), _ptr(w), _ptr(cu_seqlens), ndocs, max_doc_len, T, Hi, Di, c, budget, _ptr(out),
+        _ptr(scores_out), ld, _ptr(workspace), workspace.numel(), _ptr(err), _stream(dev))
+    _check(st, "sparse_index_score_topk")
+    return out
+
+
+def topk_from_scores(scores: torch.Tensor, cu_seqlens: torch.Tensor, c: int, budget: int, *,
+                     ndocs: int | None = None, max_doc_len: int | None = None, out: torch.Tensor | None = None,
+                     err: torch.Tensor | None = None) -> torch.Tensor:
+    """Routes from given FP32 block scores [T, ld] (top-k, bitmap, expansion)."""
+    _need(scores, "scores", torch.float32, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    if scores.stride(1) != 1:
+        raise ValueError("scores must have unit inner stride")
+    T = scores.shape[0]
+    ndocs, max_doc_len = _doc_stats(cu_seqlens, ndocs, max_doc_len)
+    dev = scores.device
+    if out is None:
+        out = torch.empty((T, budget + c - 1), dtype=torch.int32, device=dev)
+    if err is None:
+        err = device_error_flag(dev)
+    st = lib().irs_topk_from_scores(_ptr(scores), scores.stride(0), _ptr(cu_seqlens), ndocs, max_doc_len, T, c,
+                                    budget, _ptr(out), _ptr(err), _stream(dev))
+    _check(st, "topk_from_scores")
+    return out
+
+
+def compose_window_routes(route_ids: torch.Tensor, cu_seqlens: torch.Tensor, window: int, *,
+                          out: torch.Tensor | None = None, err: torch.Tensor | None = None) -> torch.Tensor:
+    """[causal window of `window` tokens | route with in-window IDs set to -1], int32 [T, window + W]."""
+    _need(route_ids, "route_ids", torch.int32, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    if not route_ids.is_contiguous():
+        raise ValueError("route_ids must be contiguous")
+    T, W = route_ids.shape
+    dev = route_ids.device
+    if out is None:
+        out = torch.empty((T, window + W), dtype=torch.int32, device=dev)
+    if err is None:
+        err = device_error_flag(dev)
+    st = lib().irs_compose_window_routes(_ptr(route_ids), W, _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, window,
+                                         _ptr(out), _ptr(err), _stream(dev))
+    _check(st, "compose_window_routes")
+    return out
+
+
+def sparse_gqa_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, route_ids: torch.Tensor,
+                        scale: float | None = None, *, out: torch.Tensor | None = None,
+                        lse: torch.Tensor | None = None, want_lse: bool = True,
+                        err: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor | None]:
+    """Sparse attention over routed keys: (out bf16 [T, Hq, Dv], lse fp32 [T, Hq]).
+
+    q bf16 [T, Hq, Dqk], k bf16 [Tk, Hkv, Dqk], v bf16 [Tk, Hkv, Dv] (innermost dim
+    contiguous; v may be a view of k's leading Dv dims, as in latent attention),
+    route_ids int32 [T, W] with -1 padding.
+    """
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(route_ids, "route_ids", torch.int32, 2)
+    T, Hq, Dqk = q.shape
+    Tk, Hkv, Dk = k.shape
+    Tv, Hv, Dv = v.shape
+    if Dk != Dqk or Tv != Tk or Hv != Hkv or route_ids.shape[0] != T:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)} "
+                         f"route {tuple(route_ids.shape)}")
+    for name, t in (("q", q), ("k", k), ("v", v), ("route_ids", route_ids)):
+        if t.stride(-1) != 1:
+            raise ValueError(f"{name} must have unit inner stride")
+    W = route_ids.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(Dqk)
+    dev = q.device
+    if out is None:
+        out = torch.empty((T, Hq, Dv), dtype=torch.bfloat16, device=dev)
+    elif tuple(out.shape) != (T, Hq, Dv) or not out.is_contiguous() or out.dtype != torch.bfloat16:
+        raise ValueError("out must be a contiguous bf16 tensor [T, Hq, Dv]")
+    if lse is not None and (tuple(lse.shape) != (T, Hq) or not lse.is_contiguous() or lse.dtype != torch.float32):
+        raise ValueError("lse must be a contiguous fp32 tensor [T, Hq]")
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+    if err is None:
+        err = device_error_flag(dev)
+    st = lib().irs_sparse_gqa_attn_fwd(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1), _ptr(v), v.stride(0), v.stride(1),
+        _ptr(route_ids), route_ids.stride(0), T, Tk, Hq, Hkv, Dqk, Dv, W, float(scale), _ptr(out), _ptr(lse),
+        _ptr(err), _stream(dev))
+    _check(st, "sparse_gqa_attn_fwd")
+    return out, lse

@@ -1,0 +1,258 @@
+// C ABI of libirs.so: argument validation (by the pages' error categories), device
+// checks, TMA descriptor encoding and kernel launches. See include/irs.h for the
+// contract of every entry point.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "irs_internal.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+irs_status fail(irs_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+struct DeviceInfo {
+  bool checked = false;
+  bool ok = false;
+  int num_sms = 0;
+  size_t score_smem = 0, topk_smem = 0, attn_smem = 0;   // largest values configured so far
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// The current device must be an sm_103 GPU; returns its slot.
+irs_status current_device(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(IRS_ERR_RUNTIME, "no CUDA device: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(IRS_ERR_RUNTIME, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.checked) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    d.checked = true;
+    d.ok = (major == 10 && minor == 3);
+    d.num_sms = sms;
+  }
+  if (!d.ok) return fail(IRS_ERR_RUNTIME, "libirs needs an sm_103 (GB300) device; device %d is not one", dev);
+  *out = &d;
+  return IRS_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map [rows][inner] (inner contiguous), SW128 boxes of {64, box_rows}.
+irs_status make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(IRS_ERR_RUNTIME, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(IRS_ERR_RUNTIME, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return IRS_OK;
+}
+
+irs_status launch_status(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(IRS_ERR_RUNTIME, "%s: %s", what, cudaGetErrorString(e));
+  return IRS_OK;
+}
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
+irs_status check_index_sizes(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len) {
+  if (T < 1) return fail(IRS_ERR_VALUE, "T must be >= 1 (got %d)", T);
+  if (ndocs < 1 || ndocs > T) return fail(IRS_ERR_VALUE, "ndocs must be in [1, T] (got %d)", ndocs);
+  if (max_doc_len < 1 || max_doc_len > T) return fail(IRS_ERR_VALUE, "max_doc_len must be in [1, T]");
+  if (!pow2(Hi) || Hi > 256) return fail(IRS_ERR_VALUE, "Hi must be a power of two in [1, 256] (got %d)", Hi);
+  if (Di != 64 && Di != 128) return fail(IRS_ERR_VALUE, "Di must be 64 or 128 (got %d)", Di);
+  if (c < 1) return fail(IRS_ERR_VALUE, "c must be >= 1 (got %d)", c);
+  if (budget < c || budget % c != 0) return fail(IRS_ERR_VALUE, "budget must be a positive multiple of c");
+  if ((long long)T * Hi >= (1LL << 31)) return fail(IRS_ERR_VALUE, "T*Hi too large");
+  if ((long long)budget + c - 1 >= (1LL << 24)) return fail(IRS_ERR_VALUE, "route width too large");
+  if (irs::topk_smem_bytes(max_doc_len / c > 0 ? max_doc_len / c : 1, budget / c) > kMaxSmem)
+    return fail(IRS_ERR_VALUE, "max_doc_len / c too large for the on-chip top-k (max about 48k blocks)");
+  return IRS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int irs_abi_version(void) { return 1; }
+
+const char* irs_last_error(void) { return g_msg; }
+
+size_t irs_index_workspace_bytes(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len,
+                                 int with_score_buffer) {
+  if (check_index_sizes(T, Hi, Di, c, budget, ndocs, max_doc_len) != IRS_OK) return 0;
+  return irs::plan_index(T, Hi, Di, c, budget, ndocs, max_doc_len, with_score_buffer != 0).ws_bytes;
+}
+
+irs_status irs_sparse_index_score_topk(const void* qI, const void* kI, const float* w, const int32_t* cu_seqlens,
+                                       int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
+                                       int32_t* route_ids, float* scores_dbg, int64_t ld_scores, void* workspace,
+                                       size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream) {
+  irs_status s = check_index_sizes(T, Hi, Di, c, budget, ndocs, max_doc_len);
+  if (s != IRS_OK) return s;
+  if (!qI || !kI || !w || !cu_seqlens || !route_ids || !workspace)
+    return fail(IRS_ERR_VALUE, "NULL tensor pointer");
+  if (!aligned16(qI) || !aligned16(kI)) return fail(IRS_ERR_VALUE, "qI and kI must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(IRS_ERR_VALUE, "workspace must be 256-byte aligned");
+  const irs::IndexPlan p = irs::plan_index(T, Hi, Di, c, budget, ndocs, max_doc_len, scores_dbg == nullptr);
+  if (scores_dbg != nullptr && ld_scores < p.ldS)
+    return fail(IRS_ERR_VALUE, "ld_scores must be >= max_doc_len / c (%lld)", (long long)p.ldS);
+  if (workspace_bytes < p.ws_bytes)
+    return fail(IRS_ERR_VALUE, "workspace too small: %zu < %zu bytes", workspace_bytes, p.ws_bytes);
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != IRS_OK) return s;
+  if (p.score_smem > kMaxSmem) return fail(IRS_ERR_VALUE, "score tile does not fit in shared memory");
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (dev->score_smem < p.score_smem) {
+      if ((s = launch_status(irs::configure_score_kernels(p.score_smem), "configuring scoring")) != IRS_OK) return s;
+      dev->score_smem = p.score_smem;
+    }
+    if (dev->topk_smem < p.topk_smem) {
+      if ((s = launch_status(irs::configure_topk_kernel(p.topk_smem), "configuring top-k")) != IRS_OK) return s;
+      dev->topk_smem = p.topk_smem;
+    }
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* scores = scores_dbg != nullptr ? scores_dbg : reinterpret_cast<float*>(ws + p.off_scores);
+  const int64_t ldS = scores_dbg != nullptr ? ld_scores : p.ldS;
+  CUtensorMap tm_q, tm_k;
+  if ((s = make_tmap(&tm_q, qI, (uint64_t)Di, (uint64_t)T * Hi, 256)) != IRS_OK) return s;
+  if ((s = make_tmap(&tm_k, ws + p.off_kbar, (uint64_t)Di, (uint64_t)p.nblk_cap, 128)) != IRS_OK) return s;
+  return launch_status(irs::launch_index(p, static_cast<const __nv_bfloat16*>(qI),
+                                         static_cast<const __nv_bfloat16*>(kI), w, cu_seqlens, ndocs, max_doc_len, T,
+                                         Hi, Di, c, budget, route_ids, scores, ldS, ws, err_flag, tm_q, tm_k,
+                                         reinterpret_cast<cudaStream_t>(stream)),
+                       "launching the indexer");
+}
+
+irs_status irs_topk_from_scores(const float* scores, int64_t ld_scores, const int32_t* cu_seqlens, int ndocs,
+                                int max_doc_len, int T, int c, int budget, int32_t* route_ids, int32_t* err_flag,
+                                irs_stream_t stream) {
+  irs_status s = check_index_sizes(T, 1, 64, c, budget, ndocs, max_doc_len);
+  if (s != IRS_OK) return s;
+  if (!scores || !cu_seqlens || !route_ids) return fail(IRS_ERR_VALUE, "NULL tensor pointer");
+  if (ld_scores < max_doc_len / c) return fail(IRS_ERR_VALUE, "ld_scores must be >= max_doc_len / c");
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != IRS_OK) return s;
+  const size_t smem = irs::topk_smem_bytes(max_doc_len / c > 0 ? max_doc_len / c : 1, budget / c);
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (dev->topk_smem < smem) {
+      if ((s = launch_status(irs::configure_topk_kernel(smem), "configuring top-k")) != IRS_OK) return s;
+      dev->topk_smem = smem;
+    }
+  }
+  return launch_status(irs::launch_topk_from_scores(scores, ld_scores, cu_seqlens, ndocs, max_doc_len, T, c, budget,
+                                                    route_ids, err_flag, reinterpret_cast<cudaStream_t>(stream)),
+                       "launching top-k");
+}
+
+irs_status irs_compose_window_routes(const int32_t* route_ids, int W, const int32_t* cu_seqlens, int ndocs,
+                                     int T, int window, int32_t* out, int32_t* err_flag, irs_stream_t stream) {
+  if (T < 1 || W < 1 || window < 1 || ndocs < 1 || ndocs > T)
+    return fail(IRS_ERR_VALUE, "bad sizes (T=%d W=%d window=%d ndocs=%d)", T, W, window, ndocs);
+  if ((long long)W + window >= (1LL << 24)) return fail(IRS_ERR_VALUE, "composed width too large");
+  if (!route_ids || !cu_seqlens || !out) return fail(IRS_ERR_VALUE, "NULL tensor pointer");
+  DeviceInfo* dev = nullptr;
+  irs_status s = current_device(&dev);
+  if (s != IRS_OK) return s;
+  return launch_status(irs::launch_compose_window(route_ids, W, cu_seqlens, ndocs, T, window, out, err_flag,
+                                                  reinterpret_cast<cudaStream_t>(stream)),
+                       "launching window composition");
+}
+
+irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k,
+                                   int64_t k_stride_t, int64_t k_stride_h, const void* v, int64_t v_stride_t,
+                                   int64_t v_stride_h, const int32_t* route_ids, int64_t route_stride, int T,
+                                   int Tk, int Hq, int Hkv, int Dqk, int Dv, int W, float scale, void* out,
+                                   float* lse, int32_t* err_flag, irs_stream_t stream) {
+  if (T < 0 || Tk < 1 || Hq < 1 || Hkv < 1) return fail(IRS_ERR_VALUE, "bad sizes (T=%d Tk=%d Hq=%d Hkv=%d)", T, Tk, Hq, Hkv);
+  if (Hq % Hkv != 0) return fail(IRS_ERR_VALUE, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (Dqk < 64 || Dqk > 576 || Dqk % 64 != 0) return fail(IRS_ERR_VALUE, "Dqk must be a multiple of 64 in [64, 576]");
+  if (Dv < 128 || Dv > 512 || Dv % 128 != 0) return fail(IRS_ERR_VALUE, "Dv must be a multiple of 128 in [128, 512]");
+  if (W < 1 || W > 4096) return fail(IRS_ERR_VALUE, "route width W must be in [1, 4096] (got %d)", W);
+  if (route_stride < W) return fail(IRS_ERR_VALUE, "route_stride must be >= W");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(IRS_ERR_VALUE, "scale must be positive and finite");
+  if (T == 0) return IRS_OK;
+  if (!q || !k || !v || !route_ids || !out) return fail(IRS_ERR_VALUE, "NULL tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(IRS_ERR_VALUE, "q, k, v and out must be 16-byte aligned");
+  if (q_stride_t % 8 || q_stride_h % 8 || k_stride_t % 8 || k_stride_h % 8 || v_stride_t % 8 || v_stride_h % 8)
+    return fail(IRS_ERR_VALUE, "q/k/v strides must be multiples of 8 elements (16 bytes)");
+  if (q_stride_t < 0 || q_stride_h < 0 || k_stride_t < 0 || k_stride_h < 0 || v_stride_t < 0 || v_stride_h < 0)
+    return fail(IRS_ERR_VALUE, "negative strides are not supported");
+  DeviceInfo* dev = nullptr;
+  irs_status s = current_device(&dev);
+  if (s != IRS_OK) return s;
+
+  irs::AttnArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.q_st = q_stride_t; a.q_sh = q_stride_h;
+  a.k_st = k_stride_t; a.k_sh = k_stride_h;
+  a.v_st = v_stride_t; a.v_sh = v_stride_h;
+  a.route = route_ids;
+  a.route_stride = route_stride;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.err = err_flag;
+  a.T = T; a.Tk = Tk; a.Hq = Hq; a.Hkv = Hkv; a.Dqk = Dqk; a.Dv = Dv; a.W = W;
+  a.G = Hq / Hkv;
+  a.HB = a.G < 16 ? a.G : 16;
+  a.nhb = (a.G + a.HB - 1) / a.HB;
+  a.v_alias = (v == k && v_stride_t == k_stride_t && v_stride_h == k_stride_h && Dv <= Dqk) ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const irs::AttnPlan p = irs::plan_attn(a, dev->num_sms);
+  if (p.smem > kMaxSmem) return fail(IRS_ERR_VALUE, "attention tile does not fit in shared memory");
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (dev->attn_smem < p.smem) {
+      if ((s = launch_status(irs::configure_attn_kernel(p.smem), "configuring attention")) != IRS_OK) return s;
+      dev->attn_smem = p.smem;
+    }
+  }
+  return launch_status(irs::launch_attn(a, p, reinterpret_cast<cudaStream_t>(stream)), "launching attention");
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// Internal declarations shared by the translation units of libirs.so.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/irs.h"
+
+namespace irs {
+
+// Sizes and scratch offsets of one indexer call.
+struct IndexPlan {
+  int kb;              // blocks kept per query (budget / c)
+  int QT;              // queries per score tile (256 / Hi)
+  int tau_sparse;      // first document-local position with more than kb visible blocks
+  int nblk_cap;        // rows of the pooled-key buffer (T / c)
+  int64_t ldS;         // row stride of the score buffer (max_doc_len / c)
+  int score_tiles_cap; // grid of the score kernel (upper bound on tiles)
+  int stages;          // key-tile ring depth of the score kernel
+  size_t off_meta, off_blk, off_tile, off_kbar, off_scores, ws_bytes;
+  size_t score_smem, topk_smem;
+};
+
+IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len, bool with_scores);
+size_t topk_smem_bytes(int nvis_cap, int kb);
+
+cudaError_t configure_score_kernels(size_t smem);
+cudaError_t configure_topk_kernel(size_t smem);
+cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI, const float* w,
+                         const int32_t* cu, int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
+                         int32_t* route, float* scores, int64_t ldS, uint8_t* ws, int32_t* err,
+                         const CUtensorMap& tm_q, const CUtensorMap& tm_k, cudaStream_t stream);
+cudaError_t launch_topk_from_scores(const float* scores, int64_t ldS, const int32_t* cu, int ndocs, int max_doc_len,
+                                    int T, int c, int budget, int32_t* route, int32_t* err, cudaStream_t stream);
+cudaError_t launch_compose_window(const int32_t* route, int W, const int32_t* cu, int ndocs, int T, int window,
+                                  int32_t* out, int32_t* err, cudaStream_t stream);
+
+// Gathered sparse attention.
+struct AttnArgs {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh;
+  const int32_t* route;
+  int64_t route_stride;
+  __nv_bfloat16* out;
+  float* lse;
+  int32_t* err;
+  int T, Tk, Hq, Hkv, Dqk, Dv, W;
+  int G;          // query heads per KV head
+  int HB;         // query heads handled by one work item (<= 16)
+  int nhb;        // head blocks per KV head
+  int v_alias;    // 1: values are the first Dv dims of the gathered key rows
+  int stages;
+  float scale_log2;  // scale * log2(e)
+};
+
+struct AttnPlan {
+  int stages;
+  size_t smem;
+  int grid;
+  long long items;
+};
+
+AttnPlan plan_attn(const AttnArgs& a, int num_sms);
+cudaError_t configure_attn_kernel(size_t smem);
+cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
+
+}  // namespace irs

@@ -1,0 +1,113 @@
+"""The C ABI library: loads, exports what include/irs.h declares, validates on the host.
+
+No compute call is made here: every call below fails host-side validation before the
+library touches a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import indexer_routed_sparse_gb300 as irs
+
+    if not os.path.exists(irs.LIB_PATH):
+        from indexer_routed_sparse_gb300 import build
+
+        build.build()
+    return irs.lib()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "irs.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(irs_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("irs_sparse_index_score_topk", "irs_sparse_gqa_attn_fwd", "irs_topk_from_scores",
+                 "irs_compose_window_routes", "irs_index_workspace_bytes", "irs_last_error", "irs_abi_version"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import indexer_routed_sparse_gb300 as irs
+
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"{name} declared in include/irs.h but not exported"
+        assert name in irs.exported_symbols(), f"{name} has no binding"
+    assert lib.irs_abi_version() == 1
+
+
+def test_workspace_size_rules(lib):
+    import indexer_routed_sparse_gb300 as irs
+
+    n = irs.index_workspace_bytes(8192, 16, 128, 4, 2048, 1, 8192, True)
+    # pooled keys (8192/4 x 128 bf16) + score rows (8192 x 2048 fp32) at least
+    assert n >= 2048 * 128 * 2 + 8192 * 2048 * 4
+    n0 = irs.index_workspace_bytes(8192, 16, 128, 4, 2048, 1, 8192, False)
+    assert 2048 * 128 * 2 <= n0 < n
+    assert irs.index_workspace_bytes(8192, 12, 128, 4, 2048, 1, 8192, True) == 0     # Hi not a power of two
+    assert irs.index_workspace_bytes(8192, 16, 96, 4, 2048, 1, 8192, True) == 0      # unsupported Di
+    assert irs.index_workspace_bytes(8192, 16, 128, 4, 2047, 1, 8192, True) == 0     # budget % c
+    assert n % 256 == 0
+
+
+@pytest.mark.parametrize("case, field", [
+    (dict(Hi=3), "Hi"), (dict(Di=32), "Di"), (dict(c=0), "c"), (dict(budget=6, c=4), "budget"),
+    (dict(ndocs=0), "ndocs"), (dict(max_doc_len=0), "max_doc_len"),
+])
+def test_index_validation_is_value_error(lib, case, field):
+    args = dict(T=64, Hi=4, Di=64, c=4, budget=16, ndocs=1, max_doc_len=64)
+    args.update(case)
+    st = lib.irs_sparse_index_score_topk(None, None, None, None, args["ndocs"], args["max_doc_len"], args["T"],
+                                         args["Hi"], args["Di"], args["c"], args["budget"], None, None, 0, None, 0,
+                                         None, None)
+    assert st == 2, field
+    assert lib.irs_last_error()
+
+
+def test_index_null_pointers_are_value_error(lib):
+    st = lib.irs_sparse_index_score_topk(None, None, None, None, 1, 64, 64, 4, 64, 4, 16, None, None, 0, None, 0,
+                                         None, None)
+    assert st == 2 and b"NULL" in lib.irs_last_error()
+
+
+@pytest.mark.parametrize("case", [
+    dict(Hq=6, Hkv=4), dict(Dqk=100), dict(Dqk=640), dict(Dv=64), dict(Dv=640), dict(W=0), dict(W=5000),
+    dict(scale=0.0), dict(scale=-1.0), dict(scale=float("inf")), dict(route_stride=3, W=4),
+])
+def test_attention_validation_is_value_error(lib, case):
+    a = dict(T=4, Tk=16, Hq=4, Hkv=2, Dqk=128, Dv=128, W=8, scale=0.1, route_stride=8)
+    a.update(case)
+    st = lib.irs_sparse_gqa_attn_fwd(None, 0, 0, None, 0, 0, None, 0, 0, None, a["route_stride"], a["T"], a["Tk"],
+                                     a["Hq"], a["Hkv"], a["Dqk"], a["Dv"], a["W"], a["scale"], None, None, None, None)
+    assert st == 2, case
+
+
+def test_attention_misaligned_strides_are_value_error(lib):
+    # strides must be multiples of 8 elements; checked before any device access
+    buf = ctypes.create_string_buffer(64)
+    p = ctypes.addressof(buf) + (16 - ctypes.addressof(buf) % 16) % 16
+    st = lib.irs_sparse_gqa_attn_fwd(p, 12, 128, p, 128, 128, p, 128, 128, p, 8, 4, 16, 4, 2, 128, 128, 8, 0.1, p,
+                                     None, None, None)
+    assert st == 2 and b"multiples of 8" in lib.irs_last_error()
+
+
+def test_binding_rejects_wrong_dtypes_on_cpu():
+    import torch
+
+    import indexer_routed_sparse_gb300 as irs
+
+    q = torch.zeros(4, 2, 64, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        irs.sparse_gqa_attn_fwd(q, q, q, torch.zeros(4, 4, dtype=torch.int32))
+    qb = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):   # not a CUDA tensor
+        irs.sparse_gqa_attn_fwd(qb, qb, qb, torch.zeros(4, 4, dtype=torch.int32))

@@ -1,0 +1,163 @@
+"""Sparse attention on the GPU (through the C ABI) against the CPU oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import irs_synth
+import parity
+from oracle import irs_oracle as O
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module")
+def irs():
+    import indexer_routed_sparse_gb300 as m
+
+    m.lib()
+    return m
+
+
+def attend(irs, q, k, v, routes, scale):
+    qd = torch.from_numpy(q).view(torch.bfloat16).to(DEV) if isinstance(q, np.ndarray) else q
+    kd = torch.from_numpy(k).view(torch.bfloat16).to(DEV) if isinstance(k, np.ndarray) else k
+    vd = torch.from_numpy(v).view(torch.bfloat16).to(DEV) if isinstance(v, np.ndarray) else v
+    rd = torch.from_numpy(np.ascontiguousarray(routes)).to(DEV)
+    out, lse = irs.sparse_gqa_attn_fwd(qd, kd, vd, rd, scale)
+    irs.check_device_errors(DEV)
+    return out, lse
+
+
+def test_tiny_with_oracle_routes_all_rows(irs):
+    wl = irs_synth.make("tiny")
+    a = wl.arrays
+    routes = O.index_routes(a["qI"], a["kI"], a["w"], wl.cu_seqlens, wl.c, wl.budget)
+    out, lse = attend(irs, a["q"], a["k"], a["v"], routes, wl.scale)
+    ref_o, ref_l = O.attention(a["q"], a["k"], a["v"], routes, wl.scale)
+    parity.check_attention(out, lse, ref_o, ref_l, np.arange(wl.T))
+
+
+@pytest.mark.parametrize("name", ["mid", "packed", "windowed"])
+def test_full_size_sampled_rows(irs, name):
+    wl = irs_synth.make(name)
+    a = wl.arrays
+    rows = parity.sample_rows(wl, 192, seed=2)
+    W = wl.route_width
+    routes = parity.window_like_routes(wl.T, wl.Tk, W, wl.cu_seqlens)
+    rng = np.random.default_rng(7)
+    sub = irs_synth.random_routes(rng, wl.T, wl.Tk, W, wl.cu_seqlens, frac_invalid=0.1) if wl.T <= 2048 else None
+    if sub is None:
+        # random document-confined routes for the sampled rows only
+        cu = np.asarray(wl.cu_seqlens, np.int64)
+        for t in rows:
+            s = int(cu[np.searchsorted(cu, t, side="right") - 1])
+            n_av = int(t) - s + 1
+            n = min(W, n_av)
+            ids = s + rng.choice(n_av, size=n, replace=False)
+            row = np.full(W, -1, np.int32)
+            row[rng.permutation(W)[:n]] = ids
+            routes[t] = row
+    else:
+        routes = sub
+    out, lse = attend(irs, a["q"], a["k"], a["v"], routes, wl.scale)
+    ref_o, ref_l = O.attention(a["q"], a["k"], a["v"], routes, wl.scale, rows=rows)
+    parity.check_attention(out, lse, ref_o, ref_l, rows)
+
+
+def test_latent_full_size_sampled_rows(irs):
+    wl = irs_synth.make("latent")
+    a = wl.arrays
+    rows = parity.sample_rows(wl, 96, seed=3)
+    kv = torch.from_numpy(a["kv"]).view(torch.bfloat16).to(DEV)
+    q = torch.from_numpy(a["q"]).view(torch.bfloat16).to(DEV)
+    out, lse = attend(irs, q, kv, kv[:, :, :512], a["route"], wl.scale)
+    ref_o, ref_l = O.latent_attention(a["q"], a["kv"], a["route"], wl.scale, Dv=512, rows=rows)
+    parity.check_attention(out, lse, ref_o, ref_l, rows)
+
+
+def test_latent_small_all_rows(irs):
+    wl = irs_synth.make("latent", small=True)
+    a = wl.arrays
+    kv = torch.from_numpy(a["kv"]).view(torch.bfloat16).to(DEV)
+    q = torch.from_numpy(a["q"]).view(torch.bfloat16).to(DEV)
+    out, lse = attend(irs, q, kv, kv[:, :, :512], a["route"], wl.scale)
+    rows = np.arange(0, wl.T, 7)
+    ref_o, ref_l = O.latent_attention(a["q"], a["kv"], a["route"], wl.scale, Dv=512, rows=rows)
+    parity.check_attention(out, lse, ref_o, ref_l, rows)
+
+
+@pytest.mark.parametrize("Hq,Hkv,Dqk,Dv,W", [
+    (4, 4, 64, 128, 1),        # G = 1, a single slot
+    (32, 1, 128, 128, 300),    # G = 32: two head blocks per KV head
+    (8, 2, 192, 256, 129),     # Dqk != Dv, two dv blocks, W one past a chunk
+    (6, 2, 128, 128, 4096),    # G = 3 (padded), widest route
+    (16, 16, 384, 256, 64),    # wide head dims without aliasing (one smem stage)
+])
+def test_shapes(irs, Hq, Hkv, Dqk, Dv, W):
+    T = 200
+    wl = irs_synth.custom(T, Hq, Hkv, Dqk, Dv, 2, 64, 4, 8, doc_lens=[70, 130], seed=Hq + W)
+    a = wl.arrays
+    rng = np.random.default_rng(W)
+    routes = irs_synth.random_routes(rng, T, T, W, wl.cu_seqlens, frac_invalid=0.2)
+    scale = 1.0 / math.sqrt(Dqk)
+    out, lse = attend(irs, a["q"], a["k"], a["v"], routes, scale)
+    ref_o, ref_l = O.attention(a["q"], a["k"], a["v"], routes, scale)
+    parity.check_attention(out, lse, ref_o, ref_l, np.arange(T))
+
+
+def test_empty_rows_and_out_of_range_ids(irs):
+    T = 64
+    wl = irs_synth.custom(T, 4, 2, 128, 128, 2, 64, 4, 8, seed=9)
+    a = wl.arrays
+    routes = np.full((T, 20), -1, np.int32)
+    routes[1::2, 3] = np.arange(1, T, 2)                   # one key on odd rows, none on even rows
+    routes[5, 7] = 10 * T                                  # out of range: padding + device flag
+    routes[9, 0] = -7                                      # negative but not -1: padding + flag
+    qd = torch.from_numpy(a["q"]).view(torch.bfloat16).to(DEV)
+    kd = torch.from_numpy(a["k"]).view(torch.bfloat16).to(DEV)
+    vd = torch.from_numpy(a["v"]).view(torch.bfloat16).to(DEV)
+    irs.read_device_errors(DEV)
+    out, lse = irs.sparse_gqa_attn_fwd(qd, kd, vd, torch.from_numpy(routes).to(DEV), wl.scale)
+    assert irs.read_device_errors(DEV) & irs.DEVERR_ROUTE_ID
+    ref_o, ref_l = O.attention(a["q"], a["k"], a["v"], routes, wl.scale)
+    parity.check_attention(out, lse, ref_o, ref_l, np.arange(T))
+    assert torch.all(out[0::2] == 0) and torch.all(torch.isneginf(lse[0::2]))
+
+
+def test_strided_query_view(irs):
+    T, Hq, Hkv, D = 96, 8, 2, 128
+    wl = irs_synth.custom(T, Hq, Hkv, D, D, 2, 64, 4, 8, seed=4)
+    a = wl.arrays
+    big = torch.zeros(T, Hq + 3, D + 64, dtype=torch.bfloat16, device=DEV)
+    big[:, 1:Hq + 1, 32:32 + D] = torch.from_numpy(a["q"]).view(torch.bfloat16).to(DEV)
+    qv = big[:, 1:Hq + 1, 32:32 + D]
+    rng = np.random.default_rng(1)
+    routes = irs_synth.random_routes(rng, T, T, 50, wl.cu_seqlens)
+    kd = torch.from_numpy(a["k"]).view(torch.bfloat16).to(DEV)
+    vd = torch.from_numpy(a["v"]).view(torch.bfloat16).to(DEV)
+    out, lse = irs.sparse_gqa_attn_fwd(qv, kd, vd, torch.from_numpy(routes).to(DEV), wl.scale)
+    ref_o, ref_l = O.attention(a["q"], a["k"], a["v"], routes, wl.scale)
+    parity.check_attention(out, lse, ref_o, ref_l, np.arange(T))
+
+
+def test_end_to_end_mid(irs):
+    """Indexer routes -> attention, both on the GPU; the oracle runs its own routes."""
+    wl = irs_synth.make("mid")
+    a = wl.arrays
+    t = irs_synth.as_torch(wl, device=DEV)
+    route = irs.sparse_index_score_topk(t["qI"], t["kI"], t["w"], t["cu_seqlens"], wl.c, wl.budget,
+                                        max_doc_len=wl.max_doc_len)
+    out, lse = irs.sparse_gqa_attn_fwd(t["q"], t["k"], t["v"], route, wl.scale)
+    irs.check_device_errors(DEV)
+    rows = parity.sample_rows(wl, 128, seed=5)
+    ref_r = O.index_routes(a["qI"], a["kI"], a["w"], wl.cu_seqlens, wl.c, wl.budget, rows=rows)
+    g_r = route[torch.as_tensor(rows, device=DEV)].cpu().numpy()
+    same = np.all(g_r == ref_r, axis=1)
+    assert same.mean() > 0.95
+    full_routes = np.full((wl.T, wl.route_width), -1, np.int32)
+    full_routes[rows] = ref_r
+    ref_o, ref_l = O.attention(a["q"], a["k"], a["v"], full_routes, wl.scale, rows=rows[same])
+    parity.check_attention(out, lse, ref_o, ref_l, rows[same])
