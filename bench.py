@@ -1,0 +1,438 @@
+"""Benchmark of the indexer-routed sparse attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of the mid-size single-document
+workload (B=1, S=8192, Hq=32, Hkv=8, D=128; indexer Hi=16, Di=128, c=4, budget=2048):
+  sparse_index_score_topk (layout, pool, score, top-k + expansion)  ->  sparse_gqa_attn_fwd.
+
+Prints one JSON line (rank 0). `value` is the routed sparse-attention forward rate in
+TFLOP/s over the whole step (algorithmic attention FLOPs / step time, inputs resident in
+HBM, L2 flushed between timed steps); the indexer's queries/s, each kernel's own rate and
+the roofline of the dominant kernel are reported beside it. `--impl reference` times the
+CPU oracle on a bounded row sample of the same workload instead.
+
+Multi-GPU: one process per GPU under torchrun; each rank runs its own replica of the
+workload (weak scaling, no data-path collective); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import irs_synth  # noqa: E402
+
+METRIC = "routed sparse-attn fwd TFLOP/s & % roofline; indexer score+top-k queries/s"
+WORKLOAD = "mid"
+KERNELS_PER_STEP = 5          # layout, pool, score, top-k/expand, attention
+L2_FLUSH_BYTES = 512 << 20    # > 129 MB L2
+
+
+# --------------------------------------------------------------------------------------
+# algorithmic counts (closed forms from the definitions; no GPU data involved)
+# --------------------------------------------------------------------------------------
+def valid_per_row(wl) -> np.ndarray:
+    """Valid route entries of each row: min(nvis, kb)*c + (tau+1) % c."""
+    cu = np.asarray(wl.cu_seqlens, np.int64)
+    t = np.arange(wl.T, dtype=np.int64)
+    s = cu[np.searchsorted(cu, t, side="right") - 1]
+    tau = t - s
+    nvis = (tau + 1) // wl.c
+    kb = wl.budget // wl.c
+    return np.minimum(nvis, kb) * wl.c + (tau + 1) % wl.c
+
+
+def counts(wl) -> dict:
+    vr = valid_per_row(wl)
+    pairs = int(vr.sum())
+    cu = np.asarray(wl.cu_seqlens, np.int64)
+    t = np.arange(wl.T, dtype=np.int64)
+    s = cu[np.searchsorted(cu, t, side="right") - 1]
+    nvis = (t - s + 1) // wl.c
+    kb = wl.budget // wl.c
+    sparse = nvis > kb
+    score_pairs = int(nvis[sparse].sum())
+    W = wl.route_width
+    attn_flops = 2.0 * (wl.Dqk + wl.Dv) * wl.Hq * pairs
+    attn_bytes = (pairs * wl.Hkv * (wl.Dqk + wl.Dv) * 2          # gathered K and V rows
+                  + wl.T * wl.Hq * wl.Dqk * 2                     # Q
+                  + wl.T * wl.Hq * wl.Dv * 2                      # O
+                  + wl.T * wl.Hq * 4                              # lse
+                  + wl.T * W * 4)                                 # routes
+    idx_flops = 2.0 * wl.Hi * wl.Di * score_pairs
+    idx_bytes = (wl.T * wl.Hi * wl.Di * 2 + wl.T * wl.Di * 2 + wl.T * wl.Hi * 4 + wl.T * W * 4)
+    return dict(pairs=pairs, score_pairs=score_pairs, attn_flops=attn_flops, attn_bytes=attn_bytes,
+                idx_flops=idx_flops, idx_bytes=idx_bytes, sparse_rows=int(sparse.sum()))
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# --------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.proc = None
+        self.uuid = uuid
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    """Max of a host float over ranks (identity for one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def run_gpu(args) -> dict | None:
+    import torch
+
+    import indexer_routed_sparse_gb300 as irs
+
+    world, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    irs.lib()
+    wl = irs_synth.make(WORKLOAD)
+    cnt = counts(wl)
+    peaks = load_peaks()
+
+    host = irs_synth.as_torch(wl, device="cpu", pin=True)
+    d = {k: v.to(dev) for k, v in host.items()}
+    T, W = wl.T, wl.route_width
+    route = torch.empty((T, W), dtype=torch.int32, device=dev)
+    out = torch.empty((T, wl.Hq, wl.Dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, wl.Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(irs.index_workspace_bytes(T, wl.Hi, wl.Di, wl.c, wl.budget, wl.ndocs, wl.max_doc_len, True),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    err = irs.device_error_flag(dev)
+    max_doc_len, ndocs = wl.max_doc_len, wl.ndocs
+
+    def index(dd):
+        irs.sparse_index_score_topk(dd["qI"], dd["kI"], dd["w"], dd["cu_seqlens"], wl.c, wl.budget, ndocs=ndocs,
+                                    max_doc_len=max_doc_len, out=route, workspace=ws, err=err)
+
+    def attend(dd):
+        irs.sparse_gqa_attn_fwd(dd["q"], dd["k"], dd["v"], route, wl.scale, out=out, lse=lse, err=err)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        index(d)
+        attend(d)
+    torch.cuda.synchronize(dev)
+    irs.check_device_errors(dev)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid if rank == 0 else None)
+    if rank == 0:
+        clocks.start()
+
+    # ---- device-timed region: K steps, L2 flushed before each, per-kernel events ----
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        index(d)
+        ev[i][1].record(stream)
+        attend(d)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    idx_ms = np.asarray([ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)])
+    att_ms = np.asarray([ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)])
+    step_ms_local = float(np.mean(idx_ms + att_ms))
+    step_ms = reduce_max(step_ms_local, world, dev)
+    irs.check_device_errors(dev)
+
+    # ---- end to end through the public API with host buffers ----
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    e2e_steps = max(3, args.steps // 2)
+    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(e2e_steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    for i in range(e2e_steps):
+        flush.fill_(i & 0xFF)
+        ee[i][0].record(stream)
+        for k_, v_ in host.items():
+            d[k_].copy_(v_, non_blocking=True)
+        index(d)
+        attend(d)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        ee[i][1].record(stream)
+        ee[i][1].synchronize()
+    barrier(world)
+    e2e_ms = reduce_max(float(np.mean([ee[i][0].elapsed_time(ee[i][1]) for i in range(e2e_steps)])), world, dev)
+    clk = clocks.stop() if rank == 0 else None
+    irs.check_device_errors(dev)
+
+    if rank != 0:
+        return None
+    att_avg_s = float(np.mean(att_ms)) * 1e-3
+    idx_avg_s = float(np.mean(idx_ms)) * 1e-3
+    attn_gbs = cnt["attn_bytes"] / att_avg_s / 1e9
+    attn_tflops = cnt["attn_flops"] / att_avg_s / 1e12
+    attn_roof_s = max(cnt["attn_bytes"] / (peaks["hbm_gbs"] * 1e9), cnt["attn_flops"] / (peaks["bf16_tflops"] * 1e12))
+    idx_roof_s = max(cnt["idx_bytes"] / (peaks["hbm_gbs"] * 1e9), cnt["idx_flops"] / (peaks["bf16_tflops"] * 1e12))
+    value = world * cnt["attn_flops"] / (step_ms * 1e-3) / 1e12
+    res = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v/qI/kI, U(0,1) fp32 w)",
+        "config": {"workload": "mid single-document: B=1 S=8192 Hq=32 Hkv=8 D=128, indexer Hi=16 Di=128 c=4 "
+                               "budget=2048 (route width 2051), scale 1/sqrt(128), seed 1",
+                   "l2": "flushed (512 MiB write) before every timed step", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(attn_gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                     "kernel": "attn_fwd_kernel", "peak_source": peaks["source"]},
+        "attention": {"ms": round(att_avg_s * 1e3, 4), "tflops": round(attn_tflops, 3),
+                      "routed_pairs_per_s": round(cnt["pairs"] * wl.Hq / att_avg_s, 1),
+                      "roofline_frac": round(attn_roof_s / att_avg_s, 4),
+                      "algorithmic_bytes": cnt["attn_bytes"], "flops": cnt["attn_flops"]},
+        "indexer": {"ms": round(idx_avg_s * 1e3, 4), "queries_per_s": round(wl.T / idx_avg_s, 1),
+                    "tflops": round(cnt["idx_flops"] / idx_avg_s / 1e12, 3),
+                    "roofline_frac": round(idx_roof_s / idx_avg_s, 4), "roofline_s": idx_roof_s,
+                    "algorithmic_bytes": cnt["idx_bytes"], "flops": cnt["idx_flops"]},
+        "e2e": {"value": round(world * cnt["attn_flops"] / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clk,
+        "wall_s_timed": round(wall, 3),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        res["cpu_baseline"] = cpu_baseline(wl, cnt, budget_s=args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return res
+
+
+# --------------------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# --------------------------------------------------------------------------------------
+_WL = None
+
+
+def _worker_init():
+    global _WL
+    _WL = irs_synth.make(WORKLOAD)
+
+
+def _oracle_rows(rows) -> int:
+    """Indexer + attention of the oracle on some rows; returns their valid route entries."""
+    from oracle import irs_oracle as O
+
+    wl = _WL
+    a = wl.arrays
+    rows = np.asarray(rows, np.int64)
+    r = O.index_routes(a["qI"], a["kI"], a["w"], wl.cu_seqlens, wl.c, wl.budget, rows=rows)
+    full = np.full((wl.T, wl.route_width), -1, np.int32)
+    full[rows] = r
+    O.attention(a["q"], a["k"], a["v"], full, wl.scale, rows=rows)
+    return int(np.count_nonzero(r >= 0))
+
+
+def oracle_sample(n_rows: int, cores: int, pool) -> tuple[float, int, float]:
+    """Time the oracle on n_rows rows spread over the workload; returns (seconds, pairs, flops)."""
+    wl = _WL
+    rows = np.linspace(0, wl.T - 1, n_rows).astype(np.int64)
+    shards = [rows[i::cores] for i in range(cores) if rows[i::cores].size]
+    t0 = time.perf_counter()
+    pairs = sum(pool.map(_oracle_rows, shards))
+    dt = time.perf_counter() - t0
+    return dt, pairs, 2.0 * (wl.Dqk + wl.Dv) * wl.Hq * pairs
+
+
+def make_pool(cores: int):
+    import multiprocessing as mp
+
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    os.environ.setdefault("MKL_NUM_THREADS", "1")
+    ctx = mp.get_context("spawn")
+    pool = ctx.Pool(cores, initializer=_worker_init)
+    pool.map(_worker_init_probe, range(cores))   # workers are up and have built the workload
+    return pool
+
+
+def _worker_init_probe(_):
+    return 0
+
+
+def cpu_baseline(wl, cnt, budget_s: float = 15.0) -> dict:
+    global _WL
+    _WL = wl
+    cores = os.cpu_count() or 1
+    pool = make_pool(cores)
+    try:
+        dt1, _, _ = oracle_sample(cores, cores, pool)               # calibration: one row per core
+        n = int(max(cores, min(wl.T, cores * max(1, int(budget_s / max(dt1, 1e-3))))))
+        dt, pairs, flops = oracle_sample(n, cores, pool)
+    finally:
+        pool.terminate()
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {wl.T} query rows spread evenly (indexer + attention, all {wl.Hq} heads), "
+                      f"{dt:.1f} s wall on {cores} single-threaded worker processes",
+            "seconds": round(dt, 3), "rows": n}
+
+
+def run_reference(args) -> dict | None:
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    global _WL
+    wl = irs_synth.make(WORKLOAD)
+    _WL = wl
+    cores = os.cpu_count() or 1
+    pool = make_pool(cores)
+    try:
+        dt1, _, _ = oracle_sample(cores, cores, pool)
+        per_step_s = max(0.5, args.reference_seconds / max(1, args.steps + args.warmup))
+        n = int(max(cores, min(wl.T, cores * max(1, int(per_step_s / max(dt1, 1e-3))))))
+        for _ in range(args.warmup):
+            oracle_sample(n, cores, pool)
+        times, fl = [], 0.0
+        for _ in range(args.steps):
+            dt, _, fl = oracle_sample(n, cores, pool)
+            times.append(dt)
+    finally:
+        pool.terminate()
+    ms = float(np.mean(times)) * 1e3
+    value = fl / (ms * 1e-3) / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "mid single-document: B=1 S=8192 Hq=32 Hkv=8 D=128, indexer Hi=16 Di=128 c=4 "
+                               "budget=2048, seed 1", "sample_rows_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} of {wl.T} query rows per step (indexer + attention)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("irs", "reference"), default="irs")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-seconds", type=float, default=150.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "irs":
+        args.warmup = 3
+    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

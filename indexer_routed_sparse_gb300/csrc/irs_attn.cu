@@ -1,4 +1,4 @@
-// Gathered sparse GQA / latent attention forward on sm_103a (tcgen05 + TMEM).
+// Gathered sparse GQA / latent attention forward on sm_103a (tcgen05 + TMEM + TMA gather4).
 //
 // Semantics: QSA page (nemo_automodel.components.models.qwen3_8_flash_next.qsa,
 // `gathered_qsa_gqa_attention`): query t, head h attends the keys/values of its KV
@@ -6,50 +6,61 @@
 // a positive scale. Latent attention page (`cudnn_sparse_attention`): one latent KV
 // head, keys are the full latent rows and values their first Dv dims.
 //
-// Design. A CTA owns a query row t (grid-stride over rows) and walks its KV heads and
-// head blocks (<= 16 query heads of one KV head). The valid route IDs are compacted
-// once per row into shared memory. Routed key/value rows stream through a ring of
-// shared-memory stages with 16-byte cp.async (padding rows are zero-filled, never
-// read); each chunk holds 128 keys in the SW128 atom layout. Per chunk:
-//   S^T[128 keys, 16 heads]  = K_chunk . Q^T      (UMMA M=128, N=16, K=Dqk; TMEM)
-//   online softmax over keys (lane = key; head maxima reduced across the 4 warps)
-//   O^T[dv, 16 heads]       = V_chunk^T . P^T    (UMMA M=128 per 128 dv, N=16, K=128,
-//                                                  V read MN-major straight from the
-//                                                  gathered [key][dv] tile)
-//   the running output (lane = dv) is rescaled and accumulated in registers.
-// For latent attention the value tile is the gathered key tile itself.
+// Design. A persistent CTA walks query rows t (grid-stride); for each row it walks its
+// KV heads and head blocks (<= 16 query heads of one KV head, a "sub-item"). Warp roles:
+//   warps 0..3  producer: compact the valid route IDs of the row into shared memory, load
+//               the sub-item's query tile, and gather routed K/V rows with 16-byte
+//               cp.async into a ring of 128-key stages (SW128 layout); completion is
+//               signalled per stage by cp.async-arrive on an mbarrier. (Random 256-byte
+//               rows reach about 3x the L2 bandwidth this way than with TMA gather4.)
+//   warp 4      TMEM owner and UMMA issuer: S^T = K.Q^T (M=128 keys, N=16 heads, K=Dqk)
+//               and O^T = V^T.P^T (M=128 dv per block, N=16, K=128 keys; V read MN-major
+//               from the gathered [key][dv] tile);
+//   warps 5..8  softmax and correction, one key (for S) / one dv (for O) per thread: an
+//               online softmax in base 2 with head maxima exchanged through shared memory,
+//               P written as the bf16 B operand, the chunk output rescaled and accumulated
+//               in registers, then normalised and stored.
+// S, P and O are double-buffered, so S of chunk n+1 and O of chunk n-1 run on the tensor
+// cores while the softmax warps work on chunk n, and the producer runs ahead across
+// sub-items and rows. All cross-warp waits are bounded mbarrier waits.
 #include "irs_internal.h"
 #include "irs_ptx.cuh"
 
 namespace irs {
 
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 288;   // 4 producer warps, 1 MMA warp, 4 softmax warps
+constexpr int kProducerThreads = 128;
 constexpr int kChunk = 128;   // keys per chunk (UMMA M of the score product)
-constexpr int kNH = 16;       // head columns per work item (UMMA N)
+constexpr int kNH = 16;       // head columns per sub-item (UMMA N)
 constexpr int kMaxDvBlocks = 4;
 
-struct AttnSmem {
-  uint32_t k_stage, v_stage, q_off, p_off, idx_off, red_off, bar_off, total;
+struct AttnLayout {
+  uint32_t k_bytes, v_bytes, stage_bytes, idx_words;
+  uint32_t q_off, p_off, idx_off, nv_off, red_off, fin_off, bar_off, total;
 };
 
-__host__ __device__ inline AttnSmem attn_smem_layout(int Dqk, int Dv, int W, int stages, int v_alias) {
-  AttnSmem L{};
-  L.k_stage = (uint32_t)kChunk * Dqk * 2;
-  L.v_stage = v_alias ? 0u : (uint32_t)kChunk * Dv * 2;
-  uint32_t off = (L.k_stage + L.v_stage) * stages;
+__host__ __device__ inline AttnLayout attn_layout(int Dqk, int Dv, int W, int stages, int v_alias) {
+  AttnLayout L{};
+  L.k_bytes = (uint32_t)kChunk * Dqk * 2;
+  L.v_bytes = v_alias ? 0u : (uint32_t)kChunk * Dv * 2;
+  L.stage_bytes = L.k_bytes + L.v_bytes;
+  L.idx_words = (uint32_t)((W + kChunk - 1) / kChunk) * kChunk;
+  uint32_t off = L.stage_bytes * stages;
   L.q_off = off;
-  off += (uint32_t)kNH * Dqk * 2;
+  off += 2u * kNH * Dqk * 2;
   off = (off + 1023u) & ~1023u;
   L.p_off = off;
-  off += (uint32_t)kNH * kChunk * 2;
+  off += 2u * kNH * kChunk * 2;
   L.idx_off = off;
-  off += (uint32_t)W * 4;
-  off = (off + 15u) & ~15u;
+  off += L.idx_words * 4;   // one buffer: only the producer reads the IDs
+  L.nv_off = off;
+  off += 16 + 32;           // sNv[2] and the producer's per-warp counts
   L.red_off = off;
-  off += 4 * kNH * 4 + 64;
-  off = (off + 15u) & ~15u;
+  off += 2 * 4 * kNH * 4;
+  L.fin_off = off;
+  off += 2 * 4 * kNH * 4;
   L.bar_off = off;
-  off += 64;
+  off += 40 * 8 + 16;
   L.total = off + 1024;   // alignment slack
   return L;
 }
@@ -65,290 +76,430 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// Issue the gathers of one chunk (keys [c*128, c*128+128) of the compacted row) into a stage.
-__device__ __forceinline__ void issue_chunk(const AttnArgs& a, int g, int c, int nvalid, const int32_t* sIdx,
-                                            uint8_t* sK, uint8_t* sV, int tid) {
-  const int kc = a.Dqk >> 3;   // 16-byte chunks per key row
-  const __nv_bfloat16* kbase = a.k + (long long)g * a.k_sh;
-  const uint32_t dK = smem_u32(sK);
-  for (int i = tid; i < kChunk * kc; i += kAttnThreads) {
-    const int r = i / kc, j = i - r * kc;
-    const int idx = c * kChunk + r;
-    const int id = idx < nvalid ? sIdx[idx] : -1;
-    const __nv_bfloat16* src = id >= 0 ? kbase + (long long)id * a.k_st + j * 8 : a.k;
-    cp_async_16(dK + sw128_offset(r, j * 8, kChunk), src, id >= 0 ? 16u : 0u);
-  }
-  if (!a.v_alias) {
-    const int vc = a.Dv >> 3;
-    const __nv_bfloat16* vbase = a.v + (long long)g * a.v_sh;
-    const uint32_t dV = smem_u32(sV);
-    for (int i = tid; i < kChunk * vc; i += kAttnThreads) {
-      const int r = i / vc, j = i - r * vc;
-      const int idx = c * kChunk + r;
-      const int id = idx < nvalid ? sIdx[idx] : -1;
-      const __nv_bfloat16* src = id >= 0 ? vbase + (long long)id * a.v_st + j * 8 : a.v;
-      cp_async_16(dV + sw128_offset(r, j * 8, kChunk), src, id >= 0 ? 16u : 0u);
-    }
+template <int NH>
+__device__ __forceinline__ void tmem_ld_nh(uint32_t taddr, float (&v)[NH]) {
+  if constexpr (NH == 4) tmem_ld4(taddr, v);
+  else if constexpr (NH == 8) tmem_ld8(taddr, v);
+  else tmem_ld16(taddr, v);
+}
+
+// Gather `rows` routed rows of kc 16-byte pieces each into a SW128 operand tile with
+// 16-byte cp.async, spread over the 128 producer threads (piece i = r*kc + j goes to
+// thread i % 128). ids[r] are valid row indices.
+__device__ __forceinline__ void gather_rows(uint32_t dst, const __nv_bfloat16* src, int64_t row_stride,
+                                            const int32_t* ids, int rows, int kc, int ptid) {
+  int r = ptid / kc, j = ptid - (ptid / kc) * kc;
+  const int dr = kProducerThreads / kc, dj = kProducerThreads - dr * kc;
+  while (r < rows) {
+    const int id = ids[r];
+    cp_async_16(dst + sw128_offset(r, j * 8, kChunk), src + (int64_t)id * row_stride + j * 8, 16u);
+    r += dr;
+    j += dj;
+    if (j >= kc) { j -= kc; ++r; }
   }
 }
 
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(AttnArgs a) {
+struct AttnBars {
+  uint64_t* kv_full;
+  uint64_t* kv_empty;
+  uint64_t* q_full;    // [2]
+  uint64_t* q_empty;   // [2]
+  uint64_t* idx_full;  // [2]
+  uint64_t* idx_empty; // [2]
+  uint64_t* s_full;    // [2]
+  uint64_t* s_empty;   // [2]
+  uint64_t* p_full;    // [2]
+  uint64_t* p_empty;   // [2]
+  uint64_t* o_full;    // [2]
+  uint64_t* o_empty;   // [2]
+  uint64_t* red;       // [2] chunk-max exchange among the softmax warps
+  uint64_t* fin;       // [2] row-sum exchange
+};
+
+template <int NH>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnMaps maps, AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const AttnSmem Lay = attn_smem_layout(a.Dqk, a.Dv, a.W, a.stages, a.v_alias);
-  uint8_t* sQ = smem + Lay.q_off;
-  uint8_t* sP = smem + Lay.p_off;
-  int32_t* sIdx = reinterpret_cast<int32_t*>(smem + Lay.idx_off);
-  float* sRed = reinterpret_cast<float*>(smem + Lay.red_off);        // [4 warps][16]
-  int* sCnt = reinterpret_cast<int*>(sRed + 4 * kNH);                 // [4] + running
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Lay.bar_off);    // [0] S done, [1] O done
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
+  const int ST = a.stages;
+  const AttnLayout Ly = attn_layout(a.Dqk, a.Dv, a.W, ST, a.v_alias);
+  uint8_t* sQ = smem + Ly.q_off;                                  // [2][16 rows x Dqk]
+  uint8_t* sP = smem + Ly.p_off;                                  // [2][16 rows x 128 keys]
+  int32_t* sIdx = reinterpret_cast<int32_t*>(smem + Ly.idx_off);  // [idx_words] (producer only)
+  int32_t* sNv = reinterpret_cast<int32_t*>(smem + Ly.nv_off);    // [2]
+  int32_t* sCnt = sNv + 4;                                        // [4] producer warp counts
+  float* sRed = reinterpret_cast<float*>(smem + Ly.red_off);      // [2][4][16]
+  float* sFin = reinterpret_cast<float*>(smem + Ly.fin_off);      // [2][4][16]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Ly.bar_off);
+  AttnBars B;
+  B.kv_full = bar;
+  B.kv_empty = bar + ST;
+  B.q_full = bar + 2 * ST;
+  B.q_empty = B.q_full + 2;
+  B.idx_full = B.q_empty + 2;
+  B.idx_empty = B.idx_full + 2;
+  B.s_full = B.idx_empty + 2;
+  B.s_empty = B.s_full + 2;
+  B.p_full = B.s_empty + 2;
+  B.p_empty = B.p_full + 2;
+  B.o_full = B.p_empty + 2;
+  B.o_empty = B.o_full + 2;
+  B.red = B.o_empty + 2;
+  B.fin = B.red + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(B.fin + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ST = a.stages;
-  const uint32_t stage_bytes = Lay.k_stage + Lay.v_stage;
-  const int ndvb = a.Dv / 128;
+  const int katoms = a.Dqk >> 6;
+  const int vatoms = a.Dv >> 6;
+  const int ndvb = a.Dv >> 7;
+  const int qc = a.Dqk >> 3;
+  const int n_sub = a.ng * a.nhb;   // sub-items per row
   constexpr uint32_t IDESC_S = idesc_bf16(kChunk, kNH, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16(128, kNH, true, false);
 
+  // ---- set-up: zero the operand buffers (stale rows must stay finite), barriers, TMEM ----
+  {
+    uint4* z = reinterpret_cast<uint4*>(smem);
+    const uint32_t nz = Ly.idx_off / 16;
+    for (uint32_t i = tid; i < nz; i += kAttnThreads) z[i] = make_uint4(0, 0, 0, 0);
+    if (tid < 2) sNv[tid] = 0;
+    fence_proxy_async_smem();
+  }
   if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+    for (int s = 0; s < ST; ++s) { mbar_init(&B.kv_full[s], kProducerThreads); mbar_init(&B.kv_empty[s], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B.q_full[i], 1);
+      mbar_init(&B.q_empty[i], 1);
+      mbar_init(&B.idx_full[i], 1);
+      mbar_init(&B.idx_empty[i], 5);
+      mbar_init(&B.s_full[i], 1);
+      mbar_init(&B.s_empty[i], 4);
+      mbar_init(&B.p_full[i], 4);
+      mbar_init(&B.p_empty[i], 1);
+      mbar_init(&B.o_full[i], 1);
+      mbar_init(&B.o_empty[i], 4);
+      mbar_init(&B.red[i], 4);
+      mbar_init(&B.fin[i], 4);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
-    tmem_alloc(tslot, 128);
+  if (warp == 4) {
+    tmem_alloc(tslot, 256);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const uint32_t tS = tbase;                 // columns [0, 16)
-  const uint32_t tO = tbase + kNH;           // columns [16, 16 + 16*ndvb)
-  const uint32_t lane_addr = tmem_lane_base(warp);
-  uint32_t ph_s = 0, ph_o = 0;
 
-  for (long long t = blockIdx.x; t < a.T && !*abort_flag; t += gridDim.x) {
-    // ---- compact the valid route IDs of row t ----
-    const int32_t* rrow = a.route + t * a.route_stride;
-    int running = 0;
-    for (int base = 0; base < a.W; base += kAttnThreads) {
-      const int i = base + tid;
-      const int id = i < a.W ? __ldg(rrow + i) : -1;
-      const bool ok = id >= 0 && id < a.Tk;
-      if (i < a.W && id != -1 && !ok) record_error(a.err, IRS_DEVERR_ROUTE_ID);
-      const uint32_t bal = __ballot_sync(0xffffffffu, ok);
-      if (lane == 0) sCnt[warp] = __popc(bal);
-      __syncthreads();
-      int before = running;
-      for (int w2 = 0; w2 < warp; ++w2) before += sCnt[w2];
-      if (ok) sIdx[before + __popc(bal & ((1u << lane) - 1u))] = id;
-      running += sCnt[0] + sCnt[1] + sCnt[2] + sCnt[3];
-      __syncthreads();
-    }
-    const int nvalid = running;
-    const int nchunks = (nvalid + kChunk - 1) / kChunk;
-
-    for (int g = 0; g < a.Hkv && !*abort_flag; ++g) {
-      for (int hb = 0; hb < a.nhb && !*abort_flag; ++hb) {
-        const int h0 = g * a.G + hb * a.HB;
+  if (warp < 4) {
+    // =========================== producer (warps 0..3) ===========================
+    const int ptid = tid;
+    uint32_t n = 0, u = 0, qi = 0;
+    bool alive = true;
+    for (long long t = blockIdx.x; t < a.T && alive; t += gridDim.x, ++qi) {
+      const int b = qi & 1;
+      bool ok = qi < 2 || mbar_wait(&B.idx_empty[b], ((qi >> 1) - 1) & 1, abort_flag, a.err);
+      alive = named_bar_and(1, kProducerThreads, ok);
+      if (!alive) break;
+      // ---- compact the valid IDs of route row t (8 loads in flight per thread) ----
+      const int32_t* rrow = a.route + t * a.route_stride;
+      int run = 0;
+      for (int base = 0; base < a.W; base += 8 * kProducerThreads) {
+        int ids[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int i = base + k * kProducerThreads + ptid;
+          ids[k] = i < a.W ? __ldg(rrow + i) : -1;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (base + k * kProducerThreads >= a.W) break;
+          const int i = base + k * kProducerThreads + ptid;
+          const int id = ids[k];
+          const bool okid = id >= 0 && id < a.Tk;
+          if (i < a.W && id != -1 && !okid && a.g0 == 0) record_error(a.err, IRS_DEVERR_ROUTE_ID);
+          const uint32_t bal = __ballot_sync(0xffffffffu, okid);
+          if (lane == 0) sCnt[warp] = __popc(bal);
+          named_bar_sync(1, kProducerThreads);
+          int before = run;
+          for (int w2 = 0; w2 < warp; ++w2) before += sCnt[w2];
+          if (okid) sIdx[before + __popc(bal & ((1u << lane) - 1u))] = id;
+          run += sCnt[0] + sCnt[1] + sCnt[2] + sCnt[3];
+          named_bar_sync(1, kProducerThreads);
+        }
+      }
+      if (ptid == 0) sNv[b] = run;
+      named_bar_sync(1, kProducerThreads);
+      if (ptid == 0) mbar_arrive(&B.idx_full[b]);
+      const int nv = run;
+      if (nv == 0) continue;
+      const int nchunks = (nv + kChunk - 1) / kChunk;
+      for (int sub = 0; sub < n_sub && alive; ++sub, ++u) {
+        const int g = sub / a.nhb, hb = sub - g * a.nhb;
+        const int h0 = (a.g0 + g) * a.G + hb * a.HB;
         const int nh = min(a.HB, a.G - hb * a.HB);
-        // ---- Q tile (16 rows, zero beyond nh) in the SW128 K-major layout ----
-        {
-          const int qc = a.Dqk >> 3;
-          for (int i = tid; i < kNH * qc; i += kAttnThreads) {
-            const int r = i / qc, j = i - r * qc;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < nh) v = __ldg(reinterpret_cast<const uint4*>(a.q + t * a.q_st + (long long)(h0 + r) * a.q_sh + j * 8));
-            *reinterpret_cast<uint4*>(sQ + sw128_offset(r, j * 8, kNH)) = v;
+        const int qb = u & 1;
+        ok = u < 2 || mbar_wait(&B.q_empty[qb], ((u >> 1) - 1) & 1, abort_flag, a.err);
+        alive = named_bar_and(1, kProducerThreads, ok);
+        if (!alive) break;
+        uint8_t* q_dst = sQ + qb * (kNH * a.Dqk * 2);
+        for (int i = ptid; i < nh * qc; i += kProducerThreads) {
+          const int r = i / qc, j = i - r * qc;
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.q + t * a.q_st + (long long)(h0 + r) * a.q_sh + j * 8));
+          *reinterpret_cast<uint4*>(q_dst + sw128_offset(r, j * 8, kNH)) = v;
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, kProducerThreads);
+        if (ptid == 0) mbar_arrive(&B.q_full[qb]);
+        const __nv_bfloat16* kbase = a.k + (long long)(a.g0 + g) * a.k_sh;
+        const __nv_bfloat16* vbase = a.v + (long long)(a.g0 + g) * a.v_sh;
+        for (int c = 0; c < nchunks; ++c, ++n) {
+          const int st = n % ST;
+          ok = (int)n < ST || mbar_wait(&B.kv_empty[st], ((n / ST) - 1) & 1, abort_flag, a.err);
+          alive = named_bar_and(1, kProducerThreads, ok);
+          if (!alive) break;
+          const int rows = min(kChunk, nv - c * kChunk);
+          const int32_t* ids = sIdx + c * kChunk;
+          uint8_t* stage = smem + (uint32_t)st * Ly.stage_bytes;
+          gather_rows(smem_u32(stage), kbase, a.k_st, ids, rows, qc, ptid);
+          if (!a.v_alias) gather_rows(smem_u32(stage + Ly.k_bytes), vbase, a.v_st, ids, rows, a.Dv >> 3, ptid);
+          cp_async_mbar_arrive_noinc(&B.kv_full[st]);
+        }
+      }
+    }
+    cp_async_wait_pending(0);   // nothing of this CTA's gathers is in flight when it leaves
+  } else if (warp == 4) {
+    // =========================== UMMA issuer ===========================
+    if (lane == 0) {
+      uint32_t n = 0, u = 0, qi = 0;
+      bool alive = true;
+      auto issue_o = [&](uint32_t m) -> bool {
+        const int pb = m & 1;
+        if (!mbar_wait(&B.p_full[pb], (m >> 1) & 1, abort_flag, a.err)) return false;
+        if (m >= 2 && !mbar_wait(&B.o_empty[pb], ((m >> 1) - 1) & 1, abort_flag, a.err)) return false;
+        tc_fence_after();
+        const uint8_t* stage = smem + (uint32_t)(m % ST) * Ly.stage_bytes;
+        const uint32_t vb = smem_u32(a.v_alias ? stage : stage + Ly.k_bytes);
+        const uint32_t pbase = smem_u32(sP + pb * (kNH * kChunk * 2));
+        for (int blk = 0; blk < ndvb; ++blk) {
+          for (int ks = 0; ks < kChunk / 16; ++ks) {
+            const uint64_t ad = sdesc_sw128(vb + (2 * blk) * (kChunk * 128) + ks * 2048, kChunk * 128, 1024);
+            const uint64_t bd = sdesc_sw128(pbase + (ks >> 2) * (kNH * 128) + (ks & 3) * 32, 16, 1024);
+            umma_bf16(tbase + 32 + pb * (kNH * kMaxDvBlocks) + blk * kNH, ad, bd, IDESC_O, ks > 0);
           }
         }
-        if (nvalid == 0) {
-          // reading: no valid key -> zeros and -inf
-          for (int i = tid; i < nh * a.Dv; i += kAttnThreads) {
-            const int h = i / a.Dv, dv = i - h * a.Dv;
-            a.out[(t * a.Hq + h0 + h) * a.Dv + dv] = __float2bfloat16_rn(0.f);
-          }
-          if (a.lse != nullptr && tid < nh) a.lse[t * a.Hq + h0 + tid] = -INFINITY;
-          __syncthreads();
-          continue;
-        }
-        // ---- prologue: start the first ST chunks ----
-        for (int c = 0; c < ST; ++c) {
-          if (c < nchunks)
-            issue_chunk(a, g, c, nvalid, sIdx, smem + (uint32_t)c * stage_bytes,
-                        smem + (uint32_t)c * stage_bytes + Lay.k_stage, tid);
-          cp_async_commit();
-        }
-        float m[kNH], l[kNH], acc[kMaxDvBlocks][kNH], alpha[kNH];
-#pragma unroll
-        for (int h = 0; h < kNH; ++h) {
-          m[h] = -INFINITY;
-          l[h] = 0.f;
-#pragma unroll
-          for (int b = 0; b < kMaxDvBlocks; ++b) acc[b][h] = 0.f;
-        }
-        for (int c = 0; c < nchunks; ++c) {
-          const int st = c % ST;
-          uint8_t* sK = smem + (uint32_t)st * stage_bytes;
-          uint8_t* sV = a.v_alias ? sK : sK + Lay.k_stage;
-          cp_async_wait_pending(ST - 1);
-          fence_proxy_async_smem();
-          __syncthreads();
-          // ---- S^T = K . Q^T ----
-          if (tid == 0) {
+        umma_commit(&B.o_full[pb]);
+        umma_commit(&B.p_empty[pb]);
+        umma_commit(&B.kv_empty[m % ST]);
+        return true;
+      };
+      for (long long t = blockIdx.x; t < a.T && alive; t += gridDim.x, ++qi) {
+        const int b = qi & 1;
+        if (!mbar_wait(&B.idx_full[b], (qi >> 1) & 1, abort_flag, a.err)) { alive = false; break; }
+        const int nv = sNv[b];
+        mbar_arrive(&B.idx_empty[b]);
+        if (nv == 0) continue;
+        const int nchunks = (nv + kChunk - 1) / kChunk;
+        for (int sub = 0; sub < n_sub && alive; ++sub, ++u) {
+          const int qb = u & 1;
+          if (!mbar_wait(&B.q_full[qb], (u >> 1) & 1, abort_flag, a.err)) { alive = false; break; }
+          const uint32_t qbase = smem_u32(sQ + qb * (kNH * a.Dqk * 2));
+          for (int c = 0; c < nchunks; ++c, ++n) {
+            const int st = n % ST, sb = n & 1;
+            // with a single stage, chunk n can only be gathered once O of chunk n-1 is done
+            if (ST == 1 && c > 0 && !issue_o(n - 1)) { alive = false; break; }
+            if (!mbar_wait(&B.kv_full[st], (n / ST) & 1, abort_flag, a.err)) { alive = false; break; }
+            if (n >= 2 && !mbar_wait(&B.s_empty[sb], ((n >> 1) - 1) & 1, abort_flag, a.err)) { alive = false; break; }
+            fence_proxy_async_smem();   // gathered rows (generic-proxy writes) -> UMMA reads
             tc_fence_after();
-            const uint32_t kb = smem_u32(sK), qb = smem_u32(sQ);
+            const uint32_t kb = smem_u32(smem + (uint32_t)st * Ly.stage_bytes);
             for (int ks = 0; ks < a.Dqk / 16; ++ks) {
               const uint64_t ad = sdesc_sw128(kb + (ks >> 2) * (kChunk * 128) + (ks & 3) * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(qb + (ks >> 2) * (kNH * 128) + (ks & 3) * 32, 16, 1024);
-              umma_bf16(tS, ad, bd, IDESC_S, ks > 0);
+              const uint64_t bd = sdesc_sw128(qbase + (ks >> 2) * (kNH * 128) + (ks & 3) * 32, 16, 1024);
+              umma_bf16(tbase + sb * kNH, ad, bd, IDESC_S, ks > 0);
             }
-            umma_commit(&bar[0]);
+            umma_commit(&B.s_full[sb]);
+            if (c == nchunks - 1) umma_commit(&B.q_empty[qb]);
+            if (ST > 1 && c > 0 && !issue_o(n - 1)) { alive = false; break; }
           }
-          const bool ok_s = mbar_wait(&bar[0], ph_s, abort_flag, a.err);
-          ph_s ^= 1;
-          tc_fence_after();
-          float s[kNH];
-          tmem_ld16(tS + lane_addr, s);
-          tmem_ld_wait();
-          const int key = c * kChunk + warp * 32 + lane;
-          const bool kvalid = key < nvalid;
-          // ---- online softmax (base-2 exponent domain) ----
+          if (alive && !issue_o(n - 1)) alive = false;
+        }
+      }
+    }
+  } else {
+    // =========================== softmax + correction (warps 5..8) ===========================
+    const int sw = warp - 5;
+    const int lanerow = (warp & 3) * 32 + lane;      // TMEM lane: key of S, dv of O
+    const uint32_t lane_addr = tmem_lane_base(warp);
+    uint32_t n = 0, u = 0, qi = 0;
+    for (long long t = blockIdx.x; t < a.T; t += gridDim.x, ++qi) {
+      const int b = qi & 1;
+      mbar_wait(&B.idx_full[b], (qi >> 1) & 1, abort_flag, a.err);
+      const int nv = min(max(sNv[b], 0), a.W);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.idx_empty[b]);
+      const int nchunks = (nv + kChunk - 1) / kChunk;
+      if (nv == 0) {
+        // reading: a row without any valid key gives zeros and lse = -inf
+        for (int sub = 0; sub < n_sub; ++sub) {
+          const int g = sub / a.nhb, hb = sub - g * a.nhb;
+          const int h0 = (a.g0 + g) * a.G + hb * a.HB;
+          const int nh = min(a.HB, a.G - hb * a.HB);
+          __nv_bfloat16* orow = a.out + (t * a.Hq + h0) * (long long)a.Dv;
+          for (int blk = 0; blk < ndvb; ++blk)
+            for (int h = 0; h < nh; ++h) orow[(long long)h * a.Dv + blk * 128 + lanerow] = __float2bfloat16_rn(0.f);
+          if (a.lse != nullptr && lanerow < nh) a.lse[t * a.Hq + h0 + lanerow] = -INFINITY;
+        }
+        continue;
+      }
+      for (int sub = 0; sub < n_sub; ++sub, ++u) {
+        const int g = sub / a.nhb, hb = sub - g * a.nhb;
+        const int h0 = (a.g0 + g) * a.G + hb * a.HB;
+        const int nh = min(a.HB, a.G - hb * a.HB);
+        __nv_bfloat16* orow = a.out + (t * a.Hq + h0) * (long long)a.Dv;
+        float m[NH], l[NH], al_prev[NH], acc[kMaxDvBlocks][NH];
 #pragma unroll
-          for (int h = 0; h < kNH; ++h) {
-            s[h] = (kvalid && h < nh) ? s[h] * a.scale_log2 : -INFINITY;
-            const float mx = warp_max(s[h]);
-            if (lane == 0) sRed[warp * kNH + h] = mx;
-          }
-          if (__syncthreads_or(!ok_s)) break;   // every thread leaves together on a timeout
-          float p[kNH];
+        for (int h = 0; h < NH; ++h) {
+          m[h] = -INFINITY;
+          l[h] = 0.f;
+          al_prev[h] = 1.f;
 #pragma unroll
-          for (int h = 0; h < kNH; ++h) {
-            const float cm = fmaxf(fmaxf(sRed[h], sRed[kNH + h]), fmaxf(sRed[2 * kNH + h], sRed[3 * kNH + h]));
-            const float mn = fmaxf(m[h], cm);
-            const float base = mn == -INFINITY ? 0.f : mn;
-            alpha[h] = exp2f(m[h] - base);
-            p[h] = exp2f(s[h] - base);
-            l[h] = l[h] * alpha[h] + p[h];
-            m[h] = mn;
-          }
-          // P (bf16) as the K-major B operand: row h, key column (warp*32 + lane)
-          {
-            const int r = warp * 32 + lane;
-#pragma unroll
-            for (int h = 0; h < kNH; ++h)
-              *reinterpret_cast<__nv_bfloat16*>(sP + sw128_offset(h, r, kNH)) = __float2bfloat16_rn(p[h]);
-          }
-          tc_fence_before();
-          fence_proxy_async_smem();
-          __syncthreads();
-          // ---- O^T_chunk = V^T . P^T ----
-          if (tid == 0) {
-            tc_fence_after();
-            const uint32_t vb = smem_u32(sV), pb = smem_u32(sP);
-            for (int b = 0; b < ndvb; ++b) {
-              for (int ks = 0; ks < kChunk / 16; ++ks) {
-                const uint64_t ad = sdesc_sw128(vb + (2 * b) * (kChunk * 128) + ks * 2048, kChunk * 128, 1024);
-                const uint64_t bd = sdesc_sw128(pb + (ks >> 2) * (kNH * 128) + (ks & 3) * 32, 16, 1024);
-                umma_bf16(tO + b * kNH, ad, bd, IDESC_O, ks > 0);
-              }
-            }
-            umma_commit(&bar[1]);
-          }
-          const bool ok_o = mbar_wait(&bar[1], ph_o, abort_flag, a.err);
-          ph_o ^= 1;
+          for (int blk = 0; blk < kMaxDvBlocks; ++blk) acc[blk][h] = 0.f;
+        }
+        auto correct = [&](uint32_t mm) {
+          const int ob = mm & 1;
+          mbar_wait(&B.o_full[ob], (mm >> 1) & 1, abort_flag, a.err);
           tc_fence_after();
 #pragma unroll
-          for (int b = 0; b < kMaxDvBlocks; ++b) {
-            if (b < ndvb) {
-              float o[kNH];
-              tmem_ld16(tO + b * kNH + lane_addr, o);
+          for (int blk = 0; blk < kMaxDvBlocks; ++blk)
+            if (blk < ndvb) {
+              float o[NH];
+              tmem_ld_nh<NH>(tbase + 32 + ob * (kNH * kMaxDvBlocks) + blk * kNH + lane_addr, o);
               tmem_ld_wait();
 #pragma unroll
-              for (int h = 0; h < kNH; ++h) acc[b][h] = acc[b][h] * alpha[h] + o[h];
+              for (int h = 0; h < NH; ++h) acc[blk][h] = fmaf(acc[blk][h], al_prev[h], o[h]);
             }
-          }
           tc_fence_before();
-          // every thread is done with this stage's smem and with S/O in TMEM
-          if (__syncthreads_or(!ok_o)) break;
-          // ---- refill the stage just consumed ----
-          const int cn = c + ST;
-          if (cn < nchunks)
-            issue_chunk(a, g, cn, nvalid, sIdx, smem + (uint32_t)st * stage_bytes,
-                        smem + (uint32_t)st * stage_bytes + Lay.k_stage, tid);
-          cp_async_commit();
-        }
-        cp_async_wait_pending(0);
-        if (*abort_flag) break;
-        // ---- finalize: row sums across the 128 key lanes, normalise, store ----
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B.o_empty[ob]);
+        };
+        for (int c = 0; c < nchunks; ++c, ++n) {
+          const int sb = n & 1;
+          mbar_wait(&B.s_full[sb], (n >> 1) & 1, abort_flag, a.err);
+          tc_fence_after();
+          float s[NH];
+          tmem_ld_nh<NH>(tbase + sb * kNH + lane_addr, s);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B.s_empty[sb]);
+          const bool kvalid = c * kChunk + lanerow < nv;
+          float* red = sRed + sb * (4 * kNH);
 #pragma unroll
-        for (int h = 0; h < kNH; ++h) {
-          const float sm = warp_sum(l[h]);
-          if (lane == 0) sRed[warp * kNH + h] = sm;
-        }
-        __syncthreads();
-        float inv[kNH];
-#pragma unroll
-        for (int h = 0; h < kNH; ++h) {
-          const float tot = sRed[h] + sRed[kNH + h] + sRed[2 * kNH + h] + sRed[3 * kNH + h];
-          inv[h] = tot > 0.f ? 1.f / tot : 0.f;
-          l[h] = tot;
-        }
-        const int dvl = warp * 32 + lane;
-#pragma unroll
-        for (int b = 0; b < kMaxDvBlocks; ++b) {
-          if (b < ndvb) {
-#pragma unroll
-            for (int h = 0; h < kNH; ++h)
-              if (h < nh) a.out[(t * a.Hq + h0 + h) * a.Dv + b * 128 + dvl] = __float2bfloat16_rn(acc[b][h] * inv[h]);
+          for (int h = 0; h < NH; ++h) {
+            s[h] = (kvalid && h < nh) ? s[h] * a.scale_log2 : -INFINITY;
+            const float mx = warp_max(s[h]);
+            if (lane == 0) red[sw * kNH + h] = mx;
           }
-        }
-        if (a.lse != nullptr && tid < kNH) {
-          // lse = ln(2) * (m + log2(l)) with m in the base-2 domain
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B.red[sb]);
+          mbar_wait(&B.red[sb], (n >> 1) & 1, abort_flag, a.err);
+          float al[NH], p[NH];
 #pragma unroll
-          for (int h = 0; h < kNH; ++h)
-            if (h == tid && h < nh)
-              a.lse[t * a.Hq + h0 + h] = l[h] > 0.f ? (m[h] + log2f(l[h])) * 0.69314718055994531f : -INFINITY;
+          for (int h = 0; h < NH; ++h) {
+            const float cm = fmaxf(fmaxf(red[h], red[kNH + h]), fmaxf(red[2 * kNH + h], red[3 * kNH + h]));
+            const float mn = fmaxf(m[h], cm);
+            const float base = mn == -INFINITY ? 0.f : mn;
+            al[h] = exp2f(m[h] - base);
+            p[h] = exp2f(s[h] - base);
+            l[h] = fmaf(l[h], al[h], p[h]);
+            m[h] = mn;
+          }
+          if (n >= 2) mbar_wait(&B.p_empty[sb], ((n >> 1) - 1) & 1, abort_flag, a.err);
+          uint8_t* pdst = sP + sb * (kNH * kChunk * 2);
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+            *reinterpret_cast<__nv_bfloat16*>(pdst + sw128_offset(h, lanerow, kNH)) = __float2bfloat16_rn(p[h]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B.p_full[sb]);
+          if (c > 0) correct(n - 1);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) al_prev[h] = al[h];
         }
-        __syncthreads();
+        correct(n - 1);
+        // ---- finalize: row sums over the 128 key lanes, normalise, store ----
+        const int fb = u & 1;
+        float* fin = sFin + fb * (4 * kNH);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const float sm = warp_sum(l[h]);
+          if (lane == 0) fin[sw * kNH + h] = sm;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.fin[fb]);
+        mbar_wait(&B.fin[fb], (u >> 1) & 1, abort_flag, a.err);
+        float inv[NH], tot[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          tot[h] = fin[h] + fin[kNH + h] + fin[2 * kNH + h] + fin[3 * kNH + h];
+          inv[h] = tot[h] > 0.f ? 1.f / tot[h] : 0.f;
+        }
+#pragma unroll
+        for (int blk = 0; blk < kMaxDvBlocks; ++blk)
+          if (blk < ndvb) {
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+              if (h < nh) orow[(long long)h * a.Dv + blk * 128 + lanerow] = __float2bfloat16_rn(acc[blk][h] * inv[h]);
+          }
+        if (a.lse != nullptr && lanerow < nh) {
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+            if (h == lanerow)
+              a.lse[t * a.Hq + h0 + h] = tot[h] > 0.f ? (m[h] + log2f(tot[h])) * 0.69314718055994531f : -INFINITY;
+        }
       }
     }
   }
-  cp_async_wait_pending(0);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 4) {
     tc_fence_after();
-    tmem_dealloc(tbase, 128);
+    tmem_dealloc(tbase, 256);
   }
 }
 
 AttnPlan plan_attn(const AttnArgs& a, int num_sms) {
   AttnPlan p{};
   p.items = a.T;
-  int st = 3;
-  while (st > 1 && attn_smem_layout(a.Dqk, a.Dv, a.W, st, a.v_alias).total > 227 * 1024) --st;
+  int st = 4;
+  while (st > 1 && attn_layout(a.Dqk, a.Dv, a.W, st, a.v_alias).total > 227 * 1024) --st;
   p.stages = st;
-  p.smem = attn_smem_layout(a.Dqk, a.Dv, a.W, st, a.v_alias).total;
-  const int per_sm = p.smem <= 113 * 1024 ? 2 : 1;
-  const long long g = (long long)num_sms * per_sm;
-  p.grid = (int)(p.items < g ? p.items : g);
+  p.smem = attn_layout(a.Dqk, a.Dv, a.W, st, a.v_alias).total;
+  p.grid = (int)(a.T < num_sms ? a.T : num_sms);
   if (p.grid < 1) p.grid = 1;
+  p.nh_class = a.HB <= 4 ? 4 : (a.HB <= 8 ? 8 : 16);
   return p;
 }
 
 cudaError_t configure_attn_kernel(size_t smem) {
-  return cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attn_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attn_fwd_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
-cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream) {
+cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, const AttnPlan& p, cudaStream_t stream) {
   AttnArgs b = a;
   b.stages = p.stages;
-  attn_fwd_kernel<<<p.grid, kAttnThreads, p.smem, stream>>>(b);
+  switch (p.nh_class) {
+    case 4: attn_fwd_kernel<4><<<p.grid, kAttnThreads, p.smem, stream>>>(maps, b); break;
+    case 8: attn_fwd_kernel<8><<<p.grid, kAttnThreads, p.smem, stream>>>(maps, b); break;
+    default: attn_fwd_kernel<16><<<p.grid, kAttnThreads, p.smem, stream>>>(maps, b); break;
+  }
   return cudaGetLastError();
 }
 

@@ -155,9 +155,10 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
 // the MMAs of tile j+1. The epilogue thread of lane b reads its 256 columns and reduces
 // each query's heads in order: s = sum_h w[t,h] * max(acc, 0) (FP32 FMA chain).
 //
-// Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 2..5 = epilogue.
+// Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 2..9 = epilogue (two warps per TMEM
+// lane quarter, each taking half of the 256 columns).
 // =====================================================================================
-constexpr int kScoreThreads = 192;
+constexpr int kScoreThreads = 320;   // producer, MMA, 8 epilogue warps
 constexpr int kScoreN = 256;          // (query, head) columns per tile
 constexpr int kScoreM = 128;          // key blocks per tile
 
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     for (int s = 0; s < ST; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     mbar_init(bfull, 1);
     mbar_init(&tfull[0], 1); mbar_init(&tfull[1], 1);
-    mbar_init(&tempty[0], 4); mbar_init(&tempty[1], 4);
+    mbar_init(&tempty[0], 8); mbar_init(&tempty[1], 8);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -285,30 +286,63 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue: warps 2..5 ----------------
+    // ---------------- epilogue: warps 2..9 ----------------
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    // a query's Hi columns never straddle the two halves unless Hi > 128: then half 0 does all
+    const int col0 = Hi > 128 ? 0 : half * (kScoreN / 2);
+    const int ncols = Hi > 128 ? (half == 0 ? kScoreN : 0) : kScoreN / 2;
     const uint32_t lane_addr = tmem_lane_base(warp);
     for (int j = 0; j < nbt; ++j) {
       const int buf = j & 1;
       if (!mbar_wait(&tfull[buf], (j >> 1) & 1, abort_flag, a.err)) break;
       tc_fence_after();
       const int blk = j * kScoreM + quarter * 32 + lane;
-      float acc = 0.f;
-      for (int cc = 0; cc < kScoreN / 32; ++cc) {
+      float carry = 0.f;
+      for (int cc = col0; cc < col0 + ncols; cc += 32) {
         float v[32];
-        tmem_ld32(tbase + lane_addr + buf * kScoreN + cc * 32, v);
+        tmem_ld32(tbase + lane_addr + buf * kScoreN + cc, v);
+        const float4* w4 = reinterpret_cast<const float4*>(sW + cc);
+        float prod[32];
         tmem_ld_wait();
 #pragma unroll
+        for (int k4 = 0; k4 < 8; ++k4) {
+          const float4 ww = w4[k4];
+          prod[4 * k4 + 0] = ww.x * fmaxf(v[4 * k4 + 0], 0.f);
+          prod[4 * k4 + 1] = ww.y * fmaxf(v[4 * k4 + 1], 0.f);
+          prod[4 * k4 + 2] = ww.z * fmaxf(v[4 * k4 + 2], 0.f);
+          prod[4 * k4 + 3] = ww.w * fmaxf(v[4 * k4 + 3], 0.f);
+        }
+        // pairwise sums inside each query's group of Hi columns (log depth)
+#pragma unroll
+        for (int lvl = 0; lvl < 5; ++lvl) {
+          const int stride = 1 << lvl;
+          if (stride < Hi) {
+#pragma unroll
+            for (int k = 0; k < 32; k += 2 * stride) prod[k] += prod[k + stride];
+          }
+        }
+#pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const int col = cc * 32 + k;
-          acc = fmaf(sW[col], fmaxf(v[k], 0.f), acc);
-          if ((col & (Hi - 1)) == Hi - 1) {
-            const int qi = col / Hi;
+          if (Hi <= 32) {
+            if ((k & (Hi - 1)) == 0) {
+              const int qi = (cc + k) / Hi;
+              if (qi < nq) {
+                const int nvis = (tau0 + qi + 1) / a.c;
+                if (blk < nvis) a.scores[(long long)(t0 + qi) * a.ldS + blk] = prod[k];
+              }
+            }
+          }
+        }
+        if (Hi > 32) {
+          carry += prod[0];
+          if (((cc + 32) & (Hi - 1)) == 0) {
+            const int qi = cc / Hi;
             if (qi < nq) {
               const int nvis = (tau0 + qi + 1) / a.c;
-              if (blk < nvis) a.scores[(long long)(t0 + qi) * a.ldS + blk] = acc;
+              if (blk < nvis) a.scores[(long long)(t0 + qi) * a.ldS + blk] = carry;
             }
-            acc = 0.f;
+            carry = 0.f;
           }
         }
       }

@@ -39,6 +39,13 @@ cudaError_t launch_compose_window(const int32_t* route, int W, const int32_t* cu
                                   int32_t* out, int32_t* err, cudaStream_t stream);
 
 // Gathered sparse attention.
+constexpr int kMaxKvMaps = 8;   // KV heads handled by one launch (one gather map per head)
+
+struct AttnMaps {
+  CUtensorMap k[kMaxKvMaps];    // [Tk rows x Dqk] of KV head g0+i, box {64, 1}, SW128
+  CUtensorMap v[kMaxKvMaps];    // [Tk rows x Dv]  (unused when v aliases k)
+};
+
 struct AttnArgs {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
@@ -51,8 +58,9 @@ struct AttnArgs {
   int32_t* err;
   int T, Tk, Hq, Hkv, Dqk, Dv, W;
   int G;          // query heads per KV head
-  int HB;         // query heads handled by one work item (<= 16)
+  int HB;         // query heads handled by one sub-item (<= 16)
   int nhb;        // head blocks per KV head
+  int g0, ng;     // KV heads [g0, g0+ng) handled by this launch
   int v_alias;    // 1: values are the first Dv dims of the gathered key rows
   int stages;
   float scale_log2;  // scale * log2(e)
@@ -63,10 +71,11 @@ struct AttnPlan {
   size_t smem;
   int grid;
   long long items;
+  int nh_class;   // 4, 8 or 16: head loop length of the softmax warps
 };
 
 AttnPlan plan_attn(const AttnArgs& a, int num_sms);
 cudaError_t configure_attn_kernel(size_t smem);
-cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
+cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 
 }  // namespace irs
