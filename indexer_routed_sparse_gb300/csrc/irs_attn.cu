@@ -88,6 +88,17 @@ __device__ __forceinline__ void tmem_ld_nh(uint32_t taddr, float (&v)[NH]) {
 // thread i % 128). ids[r] are valid row indices.
 __device__ __forceinline__ void gather_rows(uint32_t dst, const __nv_bfloat16* src, int64_t row_stride,
                                             const int32_t* ids, int rows, int kc, int ptid) {
+  if (kProducerThreads % kc == 0 && ((kProducerThreads / kc) & 7) == 0) {
+    // fixed 16-byte column per thread; rows step by a multiple of 8, so the swizzle is fixed
+    const int j = ptid % kc;
+    const int dr = kProducerThreads / kc;
+    int r = ptid / kc;
+    uint32_t d = dst + sw128_offset(r, j * 8, kChunk);
+    const __nv_bfloat16* sj = src + j * 8;
+#pragma unroll 4
+    for (; r < rows; r += dr, d += dr * 128) cp_async_16(d, sj + (int64_t)ids[r] * row_stride, 16u);
+    return;
+  }
   int r = ptid / kc, j = ptid - (ptid / kc) * kc;
   const int dr = kProducerThreads / kc, dj = kProducerThreads - dr * kc;
   while (r < rows) {

@@ -155,10 +155,10 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
 // the MMAs of tile j+1. The epilogue thread of lane b reads its 256 columns and reduces
 // each query's heads in order: s = sum_h w[t,h] * max(acc, 0) (FP32 FMA chain).
 //
-// Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 2..9 = epilogue (two warps per TMEM
-// lane quarter, each taking half of the 256 columns).
+// Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 2..17 = epilogue (four warps per
+// TMEM lane quarter, each taking a quarter of the 256 columns, or whole queries if Hi > 64).
 // =====================================================================================
-constexpr int kScoreThreads = 320;   // producer, MMA, 8 epilogue warps
+constexpr int kScoreThreads = 576;   // producer, MMA, 16 epilogue warps
 constexpr int kScoreN = 256;          // (query, head) columns per tile
 constexpr int kScoreM = 128;          // key blocks per tile
 
@@ -174,7 +174,7 @@ struct ScoreArgs {
   int ndocs, T, Hi, c, kb, QT, tau_sparse, stages;
 };
 
-template <int DI>
+template <int DI, int HI>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, ScoreArgs a) {
   constexpr int KATOMS = DI / 64;
@@ -190,7 +190,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   uint8_t* sA = smem + B_BYTES;
   const int ST = a.stages;
   float* sW = reinterpret_cast<float*>(sA + (size_t)ST * A_STAGE);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sW + kScoreN);
+  int* sNvis = reinterpret_cast<int*>(sW + kScoreN);                 // [QT] visible blocks per query
+  uint64_t* full = reinterpret_cast<uint64_t*>(sNvis + kScoreN);
   uint64_t* empty = full + ST;
   uint64_t* bfull = empty + ST;
   uint64_t* tfull = bfull + 1;
@@ -212,19 +213,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int nvis_last = (tau0 + nq) / a.c;
   const int nbt = (nvis_last + kScoreM - 1) / kScoreM;
   const int blk0 = a.blk_off[d];
-  const int Hi = a.Hi;
+  constexpr int Hi = HI;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // per-tile head weights (columns of the accumulator are (query, head) = row-major [QT][Hi])
   for (int i = tid; i < kScoreN; i += kScoreThreads) {
     const long long gi = (long long)t0 * Hi + i;
     sW[i] = (i < a.QT * Hi && gi < (long long)a.T * Hi) ? a.w[gi] : 0.f;
+    sNvis[i] = i < nq ? (tau0 + i + 1) / a.c : 0;   // rows past the document see nothing
   }
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     mbar_init(bfull, 1);
     mbar_init(&tfull[0], 1); mbar_init(&tfull[1], 1);
-    mbar_init(&tempty[0], 8); mbar_init(&tempty[1], 8);
+    mbar_init(&tempty[0], 16); mbar_init(&tempty[1], 16);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -286,63 +288,55 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue: warps 2..9 ----------------
+    // ---------------- epilogue: warps 2..17 ----------------
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
-    // a query's Hi columns never straddle the two halves unless Hi > 128: then half 0 does all
-    const int col0 = Hi > 128 ? 0 : half * (kScoreN / 2);
-    const int ncols = Hi > 128 ? (half == 0 ? kScoreN : 0) : kScoreN / 2;
+    const int part = (warp - 2) >> 2;
+    // each warp takes kHalfCols consecutive columns; a query's Hi columns stay in one warp
+    constexpr int kHalfCols = HI > 64 ? HI : 64;
+    const int col0 = part * kHalfCols;
+    const bool active = col0 < kScoreN;
     const uint32_t lane_addr = tmem_lane_base(warp);
     for (int j = 0; j < nbt; ++j) {
       const int buf = j & 1;
       if (!mbar_wait(&tfull[buf], (j >> 1) & 1, abort_flag, a.err)) break;
       tc_fence_after();
-      const int blk = j * kScoreM + quarter * 32 + lane;
-      float carry = 0.f;
-      for (int cc = col0; cc < col0 + ncols; cc += 32) {
-        float v[32];
-        tmem_ld32(tbase + lane_addr + buf * kScoreN + cc, v);
-        const float4* w4 = reinterpret_cast<const float4*>(sW + cc);
-        float prod[32];
-        tmem_ld_wait();
+      if (active) {
+        const int blk = j * kScoreM + quarter * 32 + lane;
+        float carry = 0.f;
+#pragma unroll 1
+        for (int cc = col0; cc < col0 + kHalfCols; cc += 32) {
+          float v[32];
+          tmem_ld32(tbase + lane_addr + buf * kScoreN + cc, v);
+          const float4* w4 = reinterpret_cast<const float4*>(sW + cc);
+          float prod[32];
+          tmem_ld_wait();
 #pragma unroll
-        for (int k4 = 0; k4 < 8; ++k4) {
-          const float4 ww = w4[k4];
-          prod[4 * k4 + 0] = ww.x * fmaxf(v[4 * k4 + 0], 0.f);
-          prod[4 * k4 + 1] = ww.y * fmaxf(v[4 * k4 + 1], 0.f);
-          prod[4 * k4 + 2] = ww.z * fmaxf(v[4 * k4 + 2], 0.f);
-          prod[4 * k4 + 3] = ww.w * fmaxf(v[4 * k4 + 3], 0.f);
-        }
-        // pairwise sums inside each query's group of Hi columns (log depth)
+          for (int k4 = 0; k4 < 8; ++k4) {
+            const float4 ww = w4[k4];
+            prod[4 * k4 + 0] = ww.x * fmaxf(v[4 * k4 + 0], 0.f);
+            prod[4 * k4 + 1] = ww.y * fmaxf(v[4 * k4 + 1], 0.f);
+            prod[4 * k4 + 2] = ww.z * fmaxf(v[4 * k4 + 2], 0.f);
+            prod[4 * k4 + 3] = ww.w * fmaxf(v[4 * k4 + 3], 0.f);
+          }
+          // pairwise sums inside each query's group of Hi columns (log depth)
 #pragma unroll
-        for (int lvl = 0; lvl < 5; ++lvl) {
-          const int stride = 1 << lvl;
-          if (stride < Hi) {
+          for (int stride = 1; stride < 32 && stride < HI; stride *= 2) {
 #pragma unroll
             for (int k = 0; k < 32; k += 2 * stride) prod[k] += prod[k + stride];
           }
-        }
+          if constexpr (HI <= 32) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          if (Hi <= 32) {
-            if ((k & (Hi - 1)) == 0) {
-              const int qi = (cc + k) / Hi;
-              if (qi < nq) {
-                const int nvis = (tau0 + qi + 1) / a.c;
-                if (blk < nvis) a.scores[(long long)(t0 + qi) * a.ldS + blk] = prod[k];
-              }
+            for (int k = 0; k < 32; k += HI) {
+              const int qi = (cc + k) / HI;
+              if (blk < sNvis[qi]) a.scores[(long long)(t0 + qi) * a.ldS + blk] = prod[k];
             }
-          }
-        }
-        if (Hi > 32) {
-          carry += prod[0];
-          if (((cc + 32) & (Hi - 1)) == 0) {
-            const int qi = cc / Hi;
-            if (qi < nq) {
-              const int nvis = (tau0 + qi + 1) / a.c;
-              if (blk < nvis) a.scores[(long long)(t0 + qi) * a.ldS + blk] = carry;
+          } else {
+            carry += prod[0];
+            if (((cc + 32) & (HI - 1)) == 0) {
+              const int qi = cc / HI;
+              if (blk < sNvis[qi]) a.scores[(long long)(t0 + qi) * a.ldS + blk] = carry;
+              carry = 0.f;
             }
-            carry = 0.f;
           }
         }
       }
@@ -391,8 +385,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_expand_kernel(TopkArgs a) {
   int32_t* pfx = reinterpret_cast<int32_t*>(eqw + nw_cap);
   const int kb = a.budget / a.c;
   int32_t* sel = pfx + nw_cap;
-  __shared__ int hist[256];
-  __shared__ int s_digit, s_above;
+  __shared__ int hist[2 * 4 * 256];   // two buffers x one histogram per warp
+  __shared__ int s_digit, s_above, s_bin;
+  __shared__ uint32_t s_diff[4];
 
   if (a.meta != nullptr && a.meta[0] != 1) return;
   const int t = blockIdx.x;
@@ -414,25 +409,49 @@ __global__ void __launch_bounds__(kTopkThreads) topk_expand_kernel(TopkArgs a) {
 
   if (sparse) {
     const float* row = a.scores + (long long)t * a.ldS;
-    for (int i = tid; i < nvis; i += kTopkThreads) keys[i] = order_key(__ldg(row + i));
+    uint32_t diff = 0;
+    const uint32_t key0 = order_key(__ldg(row));
+    for (int i = tid; i < nvis; i += kTopkThreads) {
+      const uint32_t k = order_key(__ldg(row + i));
+      keys[i] = k;
+      diff |= k ^ key0;
+    }
+    // bits above the highest differing bit are common to every key of the row: the radix
+    // passes start below them (scores of one row share sign and most exponent bits)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) diff |= __shfl_xor_sync(0xffffffffu, diff, o);
+    if (lane == 0) s_diff[warp] = diff;
+    for (int i = tid; i < 1024; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
-    // ---- radix select: find the key of the kb-th largest element ----
-    uint32_t prefix = 0, mask = 0;
+    diff = s_diff[0] | s_diff[1] | s_diff[2] | s_diff[3];
+    // ---- radix select: the kb-th largest key, MSB first, 8-bit digits ----
+    const int hb = diff ? 31 - __clz(diff) : -1;
+    // all keys equal (hb < 0): the threshold is that key and the lowest indices win
+    uint32_t mask = hb < 0 ? 0xFFFFFFFFu : (hb >= 31 ? 0u : ~((2u << hb) - 1u));
+    uint32_t prefix = key0 & mask;
     int rem = kb;
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      hist[tid] = 0;
-      hist[tid + 128] = 0;
-      __syncthreads();
+    int buf = 0;
+    for (int top = hb; top >= 0; top -= 8) {
+      const int shift = top - 7 > 0 ? top - 7 : 0;
+      const int width = top - shift + 1;
+      const uint32_t dmask = (1u << width) - 1u;
+      int* hw = hist + buf * 1024 + warp * 256;
       for (int i = tid; i < nvis; i += kTopkThreads) {
         const uint32_t k = keys[i];
-        if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255], 1);
+        if ((k & mask) == prefix) atomicAdd(&hw[(k >> shift) & dmask], 1);
       }
+      // clear the other histogram for the next pass while this one is counted
+      for (int i = tid; i < 1024; i += kTopkThreads) hist[(buf ^ 1) * 1024 + i] = 0;
       __syncthreads();
       if (warp == 0) {
+        const int* h = hist + buf * 1024;
         int loc[8], lsum = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) { loc[i] = hist[255 - 8 * lane - i]; lsum += loc[i]; }
+        for (int i = 0; i < 8; ++i) {
+          const int bin = 255 - 8 * lane - i;
+          loc[i] = h[bin] + h[256 + bin] + h[512 + bin] + h[768 + bin];
+          lsum += loc[i];
+        }
         int incl = lsum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -444,25 +463,29 @@ __global__ void __launch_bounds__(kTopkThreads) topk_expand_kernel(TopkArgs a) {
           int run = excl;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            if (run + loc[i] >= rem) { s_digit = 255 - 8 * lane - i; s_above = run; break; }
+            if (run + loc[i] >= rem) { s_digit = 255 - 8 * lane - i; s_above = run; s_bin = loc[i]; break; }
             run += loc[i];
           }
         }
       }
       __syncthreads();
       prefix |= (uint32_t)s_digit << shift;
-      mask |= 0xFFu << shift;
+      mask |= dmask << shift;
       rem -= s_above;
-      __syncthreads();
+      buf ^= 1;
+      // the threshold bin is taken whole: no lower digit can change the selection
+      if (s_bin == rem) break;
     }
-    const uint32_t thr = prefix;       // key of the kb-th largest score
+    // selected: (key & mask) > prefix, plus the `rem` lowest-index keys with (key & mask) == prefix
+    const uint32_t thr = prefix;
     // ---- bitmap words of "greater" and "equal" elements ----
     const int nw = (nvis + 31) / 32;
     for (int base = 0; base < nw * 32; base += kTopkThreads) {
       const int i = base + tid;
       const uint32_t k = i < nvis ? keys[i] : 0u;
-      const uint32_t g = __ballot_sync(0xffffffffu, i < nvis && k > thr);
-      const uint32_t q = __ballot_sync(0xffffffffu, i < nvis && k == thr);
+      const uint32_t km = k & mask;
+      const uint32_t g = __ballot_sync(0xffffffffu, i < nvis && km > thr);
+      const uint32_t q = __ballot_sync(0xffffffffu, i < nvis && km == thr);
       const int wi = (base >> 5) + warp;
       if (lane == 0 && wi < nw) { gtw[wi] = g; eqw[wi] = q; }
     }
@@ -521,18 +544,23 @@ __global__ void __launch_bounds__(kTopkThreads) topk_expand_kernel(TopkArgs a) {
   }
   // ---- route row: [selected blocks x c tokens | -1 ...][tail tokens | -1 ...] ----
   const int c = a.c;
-  for (int slot = tid; slot < W; slot += kTopkThreads) {
-    int v = -1;
-    if (slot < nsel * c) {
-      const int r = slot / c;
-      const int j = slot - r * c;
+  const int nblk_slots = nsel * c;
+  if ((c & (c - 1)) == 0) {
+    const int cs = __ffs(c) - 1;
+    for (int slot = tid; slot < nblk_slots; slot += kTopkThreads) {
+      const int r = slot >> cs;
       const int b = sparse ? sel[r] : r;
-      v = s + b * c + j;
-    } else if (slot >= a.budget) {
-      const int j = slot - a.budget;
-      if (j < ntail) v = s + nvis * c + j;
+      out[slot] = s + (b << cs) + (slot & (c - 1));
     }
-    out[slot] = v;
+  } else {
+    for (int r = tid; r < nsel; r += kTopkThreads) {
+      const int b = sparse ? sel[r] : r;
+      for (int j = 0; j < c; ++j) out[r * c + j] = s + b * c + j;
+    }
+  }
+  for (int slot = nblk_slots + tid; slot < W; slot += kTopkThreads) {
+    const int j = slot - a.budget;
+    out[slot] = (j >= 0 && j < ntail) ? s + nvis * c + j : -1;
   }
 }
 
@@ -569,6 +597,29 @@ __global__ void __launch_bounds__(128) compose_window_kernel(const int32_t* __re
 // =====================================================================================
 // host launchers
 // =====================================================================================
+template <int DI>
+static cudaError_t launch_score_di(int Hi, int grid, size_t smem, cudaStream_t st, const CUtensorMap& tq,
+                                   const CUtensorMap& tk, const ScoreArgs& sa) {
+  switch (Hi) {
+    case 1: score_kernel<DI, 1><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
+    case 2: score_kernel<DI, 2><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
+    case 4: score_kernel<DI, 4><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
+    case 8: score_kernel<DI, 8><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
+    case 16: score_kernel<DI, 16><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
+    case 32: score_kernel<DI, 32><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
+    case 64: score_kernel<DI, 64><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
+    case 128: score_kernel<DI, 128><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
+    default: score_kernel<DI, 256><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
+  }
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_score(int Di, int Hi, int grid, size_t smem, cudaStream_t st, const CUtensorMap& tq,
+                                const CUtensorMap& tk, const ScoreArgs& sa) {
+  return Di == 64 ? launch_score_di<64>(Hi, grid, smem, st, tq, tk, sa)
+                  : launch_score_di<128>(Hi, grid, smem, st, tq, tk, sa);
+}
+
 IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len, bool with_scores) {
   IndexPlan p{};
   p.kb = budget / c;
@@ -593,7 +644,7 @@ IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int ma
   p.stages = Di == 64 ? 6 : 4;
   const size_t b_bytes = (size_t)kScoreN * Di * 2;
   const size_t a_bytes = (size_t)p.stages * kScoreM * Di * 2;
-  p.score_smem = 1024 + b_bytes + a_bytes + kScoreN * 4 + (2 * p.stages + 5) * 8 + 16;
+  p.score_smem = 1024 + b_bytes + a_bytes + kScoreN * 8 + (2 * p.stages + 5) * 8 + 16;
   p.topk_smem = topk_smem_bytes(p.ldS, p.kb);
   return p;
 }
@@ -621,11 +672,8 @@ cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv
   }
   ScoreArgs sa{w, cu, blk_off, tile_off, meta, scores, ldS, err, ndocs, T, Hi, c, p.kb, p.QT, p.tau_sparse,
                p.stages};
-  if (Di == 64) {
-    score_kernel<64><<<p.score_tiles_cap, kScoreThreads, p.score_smem, stream>>>(tm_q, tm_k, sa);
-  } else {
-    score_kernel<128><<<p.score_tiles_cap, kScoreThreads, p.score_smem, stream>>>(tm_q, tm_k, sa);
-  }
+  const cudaError_t le = launch_score(Di, Hi, p.score_tiles_cap, p.score_smem, stream, tm_q, tm_k, sa);
+  if (le != cudaSuccess) return le;
   TopkArgs ta{scores, ldS, cu, meta, route, err, ndocs, T, c, budget, max_doc_len, (int)p.ldS};
   topk_expand_kernel<<<T, kTopkThreads, p.topk_smem, stream>>>(ta);
   return cudaGetLastError();
@@ -646,10 +694,25 @@ cudaError_t launch_compose_window(const int32_t* route, int W, const int32_t* cu
   return cudaGetLastError();
 }
 
+template <int DI, int HI>
+static cudaError_t score_attr(size_t smem) {
+  return cudaFuncSetAttribute(score_kernel<DI, HI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+template <int DI>
+static cudaError_t score_attr_all(size_t smem) {
+  cudaError_t e = cudaSuccess;
+  for (cudaError_t x : {score_attr<DI, 1>(smem), score_attr<DI, 2>(smem), score_attr<DI, 4>(smem),
+                        score_attr<DI, 8>(smem), score_attr<DI, 16>(smem), score_attr<DI, 32>(smem),
+                        score_attr<DI, 64>(smem), score_attr<DI, 128>(smem), score_attr<DI, 256>(smem)})
+    if (x != cudaSuccess) e = x;
+  return e;
+}
+
 cudaError_t configure_score_kernels(size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(score_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = score_attr_all<64>(smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(score_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return score_attr_all<128>(smem);
 }
 
 cudaError_t configure_topk_kernel(size_t smem) {

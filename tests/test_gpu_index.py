@@ -136,3 +136,26 @@ def test_malformed_cu_seqlens_sets_the_device_flag(irs):
     assert irs.read_device_errors(dev) & irs.DEVERR_CU_SEQLENS
     # the context is still usable afterwards
     run_index(irs, wl)
+
+
+@pytest.mark.parametrize("kind", ["constant", "two_values", "signed_zero", "negative", "wide_range"])
+def test_topk_degenerate_scores_bit_exact(irs, kind):
+    """Ties everywhere, -0/+0, negative and widely spread scores: routes equal the oracle's."""
+    rng = np.random.default_rng(len(kind))
+    cu = np.asarray([0, 700, 2000], np.int32)
+    T, c, budget = 2000, 2, 64
+    ld = 1300 // c
+    if kind == "constant":
+        sc = np.full((T, ld), 0.75, np.float32)
+    elif kind == "two_values":
+        sc = rng.choice(np.asarray([1.0, 2.0], np.float32), size=(T, ld))
+    elif kind == "signed_zero":
+        sc = rng.choice(np.asarray([0.0, -0.0, 1e-30], np.float32), size=(T, ld))
+    elif kind == "negative":
+        sc = -rng.random((T, ld), dtype=np.float32)
+    else:
+        sc = (rng.standard_normal((T, ld)) * np.exp(rng.uniform(-30, 30, (T, ld)))).astype(np.float32)
+    dev = torch.device("cuda", 0)
+    r = irs.topk_from_scores(torch.from_numpy(sc).to(dev), torch.from_numpy(cu).to(dev), c, budget)
+    irs.check_device_errors(dev)
+    np.testing.assert_array_equal(r.cpu().numpy(), O.routes_from_scores(sc, cu, T, c, budget))
