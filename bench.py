@@ -73,6 +73,27 @@ def counts(wl) -> dict:
                 idx_flops=idx_flops, idx_bytes=idx_bytes, sparse_rows=int(sparse.sum()))
 
 
+def profile_traffic(name: str, source: str) -> int | None:
+    """DRAM bytes per launch recorded by the committed ncu summary, if it was taken on the
+    kernel source as it is now (else None)."""
+    import hashlib
+
+    prof = os.path.join(ROOT, "profiles", name)
+    src = os.path.join(ROOT, source)
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    rec = {}
+    with open(prof) as f:
+        for line in f:
+            if ":" in line and not line.startswith(("|", "#")):
+                k, _, v = line.partition(":")
+                rec[k.strip()] = v.strip()
+    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if rec.get("source_sha256_16") != cur or "dram_bytes_per_launch" not in rec:
+        return None
+    return int(rec["dram_bytes_per_launch"])
+
+
 def load_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -288,7 +309,8 @@ def run_gpu(args) -> dict | None:
                                "budget=2048 (route width 2051), scale 1/sqrt(128), seed 1",
                    "l2": "flushed (512 MiB write) before every timed step", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(attn_gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(attn_gbs / peaks["hbm_gbs"], 4),
+                     "traffic": profile_traffic("attn_fwd_mid.md", "indexer_routed_sparse_gb300/csrc/irs_attn.cu"),
                      "kernel": "attn_fwd_kernel", "peak_source": peaks["source"]},
         "attention": {"ms": round(att_avg_s * 1e3, 4), "tflops": round(attn_tflops, 3),
                       "routed_pairs_per_s": round(cnt["pairs"] * wl.Hq / att_avg_s, 1),
