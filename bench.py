@@ -32,7 +32,6 @@ import irs_synth  # noqa: E402
 
 METRIC = "routed sparse-attn fwd TFLOP/s & % roofline; indexer score+top-k queries/s"
 WORKLOAD = "mid"
-KERNELS_PER_STEP = 5          # layout, pool, score, top-k/expand, attention
 L2_FLUSH_BYTES = 512 << 20    # > 129 MB L2
 
 
@@ -50,9 +49,23 @@ def valid_per_row(wl) -> np.ndarray:
     return np.minimum(nvis, kb) * wl.c + (tau + 1) % wl.c
 
 
-def counts(wl) -> dict:
-    vr = valid_per_row(wl)
-    pairs = int(vr.sum())
+def counts(wl, pairs: int | None = None) -> dict:
+    """Algorithmic FLOPs and bytes of one step (closed forms from the definitions).
+
+    The number of valid (query, key) pairs is the closed form min(nvis, kb)*c + (tau+1) % c per
+    row, except where it depends on data: the latent workload's routes are an input (counted
+    from them) and the windowed workload's composed routes drop indexer IDs inside the window
+    (counted from the routes the step attends, passed in as `pairs`).
+    """
+    if wl.latent:
+        pairs = int(np.count_nonzero(np.asarray(wl.arrays["route"]) >= 0))
+        attn_flops = 2.0 * (wl.Dqk + wl.Dv) * wl.Hq * pairs
+        attn_bytes = (pairs * wl.Dqk * 2 + wl.T * wl.Hq * wl.Dqk * 2 + wl.T * wl.Hq * wl.Dv * 2 + wl.T * wl.Hq * 4
+                      + wl.T * wl.route_width * 4)
+        return dict(pairs=pairs, score_pairs=0, attn_flops=attn_flops, attn_bytes=attn_bytes, idx_flops=0.0,
+                    idx_bytes=0, sparse_rows=0)
+    if pairs is None:
+        pairs = int(valid_per_row(wl).sum())
     cu = np.asarray(wl.cu_seqlens, np.int64)
     t = np.arange(wl.T, dtype=np.int64)
     s = cu[np.searchsorted(cu, t, side="right") - 1]
@@ -68,9 +81,21 @@ def counts(wl) -> dict:
                   + wl.T * wl.Hq * 4                              # lse
                   + wl.T * W * 4)                                 # routes
     idx_flops = 2.0 * wl.Hi * wl.Di * score_pairs
-    idx_bytes = (wl.T * wl.Hi * wl.Di * 2 + wl.T * wl.Di * 2 + wl.T * wl.Hi * 4 + wl.T * W * 4)
+    W_idx = wl.budget + wl.c - 1
+    idx_bytes = (wl.T * wl.Hi * wl.Di * 2 + wl.T * wl.Di * 2 + wl.T * wl.Hi * 4 + wl.T * W_idx * 4)
     return dict(pairs=pairs, score_pairs=score_pairs, attn_flops=attn_flops, attn_bytes=attn_bytes,
                 idx_flops=idx_flops, idx_bytes=idx_bytes, sparse_rows=int(sparse.sum()))
+
+
+def describe(wl) -> str:
+    if wl.latent:
+        return (f"{wl.name}: {wl.T} queries x {wl.Hq} heads x {wl.Dqk}, latent {wl.Tk} x {wl.Dqk}, Dv {wl.Dv}, "
+                f"route width {wl.route_width}, seed {wl.seed}")
+    docs = f"{wl.ndocs} documents" if wl.ndocs > 1 else "single document"
+    win = f", window {wl.window}" if wl.window else ""
+    return (f"{wl.name} ({docs}): T={wl.T} Hq={wl.Hq} Hkv={wl.Hkv} Dqk={wl.Dqk} Dv={wl.Dv}, indexer Hi={wl.Hi} "
+            f"Di={wl.Di} c={wl.c} budget={wl.budget}{win} (route width {wl.route_width}), scale 1/sqrt({wl.Dqk}), "
+            f"seed {wl.seed}")
 
 
 def profile_traffic(name: str, source: str) -> int | None:
@@ -196,28 +221,39 @@ def run_gpu(args) -> dict | None:
 
         dist.init_process_group("nccl", device_id=dev)
     irs.lib()
-    wl = irs_synth.make(WORKLOAD)
-    cnt = counts(wl)
+    wl = irs_synth.make(args.workload)
     peaks = load_peaks()
 
     host = irs_synth.as_torch(wl, device="cpu", pin=True)
     d = {k: v.to(dev) for k, v in host.items()}
-    T, W = wl.T, wl.route_width
-    route = torch.empty((T, W), dtype=torch.int32, device=dev)
+    T = wl.T
     out = torch.empty((T, wl.Hq, wl.Dv), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((T, wl.Hq), dtype=torch.float32, device=dev)
-    ws = torch.empty(irs.index_workspace_bytes(T, wl.Hi, wl.Di, wl.c, wl.budget, wl.ndocs, wl.max_doc_len, True),
-                     dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     err = irs.device_error_flag(dev)
-    max_doc_len, ndocs = wl.max_doc_len, wl.ndocs
+    has_index = not wl.latent
+    if has_index:
+        W_idx = wl.budget + wl.c - 1
+        route_idx = torch.empty((T, W_idx), dtype=torch.int32, device=dev)
+        route = torch.empty((T, wl.route_width), dtype=torch.int32, device=dev) if wl.window else route_idx
+        ws = torch.empty(irs.index_workspace_bytes(T, wl.Hi, wl.Di, wl.c, wl.budget, wl.ndocs, wl.max_doc_len, True),
+                         dtype=torch.uint8, device=dev)
+        max_doc_len, ndocs = wl.max_doc_len, wl.ndocs
+    kv_v = d["kv"][:, :, :wl.Dv] if wl.latent else None
 
     def index(dd):
+        if not has_index:
+            return
         irs.sparse_index_score_topk(dd["qI"], dd["kI"], dd["w"], dd["cu_seqlens"], wl.c, wl.budget, ndocs=ndocs,
-                                    max_doc_len=max_doc_len, out=route, workspace=ws, err=err)
+                                    max_doc_len=max_doc_len, out=route_idx, workspace=ws, err=err)
+        if wl.window:
+            irs.compose_window_routes(route_idx, dd["cu_seqlens"], wl.window, out=route, err=err)
 
     def attend(dd):
-        irs.sparse_gqa_attn_fwd(dd["q"], dd["k"], dd["v"], route, wl.scale, out=out, lse=lse, err=err)
+        if wl.latent:
+            irs.sparse_gqa_attn_fwd(dd["q"], dd["kv"], kv_v, dd["route"], wl.scale, out=out, lse=lse, err=err)
+        else:
+            irs.sparse_gqa_attn_fwd(dd["q"], dd["k"], dd["v"], route, wl.scale, out=out, lse=lse, err=err)
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
@@ -225,6 +261,10 @@ def run_gpu(args) -> dict | None:
         attend(d)
     torch.cuda.synchronize(dev)
     irs.check_device_errors(dev)
+    # valid pairs: closed form, except for the window-composed routes (data dependent)
+    pairs = int((route >= 0).sum().item()) if (has_index and wl.window) else None
+    cnt = counts(wl, pairs)
+    kernels_per_step = (4 if has_index else 0) + (1 if wl.window else 0) + (wl.Hkv + 7) // 8
 
     uuid = None
     try:
@@ -290,8 +330,17 @@ def run_gpu(args) -> dict | None:
     attn_gbs = cnt["attn_bytes"] / att_avg_s / 1e9
     attn_tflops = cnt["attn_flops"] / att_avg_s / 1e12
     attn_roof_s = max(cnt["attn_bytes"] / (peaks["hbm_gbs"] * 1e9), cnt["attn_flops"] / (peaks["bf16_tflops"] * 1e12))
-    idx_roof_s = max(cnt["idx_bytes"] / (peaks["hbm_gbs"] * 1e9), cnt["idx_flops"] / (peaks["bf16_tflops"] * 1e12))
+    attn_bound = "hbm" if cnt["attn_bytes"] / peaks["hbm_gbs"] >= cnt["attn_flops"] / (peaks["bf16_tflops"] * 1e3) \
+        else "tensor"
     value = world * cnt["attn_flops"] / (step_ms * 1e-3) / 1e12
+    if attn_bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(attn_gbs / peaks["hbm_gbs"], 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(attn_tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(attn_tflops / peaks["bf16_tflops"], 4)}
+    roof.update({"traffic": profile_traffic(f"attn_fwd_{wl.name}.md", "indexer_routed_sparse_gb300/csrc/irs_attn.cu"),
+                 "kernel": "attn_fwd_kernel", "peak_source": peaks["source"]})
     res = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -304,29 +353,28 @@ def run_gpu(args) -> dict | None:
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 q/k/v/qI/kI, U(0,1) fp32 w)",
-        "config": {"workload": "mid single-document: B=1 S=8192 Hq=32 Hkv=8 D=128, indexer Hi=16 Di=128 c=4 "
-                               "budget=2048 (route width 2051), scale 1/sqrt(128), seed 1",
-                   "l2": "flushed (512 MiB write) before every timed step", "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(attn_gbs / peaks["hbm_gbs"], 4),
-                     "traffic": profile_traffic("attn_fwd_mid.md", "indexer_routed_sparse_gb300/csrc/irs_attn.cu"),
-                     "kernel": "attn_fwd_kernel", "peak_source": peaks["source"]},
+        "data": "synthetic (seeded N(0,1) bf16 inputs, U(0,1) fp32 head weights)",
+        "config": {"workload": describe(wl), "l2": "flushed (512 MiB write) before every timed step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
         "attention": {"ms": round(att_avg_s * 1e3, 4), "tflops": round(attn_tflops, 3),
                       "routed_pairs_per_s": round(cnt["pairs"] * wl.Hq / att_avg_s, 1),
-                      "roofline_frac": round(attn_roof_s / att_avg_s, 4),
-                      "algorithmic_bytes": cnt["attn_bytes"], "flops": cnt["attn_flops"]},
-        "indexer": {"ms": round(idx_avg_s * 1e3, 4), "queries_per_s": round(wl.T / idx_avg_s, 1),
-                    "tflops": round(cnt["idx_flops"] / idx_avg_s / 1e12, 3),
-                    "roofline_frac": round(idx_roof_s / idx_avg_s, 4), "roofline_s": idx_roof_s,
-                    "algorithmic_bytes": cnt["idx_bytes"], "flops": cnt["idx_flops"]},
+                      "roofline_frac": round(attn_roof_s / att_avg_s, 4), "roofline_ms": round(attn_roof_s * 1e3, 4),
+                      "algorithmic_bytes": cnt["attn_bytes"], "flops": cnt["attn_flops"], "valid_pairs": cnt["pairs"]},
         "e2e": {"value": round(world * cnt["attn_flops"] / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": kernels_per_step * args.steps,
         "clocks": clk,
         "wall_s_timed": round(wall, 3),
     }
-    if not args.no_cpu_baseline and world == 1:
+    if has_index:
+        idx_roof_s = max(cnt["idx_bytes"] / (peaks["hbm_gbs"] * 1e9), cnt["idx_flops"] / (peaks["bf16_tflops"] * 1e12))
+        res["indexer"] = {"ms": round(idx_avg_s * 1e3, 4), "queries_per_s": round(wl.T / idx_avg_s, 1),
+                          "tflops": round(cnt["idx_flops"] / idx_avg_s / 1e12, 3),
+                          "roofline_frac": round(idx_roof_s / idx_avg_s, 4), "roofline_us": round(idx_roof_s * 1e6, 2),
+                          "algorithmic_bytes": cnt["idx_bytes"], "flops": cnt["idx_flops"],
+                          "includes_window_composition": bool(wl.window)}
+    if not args.no_cpu_baseline and world == 1 and args.workload == WORKLOAD:
         res["cpu_baseline"] = cpu_baseline(wl, cnt, budget_s=args.cpu_seconds)
     if world > 1:
         import torch.distributed as dist
@@ -445,6 +493,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("irs", "reference"), default="irs")
+    ap.add_argument("--workload", choices=irs_synth.WORKLOADS, default=WORKLOAD,
+                    help="workload of the step (the headline line uses the mid workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=150.0)

@@ -28,8 +28,8 @@
 
 namespace irs {
 
-constexpr int kAttnThreads = 288;   // 4 producer warps, 1 MMA warp, 4 softmax warps
-constexpr int kProducerThreads = 128;
+// Warps: PW producer warps, then 1 MMA warp, then 4 softmax warps (32*(PW+5) threads).
+__host__ __device__ constexpr int attn_threads(int pw) { return 32 * (pw + 5); }
 constexpr int kChunk = 128;   // keys per chunk (UMMA M of the score product)
 constexpr int kNH = 16;       // head columns per sub-item (UMMA N)
 constexpr int kMaxDvBlocks = 4;
@@ -84,26 +84,42 @@ __device__ __forceinline__ void tmem_ld_nh(uint32_t taddr, float (&v)[NH]) {
 }
 
 // Gather `rows` routed rows of kc 16-byte pieces each into a SW128 operand tile with
-// 16-byte cp.async, spread over the 128 producer threads (piece i = r*kc + j goes to
-// thread i % 128). ids[r] are valid row indices.
+// 16-byte cp.async, spread over the PT producer threads (piece i = r*kc + j goes to
+// thread i % PT). ids[r] are valid row indices. When a second tile (V) has the same row
+// width, both are gathered in the same pass so each row index is read once.
+template <int PT>
 __device__ __forceinline__ void gather_rows(uint32_t dst, const __nv_bfloat16* src, int64_t row_stride,
+                                            uint32_t dst2, const __nv_bfloat16* src2, int64_t row_stride2,
                                             const int32_t* ids, int rows, int kc, int ptid) {
-  if (kProducerThreads % kc == 0 && ((kProducerThreads / kc) & 7) == 0) {
+  if (PT % kc == 0 && ((PT / kc) & 7) == 0) {
     // fixed 16-byte column per thread; rows step by a multiple of 8, so the swizzle is fixed
     const int j = ptid % kc;
-    const int dr = kProducerThreads / kc;
+    const int dr = PT / kc;
     int r = ptid / kc;
-    uint32_t d = dst + sw128_offset(r, j * 8, kChunk);
+    const uint32_t off = sw128_offset(r, j * 8, kChunk);
+    uint32_t d = dst + off, d2 = dst2 + off;
     const __nv_bfloat16* sj = src + j * 8;
+    const __nv_bfloat16* sj2 = src2 + j * 8;
+    if (src2 != nullptr) {
 #pragma unroll 4
-    for (; r < rows; r += dr, d += dr * 128) cp_async_16(d, sj + (int64_t)ids[r] * row_stride, 16u);
+      for (; r < rows; r += dr, d += dr * 128, d2 += dr * 128) {
+        const int64_t id = ids[r];
+        cp_async_16(d, sj + id * row_stride, 16u);
+        cp_async_16(d2, sj2 + id * row_stride2, 16u);
+      }
+    } else {
+#pragma unroll 4
+      for (; r < rows; r += dr, d += dr * 128) cp_async_16(d, sj + (int64_t)ids[r] * row_stride, 16u);
+    }
     return;
   }
   int r = ptid / kc, j = ptid - (ptid / kc) * kc;
-  const int dr = kProducerThreads / kc, dj = kProducerThreads - dr * kc;
+  const int dr = PT / kc, dj = PT - dr * kc;
   while (r < rows) {
-    const int id = ids[r];
-    cp_async_16(dst + sw128_offset(r, j * 8, kChunk), src + (int64_t)id * row_stride + j * 8, 16u);
+    const int64_t id = ids[r];
+    const uint32_t off = sw128_offset(r, j * 8, kChunk);
+    cp_async_16(dst + off, src + id * row_stride + j * 8, 16u);
+    if (src2 != nullptr) cp_async_16(dst2 + off, src2 + id * row_stride2 + j * 8, 16u);
     r += dr;
     j += dj;
     if (j >= kc) { j -= kc; ++r; }
@@ -127,8 +143,11 @@ struct AttnBars {
   uint64_t* fin;       // [2] row-sum exchange
 };
 
-template <int NH>
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnMaps maps, AttnArgs a) {
+template <int NH, int PW>
+__global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __grid_constant__ AttnMaps maps, AttnArgs a) {
+  constexpr int kThreads = attn_threads(PW);
+  constexpr int kProducerThreads = 32 * PW;
+  constexpr int kMmaWarp = PW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int ST = a.stages;
@@ -137,7 +156,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
   uint8_t* sP = smem + Ly.p_off;                                  // [2][16 rows x 128 keys]
   int32_t* sIdx = reinterpret_cast<int32_t*>(smem + Ly.idx_off);  // [idx_words] (producer only)
   int32_t* sNv = reinterpret_cast<int32_t*>(smem + Ly.nv_off);    // [2]
-  int32_t* sCnt = sNv + 4;                                        // [4] producer warp counts
+  int32_t* sCnt = sNv + 4;                                        // [PW] producer warp counts
   float* sRed = reinterpret_cast<float*>(smem + Ly.red_off);      // [2][4][16]
   float* sFin = reinterpret_cast<float*>(smem + Ly.fin_off);      // [2][4][16]
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Ly.bar_off);
@@ -172,7 +191,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
   {
     uint4* z = reinterpret_cast<uint4*>(smem);
     const uint32_t nz = Ly.idx_off / 16;
-    for (uint32_t i = tid; i < nz; i += kAttnThreads) z[i] = make_uint4(0, 0, 0, 0);
+    for (uint32_t i = tid; i < nz; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
     if (tid < 2) sNv[tid] = 0;
     fence_proxy_async_smem();
   }
@@ -195,7 +214,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tslot, 256);
     tmem_relinquish();
   }
@@ -204,8 +223,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  if (warp < 4) {
-    // =========================== producer (warps 0..3) ===========================
+  if (warp < PW) {
+    // =========================== producer (warps 0..PW-1) ===========================
     const int ptid = tid;
     uint32_t n = 0, u = 0, qi = 0;
     bool alive = true;
@@ -237,7 +256,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
           int before = run;
           for (int w2 = 0; w2 < warp; ++w2) before += sCnt[w2];
           if (okid) sIdx[before + __popc(bal & ((1u << lane) - 1u))] = id;
-          run += sCnt[0] + sCnt[1] + sCnt[2] + sCnt[3];
+          for (int w2 = 0; w2 < PW; ++w2) run += sCnt[w2];
           named_bar_sync(1, kProducerThreads);
         }
       }
@@ -274,14 +293,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
           const int rows = min(kChunk, nv - c * kChunk);
           const int32_t* ids = sIdx + c * kChunk;
           uint8_t* stage = smem + (uint32_t)st * Ly.stage_bytes;
-          gather_rows(smem_u32(stage), kbase, a.k_st, ids, rows, qc, ptid);
-          if (!a.v_alias) gather_rows(smem_u32(stage + Ly.k_bytes), vbase, a.v_st, ids, rows, a.Dv >> 3, ptid);
+          if (a.v_alias) {
+            gather_rows<kProducerThreads>(smem_u32(stage), kbase, a.k_st, 0, nullptr, 0, ids, rows, qc, ptid);
+          } else if (a.Dv == a.Dqk) {
+            gather_rows<kProducerThreads>(smem_u32(stage), kbase, a.k_st, smem_u32(stage + Ly.k_bytes), vbase, a.v_st,
+                                          ids, rows, qc, ptid);
+          } else {
+            gather_rows<kProducerThreads>(smem_u32(stage), kbase, a.k_st, 0, nullptr, 0, ids, rows, qc, ptid);
+            gather_rows<kProducerThreads>(smem_u32(stage + Ly.k_bytes), vbase, a.v_st, 0, nullptr, 0, ids, rows,
+                                          a.Dv >> 3, ptid);
+          }
           cp_async_mbar_arrive_noinc(&B.kv_full[st]);
         }
       }
     }
     cp_async_wait_pending(0);   // nothing of this CTA's gathers is in flight when it leaves
-  } else if (warp == 4) {
+  } else if (warp == kMmaWarp) {
     // =========================== UMMA issuer ===========================
     if (lane == 0) {
       uint32_t n = 0, u = 0, qi = 0;
@@ -340,8 +367,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
       }
     }
   } else {
-    // =========================== softmax + correction (warps 5..8) ===========================
-    const int sw = warp - 5;
+    // =========================== softmax + correction (warps PW+1 .. PW+4) ===========================
+    const int sw = warp - (PW + 1);
     const int lanerow = (warp & 3) * 32 + lane;      // TMEM lane: key of S, dv of O
     const uint32_t lane_addr = tmem_lane_base(warp);
     uint32_t n = 0, u = 0, qi = 0;
@@ -476,7 +503,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(const __grid_
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, 256);
   }
@@ -495,21 +522,35 @@ AttnPlan plan_attn(const AttnArgs& a, int num_sms) {
   return p;
 }
 
+// 8 producer warps where the softmax warps' registers leave room (heads <= 8), else 4
+template <int NH>
+constexpr int producer_warps() { return NH <= 8 ? 8 : 4; }
+
 cudaError_t configure_attn_kernel(size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<4, producer_warps<4>()>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_fwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(attn_fwd_kernel<8, producer_warps<8>()>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_fwd_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return cudaFuncSetAttribute(attn_fwd_kernel<16, producer_warps<16>()>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem);
 }
 
 cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, const AttnPlan& p, cudaStream_t stream) {
   AttnArgs b = a;
   b.stages = p.stages;
   switch (p.nh_class) {
-    case 4: attn_fwd_kernel<4><<<p.grid, kAttnThreads, p.smem, stream>>>(maps, b); break;
-    case 8: attn_fwd_kernel<8><<<p.grid, kAttnThreads, p.smem, stream>>>(maps, b); break;
-    default: attn_fwd_kernel<16><<<p.grid, kAttnThreads, p.smem, stream>>>(maps, b); break;
+    case 4:
+      attn_fwd_kernel<4, producer_warps<4>()><<<p.grid, attn_threads(producer_warps<4>()), p.smem, stream>>>(maps, b);
+      break;
+    case 8:
+      attn_fwd_kernel<8, producer_warps<8>()><<<p.grid, attn_threads(producer_warps<8>()), p.smem, stream>>>(maps, b);
+      break;
+    default:
+      attn_fwd_kernel<16, producer_warps<16>()><<<p.grid, attn_threads(producer_warps<16>()), p.smem, stream>>>(maps,
+                                                                                                                b);
+      break;
   }
   return cudaGetLastError();
 }
