@@ -143,7 +143,7 @@ struct AttnBars {
   uint64_t* fin;       // [2] row-sum exchange
 };
 
-template <int NH, int PW>
+template <int NH, int DVB, int PW>
 __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __grid_constant__ AttnMaps maps, AttnArgs a) {
   constexpr int kThreads = attn_threads(PW);
   constexpr int kProducerThreads = 32 * PW;
@@ -397,27 +397,28 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
         const int h0 = (a.g0 + g) * a.G + hb * a.HB;
         const int nh = min(a.HB, a.G - hb * a.HB);
         __nv_bfloat16* orow = a.out + (t * a.Hq + h0) * (long long)a.Dv;
-        float m[NH], l[NH], al_prev[NH], acc[kMaxDvBlocks][NH];
+        float m[NH], l[NH], al[NH], acc[DVB][NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
           m[h] = -INFINITY;
           l[h] = 0.f;
-          al_prev[h] = 1.f;
+          al[h] = 1.f;
 #pragma unroll
-          for (int blk = 0; blk < kMaxDvBlocks; ++blk) acc[blk][h] = 0.f;
+          for (int blk = 0; blk < DVB; ++blk) acc[blk][h] = 0.f;
         }
+        // acc <- acc * al + O of chunk mm (al: rescale factor of chunk mm)
         auto correct = [&](uint32_t mm) {
           const int ob = mm & 1;
           mbar_wait(&B.o_full[ob], (mm >> 1) & 1, abort_flag, a.err);
           tc_fence_after();
 #pragma unroll
-          for (int blk = 0; blk < kMaxDvBlocks; ++blk)
+          for (int blk = 0; blk < DVB; ++blk)
             if (blk < ndvb) {
               float o[NH];
               tmem_ld_nh<NH>(tbase + 32 + ob * (kNH * kMaxDvBlocks) + blk * kNH + lane_addr, o);
               tmem_ld_wait();
 #pragma unroll
-              for (int h = 0; h < NH; ++h) acc[blk][h] = fmaf(acc[blk][h], al_prev[h], o[h]);
+              for (int h = 0; h < NH; ++h) acc[blk][h] = fmaf(acc[blk][h], al[h], o[h]);
             }
           tc_fence_before();
           __syncwarp();
@@ -433,6 +434,9 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&B.s_empty[sb]);
+          // the previous chunk's output is issued right after this chunk's scores: fold it
+          // in now, with the rescale factor that belongs to it
+          if (c > 0) correct(n - 1);
           const bool kvalid = c * kChunk + lanerow < nv;
           float* red = sRed + sb * (4 * kNH);
 #pragma unroll
@@ -444,28 +448,24 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           __syncwarp();
           if (lane == 0) mbar_arrive(&B.red[sb]);
           mbar_wait(&B.red[sb], (n >> 1) & 1, abort_flag, a.err);
-          float al[NH], p[NH];
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
             const float cm = fmaxf(fmaxf(red[h], red[kNH + h]), fmaxf(red[2 * kNH + h], red[3 * kNH + h]));
             const float mn = fmaxf(m[h], cm);
             const float base = mn == -INFINITY ? 0.f : mn;
             al[h] = exp2f(m[h] - base);
-            p[h] = exp2f(s[h] - base);
-            l[h] = fmaf(l[h], al[h], p[h]);
+            s[h] = exp2f(s[h] - base);   // p
+            l[h] = fmaf(l[h], al[h], s[h]);
             m[h] = mn;
           }
           if (n >= 2) mbar_wait(&B.p_empty[sb], ((n >> 1) - 1) & 1, abort_flag, a.err);
           uint8_t* pdst = sP + sb * (kNH * kChunk * 2);
 #pragma unroll
           for (int h = 0; h < NH; ++h)
-            *reinterpret_cast<__nv_bfloat16*>(pdst + sw128_offset(h, lanerow, kNH)) = __float2bfloat16_rn(p[h]);
+            *reinterpret_cast<__nv_bfloat16*>(pdst + sw128_offset(h, lanerow, kNH)) = __float2bfloat16_rn(s[h]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&B.p_full[sb]);
-          if (c > 0) correct(n - 1);
-#pragma unroll
-          for (int h = 0; h < NH; ++h) al_prev[h] = al[h];
         }
         correct(n - 1);
         // ---- finalize: row sums over the 128 key lanes, normalise, store ----
@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           inv[h] = tot[h] > 0.f ? 1.f / tot[h] : 0.f;
         }
 #pragma unroll
-        for (int blk = 0; blk < kMaxDvBlocks; ++blk)
+        for (int blk = 0; blk < DVB; ++blk)
           if (blk < ndvb) {
 #pragma unroll
             for (int h = 0; h < NH; ++h)
@@ -522,35 +522,45 @@ AttnPlan plan_attn(const AttnArgs& a, int num_sms) {
   return p;
 }
 
-// 8 producer warps where the softmax warps' registers leave room (heads <= 8), else 4
-template <int NH>
-constexpr int producer_warps() { return NH <= 8 ? 8 : 4; }
+// 8 producer warps where the softmax warps' registers leave room, else 4
+template <int NH, int DVB>
+constexpr int producer_warps() { return NH * DVB <= 32 ? 8 : 4; }
+
+template <int NH, int DVB>
+static cudaError_t attn_attr(size_t smem) {
+  return cudaFuncSetAttribute(attn_fwd_kernel<NH, DVB, producer_warps<NH, DVB>()>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
 
 cudaError_t configure_attn_kernel(size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<4, producer_warps<4>()>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_fwd_kernel<8, producer_warps<8>()>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_fwd_kernel<16, producer_warps<16>()>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem);
+  cudaError_t e = cudaSuccess;
+  for (cudaError_t x : {attn_attr<4, 1>(smem), attn_attr<4, 2>(smem), attn_attr<4, 4>(smem), attn_attr<8, 1>(smem),
+                        attn_attr<8, 2>(smem), attn_attr<8, 4>(smem), attn_attr<16, 1>(smem), attn_attr<16, 2>(smem),
+                        attn_attr<16, 4>(smem)})
+    if (x != cudaSuccess) e = x;
+  return e;
+}
+
+template <int NH, int DVB>
+static void launch_variant(const AttnMaps& maps, const AttnArgs& b, const AttnPlan& p, cudaStream_t stream) {
+  constexpr int PW = producer_warps<NH, DVB>();
+  attn_fwd_kernel<NH, DVB, PW><<<p.grid, attn_threads(PW), p.smem, stream>>>(maps, b);
 }
 
 cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, const AttnPlan& p, cudaStream_t stream) {
   AttnArgs b = a;
   b.stages = p.stages;
-  switch (p.nh_class) {
-    case 4:
-      attn_fwd_kernel<4, producer_warps<4>()><<<p.grid, attn_threads(producer_warps<4>()), p.smem, stream>>>(maps, b);
-      break;
-    case 8:
-      attn_fwd_kernel<8, producer_warps<8>()><<<p.grid, attn_threads(producer_warps<8>()), p.smem, stream>>>(maps, b);
-      break;
-    default:
-      attn_fwd_kernel<16, producer_warps<16>()><<<p.grid, attn_threads(producer_warps<16>()), p.smem, stream>>>(maps,
-                                                                                                                b);
-      break;
+  const int dvb = (a.Dv + 127) / 128 <= 1 ? 1 : ((a.Dv + 127) / 128 <= 2 ? 2 : 4);
+  switch (p.nh_class * 10 + dvb) {
+    case 41: launch_variant<4, 1>(maps, b, p, stream); break;
+    case 42: launch_variant<4, 2>(maps, b, p, stream); break;
+    case 44: launch_variant<4, 4>(maps, b, p, stream); break;
+    case 81: launch_variant<8, 1>(maps, b, p, stream); break;
+    case 82: launch_variant<8, 2>(maps, b, p, stream); break;
+    case 84: launch_variant<8, 4>(maps, b, p, stream); break;
+    case 161: launch_variant<16, 1>(maps, b, p, stream); break;
+    case 162: launch_variant<16, 2>(maps, b, p, stream); break;
+    default: launch_variant<16, 4>(maps, b, p, stream); break;
   }
   return cudaGetLastError();
 }
