@@ -110,6 +110,30 @@ irs_status irs_sparse_index_score_topk(const void* qI, const void* kI, const flo
                                        size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream);
 
 /*
+ * irs_sparse_index_score_topk without a workspace: the same computation and arguments,
+ * minus `workspace` / `workspace_bytes`. The reference pages have no counterpart; this
+ * entry point exists for callers that cannot allocate device memory for the library,
+ * such as plugins of inference runtimes that are given no allocator, or loops that must
+ * not risk the device-wide synchronisation a cudaMalloc can cause. It allocates nothing:
+ * its scratch is one fixed 16 MiB device array inside libirs.so (every GPU that loads
+ * the library holds it until the process exits).
+ *
+ * - Sizes whose scratch (irs_index_workspace_bytes(..., with_score_buffer)) exceeds
+ *   16 MiB are rejected with IRS_ERR_VALUE. Passing a score buffer (scores_dbg) keeps
+ *   the FP32 score rows out of the scratch; the rest is small (the pooled keys
+ *   [floor(T/c), Di] bf16 plus per-document offsets).
+ * - The first call on a device looks up the array's device address for that device;
+ *   make that first call before any stream capture.
+ * - All calls share the one array, which keeps whatever the last call left there (the
+ *   kernels write every scratch word they read). Calls whose work overlaps on the GPU
+ *   (different streams, or different host threads) race on it: serialise them.
+ */
+irs_status irs_sparse_index_score_topk_noalloc(const void* qI, const void* kI, const float* w,
+                                               const int32_t* cu_seqlens, int ndocs, int max_doc_len, int T, int Hi,
+                                               int Di, int c, int budget, int32_t* route_ids, float* scores_dbg,
+                                               int64_t ld_scores, int32_t* err_flag, irs_stream_t stream);
+
+/*
  * Top-k, bitmap packing and expansion from given FP32 scores (the second half of
  * irs_sparse_index_score_topk), so that routes can be compared bit for bit with an
  * independent implementation that selects from the same scores.

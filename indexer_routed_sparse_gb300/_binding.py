@@ -35,6 +35,7 @@ _SIGNATURES = {
     "irs_last_error": (ctypes.c_char_p, []),
     "irs_index_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "irs_sparse_index_score_topk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I64, _P, _SZ, _P, _P]),
+    "irs_sparse_index_score_topk_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I64, _P, _P]),
     "irs_topk_from_scores": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "irs_compose_window_routes": (_I, [_P, _I, _P, _I, _I, _I, _P, _P, _P]),
     "irs_sparse_gqa_attn_fwd": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I, _I, _I, _I, _I, _I,

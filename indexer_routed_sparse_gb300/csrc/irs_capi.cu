@@ -292,3 +292,79 @@ irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_
 }
 
 }  // extern "C"
+
+// =====================================================================================
+// Indexer without allocation: the scratch lives in one fixed device array.
+//
+// For callers that cannot hand the library a workspace: code that runs where cudaMalloc
+// is not allowed or not wanted, e.g. plugin interfaces of inference runtimes that give a
+// plugin no allocator, or latency-critical loops that must not risk the device-wide
+// synchronisation an allocation can cause. The array is a file-scope __device__ object,
+// so every GPU that loads this library holds it until the process exits.
+// =====================================================================================
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+void* g_noalloc_addr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+}  // namespace
+
+extern "C" irs_status irs_sparse_index_score_topk_noalloc(const void* qI, const void* kI, const float* w,
+                                                          const int32_t* cu_seqlens, int ndocs, int max_doc_len, int T,
+                                                          int Hi, int Di, int c, int budget, int32_t* route_ids,
+                                                          float* scores_dbg, int64_t ld_scores, int32_t* err_flag,
+                                                          irs_stream_t stream) {
+  irs_status s = check_index_sizes(T, Hi, Di, c, budget, ndocs, max_doc_len);
+  if (s != IRS_OK) return s;
+  if (!qI || !kI || !w || !cu_seqlens || !route_ids) return fail(IRS_ERR_VALUE, "NULL tensor pointer");
+  if (!aligned16(qI) || !aligned16(kI)) return fail(IRS_ERR_VALUE, "qI and kI must be 16-byte aligned");
+  const irs::IndexPlan p = irs::plan_index(T, Hi, Di, c, budget, ndocs, max_doc_len, scores_dbg == nullptr);
+  if (scores_dbg != nullptr && ld_scores < p.ldS)
+    return fail(IRS_ERR_VALUE, "ld_scores must be >= max_doc_len / c (%lld)", (long long)p.ldS);
+  if (p.ws_bytes > kNoAllocScratchBytes)
+    return fail(IRS_ERR_VALUE,
+                "these sizes need %zu bytes of scratch but the fixed array holds %zu: pass a score buffer "
+                "(scores_dbg) to drop the score rows from the scratch, or use irs_sparse_index_score_topk",
+                p.ws_bytes, kNoAllocScratchBytes);
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != IRS_OK) return s;
+  int ordinal = 0;
+  if (cudaGetDevice(&ordinal) != cudaSuccess) return fail(IRS_ERR_RUNTIME, "cudaGetDevice failed");
+  uint8_t* ws = nullptr;
+  {
+    // once per device, with that device current: the array's device address
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_addr[ordinal] == nullptr) {
+      void* addr = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+      if (e != cudaSuccess)
+        return fail(IRS_ERR_RUNTIME, "cudaGetSymbolAddress of the fixed scratch failed: %s", cudaGetErrorString(e));
+      g_noalloc_addr[ordinal] = addr;
+    }
+    ws = static_cast<uint8_t*>(g_noalloc_addr[ordinal]);
+  }
+  if (p.score_smem > kMaxSmem) return fail(IRS_ERR_VALUE, "score tile does not fit in shared memory");
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (dev->score_smem < p.score_smem) {
+      if ((s = launch_status(irs::configure_score_kernels(p.score_smem), "configuring scoring")) != IRS_OK) return s;
+      dev->score_smem = p.score_smem;
+    }
+    if (dev->topk_smem < p.topk_smem) {
+      if ((s = launch_status(irs::configure_topk_kernel(p.topk_smem), "configuring top-k")) != IRS_OK) return s;
+      dev->topk_smem = p.topk_smem;
+    }
+  }
+  float* scores = scores_dbg != nullptr ? scores_dbg : reinterpret_cast<float*>(ws + p.off_scores);
+  const int64_t ldS = scores_dbg != nullptr ? ld_scores : p.ldS;
+  CUtensorMap tm_q, tm_k;
+  if ((s = make_tmap(&tm_q, qI, (uint64_t)Di, (uint64_t)T * Hi, 256)) != IRS_OK) return s;
+  if ((s = make_tmap(&tm_k, ws + p.off_kbar, (uint64_t)Di, (uint64_t)p.nblk_cap, 128)) != IRS_OK) return s;
+  return launch_status(irs::launch_index(p, static_cast<const __nv_bfloat16*>(qI),
+                                         static_cast<const __nv_bfloat16*>(kI), w, cu_seqlens, ndocs, max_doc_len, T,
+                                         Hi, Di, c, budget, route_ids, scores, ldS, ws, err_flag, tm_q, tm_k,
+                                         reinterpret_cast<cudaStream_t>(stream)),
+                       "launching the indexer (fixed scratch)");
+}
