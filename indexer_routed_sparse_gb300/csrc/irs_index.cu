@@ -174,6 +174,16 @@ struct ScoreArgs {
   int ndocs, T, Hi, c, kb, QT, tau_sparse, stages;
 };
 
+__device__ __forceinline__ int rot_tile(int j, int jrot, int nbt) {
+  const int r = j + jrot;
+  return r >= nbt ? r - nbt : r;
+}
+
+__device__ __forceinline__ float w4f(const float4* w4, int k) {
+  const float4 v = w4[k >> 2];
+  return (k & 3) == 0 ? v.x : ((k & 3) == 1 ? v.y : ((k & 3) == 2 ? v.z : v.w));
+}
+
 template <int DI, int HI>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, ScoreArgs a) {
@@ -212,6 +222,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int t0 = s_doc + tau0;
   const int nvis_last = (tau0 + nq) / a.c;
   const int nbt = (nvis_last + kScoreM - 1) / kScoreM;
+  // CTAs start at different key tiles so that concurrent CTAs do not all read the same
+  // 32 KB of pooled keys from L2 at the same moment
+  const int jrot = (int)(blockIdx.x % (unsigned)max(nbt, 1));
   const int blk0 = a.blk_off[d];
   constexpr int Hi = HI;
 
@@ -251,8 +264,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int s = j % ST;
         if (j >= ST && !mbar_wait(&empty[s], ((j / ST) - 1) & 1, abort_flag, a.err)) break;
         mbar_arrive_expect_tx(&full[s], A_STAGE);
+        const int bt = rot_tile(j, jrot, nbt);
         for (int ka = 0; ka < KATOMS; ++ka)
-          tma_load_2d(sA + (size_t)s * A_STAGE + ka * A_ATOM, &tm_k, ka * 64, blk0 + j * kScoreM, &full[s]);
+          tma_load_2d(sA + (size_t)s * A_STAGE + ka * A_ATOM, &tm_k, ka * 64, blk0 + bt * kScoreM, &full[s]);
         issued = j + 1;
       }
       if (*abort_flag) {
@@ -301,42 +315,51 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (!mbar_wait(&tfull[buf], (j >> 1) & 1, abort_flag, a.err)) break;
       tc_fence_after();
       if (active) {
-        const int blk = j * kScoreM + quarter * 32 + lane;
+        const int blk = rot_tile(j, jrot, nbt) * kScoreM + quarter * 32 + lane;
         float carry = 0.f;
 #pragma unroll 1
-        for (int cc = col0; cc < col0 + kHalfCols; cc += 32) {
-          float v[32];
-          tmem_ld32(tbase + lane_addr + buf * kScoreN + cc, v);
-          const float4* w4 = reinterpret_cast<const float4*>(sW + cc);
-          float prod[32];
+        for (int cc = col0; cc < col0 + kHalfCols; cc += 64) {
+          float v2[2][32];
+          tmem_ld32(tbase + lane_addr + buf * kScoreN + cc, v2[0]);
+          if (kHalfCols > 32) tmem_ld32(tbase + lane_addr + buf * kScoreN + cc + 32, v2[1]);
           tmem_ld_wait();
 #pragma unroll
-          for (int k4 = 0; k4 < 8; ++k4) {
-            const float4 ww = w4[k4];
-            prod[4 * k4 + 0] = ww.x * fmaxf(v[4 * k4 + 0], 0.f);
-            prod[4 * k4 + 1] = ww.y * fmaxf(v[4 * k4 + 1], 0.f);
-            prod[4 * k4 + 2] = ww.z * fmaxf(v[4 * k4 + 2], 0.f);
-            prod[4 * k4 + 3] = ww.w * fmaxf(v[4 * k4 + 3], 0.f);
-          }
-          // pairwise sums inside each query's group of Hi columns (log depth)
+          for (int half2 = 0; half2 < 2; ++half2) {
+          if (half2 == 1 && kHalfCols <= 32) break;
+          const int ccx = cc + 32 * half2;
+          const float* v = v2[half2];
+          const float4* w4 = reinterpret_cast<const float4*>(sW + ccx);
+          // per query: 4 interleaved FMA chains over its heads (h mod 4), then combined;
+          // prod[q0] holds the sum of the group of columns starting at q0
+          float prod[32];
+          constexpr int G = HI < 32 ? HI : 32;        // columns of one query inside this chunk
+          constexpr int CH = G < 4 ? G : 4;           // independent chains per query
 #pragma unroll
-          for (int stride = 1; stride < 32 && stride < HI; stride *= 2) {
+          for (int q0 = 0; q0 < 32; q0 += G) {
+            float acc4[CH];
 #pragma unroll
-            for (int k = 0; k < 32; k += 2 * stride) prod[k] += prod[k + stride];
+            for (int cidx = 0; cidx < CH; ++cidx) acc4[cidx] = 0.f;
+#pragma unroll
+            for (int k = 0; k < G; ++k) acc4[k % CH] = fmaf(w4f(w4, q0 + k), fmaxf(v[q0 + k], 0.f), acc4[k % CH]);
+            float sum = acc4[0];
+#pragma unroll
+            for (int cidx = 1; cidx < CH; ++cidx) sum += acc4[cidx];
+            prod[q0] = sum;
           }
           if constexpr (HI <= 32) {
 #pragma unroll
             for (int k = 0; k < 32; k += HI) {
-              const int qi = (cc + k) / HI;
+              const int qi = (ccx + k) / HI;
               if (blk < sNvis[qi]) a.scores[(long long)(t0 + qi) * a.ldS + blk] = prod[k];
             }
           } else {
             carry += prod[0];
-            if (((cc + 32) & (HI - 1)) == 0) {
-              const int qi = cc / HI;
+            if (((ccx + 32) & (HI - 1)) == 0) {
+              const int qi = ccx / HI;
               if (blk < sNvis[qi]) a.scores[(long long)(t0 + qi) * a.ldS + blk] = carry;
               carry = 0.f;
             }
+          }
           }
         }
       }
@@ -564,6 +587,191 @@ __global__ void __launch_bounds__(kTopkThreads) topk_expand_kernel(TopkArgs a) {
   }
 }
 
+// Register variant of the per-row CTA kernel for rows of at most 128*KPT visible blocks:
+// the row's keys stay in registers (element i = tid + 128k) and every scan is done by all
+// 128 threads (block scans), so no warp waits on a serial section. Same selection rule and
+// route layout as topk_expand_kernel.
+struct BlockScan2 {
+  int a, b;
+};
+
+// Exclusive block-wide scan of two ints over 128 threads (ascending thread order); also
+// returns the totals. `red` is 8 ints of shared scratch. Contains two __syncthreads.
+__device__ __forceinline__ BlockScan2 block_exscan2(int x, int y, int* red, int& tx, int& ty) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int ix = x, iy = y;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ux = __shfl_up_sync(0xffffffffu, ix, o), uy = __shfl_up_sync(0xffffffffu, iy, o);
+    if (lane >= o) { ix += ux; iy += uy; }
+  }
+  if (lane == 31) { red[warp] = ix; red[4 + warp] = iy; }
+  __syncthreads();
+  int bx = 0, by = 0;
+  tx = 0;
+  ty = 0;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int rx = red[w], ry = red[4 + w];
+    if (w < warp) { bx += rx; by += ry; }
+    tx += rx;
+    ty += ry;
+  }
+  __syncthreads();
+  return BlockScan2{bx + ix - x, by + iy - y};
+}
+
+template <int KPT>
+__global__ void __launch_bounds__(kTopkThreads) topk_reg_kernel(TopkArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const int kb = a.budget / a.c;
+  int32_t* sel = reinterpret_cast<int32_t*>(smem_raw);   // [kb]
+  __shared__ int hist[256];
+  __shared__ int red[8];
+  __shared__ int s_res[4];
+  __shared__ uint32_t s_diff[4];
+  __shared__ uint32_t s_bits[KPT * 4];
+  if (a.meta != nullptr && a.meta[0] != 1) return;
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int W = a.budget + a.c - 1;
+  int32_t* out = a.route + (long long)t * W;
+  const int d = find_doc(a.cu, a.ndocs, t);
+  const int s = a.cu[d], e = a.cu[d + 1];
+  if (!(s <= t && t < e && e <= a.T && e - s <= a.max_doc_len)) {
+    if (tid == 0) record_error(a.err, IRS_DEVERR_CU_SEQLENS);
+    return;
+  }
+  const int tau = t - s;
+  const int nvis = (tau + 1) / a.c;
+  const int ntail = (tau + 1) % a.c;
+  const bool sparse = nvis > kb;
+  const int nsel = sparse ? kb : nvis;
+  if (sparse) {
+    const float* row = a.scores + (long long)t * a.ldS;
+    const uint32_t key0 = order_key(__ldg(row));
+    uint32_t key[KPT];
+    uint32_t diff = 0;
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+      const int i = tid + kTopkThreads * k;
+      key[k] = i < nvis ? order_key(__ldg(row + i)) : 0u;
+      if (i < nvis) diff |= key[k] ^ key0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) diff |= __shfl_xor_sync(0xffffffffu, diff, o);
+    if (lane == 0) s_diff[warp] = diff;
+    hist[tid] = 0;
+    hist[tid + 128] = 0;
+    __syncthreads();
+    diff = s_diff[0] | s_diff[1] | s_diff[2] | s_diff[3];
+    const int hb = diff ? 31 - __clz(diff) : -1;
+    uint32_t mask = hb < 0 ? 0xFFFFFFFFu : (hb >= 31 ? 0u : ~((2u << hb) - 1u));
+    uint32_t prefix = key0 & mask;
+    int rem = kb;
+    for (int top = hb; top >= 0; top -= 8) {
+      const int shift = top - 7 > 0 ? top - 7 : 0;
+      const uint32_t dmask = (1u << (top - shift + 1)) - 1u;
+#pragma unroll
+      for (int k = 0; k < KPT; ++k) {
+        const int i = tid + kTopkThreads * k;
+        if (i < nvis && (key[k] & mask) == prefix) atomicAdd(&hist[(key[k] >> shift) & dmask], 1);
+      }
+      __syncthreads();
+      // thread i owns bins 255-2i and 254-2i (descending digit order)
+      const int h0 = hist[255 - 2 * tid], h1 = hist[254 - 2 * tid];
+      int tot_unused, tot2;
+      const BlockScan2 ex = block_exscan2(h0 + h1, 0, red, tot_unused, tot2);
+      // digits above this thread's pair hold ex.a keys
+      if (ex.a < rem && rem <= ex.a + h0 + h1) {
+        if (rem <= ex.a + h0) { s_res[0] = 255 - 2 * tid; s_res[1] = ex.a; s_res[2] = h0; }
+        else { s_res[0] = 254 - 2 * tid; s_res[1] = ex.a + h0; s_res[2] = h1; }
+      }
+      hist[tid] = 0;              // every read of hist is behind the scan's barriers
+      hist[tid + 128] = 0;
+      __syncthreads();
+      prefix |= (uint32_t)s_res[0] << shift;
+      mask |= dmask << shift;
+      rem -= s_res[1];
+      const int bin = s_res[2];
+      __syncthreads();            // s_res is rewritten by the next pass
+      if (bin == rem) break;      // the threshold bin is taken whole
+    }
+    const uint32_t thr = prefix;
+    // ---- bitmap words: word 4k + warp = blocks 128k + 32 warp .. +31 ----
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+      const int i = tid + kTopkThreads * k;
+      const uint32_t km = key[k] & mask;
+      const uint32_t g = __ballot_sync(0xffffffffu, i < nvis && km > thr);
+      const uint32_t q = __ballot_sync(0xffffffffu, i < nvis && km == thr);
+      if (lane == 0) { s_bits[4 * k + warp] = g; hist[4 * k + warp] = (int)q; }
+    }
+    __syncthreads();
+    // thread i owns word i (KPT*4 <= 128 words)
+    const int nw = (nvis + 31) / 32;
+    const uint32_t g = tid < nw ? s_bits[tid] : 0u;
+    const uint32_t q = tid < nw ? (uint32_t)hist[tid] : 0u;
+    int te, ts;
+    const BlockScan2 eqx = block_exscan2(__popc(q), 0, red, te, ts);
+    uint32_t take = 0;
+    if (eqx.a < rem) {
+      const int want = rem - eqx.a;
+      if (want >= __popc(q)) take = q;
+      else {
+        uint32_t x = q;
+        for (int r = 0; r < want; ++r) { take |= x & (~x + 1u); x &= x - 1u; }
+      }
+    }
+    const uint32_t bits = g | take;
+    const BlockScan2 selx = block_exscan2(__popc(bits), 0, red, te, ts);
+    uint32_t x = bits;
+    int r = selx.a;
+    while (x) {
+      const int b = __ffs(x) - 1;
+      if (r < kb) sel[r] = tid * 32 + b;
+      ++r;
+      x &= x - 1u;
+    }
+    __syncthreads();
+  }
+  const int c = a.c;
+  const int nblk_slots = nsel * c;
+  if ((c & (c - 1)) == 0) {
+    const int cs = __ffs(c) - 1;
+    for (int slot = tid; slot < nblk_slots; slot += kTopkThreads) {
+      const int rr = slot >> cs;
+      const int b = sparse ? sel[rr] : rr;
+      out[slot] = s + (b << cs) + (slot & (c - 1));
+    }
+  } else {
+    for (int rr = tid; rr < nsel; rr += kTopkThreads) {
+      const int b = sparse ? sel[rr] : rr;
+      for (int j = 0; j < c; ++j) out[rr * c + j] = s + b * c + j;
+    }
+  }
+  for (int slot = nblk_slots + tid; slot < W; slot += kTopkThreads) {
+    const int j = slot - a.budget;
+    out[slot] = (j >= 0 && j < ntail) ? s + nvis * c + j : -1;
+  }
+}
+
+// Launch the top-k + expansion for every row: the register variant when the longest row
+// has at most 2048 visible blocks, else the shared-memory variant.
+static cudaError_t launch_topk(const TopkArgs& ta, int kb, cudaStream_t stream, size_t cta_smem) {
+  const int nv = ta.nvis_cap;
+  const size_t smem = (size_t)kb * 4;
+  if (nv <= 2048 && smem <= 48 * 1024) {
+    if (nv <= 256) topk_reg_kernel<2><<<ta.T, kTopkThreads, smem, stream>>>(ta);
+    else if (nv <= 512) topk_reg_kernel<4><<<ta.T, kTopkThreads, smem, stream>>>(ta);
+    else if (nv <= 1024) topk_reg_kernel<8><<<ta.T, kTopkThreads, smem, stream>>>(ta);
+    else topk_reg_kernel<16><<<ta.T, kTopkThreads, smem, stream>>>(ta);
+    return cudaGetLastError();
+  }
+  topk_expand_kernel<<<ta.T, kTopkThreads, cta_smem, stream>>>(ta);
+  return cudaGetLastError();
+}
+
 // =====================================================================================
 // a5': sliding window composed in front of an indexer route.
 // =====================================================================================
@@ -675,17 +883,14 @@ cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv
   const cudaError_t le = launch_score(Di, Hi, p.score_tiles_cap, p.score_smem, stream, tm_q, tm_k, sa);
   if (le != cudaSuccess) return le;
   TopkArgs ta{scores, ldS, cu, meta, route, err, ndocs, T, c, budget, max_doc_len, (int)p.ldS};
-  topk_expand_kernel<<<T, kTopkThreads, p.topk_smem, stream>>>(ta);
-  return cudaGetLastError();
+  return launch_topk(ta, p.kb, stream, p.topk_smem);
 }
 
 cudaError_t launch_topk_from_scores(const float* scores, int64_t ldS, const int32_t* cu, int ndocs, int max_doc_len,
                                     int T, int c, int budget, int32_t* route, int32_t* err, cudaStream_t stream) {
   const int nvis_cap = max_doc_len / c > 0 ? max_doc_len / c : 1;
   TopkArgs ta{scores, ldS, cu, nullptr, route, err, ndocs, T, c, budget, max_doc_len, nvis_cap};
-  const size_t smem = topk_smem_bytes(nvis_cap, budget / c);
-  topk_expand_kernel<<<T, kTopkThreads, smem, stream>>>(ta);
-  return cudaGetLastError();
+  return launch_topk(ta, budget / c, stream, topk_smem_bytes(nvis_cap, budget / c));
 }
 
 cudaError_t launch_compose_window(const int32_t* route, int W, const int32_t* cu, int ndocs, int T, int window,
