@@ -8,19 +8,24 @@
 //
 // Design. A persistent CTA walks query rows t (grid-stride); for each row it walks its
 // KV heads and head blocks (<= 16 query heads of one KV head, a "sub-item"). Warp roles:
-//   warps 0..3  producer: compact the valid route IDs of the row into shared memory, load
-//               the sub-item's query tile, and gather routed K/V rows with 16-byte
-//               cp.async into a ring of 128-key stages (SW128 layout); completion is
-//               signalled per stage by cp.async-arrive on an mbarrier. (Random 256-byte
-//               rows reach about 3x the L2 bandwidth this way than with TMA gather4.)
-//   warp 4      TMEM owner and UMMA issuer: S^T = K.Q^T (M=128 keys, N=16 heads, K=Dqk)
+//   producer warps (8, or 4 for the widest head/dv tiles): compact the valid route IDs of
+//               the row into shared memory, then per sub-item copy the query tile and
+//               gather the routed K/V rows with 16-byte cp.async into a ring of 128-key
+//               stages (SW128 layout); completion reaches the stage's mbarrier by
+//               cp.async-arrive. (Random 256-byte rows reach about 3x the L2 bandwidth
+//               this way than with TMA gather4.)
+//   1 MMA warp  TMEM owner and UMMA issuer: S^T = K.Q^T (M=128 keys, N=16 heads, K=Dqk)
 //               and O^T = V^T.P^T (M=128 dv per block, N=16, K=128 keys; V read MN-major
-//               from the gathered [key][dv] tile);
-//   warps 5..8  softmax and correction, one key (for S) / one dv (for O) per thread: an
-//               online softmax in base 2 with head maxima exchanged through shared memory,
-//               P written as the bf16 B operand, the chunk output rescaled and accumulated
-//               in registers, then normalised and stored.
-// S, P and O are double-buffered, so S of chunk n+1 and O of chunk n-1 run on the tensor
+//               from the gathered [key][dv] tile). S goes out as each stage lands; the O
+//               product of a chunk goes out as soon as its P is written (also while the
+//               issuer waits for a stage), and its completion releases the stage. Each
+//               product is issued as a fully unrolled run of tcgen05.mma (an issue loop
+//               with a run-time trip count costs about twice as much per instruction).
+//   4 softmax warps, one key (for S) / one dv (for O) per thread: an online softmax in
+//               base 2 with head maxima exchanged through shared memory, P written as the
+//               bf16 B operand, then the previous chunk's output rescaled and accumulated
+//               in registers; at the end normalised and stored.
+// S, P and O are double-buffered, so S of chunk n+1 and O of chunk n run on the tensor
 // cores while the softmax warps work on chunk n, and the producer runs ahead across
 // sub-items and rows. All cross-warp waits are bounded mbarrier waits.
 #include "irs_internal.h"
@@ -126,6 +131,52 @@ __device__ __forceinline__ void gather_rows(uint32_t dst, const __nv_bfloat16* s
   }
 }
 
+// S^T (+)= K.Q^T over KA SW128 atoms of Dqk (4 k-steps of 16 per atom).
+template <int KA>
+__device__ __forceinline__ void issue_scores(uint32_t d, uint32_t kb, uint32_t qb, uint32_t idesc) {
+#pragma unroll
+  for (int ks = 0; ks < 4 * KA; ++ks) {
+    const uint64_t ad = sdesc_sw128(kb + (ks >> 2) * (kChunk * 128) + (ks & 3) * 32, 16, 1024);
+    const uint64_t bd = sdesc_sw128(qb + (ks >> 2) * (kNH * 128) + (ks & 3) * 32, 16, 1024);
+    umma_bf16(d, ad, bd, idesc, ks > 0);
+  }
+}
+__device__ __forceinline__ void issue_scores_any(int katoms, uint32_t d, uint32_t kb, uint32_t qb, uint32_t idesc) {
+  switch (katoms) {
+    case 1: issue_scores<1>(d, kb, qb, idesc); break;
+    case 2: issue_scores<2>(d, kb, qb, idesc); break;
+    case 3: issue_scores<3>(d, kb, qb, idesc); break;
+    case 4: issue_scores<4>(d, kb, qb, idesc); break;
+    case 5: issue_scores<5>(d, kb, qb, idesc); break;
+    case 6: issue_scores<6>(d, kb, qb, idesc); break;
+    case 7: issue_scores<7>(d, kb, qb, idesc); break;
+    case 8: issue_scores<8>(d, kb, qb, idesc); break;
+    default: issue_scores<9>(d, kb, qb, idesc); break;
+  }
+}
+// O^T = V^T.P^T for NB blocks of 128 dv (V MN-major: two 64-dv atoms of 128 key rows
+// per block; P K-major: 16 head rows of 128 keys).
+template <int NB>
+__device__ __forceinline__ void issue_output(uint32_t d, uint32_t vb, uint32_t pb, uint32_t idesc) {
+#pragma unroll
+  for (int blk = 0; blk < NB; ++blk) {
+#pragma unroll
+    for (int ks = 0; ks < kChunk / 16; ++ks) {
+      const uint64_t ad = sdesc_sw128(vb + (2 * blk) * (kChunk * 128) + ks * 2048, kChunk * 128, 1024);
+      const uint64_t bd = sdesc_sw128(pb + (ks >> 2) * (kNH * 128) + (ks & 3) * 32, 16, 1024);
+      umma_bf16(d + blk * kNH, ad, bd, idesc, ks > 0);
+    }
+  }
+}
+__device__ __forceinline__ void issue_output_any(int ndvb, uint32_t d, uint32_t vb, uint32_t pb, uint32_t idesc) {
+  switch (ndvb) {
+    case 1: issue_output<1>(d, vb, pb, idesc); break;
+    case 2: issue_output<2>(d, vb, pb, idesc); break;
+    case 3: issue_output<3>(d, vb, pb, idesc); break;
+    default: issue_output<4>(d, vb, pb, idesc); break;
+  }
+}
+
 struct AttnBars {
   uint64_t* kv_full;
   uint64_t* kv_empty;
@@ -180,7 +231,6 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int katoms = a.Dqk >> 6;
-  const int vatoms = a.Dv >> 6;
   const int ndvb = a.Dv >> 7;
   const int qc = a.Dqk >> 3;
   const int n_sub = a.ng * a.nhb;   // sub-items per row
@@ -198,7 +248,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) { mbar_init(&B.kv_full[s], kProducerThreads); mbar_init(&B.kv_empty[s], 1); }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&B.q_full[i], 1);
+      mbar_init(&B.q_full[i], kProducerThreads);
       mbar_init(&B.q_empty[i], 1);
       mbar_init(&B.idx_full[i], 1);
       mbar_init(&B.idx_empty[i], 5);
@@ -274,15 +324,12 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
         ok = u < 2 || mbar_wait(&B.q_empty[qb], ((u >> 1) - 1) & 1, abort_flag, a.err);
         alive = named_bar_and(1, kProducerThreads, ok);
         if (!alive) break;
-        uint8_t* q_dst = sQ + qb * (kNH * a.Dqk * 2);
+        const uint32_t q_dst = smem_u32(sQ + qb * (kNH * a.Dqk * 2));
         for (int i = ptid; i < nh * qc; i += kProducerThreads) {
           const int r = i / qc, j = i - r * qc;
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.q + t * a.q_st + (long long)(h0 + r) * a.q_sh + j * 8));
-          *reinterpret_cast<uint4*>(q_dst + sw128_offset(r, j * 8, kNH)) = v;
+          cp_async_16(q_dst + sw128_offset(r, j * 8, kNH), a.q + t * a.q_st + (long long)(h0 + r) * a.q_sh + j * 8, 16u);
         }
-        fence_proxy_async_smem();
-        named_bar_sync(1, kProducerThreads);
-        if (ptid == 0) mbar_arrive(&B.q_full[qb]);
+        cp_async_mbar_arrive_noinc(&B.q_full[qb]);
         const __nv_bfloat16* kbase = a.k + (long long)(a.g0 + g) * a.k_sh;
         const __nv_bfloat16* vbase = a.v + (long long)(a.g0 + g) * a.v_sh;
         for (int c = 0; c < nchunks; ++c, ++n) {
@@ -311,59 +358,73 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
   } else if (warp == kMmaWarp) {
     // =========================== UMMA issuer ===========================
     if (lane == 0) {
-      uint32_t n = 0, u = 0, qi = 0;
+      uint32_t n = 0, u = 0, qi = 0, o_next = 0;   // o_next: oldest chunk whose O is not issued
       bool alive = true;
-      auto issue_o = [&](uint32_t m) -> bool {
+      auto issue_o = [&](uint32_t m) {
         const int pb = m & 1;
-        if (!mbar_wait(&B.p_full[pb], (m >> 1) & 1, abort_flag, a.err)) return false;
-        if (m >= 2 && !mbar_wait(&B.o_empty[pb], ((m >> 1) - 1) & 1, abort_flag, a.err)) return false;
         tc_fence_after();
         const uint8_t* stage = smem + (uint32_t)(m % ST) * Ly.stage_bytes;
         const uint32_t vb = smem_u32(a.v_alias ? stage : stage + Ly.k_bytes);
-        const uint32_t pbase = smem_u32(sP + pb * (kNH * kChunk * 2));
-        for (int blk = 0; blk < ndvb; ++blk) {
-          for (int ks = 0; ks < kChunk / 16; ++ks) {
-            const uint64_t ad = sdesc_sw128(vb + (2 * blk) * (kChunk * 128) + ks * 2048, kChunk * 128, 1024);
-            const uint64_t bd = sdesc_sw128(pbase + (ks >> 2) * (kNH * 128) + (ks & 3) * 32, 16, 1024);
-            umma_bf16(tbase + 32 + pb * (kNH * kMaxDvBlocks) + blk * kNH, ad, bd, IDESC_O, ks > 0);
-          }
-        }
+        issue_output_any(ndvb, tbase + 32 + pb * (kNH * kMaxDvBlocks), vb, smem_u32(sP + pb * (kNH * kChunk * 2)),
+                         IDESC_O);
         umma_commit(&B.o_full[pb]);
         umma_commit(&B.p_empty[pb]);
         umma_commit(&B.kv_empty[m % ST]);
-        return true;
+      };
+      // O of chunk m may go once its P is written and the O buffer it reuses is drained
+      auto o_ready = [&](uint32_t m) -> bool {
+        const int pb = m & 1;
+        return mbar_test(&B.p_full[pb], (m >> 1) & 1) && (m < 2 || mbar_test(&B.o_empty[pb], ((m >> 1) - 1) & 1));
+      };
+      // bounded wait that issues ready O products meanwhile (only of chunks whose S is out)
+      auto wait_issuing_o = [&](uint64_t* bar, uint32_t parity) -> bool {
+        unsigned long long t0 = 0;
+        while (true) {
+          if (mbar_test(bar, parity)) return true;
+          if (o_next < n && o_ready(o_next)) {
+            issue_o(o_next++);
+            continue;
+          }
+          if (*abort_flag) return false;
+          const unsigned long long now = globaltimer_ns();
+          if (t0 == 0) t0 = now;
+          else if (now - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            record_error(a.err, IRS_DEVERR_TIMEOUT);
+            return false;
+          }
+        }
       };
       for (long long t = blockIdx.x; t < a.T && alive; t += gridDim.x, ++qi) {
         const int b = qi & 1;
-        if (!mbar_wait(&B.idx_full[b], (qi >> 1) & 1, abort_flag, a.err)) { alive = false; break; }
+        if (!wait_issuing_o(&B.idx_full[b], (qi >> 1) & 1)) { alive = false; break; }
         const int nv = sNv[b];
         mbar_arrive(&B.idx_empty[b]);
         if (nv == 0) continue;
         const int nchunks = (nv + kChunk - 1) / kChunk;
         for (int sub = 0; sub < n_sub && alive; ++sub, ++u) {
           const int qb = u & 1;
-          if (!mbar_wait(&B.q_full[qb], (u >> 1) & 1, abort_flag, a.err)) { alive = false; break; }
+          if (!wait_issuing_o(&B.q_full[qb], (u >> 1) & 1)) { alive = false; break; }
           const uint32_t qbase = smem_u32(sQ + qb * (kNH * a.Dqk * 2));
           for (int c = 0; c < nchunks; ++c, ++n) {
             const int st = n % ST, sb = n & 1;
-            // with a single stage, chunk n can only be gathered once O of chunk n-1 is done
-            if (ST == 1 && c > 0 && !issue_o(n - 1)) { alive = false; break; }
-            if (!mbar_wait(&B.kv_full[st], (n / ST) & 1, abort_flag, a.err)) { alive = false; break; }
-            if (n >= 2 && !mbar_wait(&B.s_empty[sb], ((n >> 1) - 1) & 1, abort_flag, a.err)) { alive = false; break; }
+            if (!wait_issuing_o(&B.kv_full[st], (n / ST) & 1)) { alive = false; break; }
+            if (n >= 2 && !wait_issuing_o(&B.s_empty[sb], ((n >> 1) - 1) & 1)) { alive = false; break; }
             fence_proxy_async_smem();   // gathered rows (generic-proxy writes) -> UMMA reads
             tc_fence_after();
-            const uint32_t kb = smem_u32(smem + (uint32_t)st * Ly.stage_bytes);
-            for (int ks = 0; ks < a.Dqk / 16; ++ks) {
-              const uint64_t ad = sdesc_sw128(kb + (ks >> 2) * (kChunk * 128) + (ks & 3) * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(qbase + (ks >> 2) * (kNH * 128) + (ks & 3) * 32, 16, 1024);
-              umma_bf16(tbase + sb * kNH, ad, bd, IDESC_S, ks > 0);
-            }
+            issue_scores_any(katoms, tbase + sb * kNH, smem_u32(smem + (uint32_t)st * Ly.stage_bytes), qbase, IDESC_S);
             umma_commit(&B.s_full[sb]);
             if (c == nchunks - 1) umma_commit(&B.q_empty[qb]);
-            if (ST > 1 && c > 0 && !issue_o(n - 1)) { alive = false; break; }
+            if (o_next < n && o_ready(o_next)) issue_o(o_next++);
           }
-          if (alive && !issue_o(n - 1)) alive = false;
         }
+      }
+      // drain: the O products of the last chunks
+      while (alive && o_next < n) {
+        const int pb = o_next & 1;
+        if (!mbar_wait(&B.p_full[pb], (o_next >> 1) & 1, abort_flag, a.err)) break;
+        if (o_next >= 2 && !mbar_wait(&B.o_empty[pb], ((o_next >> 1) - 1) & 1, abort_flag, a.err)) break;
+        issue_o(o_next++);
       }
     }
   } else {
@@ -397,16 +458,17 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
         const int h0 = (a.g0 + g) * a.G + hb * a.HB;
         const int nh = min(a.HB, a.G - hb * a.HB);
         __nv_bfloat16* orow = a.out + (t * a.Hq + h0) * (long long)a.Dv;
-        float m[NH], l[NH], al[NH], acc[DVB][NH];
+        float m[NH], l[NH], al[NH], alp[NH], acc[DVB][NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
           m[h] = -INFINITY;
           l[h] = 0.f;
           al[h] = 1.f;
+          alp[h] = 1.f;
 #pragma unroll
           for (int blk = 0; blk < DVB; ++blk) acc[blk][h] = 0.f;
         }
-        // acc <- acc * al + O of chunk mm (al: rescale factor of chunk mm)
+        // acc <- acc * alp + O of chunk mm (alp: rescale factor of chunk mm)
         auto correct = [&](uint32_t mm) {
           const int ob = mm & 1;
           mbar_wait(&B.o_full[ob], (mm >> 1) & 1, abort_flag, a.err);
@@ -418,7 +480,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
               tmem_ld_nh<NH>(tbase + 32 + ob * (kNH * kMaxDvBlocks) + blk * kNH + lane_addr, o);
               tmem_ld_wait();
 #pragma unroll
-              for (int h = 0; h < NH; ++h) acc[blk][h] = fmaf(acc[blk][h], al[h], o[h]);
+              for (int h = 0; h < NH; ++h) acc[blk][h] = fmaf(acc[blk][h], alp[h], o[h]);
             }
           tc_fence_before();
           __syncwarp();
@@ -434,9 +496,6 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&B.s_empty[sb]);
-          // the previous chunk's output is issued right after this chunk's scores: fold it
-          // in now, with the rescale factor that belongs to it
-          if (c > 0) correct(n - 1);
           const bool kvalid = c * kChunk + lanerow < nv;
           float* red = sRed + sb * (4 * kNH);
 #pragma unroll
@@ -466,6 +525,11 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&B.p_full[sb]);
+          // P of this chunk is out; now fold in the previous chunk's output, which ran on
+          // the tensor cores meanwhile, with the rescale factor that belongs to it
+          if (c > 0) correct(n - 1);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) alp[h] = al[h];
         }
         correct(n - 1);
         // ---- finalize: row sums over the 128 key lanes, normalise, store ----
