@@ -14,13 +14,15 @@
 //               stages (SW128 layout); completion reaches the stage's mbarrier by
 //               cp.async-arrive. (Random 256-byte rows reach about 3x the L2 bandwidth
 //               this way than with TMA gather4.)
-//   1 MMA warp  TMEM owner and UMMA issuer: S^T = K.Q^T (M=128 keys, N=16 heads, K=Dqk)
-//               and O^T = V^T.P^T (M=128 dv per block, N=16, K=128 keys; V read MN-major
-//               from the gathered [key][dv] tile). S goes out as each stage lands; the O
-//               product of a chunk goes out as soon as its P is written (also while the
-//               issuer waits for a stage), and its completion releases the stage. Each
-//               product is issued as a fully unrolled run of tcgen05.mma (an issue loop
-//               with a run-time trip count costs about twice as much per instruction).
+//   S warp      TMEM owner; issues S^T = K.Q^T (M=128 keys, N=16 heads, K=Dqk) as each
+//               stage lands.
+//   O warp      issues O^T = V^T.P^T (M=128 dv per block, N=16, K=128 keys; V read
+//               MN-major from the gathered [key][dv] tile) as soon as a chunk's P is
+//               written; its completion releases the stage. The thread that issues
+//               tcgen05.mma runs in step with the tensor pipe (its waits, fences and
+//               commits leave the pipe idle), so two issuers keep it fed. Each product is
+//               a fully unrolled run of tcgen05.mma with descriptors formed as base plus a
+//               constant (a run-time trip count doubles the cost per instruction).
 //   4 softmax warps, one key (for S) / one dv (for O) per thread: an online softmax in
 //               base 2 with head maxima exchanged through shared memory, P written as the
 //               bf16 B operand, then the previous chunk's output rescaled and accumulated
@@ -33,8 +35,8 @@
 
 namespace irs {
 
-// Warps: PW producer warps, then 1 MMA warp, then 4 softmax warps (32*(PW+5) threads).
-__host__ __device__ constexpr int attn_threads(int pw) { return 32 * (pw + 5); }
+// Warps: PW producer warps, the S issuer, the O issuer, then 4 softmax warps (32*(PW+6) threads).
+__host__ __device__ constexpr int attn_threads(int pw) { return 32 * (pw + 6); }
 constexpr int kChunk = 128;   // keys per chunk (UMMA M of the score product)
 constexpr int kNH = 16;       // head columns per sub-item (UMMA N)
 constexpr int kMaxDvBlocks = 4;
@@ -131,15 +133,16 @@ __device__ __forceinline__ void gather_rows(uint32_t dst, const __nv_bfloat16* s
   }
 }
 
-// S^T (+)= K.Q^T over KA SW128 atoms of Dqk (4 k-steps of 16 per atom).
+// S^T (+)= K.Q^T over KA SW128 atoms of Dqk (4 k-steps of 16 per atom). Descriptors are
+// one base descriptor plus a compile-time start-address step (the 14-bit start field cannot
+// carry: shared addresses stay below 256 KB).
 template <int KA>
 __device__ __forceinline__ void issue_scores(uint32_t d, uint32_t kb, uint32_t qb, uint32_t idesc) {
+  const uint64_t a0 = sdesc_sw128(kb, 16, 1024), b0 = sdesc_sw128(qb, 16, 1024);
 #pragma unroll
-  for (int ks = 0; ks < 4 * KA; ++ks) {
-    const uint64_t ad = sdesc_sw128(kb + (ks >> 2) * (kChunk * 128) + (ks & 3) * 32, 16, 1024);
-    const uint64_t bd = sdesc_sw128(qb + (ks >> 2) * (kNH * 128) + (ks & 3) * 32, 16, 1024);
-    umma_bf16(d, ad, bd, idesc, ks > 0);
-  }
+  for (int ks = 0; ks < 4 * KA; ++ks)
+    umma_bf16(d, a0 + (uint64_t)(((ks >> 2) * (kChunk * 128) + (ks & 3) * 32) >> 4),
+              b0 + (uint64_t)(((ks >> 2) * (kNH * 128) + (ks & 3) * 32) >> 4), idesc, ks > 0);
 }
 __device__ __forceinline__ void issue_scores_any(int katoms, uint32_t d, uint32_t kb, uint32_t qb, uint32_t idesc) {
   switch (katoms) {
@@ -158,14 +161,13 @@ __device__ __forceinline__ void issue_scores_any(int katoms, uint32_t d, uint32_
 // per block; P K-major: 16 head rows of 128 keys).
 template <int NB>
 __device__ __forceinline__ void issue_output(uint32_t d, uint32_t vb, uint32_t pb, uint32_t idesc) {
+  const uint64_t a0 = sdesc_sw128(vb, kChunk * 128, 1024), b0 = sdesc_sw128(pb, 16, 1024);
 #pragma unroll
   for (int blk = 0; blk < NB; ++blk) {
 #pragma unroll
-    for (int ks = 0; ks < kChunk / 16; ++ks) {
-      const uint64_t ad = sdesc_sw128(vb + (2 * blk) * (kChunk * 128) + ks * 2048, kChunk * 128, 1024);
-      const uint64_t bd = sdesc_sw128(pb + (ks >> 2) * (kNH * 128) + (ks & 3) * 32, 16, 1024);
-      umma_bf16(d + blk * kNH, ad, bd, idesc, ks > 0);
-    }
+    for (int ks = 0; ks < kChunk / 16; ++ks)
+      umma_bf16(d + blk * kNH, a0 + (uint64_t)(((2 * blk) * (kChunk * 128) + ks * 2048) >> 4),
+                b0 + (uint64_t)(((ks >> 2) * (kNH * 128) + (ks & 3) * 32) >> 4), idesc, ks > 0);
   }
 }
 __device__ __forceinline__ void issue_output_any(int ndvb, uint32_t d, uint32_t vb, uint32_t pb, uint32_t idesc) {
@@ -186,8 +188,7 @@ struct AttnBars {
   uint64_t* idx_empty; // [2]
   uint64_t* s_full;    // [2]
   uint64_t* s_empty;   // [2]
-  uint64_t* p_full;    // [2]
-  uint64_t* p_empty;   // [2]
+  uint64_t* p_full;    // [2] (a P buffer is free again once O of its chunk is done: o_full)
   uint64_t* o_full;    // [2]
   uint64_t* o_empty;   // [2]
   uint64_t* red;       // [2] chunk-max exchange among the softmax warps
@@ -198,7 +199,8 @@ template <int NH, int DVB, int PW>
 __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __grid_constant__ AttnMaps maps, AttnArgs a) {
   constexpr int kThreads = attn_threads(PW);
   constexpr int kProducerThreads = 32 * PW;
-  constexpr int kMmaWarp = PW;
+  constexpr int kSWarp = PW;       // TMEM owner, issues the S products
+  constexpr int kOWarp = PW + 1;   // issues the O products
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int ST = a.stages;
@@ -221,8 +223,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
   B.s_full = B.idx_empty + 2;
   B.s_empty = B.s_full + 2;
   B.p_full = B.s_empty + 2;
-  B.p_empty = B.p_full + 2;
-  B.o_full = B.p_empty + 2;
+  B.o_full = B.p_full + 2;
   B.o_empty = B.o_full + 2;
   B.red = B.o_empty + 2;
   B.fin = B.red + 2;
@@ -251,11 +252,10 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
       mbar_init(&B.q_full[i], kProducerThreads);
       mbar_init(&B.q_empty[i], 1);
       mbar_init(&B.idx_full[i], 1);
-      mbar_init(&B.idx_empty[i], 5);
+      mbar_init(&B.idx_empty[i], 6);
       mbar_init(&B.s_full[i], 1);
       mbar_init(&B.s_empty[i], 4);
       mbar_init(&B.p_full[i], 4);
-      mbar_init(&B.p_empty[i], 1);
       mbar_init(&B.o_full[i], 1);
       mbar_init(&B.o_empty[i], 4);
       mbar_init(&B.red[i], 4);
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kSWarp) {
     tmem_alloc(tslot, 256);
     tmem_relinquish();
   }
@@ -355,81 +355,69 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
       }
     }
     cp_async_wait_pending(0);   // nothing of this CTA's gathers is in flight when it leaves
-  } else if (warp == kMmaWarp) {
-    // =========================== UMMA issuer ===========================
+  } else if (warp == kSWarp) {
+    // =========================== S issuer ===========================
+    // The issuing thread runs in step with the tensor pipe, so S and O products come from
+    // two warps: each one's waits, fences and commits overlap the other's MMAs, and O of a
+    // chunk never queues behind S of a chunk whose stage has not landed.
     if (lane == 0) {
-      uint32_t n = 0, u = 0, qi = 0, o_next = 0;   // o_next: oldest chunk whose O is not issued
+      uint32_t n = 0, u = 0, qi = 0;
       bool alive = true;
-      auto issue_o = [&](uint32_t m) {
-        const int pb = m & 1;
-        tc_fence_after();
-        const uint8_t* stage = smem + (uint32_t)(m % ST) * Ly.stage_bytes;
-        const uint32_t vb = smem_u32(a.v_alias ? stage : stage + Ly.k_bytes);
-        issue_output_any(ndvb, tbase + 32 + pb * (kNH * kMaxDvBlocks), vb, smem_u32(sP + pb * (kNH * kChunk * 2)),
-                         IDESC_O);
-        umma_commit(&B.o_full[pb]);
-        umma_commit(&B.p_empty[pb]);
-        umma_commit(&B.kv_empty[m % ST]);
-      };
-      // O of chunk m may go once its P is written and the O buffer it reuses is drained
-      auto o_ready = [&](uint32_t m) -> bool {
-        const int pb = m & 1;
-        return mbar_test(&B.p_full[pb], (m >> 1) & 1) && (m < 2 || mbar_test(&B.o_empty[pb], ((m >> 1) - 1) & 1));
-      };
-      // bounded wait that issues ready O products meanwhile (only of chunks whose S is out)
-      auto wait_issuing_o = [&](uint64_t* bar, uint32_t parity) -> bool {
-        unsigned long long t0 = 0;
-        while (true) {
-          if (mbar_test(bar, parity)) return true;
-          if (o_next < n && o_ready(o_next)) {
-            issue_o(o_next++);
-            continue;
-          }
-          if (*abort_flag) return false;
-          const unsigned long long now = globaltimer_ns();
-          if (t0 == 0) t0 = now;
-          else if (now - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            record_error(a.err, IRS_DEVERR_TIMEOUT);
-            return false;
-          }
-        }
-      };
       for (long long t = blockIdx.x; t < a.T && alive; t += gridDim.x, ++qi) {
         const int b = qi & 1;
-        if (!wait_issuing_o(&B.idx_full[b], (qi >> 1) & 1)) { alive = false; break; }
+        if (!mbar_wait(&B.idx_full[b], (qi >> 1) & 1, abort_flag, a.err)) { alive = false; break; }
         const int nv = sNv[b];
         mbar_arrive(&B.idx_empty[b]);
         if (nv == 0) continue;
         const int nchunks = (nv + kChunk - 1) / kChunk;
         for (int sub = 0; sub < n_sub && alive; ++sub, ++u) {
           const int qb = u & 1;
-          if (!wait_issuing_o(&B.q_full[qb], (u >> 1) & 1)) { alive = false; break; }
+          if (!mbar_wait(&B.q_full[qb], (u >> 1) & 1, abort_flag, a.err)) { alive = false; break; }
           const uint32_t qbase = smem_u32(sQ + qb * (kNH * a.Dqk * 2));
           for (int c = 0; c < nchunks; ++c, ++n) {
             const int st = n % ST, sb = n & 1;
-            if (!wait_issuing_o(&B.kv_full[st], (n / ST) & 1)) { alive = false; break; }
-            if (n >= 2 && !wait_issuing_o(&B.s_empty[sb], ((n >> 1) - 1) & 1)) { alive = false; break; }
+            if (!mbar_wait(&B.kv_full[st], (n / ST) & 1, abort_flag, a.err)) { alive = false; break; }
+            if (n >= 2 && !mbar_wait(&B.s_empty[sb], ((n >> 1) - 1) & 1, abort_flag, a.err)) { alive = false; break; }
             fence_proxy_async_smem();   // gathered rows (generic-proxy writes) -> UMMA reads
             tc_fence_after();
             issue_scores_any(katoms, tbase + sb * kNH, smem_u32(smem + (uint32_t)st * Ly.stage_bytes), qbase, IDESC_S);
             umma_commit(&B.s_full[sb]);
             if (c == nchunks - 1) umma_commit(&B.q_empty[qb]);
-            if (o_next < n && o_ready(o_next)) issue_o(o_next++);
           }
         }
       }
-      // drain: the O products of the last chunks
-      while (alive && o_next < n) {
-        const int pb = o_next & 1;
-        if (!mbar_wait(&B.p_full[pb], (o_next >> 1) & 1, abort_flag, a.err)) break;
-        if (o_next >= 2 && !mbar_wait(&B.o_empty[pb], ((o_next >> 1) - 1) & 1, abort_flag, a.err)) break;
-        issue_o(o_next++);
+    }
+  } else if (warp == kOWarp) {
+    // =========================== O issuer ===========================
+    // O of chunk m goes once its P is written and the O buffer it reuses has been read;
+    // its completion frees the P buffer and the K/V stage.
+    if (lane == 0) {
+      uint32_t m = 0, qi = 0;
+      bool alive = true;
+      for (long long t = blockIdx.x; t < a.T && alive; t += gridDim.x, ++qi) {
+        const int b = qi & 1;
+        if (!mbar_wait(&B.idx_full[b], (qi >> 1) & 1, abort_flag, a.err)) { alive = false; break; }
+        const int nv = sNv[b];
+        mbar_arrive(&B.idx_empty[b]);
+        if (nv == 0) continue;
+        const int total = ((nv + kChunk - 1) / kChunk) * n_sub;
+        for (int j = 0; j < total; ++j, ++m) {
+          const int pb = m & 1;
+          if (!mbar_wait(&B.p_full[pb], (m >> 1) & 1, abort_flag, a.err)) { alive = false; break; }
+          if (m >= 2 && !mbar_wait(&B.o_empty[pb], ((m >> 1) - 1) & 1, abort_flag, a.err)) { alive = false; break; }
+          tc_fence_after();
+          const uint8_t* stage = smem + (uint32_t)(m % ST) * Ly.stage_bytes;
+          const uint32_t vb = smem_u32(a.v_alias ? stage : stage + Ly.k_bytes);
+          issue_output_any(ndvb, tbase + 32 + pb * (kNH * kMaxDvBlocks), vb, smem_u32(sP + pb * (kNH * kChunk * 2)),
+                           IDESC_O);
+          umma_commit(&B.o_full[pb]);
+          umma_commit(&B.kv_empty[m % ST]);
+        }
       }
     }
   } else {
     // =========================== softmax + correction (warps PW+1 .. PW+4) ===========================
-    const int sw = warp - (PW + 1);
+    const int sw = warp - (PW + 2);
     const int lanerow = (warp & 3) * 32 + lane;      // TMEM lane: key of S, dv of O
     const uint32_t lane_addr = tmem_lane_base(warp);
     uint32_t n = 0, u = 0, qi = 0;
@@ -517,7 +505,8 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
             l[h] = fmaf(l[h], al[h], s[h]);
             m[h] = mn;
           }
-          if (n >= 2) mbar_wait(&B.p_empty[sb], ((n >> 1) - 1) & 1, abort_flag, a.err);
+          // P buffer sb was last read by O of chunk n-2, whose completion this warp has
+          // already seen (o_full) when it folded that chunk in
           uint8_t* pdst = sP + sb * (kNH * kChunk * 2);
 #pragma unroll
           for (int h = 0; h < NH; ++h)
@@ -567,7 +556,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kSWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, 256);
   }
