@@ -72,15 +72,45 @@ __host__ __device__ inline AttnLayout attn_layout(int Dqk, int Dv, int W, int st
   return L;
 }
 
-__device__ __forceinline__ float warp_max(float x) {
+// Reduce NH per-lane values over the warp with op in a transposed butterfly: at each of the
+// first log2(NH) steps a lane keeps half of its values and swaps the other half with its
+// partner, so NH values take NH-1 + (5 - log2 NH) shuffles instead of 5*NH. On return
+// lane L holds the reduction of value head_of(L); lanes with the low (5 - log2 NH) bits
+// clear own the result.
+template <int NH>
+__device__ __forceinline__ constexpr int log2_nh() { return NH == 4 ? 2 : (NH == 8 ? 3 : 4); }
+template <int NH>
+__device__ __forceinline__ int transposed_head(int lane) {
+  int h = 0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
+  for (int lvl = 0; lvl < log2_nh<NH>(); ++lvl)
+    if (lane & (16 >> lvl)) h += NH >> (lvl + 1);
+  return h;
 }
-__device__ __forceinline__ float warp_sum(float x) {
+template <int NH, bool MAX>
+__device__ __forceinline__ float warp_reduce_transposed(const float (&x)[NH], int lane) {
+  float v[NH];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
+  for (int h = 0; h < NH; ++h) v[h] = x[h];
+#pragma unroll
+  for (int lvl = 0; lvl < log2_nh<NH>(); ++lvl) {
+    const int half = NH >> (lvl + 1), o = 16 >> lvl;
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? v[i] : v[i + half];
+      const float keep = up ? v[i + half] : v[i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, o);
+      v[i] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int o = 16 >> log2_nh<NH>(); o > 0; o >>= 1) {
+    const float got = __shfl_xor_sync(0xffffffffu, r, o);
+    r = MAX ? fmaxf(r, got) : r + got;
+  }
+  return r;
 }
 
 template <int NH>
@@ -91,37 +121,52 @@ __device__ __forceinline__ void tmem_ld_nh(uint32_t taddr, float (&v)[NH]) {
 }
 
 // Gather `rows` routed rows of kc 16-byte pieces each into a SW128 operand tile with
-// 16-byte cp.async, spread over the PT producer threads (piece i = r*kc + j goes to
-// thread i % PT). ids[r] are valid row indices. When a second tile (V) has the same row
-// width, both are gathered in the same pass so each row index is read once.
+// 16-byte cp.async, spread over the PT producer threads. When a second tile (V) has the
+// same row width, both are gathered in the same pass so each row index is read once.
+// ids[r] are valid row indices.
 template <int PT>
 __device__ __forceinline__ void gather_rows(uint32_t dst, const __nv_bfloat16* src, int64_t row_stride,
                                             uint32_t dst2, const __nv_bfloat16* src2, int64_t row_stride2,
                                             const int32_t* ids, int rows, int kc, int ptid) {
-  if (PT % kc == 0 && ((PT / kc) & 7) == 0) {
-    // fixed 16-byte column per thread; rows step by a multiple of 8, so the swizzle is fixed
+  const int dr = PT / kc;   // rows per pass
+  if (dr >= 2) {
+    // each thread keeps one 16-byte column j and walks rows r0, r0+dr, ...; the last
+    // PT - dr*kc threads stay idle
+    if (ptid >= dr * kc) return;
     const int j = ptid % kc;
-    const int dr = PT / kc;
     int r = ptid / kc;
-    const uint32_t off = sw128_offset(r, j * 8, kChunk);
-    uint32_t d = dst + off, d2 = dst2 + off;
     const __nv_bfloat16* sj = src + j * 8;
     const __nv_bfloat16* sj2 = src2 + j * 8;
-    if (src2 != nullptr) {
+    if ((dr & 7) == 0) {
+      // rows step by a multiple of 8: the swizzled chunk position is fixed
+      const uint32_t off = sw128_offset(r, j * 8, kChunk);
+      uint32_t d = dst + off, d2 = dst2 + off;
+      if (src2 != nullptr) {
 #pragma unroll 4
-      for (; r < rows; r += dr, d += dr * 128, d2 += dr * 128) {
-        const int64_t id = ids[r];
-        cp_async_16(d, sj + id * row_stride, 16u);
-        cp_async_16(d2, sj2 + id * row_stride2, 16u);
+        for (; r < rows; r += dr, d += dr * 128, d2 += dr * 128) {
+          const int64_t id = ids[r];
+          cp_async_16(d, sj + id * row_stride, 16u);
+          cp_async_16(d2, sj2 + id * row_stride2, 16u);
+        }
+      } else {
+#pragma unroll 4
+        for (; r < rows; r += dr, d += dr * 128) cp_async_16(d, sj + (int64_t)ids[r] * row_stride, 16u);
       }
     } else {
+      const uint32_t atom = (uint32_t)(j >> 3) * (kChunk * 128);
+      const uint32_t jc = (uint32_t)(j & 7);
 #pragma unroll 4
-      for (; r < rows; r += dr, d += dr * 128) cp_async_16(d, sj + (int64_t)ids[r] * row_stride, 16u);
+      for (; r < rows; r += dr) {
+        const int64_t id = ids[r];
+        const uint32_t off = atom + (uint32_t)r * 128 + ((jc ^ ((uint32_t)r & 7)) << 4);
+        cp_async_16(dst + off, sj + id * row_stride, 16u);
+        if (src2 != nullptr) cp_async_16(dst2 + off, sj2 + id * row_stride2, 16u);
+      }
     }
     return;
   }
   int r = ptid / kc, j = ptid - (ptid / kc) * kc;
-  const int dr = PT / kc, dj = PT - dr * kc;
+  const int dj = PT - dr * kc;
   while (r < rows) {
     const int64_t id = ids[r];
     const uint32_t off = sw128_offset(r, j * 8, kChunk);
@@ -275,14 +320,16 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
 
   if (warp < PW) {
     // =========================== producer (warps 0..PW-1) ===========================
+    // The producer threads agree (named_bar_and) once per row; inside a row each thread
+    // waits for its stages on its own, so warps run ahead of one another. A thread whose
+    // wait gave up stops issuing and carries that into the next agreement.
     const int ptid = tid;
     uint32_t n = 0, u = 0, qi = 0;
-    bool alive = true;
-    for (long long t = blockIdx.x; t < a.T && alive; t += gridDim.x, ++qi) {
+    bool mine = true;
+    for (long long t = blockIdx.x; t < a.T; t += gridDim.x, ++qi) {
       const int b = qi & 1;
-      bool ok = qi < 2 || mbar_wait(&B.idx_empty[b], ((qi >> 1) - 1) & 1, abort_flag, a.err);
-      alive = named_bar_and(1, kProducerThreads, ok);
-      if (!alive) break;
+      const bool ok = mine && (qi < 2 || mbar_wait(&B.idx_empty[b], ((qi >> 1) - 1) & 1, abort_flag, a.err));
+      if (!named_bar_and(1, kProducerThreads, ok)) break;
       // ---- compact the valid IDs of route row t (8 loads in flight per thread) ----
       const int32_t* rrow = a.route + t * a.route_stride;
       int run = 0;
@@ -316,14 +363,12 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
       const int nv = run;
       if (nv == 0) continue;
       const int nchunks = (nv + kChunk - 1) / kChunk;
-      for (int sub = 0; sub < n_sub && alive; ++sub, ++u) {
+      for (int sub = 0; sub < n_sub && mine; ++sub, ++u) {
         const int g = sub / a.nhb, hb = sub - g * a.nhb;
         const int h0 = (a.g0 + g) * a.G + hb * a.HB;
         const int nh = min(a.HB, a.G - hb * a.HB);
         const int qb = u & 1;
-        ok = u < 2 || mbar_wait(&B.q_empty[qb], ((u >> 1) - 1) & 1, abort_flag, a.err);
-        alive = named_bar_and(1, kProducerThreads, ok);
-        if (!alive) break;
+        if (u >= 2 && !mbar_wait(&B.q_empty[qb], ((u >> 1) - 1) & 1, abort_flag, a.err)) { mine = false; break; }
         const uint32_t q_dst = smem_u32(sQ + qb * (kNH * a.Dqk * 2));
         for (int i = ptid; i < nh * qc; i += kProducerThreads) {
           const int r = i / qc, j = i - r * qc;
@@ -334,9 +379,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
         const __nv_bfloat16* vbase = a.v + (long long)(a.g0 + g) * a.v_sh;
         for (int c = 0; c < nchunks; ++c, ++n) {
           const int st = n % ST;
-          ok = (int)n < ST || mbar_wait(&B.kv_empty[st], ((n / ST) - 1) & 1, abort_flag, a.err);
-          alive = named_bar_and(1, kProducerThreads, ok);
-          if (!alive) break;
+          if ((int)n >= ST && !mbar_wait(&B.kv_empty[st], ((n / ST) - 1) & 1, abort_flag, a.err)) { mine = false; break; }
           const int rows = min(kChunk, nv - c * kChunk);
           const int32_t* ids = sIdx + c * kChunk;
           uint8_t* stage = smem + (uint32_t)st * Ly.stage_bytes;
@@ -487,10 +530,10 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           const bool kvalid = c * kChunk + lanerow < nv;
           float* red = sRed + sb * (4 * kNH);
 #pragma unroll
-          for (int h = 0; h < NH; ++h) {
-            s[h] = (kvalid && h < nh) ? s[h] * a.scale_log2 : -INFINITY;
-            const float mx = warp_max(s[h]);
-            if (lane == 0) red[sw * kNH + h] = mx;
+          for (int h = 0; h < NH; ++h) s[h] = (kvalid && h < nh) ? s[h] * a.scale_log2 : -INFINITY;
+          {
+            const float mx = warp_reduce_transposed<NH, true>(s, lane);
+            if ((lane & ((32 >> log2_nh<NH>()) - 1)) == 0) red[sw * kNH + transposed_head<NH>(lane)] = mx;
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&B.red[sb]);
@@ -524,10 +567,9 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
         // ---- finalize: row sums over the 128 key lanes, normalise, store ----
         const int fb = u & 1;
         float* fin = sFin + fb * (4 * kNH);
-#pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const float sm = warp_sum(l[h]);
-          if (lane == 0) fin[sw * kNH + h] = sm;
+        {
+          const float sm = warp_reduce_transposed<NH, false>(l, lane);
+          if ((lane & ((32 >> log2_nh<NH>()) - 1)) == 0) fin[sw * kNH + transposed_head<NH>(lane)] = sm;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.fin[fb]);
@@ -575,9 +617,10 @@ AttnPlan plan_attn(const AttnArgs& a, int num_sms) {
   return p;
 }
 
-// 8 producer warps where the softmax warps' registers leave room, else 4
+// Producer warps by softmax register need: a warp scheduler holds 16K registers, so with
+// 14 warps (4 on some schedulers) a thread gets at most 128, with 12 warps 168.
 template <int NH, int DVB>
-constexpr int producer_warps() { return NH * DVB <= 32 ? 8 : 4; }
+constexpr int producer_warps() { return NH * DVB <= 8 ? 8 : (NH * DVB <= 32 ? 6 : 4); }
 
 template <int NH, int DVB>
 static cudaError_t attn_attr(size_t smem) {
