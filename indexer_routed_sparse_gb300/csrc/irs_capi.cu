@@ -30,7 +30,7 @@ struct DeviceInfo {
   bool checked = false;
   bool ok = false;
   int num_sms = 0;
-  size_t score_smem = 0, topk_smem = 0, attn_smem = 0;   // largest values configured so far
+  size_t score_smem = 0, topk_smem = 0, attn_smem = 0, mla_smem = 0;   // largest values configured so far
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -259,6 +259,18 @@ irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_
   a.nhb = (a.G + a.HB - 1) / a.HB;
   a.v_alias = (v == k && v_stride_t == k_stride_t && v_stride_h == k_stride_h && Dv <= Dqk) ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
+  if (irs::mla_supported(a)) {
+    const size_t smem = irs::mla_smem_bytes(a);
+    {
+      std::lock_guard<std::mutex> lk(g_dev_mu);
+      if (dev->mla_smem < smem) {
+        if ((s = launch_status(irs::configure_mla_kernel(smem), "configuring latent attention")) != IRS_OK) return s;
+        dev->mla_smem = smem;
+      }
+    }
+    return launch_status(irs::launch_mla(a, dev->num_sms, reinterpret_cast<cudaStream_t>(stream)),
+                         "launching latent attention");
+  }
   const irs::AttnPlan p = irs::plan_attn(a, dev->num_sms);
   if (p.smem > kMaxSmem) return fail(IRS_ERR_VALUE, "attention tile does not fit in shared memory");
   {

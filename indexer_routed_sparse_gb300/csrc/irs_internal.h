@@ -75,6 +75,13 @@ struct AttnPlan {
 };
 
 AttnPlan plan_attn(const AttnArgs& a, int num_sms);
+
+// Latent attention (one KV head whose rows are keys and, by their first Dv dims, values):
+// 64 query heads per work item with the output accumulated in TMEM.
+bool mla_supported(const AttnArgs& a);
+size_t mla_smem_bytes(const AttnArgs& a);
+cudaError_t configure_mla_kernel(size_t smem);
+cudaError_t launch_mla(const AttnArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t configure_attn_kernel(size_t smem);
 cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 

@@ -89,6 +89,36 @@ def test_latent_small_all_rows(irs):
     parity.check_attention(out, lse, ref_o, ref_l, rows)
 
 
+@pytest.mark.parametrize("Hq,Dqk,Dv,W,holes,boost", [
+    (64, 576, 512, 300, True, 1.0),     # one 64-head block, -1 holes, rows without keys
+    (128, 192, 128, 129, False, 1.0),   # narrow latent rows, W one past two 64-key chunks
+    (128, 576, 256, 700, True, 1.0),    # two dv blocks
+    (64, 576, 512, 600, False, 12.0),   # later keys' non-value dims 12x larger: maxima move, O is rescaled
+])
+def test_latent_kernel_shapes(irs, Hq, Dqk, Dv, W, holes, boost):
+    """One latent KV head whose rows are the keys and, by their first Dv dims, the values."""
+    T, Tk = 96, 1200
+    rng = np.random.default_rng(Hq * 7 + W)
+    q = irs_synth.f32_to_bf16_bits(rng.standard_normal((T, Hq, Dqk), dtype=np.float32))
+    kvf = rng.standard_normal((Tk, 1, Dqk), dtype=np.float32)
+    kvf[Tk // 2:, :, Dv:] *= boost   # scores grow along the route; values keep their scale
+    kv = irs_synth.f32_to_bf16_bits(kvf)
+    routes = np.full((T, W), -1, np.int32)
+    for t in range(T):
+        if t % 17 == 5:
+            continue                                   # a row without any valid slot
+        n = int(rng.integers(1, W + 1))
+        ids = np.sort(rng.choice(Tk, size=n, replace=False)).astype(np.int32)
+        slots = np.sort(rng.permutation(W)[:n]) if holes else np.arange(n)
+        routes[t, slots] = ids
+    kvd = torch.from_numpy(kv).view(torch.bfloat16).to(DEV)
+    scale = 1.0 / math.sqrt(Dqk)
+    out, lse = attend(irs, q, kvd, kvd[:, :, :Dv], routes, scale)
+    ref_o, ref_l = O.latent_attention(q, kv, routes, scale, Dv=Dv)
+    parity.check_attention(out, lse, ref_o, ref_l, np.arange(T))
+    assert torch.all(out[5] == 0) and torch.all(torch.isneginf(lse[5]))
+
+
 @pytest.mark.parametrize("Hq,Hkv,Dqk,Dv,W", [
     (4, 4, 64, 128, 1),        # G = 1, a single slot
     (32, 1, 128, 128, 300),    # G = 32: two head blocks per KV head
