@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
             if (blk < ndvb) {
               float o[NH];
               tmem_ld_nh<NH>(tbase + 32 + ob * (kNH * kMaxDvBlocks) + blk * kNH + lane_addr, o);
-              tmem_ld_wait();
+              tmem_ld_wait_regs(o);
 #pragma unroll
               for (int h = 0; h < NH; ++h) acc[blk][h] = fmaf(acc[blk][h], alp[h], o[h]);
             }
@@ -523,7 +523,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           tc_fence_after();
           float s[NH];
           tmem_ld_nh<NH>(tbase + sb * kNH + lane_addr, s);
-          tmem_ld_wait();
+          tmem_ld_wait_regs(s);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&B.s_empty[sb]);

@@ -322,7 +322,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           float v2[2][32];
           tmem_ld32(tbase + lane_addr + buf * kScoreN + cc, v2[0]);
           if (kHalfCols > 32) tmem_ld32(tbase + lane_addr + buf * kScoreN + cc + 32, v2[1]);
-          tmem_ld_wait();
+          tmem_ld_wait_regs(v2[0]);
+          tmem_ld_wait_regs(v2[1]);
 #pragma unroll
           for (int half2 = 0; half2 < 2; ++half2) {
           if (half2 == 1 && kHalfCols <= 32) break;

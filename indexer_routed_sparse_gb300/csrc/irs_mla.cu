@@ -15,11 +15,16 @@
 //   * S^T = K.Q^T runs as M=128 (keys) x N=64 (heads): rows 64..127 read the next atom and
 //     are ignored (a 64-row chunk keeps two stages in 227 KB);
 //   * O^T = V^T.P^T (M=128 dv per block, N=64 heads, K=64 keys) accumulates in TMEM over
-//     the whole route (4 blocks x 64 columns for Dv = 512), with P^T written over the last
-//     key atom of the stage, which S no longer needs (so Dqk >= Dv + 64);
-//   * the running maxima move only when a head's chunk maximum exceeds them by more than
-//     2^8 (base-2 scores), and only then is O^T rescaled in TMEM, by the same four warps
-//     that later normalise and store it.
+//     the whole route (4 blocks x 64 columns for Dv = 512); P is written key-major (one
+//     128-byte row of 64 heads per key, read as an MN-major operand) over the last key
+//     atom of the stage, which S no longer needs (so Dqk >= Dv + 64);
+//   * row sums stay in FP32: each softmax thread (one key) accumulates its 64 unrounded
+//     probabilities in its own TMEM row beside O^T, and the rows are summed over the keys
+//     once per item;
+//   * running maxima move only when a score exceeds them by more than 2^8 (base-2
+//     scores). Each softmax thread checks its 64 scores against that bound and the two
+//     softmax warps vote; only then (and at the start of an item) are the head maxima
+//     reduced over the keys, and O^T and l^T rescaled in TMEM.
 // Consecutive items are the two head blocks of one query, so neighbouring CTAs gather
 // the same rows and the second read is an L2 hit.
 //
@@ -42,7 +47,9 @@ constexpr int kMlaPW = 9;                  // producer warps (288 threads: 4 row
 constexpr int kMlaProducers = 32 * kMlaPW;
 constexpr int kMlaThreads = 32 * (kMlaPW + 6);
 constexpr float kRescaleLog2 = 8.f;
-constexpr uint32_t kTmemCols = 512;        // S^T 2 x 64 columns, O^T up to 4 x 64 columns
+constexpr uint32_t kTmemCols = 512;        // S^T 2 x 64, O^T up to 4 x 64, row sums 64 columns
+constexpr uint32_t kOCol = 2 * kMH;        // first O^T column
+constexpr uint32_t kLCol = 6 * kMH;        // per-key FP32 row sums (lanes 0..63)
 
 struct MlaLayout {
   uint32_t stage_bytes, q_off, idx_off, misc_off, bar_off, total;
@@ -55,9 +62,9 @@ __host__ __device__ inline MlaLayout mla_layout(int Dqk, int W) {
   L.q_off = L.stage_bytes * kMlaStages;
   L.idx_off = L.q_off + katoms * kAtom;
   L.misc_off = L.idx_off + (uint32_t)((W + 63) / 64) * 64 * 4;
-  // m_run[64] alpha[64] red[2][64] lfin[2][64] flag[2] nv[2] cnt[kMlaPW]
-  L.bar_off = L.misc_off + (64 + 64 + 128 + 128) * 4 + (2 + 2 + 12) * 4;
-  L.total = L.bar_off + 32 * 8 + 16;
+  // m_run[64] thr[64] alpha[64] red[2][64] | flagw[2][2] flag[2] nv[2] cnt[kMlaPW]
+  L.bar_off = L.misc_off + (64 * 3 + 128) * 4 + (4 + 2 + 2 + 12) * 4;
+  L.total = L.bar_off + 24 * 8 + 16;
   return L;
 }
 
@@ -118,16 +125,17 @@ __device__ __forceinline__ void mla_issue_s_any(int katoms, uint32_t d, uint32_t
   }
 }
 // O^T (+)= V^T.P^T for NB blocks of 128 dv: A = V^T read MN-major from the stage (two
-// 64-dv atoms per block, LBO = one atom), B = P^T (64 head rows x 64 keys, one atom).
+// 64-dv atoms per block, LBO = one atom), B = P stored key-major (64 key rows x 64 heads,
+// MN-major operand).
 template <int NB>
 __device__ __forceinline__ void mla_issue_o(uint32_t d, uint32_t vb, uint32_t pb, uint32_t idesc, bool acc) {
-  const uint64_t a0 = sdesc_sw128(vb, kAtom, 1024), b0 = sdesc_sw128(pb, 16, 1024);
+  const uint64_t a0 = sdesc_sw128(vb, kAtom, 1024), b0 = sdesc_sw128(pb, kAtom, 1024);
 #pragma unroll
   for (int blk = 0; blk < NB; ++blk) {
 #pragma unroll
     for (int ks = 0; ks < kMK / 16; ++ks)
       umma_bf16(d + blk * kMH, a0 + (uint64_t)(((2 * blk) * kAtom + ks * 2048) >> 4),
-                b0 + (uint64_t)((ks * 32) >> 4), idesc, (acc || ks > 0) ? 1u : 0u);
+                b0 + (uint64_t)((ks * 2048) >> 4), idesc, (acc || ks > 0) ? 1u : 0u);
   }
 }
 __device__ __forceinline__ void mla_issue_o_any(int ndvb, uint32_t d, uint32_t vb, uint32_t pb, uint32_t idesc,
@@ -139,7 +147,6 @@ __device__ __forceinline__ void mla_issue_o_any(int ndvb, uint32_t d, uint32_t v
     default: mla_issue_o<4>(d, vb, pb, idesc, acc); break;
   }
 }
-
 // rows x kc 16-byte pieces into a tile of 64-row SW128 atoms (row stride `stride`
 // elements; row r comes from base + ids[r] * stride, or base + r * stride without ids)
 __device__ __forceinline__ void mla_copy_rows(uint32_t dst, const __nv_bfloat16* base, int64_t stride,
@@ -178,10 +185,11 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
   uint8_t* sQ = smem + Ly.q_off;
   int32_t* sIdx = reinterpret_cast<int32_t*>(smem + Ly.idx_off);
   float* m_run = reinterpret_cast<float*>(smem + Ly.misc_off);
-  float* alpha = m_run + 64;
+  float* thr = m_run + 64;       // m_run + 8: beyond it a score moves the running maximum
+  float* alpha = thr + 64;
   float* red = alpha + 64;       // [2 softmax warps][64]
-  float* lfin = red + 128;       // [2][64]
-  int32_t* flag = reinterpret_cast<int32_t*>(lfin + 128);   // [2]
+  int32_t* flagw = reinterpret_cast<int32_t*>(red + 128);   // [2 chunk parities][2 softmax warps]
+  int32_t* flag = flagw + 4;                                // [2] chunk needs an O/l rescale
   int32_t* sNv = flag + 2;                                  // [2]
   int32_t* sCnt = sNv + 2;                                  // [kMlaPW]
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Ly.bar_off);
@@ -195,15 +203,16 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
   uint64_t* s_empty = bar + 12;      // [2]
   uint64_t* p_full = bar + 14;       // [2]
   uint64_t* red_bar = bar + 16;
-  uint64_t* stat_bar = bar + 17;
-  uint64_t* corr_bar = bar + 18;
-  uint64_t* fin_bar = bar + 19;
+  uint64_t* red2_bar = bar + 17;
+  uint64_t* stat_bar = bar + 18;
+  uint64_t* corr_bar = bar + 19;
+  uint64_t* fin_bar = bar + 22;
   uint64_t* o_full = bar + 20;
   uint64_t* o_free = bar + 21;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 32);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 24);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   constexpr uint32_t IDESC_S = idesc_bf16(128, kMH, false, false);
-  constexpr uint32_t IDESC_O = idesc_bf16(128, kMH, true, false);
+  constexpr uint32_t IDESC_O = idesc_bf16(128, kMH, true, true);
 
   // ---- set-up: finite operand memory (S^T reads 64 rows past every atom), barriers, TMEM ----
   {
@@ -224,6 +233,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
     mbar_init(q_full, kMlaProducers);
     mbar_init(q_empty, 1);
     mbar_init(red_bar, 4);
+    mbar_init(red2_bar, 2);
     mbar_init(stat_bar, 1);
     mbar_init(corr_bar, 4);
     mbar_init(fin_bar, 2);
@@ -352,7 +362,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
           }
           tc_fence_after();
           const uint32_t stage = smem_u32(smem + (m & 1) * Ly.stage_bytes);
-          mla_issue_o_any(ndvb, tbase + 2 * kMH, stage, stage + (uint32_t)(katoms - 1) * kAtom, IDESC_O, c > 0);
+          const uint32_t pkeys = stage + (uint32_t)(katoms - 1) * kAtom;
+          mla_issue_o_any(ndvb, tbase + kOCol, stage, pkeys, IDESC_O, c > 0);
           umma_commit(o_full);
           umma_commit(&kv_empty[m & 1]);
         }
@@ -364,7 +375,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
     const int lanerow = q * 32 + lane;            // key of S (q < 2), dv of O
     const uint32_t lane_addr = tmem_lane_base(warp);
     const int hA = mla_head(lane);                // heads this lane reduces: hA, hA + 1
-    uint32_t n = 0, qi = 0, uq = 0, kcorr = 0;
+    uint32_t n = 0, qi = 0, uq = 0, kslow = 0, kcorr = 0;
     for (long long it = blockIdx.x; it < items; it += gridDim.x, ++qi) {
       const long long t = it / nhb;
       const int h0 = (int)(it - t * nhb) * kMH;
@@ -385,7 +396,6 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
         continue;
       }
       const int nchunks = (nv + kMK - 1) / kMK;
-      float lA = 0.f, lB = 0.f;   // this warp's share of the row sums of heads hA, hA+1 (q < 2)
       for (int c = 0; c < nchunks; ++c, ++n) {
         const int sb = n & 1;
         float s[64];
@@ -394,77 +404,124 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
           tc_fence_after();
           tmem_ld32(tbase + sb * kMH + lane_addr, *reinterpret_cast<float(*)[32]>(&s[0]));
           tmem_ld32(tbase + sb * kMH + 32 + lane_addr, *reinterpret_cast<float(*)[32]>(&s[32]));
-          tmem_ld_wait();
+          tmem_ld_wait_regs(s);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&s_empty[sb]);
           const bool kvalid = c * kMK + lanerow < nv;
-#pragma unroll
-          for (int h = 0; h < 64; ++h) s[h] = kvalid ? s[h] * a.scale_log2 : -INFINITY;
-          float r0, r1;
-          mla_reduce64<true>(s, lane, r0, r1);
-          red[q * 64 + hA] = r0;
-          red[q * 64 + hA + 1] = r1;
-          __syncwarp();
-        }
-        if (lane == 0) mbar_arrive(red_bar);
-        if (q == 0) {
-          // new running maxima, rescale factors and the rescale flag of this chunk
-          mbar_wait(red_bar, n & 1, abort_flag, a.err);
-          bool need = false;
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int h = hA + e;
-            const float cm = fmaxf(red[h], red[64 + h]);
-            float mn = cm, al = 1.f;
-            if (c > 0) {
-              const float mo = m_run[h];
-              if (cm > mo + kRescaleLog2) {
-                al = exp2f(mo - cm);
-                need = true;
-              } else {
-                mn = mo;
-              }
-            }
-            m_run[h] = mn;
-            alpha[h] = al;
-          }
-          need = __any_sync(0xffffffffu, need);
-          if (lane == 0) flag[sb] = need ? 1 : 0;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(stat_bar);
-        } else {
-          mbar_wait(stat_bar, n & 1, abort_flag, a.err);
-        }
-        if (q < 2) {
-          // P^T over the last key atom of the stage (S of this chunk is complete)
-          uint8_t* pdst = smem + (n & 1) * Ly.stage_bytes + (katoms - 1) * kAtom;
+          bool ex = c == 0;
 #pragma unroll
           for (int h = 0; h < 64; ++h) {
-            s[h] = exp2f(s[h] - m_run[h]);
-            *reinterpret_cast<__nv_bfloat16*>(pdst + sw128_offset(h, lanerow, kMH)) = __float2bfloat16_rn(s[h]);
+            s[h] = kvalid ? s[h] * a.scale_log2 : -INFINITY;
+            ex = ex || s[h] > thr[h];
           }
-          float r0, r1;
-          mla_reduce64<false>(s, lane, r0, r1);
-          lA = fmaf(lA, alpha[hA], r0);
-          lB = fmaf(lB, alpha[hA + 1], r1);
+          ex = __any_sync(0xffffffffu, ex);
+          if (lane == 0) flagw[sb * 2 + q] = ex ? 1 : 0;
+          __syncwarp();
+        }
+        // o_full completes once per chunk; a parity wait is only sound if every phase is
+        // waited in order, before the next one can complete. Warps 2 and 3 wait for O of
+        // the previous chunk here (O of this chunk needs their arrival below), warps 0 and 1
+        // before they release this chunk's P.
+        if (q >= 2 && c > 0) mbar_wait(o_full, (n - 1) & 1, abort_flag, a.err);
+        if (lane == 0) mbar_arrive(red_bar);
+        mbar_wait(red_bar, n & 1, abort_flag, a.err);
+        const bool slow = (flagw[sb * 2] | flagw[sb * 2 + 1]) != 0;
+        if (slow) {
+          // reduce the head maxima over the 64 keys; move those that grew past the bound
+          if (q < 2) {
+            float r0, r1;
+            mla_reduce64<true>(s, lane, r0, r1);
+            red[q * 64 + hA] = r0;
+            red[q * 64 + hA + 1] = r1;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(red2_bar);
+          }
+          if (q == 0) {
+            mbar_wait(red2_bar, kslow & 1, abort_flag, a.err);
+            bool need = false;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int h = hA + e;
+              const float cm = fmaxf(red[h], red[64 + h]);
+              float mn = cm, al = 1.f;
+              if (c > 0) {
+                const float mo = m_run[h];
+                if (cm > mo + kRescaleLog2) {
+                  al = exp2f(mo - cm);
+                  need = true;
+                } else {
+                  mn = mo;
+                }
+              }
+              m_run[h] = mn;
+              thr[h] = mn + kRescaleLog2;
+              alpha[h] = al;
+            }
+            need = __any_sync(0xffffffffu, need);
+            if (lane == 0) flag[sb] = need ? 1 : 0;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(stat_bar);
+          } else {
+            mbar_wait(stat_bar, kslow & 1, abort_flag, a.err);
+          }
+          ++kslow;
+        } else if (q == 0 && lane == 0) {
+          flag[sb] = 0;
+        }
+        if (q < 2) {
+          // P key-major over the last key atom of the stage (S of this chunk is complete):
+          // row `lanerow`, 16-byte chunk j = heads 8j..8j+7 at position j ^ (row & 7)
+#pragma unroll
+          for (int h = 0; h < 64; ++h) s[h] = exp2f(s[h] - m_run[h]);
+          // this key's FP32 row sums: l <- l * alpha (when the maxima moved) + p
+          const bool resc = slow && flag[sb] != 0;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float lp[32];
+            const uint32_t ta = tbase + kLCol + half * 32 + lane_addr;
+            if (c > 0) {
+              tmem_ld32(ta, lp);
+              tmem_ld_wait_regs(lp);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float old = c > 0 ? (resc ? lp[i] * alpha[half * 32 + i] : lp[i]) : 0.f;
+              lp[i] = old + s[half * 32 + i];
+            }
+            tmem_st32(ta, lp);
+            tmem_st_wait();
+          }
+          uint8_t* prow = smem + (n & 1) * Ly.stage_bytes + (katoms - 1) * kAtom + lanerow * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int h = 8 * j + 2 * e;
+              const __nv_bfloat162 two = __floats2bfloat162_rn(s[h], s[h + 1]);
+              pk[e] = *reinterpret_cast<const uint32_t*>(&two);
+            }
+            *reinterpret_cast<uint4*>(prow + ((j ^ (lanerow & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
           fence_proxy_async_smem();
+          if (c > 0) mbar_wait(o_full, (n - 1) & 1, abort_flag, a.err);
           __syncwarp();
           if (lane == 0) mbar_arrive(&p_full[sb]);
         }
-        if (flag[sb]) {
-          // O^T holds chunks 0..c-1 at the old maxima: wait for chunk c-1, rescale
-          mbar_wait(o_full, (n - 1) & 1, abort_flag, a.err);
+        if (slow && flag[sb]) {
+          // O^T and l^T hold chunks 0..c-1 at the old maxima (all complete: waited above)
           tc_fence_after();
           for (int blk = 0; blk < ndvb; ++blk)
             for (int half = 0; half < 2; ++half) {
               float v[32];
-              const uint32_t ta = tbase + 2 * kMH + blk * kMH + half * 32 + lane_addr;
+              const uint32_t ta = tbase + kOCol + blk * kMH + half * 32 + lane_addr;
               tmem_ld32(ta, v);
-              tmem_ld_wait();
+              tmem_ld_wait_regs(v);
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] *= alpha[half * 32 + i];
               tmem_st32(ta, v);
+              tmem_st_wait();   // the registers are reused by the next load
             }
           tmem_st_wait();
           tc_fence_before();
@@ -474,40 +531,50 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
           ++kcorr;
         }
       }
-      // ---- epilogue: O^T / l -> out, lse ----
+      // ---- epilogue: sum the per-key row sums over the 64 keys, then O^T / l -> out, lse ----
       if (q < 2) {
-        lfin[q * 64 + hA] = lA;
-        lfin[q * 64 + hA + 1] = lB;
+        float lp[64];
+        tmem_ld32(tbase + kLCol + lane_addr, *reinterpret_cast<float(*)[32]>(&lp[0]));
+        tmem_ld32(tbase + kLCol + 32 + lane_addr, *reinterpret_cast<float(*)[32]>(&lp[32]));
+        tmem_ld_wait_regs(lp);
+        float r0, r1;
+        mla_reduce64<false>(lp, lane, r0, r1);
+        red[q * 64 + hA] = r0;
+        red[q * 64 + hA + 1] = r1;
         __syncwarp();
         if (lane == 0) mbar_arrive(fin_bar);
       }
       mbar_wait(fin_bar, uq & 1, abort_flag, a.err);
+      ++uq;
       mbar_wait(o_full, (n - 1) & 1, abort_flag, a.err);
       tc_fence_after();
-      for (int blk = 0; blk < ndvb; ++blk)
-        for (int half = 0; half < 2; ++half) {
-          float v[32];
-          tmem_ld32(tbase + 2 * kMH + blk * kMH + half * 32 + lane_addr, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int h = half * 32 + i;
-            const float l = lfin[h] + lfin[64 + h];
-            orow[(int64_t)h * a.Dv + blk * 128 + lanerow] = __float2bfloat16_rn(l > 0.f ? v[i] / l : 0.f);
-          }
-        }
       if (a.lse != nullptr && q == 0) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int h = hA + e;
-          const float l = lfin[h] + lfin[64 + h];
+          const int h = lane + 32 * e;
+          const float l = red[h] + red[64 + h];
           a.lse[t * a.Hq + h0 + h] = l > 0.f ? (m_run[h] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        }
+      }
+      for (int half = 0; half < 2; ++half) {
+        float inv[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float l = red[half * 32 + i] + red[64 + half * 32 + i];
+          inv[i] = l > 0.f ? 1.f / l : 0.f;
+        }
+        for (int blk = 0; blk < ndvb; ++blk) {
+          float v[32];
+          tmem_ld32(tbase + kOCol + blk * kMH + half * 32 + lane_addr, v);
+          tmem_ld_wait_regs(v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            orow[(int64_t)(half * 32 + i) * a.Dv + blk * 128 + lanerow] = __float2bfloat16_rn(v[i] * inv[i]);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);
-      ++uq;
     }
   }
   tc_fence_before();

@@ -198,6 +198,16 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  
 __device__ __forceinline__ uint32_t tmem_lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// tcgen05.ld fills its destination registers asynchronously, but the compiler sees them
+// as written when the load statement ends and may move their uses above a separate
+// wait. Waiting through this helper ties every loaded register to the wait: each passes
+// through an empty statement ordered after it, so no use can be scheduled earlier.
+template <int N>
+__device__ __forceinline__ void tmem_ld_wait_regs(float (&v)[N]) {
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]));
+}
 
 // 32 lanes x 4 / 8 columns of 32 bits
 __device__ __forceinline__ void tmem_ld4(uint32_t taddr, float* v) {
