@@ -543,8 +543,8 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
             const float cm = fmaxf(fmaxf(red[h], red[kNH + h]), fmaxf(red[2 * kNH + h], red[3 * kNH + h]));
             const float mn = fmaxf(m[h], cm);
             const float base = mn == -INFINITY ? 0.f : mn;
-            al[h] = exp2f(m[h] - base);
-            s[h] = exp2f(s[h] - base);   // p
+            al[h] = ex2_approx(m[h] - base);
+            s[h] = ex2_approx(s[h] - base);   // p
             l[h] = fmaf(l[h], al[h], s[h]);
             m[h] = mn;
           }

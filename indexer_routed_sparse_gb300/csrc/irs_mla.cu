@@ -24,7 +24,9 @@
 //   * running maxima move only when a score exceeds them by more than 2^8 (base-2
 //     scores). Each softmax thread checks its 64 scores against that bound and the two
 //     softmax warps vote; only then (and at the start of an item) are the head maxima
-//     reduced over the keys, and O^T and l^T rescaled in TMEM.
+//     reduced over the keys, and O^T and the row sums rescaled in TMEM. The maxima are
+//     kept in TMEM beside the row sums, one copy per softmax lane: the hot path reads no
+//     shared memory, whose load queue the producers' copies keep full.
 // Consecutive items are the two head blocks of one query, so neighbouring CTAs gather
 // the same rows and the second read is an L2 hit.
 //
@@ -50,6 +52,7 @@ constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kTmemCols = 512;        // S^T 2 x 64, O^T up to 4 x 64, row sums 64 columns
 constexpr uint32_t kOCol = 2 * kMH;        // first O^T column
 constexpr uint32_t kLCol = 6 * kMH;        // per-key FP32 row sums (lanes 0..63)
+constexpr uint32_t kMCol = 7 * kMH;        // running head maxima, one copy per softmax lane
 
 struct MlaLayout {
   uint32_t stage_bytes, q_off, idx_off, misc_off, bar_off, total;
@@ -62,32 +65,29 @@ __host__ __device__ inline MlaLayout mla_layout(int Dqk, int W) {
   L.q_off = L.stage_bytes * kMlaStages;
   L.idx_off = L.q_off + katoms * kAtom;
   L.misc_off = L.idx_off + (uint32_t)((W + 63) / 64) * 64 * 4;
-  // m_run[64] thr[64] alpha[64] red[2][64] | flagw[2][2] flag[2] nv[2] cnt[kMlaPW]
-  L.bar_off = L.misc_off + (64 * 3 + 128) * 4 + (4 + 2 + 2 + 12) * 4;
+  // m_run[64] alpha[64] red[2][64] | flagw[2][2] flag[2] nv[2] cnt[kMlaPW]
+  L.bar_off = L.misc_off + (64 * 2 + 128) * 4 + (4 + 2 + 2 + 12) * 4;
   L.total = L.bar_off + 24 * 8 + 16;
   return L;
 }
 
-// transposed butterfly over 64 values per lane: on return lane L holds the reduction of
-// heads mla_head(L) and mla_head(L) + 1 over the warp
-__device__ __forceinline__ int mla_head(int lane) {
-  return ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 + ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4 +
-         (lane & 1) * 2;
-}
+// transposed butterfly over 32 values per lane: at each step a lane keeps half of its
+// values and swaps the other half with its partner, so lane L ends with the reduction of
+// value L over the warp (31 shuffles instead of 5 x 32)
 template <bool MAX>
-__device__ __forceinline__ void mla_reduce64(const float (&x)[64], int lane, float& r0, float& r1) {
-  float v[32];
+__device__ __forceinline__ float mla_reduce32(const float (&x)[32], int lane) {
+  float v[16];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < 16; ++i) {
     const bool up = (lane & 16) != 0;
-    const float send = up ? x[i] : x[i + 32];
-    const float keep = up ? x[i + 32] : x[i];
+    const float send = up ? x[i] : x[i + 16];
+    const float keep = up ? x[i + 16] : x[i];
     const float got = __shfl_xor_sync(0xffffffffu, send, 16);
     v[i] = MAX ? fmaxf(keep, got) : keep + got;
   }
 #pragma unroll
   for (int lvl = 1; lvl < 5; ++lvl) {
-    const int half = 32 >> lvl, o = 16 >> lvl;
+    const int half = 16 >> lvl, o = 16 >> lvl;
     const bool up = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < half; ++i) {
@@ -97,8 +97,7 @@ __device__ __forceinline__ void mla_reduce64(const float (&x)[64], int lane, flo
       v[i] = MAX ? fmaxf(keep, got) : keep + got;
     }
   }
-  r0 = v[0];
-  r1 = v[1];
+  return v[0];
 }
 
 // S^T (+)= K.Q^T: A = stage (64-row atoms, rows 64..127 of the M=128 product fall in the
@@ -185,8 +184,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
   uint8_t* sQ = smem + Ly.q_off;
   int32_t* sIdx = reinterpret_cast<int32_t*>(smem + Ly.idx_off);
   float* m_run = reinterpret_cast<float*>(smem + Ly.misc_off);
-  float* thr = m_run + 64;       // m_run + 8: beyond it a score moves the running maximum
-  float* alpha = thr + 64;
+  float* alpha = m_run + 64;
   float* red = alpha + 64;       // [2 softmax warps][64]
   int32_t* flagw = reinterpret_cast<int32_t*>(red + 128);   // [2 chunk parities][2 softmax warps]
   int32_t* flag = flagw + 4;                                // [2] chunk needs an O/l rescale
@@ -374,7 +372,6 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
     const int q = warp & 3;                       // TMEM lane quarter
     const int lanerow = q * 32 + lane;            // key of S (q < 2), dv of O
     const uint32_t lane_addr = tmem_lane_base(warp);
-    const int hA = mla_head(lane);                // heads this lane reduces: hA, hA + 1
     uint32_t n = 0, qi = 0, uq = 0, kslow = 0, kcorr = 0;
     for (long long it = blockIdx.x; it < items; it += gridDim.x, ++qi) {
       const long long t = it / nhb;
@@ -398,22 +395,25 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
       const int nchunks = (nv + kMK - 1) / kMK;
       for (int c = 0; c < nchunks; ++c, ++n) {
         const int sb = n & 1;
-        float s[64];
+        const bool kvalid = c * kMK + lanerow < nv;
+        const uint32_t sbuf = tbase + sb * kMH + lane_addr;
+        // Scores stay in TMEM until P is out: each pass re-reads 16 heads at a time, so few
+        // registers are live (spills would queue behind the producers' copies).
         if (q < 2) {
           mbar_wait(&s_full[sb], (n >> 1) & 1, abort_flag, a.err);
           tc_fence_after();
-          tmem_ld32(tbase + sb * kMH + lane_addr, *reinterpret_cast<float(*)[32]>(&s[0]));
-          tmem_ld32(tbase + sb * kMH + 32 + lane_addr, *reinterpret_cast<float(*)[32]>(&s[32]));
-          tmem_ld_wait_regs(s);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_empty[sb]);
-          const bool kvalid = c * kMK + lanerow < nv;
           bool ex = c == 0;
+          if (!ex) {
 #pragma unroll
-          for (int h = 0; h < 64; ++h) {
-            s[h] = kvalid ? s[h] * a.scale_log2 : -INFINITY;
-            ex = ex || s[h] > thr[h];
+            for (int qq = 0; qq < 4; ++qq) {
+              float v[16], mr[16];
+              tmem_ld16(sbuf + qq * 16, v);
+              tmem_ld16(tbase + kMCol + qq * 16 + lane_addr, mr);
+              tmem_ld_wait_regs(v);
+              tmem_ld_wait_regs(mr);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) ex = ex || (kvalid && v[i] * a.scale_log2 > mr[i] + kRescaleLog2);
+            }
           }
           ex = __any_sync(0xffffffffu, ex);
           if (lane == 0) flagw[sb * 2 + q] = ex ? 1 : 0;
@@ -430,10 +430,15 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
         if (slow) {
           // reduce the head maxima over the 64 keys; move those that grew past the bound
           if (q < 2) {
-            float r0, r1;
-            mla_reduce64<true>(s, lane, r0, r1);
-            red[q * 64 + hA] = r0;
-            red[q * 64 + hA + 1] = r1;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              float v[32];
+              tmem_ld32(sbuf + half * 32, v);
+              tmem_ld_wait_regs(v);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = kvalid ? v[i] * a.scale_log2 : -INFINITY;
+              red[q * 64 + half * 32 + lane] = mla_reduce32<true>(v, lane);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(red2_bar);
           }
@@ -442,20 +447,19 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
             bool need = false;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int h = hA + e;
+              const int h = lane + 32 * e;
               const float cm = fmaxf(red[h], red[64 + h]);
               float mn = cm, al = 1.f;
               if (c > 0) {
                 const float mo = m_run[h];
                 if (cm > mo + kRescaleLog2) {
-                  al = exp2f(mo - cm);
+                  al = ex2_approx(mo - cm);
                   need = true;
                 } else {
                   mn = mo;
                 }
               }
               m_run[h] = mn;
-              thr[h] = mn + kRescaleLog2;
               alpha[h] = al;
             }
             need = __any_sync(0xffffffffu, need);
@@ -466,44 +470,67 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
             mbar_wait(stat_bar, kslow & 1, abort_flag, a.err);
           }
           ++kslow;
+          if (q < 2) {
+            // every softmax lane keeps its own copy of the maxima in TMEM
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              float mr[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) mr[i] = m_run[half * 32 + i];
+              tmem_st32(tbase + kMCol + half * 32 + lane_addr, mr);
+              tmem_st_wait();
+            }
+          }
         } else if (q == 0 && lane == 0) {
           flag[sb] = 0;
         }
         if (q < 2) {
-          // P key-major over the last key atom of the stage (S of this chunk is complete):
-          // row `lanerow`, 16-byte chunk j = heads 8j..8j+7 at position j ^ (row & 7)
-#pragma unroll
-          for (int h = 0; h < 64; ++h) s[h] = exp2f(s[h] - m_run[h]);
-          // this key's FP32 row sums: l <- l * alpha (when the maxima moved) + p
+          // p = 2^(s - m) per head; this key's FP32 row sums l <- l * alpha (when the maxima
+          // moved) + p; P key-major over the last key atom of the stage (S of this chunk is
+          // complete): row `lanerow`, 16-byte chunk j = heads 8j..8j+7 at position j ^ (row & 7)
           const bool resc = slow && flag[sb] != 0;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float lp[32];
-            const uint32_t ta = tbase + kLCol + half * 32 + lane_addr;
-            if (c > 0) {
-              tmem_ld32(ta, lp);
-              tmem_ld_wait_regs(lp);
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float old = c > 0 ? (resc ? lp[i] * alpha[half * 32 + i] : lp[i]) : 0.f;
-              lp[i] = old + s[half * 32 + i];
-            }
-            tmem_st32(ta, lp);
-            tmem_st_wait();
-          }
           uint8_t* prow = smem + (n & 1) * Ly.stage_bytes + (katoms - 1) * kAtom + lanerow * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint32_t pk[4];
+          for (int qq = 0; qq < 4; ++qq) {
+            float v[16], lp[16], mr[16];
+            tmem_ld16(sbuf + qq * 16, v);
+            tmem_ld16(tbase + kMCol + qq * 16 + lane_addr, mr);
+            const uint32_t ta = tbase + kLCol + qq * 16 + lane_addr;
+            if (c > 0) tmem_ld16(ta, lp);
+            tmem_ld_wait_regs(v);
+            tmem_ld_wait_regs(mr);
+            if (c > 0) tmem_ld_wait_regs(lp);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int h = 8 * j + 2 * e;
-              const __nv_bfloat162 two = __floats2bfloat162_rn(s[h], s[h + 1]);
-              pk[e] = *reinterpret_cast<const uint32_t*>(&two);
+            for (int i = 0; i < 16; ++i) v[i] = kvalid ? ex2_approx(v[i] * a.scale_log2 - mr[i]) : 0.f;
+            // explicit (warp-uniform) branches keep the rare rescale factor loads off the
+            // common path
+            if (c == 0) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) lp[i] = v[i];
+            } else if (!resc) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) lp[i] += v[i];
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) lp[i] = fmaf(lp[i], alpha[qq * 16 + i], v[i]);
             }
-            *reinterpret_cast<uint4*>(prow + ((j ^ (lanerow & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            tmem_st16(ta, lp);
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 two = __floats2bfloat162_rn(v[8 * jj + 2 * e], v[8 * jj + 2 * e + 1]);
+                pk[e] = *reinterpret_cast<const uint32_t*>(&two);
+              }
+              const int j = qq * 2 + jj;
+              *reinterpret_cast<uint4*>(prow + ((j ^ (lanerow & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            tmem_st_wait();   // lp's registers are reused by the next pass
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[sb]);
           fence_proxy_async_smem();
           if (c > 0) mbar_wait(o_full, (n - 1) & 1, abort_flag, a.err);
           __syncwarp();
@@ -533,14 +560,13 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
       }
       // ---- epilogue: sum the per-key row sums over the 64 keys, then O^T / l -> out, lse ----
       if (q < 2) {
-        float lp[64];
-        tmem_ld32(tbase + kLCol + lane_addr, *reinterpret_cast<float(*)[32]>(&lp[0]));
-        tmem_ld32(tbase + kLCol + 32 + lane_addr, *reinterpret_cast<float(*)[32]>(&lp[32]));
-        tmem_ld_wait_regs(lp);
-        float r0, r1;
-        mla_reduce64<false>(lp, lane, r0, r1);
-        red[q * 64 + hA] = r0;
-        red[q * 64 + hA + 1] = r1;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float lp[32];
+          tmem_ld32(tbase + kLCol + half * 32 + lane_addr, lp);
+          tmem_ld_wait_regs(lp);
+          red[q * 64 + half * 32 + lane] = mla_reduce32<false>(lp, lane);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(fin_bar);
       }
