@@ -503,6 +503,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
         auto correct = [&](uint32_t mm) {
           const int ob = mm & 1;
           mbar_wait(&B.o_full[ob], (mm >> 1) & 1, abort_flag, a.err);
+          __syncwarp();   // converge after the polling wait: tcgen05.ld is warp-aligned
           tc_fence_after();
 #pragma unroll
           for (int blk = 0; blk < DVB; ++blk)
@@ -520,6 +521,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
         for (int c = 0; c < nchunks; ++c, ++n) {
           const int sb = n & 1;
           mbar_wait(&B.s_full[sb], (n >> 1) & 1, abort_flag, a.err);
+          __syncwarp();
           tc_fence_after();
           float s[NH];
           tmem_ld_nh<NH>(tbase + sb * kNH + lane_addr, s);

@@ -312,7 +312,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const uint32_t lane_addr = tmem_lane_base(warp);
     for (int j = 0; j < nbt; ++j) {
       const int buf = j & 1;
-      if (!mbar_wait(&tfull[buf], (j >> 1) & 1, abort_flag, a.err)) break;
+      // one decision per warp, taken after every lane's wait: tcgen05.ld is warp-aligned
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], (j >> 1) & 1, abort_flag, a.err))) break;
       tc_fence_after();
       if (active) {
         const int blk = rot_tile(j, jrot, nbt) * kScoreM + quarter * 32 + lane;

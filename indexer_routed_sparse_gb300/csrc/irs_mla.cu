@@ -401,19 +401,28 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
         // registers are live (spills would queue behind the producers' copies).
         if (q < 2) {
           mbar_wait(&s_full[sb], (n >> 1) & 1, abort_flag, a.err);
+          __syncwarp();   // converge after the polling wait: tcgen05.ld/st are warp-aligned
           tc_fence_after();
           bool ex = c == 0;
-          if (!ex) {
+          if (!ex) {   // warp-uniform: tcgen05.ld is a .sync.aligned (whole-warp) instruction
+            // largest margin of this key's scores over the running maxima
+            float d = -INFINITY;
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-              float v[16], mr[16];
-              tmem_ld16(sbuf + qq * 16, v);
-              tmem_ld16(tbase + kMCol + qq * 16 + lane_addr, mr);
+            for (int half = 0; half < 2; ++half) {
+              float v[16], w[16], mr[16], mw[16];
+              tmem_ld16(sbuf + half * 32, v);
+              tmem_ld16(sbuf + half * 32 + 16, w);
+              tmem_ld16(tbase + kMCol + half * 32 + lane_addr, mr);
+              tmem_ld16(tbase + kMCol + half * 32 + 16 + lane_addr, mw);
               tmem_ld_wait_regs(v);
+              tmem_ld_wait_regs(w);
               tmem_ld_wait_regs(mr);
+              tmem_ld_wait_regs(mw);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) ex = ex || (kvalid && v[i] * a.scale_log2 > mr[i] + kRescaleLog2);
+              for (int i = 0; i < 16; ++i)
+                d = fmaxf(d, fmaxf(fmaf(v[i], a.scale_log2, -mr[i]), fmaf(w[i], a.scale_log2, -mw[i])));
             }
+            ex = kvalid && d > kRescaleLog2;
           }
           ex = __any_sync(0xffffffffu, ex);
           if (lane == 0) flagw[sb * 2 + q] = ex ? 1 : 0;
@@ -426,6 +435,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
         if (q >= 2 && c > 0) mbar_wait(o_full, (n - 1) & 1, abort_flag, a.err);
         if (lane == 0) mbar_arrive(red_bar);
         mbar_wait(red_bar, n & 1, abort_flag, a.err);
+        __syncwarp();
         const bool slow = (flagw[sb * 2] | flagw[sb * 2 + 1]) != 0;
         if (slow) {
           // reduce the head maxima over the 64 keys; move those that grew past the bound
@@ -469,6 +479,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
           } else {
             mbar_wait(stat_bar, kslow & 1, abort_flag, a.err);
           }
+          __syncwarp();
           ++kslow;
           if (q < 2) {
             // every softmax lane keeps its own copy of the maxima in TMEM
@@ -537,7 +548,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
           if (lane == 0) mbar_arrive(&p_full[sb]);
         }
         if (slow && flag[sb]) {
-          // O^T and l^T hold chunks 0..c-1 at the old maxima (all complete: waited above)
+          // O^T holds chunks 0..c-1 at the old maxima (all complete: waited above)
+          __syncwarp();
           tc_fence_after();
           for (int blk = 0; blk < ndvb; ++blk)
             for (int half = 0; half < 2; ++half) {
@@ -573,6 +585,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
       mbar_wait(fin_bar, uq & 1, abort_flag, a.err);
       ++uq;
       mbar_wait(o_full, (n - 1) & 1, abort_flag, a.err);
+      __syncwarp();
       tc_fence_after();
       if (a.lse != nullptr && q == 0) {
 #pragma unroll
