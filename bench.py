@@ -221,7 +221,7 @@ def run_gpu(args) -> dict | None:
 
         dist.init_process_group("nccl", device_id=dev)
     irs.lib()
-    wl = irs_synth.make(args.workload)
+    wl = irs_synth.make(args.workload, small=args.small)
     peaks = load_peaks()
 
     host = irs_synth.as_torch(wl, device="cpu", pin=True)
@@ -339,8 +339,11 @@ def run_gpu(args) -> dict | None:
     else:
         roof = {"bound": "tensor", "achieved": round(attn_tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(attn_tflops / peaks["bf16_tflops"], 4)}
-    roof.update({"traffic": profile_traffic(f"attn_fwd_{wl.name}.md", "indexer_routed_sparse_gb300/csrc/irs_attn.cu"),
-                 "kernel": "attn_fwd_kernel", "peak_source": peaks["source"]})
+    # the latent workload runs on the latent-attention kernel, the others on the GQA kernel
+    kname, ksrc = (("mla_fwd_kernel", "irs_mla.cu") if wl.latent else ("attn_fwd_kernel", "irs_attn.cu"))
+    kprof = f"{kname.replace('_kernel', '')}_{wl.name}{'_small' if args.small else ''}.md"
+    roof.update({"traffic": profile_traffic(kprof, f"indexer_routed_sparse_gb300/csrc/{ksrc}"),
+                 "kernel": kname, "peak_source": peaks["source"]})
     res = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -375,7 +378,7 @@ def run_gpu(args) -> dict | None:
                           "algorithmic_bytes": cnt["idx_bytes"], "flops": cnt["idx_flops"],
                           "includes_window_composition": bool(wl.window)}
     if not args.no_cpu_baseline and world == 1 and args.workload == WORKLOAD:
-        res["cpu_baseline"] = cpu_baseline(wl, cnt, budget_s=args.cpu_seconds)
+        res["cpu_baseline"] = cpu_baseline(wl, cnt, budget_s=args.cpu_seconds, small=args.small)
     if world > 1:
         import torch.distributed as dist
 
@@ -389,9 +392,9 @@ def run_gpu(args) -> dict | None:
 _WL = None
 
 
-def _worker_init():
+def _worker_init(name: str = WORKLOAD, small: bool = False):
     global _WL
-    _WL = irs_synth.make(WORKLOAD)
+    _WL = irs_synth.make(name, small=small)
 
 
 def _oracle_rows(rows) -> int:
@@ -401,9 +404,16 @@ def _oracle_rows(rows) -> int:
     wl = _WL
     a = wl.arrays
     rows = np.asarray(rows, np.int64)
+    if wl.latent:   # routes are given; attention over the latent rows only
+        O.latent_attention(a["q"], a["kv"], a["route"], wl.scale, Dv=wl.Dv, rows=rows)
+        return int(np.count_nonzero(a["route"][rows] >= 0))
     r = O.index_routes(a["qI"], a["kI"], a["w"], wl.cu_seqlens, wl.c, wl.budget, rows=rows)
-    full = np.full((wl.T, wl.route_width), -1, np.int32)
+    full = np.full((wl.T, r.shape[1]), -1, np.int32)
     full[rows] = r
+    if wl.window:
+        r = O.compose_window(full, wl.cu_seqlens, wl.T, wl.window, rows=rows)
+        full = np.full((wl.T, r.shape[1]), -1, np.int32)
+        full[rows] = r
     O.attention(a["q"], a["k"], a["v"], full, wl.scale, rows=rows)
     return int(np.count_nonzero(r >= 0))
 
@@ -419,14 +429,14 @@ def oracle_sample(n_rows: int, cores: int, pool) -> tuple[float, int, float]:
     return dt, pairs, 2.0 * (wl.Dqk + wl.Dv) * wl.Hq * pairs
 
 
-def make_pool(cores: int):
+def make_pool(cores: int, name: str = WORKLOAD, small: bool = False):
     import multiprocessing as mp
 
     os.environ.setdefault("OMP_NUM_THREADS", "1")
     os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
     os.environ.setdefault("MKL_NUM_THREADS", "1")
     ctx = mp.get_context("spawn")
-    pool = ctx.Pool(cores, initializer=_worker_init)
+    pool = ctx.Pool(cores, initializer=_worker_init, initargs=(name, small))
     pool.map(_worker_init_probe, range(cores))   # workers are up and have built the workload
     return pool
 
@@ -435,11 +445,11 @@ def _worker_init_probe(_):
     return 0
 
 
-def cpu_baseline(wl, cnt, budget_s: float = 15.0) -> dict:
+def cpu_baseline(wl, cnt, budget_s: float = 15.0, small: bool = False) -> dict:
     global _WL
     _WL = wl
     cores = os.cpu_count() or 1
-    pool = make_pool(cores)
+    pool = make_pool(cores, wl.name, small)
     try:
         dt1, _, _ = oracle_sample(cores, cores, pool)               # calibration: one row per core
         n = int(max(cores, min(wl.T, cores * max(1, int(budget_s / max(dt1, 1e-3))))))
@@ -447,7 +457,8 @@ def cpu_baseline(wl, cnt, budget_s: float = 15.0) -> dict:
     finally:
         pool.terminate()
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} of {wl.T} query rows spread evenly (indexer + attention, all {wl.Hq} heads), "
+            "sample": f"{n} of {wl.T} query rows spread evenly ({'attention' if wl.latent else 'indexer + attention'}, "
+                      f"all {wl.Hq} heads), "
                       f"{dt:.1f} s wall on {cores} single-threaded worker processes",
             "seconds": round(dt, 3), "rows": n}
 
@@ -495,6 +506,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("irs", "reference"), default="irs")
     ap.add_argument("--workload", choices=irs_synth.WORKLOADS, default=WORKLOAD,
                     help="workload of the step (the headline line uses the mid workload)")
+    ap.add_argument("--small", action="store_true",
+                    help="the workload's reduced-size variant (test sizes; for profiler captures, not a bench line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=150.0)
