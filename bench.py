@@ -451,6 +451,7 @@ def cpu_baseline(wl, cnt, budget_s: float = 15.0, small: bool = False) -> dict:
     cores = os.cpu_count() or 1
     pool = make_pool(cores, wl.name, small)
     try:
+        oracle_sample(cores, cores, pool)                           # first calls per worker run slow
         dt1, _, _ = oracle_sample(cores, cores, pool)               # calibration: one row per core
         n = int(max(cores, min(wl.T, cores * max(1, int(budget_s / max(dt1, 1e-3))))))
         dt, pairs, flops = oracle_sample(n, cores, pool)
