@@ -43,7 +43,7 @@ constexpr int kMaxDvBlocks = 4;
 
 struct AttnLayout {
   uint32_t k_bytes, v_bytes, stage_bytes, idx_words;
-  uint32_t q_off, p_off, idx_off, nv_off, red_off, fin_off, bar_off, total;
+  uint32_t q_off, p_off, idx_off, nv_off, run_off, red_off, fin_off, bar_off, total;
 };
 
 __host__ __device__ inline AttnLayout attn_layout(int Dqk, int Dv, int W, int stages, int v_alias) {
@@ -68,6 +68,8 @@ __host__ __device__ inline AttnLayout attn_layout(int Dqk, int Dv, int W, int st
   off += 2 * 4 * kNH * 4;
   L.bar_off = off;
   off += 40 * 8 + 16;
+  L.run_off = off;
+  off += L.idx_words / 64 * 4;   // per 64-slot group: 1 = 64 consecutive token IDs
   L.total = off + 1024;   // alignment slack
   return L;
 }
@@ -255,6 +257,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
   int32_t* sIdx = reinterpret_cast<int32_t*>(smem + Ly.idx_off);  // [idx_words] (producer only)
   int32_t* sNv = reinterpret_cast<int32_t*>(smem + Ly.nv_off);    // [2]
   int32_t* sCnt = sNv + 4;                                        // [PW] producer warp counts
+  int32_t* sRun = reinterpret_cast<int32_t*>(smem + Ly.run_off);  // [idx_words / 64]
   float* sRed = reinterpret_cast<float*>(smem + Ly.red_off);      // [2][4][16]
   float* sFin = reinterpret_cast<float*>(smem + Ly.fin_off);      // [2][4][16]
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Ly.bar_off);
@@ -292,6 +295,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
     fence_proxy_async_smem();
   }
   if (tid == 0) {
+    // kv_full: one cp.async arrival per producer thread (TMA tiles add transaction bytes)
     for (int s = 0; s < ST; ++s) { mbar_init(&B.kv_full[s], kProducerThreads); mbar_init(&B.kv_empty[s], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.q_full[i], kProducerThreads);
@@ -362,6 +366,19 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
       if (ptid == 0) mbar_arrive(&B.idx_full[b]);
       const int nv = run;
       if (nv == 0) continue;
+      // 64-slot groups holding 64 consecutive token IDs (e.g. a sliding window, or whole
+      // 64-token blocks) are loaded as one TMA tile per 64-dim atom instead of 16-byte copies
+      // (bit g of runmask; the same for every KV head and head block of the row)
+      uint64_t runmask = 0;
+      if (a.tile_runs) {
+        const int ngrp = nv >> 6;
+        for (int gi = ptid; gi < ngrp; gi += kProducerThreads) sRun[gi] = 1;
+        named_bar_sync(1, kProducerThreads);
+        for (int i = ptid; i < (ngrp << 6); i += kProducerThreads)
+          if ((i & 63) != 0 && sIdx[i] != sIdx[i - 1] + 1) sRun[i >> 6] = 0;
+        named_bar_sync(1, kProducerThreads);
+        for (int gi = 0; gi < ngrp; ++gi) runmask |= (uint64_t)(sRun[gi] != 0) << gi;
+      }
       const int nchunks = (nv + kChunk - 1) / kChunk;
       for (int sub = 0; sub < n_sub && mine; ++sub, ++u) {
         const int g = sub / a.nhb, hb = sub - g * a.nhb;
@@ -383,15 +400,56 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           const int rows = min(kChunk, nv - c * kChunk);
           const int32_t* ids = sIdx + c * kChunk;
           uint8_t* stage = smem + (uint32_t)st * Ly.stage_bytes;
-          if (a.v_alias) {
-            gather_rows<kProducerThreads>(smem_u32(stage), kbase, a.k_st, 0, nullptr, 0, ids, rows, qc, ptid);
-          } else if (a.Dv == a.Dqk) {
-            gather_rows<kProducerThreads>(smem_u32(stage), kbase, a.k_st, smem_u32(stage + Ly.k_bytes), vbase, a.v_st,
-                                          ids, rows, qc, ptid);
+          // halves of the chunk that are runs of 64 consecutive rows: TMA tiles
+          const bool run0 = ((runmask >> (2 * c)) & 1u) != 0;
+          const bool run1 = rows == kChunk && ((runmask >> (2 * c + 1)) & 1u) != 0;
+          if (!run0 && !run1) {
+            if (a.v_alias) {
+              gather_rows<kProducerThreads>(smem_u32(stage), kbase, a.k_st, 0, nullptr, 0, ids, rows, qc, ptid);
+            } else if (a.Dv == a.Dqk) {
+              gather_rows<kProducerThreads>(smem_u32(stage), kbase, a.k_st, smem_u32(stage + Ly.k_bytes), vbase,
+                                            a.v_st, ids, rows, qc, ptid);
+            } else {
+              gather_rows<kProducerThreads>(smem_u32(stage), kbase, a.k_st, 0, nullptr, 0, ids, rows, qc, ptid);
+              gather_rows<kProducerThreads>(smem_u32(stage + Ly.k_bytes), vbase, a.v_st, 0, nullptr, 0, ids, rows,
+                                            a.Dv >> 3, ptid);
+            }
           } else {
-            gather_rows<kProducerThreads>(smem_u32(stage), kbase, a.k_st, 0, nullptr, 0, ids, rows, qc, ptid);
-            gather_rows<kProducerThreads>(smem_u32(stage + Ly.k_bytes), vbase, a.v_st, 0, nullptr, 0, ids, rows,
-                                          a.Dv >> 3, ptid);
+            if (ptid == 0) {
+              // the bytes are announced before the tiles are issued and before this thread's
+              // own arrival, so the phase cannot complete without them
+              const uint32_t half_bytes = 64u * 128u * (uint32_t)(katoms + (a.v_alias ? 0 : a.Dv >> 6));
+              mbar_expect_tx(&B.kv_full[st], ((run0 ? 1u : 0u) + (run1 ? 1u : 0u)) * half_bytes);
+#pragma unroll 1
+              for (int h = 0; h < 2; ++h) {
+                if (!(h == 0 ? run0 : run1)) continue;
+                const int y = ids[64 * h];
+                for (int at = 0; at < katoms; ++at)
+                  tma_load_2d(stage + at * (kChunk * 128) + h * 8192, &maps.k[g], at * 64, y, &B.kv_full[st]);
+                if (!a.v_alias)
+                  for (int at = 0; at < (a.Dv >> 6); ++at)
+                    tma_load_2d(stage + Ly.k_bytes + at * (kChunk * 128) + h * 8192, &maps.v[g], at * 64, y,
+                                &B.kv_full[st]);
+              }
+            }
+            // the half that is not a run, by 16-byte copies
+            const int r_lo = run0 ? 64 : 0, gr = (run1 ? 64 : rows) - r_lo;
+            if (gr > 0) {
+              const uint32_t roff = (uint32_t)r_lo * 128u;   // row offset inside every 128-row atom
+              const int32_t* gids = ids + r_lo;
+              if (a.v_alias) {
+                gather_rows<kProducerThreads>(smem_u32(stage) + roff, kbase, a.k_st, 0, nullptr, 0, gids, gr, qc,
+                                              ptid);
+              } else if (a.Dv == a.Dqk) {
+                gather_rows<kProducerThreads>(smem_u32(stage) + roff, kbase, a.k_st,
+                                              smem_u32(stage + Ly.k_bytes) + roff, vbase, a.v_st, gids, gr, qc, ptid);
+              } else {
+                gather_rows<kProducerThreads>(smem_u32(stage) + roff, kbase, a.k_st, 0, nullptr, 0, gids, gr, qc,
+                                              ptid);
+                gather_rows<kProducerThreads>(smem_u32(stage + Ly.k_bytes) + roff, vbase, a.v_st, 0, nullptr, 0, gids,
+                                              gr, a.Dv >> 3, ptid);
+              }
+            }
           }
           cp_async_mbar_arrive_noinc(&B.kv_full[st]);
         }

@@ -87,18 +87,19 @@ irs_status make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
   return IRS_OK;
 }
 
-// 2-D bf16 gather map: rows of `inner` elements `row_stride` elements apart, box {64, 1}.
-irs_status make_gather_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride) {
+// 2-D bf16 row-tile map: rows of `inner` elements `row_stride` elements apart, box {64, 64}
+// (one SW128 atom of 64 consecutive rows).
+irs_status make_row_tile_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride) {
   auto fn = encode_fn();
   if (fn == nullptr) return fail(IRS_ERR_RUNTIME, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {row_stride * 2};
-  cuuint32_t box[2] = {64, 1};
+  cuuint32_t box[2] = {64, 64};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(IRS_ERR_RUNTIME, "cuTensorMapEncodeTiled (gather) failed (%d)", (int)r);
+  if (r != CUDA_SUCCESS) return fail(IRS_ERR_RUNTIME, "cuTensorMapEncodeTiled (row tiles) failed (%d)", (int)r);
   return IRS_OK;
 }
 
@@ -285,12 +286,15 @@ irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_
     const int ng = Hkv - g0 < irs::kMaxKvMaps ? Hkv - g0 : irs::kMaxKvMaps;
     irs::AttnMaps maps;
     memset(&maps, 0, sizeof(maps));
-    for (int i = 0; i < ng; ++i) {
+    // runs of 64 consecutive routed rows load as TMA tiles (needs at least 64 key rows)
+    a.tile_runs = Tk >= 64 ? 1 : 0;
+    for (int i = 0; i < ng && a.tile_runs; ++i) {
       const __nv_bfloat16* kb = a.k + (int64_t)(g0 + i) * k_stride_h;
-      if ((s = make_gather_map(&maps.k[i], kb, (uint64_t)Dqk, (uint64_t)Tk, (uint64_t)k_stride_t)) != IRS_OK) return s;
+      if ((s = make_row_tile_map(&maps.k[i], kb, (uint64_t)Dqk, (uint64_t)Tk, (uint64_t)k_stride_t)) != IRS_OK)
+        return s;
       if (!a.v_alias) {
         const __nv_bfloat16* vb = a.v + (int64_t)(g0 + i) * v_stride_h;
-        if ((s = make_gather_map(&maps.v[i], vb, (uint64_t)Dv, (uint64_t)Tk, (uint64_t)v_stride_t)) != IRS_OK)
+        if ((s = make_row_tile_map(&maps.v[i], vb, (uint64_t)Dv, (uint64_t)Tk, (uint64_t)v_stride_t)) != IRS_OK)
           return s;
       }
     }

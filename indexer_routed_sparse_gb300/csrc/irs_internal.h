@@ -42,7 +42,7 @@ cudaError_t launch_compose_window(const int32_t* route, int W, const int32_t* cu
 constexpr int kMaxKvMaps = 8;   // KV heads handled by one launch (one gather map per head)
 
 struct AttnMaps {
-  CUtensorMap k[kMaxKvMaps];    // [Tk rows x Dqk] of KV head g0+i, box {64, 1}, SW128
+  CUtensorMap k[kMaxKvMaps];    // [Tk rows x Dqk] of KV head g0+i, box {64, 64}, SW128
   CUtensorMap v[kMaxKvMaps];    // [Tk rows x Dv]  (unused when v aliases k)
 };
 
@@ -62,6 +62,7 @@ struct AttnArgs {
   int nhb;        // head blocks per KV head
   int g0, ng;     // KV heads [g0, g0+ng) handled by this launch
   int v_alias;    // 1: values are the first Dv dims of the gathered key rows
+  int tile_runs;  // 1: the maps are valid; 64 consecutive routed rows load as one TMA tile
   int stages;
   float scale_log2;  // scale * log2(e)
 };

@@ -119,6 +119,48 @@ def test_latent_kernel_shapes(irs, Hq, Dqk, Dv, W, holes, boost):
     assert torch.all(out[5] == 0) and torch.all(torch.isneginf(lse[5]))
 
 
+@pytest.mark.parametrize("Hq,Hkv,Dqk,Dv,alias", [
+    (8, 2, 192, 128, False),   # separate value rows, Dqk != Dv
+    (8, 2, 128, 128, False),   # K and V gathered in one pass where copied
+    (4, 1, 256, 128, True),    # values are the first Dv dims of the key rows
+])
+def test_consecutive_runs_and_copies(irs, Hq, Hkv, Dqk, Dv, alias):
+    """Routes mixing 64-key runs of consecutive tokens (loaded as tiles) with scattered keys
+    (16-byte copies): each 128-key chunk has both halves runs, one or the other, or none,
+    plus a partial last chunk and -1 holes between runs."""
+    T, Tk = 40, 4096
+    wl = irs_synth.custom(Tk, Hq, Hkv, Dqk, Dv, 2, 64, 4, 8, doc_lens=[Tk], seed=Dqk + Hkv)
+    a = wl.arrays
+    rng = np.random.default_rng(Dqk)
+    W = 700
+    routes = np.full((T, W), -1, np.int32)
+    for t in range(T):
+        pieces = []
+        for half in range(10):
+            kind = (t + half) % 4
+            if kind == 3:
+                continue
+            if kind < 2:                                    # a run of 64 consecutive tokens
+                start = int(rng.integers(0, Tk - 64))
+                pieces.append(np.arange(start, start + 64))
+            else:                                           # 64 scattered tokens
+                pieces.append(rng.choice(Tk, 64, replace=False))
+        ids = np.concatenate(pieces + [rng.choice(Tk, t % 37, replace=False)])
+        _, first = np.unique(ids, return_index=True)        # distinct IDs, first occurrence order
+        ids = ids[np.sort(first)][:W - 20]
+        slots = np.arange(len(ids)) + np.minimum(np.arange(len(ids)) // 200, 20)   # a few holes
+        routes[t, slots] = ids.astype(np.int32)
+    q = a["q"][:T]
+    if alias:
+        kd = torch.from_numpy(a["k"]).view(torch.bfloat16).to(DEV)
+        out, lse = attend(irs, q, kd, kd[:, :, :Dv], routes, 1.0 / math.sqrt(Dqk))
+        ref_o, ref_l = O.attention(q, a["k"], a["k"][:, :, :Dv], routes, 1.0 / math.sqrt(Dqk))
+    else:
+        out, lse = attend(irs, q, a["k"], a["v"], routes, 1.0 / math.sqrt(Dqk))
+        ref_o, ref_l = O.attention(q, a["k"], a["v"], routes, 1.0 / math.sqrt(Dqk))
+    parity.check_attention(out, lse, ref_o, ref_l, np.arange(T))
+
+
 @pytest.mark.parametrize("Hq,Hkv,Dqk,Dv,W", [
     (4, 4, 64, 128, 1),        # G = 1, a single slot
     (32, 1, 128, 128, 300),    # G = 32: two head blocks per KV head
