@@ -397,35 +397,68 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
         const int sb = n & 1;
         const bool kvalid = c * kMK + lanerow < nv;
         const uint32_t sbuf = tbase + sb * kMH + lane_addr;
-        // Scores stay in TMEM until P is out: each pass re-reads 16 heads at a time, so few
-        // registers are live (spills would queue behind the producers' copies).
+        uint8_t* prow = smem + (n & 1) * Ly.stage_bytes + (katoms - 1) * kAtom + lanerow * 128;
+        // p = 2^(s - m) for this key's 64 heads, 16 at a time from TMEM (scores and maxima
+        // stay there, so few registers are live; spills would queue behind the producers'
+        // copies). The FP32 row sums in TMEM are set (mode 0), accumulated (1), or rescaled
+        // and accumulated (2); P goes key-major over the last key atom of the stage (S of
+        // this chunk is complete): row `lanerow`, 16-byte chunk j = heads 8j..8j+7 at chunk
+        // position j ^ (row & 7). Returns the largest margin s - m over the heads.
+        auto p_pass = [&](int mode) -> float {
+          float dmax = -INFINITY;
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            float v[16], lp[16], mr[16];
+            tmem_ld16(sbuf + qq * 16, v);
+            tmem_ld16(tbase + kMCol + qq * 16 + lane_addr, mr);
+            const uint32_t ta = tbase + kLCol + qq * 16 + lane_addr;
+            if (mode != 0) tmem_ld16(ta, lp);
+            tmem_ld_wait_regs(v);
+            tmem_ld_wait_regs(mr);
+            if (mode != 0) tmem_ld_wait_regs(lp);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float x = fmaf(v[i], a.scale_log2, -mr[i]);
+              dmax = fmaxf(dmax, x);
+              v[i] = kvalid ? ex2_approx(x) : 0.f;
+            }
+            // explicit (warp-uniform) branches keep the rare rescale factor loads off the
+            // common path
+            if (mode == 0) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) lp[i] = v[i];
+            } else if (mode == 1) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) lp[i] += v[i];
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) lp[i] = fmaf(lp[i], alpha[qq * 16 + i], v[i]);
+            }
+            tmem_st16(ta, lp);
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 two = __floats2bfloat162_rn(v[8 * jj + 2 * e], v[8 * jj + 2 * e + 1]);
+                pk[e] = *reinterpret_cast<const uint32_t*>(&two);
+              }
+              const int j = qq * 2 + jj;
+              *reinterpret_cast<uint4*>(prow + ((j ^ (lanerow & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            tmem_st_wait();   // lp's registers are reused by the next pass
+          }
+          return kvalid ? dmax : -INFINITY;
+        };
         if (q < 2) {
           mbar_wait(&s_full[sb], (n >> 1) & 1, abort_flag, a.err);
           __syncwarp();   // converge after the polling wait: tcgen05.ld/st are warp-aligned
           tc_fence_after();
-          bool ex = c == 0;
-          if (!ex) {   // warp-uniform: tcgen05.ld is a .sync.aligned (whole-warp) instruction
-            // largest margin of this key's scores over the running maxima
-            float d = -INFINITY;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              float v[16], w[16], mr[16], mw[16];
-              tmem_ld16(sbuf + half * 32, v);
-              tmem_ld16(sbuf + half * 32 + 16, w);
-              tmem_ld16(tbase + kMCol + half * 32 + lane_addr, mr);
-              tmem_ld16(tbase + kMCol + half * 32 + 16 + lane_addr, mw);
-              tmem_ld_wait_regs(v);
-              tmem_ld_wait_regs(w);
-              tmem_ld_wait_regs(mr);
-              tmem_ld_wait_regs(mw);
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                d = fmaxf(d, fmaxf(fmaf(v[i], a.scale_log2, -mr[i]), fmaf(w[i], a.scale_log2, -mw[i])));
-            }
-            ex = kvalid && d > kRescaleLog2;
-          }
-          ex = __any_sync(0xffffffffu, ex);
-          if (lane == 0) flagw[sb * 2 + q] = ex ? 1 : 0;
+          // after the first chunk of a route, P and the row sums are computed at once with the
+          // current maxima; the vote below keeps them unless some score passed its bound
+          const bool ex = c == 0 || p_pass(1) > kRescaleLog2;   // c is warp-uniform
+          const bool any = __any_sync(0xffffffffu, ex);
+          if (lane == 0) flagw[sb * 2 + q] = any ? 1 : 0;
           __syncwarp();
         }
         // o_full completes once per chunk; a parity wait is only sound if every phase is
@@ -438,6 +471,24 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
         __syncwarp();
         const bool slow = (flagw[sb * 2] | flagw[sb * 2 + 1]) != 0;
         if (slow) {
+          if (q < 2 && c > 0) {
+            // take the speculative p (at the old maxima, still in TMEM) back out of the sums
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              float v[16], lp[16], mr[16];
+              const uint32_t ta = tbase + kLCol + qq * 16 + lane_addr;
+              tmem_ld16(sbuf + qq * 16, v);
+              tmem_ld16(tbase + kMCol + qq * 16 + lane_addr, mr);
+              tmem_ld16(ta, lp);
+              tmem_ld_wait_regs(v);
+              tmem_ld_wait_regs(mr);
+              tmem_ld_wait_regs(lp);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) lp[i] -= kvalid ? ex2_approx(fmaf(v[i], a.scale_log2, -mr[i])) : 0.f;
+              tmem_st16(ta, lp);
+              tmem_st_wait();
+            }
+          }
           // reduce the head maxima over the 64 keys; move those that grew past the bound
           if (q < 2) {
 #pragma unroll
@@ -491,54 +542,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
               tmem_st32(tbase + kMCol + half * 32 + lane_addr, mr);
               tmem_st_wait();
             }
+            (void)p_pass(c == 0 ? 0 : (flag[sb] != 0 ? 2 : 1));
           }
         } else if (q == 0 && lane == 0) {
           flag[sb] = 0;
         }
         if (q < 2) {
-          // p = 2^(s - m) per head; this key's FP32 row sums l <- l * alpha (when the maxima
-          // moved) + p; P key-major over the last key atom of the stage (S of this chunk is
-          // complete): row `lanerow`, 16-byte chunk j = heads 8j..8j+7 at position j ^ (row & 7)
-          const bool resc = slow && flag[sb] != 0;
-          uint8_t* prow = smem + (n & 1) * Ly.stage_bytes + (katoms - 1) * kAtom + lanerow * 128;
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            float v[16], lp[16], mr[16];
-            tmem_ld16(sbuf + qq * 16, v);
-            tmem_ld16(tbase + kMCol + qq * 16 + lane_addr, mr);
-            const uint32_t ta = tbase + kLCol + qq * 16 + lane_addr;
-            if (c > 0) tmem_ld16(ta, lp);
-            tmem_ld_wait_regs(v);
-            tmem_ld_wait_regs(mr);
-            if (c > 0) tmem_ld_wait_regs(lp);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = kvalid ? ex2_approx(v[i] * a.scale_log2 - mr[i]) : 0.f;
-            // explicit (warp-uniform) branches keep the rare rescale factor loads off the
-            // common path
-            if (c == 0) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) lp[i] = v[i];
-            } else if (!resc) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) lp[i] += v[i];
-            } else {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) lp[i] = fmaf(lp[i], alpha[qq * 16 + i], v[i]);
-            }
-            tmem_st16(ta, lp);
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-              uint32_t pk[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 two = __floats2bfloat162_rn(v[8 * jj + 2 * e], v[8 * jj + 2 * e + 1]);
-                pk[e] = *reinterpret_cast<const uint32_t*>(&two);
-              }
-              const int j = qq * 2 + jj;
-              *reinterpret_cast<uint4*>(prow + ((j ^ (lanerow & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-            tmem_st_wait();   // lp's registers are reused by the next pass
-          }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&s_empty[sb]);
