@@ -13,7 +13,11 @@
 //               gather the routed K/V rows with 16-byte cp.async into a ring of 128-key
 //               stages (SW128 layout); completion reaches the stage's mbarrier by
 //               cp.async-arrive. (Random 256-byte rows reach about 3x the L2 bandwidth
-//               this way than with TMA gather4.)
+//               this way than with TMA gather4.) When the key/value rows exceed half the
+//               L2 (variant RUNS), 64-slot groups of a route that hold 64 consecutive
+//               tokens (a sliding window, whole 64-token blocks) load instead as one TMA
+//               row tile per 64-dim atom, announced on the same barrier as transaction
+//               bytes: far more bytes in flight for DRAM latency than the copies.
 //   S warp      TMEM owner; issues S^T = K.Q^T (M=128 keys, N=16 heads, K=Dqk) as each
 //               stage lands.
 //   O warp      issues O^T = V^T.P^T (M=128 dv per block, N=16, K=128 keys; V read
@@ -242,7 +246,7 @@ struct AttnBars {
   uint64_t* fin;       // [2] row-sum exchange
 };
 
-template <int NH, int DVB, int PW>
+template <int NH, int DVB, int PW, bool RUNS>
 __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __grid_constant__ AttnMaps maps, AttnArgs a) {
   constexpr int kThreads = attn_threads(PW);
   constexpr int kProducerThreads = 32 * PW;
@@ -370,7 +374,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
       // 64-token blocks) are loaded as one TMA tile per 64-dim atom instead of 16-byte copies
       // (bit g of runmask; the same for every KV head and head block of the row)
       uint64_t runmask = 0;
-      if (a.tile_runs) {
+      if (RUNS) {
         const int ngrp = nv >> 6;
         for (int gi = ptid; gi < ngrp; gi += kProducerThreads) sRun[gi] = 1;
         named_bar_sync(1, kProducerThreads);
@@ -401,8 +405,8 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           const int32_t* ids = sIdx + c * kChunk;
           uint8_t* stage = smem + (uint32_t)st * Ly.stage_bytes;
           // halves of the chunk that are runs of 64 consecutive rows: TMA tiles
-          const bool run0 = ((runmask >> (2 * c)) & 1u) != 0;
-          const bool run1 = rows == kChunk && ((runmask >> (2 * c + 1)) & 1u) != 0;
+          const bool run0 = RUNS && ((runmask >> (2 * c)) & 1u) != 0;
+          const bool run1 = RUNS && rows == kChunk && ((runmask >> (2 * c + 1)) & 1u) != 0;
           if (!run0 && !run1) {
             if (a.v_alias) {
               gather_rows<kProducerThreads>(smem_u32(stage), kbase, a.k_st, 0, nullptr, 0, ids, rows, qc, ptid);
@@ -414,7 +418,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
               gather_rows<kProducerThreads>(smem_u32(stage + Ly.k_bytes), vbase, a.v_st, 0, nullptr, 0, ids, rows,
                                             a.Dv >> 3, ptid);
             }
-          } else {
+          } else if constexpr (RUNS) {
             if (ptid == 0) {
               // the bytes are announced before the tiles are issued and before this thread's
               // own arrival, so the phase cannot complete without them
@@ -684,7 +688,10 @@ constexpr int producer_warps() { return NH * DVB <= 8 ? 8 : (NH * DVB <= 32 ? 6 
 
 template <int NH, int DVB>
 static cudaError_t attn_attr(size_t smem) {
-  return cudaFuncSetAttribute(attn_fwd_kernel<NH, DVB, producer_warps<NH, DVB>()>,
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<NH, DVB, producer_warps<NH, DVB>(), false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attn_fwd_kernel<NH, DVB, producer_warps<NH, DVB>(), true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
@@ -697,10 +704,15 @@ cudaError_t configure_attn_kernel(size_t smem) {
   return e;
 }
 
+// The row-tile path is a separate instantiation: its code in the producer loop costs the
+// all-copy path a few percent even when no chunk takes it.
 template <int NH, int DVB>
 static void launch_variant(const AttnMaps& maps, const AttnArgs& b, const AttnPlan& p, cudaStream_t stream) {
   constexpr int PW = producer_warps<NH, DVB>();
-  attn_fwd_kernel<NH, DVB, PW><<<p.grid, attn_threads(PW), p.smem, stream>>>(maps, b);
+  if (b.tile_runs)
+    attn_fwd_kernel<NH, DVB, PW, true><<<p.grid, attn_threads(PW), p.smem, stream>>>(maps, b);
+  else
+    attn_fwd_kernel<NH, DVB, PW, false><<<p.grid, attn_threads(PW), p.smem, stream>>>(maps, b);
 }
 
 cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, const AttnPlan& p, cudaStream_t stream) {

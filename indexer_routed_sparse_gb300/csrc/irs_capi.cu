@@ -30,6 +30,7 @@ struct DeviceInfo {
   bool checked = false;
   bool ok = false;
   int num_sms = 0;
+  size_t l2_bytes = 0;
   size_t score_smem = 0, topk_smem = 0, attn_smem = 0, mla_smem = 0;   // largest values configured so far
 };
 constexpr int kMaxDevices = 64;
@@ -49,6 +50,9 @@ irs_status current_device(DeviceInfo** out) {
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int l2 = 0;
+    cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    d.l2_bytes = (size_t)(l2 > 0 ? l2 : 0);
     d.checked = true;
     d.ok = (major == 10 && minor == 3);
     d.num_sms = sms;
@@ -286,8 +290,11 @@ irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_
     const int ng = Hkv - g0 < irs::kMaxKvMaps ? Hkv - g0 : irs::kMaxKvMaps;
     irs::AttnMaps maps;
     memset(&maps, 0, sizeof(maps));
-    // runs of 64 consecutive routed rows load as TMA tiles (needs at least 64 key rows)
-    a.tile_runs = Tk >= 64 ? 1 : 0;
+    // Runs of 64 consecutive routed rows load as TMA row tiles when the key/value rows cannot
+    // stay L2-resident (more than half the L2): the tiles keep many more bytes in flight for
+    // DRAM latency than 16-byte copies. Rows that do stay in L2 are served faster by the copies.
+    const double kv_bytes = (double)Tk * Hkv * (Dqk + (a.v_alias ? 0 : Dv)) * 2.0;
+    a.tile_runs = (Tk >= 64 && kv_bytes > 0.5 * (double)dev->l2_bytes) ? 1 : 0;
     for (int i = 0; i < ng && a.tile_runs; ++i) {
       const __nv_bfloat16* kb = a.k + (int64_t)(g0 + i) * k_stride_h;
       if ((s = make_row_tile_map(&maps.k[i], kb, (uint64_t)Dqk, (uint64_t)Tk, (uint64_t)k_stride_t)) != IRS_OK)

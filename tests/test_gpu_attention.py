@@ -119,20 +119,21 @@ def test_latent_kernel_shapes(irs, Hq, Dqk, Dv, W, holes, boost):
     assert torch.all(out[5] == 0) and torch.all(torch.isneginf(lse[5]))
 
 
-@pytest.mark.parametrize("Hq,Hkv,Dqk,Dv,alias", [
-    (8, 2, 192, 128, False),   # separate value rows, Dqk != Dv
-    (8, 2, 128, 128, False),   # K and V gathered in one pass where copied
-    (4, 1, 256, 128, True),    # values are the first Dv dims of the key rows
+@pytest.mark.parametrize("Hq,Hkv,Dqk,Dv,alias,Tk", [
+    (8, 2, 192, 128, False, 98304),    # separate value rows, Dqk != Dv (126 MB of K/V)
+    (8, 2, 128, 128, False, 98304),    # K and V gathered in one pass where copied (100 MB)
+    (4, 1, 256, 128, True, 196608),    # values are the first Dv dims of the key rows (100 MB)
 ])
-def test_consecutive_runs_and_copies(irs, Hq, Hkv, Dqk, Dv, alias):
-    """Routes mixing 64-key runs of consecutive tokens (loaded as tiles) with scattered keys
-    (16-byte copies): each 128-key chunk has both halves runs, one or the other, or none,
-    plus a partial last chunk and -1 holes between runs."""
-    T, Tk = 40, 4096
-    wl = irs_synth.custom(Tk, Hq, Hkv, Dqk, Dv, 2, 64, 4, 8, doc_lens=[Tk], seed=Dqk + Hkv)
-    a = wl.arrays
-    rng = np.random.default_rng(Dqk)
-    W = 700
+def test_consecutive_runs_and_copies(irs, Hq, Hkv, Dqk, Dv, alias, Tk):
+    """Routes mixing 64-key runs of consecutive tokens with scattered keys: each 128-key
+    chunk has both halves runs, one or the other, or none, plus a partial last chunk and -1
+    holes between runs. The K/V sets exceed half the L2, which selects the attention
+    variant that loads runs as TMA row tiles (the others by 16-byte copies)."""
+    T, W = 40, 700
+    rng = np.random.default_rng(Dqk + Tk)
+    q = irs_synth.f32_to_bf16_bits(rng.standard_normal((T, Hq, Dqk), dtype=np.float32))
+    k = irs_synth.f32_to_bf16_bits(rng.standard_normal((Tk, Hkv, Dqk), dtype=np.float32))
+    v = None if alias else irs_synth.f32_to_bf16_bits(rng.standard_normal((Tk, Hkv, Dv), dtype=np.float32))
     routes = np.full((T, W), -1, np.int32)
     for t in range(T):
         pieces = []
@@ -150,14 +151,14 @@ def test_consecutive_runs_and_copies(irs, Hq, Hkv, Dqk, Dv, alias):
         ids = ids[np.sort(first)][:W - 20]
         slots = np.arange(len(ids)) + np.minimum(np.arange(len(ids)) // 200, 20)   # a few holes
         routes[t, slots] = ids.astype(np.int32)
-    q = a["q"][:T]
+    scale = 1.0 / math.sqrt(Dqk)
+    kd = torch.from_numpy(k).view(torch.bfloat16).to(DEV)
     if alias:
-        kd = torch.from_numpy(a["k"]).view(torch.bfloat16).to(DEV)
-        out, lse = attend(irs, q, kd, kd[:, :, :Dv], routes, 1.0 / math.sqrt(Dqk))
-        ref_o, ref_l = O.attention(q, a["k"], a["k"][:, :, :Dv], routes, 1.0 / math.sqrt(Dqk))
+        out, lse = attend(irs, q, kd, kd[:, :, :Dv], routes, scale)
+        ref_o, ref_l = O.attention(q, k, k[:, :, :Dv], routes, scale)
     else:
-        out, lse = attend(irs, q, a["k"], a["v"], routes, 1.0 / math.sqrt(Dqk))
-        ref_o, ref_l = O.attention(q, a["k"], a["v"], routes, 1.0 / math.sqrt(Dqk))
+        out, lse = attend(irs, q, kd, v, routes, scale)
+        ref_o, ref_l = O.attention(q, k, v, routes, scale)
     parity.check_attention(out, lse, ref_o, ref_l, np.arange(T))
 
 
