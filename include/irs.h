@@ -185,6 +185,12 @@ irs_status irs_compose_window_routes(const int32_t* route_ids, int W, const int3
  *        1 <= W <= 4096
  * scale > 0 (finite)
  * out   bf16 [T, Hq, Dv] contiguous;  lse  fp32 [T, Hq] contiguous (may be NULL)
+ *
+ * Kernels (results are the same definition either way): latent shapes (Hkv == 1, v the
+ * first Dv dims of k, Hq % 64 == 0, Dqk >= Dv + 64, W <= 2048) run a kernel that keeps
+ * 64 query heads' output in tensor memory; all other shapes run the GQA kernel, which
+ * loads runs of 64 consecutive routed rows as TMA tiles when the K/V rows exceed half the
+ * L2. Every on-device wait is bounded; one that gives up sets IRS_DEVERR_TIMEOUT.
  */
 irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k,
                                    int64_t k_stride_t, int64_t k_stride_h, const void* v, int64_t v_stride_t,
