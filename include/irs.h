@@ -198,6 +198,16 @@ irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_
                                    int Tk, int Hq, int Hkv, int Dqk, int Dv, int W, float scale, void* out,
                                    float* lse, int32_t* err_flag, irs_stream_t stream);
 
+/*
+ * Failure-detection self-test (no counterpart on the reference pages). Launches one
+ * bounded on-device wait on a barrier phase that nothing completes: after limit_ns
+ * (1e6 .. 2e9) the wait gives up, ORs IRS_DEVERR_TIMEOUT into *err_flag and the kernel
+ * returns, leaving the context usable. It is the same bounded wait every kernel of this
+ * library uses, so a caller can check on its own device that a stalled pipeline reports
+ * an error instead of hanging. err_flag: one device int32 (required).
+ */
+irs_status irs_check_bounded_wait(uint64_t limit_ns, int32_t* err_flag, irs_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

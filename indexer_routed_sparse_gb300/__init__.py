@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     DEVERR_ROUTE_ID,
     DEVERR_TIMEOUT,
     LIB_PATH,
+    check_bounded_wait,
     check_device_errors,
     compose_window_routes,
     device_error_flag,

@@ -40,6 +40,7 @@ _SIGNATURES = {
     "irs_compose_window_routes": (_I, [_P, _I, _P, _I, _I, _I, _P, _P, _P]),
     "irs_sparse_gqa_attn_fwd": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I, _I, _I, _I, _I, _I,
                                      _I, _F, _P, _P, _P, _P]),
+    "irs_check_bounded_wait": (_I, [ctypes.c_uint64, _P, _P]),
 }
 
 
@@ -262,3 +263,14 @@ def sparse_gqa_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, route
         _ptr(err), _stream(dev))
     _check(st, "sparse_gqa_attn_fwd")
     return out, lse
+
+
+def check_bounded_wait(limit_ms: float = 20.0, device=None, err: torch.Tensor | None = None) -> torch.Tensor:
+    """Run one on-device wait that nothing releases; it gives up after `limit_ms` and sets
+    DEVERR_TIMEOUT in the returned error word (asynchronous on the current stream)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = lib().irs_check_bounded_wait(int(limit_ms * 1e6), _ptr(err), _stream(dev))
+    _check(st, "check_bounded_wait")
+    return err

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "irs_internal.h"
+#include "irs_ptx.cuh"
 
 namespace {
 
@@ -390,4 +391,35 @@ extern "C" irs_status irs_sparse_index_score_topk_noalloc(const void* qI, const 
                                          Hi, Di, c, budget, route_ids, scores, ldS, ws, err_flag, tm_q, tm_k,
                                          reinterpret_cast<cudaStream_t>(stream)),
                        "launching the indexer (fixed scratch)");
+}
+
+// =====================================================================================
+// Failure-detection self-test: one bounded wait on an mbarrier phase that nothing
+// completes. The wait gives up after limit_ns, records IRS_DEVERR_TIMEOUT and the kernel
+// returns, so the context stays usable (no trap, no fault, no endless loop).
+// =====================================================================================
+namespace {
+
+__global__ void bounded_wait_probe_kernel(int32_t* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_word;
+  if (threadIdx.x != 0) return;
+  irs::mbar_init(&bar, 1);
+  abort_word = 0;
+  irs::fence_mbar_init();
+  volatile int* abort_flag = &abort_word;
+  (void)irs::mbar_wait(&bar, 0, abort_flag, err, limit_ns);   // nobody arrives: gives up
+}
+
+}  // namespace
+
+extern "C" irs_status irs_check_bounded_wait(uint64_t limit_ns, int32_t* err_flag, irs_stream_t stream) {
+  if (err_flag == nullptr) return fail(IRS_ERR_VALUE, "err_flag must be a device int32");
+  if (limit_ns < 1000000ull || limit_ns > 2000000000ull)
+    return fail(IRS_ERR_VALUE, "limit_ns must be in [1e6, 2e9] (got %llu)", (unsigned long long)limit_ns);
+  DeviceInfo* dev = nullptr;
+  irs_status s = current_device(&dev);
+  if (s != IRS_OK) return s;
+  bounded_wait_probe_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err_flag, limit_ns);
+  return launch_status(cudaGetLastError(), "launching the bounded-wait check");
 }
