@@ -1,4 +1,4 @@
-// Gathered sparse GQA / latent attention forward on sm_103a (tcgen05 + TMEM + TMA gather4).
+// Gathered sparse GQA attention forward on sm_103a (tcgen05 + TMEM; cp.async gathers, TMA row tiles).
 //
 // Semantics: QSA page (nemo_automodel.components.models.qwen3_8_flash_next.qsa,
 // `gathered_qsa_gqa_attention`): query t, head h attends the keys/values of its KV

@@ -286,7 +286,7 @@ irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_
       dev->attn_smem = p.smem;
     }
   }
-  // one launch per group of up to kMaxKvMaps KV heads (one gather map per head)
+  // one launch per group of up to kMaxKvMaps KV heads (one row-tile map per head and operand)
   for (int g0 = 0; g0 < Hkv; g0 += irs::kMaxKvMaps) {
     const int ng = Hkv - g0 < irs::kMaxKvMaps ? Hkv - g0 : irs::kMaxKvMaps;
     irs::AttnMaps maps;

@@ -39,7 +39,7 @@ cudaError_t launch_compose_window(const int32_t* route, int W, const int32_t* cu
                                   int32_t* out, int32_t* err, cudaStream_t stream);
 
 // Gathered sparse attention.
-constexpr int kMaxKvMaps = 8;   // KV heads handled by one launch (one gather map per head)
+constexpr int kMaxKvMaps = 8;   // KV heads handled by one launch (one row-tile map per head)
 
 struct AttnMaps {
   CUtensorMap k[kMaxKvMaps];    // [Tk rows x Dqk] of KV head g0+i, box {64, 64}, SW128
