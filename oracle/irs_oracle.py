@@ -33,7 +33,9 @@ Sources (NVIDIA NeMo AutoModel API reference pages):
   consecutive query heads share one KV group.
 * "nemo_automodel.components.models.common.cudnn_sparse_attention":
   latent attention, q [Tq,H,576], kv_latent [Tk,1,576], values are the first
-  512 latent dims, int32 indices with -1 invalid.
+  512 latent dims, int32 indices with -1 invalid; ``_CudnnSparseAttention``
+  pairs the forward with a backward that maps the BF16 output gradient to the
+  query and latent-KV gradients.
 
 Readings where the pages are silent or loose (each one is listed in the design
 notes of the repository):
@@ -384,6 +386,89 @@ def attention(q_bits, k_bits, v_bits, routes, scale: float, rows=None):
 def latent_attention(q_bits, kv_bits, routes, scale: float, Dv: int = 512, rows=None):
     """Latent (MLA) attention: keys are the full latent rows, values their first Dv dims."""
     return attention(q_bits, kv_bits, kv_bits[:, :, :Dv], routes, scale, rows=rows)
+
+
+# --------------------------------------------------------------------------------------
+# a7: backward of the gathered sparse attention (latent attention page,
+# `_CudnnSparseAttention.backward`: the BF16 output gradient is mapped to gradients of
+# the query and of the gathered K/V rows; the FA4 page's reverse block lists serve the
+# same key-side gradients for GQA)
+# --------------------------------------------------------------------------------------
+
+
+def attend_row_grad(q_t: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float, Hkv: int,
+                    dO_t: np.ndarray):
+    """Gradients of sum(out_t * dO_t) for one query row over its gathered keys.
+
+    q_t float64 [Hq, Dqk]; K float64 [n, Hkv, Dqk]; V float64 [n, Hkv, Dv];
+    dO_t float64 [Hq, Dv]. With p[h] = softmax over r of scale * K[r,g] . q[h] and
+    out[h] = sum_r p[h,r] V[r,g] (g the KV group of h):
+      dV[r,g] = sum over h in g of p[h,r] dO[h]
+      dp[h,r] = dO[h] . V[r,g]
+      ds[h,r] = p[h,r] (dp[h,r] - sum_r' p[h,r'] dp[h,r'])    (softmax Jacobian)
+      dq[h]   = scale * sum_r ds[h,r] K[r,g]
+      dK[r,g] = scale * sum over h in g of ds[h,r] q[h]
+    Returns dq [Hq, Dqk], dK [n, Hkv, Dqk], dV [n, Hkv, Dv]. A row without keys has a
+    constant output (reading R7), so all of its gradients are zero.
+    """
+    Hq, Dqk = q_t.shape
+    n = K.shape[0]
+    Dv = V.shape[2]
+    dq = np.zeros((Hq, Dqk), dtype=np.float64)
+    dK = np.zeros((n, Hkv, Dqk), dtype=np.float64)
+    dV = np.zeros((n, Hkv, Dv), dtype=np.float64)
+    if n == 0:
+        return dq, dK, dV
+    for h in range(Hq):
+        g = kv_group(h, Hq, Hkv)
+        s = scale * (K[:, g, :] @ q_t[h])        # [n]
+        e = np.exp(s - np.max(s))
+        p = e / np.sum(e)
+        dV[:, g, :] += np.outer(p, dO_t[h])
+        dp = V[:, g, :] @ dO_t[h]                # [n]
+        ds = p * (dp - np.sum(p * dp))
+        dq[h] = scale * (ds @ K[:, g, :])
+        dK[:, g, :] += scale * np.outer(ds, q_t[h])
+    return dq, dK, dV
+
+
+def attention_bwd(q_bits, k_bits, v_bits, routes, scale: float, dout_bits, rows=None):
+    """Backward of `attention` for the loss sum(out * dout).
+
+    dout_bits bf16 bits [T, Hq, Dv]. The key and value gradients of every routed ID are
+    summed over the requested rows. Returns dq float32 [len(rows), Hq, Dqk], dk float32
+    [Tk, Hkv, Dqk] and dv float32 [Tk, Hkv, Dv], accumulated in float64.
+    """
+    T, Hq, Dqk = q_bits.shape
+    Tk, Hkv, _ = k_bits.shape
+    Dv = v_bits.shape[2]
+    if Hq % Hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    if not scale > 0:
+        raise ValueError("scale must be positive")
+    rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
+    dq = np.zeros((rows.shape[0], Hq, Dqk), dtype=np.float64)
+    dk = np.zeros((Tk, Hkv, Dqk), dtype=np.float64)
+    dv = np.zeros((Tk, Hkv, Dv), dtype=np.float64)
+    for i, t in enumerate(rows):
+        ids = np.asarray(routes[t], dtype=np.int64)
+        ids = ids[(ids >= 0) & (ids < Tk)]
+        gq, gK, gV = attend_row_grad(bf16_to_f64(q_bits[t]), bf16_to_f64(k_bits[ids]),
+                                     bf16_to_f64(v_bits[ids]), scale, Hkv, bf16_to_f64(dout_bits[t]))
+        dq[i] = gq
+        np.add.at(dk, ids, gK)
+        np.add.at(dv, ids, gV)
+    return dq.astype(np.float32), dk.astype(np.float32), dv.astype(np.float32)
+
+
+def latent_attention_bwd(q_bits, kv_bits, routes, scale: float, dout_bits, Dv: int = 512, rows=None):
+    """Backward of `latent_attention`: the latent rows are both the keys and (by their
+    first Dv dims) the values, so their gradient is the key gradient plus the value
+    gradient on those dims. Returns dq [len(rows), Hq, Dqk] and dkv [Tk, 1, Dqk]."""
+    dq, dk, dv = attention_bwd(q_bits, kv_bits, kv_bits[:, :, :Dv], routes, scale, dout_bits, rows=rows)
+    dkv = dk.astype(np.float64)
+    dkv[:, :, :Dv] += dv
+    return dq, dkv.astype(np.float32)
 
 
 # --------------------------------------------------------------------------------------

@@ -463,6 +463,141 @@ def pin_latent_attention(O):
     np.testing.assert_allclose(lse, ref_l, rtol=1e-5, atol=1e-6)
 
 
+# --------------------------------------------------------------------------------------
+# a7: attention backward
+# --------------------------------------------------------------------------------------
+
+
+def route_mask(routes, T, Tk):
+    allowed = torch.zeros(T, Tk, dtype=torch.bool)
+    for t in range(T):
+        ids = [int(x) for x in routes[t] if 0 <= int(x) < Tk]
+        allowed[t, ids] = True
+    return allowed
+
+
+def sdpa_backward(q, k, v, allowed, scale, dout):
+    """Library reference: torch autograd through dense SDPA with the route mask.
+
+    q [T, Hq, D], k [Tk, Hkv, D], v [Tk, Hkv, Dv]: float64 tensors that are, or are
+    views of, leaves with requires_grad; the KV heads are repeated for their query
+    heads, so autograd sums each group's gradient. Backpropagates sum(out * dout).
+    """
+    G = q.shape[1] // k.shape[1]
+    kk = k.repeat_interleave(G, dim=1).permute(1, 0, 2)
+    vv = v.repeat_interleave(G, dim=1).permute(1, 0, 2)
+    out = torch.nn.functional.scaled_dot_product_attention(
+        q.permute(1, 0, 2), kk, vv, attn_mask=allowed.unsqueeze(0), scale=scale)
+    (out.permute(1, 0, 2) * dout).sum().backward()
+
+
+def random_bf16(rng, shape):
+    return torch_bf16_bits(rng.standard_normal(shape).astype(np.float32))
+
+
+def pin_attention_bwd_vs_autograd(O):
+    import irs_synth
+
+    for seed, (Hq, Hkv, Dqk, Dv), lens in ((11, (4, 2, 16, 8), [40]), (12, (6, 3, 8, 16), [10, 25, 15]),
+                                            (13, (4, 1, 24, 24), [3, 47])):
+        T = sum(lens)
+        wl = irs_synth.custom(T, Hq, Hkv, Dqk, Dv, 2, 8, 4, 8, doc_lens=lens, seed=seed)
+        rng = np.random.default_rng(seed)
+        routes = irs_synth.random_routes(rng, T, T, 12, wl.cu_seqlens)
+        dout = random_bf16(rng, (T, Hq, Dv))
+        scale = 0.3
+        dq, dk, dv = O.attention_bwd(wl.arrays["q"], wl.arrays["k"], wl.arrays["v"], routes, scale, dout)
+        q = torch.from_numpy(bits_to_f64(wl.arrays["q"])).requires_grad_(True)
+        k = torch.from_numpy(bits_to_f64(wl.arrays["k"])).requires_grad_(True)
+        v = torch.from_numpy(bits_to_f64(wl.arrays["v"])).requires_grad_(True)
+        sdpa_backward(q, k, v, route_mask(routes, T, T), scale, torch.from_numpy(bits_to_f64(dout)))
+        np.testing.assert_allclose(dq, q.grad.numpy(), rtol=1e-5, atol=1e-6)
+        np.testing.assert_allclose(dk, k.grad.numpy(), rtol=1e-5, atol=1e-6)
+        np.testing.assert_allclose(dv, v.grad.numpy(), rtol=1e-5, atol=1e-6)
+
+
+def pin_latent_attention_bwd(O):
+    """The latent rows are one leaf used as keys and, by their first Dv dims, as values."""
+    import irs_synth
+
+    rng = np.random.default_rng(16)
+    Tq, H, D, Dv, Tk = 6, 4, 64, 48, 200
+    q_bits = random_bf16(rng, (Tq, H, D))
+    kv_bits = random_bf16(rng, (Tk, 1, D))
+    r = irs_synth.latent_routes(rng, Tq, Tk, 16)
+    dout = random_bf16(rng, (Tq, H, Dv))
+    dq, dkv = O.latent_attention_bwd(q_bits, kv_bits, r, 0.125, dout, Dv=Dv)
+    q = torch.from_numpy(bits_to_f64(q_bits)).requires_grad_(True)
+    lat = torch.from_numpy(bits_to_f64(kv_bits)).requires_grad_(True)
+    sdpa_backward(q, lat, lat[:, :, :Dv], route_mask(r, Tq, Tk), 0.125, torch.from_numpy(bits_to_f64(dout)))
+    np.testing.assert_allclose(dq, q.grad.numpy(), rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(dkv, lat.grad.numpy(), rtol=1e-5, atol=1e-6)
+
+
+def pin_attention_bwd_finite_diff(O):
+    """Central differences of the oracle's own forward (pinned to SDPA above) along
+    random directions agree with its gradients."""
+    rng = np.random.default_rng(17)
+    Hq, Hkv, n, D, Dv, scale = 4, 2, 5, 6, 3, 0.7
+    q = rng.standard_normal((Hq, D))
+    K = rng.standard_normal((n, Hkv, D))
+    V = rng.standard_normal((n, Hkv, Dv))
+    dO = rng.standard_normal((Hq, Dv))
+    gq, gK, gV = O.attend_row_grad(q, K, V, scale, Hkv, dO)
+
+    def f(qq, KK, VV):
+        return float(np.sum(O.attend_row(qq, KK, VV, scale, Hkv)[0] * dO))
+
+    eps = 1e-5
+    for _ in range(4):
+        uq, uK, uV = rng.standard_normal(q.shape), rng.standard_normal(K.shape), rng.standard_normal(V.shape)
+        for grad, u, bump in ((gq, uq, lambda e, u=uq: (q + e * u, K, V)),
+                              (gK, uK, lambda e, u=uK: (q, K + e * u, V)),
+                              (gV, uV, lambda e, u=uV: (q, K, V + e * u))):
+            fd = (f(*bump(eps)) - f(*bump(-eps))) / (2 * eps)
+            assert abs(fd - float(np.sum(grad * u))) <= 1e-7 * max(1.0, abs(fd)), (fd, float(np.sum(grad * u)))
+
+
+def pin_attention_bwd_invariants(O):
+    import irs_synth
+
+    T, Hq, Hkv, D, Dv = 24, 4, 2, 16, 8
+    wl = irs_synth.custom(T, Hq, Hkv, D, Dv, 2, 8, 4, 8, seed=18)
+    rng = np.random.default_rng(18)
+    routes = irs_synth.random_routes(rng, T, T, 10, wl.cu_seqlens)
+    q, k, v = wl.arrays["q"], wl.arrays["k"], wl.arrays["v"]
+    dout = random_bf16(rng, (T, Hq, Dv))
+    dO = bits_to_f64(dout)
+    G = Hq // Hkv
+    scale = 1.0 / math.sqrt(D)
+    dq, dk, dv = O.attention_bwd(q, k, v, routes, scale, dout)
+    # softmax is shift-invariant in the keys: each row's key gradients sum to zero
+    tot = dk.astype(np.float64).sum(axis=0)
+    assert np.all(np.abs(tot) <= 1e-5 * np.abs(dk).astype(np.float64).sum(axis=0) + 1e-7), tot
+    # the weights of a row sum to one: its value gradients add up to the group's dO
+    want = dO.reshape(T, Hkv, G, Dv).sum(axis=(0, 2))
+    np.testing.assert_allclose(dv.astype(np.float64).sum(axis=0), want, rtol=1e-5, atol=1e-5)
+    # moving, adding or removing -1 slots, or permuting the IDs, changes nothing
+    r2 = np.full((T, 17), -1, np.int32)
+    for t in range(T):
+        vals = routes[t][routes[t] >= 0]
+        r2[t, np.sort(rng.choice(17, size=vals.shape[0], replace=False))] = rng.permutation(vals)
+    for got, ref in zip(O.attention_bwd(q, k, v, r2, scale, dout), (dq, dk, dv)):
+        np.testing.assert_allclose(got, ref, rtol=1e-6, atol=1e-7)
+    # one key per row: the output is that value row whatever q and k are
+    r4 = np.full((T, 5), -1, np.int32)
+    r4[:, 2] = np.arange(T) // 2
+    dq4, dk4, dv4 = O.attention_bwd(q, k, v, r4, scale, dout)
+    assert np.all(dq4 == 0) and np.all(dk4 == 0)
+    want4 = np.zeros((T, Hkv, Dv))
+    for t in range(T):
+        want4[t // 2] += dO[t].reshape(Hkv, G, Dv).sum(axis=1)
+    np.testing.assert_allclose(dv4, want4, rtol=1e-6, atol=1e-6)
+    # rows without keys have a constant output: no gradient anywhere
+    z = O.attention_bwd(q, k, v, np.full((T, 3), -1, np.int32), scale, dout)
+    assert all(np.all(x == 0) for x in z)
+
+
 def pin_window_compose(O):
     rng = np.random.default_rng(4)
     cu = np.asarray([0, 30, 100], np.int32)
@@ -502,4 +637,8 @@ ALL_PINS = [
     pin_attention_invariants,
     pin_latent_attention,
     pin_window_compose,
+    pin_attention_bwd_vs_autograd,
+    pin_latent_attention_bwd,
+    pin_attention_bwd_finite_diff,
+    pin_attention_bwd_invariants,
 ]

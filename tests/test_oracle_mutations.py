@@ -127,6 +127,53 @@ def _compose_shifted(routes, cu_seqlens, T, window, rows=None):
     return out
 
 
+def _row_grad_variant(centre=True, dk_scale=True, normalise=True, key_group=None):
+    """attend_row_grad with one planted mistake (the flags select which)."""
+    def grad(q_t, K, V, scale, Hkv, dO_t):
+        Hq, Dqk = q_t.shape
+        n = K.shape[0]
+        dq = np.zeros((Hq, Dqk))
+        dK = np.zeros((n, Hkv, Dqk))
+        dV = np.zeros((n, Hkv, V.shape[2]))
+        if n == 0:
+            return dq, dK, dV
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            gk = g if key_group is None else key_group(h, Hq, Hkv)
+            s = scale * (K[:, g, :] @ q_t[h])
+            e = np.exp(s - np.max(s))
+            p = e / np.sum(e)
+            dV[:, g, :] += np.outer(p if normalise else e, dO_t[h])
+            dp = V[:, g, :] @ dO_t[h]
+            ds = p * (dp - np.sum(p * dp)) if centre else p * dp
+            dq[h] = scale * (ds @ K[:, g, :])
+            dK[:, gk, :] += (scale if dk_scale else 1.0) * np.outer(ds, q_t[h])
+        return dq, dK, dV
+    return grad
+
+
+def _bwd_scatter_overwrites(q_bits, k_bits, v_bits, routes, scale, dout_bits, rows=None):
+    T, Hq, Dqk = q_bits.shape
+    Tk, Hkv, _ = k_bits.shape
+    dq = np.zeros((T, Hq, Dqk))
+    dk = np.zeros((Tk, Hkv, Dqk))
+    dv = np.zeros((Tk, Hkv, v_bits.shape[2]))
+    for t in range(T):
+        ids = np.asarray(routes[t], np.int64)
+        ids = ids[(ids >= 0) & (ids < Tk)]
+        gq, gK, gV = O.attend_row_grad(O.bf16_to_f64(q_bits[t]), O.bf16_to_f64(k_bits[ids]),
+                                       O.bf16_to_f64(v_bits[ids]), scale, Hkv, O.bf16_to_f64(dout_bits[t]))
+        dq[t] = gq
+        dk[ids] = gK
+        dv[ids] = gV
+    return dq.astype(np.float32), dk.astype(np.float32), dv.astype(np.float32)
+
+
+def _latent_bwd_no_value_grad(q_bits, kv_bits, routes, scale, dout_bits, Dv=512, rows=None):
+    dq, dk, _ = O.attention_bwd(q_bits, kv_bits, kv_bits[:, :, :Dv], routes, scale, dout_bits, rows=rows)
+    return dq, dk
+
+
 _REAL_ATTEND = O.attend_row
 _REAL_COMPOSE = O.compose_window
 
@@ -149,6 +196,12 @@ MUTATIONS = {
     "scale_ignored": ("attend_row", _attend_no_scale),
     "lse_missing_max": ("attend_row", _attend_lse_no_max),
     "window_shifted": ("compose_window", _compose_shifted),
+    "bwd_softmax_not_centred": ("attend_row_grad", _row_grad_variant(centre=False)),
+    "bwd_dk_without_scale": ("attend_row_grad", _row_grad_variant(dk_scale=False)),
+    "bwd_dv_unnormalised": ("attend_row_grad", _row_grad_variant(normalise=False)),
+    "bwd_dk_group_modulo": ("attend_row_grad", _row_grad_variant(key_group=lambda h, Hq, Hkv: h % Hkv)),
+    "bwd_scatter_overwrites": ("attention_bwd", _bwd_scatter_overwrites),
+    "bwd_latent_drops_value_grad": ("latent_attention_bwd", _latent_bwd_no_value_grad),
 }
 
 
