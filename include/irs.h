@@ -199,6 +199,41 @@ irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_
                                    float* lse, int32_t* err_flag, irs_stream_t stream);
 
 /*
+ * sparse_gqa_attn_bwd(q, k, v, route_ids, out, lse, dout, scale) -> dq, dk, dv
+ *
+ * Latent attention page, `_CudnnSparseAttention.backward` (the BF16 output gradient is
+ * mapped to gradients of the query and of the gathered K/V rows); the same gradients
+ * for the GQA routes of the QSA page. The backward of irs_sparse_gqa_attn_fwd for the
+ * loss sum(out * dout). With the notation above and the forward's out and lse:
+ *   p_r   = exp(s_r - lse),   D = dout[t,h,:] . out[t,h,:]
+ *   ds_r  = p_r (dout[t,h,:] . v[r,g,:] - D)
+ *   dq[t,h,:]  = scale * sum_r ds_r k[r,g,:]          (written)
+ *   dk[r,g,:] += scale * ds_r q[t,h,:]                  (added, over every t and h in g)
+ *   dv[r,g,:] += p_r dout[t,h,:]                        (added)
+ * D is taken from the BF16 forward output, as the forward saves it; route semantics
+ * (padding, IRS_DEVERR_ROUTE_ID, distinct IDs) are those of the forward.
+ *
+ * q, k, v, route_ids, T, Tk, Hq, Hkv, Dqk, Dv, W, scale: as for the forward (same limits)
+ * out   bf16 [T, Hq, Dv] contiguous: the forward's output
+ * lse   fp32 [T, Hq] contiguous: the forward's lse (natural log; required)
+ * dout  bf16 [T, Hq, Dv] contiguous
+ * dq    fp32 [T, Hq, Dqk] contiguous, overwritten
+ * dk    fp32 [Tk, Hkv, Dqk] contiguous, 16-byte aligned, ACCUMULATED (zero it first)
+ * dv    fp32 [Tk, Hkv, Dv] contiguous, 16-byte aligned, accumulated; dv may equal dk
+ *       (Dv <= Dqk): the value gradient is then added into the first Dv dims of each dk
+ *       row, which is the gradient of latent rows used as keys and values
+ * The accumulation uses FP32 atomics, so dk and dv are not bit-reproducible across runs.
+ * CUDA-core kernel (no tensor cores yet): one CTA per (query, KV head, block of up to
+ * 16 query heads); it waits on nothing outside itself.
+ */
+irs_status irs_sparse_gqa_attn_bwd(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k,
+                                   int64_t k_stride_t, int64_t k_stride_h, const void* v, int64_t v_stride_t,
+                                   int64_t v_stride_h, const int32_t* route_ids, int64_t route_stride,
+                                   const void* out, const float* lse, const void* dout, int T, int Tk, int Hq,
+                                   int Hkv, int Dqk, int Dv, int W, float scale, float* dq, float* dk, float* dv,
+                                   int32_t* err_flag, irs_stream_t stream);
+
+/*
  * Failure-detection self-test (no counterpart on the reference pages). Launches one
  * bounded on-device wait on a barrier phase that nothing completes: after limit_ns
  * (1e6 .. 2e9) the wait gives up, ORs IRS_DEVERR_TIMEOUT into *err_flag and the kernel

@@ -5,6 +5,7 @@ this package is its thin Python binding. Names follow the C entry points:
 
 * ``sparse_index_score_topk(qI, kI, w, cu_seqlens, c, budget) -> route_ids``
 * ``sparse_gqa_attn_fwd(q, k, v, route_ids, scale) -> (out, lse)``
+* ``sparse_gqa_attn_bwd(q, k, v, route_ids, out, lse, dout, scale) -> (dq, dk, dv)``
 * ``topk_from_scores(scores, cu_seqlens, c, budget) -> route_ids``
 * ``compose_window_routes(route_ids, cu_seqlens, window) -> route_ids``
 """
@@ -21,6 +22,7 @@ from ._binding import (  # noqa: F401
     index_workspace_bytes,
     lib,
     read_device_errors,
+    sparse_gqa_attn_bwd,
     sparse_gqa_attn_fwd,
     sparse_index_score_topk,
     topk_from_scores,

@@ -40,6 +40,8 @@ _SIGNATURES = {
     "irs_compose_window_routes": (_I, [_P, _I, _P, _I, _I, _I, _P, _P, _P]),
     "irs_sparse_gqa_attn_fwd": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I, _I, _I, _I, _I, _I,
                                      _I, _F, _P, _P, _P, _P]),
+    "irs_sparse_gqa_attn_bwd": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _P, _P, _P, _I, _I,
+                                     _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
     "irs_check_bounded_wait": (_I, [ctypes.c_uint64, _P, _P]),
 }
 
@@ -263,6 +265,66 @@ def sparse_gqa_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, route
         _ptr(err), _stream(dev))
     _check(st, "sparse_gqa_attn_fwd")
     return out, lse
+
+
+def _values_alias_keys(k: torch.Tensor, v: torch.Tensor) -> bool:
+    return v.data_ptr() == k.data_ptr() and v.stride(0) == k.stride(0) and v.stride(1) == k.stride(1)
+
+
+def sparse_gqa_attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, route_ids: torch.Tensor,
+                        out: torch.Tensor, lse: torch.Tensor, dout: torch.Tensor, scale: float | None = None, *,
+                        dq: torch.Tensor | None = None, dk: torch.Tensor | None = None,
+                        dv: torch.Tensor | None = None,
+                        err: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor | None]:
+    """Backward of `sparse_gqa_attn_fwd` for the loss sum(out * dout): (dq, dk, dv), fp32.
+
+    out and lse are the forward's outputs, dout bf16 [T, Hq, Dv]. When v is a view of k's
+    leading Dv dims (latent attention), the rows are one tensor: its gradient is returned
+    as dk [Tk, Hkv, Dqk] (key plus value gradient) and dv is None. dk and dv, if given,
+    are added to; by default they are allocated zeroed.
+    """
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(route_ids, "route_ids", torch.int32, 2)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    _need(dout, "dout", torch.bfloat16, 3)
+    T, Hq, Dqk = q.shape
+    Tk, Hkv, Dk = k.shape
+    Tv, Hv, Dv = v.shape
+    if Dk != Dqk or Tv != Tk or Hv != Hkv or route_ids.shape[0] != T:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)} "
+                         f"route {tuple(route_ids.shape)}")
+    for name, t in (("q", q), ("k", k), ("v", v), ("route_ids", route_ids)):
+        if t.stride(-1) != 1:
+            raise ValueError(f"{name} must have unit inner stride")
+    for name, t, shape in (("out", out, (T, Hq, Dv)), ("dout", dout, (T, Hq, Dv)), ("lse", lse, (T, Hq))):
+        if tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous with shape {shape}")
+    W = route_ids.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(Dqk)
+    dev = q.device
+    shared = _values_alias_keys(k, v) and Dv <= Dqk
+    if dq is None:
+        dq = torch.empty((T, Hq, Dqk), dtype=torch.float32, device=dev)
+    if dk is None:
+        dk = torch.zeros((Tk, Hkv, Dqk), dtype=torch.float32, device=dev)
+    if not shared and dv is None:
+        dv = torch.zeros((Tk, Hkv, Dv), dtype=torch.float32, device=dev)
+    for name, t, shape in (("dq", dq, (T, Hq, Dqk)), ("dk", dk, (Tk, Hkv, Dqk))) + (
+            () if shared else (("dv", dv, (Tk, Hkv, Dv)),)):
+        if t.dtype != torch.float32 or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 tensor {shape}")
+    if err is None:
+        err = device_error_flag(dev)
+    st = lib().irs_sparse_gqa_attn_bwd(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1), _ptr(v), v.stride(0), v.stride(1),
+        _ptr(route_ids), route_ids.stride(0), _ptr(out), _ptr(lse), _ptr(dout), T, Tk, Hq, Hkv, Dqk, Dv, W,
+        float(scale), _ptr(dq), _ptr(dk), _ptr(dk if shared else dv), _ptr(err), _stream(dev))
+    _check(st, "sparse_gqa_attn_bwd")
+    return dq, dk, (None if shared else dv)
 
 
 def check_bounded_wait(limit_ms: float = 20.0, device=None, err: torch.Tensor | None = None) -> torch.Tensor:

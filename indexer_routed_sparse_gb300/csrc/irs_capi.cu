@@ -32,7 +32,7 @@ struct DeviceInfo {
   bool ok = false;
   int num_sms = 0;
   size_t l2_bytes = 0;
-  size_t score_smem = 0, topk_smem = 0, attn_smem = 0, mla_smem = 0;   // largest values configured so far
+  size_t score_smem = 0, topk_smem = 0, attn_smem = 0, mla_smem = 0, bwd_smem = 0;   // largest configured so far
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -313,6 +313,71 @@ irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_
       return s;
   }
   return IRS_OK;
+}
+
+
+irs_status irs_sparse_gqa_attn_bwd(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k,
+                                   int64_t k_stride_t, int64_t k_stride_h, const void* v, int64_t v_stride_t,
+                                   int64_t v_stride_h, const int32_t* route_ids, int64_t route_stride,
+                                   const void* out, const float* lse, const void* dout, int T, int Tk, int Hq,
+                                   int Hkv, int Dqk, int Dv, int W, float scale, float* dq, float* dk, float* dv,
+                                   int32_t* err_flag, irs_stream_t stream) {
+  if (T < 0 || Tk < 1 || Hq < 1 || Hkv < 1) return fail(IRS_ERR_VALUE, "bad sizes (T=%d Tk=%d Hq=%d Hkv=%d)", T, Tk, Hq, Hkv);
+  if (Hq % Hkv != 0) return fail(IRS_ERR_VALUE, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (Dqk < 64 || Dqk > 576 || Dqk % 64 != 0) return fail(IRS_ERR_VALUE, "Dqk must be a multiple of 64 in [64, 576]");
+  if (Dv < 128 || Dv > 512 || Dv % 128 != 0) return fail(IRS_ERR_VALUE, "Dv must be a multiple of 128 in [128, 512]");
+  if (W < 1 || W > 4096) return fail(IRS_ERR_VALUE, "route width W must be in [1, 4096] (got %d)", W);
+  if (route_stride < W) return fail(IRS_ERR_VALUE, "route_stride must be >= W");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(IRS_ERR_VALUE, "scale must be positive and finite");
+  if (T == 0) return IRS_OK;
+  if (!q || !k || !v || !route_ids || !out || !lse || !dout || !dq || !dk || !dv)
+    return fail(IRS_ERR_VALUE, "NULL tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv))
+    return fail(IRS_ERR_VALUE, "q, k, v, dk and dv must be 16-byte aligned");
+  if (q_stride_t % 8 || q_stride_h % 8 || k_stride_t % 8 || k_stride_h % 8 || v_stride_t % 8 || v_stride_h % 8)
+    return fail(IRS_ERR_VALUE, "q/k/v strides must be multiples of 8 elements (16 bytes)");
+  if (q_stride_t < 0 || q_stride_h < 0 || k_stride_t < 0 || k_stride_h < 0 || v_stride_t < 0 || v_stride_h < 0)
+    return fail(IRS_ERR_VALUE, "negative strides are not supported");
+  if (dv == dk && Dv > Dqk) return fail(IRS_ERR_VALUE, "dv may share dk's buffer only when Dv <= Dqk");
+  if ((long long)T * Hkv * ((Hq / Hkv + irs::bwd_max_heads() - 1) / irs::bwd_max_heads()) > 0x7fffffffLL)
+    return fail(IRS_ERR_VALUE, "too many work items");
+  DeviceInfo* dev = nullptr;
+  irs_status s = current_device(&dev);
+  if (s != IRS_OK) return s;
+
+  irs::BwdArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.q_st = q_stride_t; a.q_sh = q_stride_h;
+  a.k_st = k_stride_t; a.k_sh = k_stride_h;
+  a.v_st = v_stride_t; a.v_sh = v_stride_h;
+  a.route = route_ids;
+  a.route_stride = route_stride;
+  a.out = static_cast<const __nv_bfloat16*>(out);
+  a.lse = lse;
+  a.dout = static_cast<const __nv_bfloat16*>(dout);
+  a.dq = dq; a.dk = dk; a.dv = dv;
+  a.err = err_flag;
+  a.T = T; a.Tk = Tk; a.Hq = Hq; a.Hkv = Hkv; a.Dqk = Dqk; a.Dv = Dv; a.W = W;
+  a.G = Hq / Hkv;
+  a.HB = a.G < irs::bwd_max_heads() ? a.G : irs::bwd_max_heads();
+  a.nhb = (a.G + a.HB - 1) / a.HB;
+  a.v_alias = (v == k && v_stride_t == k_stride_t && v_stride_h == k_stride_h && Dv <= Dqk) ? 1 : 0;
+  a.dv_alias = dv == dk ? 1 : 0;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.nkc = irs::bwd_pick_rows(a, kMaxSmem);
+  if (a.nkc == 0) return fail(IRS_ERR_VALUE, "backward tile does not fit in shared memory");
+  const size_t smem = irs::bwd_smem_bytes(a);
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (dev->bwd_smem < smem) {
+      if ((s = launch_status(irs::configure_bwd_kernel(smem), "configuring the backward")) != IRS_OK) return s;
+      dev->bwd_smem = smem;
+    }
+  }
+  return launch_status(irs::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)), "launching the backward");
 }
 
 }  // extern "C"

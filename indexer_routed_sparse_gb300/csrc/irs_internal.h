@@ -86,4 +86,33 @@ cudaError_t launch_mla(const AttnArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t configure_attn_kernel(size_t smem);
 cudaError_t launch_attn(const AttnMaps& maps, const AttnArgs& a, const AttnPlan& p, cudaStream_t stream);
 
+// Attention backward (CUDA cores): one CTA per (query, KV head, block of <= 16 heads).
+struct BwdArgs {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh;
+  const int32_t* route;
+  int64_t route_stride;
+  const __nv_bfloat16* out;   // [T, Hq, Dv] contiguous
+  const float* lse;           // [T, Hq]
+  const __nv_bfloat16* dout;  // [T, Hq, Dv] contiguous
+  float* dq;                  // [T, Hq, Dqk], written
+  float* dk;                  // [Tk, Hkv, Dqk], added to
+  float* dv;                  // [Tk, Hkv, Dv], added to (unused when dv_alias)
+  int32_t* err;
+  int T, Tk, Hq, Hkv, Dqk, Dv, W;
+  int G, HB, nhb;
+  int v_alias;    // 1: value rows are the first Dv dims of the key rows
+  int dv_alias;   // 1: the value gradient is added into the first Dv dims of dk's rows
+  int nkc;        // routed rows staged per step
+  float scale, scale_log2;
+};
+
+size_t bwd_smem_bytes(const BwdArgs& a);
+int bwd_pick_rows(const BwdArgs& a, size_t max_smem);
+int bwd_max_heads();
+cudaError_t configure_bwd_kernel(size_t smem);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+
 }  // namespace irs

@@ -111,3 +111,44 @@ def test_binding_rejects_wrong_dtypes_on_cpu():
     qb = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):   # not a CUDA tensor
         irs.sparse_gqa_attn_fwd(qb, qb, qb, torch.zeros(4, 4, dtype=torch.int32))
+
+
+def _bwd_call(lib, p=None, **kw):
+    a = dict(T=4, Tk=16, Hq=4, Hkv=2, Dqk=128, Dv=128, W=8, scale=0.1, route_stride=8, q_st=512, dk=p, dv=p)
+    a.update(kw)
+    return lib.irs_sparse_gqa_attn_bwd(p, a["q_st"], 128, p, 256, 128, p, 256, 128, p, a["route_stride"], p, p, p,
+                                       a["T"], a["Tk"], a["Hq"], a["Hkv"], a["Dqk"], a["Dv"], a["W"], a["scale"],
+                                       p, a["dk"], a["dv"], None, None)
+
+
+@pytest.mark.parametrize("case", [
+    dict(Hq=6, Hkv=4), dict(Dqk=100), dict(Dqk=640), dict(Dv=64), dict(Dv=640), dict(W=0), dict(W=5000),
+    dict(scale=0.0), dict(scale=float("nan")), dict(route_stride=3, W=4),
+])
+def test_backward_validation_is_value_error(lib, case):
+    assert _bwd_call(lib, None, **case) == 2, case
+
+
+def test_backward_host_checks(lib):
+    buf = ctypes.create_string_buffer(64)
+    p = ctypes.addressof(buf) + (16 - ctypes.addressof(buf) % 16) % 16
+    assert _bwd_call(lib, None) == 2 and b"NULL" in lib.irs_last_error()
+    assert _bwd_call(lib, p, q_st=12) == 2 and b"multiples of 8" in lib.irs_last_error()
+    assert _bwd_call(lib, p, dk=p + 4) == 2 and b"16-byte aligned" in lib.irs_last_error()
+    # a shared dk/dv buffer needs the value rows to fit in the key rows
+    assert _bwd_call(lib, p, Dqk=128, Dv=256) == 2 and b"Dv <= Dqk" in lib.irs_last_error()
+    assert _bwd_call(lib, p, T=0) == 0          # nothing to do
+
+
+def test_backward_binding_rejects_wrong_inputs_on_cpu():
+    import torch
+
+    import indexer_routed_sparse_gb300 as irs
+
+    qb = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
+    r = torch.zeros(4, 4, dtype=torch.int32)
+    lse = torch.zeros(4, 2)
+    with pytest.raises(TypeError):      # q must be bf16
+        irs.sparse_gqa_attn_bwd(qb.float(), qb, qb, r, qb, lse, qb)
+    with pytest.raises(ValueError):     # not CUDA tensors
+        irs.sparse_gqa_attn_bwd(qb, qb, qb, r, qb, lse, qb)

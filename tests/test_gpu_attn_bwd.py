@@ -1,0 +1,150 @@
+"""Sparse attention backward on the GPU (through the C ABI) against the CPU oracle.
+
+The kernel gets the oracle's forward outputs (out rounded to bf16, as a forward saves
+it, and the FP32 lse) and an arbitrary bf16 output gradient; its dq, dk and dv are
+compared with the oracle's backward, per tensor:
+    dq, dk:  max |gpu - ref| <= 2e-2 max |ref| + 1e-4,  mean |gpu - ref| <= 5e-3 mean |ref| + 1e-5
+    dv:      max |gpu - ref| <= 1e-4 max |ref| + 1e-6,  mean |gpu - ref| <= 2e-5 mean |ref| + 1e-7
+Reading: the kernel takes D = dO . out from the bf16 output, while the oracle sums
+p_r dO.v_r exactly. An FP32 emulation of the kernel's arithmetic on these shapes puts
+that effect at up to 3e-3 of the largest dq/dk entry and 1e-3 of the mean, about a
+sixth of the bound. dv does not involve D (FP32 sums, about 2e-6), so its tight bound
+checks every probability, key and route. The absolute floors cover gradients that are
+exactly zero in the oracle (one key per row).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import irs_synth
+from oracle import irs_oracle as O
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+TOL = {"loose": (2e-2, 1e-4, 5e-3, 1e-5), "tight": (1e-4, 1e-6, 2e-5, 1e-7)}
+
+
+@pytest.fixture(scope="module")
+def irs():
+    import indexer_routed_sparse_gb300 as m
+
+    m.lib()
+    return m
+
+
+def bf16_dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits)).view(torch.bfloat16).to(DEV)
+
+
+def check_grad(name, got, ref):
+    """dv gets the tight bound, every gradient that involves D the loose one."""
+    max_rel, max_abs, mean_rel, mean_abs = TOL["tight" if name == "dv" else "loose"]
+    got = got.double().cpu().numpy() if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, name
+    assert np.all(np.isfinite(got)), name
+    err = np.abs(got - ref)
+    assert err.max() <= max_rel * np.abs(ref).max() + max_abs, (name, err.max(), np.abs(ref).max())
+    assert err.mean() <= mean_rel * np.abs(ref).mean() + mean_abs, (name, err.mean(), np.abs(ref).mean())
+
+
+def forward_outputs(q, k, v, routes, scale):
+    out, lse = O.attention(q, k, v, routes, scale)
+    return torch.from_numpy(out).to(torch.bfloat16).to(DEV), torch.from_numpy(lse).to(DEV)
+
+
+def run_gqa(irs, q, k, v, routes, scale, dout, dk0=None):
+    out_d, lse_d = forward_outputs(q, k, v, routes, scale)
+    kd = bf16_dev(k)
+    dk = None if dk0 is None else torch.from_numpy(dk0).to(DEV)
+    dq, dk, dv = irs.sparse_gqa_attn_bwd(bf16_dev(q), kd, bf16_dev(v), torch.from_numpy(routes).to(DEV), out_d,
+                                         lse_d, bf16_dev(dout), scale, dk=dk)
+    return dq, dk, dv
+
+
+GQA_CASES = [
+    # (T, Hq, Hkv, Dqk, Dv, W, doc_lens, seed)
+    (300, 8, 2, 128, 128, 64, [120, 180], 21),      # several staged chunks, two documents
+    (200, 4, 4, 64, 128, 33, [200], 22),            # one head per KV head, Dv > Dqk
+    (150, 6, 2, 192, 128, 100, [50, 60, 40], 23),   # three heads per KV head
+    (64, 32, 1, 128, 256, 80, [64], 24),            # two head blocks per KV head
+    (512, 32, 8, 128, 128, 512, [512], 25),         # mid-workload head shape
+]
+
+
+@pytest.mark.parametrize("T, Hq, Hkv, Dqk, Dv, W, lens, seed", GQA_CASES)
+def test_gqa_backward_matches_oracle(irs, T, Hq, Hkv, Dqk, Dv, W, lens, seed):
+    wl = irs_synth.custom(T, Hq, Hkv, Dqk, Dv, 2, 64, 4, 8, doc_lens=lens, seed=seed)
+    rng = np.random.default_rng(seed)
+    routes = irs_synth.random_routes(rng, T, T, W, wl.cu_seqlens)
+    dout = irs_synth.f32_to_bf16_bits(rng.standard_normal((T, Hq, Dv)).astype(np.float32))
+    scale = 1.0 / math.sqrt(Dqk)
+    q, k, v = wl.arrays["q"], wl.arrays["k"], wl.arrays["v"]
+    dq, dk, dv = run_gqa(irs, q, k, v, routes, scale, dout)
+    irs.check_device_errors(DEV)
+    ref_dq, ref_dk, ref_dv = O.attention_bwd(q, k, v, routes, scale, dout)
+    check_grad("dq", dq, ref_dq)
+    check_grad("dk", dk, ref_dk)
+    check_grad("dv", dv, ref_dv)
+
+
+def test_gradients_are_added_to_the_given_buffers(irs):
+    T, Hq, Hkv, D = 96, 4, 2, 128
+    wl = irs_synth.custom(T, Hq, Hkv, D, D, 2, 64, 4, 8, seed=26)
+    rng = np.random.default_rng(26)
+    routes = irs_synth.random_routes(rng, T, T, 40, wl.cu_seqlens)
+    dout = irs_synth.f32_to_bf16_bits(rng.standard_normal((T, Hq, D)).astype(np.float32))
+    base = rng.standard_normal((T, Hkv, D)).astype(np.float32)
+    q, k, v = wl.arrays["q"], wl.arrays["k"], wl.arrays["v"]
+    _, dk, _ = run_gqa(irs, q, k, v, routes, 0.1, dout, dk0=base)
+    irs.check_device_errors(DEV)
+    _, ref_dk, _ = O.attention_bwd(q, k, v, routes, 0.1, dout)
+    check_grad("dk", dk.cpu().numpy() - base, ref_dk)
+
+
+def test_latent_backward_matches_oracle(irs):
+    rng = np.random.default_rng(27)
+    Tq, H, D, Dv, Tk, W = 24, 128, 576, 512, 700, 128
+    q = irs_synth.f32_to_bf16_bits(rng.standard_normal((Tq, H, D)).astype(np.float32))
+    kv = irs_synth.f32_to_bf16_bits(rng.standard_normal((Tk, 1, D)).astype(np.float32))
+    routes = irs_synth.latent_routes(rng, Tq, Tk, W)
+    dout = irs_synth.f32_to_bf16_bits(rng.standard_normal((Tq, H, Dv)).astype(np.float32))
+    scale = 1.0 / math.sqrt(D)
+    out, lse = O.latent_attention(q, kv, routes, scale, Dv=Dv)
+    kvd = bf16_dev(kv)
+    dq, dkv, dv = irs.sparse_gqa_attn_bwd(bf16_dev(q), kvd, kvd[:, :, :Dv], torch.from_numpy(routes).to(DEV),
+                                          torch.from_numpy(out).to(torch.bfloat16).to(DEV),
+                                          torch.from_numpy(lse).to(DEV), bf16_dev(dout), scale)
+    irs.check_device_errors(DEV)
+    assert dv is None
+    ref_dq, ref_dkv = O.latent_attention_bwd(q, kv, routes, scale, dout, Dv=Dv)
+    check_grad("dq", dq, ref_dq)
+    check_grad("dkv", dkv, ref_dkv)
+
+
+def test_single_key_empty_rows_and_bad_ids(irs):
+    T, Hq, Hkv, D, Tk = 64, 8, 2, 128, 64
+    wl = irs_synth.custom(T, Hq, Hkv, D, D, 2, 64, 4, 8, seed=28)
+    rng = np.random.default_rng(28)
+    q, k, v = wl.arrays["q"], wl.arrays["k"], wl.arrays["v"]
+    dout = irs_synth.f32_to_bf16_bits(rng.standard_normal((T, Hq, D)).astype(np.float32))
+    # W = 1: every row attends one key, so dq and dk vanish and dv collects dO
+    r1 = (np.arange(T, dtype=np.int32) // 2).reshape(T, 1)
+    dq, dk, dv = run_gqa(irs, q, k, v, r1, 0.2, dout)
+    irs.check_device_errors(DEV)
+    ref = O.attention_bwd(q, k, v, r1, 0.2, dout)
+    for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        check_grad(name, got, want)
+    # rows without keys give no gradient; an ID outside [-1, Tk) is padding and is reported
+    r2 = irs_synth.random_routes(rng, T, Tk, 12, wl.cu_seqlens)
+    r2[::3] = -1
+    r2[1, 0] = Tk + 5
+    dq, dk, dv = run_gqa(irs, q, k, v, r2, 0.2, dout)
+    flags = irs.read_device_errors(DEV)
+    assert flags & irs.DEVERR_ROUTE_ID
+    ref = O.attention_bwd(q, k, v, r2, 0.2, dout)
+    assert torch.all(dq[::3] == 0)
+    for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        check_grad(name, got, want)
