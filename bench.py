@@ -320,6 +320,8 @@ def run_gpu(args) -> dict | None:
         ee[i][1].synchronize()
     barrier(world)
     e2e_ms = reduce_max(float(np.mean([ee[i][0].elapsed_time(ee[i][1]) for i in range(e2e_steps)])), world, dev)
+    bwd = time_backward(args, wl, irs, d, route if has_index else d["route"], kv_v, out, lse, flush, err, stream,
+                        dev) if args.with_backward else None
     clk = clocks.stop() if rank == 0 else None
     irs.check_device_errors(dev)
 
@@ -377,6 +379,8 @@ def run_gpu(args) -> dict | None:
                           "roofline_frac": round(idx_roof_s / idx_avg_s, 4), "roofline_us": round(idx_roof_s * 1e6, 2),
                           "algorithmic_bytes": cnt["idx_bytes"], "flops": cnt["idx_flops"],
                           "includes_window_composition": bool(wl.window)}
+    if bwd is not None:
+        res["backward"] = backward_report(wl, cnt, bwd, peaks)
     if not args.no_cpu_baseline and world == 1 and args.workload == WORKLOAD:
         res["cpu_baseline"] = cpu_baseline(wl, cnt, budget_s=args.cpu_seconds, small=args.small)
     if world > 1:
@@ -384,6 +388,64 @@ def run_gpu(args) -> dict | None:
 
         dist.destroy_process_group()
     return res
+
+
+def time_backward(args, wl, irs, d, route, kv_v, out, lse, flush, err, stream, dev) -> float:
+    """Mean device time (s) of one sparse_gqa_attn_bwd call (accumulators zeroed inside the
+    call's timed region, L2 flushed before each), on the step's routes and forward outputs."""
+    import torch
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(wl.seed + 1000)
+    dout = torch.randn(out.shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    k, v = (d["kv"], kv_v) if wl.latent else (d["k"], d["v"])
+    dq = torch.empty((wl.T, wl.Hq, wl.Dqk), dtype=torch.float32, device=dev)
+    dk = torch.empty((wl.Tk, wl.Hkv, wl.Dqk), dtype=torch.float32, device=dev)
+    dv = None if wl.latent else torch.empty((wl.Tk, wl.Hkv, wl.Dv), dtype=torch.float32, device=dev)
+
+    def backward():
+        dk.zero_()
+        if dv is not None:
+            dv.zero_()
+        irs.sparse_gqa_attn_bwd(d["q"], k, v, route, out, lse, dout, wl.scale, dq=dq, dk=dk, dv=dv, err=err)
+
+    for _ in range(args.warmup):
+        backward()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        backward()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    irs.check_device_errors(dev)
+    return float(np.mean([e[0].elapsed_time(e[1]) for e in ev])) * 1e-3
+
+
+def backward_report(wl, cnt, bwd_s: float, peaks: dict) -> dict:
+    """Backward rate against the forward's roofline definition.
+
+    FLOPs per (valid pair, query head): s and dp (2 Dqk + 2 Dv), dq and dk (4 Dqk) and dv
+    (2 Dv). Bytes: the gathered K/V rows of every valid pair (as in the forward), q, dout,
+    out, lse and dq per query head, the routes, and dk/dv written once.
+    """
+    rows = 1 if wl.latent else wl.Hkv
+    kv_dims = wl.Dqk + (0 if wl.latent else wl.Dv)
+    flops = cnt["pairs"] * wl.Hq * 2.0 * (3 * wl.Dqk + 2 * wl.Dv)
+    nbytes = (cnt["pairs"] * rows * kv_dims * 2
+              + wl.T * wl.Hq * (wl.Dqk * 2 + 2 * wl.Dv * 2 + 4 + wl.Dqk * 4)
+              + wl.T * wl.route_width * 4
+              + wl.Tk * rows * kv_dims * 4)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    roof_s = max(t_hbm, t_tc)
+    return {"ms": round(bwd_s * 1e3, 4), "tflops": round(flops / bwd_s / 1e12, 3),
+            "gbs": round(nbytes / bwd_s / 1e9, 1), "bound": "hbm" if t_hbm >= t_tc else "tensor",
+            "roofline_ms": round(roof_s * 1e3, 4), "roofline_frac": round(roof_s / bwd_s, 4),
+            "algorithmic_bytes": int(nbytes), "flops": flops, "kernel": "attn_bwd_kernel",
+            "launches_per_call": 1,
+            "note": "FP32 CUDA-core kernel; timed separately, not part of the step or of value"}
 
 
 # --------------------------------------------------------------------------------------
@@ -510,6 +572,8 @@ def main(argv=None):
     ap.add_argument("--small", action="store_true",
                     help="the workload's reduced-size variant (test sizes; for profiler captures, not a bench line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--with-backward", action="store_true",
+                    help="also time sparse_gqa_attn_bwd on the step's routes (reported under 'backward')")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=150.0)
     args = ap.parse_args(argv)
