@@ -235,6 +235,26 @@ def custom(T: int, Hq: int, Hkv: int, Dqk: int, Dv: int, Hi: int, Di: int, c: in
     return wl
 
 
+def front_half_inputs(T: int, Di: int, rope_dims: int, cu_seqlens: np.ndarray, seed: int = 0,
+                      base: float = 10000.0, eps: float = 1e-6) -> dict:
+    """Inputs of the indexer front half: RMSNorm weights for queries and keys (float32,
+    U(0.5, 1.5)), eps, and a per-token rotary table [T, rope_dims] laid out as
+    cat(cos, sin). The table is what a model composes for document-local positions p
+    (restarting at every document) with angles p * base^(-i / (rope_dims / 2)); here it
+    is only a seeded input.
+    """
+    rng = np.random.default_rng(seed)
+    q_weight = rng.uniform(0.5, 1.5, Di).astype(np.float32)
+    k_weight = rng.uniform(0.5, 1.5, Di).astype(np.float32)
+    cu = np.asarray(cu_seqlens, np.int64)
+    t = np.arange(T, dtype=np.int64)
+    pos = (t - cu[np.searchsorted(cu, t, side="right") - 1]).astype(np.float64)
+    h = rope_dims // 2
+    ang = pos[:, None] * base ** (-np.arange(h, dtype=np.float64) / h)[None, :]
+    rope = np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+    return dict(q_weight=q_weight, k_weight=k_weight, eps=eps, rope=rope)
+
+
 def random_routes(rng: np.random.Generator, T: int, Tk: int, width: int, cu_seqlens: np.ndarray,
                   frac_invalid: float = 0.25) -> np.ndarray:
     """Arbitrary causal, document-confined routes with -1 holes at random slots.

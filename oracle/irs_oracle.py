@@ -22,6 +22,9 @@ Sources (NVIDIA NeMo AutoModel API reference pages):
   - ``_forward_packed`` description: with packed documents, compression groups
     restart at each document start, visibility is bounded by the document, and
     per-document IDs are offset by the document start (global flattened IDs).
+  - the same class description: the pooled keys then get K RMSNorm and
+    group-start RoPE; ``apply_qsa_rope``: per-token rotary values cat(cos, sin)
+    over the first D_rope dims, the remaining dims unchanged.
   - ``gathered_qsa_gqa_attention`` / ``_gathered_qsa_gqa_attention_chunk``:
     grouped queries [B,Q,Hkv,G,D] attend K/V [B,S,Hkv,D] at the listed global
     IDs; -1 marks invalid slots; the default scale is 1/sqrt(D).
@@ -53,6 +56,11 @@ notes of the repository):
       the top-k like any other block; the tail is then empty.
 * R6  Unstated softmax scales are 1/sqrt(D_qk).
 * R7  A row with no valid route entry produces out = 0 and lse = -inf.
+* R14 RoPE (``apply_qsa_rope``, rotary values laid out as cat(cos, sin)) rotates
+      the pairs (d, d + D_rope/2) of the first D_rope dims (rotate-half).
+* R15 Front half: keys get K RMSNorm and the rotary values of their block's first
+      token; queries get RMSNorm per head and those of their own token; each
+      result is rounded to FP32 and then once to bf16.
 * The FP32 mean is a sequential FP32 sum over the c rows of the block in
   ascending token order, followed by one IEEE division by c.
 * Route entries outside [0, Tk) are padding.
@@ -158,6 +166,67 @@ def pool_keys(kI_bits: np.ndarray, cu_seqlens: np.ndarray, c: int) -> tuple[np.n
 
 
 # --------------------------------------------------------------------------------------
+# a2'' (next): indexer front half (QSA page, indexer class: the FP32 group means get K
+# RMSNorm and group-start RoPE; `apply_qsa_rope`: the rotary values of a token are
+# cat(cos, sin) over the first D_rope dims, the other dims pass through). Readings: the
+# rotation pairs dims d and d + D_rope/2 (rotate-half, R14); queries get RMSNorm per head
+# and the rotary values of their own token; a pooled key gets those of its block's first
+# token; each normalised and rotated vector is rounded to FP32 and then once to bf16 (R15).
+# --------------------------------------------------------------------------------------
+
+
+def rms_norm(x: np.ndarray, weight: np.ndarray, eps: float) -> np.ndarray:
+    """x / sqrt(mean over the last axis of x^2 + eps) * weight, in float64."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * np.asarray(weight, dtype=np.float64)
+
+
+def apply_rope(x: np.ndarray, rope: np.ndarray) -> np.ndarray:
+    """Rotate the first D_rope dims of x [..., D] by rope [..., D_rope] = cat(cos, sin).
+
+    With h = D_rope / 2, dims d and d + h (d < h) form one pair:
+    (x_d, x_{d+h}) -> (x_d cos_d - x_{d+h} sin_d, x_{d+h} cos_d + x_d sin_d).
+    rope broadcasts against x's leading axes (one row per token for all heads).
+    """
+    y = np.array(x, dtype=np.float64, copy=True)
+    r = np.asarray(rope, dtype=np.float64)
+    h = r.shape[-1] // 2
+    cos, sin = r[..., :h], r[..., h:2 * h]
+    x1 = y[..., :h].copy()
+    x2 = y[..., h:2 * h].copy()
+    y[..., :h] = x1 * cos - x2 * sin
+    y[..., h:2 * h] = x2 * cos + x1 * sin
+    return y
+
+
+def to_bf16_values(x64: np.ndarray) -> np.ndarray:
+    """float64 -> float32 (round to nearest even) -> bf16 (round to nearest even), as float64."""
+    return round_to_bf16(np.asarray(x64, dtype=np.float64).astype(np.float32)).astype(np.float64)
+
+
+def block_start_tokens(cu_seqlens: np.ndarray, T: int, c: int) -> np.ndarray:
+    """Global index of the first token of every pooled block, in `pool_keys` order."""
+    starts, ends = doc_bounds(cu_seqlens, T)
+    out = [s + c * np.arange((e - s) // c, dtype=np.int64) for s, e in zip(starts, ends)]
+    return np.concatenate(out) if out else np.zeros(0, np.int64)
+
+
+def front_keys(kI_bits, cu_seqlens, c: int, k_weight, eps: float, rope) -> tuple[np.ndarray, np.ndarray]:
+    """Pooled index keys after K RMSNorm and group-start RoPE, as bf16 values (float64),
+    and the per-document block offsets."""
+    T = kI_bits.shape[0]
+    kbar, blk_off = pool_keys(kI_bits, cu_seqlens, c)
+    first = block_start_tokens(cu_seqlens, T, c)
+    y = apply_rope(rms_norm(kbar.astype(np.float64), k_weight, eps), np.asarray(rope)[first])
+    return to_bf16_values(y), blk_off
+
+
+def front_query_row(qI_t_bits, q_weight, eps: float, rope_t) -> np.ndarray:
+    """Index queries of one token [Hi, Di] after per-head RMSNorm and the token's RoPE."""
+    return to_bf16_values(apply_rope(rms_norm(bf16_to_f64(qI_t_bits), q_weight, eps), rope_t))
+
+
+# --------------------------------------------------------------------------------------
 # a3: visibility and block scores (QSA page `select_qsa_token_ids`; Step-5 sparse page
 # `indexer_score_tile` for the per-head FP32 weights)
 # --------------------------------------------------------------------------------------
@@ -239,13 +308,16 @@ def route_row(doc_start: int, tau: int, c: int, budget: int, scores_f32) -> np.n
 
 
 def index_routes(qI_bits, kI_bits, w, cu_seqlens, c: int, budget: int, rows=None,
-                 want_scores: bool = False, ldS: int | None = None):
+                 want_scores: bool = False, ldS: int | None = None, front: dict | None = None):
     """Indexer routes (and optionally FP32 block scores) for the requested rows.
 
     qI_bits [T, Hi, Di] bf16 bits, kI_bits [T, Di] bf16 bits, w [T, Hi] float32,
     cu_seqlens int [ndocs+1]. Returns int32 routes [len(rows), budget + c - 1];
     with want_scores also float32 scores [len(rows), ldS] (NaN where not scored:
     a row is scored only when more than budget/c blocks are visible).
+    front: optional indexer front half, a dict with q_weight [Di], k_weight [Di], eps and
+    rope [T, D_rope] (per-token cat(cos, sin)); the queries and pooled keys are then
+    normalised and rotated before scoring (`front_query_row`, `front_keys`).
     """
     if budget % c != 0 or budget <= 0 or c <= 0:
         raise ValueError("budget must be a positive multiple of c")
@@ -254,8 +326,11 @@ def index_routes(qI_bits, kI_bits, w, cu_seqlens, c: int, budget: int, rows=None
     rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
     kb = budget // c
     W = budget + c - 1
-    kbar, blk_off = pool_keys(kI_bits, cu_seqlens, c)
-    ktilde = round_to_bf16(kbar).astype(np.float64)
+    if front is None:
+        kbar, blk_off = pool_keys(kI_bits, cu_seqlens, c)
+        ktilde = round_to_bf16(kbar).astype(np.float64)
+    else:
+        ktilde, blk_off = front_keys(kI_bits, cu_seqlens, c, front["k_weight"], front["eps"], front["rope"])
     if ldS is None:
         ldS = int(np.max(ends - starts)) // c
     routes = np.full((rows.shape[0], W), -1, dtype=np.int32)
@@ -268,7 +343,9 @@ def index_routes(qI_bits, kI_bits, w, cu_seqlens, c: int, budget: int, rows=None
         sc = None
         if nv > kb:
             kt = ktilde[blk_off[d]: blk_off[d] + nv]
-            sc = block_scores(bf16_to_f64(qI_bits[t]), np.asarray(w[t], dtype=np.float64), kt)
+            q_t = (bf16_to_f64(qI_bits[t]) if front is None else
+                   front_query_row(qI_bits[t], front["q_weight"], front["eps"], np.asarray(front["rope"])[t]))
+            sc = block_scores(q_t, np.asarray(w[t], dtype=np.float64), kt)
             if want_scores:
                 scores[i, :nv] = sc
         routes[i] = route_row(s, tau, c, budget, sc)

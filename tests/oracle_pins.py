@@ -598,6 +598,120 @@ def pin_attention_bwd_invariants(O):
     assert all(np.all(x == 0) for x in z)
 
 
+# --------------------------------------------------------------------------------------
+# indexer front half: RMSNorm, RoPE, group start
+# --------------------------------------------------------------------------------------
+
+
+def pin_rms_norm_vs_torch(O):
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((5, 3, 64))
+    w = rng.uniform(0.5, 1.5, 64)
+    for eps in (1e-6, 0.1):
+        ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (64,), torch.from_numpy(w), eps).numpy()
+        np.testing.assert_allclose(O.rms_norm(x, w, eps), ref, rtol=1e-12, atol=1e-14)
+
+
+def pin_rope_golden(O):
+    recs = parse_fixture("rope_rotate_half.txt")
+    assert recs[0][0] == "rope"
+    rope = np.asarray([float(v) for v in recs[0][1]])
+    pairs = recs[1:]
+    assert len(pairs) % 2 == 0 and len(pairs) >= 4
+    for (kx, xs), (ko, outs) in zip(pairs[0::2], pairs[1::2]):
+        assert kx == "x" and ko == "out"
+        got = O.apply_rope(np.asarray([float(v) for v in xs]), rope)
+        np.testing.assert_array_equal(got, np.asarray([float(v) for v in outs]))
+
+
+def pin_rope_rotation(O):
+    """Each pair (x_d, x_{d+h}) is the complex number x_d + i x_{d+h} times e^(i theta_d)
+    (numpy complex arithmetic); the inverse rotation restores x; dot products of rotated
+    vectors depend only on the position difference."""
+    rng = np.random.default_rng(32)
+    D, Dr = 16, 8
+    h = Dr // 2
+    x = rng.standard_normal((3, D))
+    theta = rng.uniform(-np.pi, np.pi, (3, h))
+    rope = np.concatenate([np.cos(theta), np.sin(theta)], axis=-1)
+    got = O.apply_rope(x, rope)
+    z = (x[:, :h] + 1j * x[:, h:Dr]) * np.exp(1j * theta)
+    np.testing.assert_allclose(got[:, :h], z.real, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(got[:, h:Dr], z.imag, rtol=0, atol=1e-14)
+    np.testing.assert_array_equal(got[:, Dr:], x[:, Dr:])
+    inv = np.concatenate([np.cos(theta), -np.sin(theta)], axis=-1)
+    np.testing.assert_allclose(O.apply_rope(got, inv), x, rtol=0, atol=1e-14)
+    freq = 1.0 / (10000.0 ** (np.arange(h) / h))
+
+    def table(p):
+        return np.concatenate([np.cos(p * freq), np.sin(p * freq)])
+
+    q, k = rng.standard_normal(D), rng.standard_normal(D)
+    a = O.apply_rope(q, table(7.0)) @ O.apply_rope(k, table(3.0))
+    b = O.apply_rope(q, table(104.0)) @ O.apply_rope(k, table(100.0))
+    assert abs(a - b) <= 1e-9 * max(1.0, abs(a)), (a, b)
+    # one table row rotates all heads of a token alike
+    xh = rng.standard_normal((2, 3, D))
+    rows = np.concatenate([np.cos(theta[:2]), np.sin(theta[:2])], axis=-1)
+    per_head = O.apply_rope(xh, rows[:, None, :])
+    for hd in range(3):
+        np.testing.assert_array_equal(per_head[:, hd], O.apply_rope(xh[:, hd], rows))
+
+
+def pin_front_keys_group_start(O):
+    """The rotary values of exactly one token rotate by 90 degrees (cos 0, sin 1): only the
+    pooled key whose block starts at that token turns, and by an exact swap with negation."""
+    import irs_synth
+
+    T, c, Di = 40, 4, 8
+    cu = np.asarray([0, 13, 40], np.int32)
+    rng = np.random.default_rng(33)
+    kI = irs_synth.f32_to_bf16_bits(rng.standard_normal((T, Di)).astype(np.float32))
+    ident = np.tile(np.asarray([1.0, 1.0, 0.0, 0.0]), (T, 1))
+    ones = np.ones(Di)
+    base, off = O.front_keys(kI, cu, c, ones, 1e-6, ident)
+    for tok, doc, blk in ((17, 1, 1), (8, 0, 2)):              # first token of block 1 of doc 1, block 2 of doc 0
+        rope = ident.copy()
+        rope[tok] = [0.0, 0.0, 1.0, 1.0]
+        got, off2 = O.front_keys(kI, cu, c, ones, 1e-6, rope)
+        np.testing.assert_array_equal(off2, off)
+        row = int(off[doc]) + blk
+        want = base.copy()
+        want[row, 0], want[row, 1], want[row, 2], want[row, 3] = (-base[row, 2], -base[row, 3], base[row, 0],
+                                                                  base[row, 1])
+        np.testing.assert_array_equal(got, want)
+    # a token that starts no block (the second of a block, or past the last whole block) changes nothing
+    for tok in (18, 37, 12):
+        rope = ident.copy()
+        rope[tok] = [0.0, 0.0, 1.0, 1.0]
+        np.testing.assert_array_equal(O.front_keys(kI, cu, c, ones, 1e-6, rope)[0], base)
+
+
+def pin_front_scores_closed_form(O):
+    """Constant keys a and one-hot queries b e_d, unit norm weights, eps 0, identity
+    rotary values: every normalised key dim is 1 and each query head becomes
+    sign(b) sqrt(Di) e_d, so every block scores sqrt(Di) * sum over heads with b > 0 of w."""
+    T, Hi, Di, c, budget = 24, 4, 16, 4, 4
+    kI = exact_bf16_bits(np.full((T, Di), 0.5, np.float32))
+    qv = np.zeros((T, Hi, Di), np.float32)
+    rng = np.random.default_rng(34)
+    sign = np.where(rng.random((T, Hi)) < 0.5, -1.0, 1.0)
+    for t in range(T):
+        for h in range(Hi):
+            qv[t, h, (t + 3 * h) % Di] = sign[t, h] * (0.25 * (1 + h))
+    qI = exact_bf16_bits(qv)
+    w = rng.random((T, Hi), dtype=np.float32)
+    front = dict(q_weight=np.ones(Di), k_weight=np.ones(Di), eps=0.0, rope=np.tile([1.0, 0.0], (T, 1)))
+    cu = np.asarray([0, T], np.int32)
+    _, sc = O.index_routes(qI, kI, w, cu, c, budget, want_scores=True, front=front)
+    for t in range(T):
+        nv = (t + 1) // c
+        if nv <= budget // c:
+            continue
+        want = np.float32(4.0 * np.sum(w[t].astype(np.float64) * (sign[t] > 0)))
+        np.testing.assert_array_equal(sc[t, :nv], np.full(nv, want, np.float32))
+
+
 def pin_window_compose(O):
     rng = np.random.default_rng(4)
     cu = np.asarray([0, 30, 100], np.int32)
@@ -641,4 +755,9 @@ ALL_PINS = [
     pin_latent_attention_bwd,
     pin_attention_bwd_finite_diff,
     pin_attention_bwd_invariants,
+    pin_rms_norm_vs_torch,
+    pin_rope_golden,
+    pin_rope_rotation,
+    pin_front_keys_group_start,
+    pin_front_scores_closed_form,
 ]

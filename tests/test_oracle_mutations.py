@@ -174,8 +174,52 @@ def _latent_bwd_no_value_grad(q_bits, kv_bits, routes, scale, dout_bits, Dv=512,
     return dq, dk
 
 
+def _rope_interleaved(x, rope):
+    y = np.array(x, dtype=np.float64, copy=True)
+    r = np.asarray(rope, dtype=np.float64)
+    h = r.shape[-1] // 2
+    cos, sin = r[..., :h], r[..., h:2 * h]
+    x1 = y[..., 0:2 * h:2].copy()
+    x2 = y[..., 1:2 * h:2].copy()
+    y[..., 0:2 * h:2] = x1 * cos - x2 * sin
+    y[..., 1:2 * h:2] = x2 * cos + x1 * sin
+    return y
+
+
+def _rope_sign_flipped(x, rope):
+    r = np.array(rope, dtype=np.float64, copy=True)
+    h = r.shape[-1] // 2
+    r[..., h:2 * h] *= -1.0
+    return _REAL_ROPE(x, r)
+
+
+def _rms_norm_no_eps(x, weight, eps):
+    return _REAL_RMS(x, weight, 0.0)
+
+
+def _rms_norm_mean_abs(x, weight, eps):
+    x = np.asarray(x, dtype=np.float64)
+    return x / (np.mean(np.abs(x), axis=-1, keepdims=True) + eps) * np.asarray(weight, dtype=np.float64)
+
+
+def _block_end_tokens(cu_seqlens, T, c):
+    return _REAL_STARTS(cu_seqlens, T, c) + (c - 1)
+
+
+def _block_starts_without_doc_offset(cu_seqlens, T, c):
+    starts, ends = O.doc_bounds(cu_seqlens, T)
+    return np.concatenate([c * np.arange((e - s) // c, dtype=np.int64) for s, e in zip(starts, ends)])
+
+
+def _front_query_without_norm(qI_t_bits, q_weight, eps, rope_t):
+    return O.to_bf16_values(O.apply_rope(O.bf16_to_f64(qI_t_bits), rope_t))
+
+
 _REAL_ATTEND = O.attend_row
 _REAL_COMPOSE = O.compose_window
+_REAL_ROPE = O.apply_rope
+_REAL_RMS = O.rms_norm
+_REAL_STARTS = O.block_start_tokens
 
 MUTATIONS = {
     "visibility_off_by_one": ("visible_blocks", lambda tau, c: tau // c),
@@ -202,6 +246,13 @@ MUTATIONS = {
     "bwd_dk_group_modulo": ("attend_row_grad", _row_grad_variant(key_group=lambda h, Hq, Hkv: h % Hkv)),
     "bwd_scatter_overwrites": ("attention_bwd", _bwd_scatter_overwrites),
     "bwd_latent_drops_value_grad": ("latent_attention_bwd", _latent_bwd_no_value_grad),
+    "rope_interleaved_pairs": ("apply_rope", _rope_interleaved),
+    "rope_sign_flipped": ("apply_rope", _rope_sign_flipped),
+    "rms_norm_without_eps": ("rms_norm", _rms_norm_no_eps),
+    "rms_norm_mean_abs": ("rms_norm", _rms_norm_mean_abs),
+    "rope_at_block_end": ("block_start_tokens", _block_end_tokens),
+    "rope_block_start_without_doc_offset": ("block_start_tokens", _block_starts_without_doc_offset),
+    "front_query_without_norm": ("front_query_row", _front_query_without_norm),
 }
 
 

@@ -54,3 +54,19 @@ def test_random_routes_are_document_confined():
         s = 0 if t < 10 else 10
         v = r[t][r[t] >= 0]
         assert v.shape[0] >= 1 and np.all((v >= s) & (v <= t)) and len(set(v.tolist())) == v.shape[0]
+
+
+def test_front_half_inputs():
+    cu = np.asarray([0, 5, 12], np.int32)
+    a = irs_synth.front_half_inputs(12, 16, 8, cu, seed=3)
+    b = irs_synth.front_half_inputs(12, 16, 8, cu, seed=3)
+    for k in ("q_weight", "k_weight", "rope"):
+        np.testing.assert_array_equal(a[k], b[k])
+    assert a["rope"].shape == (12, 8) and a["rope"].dtype == np.float32
+    cos, sin = a["rope"][:, :4].astype(np.float64), a["rope"][:, 4:].astype(np.float64)
+    np.testing.assert_allclose(cos * cos + sin * sin, 1.0, atol=1e-6)
+    # document-local positions: position 0 at every document start (angle 0), then growing
+    for t in (0, 5):
+        np.testing.assert_array_equal(a["rope"][t], [1, 1, 1, 1, 0, 0, 0, 0])
+    np.testing.assert_array_equal(a["rope"][6], a["rope"][1])
+    assert 0.5 <= a["q_weight"].min() and a["k_weight"].max() <= 1.5
