@@ -30,8 +30,9 @@ Sources (NVIDIA NeMo AutoModel API reference pages):
     IDs; -1 marks invalid slots; the default scale is 1/sqrt(D).
 * "nemo_automodel.components.models.step5.sparse" (the Step-5 sparse page):
   ``indexer_score_tile`` fuses weighted-ReLU scoring with FP32 per-head weights
-  into an FP32 score tile; ``pack_region_bitmap`` packs selected region IDs into
-  32-bit words.
+  into an FP32 score tile (per KV group, with signed weights and E4M3-rounded
+  operands); ``Step5SparseIndexer.forward`` returns region IDs per KV group;
+  ``pack_region_bitmap`` packs selected region IDs into 32-bit words.
 * "nemo_automodel.components.models.step5.fa4" (``heads_per_group``):
   consecutive query heads share one KV group.
 * "nemo_automodel.components.models.common.cudnn_sparse_attention":
@@ -61,6 +62,8 @@ notes of the repository):
 * R15 Front half: keys get K RMSNorm and the rotary values of their block's first
       token; queries get RMSNorm per head and those of their own token; each
       result is rounded to FP32 and then once to bf16.
+* R16 E4M3 operands (Step-5): queries are rounded bf16 -> E4M3 and pooled keys
+      FP32 -> bf16 -> E4M3, ties to even, saturating past 448.
 * The FP32 mean is a sequential FP32 sum over the c rows of the block in
   ascending token order, followed by one IEEE division by c.
 * Route entries outside [0, Tk) are padding.
@@ -308,7 +311,8 @@ def route_row(doc_start: int, tau: int, c: int, budget: int, scores_f32) -> np.n
 
 
 def index_routes(qI_bits, kI_bits, w, cu_seqlens, c: int, budget: int, rows=None,
-                 want_scores: bool = False, ldS: int | None = None, front: dict | None = None):
+                 want_scores: bool = False, ldS: int | None = None, front: dict | None = None,
+                 operands: str = "bf16"):
     """Indexer routes (and optionally FP32 block scores) for the requested rows.
 
     qI_bits [T, Hi, Di] bf16 bits, kI_bits [T, Di] bf16 bits, w [T, Hi] float32,
@@ -318,7 +322,11 @@ def index_routes(qI_bits, kI_bits, w, cu_seqlens, c: int, budget: int, rows=None
     front: optional indexer front half, a dict with q_weight [Di], k_weight [Di], eps and
     rope [T, D_rope] (per-token cat(cos, sin)); the queries and pooled keys are then
     normalised and rotated before scoring (`front_query_row`, `front_keys`).
+    operands: "bf16", or "e4m3" for the Step-5 scoring operands: the bf16 queries and
+    bf16 pooled keys are further rounded to FP8 E4M3 values (`round_to_e4m3`).
     """
+    if operands not in ("bf16", "e4m3"):
+        raise ValueError("operands must be 'bf16' or 'e4m3'")
     if budget % c != 0 or budget <= 0 or c <= 0:
         raise ValueError("budget must be a positive multiple of c")
     T = qI_bits.shape[0]
@@ -331,6 +339,8 @@ def index_routes(qI_bits, kI_bits, w, cu_seqlens, c: int, budget: int, rows=None
         ktilde = round_to_bf16(kbar).astype(np.float64)
     else:
         ktilde, blk_off = front_keys(kI_bits, cu_seqlens, c, front["k_weight"], front["eps"], front["rope"])
+    if operands == "e4m3":
+        ktilde = round_to_e4m3(ktilde)
     if ldS is None:
         ldS = int(np.max(ends - starts)) // c
     routes = np.full((rows.shape[0], W), -1, dtype=np.int32)
@@ -345,6 +355,8 @@ def index_routes(qI_bits, kI_bits, w, cu_seqlens, c: int, budget: int, rows=None
             kt = ktilde[blk_off[d]: blk_off[d] + nv]
             q_t = (bf16_to_f64(qI_bits[t]) if front is None else
                    front_query_row(qI_bits[t], front["q_weight"], front["eps"], np.asarray(front["rope"])[t]))
+            if operands == "e4m3":
+                q_t = round_to_e4m3(q_t)
             sc = block_scores(q_t, np.asarray(w[t], dtype=np.float64), kt)
             if want_scores:
                 scores[i, :nv] = sc
@@ -366,6 +378,67 @@ def routes_from_scores(scores: np.ndarray, cu_seqlens, T: int, c: int, budget: i
         sc = scores[t, :nv] if nv > kb else None
         out[i] = route_row(s, tau, c, budget, sc)
     return out
+
+
+# --------------------------------------------------------------------------------------
+# Step-5 variants (Step-5 sparse page): `indexer_score_tile` scores
+# [batch, groups, queries, regions] from queries [..., groups, heads, dim] and signed FP32
+# head weights [..., groups, heads] against shared region summaries, and
+# `Step5SparseIndexer.forward` returns region IDs per KV group; its scoring operands are
+# "E4M3-rounded BF16" queries and summaries.
+# --------------------------------------------------------------------------------------
+
+
+def round_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """Nearest FP8 E4M3 value of each element (1 sign, 4 exponent bits with bias 7, 3
+    mantissa bits: normals 2^-6 .. 448, subnormals k * 2^-9), ties to even. Magnitudes
+    past 448 saturate (reading R16). Returns float64."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(a)                               # a = m * 2^ex, 0.5 <= m < 1 (ex = 0 for 0)
+    e = np.maximum(ex.astype(np.float64) - 1.0, -6.0)  # exponent of the leading bit; subnormal floor
+    quantum = np.exp2(e - 3.0)                        # spacing of E4M3 values at that exponent
+    q = np.minimum(np.round(a / quantum) * quantum, 448.0)   # numpy rounds halves to even
+    return np.copysign(q, x)
+
+
+def index_routes_grouped(qI_bits, kI_bits, w, cu_seqlens, c: int, budget: int, rows=None,
+                         operands: str = "bf16") -> np.ndarray:
+    """Per-KV-group routes int32 [len(rows), G, budget + c - 1].
+
+    qI_bits [T, G, Hi, Di], w [T, G, Hi] (signed allowed): the heads and weights of group g
+    score the shared pooled keys and group g selects its own blocks, each group exactly as
+    `index_routes` does for one.
+    """
+    G = qI_bits.shape[1]
+    return np.stack([index_routes(qI_bits[:, g], kI_bits, np.asarray(w)[:, g], cu_seqlens, c, budget, rows=rows,
+                                  operands=operands) for g in range(G)], axis=1)
+
+
+def attention_grouped(q_bits, k_bits, v_bits, routes_g, scale: float, rows=None):
+    """Sparse attention with per-KV-group routes [T, Hkv, W]: the query heads of KV head g
+    attend the IDs of routes_g[t, g]. Returns out float32 [len(rows), Hq, Dv], lse float32."""
+    T, Hq, _ = q_bits.shape
+    Tk, Hkv, _ = k_bits.shape
+    Dv = v_bits.shape[2]
+    if Hq % Hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    if not scale > 0:
+        raise ValueError("scale must be positive")
+    G = Hq // Hkv
+    rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
+    out = np.zeros((rows.shape[0], Hq, Dv), dtype=np.float32)
+    lse = np.zeros((rows.shape[0], Hq), dtype=np.float32)
+    for i, t in enumerate(rows):
+        for g in range(Hkv):
+            ids = np.asarray(routes_g[t, g], dtype=np.int64)
+            ids = ids[(ids >= 0) & (ids < Tk)]
+            hs = slice(g * G, (g + 1) * G)
+            o, l = attend_row(bf16_to_f64(q_bits[t, hs]), bf16_to_f64(k_bits[ids, g:g + 1]),
+                              bf16_to_f64(v_bits[ids, g:g + 1]), scale, 1)
+            out[i, hs] = o.astype(np.float32)
+            lse[i, hs] = l.astype(np.float32)
+    return out, lse
 
 
 # --------------------------------------------------------------------------------------

@@ -712,6 +712,128 @@ def pin_front_scores_closed_form(O):
         np.testing.assert_array_equal(sc[t, :nv], np.full(nv, want, np.float32))
 
 
+# --------------------------------------------------------------------------------------
+# Step-5 variants: E4M3 operands, per-KV-group routes
+# --------------------------------------------------------------------------------------
+
+
+def torch_e4m3(x) -> np.ndarray:
+    """Library rounding: torch's float32 -> float8_e4m3fn cast (in-range values)."""
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def pin_e4m3_vs_torch(O):
+    # every finite E4M3 value is its own rounding
+    codes = torch.arange(256, dtype=torch.int16).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    codes = codes[np.isfinite(codes)]
+    np.testing.assert_array_equal(O.round_to_e4m3(codes), codes)
+    # random magnitudes from the subnormals to the top of the range, and exact halfway points
+    rng = np.random.default_rng(35)
+    x = (rng.standard_normal(20000) * np.exp2(rng.uniform(-12, 8.5, 20000))).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    pos = np.sort(codes[codes > 0])
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
+    for v in (x, mids, -mids):
+        np.testing.assert_array_equal(O.round_to_e4m3(v.astype(np.float64)), torch_e4m3(v))
+
+
+def pin_e4m3_scores(O):
+    """Constant keys a and one-hot queries b: the score is w * ReLU(e4m3(b) * e4m3(bf16(a)))
+    with torch's casts; bf16 operands give w * ReLU(b * bf16(a))."""
+    T, Hi, Di, c, budget = 20, 2, 8, 4, 4
+    a = np.float32(0.3)
+    kI = torch_bf16_bits(np.full((T, Di), a, np.float32))
+    rng = np.random.default_rng(36)
+    qv = np.zeros((T, Hi, Di), np.float32)
+    bvals = np.asarray([0.71875, -1.3125], np.float32)            # exact in bf16, not in E4M3
+    for t in range(T):
+        for h in range(Hi):
+            qv[t, h, (t + h) % Di] = bvals[h]
+    qI = exact_bf16_bits(qv)
+    w = rng.random((T, Hi), dtype=np.float32)
+    cu = np.asarray([0, T], np.int32)
+    abf = bits_to_f64(torch_bf16_bits(np.asarray([a])))[0]
+    for operands, qk in (("e4m3", torch_e4m3(bvals) * torch_e4m3(np.asarray([abf]))[0]),
+                         ("bf16", bvals.astype(np.float64) * abf)):
+        _, sc = O.index_routes(qI, kI, w, cu, c, budget, want_scores=True, operands=operands)
+        for t in range(T):
+            nv = (t + 1) // c
+            if nv <= budget // c:
+                continue
+            want = np.float32(np.sum(w[t].astype(np.float64) * np.maximum(qk, 0.0)))
+            np.testing.assert_array_equal(sc[t, :nv], np.full(nv, want, np.float32))
+
+
+def pin_grouped_routes(O):
+    """Group g has two heads reading key dims g and g + 1 (one-hot queries) with its own
+    weights, one of them negative: its blocks are the brute-force top-k of
+    w0 ReLU(mean_g) + w1 ReLU(mean_{g+1}). Keys are multiples of 1/4 and the weights
+    binary fractions, so means and scores are exact. Identical groups reproduce the
+    shared routes."""
+    T, G, Di, c, budget = 30, 3, 4, 2, 6
+    kb = budget // c
+    rng = np.random.default_rng(37)
+    kv = rng.integers(-16, 17, size=(T, Di)).astype(np.float32) / 4
+    kI = exact_bf16_bits(kv)
+    qv = np.zeros((T, G, 2, Di), np.float32)
+    for g in range(G):
+        qv[:, g, 0, g] = 1.0
+        qv[:, g, 1, (g + 1) % Di] = 1.0
+    qI = exact_bf16_bits(qv)
+    wg = np.asarray([[0.5, 2.0], [1.0, 1.5], [1.5, -1.0]], np.float32)
+    w = np.tile(wg[None], (T, 1, 1))
+    cu = np.asarray([0, 11, T], np.int32)
+    got = O.index_routes_grouped(qI, kI, w, cu, c, budget)
+    assert got.shape == (T, G, budget + c - 1)
+    for t in range(T):
+        s, _ = doc_start_of(cu, t)
+        nv = (t - s + 1) // c
+        for g in range(G):
+            sc = []
+            for b in range(nv):
+                m = kv[s + b * c: s + b * c + c].astype(np.float64).mean(axis=0)
+                sc.append(wg[g, 0] * max(0.0, m[g]) + wg[g, 1] * max(0.0, m[(g + 1) % Di]))
+            blocks = brute_force_topk(np.asarray(sc, np.float32), kb) if nv > kb else tuple(range(nv))
+            ids = sorted(s + b * c + j for b in blocks for j in range(c))
+            assert got[t, g, :len(ids)].tolist() == ids, (t, g)
+            assert np.all(got[t, g, len(ids):budget] == -1)
+    same = O.index_routes_grouped(np.repeat(qI[:, :1], G, axis=1), kI, np.repeat(w[:, :1], G, axis=1), cu, c, budget)
+    shared = O.index_routes(qI[:, 0], kI, w[:, 0], cu, c, budget)
+    for g in range(G):
+        np.testing.assert_array_equal(same[:, g], shared)
+
+
+def pin_grouped_attention(O):
+    """Per-group routes against SDPA with a per-head mask; identical groups reduce to the
+    shared-route attention."""
+    import irs_synth
+
+    T, Hq, Hkv, D = 30, 6, 3, 16
+    wl = irs_synth.custom(T, Hq, Hkv, D, D, 2, 8, 4, 8, doc_lens=[12, 18], seed=38)
+    q, k, v = wl.arrays["q"], wl.arrays["k"], wl.arrays["v"]
+    rng = np.random.default_rng(38)
+    rg = np.stack([irs_synth.random_routes(rng, T, T, 9, wl.cu_seqlens) for _ in range(Hkv)], axis=1)
+    out, lse = O.attention_grouped(q, k, v, rg, 0.25)
+    G = Hq // Hkv
+    mask = torch.zeros(Hq, T, T, dtype=torch.bool)
+    for t in range(T):
+        for h in range(Hq):
+            ids = [int(x) for x in rg[t, h // G] if 0 <= int(x) < T]
+            mask[h, t, ids] = True
+    qq = torch.from_numpy(bits_to_f64(q)).permute(1, 0, 2)
+    kk = torch.from_numpy(bits_to_f64(k)).repeat_interleave(G, dim=1).permute(1, 0, 2)
+    vv = torch.from_numpy(bits_to_f64(v)).repeat_interleave(G, dim=1).permute(1, 0, 2)
+    ref = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=0.25)
+    np.testing.assert_allclose(out, ref.permute(1, 0, 2).numpy(), rtol=1e-5, atol=1e-6)
+    sc = (qq @ kk.transpose(1, 2) * 0.25).masked_fill(~mask, float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(sc, dim=-1).T.numpy(), rtol=1e-5, atol=1e-6)
+    r1 = rg[:, 0]
+    o1, l1 = O.attention_grouped(q, k, v, np.repeat(r1[:, None], Hkv, axis=1), 0.25)
+    o2, l2 = O.attention(q, k, v, r1, 0.25)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
 def pin_window_compose(O):
     rng = np.random.default_rng(4)
     cu = np.asarray([0, 30, 100], np.int32)
@@ -760,4 +882,8 @@ ALL_PINS = [
     pin_rope_rotation,
     pin_front_keys_group_start,
     pin_front_scores_closed_form,
+    pin_e4m3_vs_torch,
+    pin_e4m3_scores,
+    pin_grouped_routes,
+    pin_grouped_attention,
 ]

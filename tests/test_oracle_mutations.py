@@ -215,7 +215,40 @@ def _front_query_without_norm(qI_t_bits, q_weight, eps, rope_t):
     return O.to_bf16_values(O.apply_rope(O.bf16_to_f64(qI_t_bits), rope_t))
 
 
+def _e4m3_variant(subnormals=True, ties_even=True, mant_bits=3):
+    def rnd(x):
+        x = np.asarray(x, dtype=np.float64)
+        a = np.abs(x)
+        _, ex = np.frexp(a)
+        e = np.maximum(ex.astype(np.float64) - 1.0, -6.0)
+        quantum = np.exp2(e - mant_bits)
+        r = np.round(a / quantum) if ties_even else np.floor(a / quantum + 0.5)
+        q = np.minimum(r * quantum, 448.0)
+        if not subnormals:
+            q = np.where(a < 2.0 ** -6, 0.0, q)
+        return np.copysign(q, x)
+    return rnd
+
+
+def _grouped_routes_shared_weights(qI_bits, kI_bits, w, cu_seqlens, c, budget, rows=None, operands="bf16"):
+    G = qI_bits.shape[1]
+    return np.stack([O.index_routes(qI_bits[:, g], kI_bits, np.asarray(w)[:, 0], cu_seqlens, c, budget, rows=rows,
+                                    operands=operands) for g in range(G)], axis=1)
+
+
+def _grouped_routes_first_group(qI_bits, kI_bits, w, cu_seqlens, c, budget, rows=None, operands="bf16"):
+    r = O.index_routes(qI_bits[:, 0], kI_bits, np.asarray(w)[:, 0], cu_seqlens, c, budget, rows=rows,
+                       operands=operands)
+    return np.repeat(r[:, None], qI_bits.shape[1], axis=1)
+
+
+def _grouped_attention_group0(q_bits, k_bits, v_bits, routes_g, scale, rows=None):
+    return _REAL_GROUPED_ATTN(q_bits, k_bits, v_bits, np.repeat(routes_g[:, :1], routes_g.shape[1], axis=1), scale,
+                              rows)
+
+
 _REAL_ATTEND = O.attend_row
+_REAL_GROUPED_ATTN = O.attention_grouped
 _REAL_COMPOSE = O.compose_window
 _REAL_ROPE = O.apply_rope
 _REAL_RMS = O.rms_norm
@@ -253,6 +286,13 @@ MUTATIONS = {
     "rope_at_block_end": ("block_start_tokens", _block_end_tokens),
     "rope_block_start_without_doc_offset": ("block_start_tokens", _block_starts_without_doc_offset),
     "front_query_without_norm": ("front_query_row", _front_query_without_norm),
+    "e4m3_flushes_subnormals": ("round_to_e4m3", _e4m3_variant(subnormals=False)),
+    "e4m3_ties_away_from_zero": ("round_to_e4m3", _e4m3_variant(ties_even=False)),
+    "e4m3_four_mantissa_bits": ("round_to_e4m3", _e4m3_variant(mant_bits=4)),
+    "e4m3_not_applied": ("round_to_e4m3", lambda x: np.asarray(x, dtype=np.float64)),
+    "grouped_routes_shared_weights": ("index_routes_grouped", _grouped_routes_shared_weights),
+    "grouped_routes_first_group_only": ("index_routes_grouped", _grouped_routes_first_group),
+    "grouped_attention_first_group_routes": ("attention_grouped", _grouped_attention_group0),
 }
 
 
