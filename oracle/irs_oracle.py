@@ -385,7 +385,7 @@ def routes_from_scores(scores: np.ndarray, cu_seqlens, T: int, c: int, budget: i
 # [batch, groups, queries, regions] from queries [..., groups, heads, dim] and signed FP32
 # head weights [..., groups, heads] against shared region summaries, and
 # `Step5SparseIndexer.forward` returns region IDs per KV group; its scoring operands are
-# "E4M3-rounded BF16" queries and summaries.
+# bf16 queries and summaries whose values were rounded to FP8 E4M3.
 # --------------------------------------------------------------------------------------
 
 
