@@ -307,6 +307,8 @@ def sparse_gqa_attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, route
         scale = 1.0 / math.sqrt(Dqk)
     dev = q.device
     shared = _values_alias_keys(k, v) and Dv <= Dqk
+    if shared and dv is not None:
+        raise ValueError("v is a view of k: the shared row gradient is returned as dk, so dv must be None")
     if dq is None:
         dq = torch.empty((T, Hq, Dqk), dtype=torch.float32, device=dev)
     if dk is None:
