@@ -12,7 +12,8 @@
  *      document, a weighted-ReLU score per (query, visible block) on tensor cores,
  *      and a per-query top-k over blocks;
  *   2. expansion of the chosen blocks into an int32 route row of global token IDs;
- *   3. attention forward over exactly the routed keys and values.
+ *   3. attention forward over exactly the routed keys and values;
+ *   4. its backward (query, key and value gradients over the same routes).
  *
  * Conventions for every call
  *   - All tensor pointers are DEVICE pointers unless stated otherwise, owned by the
@@ -147,8 +148,8 @@ irs_status irs_topk_from_scores(const float* scores, int64_t ld_scores, const in
                                 irs_stream_t stream);
 
 /*
- * Sliding window in front of an indexer route (Step-5 layers page: GQA with windowed
- * or CSA-selected keys; the windowed workload combines both).
+ * Sliding window in front of an indexer route (Step-5 layers page: the attention keys
+ * come from a sliding window or from the CSA selection; the windowed workload uses both).
  *   out[t, j]          = t - window + 1 + j if that token is in t's document, else -1
  *   out[t, window + j] = route_ids[t, j] if it is < t - window + 1, else -1
  * so the composed row never repeats an ID.

@@ -10,18 +10,18 @@ at a time.
 Sources (NVIDIA NeMo AutoModel API reference pages):
 
 * "nemo_automodel.components.models.qwen3_8_flash_next.qsa" (the QSA page):
-  - ``Qwen3_8_FlashNextQSAIndexer`` class description: raw index keys
-    [B,S,1,D_index]; complete consecutive groups of ``compress_ratio`` keys are
-    averaged in FP32 into [B, floor(S/c), 1, D_index]; the route tensor is
-    [B, S, budget + c - 1].
-  - ``select_qsa_token_ids`` description: a query at position t sees
-    floor((t+1)/c) complete blocks; each block is scored by a sum over index
-    heads of ReLU(q_h . k_block); the best budget/c blocks are expanded to token
-    IDs and the 0..c-1 tokens of the current incomplete block are appended;
-    invalid slots are -1.
-  - ``_forward_packed`` description: with packed documents, compression groups
-    restart at each document start, visibility is bounded by the document, and
-    per-document IDs are offset by the document start (global flattened IDs).
+  - ``Qwen3_8_FlashNextQSAIndexer`` class description: the raw index keys
+    [B,S,1,D_index] are pooled by an FP32 mean over each whole run of
+    ``compress_ratio`` consecutive keys, giving [B, floor(S/c), 1, D_index]; a
+    route row has budget + c - 1 entries ([B, S, budget + c - 1]).
+  - ``select_qsa_token_ids`` description: the query at position t can see
+    floor((t+1)/c) whole blocks, each scored as a head sum of
+    ReLU(q_h . k_block); the budget/c highest-scoring blocks turn into their
+    token IDs, followed by the 0..c-1 tokens of the query's unfinished block;
+    unused slots hold -1.
+  - ``_forward_packed`` description: for packed documents the pooling runs
+    start over in each document, a query sees only its own document, and IDs
+    are positions in the flattened sequence (document start + local offset).
   - the same class description: the pooled keys then get K RMSNorm and
     group-start RoPE; ``apply_qsa_rope``: per-token rotary values cat(cos, sin)
     over the first D_rope dims, the remaining dims unchanged.
@@ -114,7 +114,7 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
 
 # --------------------------------------------------------------------------------------
 # a1: document layout (QSA page, `_forward_packed`: cu_seqlens strictly increasing,
-# starting at zero and ending at T)
+# from 0 up to T)
 # --------------------------------------------------------------------------------------
 
 
