@@ -238,7 +238,7 @@ def custom(T: int, Hq: int, Hkv: int, Dqk: int, Dv: int, Hi: int, Di: int, c: in
 def front_half_inputs(T: int, Di: int, rope_dims: int, cu_seqlens: np.ndarray, seed: int = 0,
                       base: float = 10000.0, eps: float = 1e-6) -> dict:
     """Inputs of the indexer front half: RMSNorm weights for queries and keys (float32,
-    U(0.5, 1.5)), eps, and a per-token rotary table [T, rope_dims] laid out as
+    U(0.5, 1.5)), eps, and a per-token rotary table [T, rope_dims] stored as
     cat(cos, sin). The table is what a model composes for document-local positions p
     (restarting at every document) with angles p * base^(-i / (rope_dims / 2)); here it
     is only a seeded input.

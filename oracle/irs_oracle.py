@@ -47,7 +47,7 @@ notes of the repository):
 * R1  The FP32 block mean is rounded once to bf16 (round to nearest even)
       before it is used as a scoring operand (the scores are tensor-core dot
       products of bf16 operands).
-* R2  The block score is sum_h w[t,h] * ReLU(q[t,h] . k~[b]) with no extra
+* R2  Each block scores sum_h w[t,h] * ReLU(q[t,h] . k~[b]) with no extra
       1/sqrt(D) factor: a caller who wants one folds it into w.
 * R3  Top-k ties go to the lower block index; -0.0 equals +0.0.
 * R4  A route row has fixed sections: slots [0, budget) hold the selected blocks
@@ -57,7 +57,7 @@ notes of the repository):
       the top-k like any other block; the tail is then empty.
 * R6  Unstated softmax scales are 1/sqrt(D_qk).
 * R7  A row with no valid route entry produces out = 0 and lse = -inf.
-* R14 RoPE (``apply_qsa_rope``, rotary values laid out as cat(cos, sin)) rotates
+* R14 RoPE (``apply_qsa_rope``, rotary values stored as cat(cos, sin)) rotates
       the pairs (d, d + D_rope/2) of the first D_rope dims (rotate-half).
 * R15 Front half: keys get K RMSNorm and the rotary values of their block's first
       token; queries get RMSNorm per head and those of their own token; each
