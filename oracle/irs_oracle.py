@@ -60,8 +60,9 @@ notes of the repository):
 * R14 RoPE (``apply_qsa_rope``, rotary values stored as cat(cos, sin)) rotates
       the pairs (d, d + D_rope/2) of the first D_rope dims (rotate-half).
 * R15 Front half: keys get K RMSNorm and the rotary values of their block's first
-      token; queries get RMSNorm per head and those of their own token; each
-      result is rounded to FP32 and then once to bf16.
+      token; queries get RMSNorm per head and those of their own token; the
+      transform is evaluated in FP32 (sum of squares in ascending dim order, no
+      fused multiply-add) and rounded once to bf16.
 * R16 E4M3 operands (Step-5): queries are rounded bf16 -> E4M3 and pooled keys
       FP32 -> bf16 -> E4M3, ties to even, saturating past 448.
 * The FP32 mean is a sequential FP32 sum over the c rows of the block in
@@ -174,37 +175,40 @@ def pool_keys(kI_bits: np.ndarray, cu_seqlens: np.ndarray, c: int) -> tuple[np.n
 # cat(cos, sin) over the first D_rope dims, the other dims pass through). Readings: the
 # rotation pairs dims d and d + D_rope/2 (rotate-half, R14); queries get RMSNorm per head
 # and the rotary values of their own token; a pooled key gets those of its block's first
-# token; each normalised and rotated vector is rounded to FP32 and then once to bf16 (R15).
+# token; the transform is evaluated in FP32, the precision of the kernels that round its
+# result to the bf16 scoring operand, with the sum of squares in ascending dim order and
+# every operation rounded to float32 (no fused multiply-add), then rounded once to bf16
+# (R15; the pooled mean follows the same rule, R1).
 # --------------------------------------------------------------------------------------
 
 
 def rms_norm(x: np.ndarray, weight: np.ndarray, eps: float) -> np.ndarray:
-    """x / sqrt(mean over the last axis of x^2 + eps) * weight, in float64."""
-    x = np.asarray(x, dtype=np.float64)
-    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * np.asarray(weight, dtype=np.float64)
+    """RMSNorm over the last axis in float32: ss = sum of x_d * x_d in ascending d,
+    r = sqrt(ss / D + eps), y_d = (x_d / r) * weight_d, each operation rounded to float32."""
+    x = np.asarray(x, dtype=np.float32)
+    D = x.shape[-1]
+    ss = np.zeros(x.shape[:-1], dtype=np.float32)
+    for d in range(D):
+        ss = (ss + (x[..., d] * x[..., d]).astype(np.float32)).astype(np.float32)
+    r = np.sqrt(((ss / np.float32(D)).astype(np.float32) + np.float32(eps)).astype(np.float32)).astype(np.float32)
+    return ((x / r[..., None]).astype(np.float32) * np.asarray(weight, dtype=np.float32)).astype(np.float32)
 
 
 def apply_rope(x: np.ndarray, rope: np.ndarray) -> np.ndarray:
-    """Rotate the first D_rope dims of x [..., D] by rope [..., D_rope] = cat(cos, sin).
-
-    With h = D_rope / 2, dims d and d + h (d < h) form one pair:
-    (x_d, x_{d+h}) -> (x_d cos_d - x_{d+h} sin_d, x_{d+h} cos_d + x_d sin_d).
-    rope broadcasts against x's leading axes (one row per token for all heads).
-    """
-    y = np.array(x, dtype=np.float64, copy=True)
-    r = np.asarray(rope, dtype=np.float64)
+    """Rotate the first D_rope dims of x [..., D] by rope [..., D_rope] = cat(cos, sin), in
+    float32. With h = D_rope / 2, dims d and d + h (d < h) form one pair:
+    (x_d, x_{d+h}) -> (x_d cos_d - x_{d+h} sin_d, x_{d+h} cos_d + x_d sin_d),
+    each product and each sum rounded to float32. rope broadcasts against x's leading axes
+    (one row per token for all heads)."""
+    y = np.array(x, dtype=np.float32, copy=True)
+    r = np.asarray(rope, dtype=np.float32)
     h = r.shape[-1] // 2
     cos, sin = r[..., :h], r[..., h:2 * h]
     x1 = y[..., :h].copy()
     x2 = y[..., h:2 * h].copy()
-    y[..., :h] = x1 * cos - x2 * sin
-    y[..., h:2 * h] = x2 * cos + x1 * sin
+    y[..., :h] = (x1 * cos).astype(np.float32) - (x2 * sin).astype(np.float32)
+    y[..., h:2 * h] = (x2 * cos).astype(np.float32) + (x1 * sin).astype(np.float32)
     return y
-
-
-def to_bf16_values(x64: np.ndarray) -> np.ndarray:
-    """float64 -> float32 (round to nearest even) -> bf16 (round to nearest even), as float64."""
-    return round_to_bf16(np.asarray(x64, dtype=np.float64).astype(np.float32)).astype(np.float64)
 
 
 def block_start_tokens(cu_seqlens: np.ndarray, T: int, c: int) -> np.ndarray:
@@ -220,13 +224,15 @@ def front_keys(kI_bits, cu_seqlens, c: int, k_weight, eps: float, rope) -> tuple
     T = kI_bits.shape[0]
     kbar, blk_off = pool_keys(kI_bits, cu_seqlens, c)
     first = block_start_tokens(cu_seqlens, T, c)
-    y = apply_rope(rms_norm(kbar.astype(np.float64), k_weight, eps), np.asarray(rope)[first])
-    return to_bf16_values(y), blk_off
+    y = apply_rope(rms_norm(kbar, k_weight, eps), np.asarray(rope)[first])
+    return round_to_bf16(y).astype(np.float64), blk_off
 
 
 def front_query_row(qI_t_bits, q_weight, eps: float, rope_t) -> np.ndarray:
-    """Index queries of one token [Hi, Di] after per-head RMSNorm and the token's RoPE."""
-    return to_bf16_values(apply_rope(rms_norm(bf16_to_f64(qI_t_bits), q_weight, eps), rope_t))
+    """Index queries of one token [Hi, Di] after per-head RMSNorm and the token's RoPE,
+    as bf16 values (float64)."""
+    y = apply_rope(rms_norm(bf16_to_f32(qI_t_bits), q_weight, eps), rope_t)
+    return round_to_bf16(y).astype(np.float64)
 
 
 # --------------------------------------------------------------------------------------

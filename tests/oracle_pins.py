@@ -604,12 +604,17 @@ def pin_attention_bwd_invariants(O):
 
 
 def pin_rms_norm_vs_torch(O):
+    """The float32 evaluation against torch's float64 rms_norm of the same float32 inputs:
+    within the rounding of a 64-term float32 sum, a square root, a division and a product."""
     rng = np.random.default_rng(31)
-    x = rng.standard_normal((5, 3, 64))
-    w = rng.uniform(0.5, 1.5, 64)
+    x = rng.standard_normal((5, 3, 64)).astype(np.float32)
+    w = rng.uniform(0.5, 1.5, 64).astype(np.float32)
     for eps in (1e-6, 0.1):
-        ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (64,), torch.from_numpy(w), eps).numpy()
-        np.testing.assert_allclose(O.rms_norm(x, w, eps), ref, rtol=1e-12, atol=1e-14)
+        ref = torch.nn.functional.rms_norm(torch.from_numpy(x.astype(np.float64)), (64,),
+                                           torch.from_numpy(w.astype(np.float64)), eps).numpy()
+        got = O.rms_norm(x, w, eps)
+        assert got.dtype == np.float32
+        np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-6)
 
 
 def pin_rope_golden(O):
@@ -634,13 +639,16 @@ def pin_rope_rotation(O):
     x = rng.standard_normal((3, D))
     theta = rng.uniform(-np.pi, np.pi, (3, h))
     rope = np.concatenate([np.cos(theta), np.sin(theta)], axis=-1)
+    x = x.astype(np.float32)
+    rope = rope.astype(np.float32)
     got = O.apply_rope(x, rope)
-    z = (x[:, :h] + 1j * x[:, h:Dr]) * np.exp(1j * theta)
-    np.testing.assert_allclose(got[:, :h], z.real, rtol=0, atol=1e-14)
-    np.testing.assert_allclose(got[:, h:Dr], z.imag, rtol=0, atol=1e-14)
+    xd, cd, sd = x.astype(np.float64), rope[:, :h].astype(np.float64), rope[:, h:].astype(np.float64)
+    z = (xd[:, :h] + 1j * xd[:, h:Dr]) * (cd + 1j * sd)
+    np.testing.assert_allclose(got[:, :h], z.real, rtol=0, atol=2e-6)
+    np.testing.assert_allclose(got[:, h:Dr], z.imag, rtol=0, atol=2e-6)
     np.testing.assert_array_equal(got[:, Dr:], x[:, Dr:])
-    inv = np.concatenate([np.cos(theta), -np.sin(theta)], axis=-1)
-    np.testing.assert_allclose(O.apply_rope(got, inv), x, rtol=0, atol=1e-14)
+    inv = np.concatenate([rope[:, :h], -rope[:, h:]], axis=-1)
+    np.testing.assert_allclose(O.apply_rope(got, inv), x, rtol=0, atol=4e-6)
     freq = 1.0 / (10000.0 ** (np.arange(h) / h))
 
     def table(p):
@@ -649,7 +657,7 @@ def pin_rope_rotation(O):
     q, k = rng.standard_normal(D), rng.standard_normal(D)
     a = O.apply_rope(q, table(7.0)) @ O.apply_rope(k, table(3.0))
     b = O.apply_rope(q, table(104.0)) @ O.apply_rope(k, table(100.0))
-    assert abs(a - b) <= 1e-9 * max(1.0, abs(a)), (a, b)
+    assert abs(a - b) <= 2e-5 * max(1.0, abs(a)), (a, b)
     # one table row rotates all heads of a token alike
     xh = rng.standard_normal((2, 3, D))
     rows = np.concatenate([np.cos(theta[:2]), np.sin(theta[:2])], axis=-1)

@@ -198,8 +198,9 @@ def _rms_norm_no_eps(x, weight, eps):
 
 
 def _rms_norm_mean_abs(x, weight, eps):
-    x = np.asarray(x, dtype=np.float64)
-    return x / (np.mean(np.abs(x), axis=-1, keepdims=True) + eps) * np.asarray(weight, dtype=np.float64)
+    x = np.asarray(x, dtype=np.float32)
+    return (x / (np.mean(np.abs(x), axis=-1, keepdims=True) + np.float32(eps)) * np.asarray(weight, np.float32)
+            ).astype(np.float32)
 
 
 def _block_end_tokens(cu_seqlens, T, c):
@@ -212,7 +213,7 @@ def _block_starts_without_doc_offset(cu_seqlens, T, c):
 
 
 def _front_query_without_norm(qI_t_bits, q_weight, eps, rope_t):
-    return O.to_bf16_values(O.apply_rope(O.bf16_to_f64(qI_t_bits), rope_t))
+    return O.round_to_bf16(O.apply_rope(O.bf16_to_f32(qI_t_bits), rope_t)).astype(np.float64)
 
 
 def _e4m3_variant(subnormals=True, ties_even=True, mant_bits=3):
