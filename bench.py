@@ -1,14 +1,18 @@
 """Benchmark of the indexer-routed sparse attention hot path on GB300.
 
-One step = one pass of the whole path over one batch of the mid-size single-document
-workload (B=1, S=8192, Hq=32, Hkv=8, D=128; indexer Hi=16, Di=128, c=4, budget=2048):
-  sparse_index_score_topk (layout, pool, score, top-k + expansion)  ->  sparse_gqa_attn_fwd.
+One step = one pass of the whole path over one batch of the windowed workload, the largest
+single-GPU configuration that runs every stage (T=65536 single document, Hq=64, Hkv=4,
+Dqk=192, Dv=128; indexer Hi=32, Di=128, c=64, top-16 regions; a 512-token causal window):
+  sparse_index_score_topk (layout, pool, score, top-k + expansion) -> window composition
+  -> sparse_gqa_attn_fwd.
 
 Prints one JSON line (rank 0). `value` is the routed sparse-attention forward rate in
 TFLOP/s over the whole step (algorithmic attention FLOPs / step time, inputs resident in
-HBM, L2 flushed between timed steps); the indexer's queries/s, each kernel's own rate and
-the roofline of the dominant kernel are reported beside it. `--impl reference` times the
-CPU oracle on a bounded row sample of the same workload instead.
+HBM, L2 flushed between timed steps); the indexer's queries/s, each kernel group's own rate,
+cold- and warm-L2 times (mean and median) and the roofline of the dominant kernel, against
+HBM and against an L2-aware bound, are reported beside it. `per_workload` repeats the
+measurement for the other four workloads (tiny, mid, packed, latent). `--impl reference`
+times the CPU oracle on a bounded row sample of the headline workload instead.
 
 Multi-GPU: one process per GPU under torchrun; each rank runs its own replica of the
 workload (weak scaling, no data-path collective); the step time is the max over ranks.
@@ -16,6 +20,7 @@ workload (weak scaling, no data-path collective); the step time is the max over 
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -31,7 +36,7 @@ sys.path.insert(0, ROOT)
 import irs_synth  # noqa: E402
 
 METRIC = "routed sparse-attn fwd TFLOP/s & % roofline; indexer score+top-k queries/s"
-WORKLOAD = "mid"
+WORKLOAD = "windowed"
 L2_FLUSH_BYTES = 512 << 20    # > 129 MB L2
 
 
@@ -208,6 +213,192 @@ def barrier(world: int):
         dist.barrier()
 
 
+def measure_l2_copy_gbs(dev, stream) -> float:
+    """L2 bandwidth measured live: a 16 MiB -> 16 MiB device copy that stays in L2 (read +
+    write bytes over the event time, best of 5 runs of 50 copies)."""
+    import torch
+
+    a = torch.empty(8 << 20, dtype=torch.bfloat16, device=dev).fill_(1.0)
+    b = torch.empty_like(a)
+    for _ in range(10):
+        b.copy_(a)
+    best = float("inf")
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(50):
+            b.copy_(a)
+        e1.record(stream)
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1e-3 / 50)
+    return 2.0 * a.numel() * a.element_size() / best / 1e9
+
+
+class Path:
+    """Device buffers and the two halves of one step (indexer, attention) for a workload."""
+
+    def __init__(self, irs, wl, dev, want_host: bool = False):
+        import torch
+
+        self.irs, self.wl, self.dev = irs, wl, dev
+        host = irs_synth.as_torch(wl, device="cpu", pin=want_host)
+        self.host = host if want_host else None
+        self.d = {k: v.to(dev) for k, v in host.items()}
+        T = wl.T
+        self.out = torch.empty((T, wl.Hq, wl.Dv), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((T, wl.Hq), dtype=torch.float32, device=dev)
+        self.err = irs.device_error_flag(dev)
+        self.has_index = not wl.latent
+        if self.has_index:
+            W_idx = wl.budget + wl.c - 1
+            self.route_idx = torch.empty((T, W_idx), dtype=torch.int32, device=dev)
+            self.route = (torch.empty((T, wl.route_width), dtype=torch.int32, device=dev) if wl.window
+                          else self.route_idx)
+            self.ws = torch.empty(irs.index_workspace_bytes(T, wl.Hi, wl.Di, wl.c, wl.budget, wl.ndocs,
+                                                            wl.max_doc_len, True), dtype=torch.uint8, device=dev)
+        else:
+            self.route = self.d["route"]
+        self.kv_v = self.d["kv"][:, :, :wl.Dv] if wl.latent else None
+        self.kernels_per_step = path_kernels(wl)
+
+    def index(self):
+        wl, d = self.wl, self.d
+        if not self.has_index:
+            return
+        self.irs.sparse_index_score_topk(d["qI"], d["kI"], d["w"], d["cu_seqlens"], wl.c, wl.budget, ndocs=wl.ndocs,
+                                         max_doc_len=wl.max_doc_len, out=self.route_idx, workspace=self.ws,
+                                         err=self.err)
+        if wl.window:
+            self.irs.compose_window_routes(self.route_idx, d["cu_seqlens"], wl.window, out=self.route, err=self.err)
+
+    def attend(self):
+        wl, d = self.wl, self.d
+        if wl.latent:
+            self.irs.sparse_gqa_attn_fwd(d["q"], d["kv"], self.kv_v, self.route, wl.scale, out=self.out, lse=self.lse,
+                                         err=self.err)
+        else:
+            self.irs.sparse_gqa_attn_fwd(d["q"], d["k"], d["v"], self.route, wl.scale, out=self.out, lse=self.lse,
+                                         err=self.err)
+
+    def unique_kv_rows(self) -> int:
+        """Distinct key rows the step's routes touch (outside any timed region)."""
+        import torch
+
+        r = self.route
+        ids = r[(r >= 0) & (r < self.wl.Tk)].long()
+        mask = torch.zeros(self.wl.Tk, dtype=torch.bool, device=self.dev)
+        mask[ids] = True
+        return int(mask.sum().item())
+
+    def valid_pairs(self) -> int | None:
+        """Valid pairs where they depend on data (window-composed routes); else None."""
+        if self.has_index and self.wl.window:
+            return int((self.route >= 0).sum().item())
+        return None
+
+
+def time_steps(path: Path, steps: int, flush, stream, cold: bool):
+    """Per-step device times (ms) of the indexer half and the attention half, with CUDA
+    events on the launching stream; `cold` writes a buffer larger than L2 before each step."""
+    import torch
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize(path.dev)
+    for i in range(steps):
+        if cold:
+            flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        path.index()
+        ev[i][1].record(stream)
+        path.attend()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(path.dev)
+    idx = np.asarray([e[0].elapsed_time(e[1]) for e in ev])
+    att = np.asarray([e[1].elapsed_time(e[2]) for e in ev])
+    return idx, att
+
+
+def attention_report(wl, cnt, att_ms, att_warm_ms, peaks, l2_gbs, unique_rows) -> dict:
+    """Attention rates and both rooflines for one workload (times in ms, per launch group).
+
+    HBM roofline (the spec definition): every gathered K/V byte plus Q, O, lse and
+    routes at the measured HBM copy bandwidth, or the FLOPs at the bf16 peak if slower.
+    L2-aware roofline: the distinct K/V rows (plus Q, O, lse, routes) must come from HBM
+    while every gathered byte passes through L2, at the L2 copy bandwidth measured live; the
+    bound is the slowest of those two and the tensor time.
+    """
+    att_s = float(np.mean(att_ms)) * 1e-3
+    rows_bytes = (wl.Dqk * 2) if wl.latent else wl.Hkv * (wl.Dqk + wl.Dv) * 2
+    other_bytes = cnt["attn_bytes"] - cnt["pairs"] * rows_bytes
+    t_hbm = cnt["attn_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = cnt["attn_flops"] / (peaks["bf16_tflops"] * 1e12)
+    roof_s = max(t_hbm, t_tc)
+    uniq_bytes = unique_rows * rows_bytes + other_bytes
+    t_uniq = uniq_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_l2 = cnt["attn_bytes"] / (l2_gbs * 1e9)
+    l2_roof_s = max(t_uniq, t_l2, t_tc)
+    l2_bound = "hbm (distinct rows)" if l2_roof_s == t_uniq else ("l2" if l2_roof_s == t_l2 else "tensor")
+    frac = roof_s / att_s
+    rep = {"ms": round(att_s * 1e3, 4), "ms_median": round(float(np.median(att_ms)), 4),
+           "ms_warm_l2": round(float(np.mean(att_warm_ms)), 4),
+           "ms_warm_l2_median": round(float(np.median(att_warm_ms)), 4),
+           "tflops": round(cnt["attn_flops"] / att_s / 1e12, 3),
+           "routed_pairs_per_s": round(cnt["pairs"] * wl.Hq / att_s, 1),
+           "valid_pairs": cnt["pairs"], "flops": cnt["attn_flops"], "algorithmic_bytes": int(cnt["attn_bytes"]),
+           "roofline_bound": "hbm" if t_hbm >= t_tc else "tensor", "roofline_ms": round(roof_s * 1e3, 4),
+           "roofline_frac": round(frac, 4),
+           "l2_aware": {"bound": l2_bound, "roofline_ms": round(l2_roof_s * 1e3, 4),
+                        "frac": round(l2_roof_s / att_s, 4), "distinct_kv_rows": int(unique_rows),
+                        "distinct_bytes": int(uniq_bytes), "l2_copy_gbs": round(l2_gbs, 1)}}
+    if frac > 1.0:
+        rep["note"] = ("bound not binding: the gathered K/V rows are re-read from L2, so the HBM roofline "
+                       "understates what the kernel can reach; see l2_aware")
+    return rep
+
+
+def indexer_report(wl, cnt, idx_ms, idx_warm_ms, peaks) -> dict:
+    idx_s = float(np.mean(idx_ms)) * 1e-3
+    t_hbm = cnt["idx_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = cnt["idx_flops"] / (peaks["bf16_tflops"] * 1e12)
+    roof_s = max(t_hbm, t_tc)
+    return {"ms": round(idx_s * 1e3, 4), "ms_median": round(float(np.median(idx_ms)), 4),
+            "ms_warm_l2": round(float(np.mean(idx_warm_ms)), 4),
+            "queries_per_s": round(wl.T / idx_s, 1), "tflops": round(cnt["idx_flops"] / idx_s / 1e12, 3),
+            "roofline_bound": "hbm" if t_hbm >= t_tc else "tensor",
+            "roofline_frac": round(roof_s / idx_s, 4), "roofline_us": round(roof_s * 1e6, 2),
+            "algorithmic_bytes": int(cnt["idx_bytes"]), "flops": cnt["idx_flops"],
+            "includes_window_composition": bool(wl.window)}
+
+
+def measure_other_workload(irs, name, args, dev, stream, flush, peaks, l2_gbs) -> dict:
+    """One workload other than the headline one: cold and warm step times, attention and
+    indexer rates and rooflines (no end-to-end leg, no CPU baseline)."""
+    import torch
+
+    wl = irs_synth.make(name)
+    path = Path(irs, wl, dev)
+    for _ in range(args.warmup):
+        path.index()
+        path.attend()
+    torch.cuda.synchronize(dev)
+    irs.check_device_errors(dev)
+    cnt = counts(wl, path.valid_pairs())
+    uniq = path.unique_kv_rows()
+    steps = max(3, min(args.steps, 20))
+    idx_ms, att_ms = time_steps(path, steps, flush, stream, cold=True)
+    idx_w, att_w = time_steps(path, steps, flush, stream, cold=False)
+    irs.check_device_errors(dev)
+    rep = {"workload": describe(wl), "steps": steps,
+           "ms_per_step": round(float(np.mean(idx_ms + att_ms)), 4),
+           "kernels_per_step": path.kernels_per_step,
+           "attention": attention_report(wl, cnt, att_ms, att_w, peaks, l2_gbs, uniq)}
+    if path.has_index:
+        rep["indexer"] = indexer_report(wl, cnt, idx_ms, idx_w, peaks)
+    del path
+    torch.cuda.empty_cache()
+    return rep
+
+
 def run_gpu(args) -> dict | None:
     import torch
 
@@ -223,48 +414,18 @@ def run_gpu(args) -> dict | None:
     irs.lib()
     wl = irs_synth.make(args.workload, small=args.small)
     peaks = load_peaks()
-
-    host = irs_synth.as_torch(wl, device="cpu", pin=True)
-    d = {k: v.to(dev) for k, v in host.items()}
-    T = wl.T
-    out = torch.empty((T, wl.Hq, wl.Dv), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((T, wl.Hq), dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    err = irs.device_error_flag(dev)
-    has_index = not wl.latent
-    if has_index:
-        W_idx = wl.budget + wl.c - 1
-        route_idx = torch.empty((T, W_idx), dtype=torch.int32, device=dev)
-        route = torch.empty((T, wl.route_width), dtype=torch.int32, device=dev) if wl.window else route_idx
-        ws = torch.empty(irs.index_workspace_bytes(T, wl.Hi, wl.Di, wl.c, wl.budget, wl.ndocs, wl.max_doc_len, True),
-                         dtype=torch.uint8, device=dev)
-        max_doc_len, ndocs = wl.max_doc_len, wl.ndocs
-    kv_v = d["kv"][:, :, :wl.Dv] if wl.latent else None
-
-    def index(dd):
-        if not has_index:
-            return
-        irs.sparse_index_score_topk(dd["qI"], dd["kI"], dd["w"], dd["cu_seqlens"], wl.c, wl.budget, ndocs=ndocs,
-                                    max_doc_len=max_doc_len, out=route_idx, workspace=ws, err=err)
-        if wl.window:
-            irs.compose_window_routes(route_idx, dd["cu_seqlens"], wl.window, out=route, err=err)
-
-    def attend(dd):
-        if wl.latent:
-            irs.sparse_gqa_attn_fwd(dd["q"], dd["kv"], kv_v, dd["route"], wl.scale, out=out, lse=lse, err=err)
-        else:
-            irs.sparse_gqa_attn_fwd(dd["q"], dd["k"], dd["v"], route, wl.scale, out=out, lse=lse, err=err)
-
     stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    l2_gbs = measure_l2_copy_gbs(dev, stream)
+
+    path = Path(irs, wl, dev, want_host=True)
     for _ in range(args.warmup):
-        index(d)
-        attend(d)
+        path.index()
+        path.attend()
     torch.cuda.synchronize(dev)
     irs.check_device_errors(dev)
-    # valid pairs: closed form, except for the window-composed routes (data dependent)
-    pairs = int((route >= 0).sum().item()) if (has_index and wl.window) else None
-    cnt = counts(wl, pairs)
-    kernels_per_step = (4 if has_index else 0) + (1 if wl.window else 0) + (wl.Hkv + 7) // 8
+    cnt = counts(wl, path.valid_pairs())
+    uniq = path.unique_kv_rows()
 
     uuid = None
     try:
@@ -277,30 +438,21 @@ def run_gpu(args) -> dict | None:
     if rank == 0:
         clocks.start()
 
-    # ---- device-timed region: K steps, L2 flushed before each, per-kernel events ----
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # ---- device-timed region: K steps, L2 flushed before each, per-kernel-group events ----
     barrier(world)
-    torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        ev[i][0].record(stream)
-        index(d)
-        ev[i][1].record(stream)
-        attend(d)
-        ev[i][2].record(stream)
-    torch.cuda.synchronize(dev)
+    idx_ms, att_ms = time_steps(path, args.steps, flush, stream, cold=True)
     barrier(world)
     wall = time.perf_counter() - wall0
-    idx_ms = np.asarray([ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)])
-    att_ms = np.asarray([ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)])
-    step_ms_local = float(np.mean(idx_ms + att_ms))
-    step_ms = reduce_max(step_ms_local, world, dev)
+    step_ms = reduce_max(float(np.mean(idx_ms + att_ms)), world, dev)
     irs.check_device_errors(dev)
+    # the same steps without the flush (L2 keeps what the previous step left)
+    idx_w, att_w = time_steps(path, max(3, args.steps // 2), flush, stream, cold=False)
 
     # ---- end to end through the public API with host buffers ----
-    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    host = path.host
+    out_h = torch.empty(path.out.shape, dtype=path.out.dtype, pin_memory=True)
+    lse_h = torch.empty(path.lse.shape, dtype=path.lse.dtype, pin_memory=True)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
     e2e_steps = max(3, args.steps // 2)
@@ -311,41 +463,53 @@ def run_gpu(args) -> dict | None:
         flush.fill_(i & 0xFF)
         ee[i][0].record(stream)
         for k_, v_ in host.items():
-            d[k_].copy_(v_, non_blocking=True)
-        index(d)
-        attend(d)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+            path.d[k_].copy_(v_, non_blocking=True)
+        path.index()
+        path.attend()
+        out_h.copy_(path.out, non_blocking=True)
+        lse_h.copy_(path.lse, non_blocking=True)
         ee[i][1].record(stream)
         ee[i][1].synchronize()
     barrier(world)
     e2e_ms = reduce_max(float(np.mean([ee[i][0].elapsed_time(ee[i][1]) for i in range(e2e_steps)])), world, dev)
-    bwd = time_backward(args, wl, irs, d, route if has_index else d["route"], kv_v, out, lse, flush, err, stream,
+    bwd = time_backward(args, wl, irs, path.d, path.route, path.kv_v, path.out, path.lse, flush, path.err, stream,
                         dev) if args.with_backward else None
     clk = clocks.stop() if rank == 0 else None
     irs.check_device_errors(dev)
 
-    if rank != 0:
-        return None
+    attn = attention_report(wl, cnt, att_ms, att_w, peaks, l2_gbs, uniq)
     att_avg_s = float(np.mean(att_ms)) * 1e-3
-    idx_avg_s = float(np.mean(idx_ms)) * 1e-3
-    attn_gbs = cnt["attn_bytes"] / att_avg_s / 1e9
-    attn_tflops = cnt["attn_flops"] / att_avg_s / 1e12
-    attn_roof_s = max(cnt["attn_bytes"] / (peaks["hbm_gbs"] * 1e9), cnt["attn_flops"] / (peaks["bf16_tflops"] * 1e12))
-    attn_bound = "hbm" if cnt["attn_bytes"] / peaks["hbm_gbs"] >= cnt["attn_flops"] / (peaks["bf16_tflops"] * 1e3) \
-        else "tensor"
     value = world * cnt["attn_flops"] / (step_ms * 1e-3) / 1e12
-    if attn_bound == "hbm":
-        roof = {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(attn_gbs / peaks["hbm_gbs"], 4)}
+    if attn["roofline_bound"] == "hbm":
+        achieved = cnt["attn_bytes"] / att_avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4)}
     else:
-        roof = {"bound": "tensor", "achieved": round(attn_tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(attn_tflops / peaks["bf16_tflops"], 4)}
+        achieved = cnt["attn_flops"] / att_avg_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4)}
     # the latent workload runs on the latent-attention kernel, the others on the GQA kernel
     kname, ksrc = (("mla_fwd_kernel", "irs_mla.cu") if wl.latent else ("attn_fwd_kernel", "irs_attn.cu"))
     kprof = f"{kname.replace('_kernel', '')}_{wl.name}{'_small' if args.small else ''}.md"
     roof.update({"traffic": profile_traffic(kprof, f"indexer_routed_sparse_gb300/csrc/{ksrc}"),
-                 "kernel": kname, "peak_source": peaks["source"]})
+                 "kernel": kname, "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst)",
+                 "l2_aware_frac": attn["l2_aware"]["frac"], "l2_aware_bound": attn["l2_aware"]["bound"]})
+    if roof["frac"] > 1.0:
+        roof["note"] = "bound not binding (gathered rows re-read from L2): see l2_aware_frac"
+    del path
+    torch.cuda.empty_cache()
+    per_workload = {}
+    if not args.no_per_workload and not args.small and args.workload == WORKLOAD:
+        for name in irs_synth.WORKLOADS:
+            if name != WORKLOAD:
+                per_workload[name] = measure_other_workload(irs, name, args, dev, stream, flush, peaks, l2_gbs)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return None
     res = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -354,6 +518,7 @@ def run_gpu(args) -> dict | None:
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(step_ms, 4),
+        "ms_per_step_median": round(float(np.median(idx_ms + att_ms)), 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -362,32 +527,32 @@ def run_gpu(args) -> dict | None:
         "config": {"workload": describe(wl), "l2": "flushed (512 MiB write) before every timed step",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
-        "attention": {"ms": round(att_avg_s * 1e3, 4), "tflops": round(attn_tflops, 3),
-                      "routed_pairs_per_s": round(cnt["pairs"] * wl.Hq / att_avg_s, 1),
-                      "roofline_frac": round(attn_roof_s / att_avg_s, 4), "roofline_ms": round(attn_roof_s * 1e3, 4),
-                      "algorithmic_bytes": cnt["attn_bytes"], "flops": cnt["attn_flops"], "valid_pairs": cnt["pairs"]},
+        "attention": attn,
         "e2e": {"value": round(world * cnt["attn_flops"] / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": kernels_per_step * args.steps,
+        "gpu_launches": path_kernels(wl) * args.steps,
         "clocks": clk,
         "wall_s_timed": round(wall, 3),
     }
-    if has_index:
-        idx_roof_s = max(cnt["idx_bytes"] / (peaks["hbm_gbs"] * 1e9), cnt["idx_flops"] / (peaks["bf16_tflops"] * 1e12))
-        res["indexer"] = {"ms": round(idx_avg_s * 1e3, 4), "queries_per_s": round(wl.T / idx_avg_s, 1),
-                          "tflops": round(cnt["idx_flops"] / idx_avg_s / 1e12, 3),
-                          "roofline_frac": round(idx_roof_s / idx_avg_s, 4), "roofline_us": round(idx_roof_s * 1e6, 2),
-                          "algorithmic_bytes": cnt["idx_bytes"], "flops": cnt["idx_flops"],
-                          "includes_window_composition": bool(wl.window)}
+    if not wl.latent:
+        res["indexer"] = indexer_report(wl, cnt, idx_ms, idx_w, peaks)
     if bwd is not None:
         res["backward"] = backward_report(wl, cnt, bwd, peaks)
-    if not args.no_cpu_baseline and world == 1 and args.workload == WORKLOAD:
+    if per_workload:
+        res["per_workload"] = per_workload
+    if not args.no_cpu_baseline and world == 1 and args.workload == WORKLOAD and not args.small:
         res["cpu_baseline"] = cpu_baseline(wl, cnt, budget_s=args.cpu_seconds, small=args.small)
     if world > 1:
         import torch.distributed as dist
 
         dist.destroy_process_group()
     return res
+
+
+def path_kernels(wl) -> int:
+    """Our kernels launched per step: layout, pool, score, top-k (+ window composition) and
+    one attention launch per 8 KV heads."""
+    return (0 if wl.latent else 4) + (1 if wl.window else 0) + (wl.Hkv + 7) // 8
 
 
 def time_backward(args, wl, irs, d, route, kv_v, out, lse, flush, err, stream, dev) -> float:
@@ -454,9 +619,34 @@ def backward_report(wl, cnt, bwd_s: float, peaks: dict) -> dict:
 _WL = None
 
 
-def _worker_init(name: str = WORKLOAD, small: bool = False):
+def _worker_init(name: str = WORKLOAD, small: bool = False, meta=None, shared_dir: str | None = None):
+    """Worker set-up: the workload's arrays mapped read-only from `shared_dir` (written once
+    by the parent), or drawn again from the seeded recipe when there is none."""
     global _WL
-    _WL = irs_synth.make(name, small=small)
+    if shared_dir is None:
+        _WL = irs_synth.make(name, small=small)
+        return
+    arrays = {f[:-4]: np.load(os.path.join(shared_dir, f), mmap_mode="r")
+              for f in os.listdir(shared_dir) if f.endswith(".npy")}
+    _WL = dataclasses.replace(meta, arrays=arrays)
+
+
+def share_arrays(wl) -> str | None:
+    """Write the workload's arrays once to a temporary directory (in /dev/shm when it has
+    room) so that the oracle's worker processes map them instead of drawing them again."""
+    import shutil
+    import tempfile
+
+    need = sum(int(v.nbytes) for v in wl.arrays.values()) * 1.2 + (64 << 20)
+    base = None
+    if os.path.isdir("/dev/shm") and shutil.disk_usage("/dev/shm").free > need:
+        base = "/dev/shm"
+    elif shutil.disk_usage(tempfile.gettempdir()).free <= need:
+        return None
+    d = tempfile.mkdtemp(prefix="irs_oracle_", dir=base)
+    for k, v in wl.arrays.items():
+        np.save(os.path.join(d, k + ".npy"), np.ascontiguousarray(v))
+    return d
 
 
 def _oracle_rows(rows) -> int:
@@ -491,16 +681,29 @@ def oracle_sample(n_rows: int, cores: int, pool) -> tuple[float, int, float]:
     return dt, pairs, 2.0 * (wl.Dqk + wl.Dv) * wl.Hq * pairs
 
 
-def make_pool(cores: int, name: str = WORKLOAD, small: bool = False):
+def make_pool(cores: int, wl, small: bool = False):
+    """Spawned oracle workers (spawn: never forked from a process that has used the GPU) and
+    the shared-array directory to remove afterwards (or None)."""
     import multiprocessing as mp
 
     os.environ.setdefault("OMP_NUM_THREADS", "1")
     os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
     os.environ.setdefault("MKL_NUM_THREADS", "1")
+    shared = share_arrays(wl)
     ctx = mp.get_context("spawn")
-    pool = ctx.Pool(cores, initializer=_worker_init, initargs=(name, small))
-    pool.map(_worker_init_probe, range(cores))   # workers are up and have built the workload
-    return pool
+    meta = dataclasses.replace(wl, arrays={})
+    pool = ctx.Pool(cores, initializer=_worker_init, initargs=(wl.name, small, meta, shared))
+    pool.map(_worker_init_probe, range(cores))   # workers are up and hold the workload
+    return pool, shared
+
+
+def close_pool(pool, shared: str | None):
+    import shutil
+
+    pool.terminate()
+    pool.join()
+    if shared is not None:
+        shutil.rmtree(shared, ignore_errors=True)
 
 
 def _worker_init_probe(_):
@@ -511,14 +714,14 @@ def cpu_baseline(wl, cnt, budget_s: float = 15.0, small: bool = False) -> dict:
     global _WL
     _WL = wl
     cores = os.cpu_count() or 1
-    pool = make_pool(cores, wl.name, small)
+    pool, shared = make_pool(cores, wl, small)
     try:
         oracle_sample(cores, cores, pool)                           # first calls per worker run slow
         dt1, _, _ = oracle_sample(cores, cores, pool)               # calibration: one row per core
         n = int(max(cores, min(wl.T, cores * max(1, int(budget_s / max(dt1, 1e-3))))))
         dt, pairs, flops = oracle_sample(n, cores, pool)
     finally:
-        pool.terminate()
+        close_pool(pool, shared)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} of {wl.T} query rows spread evenly ({'attention' if wl.latent else 'indexer + attention'}, "
                       f"all {wl.Hq} heads), "
@@ -534,7 +737,7 @@ def run_reference(args) -> dict | None:
     wl = irs_synth.make(WORKLOAD)
     _WL = wl
     cores = os.cpu_count() or 1
-    pool = make_pool(cores)
+    pool, shared = make_pool(cores, wl)
     try:
         dt1, _, _ = oracle_sample(cores, cores, pool)
         per_step_s = max(0.5, args.reference_seconds / max(1, args.steps + args.warmup))
@@ -546,15 +749,14 @@ def run_reference(args) -> dict | None:
             dt, _, fl = oracle_sample(n, cores, pool)
             times.append(dt)
     finally:
-        pool.terminate()
+        close_pool(pool, shared)
     ms = float(np.mean(times)) * 1e3
     value = fl / (ms * 1e-3) / 1e12
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "mid single-document: B=1 S=8192 Hq=32 Hkv=8 D=128, indexer Hi=16 Di=128 c=4 "
-                               "budget=2048, seed 1", "sample_rows_per_step": n},
+        "config": {"workload": describe(wl), "sample_rows_per_step": n},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{n} of {wl.T} query rows per step (indexer + attention)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -568,10 +770,13 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("irs", "reference"), default="irs")
     ap.add_argument("--workload", choices=irs_synth.WORKLOADS, default=WORKLOAD,
-                    help="workload of the step (the headline line uses the mid workload)")
+                    help="workload of the step (the headline line uses the windowed workload, the "
+                         "largest single-GPU configuration that runs the whole path)")
     ap.add_argument("--small", action="store_true",
                     help="the workload's reduced-size variant (test sizes; for profiler captures, not a bench line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="time only the headline workload (skip the other four)")
     ap.add_argument("--with-backward", action="store_true",
                     help="also time sparse_gqa_attn_bwd on the step's routes (reported under 'backward')")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -128,11 +128,14 @@ def index_workspace_bytes(T, Hi, Di, c, budget, ndocs, max_doc_len, with_score_b
     return int(lib().irs_index_workspace_bytes(T, Hi, Di, c, budget, ndocs, max_doc_len, int(bool(with_score_buffer))))
 
 
-def _doc_stats(cu_seqlens: torch.Tensor, ndocs, max_doc_len):
+def _doc_stats(cu_seqlens: torch.Tensor, ndocs, max_doc_len, T: int):
+    """Host sizes of the document layout without reading device data: ndocs from the
+    tensor's shape and, unless the caller gives it, T as the bound on a document's length
+    (a tighter max_doc_len shrinks the score scratch; the kernels check it on the device)."""
     if ndocs is None:
         ndocs = cu_seqlens.numel() - 1
     if max_doc_len is None:
-        max_doc_len = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item())
+        max_doc_len = T
     return int(ndocs), int(max_doc_len)
 
 
@@ -157,7 +160,7 @@ def sparse_index_score_topk(qI: torch.Tensor, kI: torch.Tensor, w: torch.Tensor,
         raise ValueError(f"shape mismatch: qI {tuple(qI.shape)}, kI {tuple(kI.shape)}, w {tuple(w.shape)}")
     if not (qI.is_contiguous() and kI.is_contiguous() and w.is_contiguous() and cu_seqlens.is_contiguous()):
         raise ValueError("qI, kI, w and cu_seqlens must be contiguous")
-    ndocs, max_doc_len = _doc_stats(cu_seqlens, ndocs, max_doc_len)
+    ndocs, max_doc_len = _doc_stats(cu_seqlens, ndocs, max_doc_len, T)
     W = budget + c - 1
     dev = qI.device
     if out is None:
@@ -191,7 +194,9 @@ def topk_from_scores(scores: torch.Tensor, cu_seqlens: torch.Tensor, c: int, bud
     if scores.stride(1) != 1:
         raise ValueError("scores must have unit inner stride")
     T = scores.shape[0]
-    ndocs, max_doc_len = _doc_stats(cu_seqlens, ndocs, max_doc_len)
+    if max_doc_len is None:   # the longest document whose block scores fit in a row of `scores`
+        max_doc_len = min(T, (scores.shape[1] + 1) * c - 1)
+    ndocs, max_doc_len = _doc_stats(cu_seqlens, ndocs, max_doc_len, T)
     dev = scores.device
     if out is None:
         out = torch.empty((T, budget + c - 1), dtype=torch.int32, device=dev)

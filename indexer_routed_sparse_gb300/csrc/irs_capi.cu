@@ -130,6 +130,22 @@ irs_status check_index_sizes(int T, int Hi, int Di, int c, int budget, int ndocs
   return IRS_OK;
 }
 
+// Raise the dynamic shared-memory limits of the indexer kernels to what this call needs.
+irs_status configure_index(DeviceInfo* dev, const irs::IndexPlan& p) {
+  if (p.score_smem > kMaxSmem) return fail(IRS_ERR_VALUE, "score tile does not fit in shared memory");
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  irs_status s = IRS_OK;
+  if (dev->score_smem < p.score_smem) {
+    if ((s = launch_status(irs::configure_score_kernels(p.score_smem), "configuring scoring")) != IRS_OK) return s;
+    dev->score_smem = p.score_smem;
+  }
+  if (dev->topk_smem < p.topk_smem) {
+    if ((s = launch_status(irs::configure_topk_kernel(p.topk_smem), "configuring top-k")) != IRS_OK) return s;
+    dev->topk_smem = p.topk_smem;
+  }
+  return IRS_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -162,18 +178,7 @@ irs_status irs_sparse_index_score_topk(const void* qI, const void* kI, const flo
     return fail(IRS_ERR_VALUE, "workspace too small: %zu < %zu bytes", workspace_bytes, p.ws_bytes);
   DeviceInfo* dev = nullptr;
   if ((s = current_device(&dev)) != IRS_OK) return s;
-  if (p.score_smem > kMaxSmem) return fail(IRS_ERR_VALUE, "score tile does not fit in shared memory");
-  {
-    std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (dev->score_smem < p.score_smem) {
-      if ((s = launch_status(irs::configure_score_kernels(p.score_smem), "configuring scoring")) != IRS_OK) return s;
-      dev->score_smem = p.score_smem;
-    }
-    if (dev->topk_smem < p.topk_smem) {
-      if ((s = launch_status(irs::configure_topk_kernel(p.topk_smem), "configuring top-k")) != IRS_OK) return s;
-      dev->topk_smem = p.topk_smem;
-    }
-  }
+  if ((s = configure_index(dev, p)) != IRS_OK) return s;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* scores = scores_dbg != nullptr ? scores_dbg : reinterpret_cast<float*>(ws + p.off_scores);
   const int64_t ldS = scores_dbg != nullptr ? ld_scores : p.ldS;
@@ -183,7 +188,7 @@ irs_status irs_sparse_index_score_topk(const void* qI, const void* kI, const flo
   return launch_status(irs::launch_index(p, static_cast<const __nv_bfloat16*>(qI),
                                          static_cast<const __nv_bfloat16*>(kI), w, cu_seqlens, ndocs, max_doc_len, T,
                                          Hi, Di, c, budget, route_ids, scores, ldS, ws, err_flag, tm_q, tm_k,
-                                         reinterpret_cast<cudaStream_t>(stream)),
+                                         dev->num_sms, reinterpret_cast<cudaStream_t>(stream)),
                        "launching the indexer");
 }
 
@@ -434,18 +439,7 @@ extern "C" irs_status irs_sparse_index_score_topk_noalloc(const void* qI, const 
     }
     ws = static_cast<uint8_t*>(g_noalloc_addr[ordinal]);
   }
-  if (p.score_smem > kMaxSmem) return fail(IRS_ERR_VALUE, "score tile does not fit in shared memory");
-  {
-    std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (dev->score_smem < p.score_smem) {
-      if ((s = launch_status(irs::configure_score_kernels(p.score_smem), "configuring scoring")) != IRS_OK) return s;
-      dev->score_smem = p.score_smem;
-    }
-    if (dev->topk_smem < p.topk_smem) {
-      if ((s = launch_status(irs::configure_topk_kernel(p.topk_smem), "configuring top-k")) != IRS_OK) return s;
-      dev->topk_smem = p.topk_smem;
-    }
-  }
+  if ((s = configure_index(dev, p)) != IRS_OK) return s;
   float* scores = scores_dbg != nullptr ? scores_dbg : reinterpret_cast<float*>(ws + p.off_scores);
   const int64_t ldS = scores_dbg != nullptr ? ld_scores : p.ldS;
   CUtensorMap tm_q, tm_k;
@@ -454,7 +448,7 @@ extern "C" irs_status irs_sparse_index_score_topk_noalloc(const void* qI, const 
   return launch_status(irs::launch_index(p, static_cast<const __nv_bfloat16*>(qI),
                                          static_cast<const __nv_bfloat16*>(kI), w, cu_seqlens, ndocs, max_doc_len, T,
                                          Hi, Di, c, budget, route_ids, scores, ldS, ws, err_flag, tm_q, tm_k,
-                                         reinterpret_cast<cudaStream_t>(stream)),
+                                         dev->num_sms, reinterpret_cast<cudaStream_t>(stream)),
                        "launching the indexer (fixed scratch)");
 }
 

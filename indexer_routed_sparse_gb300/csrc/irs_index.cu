@@ -1,19 +1,19 @@
 // Compressed-block indexer on sm_103a: document layout, FP32 block mean-pool,
-// tensor-core weighted-ReLU scoring, per-query radix top-k, bitmap packing and route
+// tensor-core weighted-ReLU scoring, per-query top-k, bitmap packing and route
 // expansion, plus the sliding-window route composition.
 //
 // Definitions follow the QSA page (nemo_automodel.components.models.qwen3_8_flash_next.qsa:
 // `select_qsa_token_ids`, `Qwen3_8_FlashNextQSAIndexer`, `_forward_packed`) and the Step-5
 // sparse page (nemo_automodel.components.models.step5.sparse: `indexer_score_tile`,
 // `pack_region_bitmap`).
-#include "irs_internal.h"
-#include "irs_ptx.cuh"
+#include "irs_index_score.cuh"
 
 namespace irs {
 
 // =====================================================================================
 // a1: document layout. One CTA validates cu_seqlens and writes, per document, the first
-// pooled-block row and the first score tile. meta[0] = 1 when the layout is valid.
+// pooled-block row and the first score tile; it also resets the tile counter of the
+// persistent score kernel. meta[0] = 1 when the layout is valid.
 // =====================================================================================
 __global__ void __launch_bounds__(1024) layout_kernel(const int32_t* __restrict__ cu, int ndocs, int T, int c,
                                                       int tau_sparse, int QT, int max_doc_len,
@@ -77,38 +77,21 @@ __global__ void __launch_bounds__(1024) layout_kernel(const int32_t* __restrict_
     meta[0] = ok;
     meta[1] = s_carry[0];
     meta[2] = s_carry[1];
+    meta[3] = 0;   // tile counter of the score kernel
     if (!ok) record_error(err, IRS_DEVERR_CU_SEQLENS);
   }
-}
-
-// Document containing token t: largest d with cu[d] <= t (cu strictly increasing).
-__device__ __forceinline__ int find_doc(const int32_t* __restrict__ cu, int ndocs, int t) {
-  int lo = 0, hi = ndocs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (cu[mid] <= t) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
-// Largest d in [0, n) with off[d] <= x (off non-decreasing, off[0] = 0 <= x).
-__device__ __forceinline__ int find_le(const int32_t* __restrict__ off, int n, int x) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (off[mid] <= x) lo = mid; else hi = mid - 1;
-  }
-  return lo;
 }
 
 // =====================================================================================
 // a2: block mean-pool. Thread = (pooled block, 8 consecutive dims). FP32 sequential sum
 // over the c rows in token order, one IEEE division by c, then round-to-nearest-even
-// to bf16 (the scoring operand).
+// to bf16 (the scoring operand). Rows past the last complete block (up to the buffer's
+// T/c rows) are zeroed: key tiles that reach into them only feed masked scores, but the
+// scratch then never holds values of an earlier call.
 // =====================================================================================
 __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restrict__ kI,
                                                    const int32_t* __restrict__ cu, int ndocs, int Di, int c,
-                                                   const int32_t* __restrict__ meta,
+                                                   int nblk_cap, const int32_t* __restrict__ meta,
                                                    const int32_t* __restrict__ blk_off,
                                                    __nv_bfloat16* __restrict__ kbar) {
   if (meta[0] != 1) return;
@@ -117,7 +100,11 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int gb = (int)(gid / chunks);
   const int ch = (int)(gid % chunks);
-  if (gb >= nblk) return;
+  if (gb >= nblk_cap) return;
+  if (gb >= nblk) {
+    reinterpret_cast<uint4*>(kbar + (long long)gb * Di)[ch] = make_uint4(0, 0, 0, 0);
+    return;
+  }
   const int d = find_le(blk_off, ndocs, gb);
   const int b = gb - blk_off[d];
   const long long row0 = (long long)cu[d] + (long long)b * c;
@@ -142,240 +129,6 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
   for (int i = 0; i < 4; ++i)
     q[i] = __floats2bfloat162_rn(__fdiv_rn(acc[2 * i], fc), __fdiv_rn(acc[2 * i + 1], fc));
   reinterpret_cast<uint4*>(kbar + (long long)gb * Di)[ch] = o;
-}
-
-// =====================================================================================
-// a3: weighted-ReLU block scores on tcgen05.
-//
-// One CTA scores one tile of QT consecutive sparse queries of one document against all
-// their visible blocks. The contraction runs transposed: the UMMA's M = 128 pooled key
-// blocks (one per TMEM lane), N = QT*Hi = 256 (query, head) columns, K = Di. The query
-// tile (B operand) stays in shared memory; 128-block key tiles (A operand) stream through
-// a TMA ring. Two TMEM accumulators (2 x 256 columns) let the epilogue of tile j overlap
-// the MMAs of tile j+1. The epilogue thread of lane b reads its 256 columns and reduces
-// each query's heads in order: s = sum_h w[t,h] * max(acc, 0) (FP32 FMA chain).
-//
-// Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 2..17 = epilogue (four warps per
-// TMEM lane quarter, each taking a quarter of the 256 columns, or whole queries if Hi > 64).
-// =====================================================================================
-constexpr int kScoreThreads = 576;   // producer, MMA, 16 epilogue warps
-constexpr int kScoreN = 256;          // (query, head) columns per tile
-constexpr int kScoreM = 128;          // key blocks per tile
-
-struct ScoreArgs {
-  const float* w;
-  const int32_t* cu;
-  const int32_t* blk_off;
-  const int32_t* tile_off;
-  const int32_t* meta;
-  float* scores;
-  int64_t ldS;
-  int32_t* err;
-  int ndocs, T, Hi, c, kb, QT, tau_sparse, stages;
-};
-
-__device__ __forceinline__ int rot_tile(int j, int jrot, int nbt) {
-  const int r = j + jrot;
-  return r >= nbt ? r - nbt : r;
-}
-
-__device__ __forceinline__ float w4f(const float4* w4, int k) {
-  const float4 v = w4[k >> 2];
-  return (k & 3) == 0 ? v.x : ((k & 3) == 1 ? v.y : ((k & 3) == 2 ? v.z : v.w));
-}
-
-template <int DI, int HI>
-__global__ void __launch_bounds__(kScoreThreads, 1)
-    score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, ScoreArgs a) {
-  constexpr int KATOMS = DI / 64;
-  constexpr uint32_t A_ATOM = kScoreM * 128;            // bytes per 64-dim atom of a key tile
-  constexpr uint32_t A_STAGE = KATOMS * A_ATOM;
-  constexpr uint32_t B_ATOM = kScoreN * 128;
-  constexpr uint32_t B_BYTES = KATOMS * B_ATOM;
-  constexpr uint32_t IDESC = idesc_bf16(kScoreM, kScoreN, false, false);
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sB = smem;
-  uint8_t* sA = smem + B_BYTES;
-  const int ST = a.stages;
-  float* sW = reinterpret_cast<float*>(sA + (size_t)ST * A_STAGE);
-  int* sNvis = reinterpret_cast<int*>(sW + kScoreN);                 // [QT] visible blocks per query
-  uint64_t* full = reinterpret_cast<uint64_t*>(sNvis + kScoreN);
-  uint64_t* empty = full + ST;
-  uint64_t* bfull = empty + ST;
-  uint64_t* tfull = bfull + 1;
-  uint64_t* tempty = tfull + 2;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(tempty + 2);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
-
-  if (a.meta[0] != 1) return;
-  const int ntiles = a.meta[2];
-  if ((int)blockIdx.x >= ntiles) return;
-  // heaviest tiles (largest visible prefix) first
-  const int tile = ntiles - 1 - (int)blockIdx.x;
-  const int d = find_le(a.tile_off, a.ndocs, tile);
-  const int s_doc = a.cu[d];
-  const int L = a.cu[d + 1] - s_doc;
-  const int tau0 = a.tau_sparse + (tile - a.tile_off[d]) * a.QT;
-  const int nq = min(a.QT, L - tau0);
-  const int t0 = s_doc + tau0;
-  const int nvis_last = (tau0 + nq) / a.c;
-  const int nbt = (nvis_last + kScoreM - 1) / kScoreM;
-  // CTAs start at different key tiles so that concurrent CTAs do not all read the same
-  // 32 KB of pooled keys from L2 at the same moment
-  const int jrot = (int)(blockIdx.x % (unsigned)max(nbt, 1));
-  const int blk0 = a.blk_off[d];
-  constexpr int Hi = HI;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // per-tile head weights (columns of the accumulator are (query, head) = row-major [QT][Hi])
-  for (int i = tid; i < kScoreN; i += kScoreThreads) {
-    const long long gi = (long long)t0 * Hi + i;
-    sW[i] = (i < a.QT * Hi && gi < (long long)a.T * Hi) ? a.w[gi] : 0.f;
-    sNvis[i] = i < nq ? (tau0 + i + 1) / a.c : 0;   // rows past the document see nothing
-  }
-  if (tid == 0) {
-    for (int s = 0; s < ST; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    mbar_init(bfull, 1);
-    mbar_init(&tfull[0], 1); mbar_init(&tfull[1], 1);
-    mbar_init(&tempty[0], 16); mbar_init(&tempty[1], 16);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(tslot, 2 * kScoreN);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *tslot;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      tma_prefetch_map(&tm_q);
-      tma_prefetch_map(&tm_k);
-      mbar_arrive_expect_tx(bfull, B_BYTES);
-      for (int ka = 0; ka < KATOMS; ++ka) tma_load_2d(sB + ka * B_ATOM, &tm_q, ka * 64, t0 * Hi, bfull);
-      int issued = 0;
-      for (int j = 0; j < nbt; ++j) {
-        const int s = j % ST;
-        if (j >= ST && !mbar_wait(&empty[s], ((j / ST) - 1) & 1, abort_flag, a.err)) break;
-        mbar_arrive_expect_tx(&full[s], A_STAGE);
-        const int bt = rot_tile(j, jrot, nbt);
-        for (int ka = 0; ka < KATOMS; ++ka)
-          tma_load_2d(sA + (size_t)s * A_STAGE + ka * A_ATOM, &tm_k, ka * 64, blk0 + bt * kScoreM, &full[s]);
-        issued = j + 1;
-      }
-      if (*abort_flag) {
-        // let copies already in flight land before the CTA leaves
-        for (int j = max(0, issued - ST); j < issued; ++j) {
-          const unsigned long long t_0 = globaltimer_ns();
-          while (!mbar_try_wait(&full[j % ST], (j / ST) & 1) && globaltimer_ns() - t_0 < kWaitLimitNs) {}
-        }
-        const unsigned long long t_1 = globaltimer_ns();
-        while (!mbar_try_wait(bfull, 0) && globaltimer_ns() - t_1 < kWaitLimitNs) {}
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      if (mbar_wait(bfull, 0, abort_flag, a.err)) {
-        for (int j = 0; j < nbt; ++j) {
-          const int s = j % ST, buf = j & 1;
-          if (j >= 2 && !mbar_wait(&tempty[buf], ((j >> 1) - 1) & 1, abort_flag, a.err)) break;
-          if (!mbar_wait(&full[s], (j / ST) & 1, abort_flag, a.err)) break;
-          tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + (size_t)s * A_STAGE);
-          const uint32_t b_base = smem_u32(sB);
-#pragma unroll
-          for (int ks = 0; ks < DI / 16; ++ks) {
-            const uint64_t ad = sdesc_sw128(a_base + (ks >> 2) * A_ATOM + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(b_base + (ks >> 2) * B_ATOM + (ks & 3) * 32, 16, 1024);
-            umma_bf16(tbase + buf * kScoreN, ad, bd, IDESC, ks > 0);
-          }
-          umma_commit(&empty[s]);
-          umma_commit(&tfull[buf]);
-        }
-      }
-    }
-  } else {
-    // ---------------- epilogue: warps 2..17 ----------------
-    const int quarter = warp & 3;
-    const int part = (warp - 2) >> 2;
-    // each warp takes kHalfCols consecutive columns; a query's Hi columns stay in one warp
-    constexpr int kHalfCols = HI > 64 ? HI : 64;
-    const int col0 = part * kHalfCols;
-    const bool active = col0 < kScoreN;
-    const uint32_t lane_addr = tmem_lane_base(warp);
-    for (int j = 0; j < nbt; ++j) {
-      const int buf = j & 1;
-      // one decision per warp, taken after every lane's wait: tcgen05.ld is warp-aligned
-      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], (j >> 1) & 1, abort_flag, a.err))) break;
-      tc_fence_after();
-      if (active) {
-        const int blk = rot_tile(j, jrot, nbt) * kScoreM + quarter * 32 + lane;
-        float carry = 0.f;
-#pragma unroll 1
-        for (int cc = col0; cc < col0 + kHalfCols; cc += 64) {
-          float v2[2][32];
-          tmem_ld32(tbase + lane_addr + buf * kScoreN + cc, v2[0]);
-          if (kHalfCols > 32) tmem_ld32(tbase + lane_addr + buf * kScoreN + cc + 32, v2[1]);
-          tmem_ld_wait_regs(v2[0]);
-          tmem_ld_wait_regs(v2[1]);
-#pragma unroll
-          for (int half2 = 0; half2 < 2; ++half2) {
-          if (half2 == 1 && kHalfCols <= 32) break;
-          const int ccx = cc + 32 * half2;
-          const float* v = v2[half2];
-          const float4* w4 = reinterpret_cast<const float4*>(sW + ccx);
-          // per query: 4 interleaved FMA chains over its heads (h mod 4), then combined;
-          // prod[q0] holds the sum of the group of columns starting at q0
-          float prod[32];
-          constexpr int G = HI < 32 ? HI : 32;        // columns of one query inside this chunk
-          constexpr int CH = G < 4 ? G : 4;           // independent chains per query
-#pragma unroll
-          for (int q0 = 0; q0 < 32; q0 += G) {
-            float acc4[CH];
-#pragma unroll
-            for (int cidx = 0; cidx < CH; ++cidx) acc4[cidx] = 0.f;
-#pragma unroll
-            for (int k = 0; k < G; ++k) acc4[k % CH] = fmaf(w4f(w4, q0 + k), fmaxf(v[q0 + k], 0.f), acc4[k % CH]);
-            float sum = acc4[0];
-#pragma unroll
-            for (int cidx = 1; cidx < CH; ++cidx) sum += acc4[cidx];
-            prod[q0] = sum;
-          }
-          if constexpr (HI <= 32) {
-#pragma unroll
-            for (int k = 0; k < 32; k += HI) {
-              const int qi = (ccx + k) / HI;
-              if (blk < sNvis[qi]) a.scores[(long long)(t0 + qi) * a.ldS + blk] = prod[k];
-            }
-          } else {
-            carry += prod[0];
-            if (((ccx + 32) & (HI - 1)) == 0) {
-              const int qi = ccx / HI;
-              if (blk < sNvis[qi]) a.scores[(long long)(t0 + qi) * a.ldS + blk] = carry;
-              carry = 0.f;
-            }
-          }
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tbase, 2 * kScoreN);
-  }
 }
 
 // =====================================================================================
@@ -807,37 +560,13 @@ __global__ void __launch_bounds__(128) compose_window_kernel(const int32_t* __re
 // =====================================================================================
 // host launchers
 // =====================================================================================
-template <int DI>
-static cudaError_t launch_score_di(int Hi, int grid, size_t smem, cudaStream_t st, const CUtensorMap& tq,
-                                   const CUtensorMap& tk, const ScoreArgs& sa) {
-  switch (Hi) {
-    case 1: score_kernel<DI, 1><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
-    case 2: score_kernel<DI, 2><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
-    case 4: score_kernel<DI, 4><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
-    case 8: score_kernel<DI, 8><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
-    case 16: score_kernel<DI, 16><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
-    case 32: score_kernel<DI, 32><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
-    case 64: score_kernel<DI, 64><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
-    case 128: score_kernel<DI, 128><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
-    default: score_kernel<DI, 256><<<grid, kScoreThreads, smem, st>>>(tq, tk, sa); break;
-  }
-  return cudaGetLastError();
-}
-
-static cudaError_t launch_score(int Di, int Hi, int grid, size_t smem, cudaStream_t st, const CUtensorMap& tq,
-                                const CUtensorMap& tk, const ScoreArgs& sa) {
-  return Di == 64 ? launch_score_di<64>(Hi, grid, smem, st, tq, tk, sa)
-                  : launch_score_di<128>(Hi, grid, smem, st, tq, tk, sa);
-}
-
 IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len, bool with_scores) {
   IndexPlan p{};
   p.kb = budget / c;
-  p.QT = kScoreN / Hi;
+  p.QT = kIdxN / Hi;
   p.tau_sparse = (p.kb + 1) * c - 1;
   p.nblk_cap = T / c > 0 ? T / c : 1;
   p.ldS = max_doc_len / c > 0 ? max_doc_len / c : 1;
-  p.score_tiles_cap = (T + p.QT - 1) / p.QT + ndocs;
   size_t off = 0;
   auto take = [&](size_t bytes, size_t align) {
     off = (off + align - 1) / align * align;
@@ -851,10 +580,8 @@ IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int ma
   p.off_kbar = take((size_t)p.nblk_cap * Di * 2, 1024);
   p.off_scores = with_scores ? take((size_t)T * p.ldS * sizeof(float), 1024) : 0;
   p.ws_bytes = (off + 255) / 256 * 256;
-  p.stages = Di == 64 ? 6 : 4;
-  const size_t b_bytes = (size_t)kScoreN * Di * 2;
-  const size_t a_bytes = (size_t)p.stages * kScoreM * Di * 2;
-  p.score_smem = 1024 + b_bytes + a_bytes + kScoreN * 8 + (2 * p.stages + 5) * 8 + 16;
+  p.stages = Di == 64 ? 8 : 5;
+  p.score_smem = Di == 64 ? IdxSmem<64>::total(p.stages) : IdxSmem<128>::total(p.stages);
   p.topk_smem = topk_smem_bytes(p.ldS, p.kb);
   return p;
 }
@@ -867,7 +594,7 @@ size_t topk_smem_bytes(int nvis_cap, int kb) {
 cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI, const float* w,
                          const int32_t* cu, int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
                          int32_t* route, float* scores, int64_t ldS, uint8_t* ws, int32_t* err,
-                         const CUtensorMap& tm_q, const CUtensorMap& tm_k, cudaStream_t stream) {
+                         const CUtensorMap& tm_q, const CUtensorMap& tm_k, int num_sms, cudaStream_t stream) {
   int32_t* meta = reinterpret_cast<int32_t*>(ws + p.off_meta);
   int32_t* blk_off = reinterpret_cast<int32_t*>(ws + p.off_blk);
   int32_t* tile_off = reinterpret_cast<int32_t*>(ws + p.off_tile);
@@ -878,11 +605,12 @@ cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv
   {
     const long long threads = (long long)p.nblk_cap * (Di / 8);
     const int grid = (int)((threads + 255) / 256);
-    pool_kernel<<<grid, 256, 0, stream>>>(kI, cu, ndocs, Di, c, meta, blk_off, kbar);
+    pool_kernel<<<grid, 256, 0, stream>>>(kI, cu, ndocs, Di, c, p.nblk_cap, meta, blk_off, kbar);
   }
-  ScoreArgs sa{w, cu, blk_off, tile_off, meta, scores, ldS, err, ndocs, T, Hi, c, p.kb, p.QT, p.tau_sparse,
-               p.stages};
-  const cudaError_t le = launch_score(Di, Hi, p.score_tiles_cap, p.score_smem, stream, tm_q, tm_k, sa);
+  IndexArgs ia{w, cu, blk_off, tile_off, meta, scores, ldS, err, ndocs, T, c, p.QT, p.tau_sparse, p.stages};
+  const int grid = num_sms < kMaxIndexCtas ? num_sms : kMaxIndexCtas;
+  const cudaError_t le = Di == 64 ? launch_score_64(Hi, grid, p.score_smem, stream, tm_q, tm_k, ia)
+                                  : launch_score_128(Hi, grid, p.score_smem, stream, tm_q, tm_k, ia);
   if (le != cudaSuccess) return le;
   TopkArgs ta{scores, ldS, cu, meta, route, err, ndocs, T, c, budget, max_doc_len, (int)p.ldS};
   return launch_topk(ta, p.kb, stream, p.topk_smem);
@@ -901,25 +629,10 @@ cudaError_t launch_compose_window(const int32_t* route, int W, const int32_t* cu
   return cudaGetLastError();
 }
 
-template <int DI, int HI>
-static cudaError_t score_attr(size_t smem) {
-  return cudaFuncSetAttribute(score_kernel<DI, HI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-}
-
-template <int DI>
-static cudaError_t score_attr_all(size_t smem) {
-  cudaError_t e = cudaSuccess;
-  for (cudaError_t x : {score_attr<DI, 1>(smem), score_attr<DI, 2>(smem), score_attr<DI, 4>(smem),
-                        score_attr<DI, 8>(smem), score_attr<DI, 16>(smem), score_attr<DI, 32>(smem),
-                        score_attr<DI, 64>(smem), score_attr<DI, 128>(smem), score_attr<DI, 256>(smem)})
-    if (x != cudaSuccess) e = x;
-  return e;
-}
-
 cudaError_t configure_score_kernels(size_t smem) {
-  cudaError_t e = score_attr_all<64>(smem);
+  cudaError_t e = configure_score_64(smem);
   if (e != cudaSuccess) return e;
-  return score_attr_all<128>(smem);
+  return configure_score_128(smem);
 }
 
 cudaError_t configure_topk_kernel(size_t smem) {

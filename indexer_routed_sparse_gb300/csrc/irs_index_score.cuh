@@ -1,0 +1,437 @@
+// The persistent block-score kernel of the indexer (weighted-ReLU scores on tcgen05).
+// Included by irs_index.cu and by the two translation units that instantiate the kernel
+// for Di = 64 and Di = 128 (compiled in parallel).
+//
+// Definitions follow the QSA page (nemo_automodel.components.models.qwen3_8_flash_next.qsa:
+// `select_qsa_token_ids`, `Qwen3_8_FlashNextQSAIndexer`) and the Step-5 sparse page
+// (nemo_automodel.components.models.step5.sparse: `indexer_score_tile`, `pack_region_bitmap`).
+#pragma once
+
+#include "irs_internal.h"
+#include "irs_ptx.cuh"
+
+namespace irs {
+
+// Document containing token t: largest d with cu[d] <= t (cu strictly increasing).
+__device__ __forceinline__ int find_doc(const int32_t* __restrict__ cu, int ndocs, int t) {
+  int lo = 0, hi = ndocs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Largest d in [0, n) with off[d] <= x (off non-decreasing, off[0] = 0 <= x).
+__device__ __forceinline__ int find_le(const int32_t* __restrict__ off, int n, int x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// =====================================================================================
+// a3: weighted-ReLU block scores on tcgen05, one persistent kernel.
+//
+// Work: tiles of QT = 256/Hi consecutive sparse queries of one document, heaviest first
+// (later tiles of a document see more blocks); CTAs take tiles from a device counter.
+//
+// The contraction runs transposed: UMMA M = 128 pooled key blocks (one TMEM lane each),
+// N = QT*Hi = 256 (query, head) columns, K = Di. The query tile (B operand, TMA) is
+// double-buffered across tiles, so the next tile's queries load while the current one's
+// key tiles run; key tiles (A operand) stream through a TMA ring of 64-dim atoms; two TMEM
+// accumulators (2 x 256 columns) let the epilogue of one key tile overlap the MMAs of the
+// next. The epilogue thread of lane b reduces each query's heads in order,
+// s = sum_h w[t,h] * max(acc, 0) (FP32 FMA chains), and writes row t of the FP32 scores.
+//
+// Warps: 0 scheduler + TMA producer (+ head weights), 1 TMEM owner + MMA issuer,
+// 2..9 epilogue (two per TMEM lane quarter, 128 columns each). Every cross-warp wait is a
+// bounded mbarrier wait.
+// =====================================================================================
+constexpr int kIdxThreads = 320;      // producer, MMA issuer, 8 epilogue warps
+constexpr int kIdxN = 256;           // (query, head) columns per tile
+constexpr int kIdxM = 128;           // key blocks per key tile
+constexpr int kEpiWarp0 = 2;
+constexpr int kNumEpi = 8;
+constexpr int kTileSlots = 4;
+constexpr int kIdxAtom = kIdxM * 128;   // bytes of one 64-dim atom of a key tile
+enum { kTileSparse = 0, kTileStop = 2 };
+
+struct TileInfo {
+  int kind, t0, n, s_doc, tau0, nbt, blk0, jrot;
+};
+
+struct IndexArgs {
+  const float* w;
+  const int32_t* cu;
+  const int32_t* blk_off;
+  const int32_t* tile_off;
+  int32_t* meta;      // [0] layout valid, [1] pooled blocks, [2] score tiles, [3] tile counter
+  float* scores;      // row t at t * ldS
+  int64_t ldS;
+  int32_t* err;
+  int ndocs, T, c, QT, tau_sparse, stages;
+};
+
+__device__ __forceinline__ int rot_tile(int j, int jrot, int nbt) {
+  const int r = j + jrot;
+  return r >= nbt ? r - nbt : r;
+}
+
+static __device__ TileInfo decode_tile(const IndexArgs& a, int id, int nsparse) {
+  TileInfo ti{};
+  ti.kind = kTileStop;
+  if (id < nsparse) {
+    const int tile = nsparse - 1 - id;   // later tiles of a document see more blocks: heaviest first
+    const int d = find_le(a.tile_off, a.ndocs, tile);
+    const int s = a.cu[d], L = a.cu[d + 1] - s;
+    ti.kind = kTileSparse;
+    ti.s_doc = s;
+    ti.tau0 = a.tau_sparse + (tile - a.tile_off[d]) * a.QT;
+    ti.n = min(a.QT, L - ti.tau0);
+    ti.t0 = s + ti.tau0;
+    ti.nbt = ((ti.tau0 + ti.n) / a.c + kIdxM - 1) / kIdxM;
+    ti.blk0 = a.blk_off[d];
+    // tiles start at different key tiles, so concurrent CTAs of one document do not all
+    // read the same pooled keys from L2 at the same moment
+    ti.jrot = id % max(ti.nbt, 1);
+  }
+  return ti;
+}
+
+__device__ __forceinline__ float w4f(const float4* w4, int k) {
+  const float4 v = w4[k >> 2];
+  return (k & 3) == 0 ? v.x : ((k & 3) == 1 ? v.y : ((k & 3) == 2 ? v.z : v.w));
+}
+
+template <int DI>
+struct IdxSmem {
+  static constexpr uint32_t kBAtom = kIdxN * 128;
+  static constexpr uint32_t kBBytes = (DI / 64) * kBAtom;
+  static constexpr uint32_t b_off = 0;                                   // [2] query tiles
+  static constexpr uint32_t a_off = 2 * kBBytes;                         // [stages] key atoms
+  __host__ __device__ static uint32_t w_off(int st) { return a_off + (uint32_t)st * kIdxAtom; }   // [2][256] fp32
+  __host__ __device__ static uint32_t part_off(int st) { return w_off(st) + 2 * kIdxN * 4; }      // [2][128] fp32
+  __host__ __device__ static uint32_t tile_off(int st) { return part_off(st) + 2 * 128 * 4; }
+  __host__ __device__ static uint32_t bar_off(int st) { return tile_off(st) + kTileSlots * sizeof(TileInfo); }
+  __host__ __device__ static uint32_t total(int st) { return bar_off(st) + (2 * st + 17) * 8 + 16 + 1024; }
+};
+
+template <int DI, int HI>
+__global__ void __launch_bounds__(kIdxThreads, 1)
+    score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       IndexArgs a) {
+  constexpr int KATOMS = DI / 64;
+  using L = IdxSmem<DI>;
+  constexpr uint32_t IDESC = idesc_bf16(kIdxM, kIdxN, false, false);
+  constexpr int kColsPerWarp = kIdxN / 2;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = a.stages;
+  uint8_t* sB = smem + L::b_off;
+  uint8_t* sA = smem + L::a_off;
+  float* sW = reinterpret_cast<float*>(smem + L::w_off(S));
+  float* sPart = reinterpret_cast<float*>(smem + L::part_off(S));
+  TileInfo* sTile = reinterpret_cast<TileInfo*>(smem + L::tile_off(S));
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + L::bar_off(S));
+  uint64_t* a_empty = a_full + S;
+  uint64_t* b_full = a_empty + S;        // [2]
+  uint64_t* b_empty = b_full + 2;        // [2]
+  uint64_t* t_full = b_empty + 2;        // [2]
+  uint64_t* t_empty = t_full + 2;        // [2]
+  uint64_t* tile_full = t_empty + 2;     // [4]
+  uint64_t* tile_empty = tile_full + 4;  // [4]
+  uint64_t* drain = tile_empty + 4;      // [1]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+
+  if (a.meta[0] != 1) return;   // malformed cu_seqlens: reported by the layout kernel
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) { mbar_init(&a_full[s], 1); mbar_init(&a_empty[s], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&b_full[i], 1 + 32);           // the TMA issuer's arrival + every producer lane (weights)
+      mbar_init(&b_empty[i], 1 + kNumEpi);     // the last MMA of the tile + every epilogue warp
+      mbar_init(&t_full[i], 1);
+      mbar_init(&t_empty[i], kNumEpi);
+    }
+    for (int i = 0; i < kTileSlots; ++i) {
+      mbar_init(&tile_full[i], 1);
+      mbar_init(&tile_empty[i], 1 + kNumEpi);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 2 * kIdxN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == 0) {
+    // ---------------- scheduler + TMA producer (whole warp; lane 0 issues) ----------------
+    const int nsparse = a.meta[2];
+    if (lane == 0) { tma_prefetch_map(&tm_q); tma_prefetch_map(&tm_k); }
+    uint32_t i = 0, nb = 0, at = 0;
+    while (true) {
+      const int slot = i & (kTileSlots - 1);
+      if (i >= kTileSlots &&
+          !__all_sync(0xffffffffu, mbar_wait(&tile_empty[slot], ((i / kTileSlots) - 1) & 1, abort_flag, a.err)))
+        break;
+      int id = 0;
+      if (lane == 0) id = atomicAdd(&a.meta[3], 1);
+      id = __shfl_sync(0xffffffffu, id, 0);
+      const TileInfo ti = decode_tile(a, id, nsparse);
+      if (lane == 0) sTile[slot] = ti;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tile_full[slot]);
+      ++i;
+      if (ti.kind == kTileStop) break;
+      const int bs = nb & 1;
+      if (nb >= 2 && !__all_sync(0xffffffffu, mbar_wait(&b_empty[bs], ((nb >> 1) - 1) & 1, abort_flag, a.err)))
+        break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&b_full[bs], L::kBBytes);
+        for (int ka = 0; ka < KATOMS; ++ka)
+          tma_load_2d(sB + bs * L::kBBytes + ka * L::kBAtom, &tm_q, ka * 64, ti.t0 * HI, &b_full[bs]);
+      }
+      // head weights of the tile's (query, head) columns (zero past the last token); all
+      // loads are issued before the stores
+      {
+        float wv[kIdxN / 32];
+#pragma unroll
+        for (int k = 0; k < kIdxN / 32; ++k) {
+          const long long gi = (long long)ti.t0 * HI + k * 32 + lane;
+          wv[k] = gi < (long long)a.T * HI ? __ldg(a.w + gi) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kIdxN / 32; ++k) sW[bs * kIdxN + k * 32 + lane] = wv[k];
+      }
+      mbar_arrive(&b_full[bs]);
+      ++nb;
+      bool ok = true;
+      if (lane == 0) {
+        for (int j = 0; j < ti.nbt && ok; ++j) {
+          const int bt = rot_tile(j, ti.jrot, ti.nbt);
+          for (int ka = 0; ka < KATOMS; ++ka, ++at) {
+            const int st = at % S;
+            if (at >= (uint32_t)S && !mbar_wait(&a_empty[st], ((at / S) - 1) & 1, abort_flag, a.err)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&a_full[st], kIdxAtom);
+            tma_load_2d(sA + (size_t)st * kIdxAtom, &tm_k, ka * 64, ti.blk0 + bt * kIdxM, &a_full[st]);
+          }
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, (int)ok, 0)) break;
+    }
+    if (lane == 0 && *abort_flag) {
+      // let the copies still in flight land before the CTA leaves
+      const uint32_t first = at > (uint32_t)S ? at - S : 0;
+      for (uint32_t x = first; x < at; ++x) {
+        const unsigned long long t0 = globaltimer_ns();
+        while (!mbar_try_wait(&a_full[x % S], (x / S) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+      }
+      for (uint32_t x = nb > 2 ? nb - 2 : 0; x < nb; ++x) {
+        const unsigned long long t0 = globaltimer_ns();
+        while (!mbar_try_wait(&b_full[x & 1], (x >> 1) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t i = 0, nb = 0, at = 0, kt = 0;
+      bool alive = true;
+      while (alive) {
+        const int slot = i & (kTileSlots - 1);
+        if (!mbar_wait(&tile_full[slot], (i / kTileSlots) & 1, abort_flag, a.err)) break;
+        const TileInfo ti = sTile[slot];
+        mbar_arrive(&tile_empty[slot]);
+        ++i;
+        if (ti.kind == kTileStop) break;
+        const int bs = nb & 1;
+        if (!mbar_wait(&b_full[bs], (nb >> 1) & 1, abort_flag, a.err)) break;
+        const uint32_t b_base = smem_u32(sB + bs * L::kBBytes);
+        for (int j = 0; j < ti.nbt && alive; ++j, ++kt) {
+          const int buf = kt & 1;
+          if (kt >= 2 && !mbar_wait(&t_empty[buf], ((kt >> 1) - 1) & 1, abort_flag, a.err)) { alive = false; break; }
+          for (int ka = 0; ka < KATOMS; ++ka, ++at) {
+            const int st = at % S;
+            if (!mbar_wait(&a_full[st], (at / S) & 1, abort_flag, a.err)) { alive = false; break; }
+            tc_fence_after();
+            const uint64_t ad = sdesc_sw128(smem_u32(sA + (size_t)st * kIdxAtom), 16, 1024);
+            const uint64_t bd = sdesc_sw128(b_base + ka * L::kBAtom, 16, 1024);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_bf16(tbase + buf * kIdxN, ad + (uint64_t)((ks * 32) >> 4), bd + (uint64_t)((ks * 32) >> 4), IDESC,
+                        (ka > 0 || ks > 0) ? 1u : 0u);
+            umma_commit(&a_empty[st]);
+          }
+          if (!alive) break;
+          umma_commit(&t_full[buf]);
+        }
+        if (!alive) break;
+        umma_commit(&b_empty[bs]);
+        ++nb;
+      }
+      // every issued MMA completes before the CTA releases its tensor memory
+      umma_commit(drain);
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+    }
+  } else {
+    // ---------------- epilogue: warps 2..9 ----------------
+    const int e = warp - kEpiWarp0;
+    const int quarter = warp & 3;
+    const int col0 = (e >> 2) * kColsPerWarp;
+    const uint32_t lane_addr = tmem_lane_base(warp);
+    uint32_t i = 0, nb = 0, kt = 0;
+    bool alive = true;
+    while (alive) {
+      const int slot = i & (kTileSlots - 1);
+      if (!__all_sync(0xffffffffu, mbar_wait(&tile_full[slot], (i / kTileSlots) & 1, abort_flag, a.err))) break;
+      const TileInfo ti = sTile[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tile_empty[slot]);
+      ++i;
+      if (ti.kind == kTileStop) break;
+      {
+        const int bs = nb & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&b_full[bs], (nb >> 1) & 1, abort_flag, a.err))) break;
+        const float* wt = sW + bs * kIdxN;
+        for (int j = 0; j < ti.nbt; ++j, ++kt) {
+          const int buf = kt & 1;
+          // one decision per warp, taken after every lane's wait: tcgen05.ld is warp-aligned
+          if (!__all_sync(0xffffffffu, mbar_wait(&t_full[buf], (kt >> 1) & 1, abort_flag, a.err))) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const int blk = rot_tile(j, ti.jrot, ti.nbt) * kIdxM + quarter * 32 + lane;
+          // query q of the tile sees block blk iff (blk+1)*c - 1 <= tau0 + q
+          const int qmin = (blk + 1) * a.c - 1 - ti.tau0;
+          float carry = 0.f;
+#pragma unroll 1
+          for (int cc = col0; cc < col0 + kColsPerWarp; cc += 64) {
+            float v2[2][32];
+            tmem_ld32(tbase + lane_addr + buf * kIdxN + cc, v2[0]);
+            tmem_ld32(tbase + lane_addr + buf * kIdxN + cc + 32, v2[1]);
+            tmem_ld_wait_regs(v2[0]);
+            tmem_ld_wait_regs(v2[1]);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int ccx = cc + 32 * h2;
+              const float* v = v2[h2];
+              const float4* w4 = reinterpret_cast<const float4*>(wt + ccx);
+              // per query: 4 interleaved FMA chains over its heads (h mod 4), then combined;
+              // prod[q0] holds the sum of the group of columns starting at q0
+              float prod[32];
+              constexpr int G = HI < 32 ? HI : 32;   // columns of one query inside this chunk
+              constexpr int CH = G < 4 ? G : 4;      // independent chains per query
+#pragma unroll
+              for (int q0 = 0; q0 < 32; q0 += G) {
+                float acc4[CH];
+#pragma unroll
+                for (int x = 0; x < CH; ++x) acc4[x] = 0.f;
+#pragma unroll
+                for (int k = 0; k < G; ++k) acc4[k % CH] = fmaf(w4f(w4, q0 + k), fmaxf(v[q0 + k], 0.f), acc4[k % CH]);
+                float sum = acc4[0];
+#pragma unroll
+                for (int x = 1; x < CH; ++x) sum += acc4[x];
+                prod[q0] = sum;
+              }
+              if constexpr (HI <= 32) {
+#pragma unroll
+                for (int k = 0; k < 32; k += HI) {
+                  const int qi = (ccx + k) / HI;
+                  if (qi >= qmin && qi < ti.n) a.scores[(int64_t)(ti.t0 + qi) * a.ldS + blk] = prod[k];
+                }
+              } else {
+                carry += prod[0];
+                if constexpr (HI <= kColsPerWarp) {
+                  if (((ccx + 32) & (HI - 1)) == 0) {
+                    const int qi = ccx / HI;
+                    if (qi >= qmin && qi < ti.n) a.scores[(int64_t)(ti.t0 + qi) * a.ldS + blk] = carry;
+                    carry = 0.f;
+                  }
+                }
+              }
+            }
+          }
+          if constexpr (HI > kColsPerWarp) {
+            // one query spans both column halves: the upper half's warp hands its partial
+            // sum to the lower half's warp of the same lane quarter (fixed order)
+            float* part = sPart + (kt & 1) * 128 + quarter * 32;
+            if (col0 != 0) part[lane] = carry;
+            named_bar_sync(1 + quarter, 64);
+            if (col0 == 0 && 0 >= qmin && ti.n > 0) a.scores[(int64_t)ti.t0 * a.ldS + blk] = carry + part[lane];
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&t_empty[buf]);
+        }
+        if (!alive) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&b_empty[bs]);   // this warp no longer reads the tile's weights
+        ++nb;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 2 * kIdxN);
+  }
+}
+
+// Host side of the Di-specific translation units.
+template <int DI>
+static cudaError_t launch_score_di(int Hi, int grid, size_t smem, cudaStream_t st, const CUtensorMap& tq,
+                                   const CUtensorMap& tk, const IndexArgs& ia) {
+  switch (Hi) {
+    case 1: score_kernel<DI, 1><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 2: score_kernel<DI, 2><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 4: score_kernel<DI, 4><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 8: score_kernel<DI, 8><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 16: score_kernel<DI, 16><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 32: score_kernel<DI, 32><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 64: score_kernel<DI, 64><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 128: score_kernel<DI, 128><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    default: score_kernel<DI, 256><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+  }
+  return cudaGetLastError();
+}
+
+template <int DI, int HI>
+static cudaError_t score_attr(size_t smem) {
+  return cudaFuncSetAttribute(score_kernel<DI, HI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+template <int DI>
+static cudaError_t score_attr_all(size_t smem) {
+  cudaError_t e = cudaSuccess;
+  for (cudaError_t x : {score_attr<DI, 1>(smem), score_attr<DI, 2>(smem), score_attr<DI, 4>(smem),
+                        score_attr<DI, 8>(smem), score_attr<DI, 16>(smem), score_attr<DI, 32>(smem),
+                        score_attr<DI, 64>(smem), score_attr<DI, 128>(smem), score_attr<DI, 256>(smem)})
+    if (x != cudaSuccess) e = x;
+  return e;
+}
+
+
+cudaError_t launch_score_64(int Hi, int grid, size_t smem, cudaStream_t st, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const IndexArgs& ia);
+cudaError_t launch_score_128(int Hi, int grid, size_t smem, cudaStream_t st, const CUtensorMap& tq,
+                             const CUtensorMap& tk, const IndexArgs& ia);
+cudaError_t configure_score_64(size_t smem);
+cudaError_t configure_score_128(size_t smem);
+
+}  // namespace irs

@@ -12,14 +12,15 @@
 namespace irs {
 
 // Sizes and scratch offsets of one indexer call.
+constexpr int kMaxIndexCtas = 160;   // persistent CTAs of the score kernel (>= one per SM)
+
 struct IndexPlan {
   int kb;              // blocks kept per query (budget / c)
   int QT;              // queries per score tile (256 / Hi)
   int tau_sparse;      // first document-local position with more than kb visible blocks
   int nblk_cap;        // rows of the pooled-key buffer (T / c)
   int64_t ldS;         // row stride of the score buffer (max_doc_len / c)
-  int score_tiles_cap; // grid of the score kernel (upper bound on tiles)
-  int stages;          // key-tile ring depth of the score kernel
+  int stages;          // 64-dim key atoms in the score kernel's TMA ring
   size_t off_meta, off_blk, off_tile, off_kbar, off_scores, ws_bytes;
   size_t score_smem, topk_smem;
 };
@@ -32,7 +33,7 @@ cudaError_t configure_topk_kernel(size_t smem);
 cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI, const float* w,
                          const int32_t* cu, int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
                          int32_t* route, float* scores, int64_t ldS, uint8_t* ws, int32_t* err,
-                         const CUtensorMap& tm_q, const CUtensorMap& tm_k, cudaStream_t stream);
+                         const CUtensorMap& tm_q, const CUtensorMap& tm_k, int num_sms, cudaStream_t stream);
 cudaError_t launch_topk_from_scores(const float* scores, int64_t ldS, const int32_t* cu, int ndocs, int max_doc_len,
                                     int T, int c, int budget, int32_t* route, int32_t* err, cudaStream_t stream);
 cudaError_t launch_compose_window(const int32_t* route, int W, const int32_t* cu, int ndocs, int T, int window,

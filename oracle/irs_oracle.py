@@ -625,13 +625,3 @@ def latent_attention_bwd(q_bits, kv_bits, routes, scale: float, dout_bits, Dv: i
     dkv = dk.astype(np.float64)
     dkv[:, :, :Dv] += dv
     return dq, dkv.astype(np.float32)
-
-
-# --------------------------------------------------------------------------------------
-# counts used by the benchmark's roofline (algorithmic, from the definitions above)
-# --------------------------------------------------------------------------------------
-
-
-def valid_pairs(routes: np.ndarray, Tk: int) -> int:
-    r = np.asarray(routes)
-    return int(np.count_nonzero((r >= 0) & (r < Tk)))
