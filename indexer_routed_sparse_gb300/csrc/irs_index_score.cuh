@@ -129,7 +129,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   constexpr int kColsPerWarp = kIdxN / 2;
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // aligned by pointer arithmetic on the __shared__ array, so that accesses through these
+  // pointers compile to shared-memory instructions
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int S = a.stages;
   uint8_t* sB = smem + L::b_off;
   uint8_t* sA = smem + L::a_off;
@@ -319,49 +321,53 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           // query q of the tile sees block blk iff (blk+1)*c - 1 <= tau0 + q
           const int qmin = (blk + 1) * a.c - 1 - ti.tau0;
           float carry = 0.f;
-#pragma unroll 1
-          for (int cc = col0; cc < col0 + kColsPerWarp; cc += 64) {
-            float v2[2][32];
-            tmem_ld32(tbase + lane_addr + buf * kIdxN + cc, v2[0]);
-            tmem_ld32(tbase + lane_addr + buf * kIdxN + cc + 32, v2[1]);
-            tmem_ld_wait_regs(v2[0]);
-            tmem_ld_wait_regs(v2[1]);
+          // the second 64 columns are read from TMEM while the first 64 are reduced
+          float v[4][32];
+          tmem_ld32(tbase + lane_addr + buf * kIdxN + col0, v[0]);
+          tmem_ld32(tbase + lane_addr + buf * kIdxN + col0 + 32, v[1]);
+          tmem_ld_wait_regs(v[0]);
+          tmem_ld_wait_regs(v[1]);
+          tmem_ld32(tbase + lane_addr + buf * kIdxN + col0 + 64, v[2]);
+          tmem_ld32(tbase + lane_addr + buf * kIdxN + col0 + 96, v[3]);
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const int ccx = cc + 32 * h2;
-              const float* v = v2[h2];
-              const float4* w4 = reinterpret_cast<const float4*>(wt + ccx);
-              // per query: 4 interleaved FMA chains over its heads (h mod 4), then combined;
-              // prod[q0] holds the sum of the group of columns starting at q0
-              float prod[32];
-              constexpr int G = HI < 32 ? HI : 32;   // columns of one query inside this chunk
-              constexpr int CH = G < 4 ? G : 4;      // independent chains per query
+          for (int c4 = 0; c4 < 4; ++c4) {
+            if (c4 == 2) {
+              tmem_ld_wait_regs(v[2]);
+              tmem_ld_wait_regs(v[3]);
+            }
+            const int ccx = col0 + 32 * c4;
+            const float4* w4 = reinterpret_cast<const float4*>(wt + ccx);
+            // per query: 4 interleaved FMA chains over its heads (h mod 4), then combined;
+            // prod[q0] holds the sum of the group of columns starting at q0
+            float prod[32];
+            constexpr int G = HI < 32 ? HI : 32;   // columns of one query inside this chunk
+            constexpr int CH = G < 4 ? G : 4;      // independent chains per query
 #pragma unroll
-              for (int q0 = 0; q0 < 32; q0 += G) {
-                float acc4[CH];
+            for (int q0 = 0; q0 < 32; q0 += G) {
+              float acc4[CH];
 #pragma unroll
-                for (int x = 0; x < CH; ++x) acc4[x] = 0.f;
+              for (int x = 0; x < CH; ++x) acc4[x] = 0.f;
 #pragma unroll
-                for (int k = 0; k < G; ++k) acc4[k % CH] = fmaf(w4f(w4, q0 + k), fmaxf(v[q0 + k], 0.f), acc4[k % CH]);
-                float sum = acc4[0];
+              for (int k = 0; k < G; ++k)
+                acc4[k % CH] = fmaf(w4f(w4, q0 + k), fmaxf(v[c4][q0 + k], 0.f), acc4[k % CH]);
+              float sum = acc4[0];
 #pragma unroll
-                for (int x = 1; x < CH; ++x) sum += acc4[x];
-                prod[q0] = sum;
+              for (int x = 1; x < CH; ++x) sum += acc4[x];
+              prod[q0] = sum;
+            }
+            if constexpr (HI <= 32) {
+#pragma unroll
+              for (int k = 0; k < 32; k += HI) {
+                const int qi = (ccx + k) / HI;
+                if (qi >= qmin && qi < ti.n) a.scores[(int64_t)(ti.t0 + qi) * a.ldS + blk] = prod[k];
               }
-              if constexpr (HI <= 32) {
-#pragma unroll
-                for (int k = 0; k < 32; k += HI) {
-                  const int qi = (ccx + k) / HI;
-                  if (qi >= qmin && qi < ti.n) a.scores[(int64_t)(ti.t0 + qi) * a.ldS + blk] = prod[k];
-                }
-              } else {
-                carry += prod[0];
-                if constexpr (HI <= kColsPerWarp) {
-                  if (((ccx + 32) & (HI - 1)) == 0) {
-                    const int qi = ccx / HI;
-                    if (qi >= qmin && qi < ti.n) a.scores[(int64_t)(ti.t0 + qi) * a.ldS + blk] = carry;
-                    carry = 0.f;
-                  }
+            } else {
+              carry += prod[0];
+              if constexpr (HI <= kColsPerWarp) {
+                if (((ccx + 32) & (HI - 1)) == 0) {
+                  const int qi = ccx / HI;
+                  if (qi >= qmin && qi < ti.n) a.scores[(int64_t)(ti.t0 + qi) * a.ldS + blk] = carry;
+                  carry = 0.f;
                 }
               }
             }
