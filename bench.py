@@ -3,8 +3,8 @@
 One step = one pass of the whole path over one batch of the windowed workload, the largest
 single-GPU configuration that runs every stage (T=65536 single document, Hq=64, Hkv=4,
 Dqk=192, Dv=128; indexer Hi=32, Di=128, c=64, top-16 regions; a 512-token causal window):
-  sparse_index_score_topk (layout, pool, score, top-k + expansion) -> window composition
-  -> sparse_gqa_attn_fwd.
+  sparse_index_score_topk (layout, pool, score, top-k + expansion) -> sparse_gqa_attn_fwd
+  with the window (the window's keys are added inside the attention kernel).
 
 Prints one JSON line (rank 0). `value` is the routed sparse-attention forward rate in
 TFLOP/s over the whole step (algorithmic attention FLOPs / step time, inputs resident in
@@ -59,8 +59,9 @@ def counts(wl, pairs: int | None = None) -> dict:
 
     The number of valid (query, key) pairs is the closed form min(nvis, kb)*c + (tau+1) % c per
     row, except where it depends on data: the latent workload's routes are an input (counted
-    from them) and the windowed workload's composed routes drop indexer IDs inside the window
-    (counted from the routes the step attends, passed in as `pairs`).
+    from them) and the windowed workload's window skips indexer IDs inside it (counted from
+    the step's routes, passed in as `pairs`). The attention reads the indexer's route rows
+    (budget + c - 1 wide); a window adds no reads.
     """
     if wl.latent:
         pairs = int(np.count_nonzero(np.asarray(wl.arrays["route"]) >= 0))
@@ -78,7 +79,7 @@ def counts(wl, pairs: int | None = None) -> dict:
     kb = wl.budget // wl.c
     sparse = nvis > kb
     score_pairs = int(nvis[sparse].sum())
-    W = wl.route_width
+    W = wl.budget + wl.c - 1
     attn_flops = 2.0 * (wl.Dqk + wl.Dv) * wl.Hq * pairs
     attn_bytes = (pairs * wl.Hkv * (wl.Dqk + wl.Dv) * 2          # gathered K and V rows
                   + wl.T * wl.Hq * wl.Dqk * 2                     # Q
@@ -274,8 +275,8 @@ class Path:
         if self.has_index:
             W_idx = wl.budget + wl.c - 1
             self.route_idx = torch.empty((T, W_idx), dtype=torch.int32, device=dev)
-            self.route = (torch.empty((T, wl.route_width), dtype=torch.int32, device=dev) if wl.window
-                          else self.route_idx)
+            # the windowed workload's window is added by the attention kernel itself
+            self.route = self.route_idx
             self.ws = torch.empty(irs.index_workspace_bytes(T, wl.Hi, wl.Di, wl.c, wl.budget, wl.ndocs,
                                                             wl.max_doc_len, True), dtype=torch.uint8, device=dev)
         else:
@@ -290,13 +291,15 @@ class Path:
         self.irs.sparse_index_score_topk(d["qI"], d["kI"], d["w"], d["cu_seqlens"], wl.c, wl.budget, ndocs=wl.ndocs,
                                          max_doc_len=wl.max_doc_len, out=self.route_idx, workspace=self.ws,
                                          err=self.err)
-        if wl.window:
-            self.irs.compose_window_routes(self.route_idx, d["cu_seqlens"], wl.window, out=self.route, err=self.err)
 
     def attend(self):
         wl, d = self.wl, self.d
         if wl.latent:
             self.irs.sparse_gqa_attn_fwd(d["q"], d["kv"], self.kv_v, self.route, wl.scale, out=self.out, lse=self.lse,
+                                         err=self.err)
+        elif wl.window:
+            self.irs.sparse_gqa_attn_fwd(d["q"], d["k"], d["v"], self.route, wl.scale, window=wl.window,
+                                         cu_seqlens=d["cu_seqlens"], ndocs=wl.ndocs, out=self.out, lse=self.lse,
                                          err=self.err)
         else:
             self.irs.sparse_gqa_attn_fwd(d["q"], d["k"], d["v"], self.route, wl.scale, out=self.out, lse=self.lse,
@@ -310,13 +313,26 @@ class Path:
         ids = r[(r >= 0) & (r < self.wl.Tk)].long()
         mask = torch.zeros(self.wl.Tk, dtype=torch.bool, device=self.dev)
         mask[ids] = True
+        if self.has_index and self.wl.window:
+            mask[:self.wl.T] = True   # every token is in its own query's window
         return int(mask.sum().item())
 
     def valid_pairs(self) -> int | None:
-        """Valid pairs where they depend on data (window-composed routes); else None."""
-        if self.has_index and self.wl.window:
-            return int((self.route >= 0).sum().item())
-        return None
+        """Valid pairs where they depend on data (the windowed workload: the window's tokens
+        plus the route IDs before it); else None."""
+        import torch
+
+        wl = self.wl
+        if not (self.has_index and wl.window):
+            return None
+        t = torch.arange(wl.T, device=self.dev, dtype=torch.int64)
+        cu = self.d["cu_seqlens"].long()
+        s = cu[torch.searchsorted(cu, t, right=True) - 1]
+        lo_w = t - wl.window + 1
+        nwin = t - torch.maximum(s, lo_w) + 1
+        r = self.route
+        routed = ((r >= 0) & (r.long() < lo_w[:, None])).sum()
+        return int((nwin.sum() + routed).item())
 
 
 def time_steps(path: Path, steps: int, flush, stream, cold: bool):
@@ -389,7 +405,7 @@ def indexer_report(wl, cnt, idx_ms, idx_warm_ms, peaks) -> dict:
             "roofline_bound": "hbm" if t_hbm >= t_tc else "tensor",
             "roofline_frac": round(roof_s / idx_s, 4), "roofline_us": round(roof_s * 1e6, 2),
             "algorithmic_bytes": int(cnt["idx_bytes"]), "flops": cnt["idx_flops"],
-            "includes_window_composition": bool(wl.window)}
+            "window": "added inside the attention kernel" if wl.window else None}
 
 
 def measure_other_workload(irs, name, args, dev, stream, flush, peaks, l2_gbs) -> dict:
@@ -573,9 +589,9 @@ def run_gpu(args) -> dict | None:
 
 
 def path_kernels(wl) -> int:
-    """Our kernels launched per step: layout, pool, score, top-k (+ window composition) and
-    one attention launch per 8 KV heads."""
-    return (0 if wl.latent else 4) + (1 if wl.window else 0) + (wl.Hkv + 7) // 8
+    """Our kernels launched per step: layout, pool, score, top-k and one attention launch per
+    8 KV heads (the window, where there is one, is added inside the attention kernel)."""
+    return (0 if wl.latent else 4) + (wl.Hkv + 7) // 8
 
 
 def time_backward(args, wl, irs, d, route, kv_v, out, lse, flush, err, stream, dev) -> float:

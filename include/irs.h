@@ -66,6 +66,8 @@ const char* irs_last_error(void);
 
 /*
  * Scratch bytes irs_sparse_index_score_topk needs for these sizes (0 on invalid sizes).
+ * QSA page, `Qwen3_8_FlashNextQSAIndexer` (the pooled keys [B, floor(S/c), 1, D_index]) and
+ * `select_qsa_token_ids` (the FP32 score tensor, which the page bounds by chunking rows).
  * The scratch holds the per-document layout, the pooled bf16 block keys
  * [floor(T/c), Di] and, when the caller passes no score buffer, the FP32 score rows
  * [T, max_doc_len / c].
@@ -96,7 +98,8 @@ size_t irs_index_workspace_bytes(int T, int Hi, int Di, int c, int budget, int n
  * w           fp32 [T, Hi] contiguous
  * cu_seqlens  int32 [ndocs + 1] DEVICE, strictly increasing, 0 .. T
  * ndocs, max_doc_len  host values: number of documents and the longest document
- * T, Hi, Di, c, budget  sizes; 1 <= Hi <= 256, Di in {64, 128}, c >= 1, budget % c == 0
+ * T, Hi, Di, c, budget  sizes; Hi a power of two in [1, 256] (IRS_ERR_VALUE otherwise),
+ *             Di in {64, 128}, c >= 1, budget % c == 0
  * route_ids   int32 [T, budget + c - 1] output
  * scores_dbg  NULL, or fp32 [T, ld_scores] output: for rows with nvis > budget/c the
  *             entries [0, nvis) receive the block scores; other entries are untouched.
@@ -125,9 +128,11 @@ irs_status irs_sparse_index_score_topk(const void* qI, const void* kI, const flo
  *   [floor(T/c), Di] bf16 plus per-document offsets).
  * - The first call on a device looks up the array's device address for that device;
  *   make that first call before any stream capture.
- * - All calls share the one array, which keeps whatever the last call left there (the
- *   kernels write every scratch word they read). Calls whose work overlaps on the GPU
- *   (different streams, or different host threads) race on it: serialise them.
+ * - All calls share the one array, which keeps whatever the last call left there. Each
+ *   call writes every scratch word it later reads (pooled-key rows past the last complete
+ *   block are zeroed, not left over), so nothing of an earlier call leaks into a result.
+ *   Calls whose work overlaps on the GPU (different streams, or different host threads)
+ *   race on it: serialise them.
  */
 irs_status irs_sparse_index_score_topk_noalloc(const void* qI, const void* kI, const float* w,
                                                const int32_t* cu_seqlens, int ndocs, int max_doc_len, int T, int Hi,
@@ -137,7 +142,10 @@ irs_status irs_sparse_index_score_topk_noalloc(const void* qI, const void* kI, c
 /*
  * Top-k, bitmap packing and expansion from given FP32 scores (the second half of
  * irs_sparse_index_score_topk), so that routes can be compared bit for bit with an
- * independent implementation that selects from the same scores.
+ * independent implementation that selects from the same scores. QSA page,
+ * `select_qsa_token_ids` (top budget/c blocks, expanded to token IDs, tail appended);
+ * Step-5 sparse page, `pack_region_bitmap` (the selection as 32-bit words). It runs the
+ * same top-k kernels as irs_sparse_index_score_topk.
  *
  * scores      fp32 [T, ld_scores]; for row t with nvis > budget/c, entries [0, nvis)
  *             are read (NaN is outside the contract); other rows are not read.
@@ -198,6 +206,32 @@ irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_
                                    int64_t v_stride_h, const int32_t* route_ids, int64_t route_stride, int T,
                                    int Tk, int Hq, int Hkv, int Dqk, int Dv, int W, float scale, void* out,
                                    float* lse, int32_t* err_flag, irs_stream_t stream);
+
+/*
+ * sparse_gqa_attn_fwd with a sliding window in front of every route row.
+ *
+ * Step-5 layers page, `Step5Attention` (a query's keys come from a sliding window and from
+ * the indexer's selection). The result equals irs_compose_window_routes followed by
+ * irs_sparse_gqa_attn_fwd, without the composed route tensor: query t (document d =
+ * [s_d, e_d) of cu_seqlens) attends the tokens max(s_d, t - window + 1) .. t, then the
+ * entries of route row t that lie before t - window + 1 (entries inside the window are
+ * skipped, so no key counts twice). Keys are taken in that order, the order of the composed
+ * route, so the outputs are bit-identical to the composed call. The window's keys are not
+ * read from memory: 64 consecutive window tokens load as one TMA row tile when the K/V
+ * rows exceed half the L2.
+ *
+ * cu_seqlens  int32 [ndocs + 1] DEVICE, strictly increasing from 0 to T (as for the
+ *             indexer); ndocs >= 1. Queries and keys share token positions (Tk >= T).
+ * window      >= 1; W + window <= 4096.
+ * Other arguments and limits as for irs_sparse_gqa_attn_fwd; every shape runs the GQA
+ * kernel (latent shapes included).
+ */
+irs_status irs_sparse_gqa_attn_fwd_windowed(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k,
+                                            int64_t k_stride_t, int64_t k_stride_h, const void* v,
+                                            int64_t v_stride_t, int64_t v_stride_h, const int32_t* route_ids,
+                                            int64_t route_stride, const int32_t* cu_seqlens, int ndocs, int window,
+                                            int T, int Tk, int Hq, int Hkv, int Dqk, int Dv, int W, float scale,
+                                            void* out, float* lse, int32_t* err_flag, irs_stream_t stream);
 
 /*
  * sparse_gqa_attn_bwd(q, k, v, route_ids, out, lse, dout, scale) -> dq, dk, dv

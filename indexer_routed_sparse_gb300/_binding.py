@@ -40,6 +40,8 @@ _SIGNATURES = {
     "irs_compose_window_routes": (_I, [_P, _I, _P, _I, _I, _I, _P, _P, _P]),
     "irs_sparse_gqa_attn_fwd": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I, _I, _I, _I, _I, _I,
                                      _I, _F, _P, _P, _P, _P]),
+    "irs_sparse_gqa_attn_fwd_windowed": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _P, _I, _I,
+                                              _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "irs_sparse_gqa_attn_bwd": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _P, _P, _P, _I, _I,
                                      _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
     "irs_check_bounded_wait": (_I, [ctypes.c_uint64, _P, _P]),
@@ -228,14 +230,17 @@ def compose_window_routes(route_ids: torch.Tensor, cu_seqlens: torch.Tensor, win
 
 
 def sparse_gqa_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, route_ids: torch.Tensor,
-                        scale: float | None = None, *, out: torch.Tensor | None = None,
+                        scale: float | None = None, *, window: int = 0, cu_seqlens: torch.Tensor | None = None,
+                        ndocs: int | None = None, out: torch.Tensor | None = None,
                         lse: torch.Tensor | None = None, want_lse: bool = True,
                         err: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor | None]:
     """Sparse attention over routed keys: (out bf16 [T, Hq, Dv], lse fp32 [T, Hq]).
 
     q bf16 [T, Hq, Dqk], k bf16 [Tk, Hkv, Dqk], v bf16 [Tk, Hkv, Dv] (innermost dim
     contiguous; v may be a view of k's leading Dv dims, as in latent attention),
-    route_ids int32 [T, W] with -1 padding.
+    route_ids int32 [T, W] with -1 padding. With window > 0 (and cu_seqlens int32
+    [ndocs + 1]) every query also attends the `window` most recent tokens of its document,
+    in front of its route; route IDs inside the window are skipped.
     """
     _need(q, "q", torch.bfloat16, 3)
     _need(k, "k", torch.bfloat16, 3)
@@ -264,6 +269,19 @@ def sparse_gqa_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, route
         lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
     if err is None:
         err = device_error_flag(dev)
+    if window:
+        if cu_seqlens is None:
+            raise ValueError("a window needs cu_seqlens")
+        _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+        if not cu_seqlens.is_contiguous():
+            raise ValueError("cu_seqlens must be contiguous")
+        nd = cu_seqlens.numel() - 1 if ndocs is None else int(ndocs)
+        st = lib().irs_sparse_gqa_attn_fwd_windowed(
+            _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1), _ptr(v), v.stride(0), v.stride(1),
+            _ptr(route_ids), route_ids.stride(0), _ptr(cu_seqlens), nd, int(window), T, Tk, Hq, Hkv, Dqk, Dv, W,
+            float(scale), _ptr(out), _ptr(lse), _ptr(err), _stream(dev))
+        _check(st, "sparse_gqa_attn_fwd (windowed)")
+        return out, lse
     st = lib().irs_sparse_gqa_attn_fwd(
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1), _ptr(v), v.stride(0), v.stride(1),
         _ptr(route_ids), route_ids.stride(0), T, Tk, Hq, Hkv, Dqk, Dv, W, float(scale), _ptr(out), _ptr(lse),

@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int ST = a.stages;
-  const AttnLayout Ly = attn_layout(a.Dqk, a.Dv, a.W, ST, a.v_alias);
+  const AttnLayout Ly = attn_layout(a.Dqk, a.Dv, a.W + a.window, ST, a.v_alias);
   uint8_t* sQ = smem + Ly.q_off;                                  // [2][16 rows x Dqk]
   uint8_t* sP = smem + Ly.p_off;                                  // [2][16 rows x 128 keys]
   int32_t* sIdx = reinterpret_cast<int32_t*>(smem + Ly.idx_off);  // [idx_words] (producer only)
@@ -338,9 +338,22 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
       const int b = qi & 1;
       const bool ok = mine && (qi < 2 || mbar_wait(&B.idx_empty[b], ((qi >> 1) - 1) & 1, abort_flag, a.err));
       if (!named_bar_and(1, kProducerThreads, ok)) break;
-      // ---- compact the valid IDs of route row t (8 loads in flight per thread) ----
+      // ---- the window's tokens first (no route reads), then the valid IDs of route row t
+      //      below the window (8 loads in flight per thread) ----
       const int32_t* rrow = a.route + t * a.route_stride;
       int run = 0;
+      int lo_w = -1;   // route IDs at or above this are inside the window: skipped
+      if (a.window > 0) {
+        int lo_d = 0, hi_d = a.ndocs - 1;   // document of t: largest d with cu[d] <= t
+        while (lo_d < hi_d) {
+          const int mid = (lo_d + hi_d + 1) >> 1;
+          if (__ldg(a.cu + mid) <= t) lo_d = mid; else hi_d = mid - 1;
+        }
+        lo_w = (int)t - a.window + 1;
+        const int lo = max(max(__ldg(a.cu + lo_d), lo_w), 0);
+        run = max(0, (int)t - lo + 1);
+        for (int i = ptid; i < run; i += kProducerThreads) sIdx[i] = lo + i;
+      }
       for (int base = 0; base < a.W; base += 8 * kProducerThreads) {
         int ids[8];
 #pragma unroll
@@ -353,8 +366,9 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           if (base + k * kProducerThreads >= a.W) break;
           const int i = base + k * kProducerThreads + ptid;
           const int id = ids[k];
-          const bool okid = id >= 0 && id < a.Tk;
-          if (i < a.W && id != -1 && !okid && a.g0 == 0) record_error(a.err, IRS_DEVERR_ROUTE_ID);
+          const bool inrange = id >= 0 && id < a.Tk;
+          if (i < a.W && id != -1 && !inrange && a.g0 == 0) record_error(a.err, IRS_DEVERR_ROUTE_ID);
+          const bool okid = inrange && (a.window == 0 || id < lo_w);
           const uint32_t bal = __ballot_sync(0xffffffffu, okid);
           if (lane == 0) sCnt[warp] = __popc(bal);
           named_bar_sync(1, kProducerThreads);
@@ -529,7 +543,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
     for (long long t = blockIdx.x; t < a.T; t += gridDim.x, ++qi) {
       const int b = qi & 1;
       mbar_wait(&B.idx_full[b], (qi >> 1) & 1, abort_flag, a.err);
-      const int nv = min(max(sNv[b], 0), a.W);
+      const int nv = min(max(sNv[b], 0), a.W + a.window);
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.idx_empty[b]);
       const int nchunks = (nv + kChunk - 1) / kChunk;
@@ -672,9 +686,9 @@ AttnPlan plan_attn(const AttnArgs& a, int num_sms) {
   AttnPlan p{};
   p.items = a.T;
   int st = 4;
-  while (st > 1 && attn_layout(a.Dqk, a.Dv, a.W, st, a.v_alias).total > 227 * 1024) --st;
+  while (st > 1 && attn_layout(a.Dqk, a.Dv, a.W + a.window, st, a.v_alias).total > 227 * 1024) --st;
   p.stages = st;
-  p.smem = attn_layout(a.Dqk, a.Dv, a.W, st, a.v_alias).total;
+  p.smem = attn_layout(a.Dqk, a.Dv, a.W + a.window, st, a.v_alias).total;
   p.grid = (int)(a.T < num_sms ? a.T : num_sms);
   if (p.grid < 1) p.grid = 1;
   p.nh_class = a.HB <= 4 ? 4 : (a.HB <= 8 ? 8 : 16);

@@ -228,11 +228,17 @@ irs_status irs_compose_window_routes(const int32_t* route_ids, int W, const int3
                        "launching window composition");
 }
 
-irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k,
-                                   int64_t k_stride_t, int64_t k_stride_h, const void* v, int64_t v_stride_t,
-                                   int64_t v_stride_h, const int32_t* route_ids, int64_t route_stride, int T,
-                                   int Tk, int Hq, int Hkv, int Dqk, int Dv, int W, float scale, void* out,
-                                   float* lse, int32_t* err_flag, irs_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Forward attention over routes, optionally with a sliding window in front of each route
+// (window > 0: cu_seqlens / ndocs give the documents the window stays inside).
+irs_status attn_fwd_impl(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k, int64_t k_stride_t,
+                         int64_t k_stride_h, const void* v, int64_t v_stride_t, int64_t v_stride_h,
+                         const int32_t* route_ids, int64_t route_stride, int T, int Tk, int Hq, int Hkv, int Dqk,
+                         int Dv, int W, float scale, const int32_t* cu_seqlens, int ndocs, int window, void* out,
+                         float* lse, int32_t* err_flag, irs_stream_t stream) {
   if (T < 0 || Tk < 1 || Hq < 1 || Hkv < 1) return fail(IRS_ERR_VALUE, "bad sizes (T=%d Tk=%d Hq=%d Hkv=%d)", T, Tk, Hq, Hkv);
   if (Hq % Hkv != 0) return fail(IRS_ERR_VALUE, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
   if (Dqk < 64 || Dqk > 576 || Dqk % 64 != 0) return fail(IRS_ERR_VALUE, "Dqk must be a multiple of 64 in [64, 576]");
@@ -270,7 +276,10 @@ irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_
   a.nhb = (a.G + a.HB - 1) / a.HB;
   a.v_alias = (v == k && v_stride_t == k_stride_t && v_stride_h == k_stride_h && Dv <= Dqk) ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
-  if (irs::mla_supported(a)) {
+  a.cu = cu_seqlens;
+  a.ndocs = ndocs;
+  a.window = window;
+  if (window == 0 && irs::mla_supported(a)) {
     const size_t smem = irs::mla_smem_bytes(a);
     {
       std::lock_guard<std::mutex> lk(g_dev_mu);
@@ -318,6 +327,36 @@ irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_
       return s;
   }
   return IRS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k,
+                                   int64_t k_stride_t, int64_t k_stride_h, const void* v, int64_t v_stride_t,
+                                   int64_t v_stride_h, const int32_t* route_ids, int64_t route_stride, int T,
+                                   int Tk, int Hq, int Hkv, int Dqk, int Dv, int W, float scale, void* out,
+                                   float* lse, int32_t* err_flag, irs_stream_t stream) {
+  return attn_fwd_impl(q, q_stride_t, q_stride_h, k, k_stride_t, k_stride_h, v, v_stride_t, v_stride_h, route_ids,
+                       route_stride, T, Tk, Hq, Hkv, Dqk, Dv, W, scale, nullptr, 0, 0, out, lse, err_flag, stream);
+}
+
+irs_status irs_sparse_gqa_attn_fwd_windowed(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k,
+                                            int64_t k_stride_t, int64_t k_stride_h, const void* v,
+                                            int64_t v_stride_t, int64_t v_stride_h, const int32_t* route_ids,
+                                            int64_t route_stride, const int32_t* cu_seqlens, int ndocs, int window,
+                                            int T, int Tk, int Hq, int Hkv, int Dqk, int Dv, int W, float scale,
+                                            void* out, float* lse, int32_t* err_flag, irs_stream_t stream) {
+  if (window < 1) return fail(IRS_ERR_VALUE, "window must be >= 1 (got %d)", window);
+  if (W < 1 || (long long)W + window > 4096)
+    return fail(IRS_ERR_VALUE, "route width plus window must be in [2, 4096] (W=%d, window=%d)", W, window);
+  if (ndocs < 1 || ndocs > T) return fail(IRS_ERR_VALUE, "ndocs must be in [1, T] (got %d)", ndocs);
+  if (Tk < T) return fail(IRS_ERR_VALUE, "the window needs key positions for every query (Tk >= T)");
+  if (cu_seqlens == nullptr) return fail(IRS_ERR_VALUE, "NULL cu_seqlens");
+  return attn_fwd_impl(q, q_stride_t, q_stride_h, k, k_stride_t, k_stride_h, v, v_stride_t, v_stride_h, route_ids,
+                       route_stride, T, Tk, Hq, Hkv, Dqk, Dv, W, scale, cu_seqlens, ndocs, window, out, lse, err_flag,
+                       stream);
 }
 
 

@@ -66,6 +66,12 @@ struct AttnArgs {
   int tile_runs;  // 1: the maps are valid; 64 consecutive routed rows load as one TMA tile
   int stages;
   float scale_log2;  // scale * log2(e)
+  // sliding window in front of the route (0 = none): query t also attends the tokens
+  // max(s_d, t - window + 1) .. t of its document (cu: cu_seqlens, ndocs entries + 1), and
+  // route IDs inside that window are skipped
+  const int32_t* cu;
+  int ndocs;
+  int window;
 };
 
 struct AttnPlan {

@@ -226,16 +226,19 @@ def test_end_to_end(irs, name, nrows):
     is then checked on every sampled row against the oracle's attention over the oracle's
     routes: the GPU attention runs again on a route tensor whose sampled rows are the
     oracle's, and rows whose routes already agreed must give bit-identical output in both
-    GPU calls. On the windowed workload the sampled rows are the real window-plus-64-token
-    -block rows (Hq 64, Hkv 4, Dqk 192, Dv 128), whose K/V exceed half the L2, so they take
-    the TMA row-tile path."""
+    GPU calls. On the windowed workload the attention kernel adds the 512-token window
+    itself (the oracle composes it into the route), and the sampled rows are the real
+    window-plus-64-token-block rows (Hq 64, Hkv 4, Dqk 192, Dv 128), whose K/V exceed half
+    the L2, so they take the TMA row-tile path."""
     wl = irs_synth.make(name)
     a = wl.arrays
     t = irs_synth.as_torch(wl, device=DEV)
     route_idx = irs.sparse_index_score_topk(t["qI"], t["kI"], t["w"], t["cu_seqlens"], wl.c, wl.budget,
                                             max_doc_len=wl.max_doc_len)
-    route = irs.compose_window_routes(route_idx, t["cu_seqlens"], wl.window) if wl.window else route_idx
-    out, lse = irs.sparse_gqa_attn_fwd(t["q"], t["k"], t["v"], route, wl.scale)
+    # the windowed workload attends its window in the attention kernel (no composed route)
+    route = route_idx
+    win = dict(window=wl.window, cu_seqlens=t["cu_seqlens"]) if wl.window else {}
+    out, lse = irs.sparse_gqa_attn_fwd(t["q"], t["k"], t["v"], route, wl.scale, **win)
     irs.check_device_errors(DEV)
     rows = parity.sample_rows(wl, nrows, seed=5)
     idx = torch.as_tensor(rows, device=DEV)
@@ -250,16 +253,53 @@ def test_end_to_end(irs, name, nrows):
         full_ri = np.full((wl.T, ref_ri.shape[1]), -1, np.int32)
         full_ri[rows] = ref_ri
         ref_r = O.compose_window(full_ri, wl.cu_seqlens, wl.T, wl.window, rows=rows)
-        np.testing.assert_array_equal(route[idx].cpu().numpy()[same], ref_r[same])
     else:
         ref_r = ref_ri
-    full = np.full((wl.T, wl.route_width), -1, np.int32)
+    full = np.full((wl.T, ref_r.shape[1]), -1, np.int32)
     full[rows] = ref_r
     ref_o, ref_l = O.attention(a["q"], a["k"], a["v"], full, wl.scale, rows=rows)
     route2 = route.clone()
-    route2[idx] = torch.from_numpy(ref_r).to(DEV)
-    out2, lse2 = irs.sparse_gqa_attn_fwd(t["q"], t["k"], t["v"], route2, wl.scale)
+    route2[idx] = torch.from_numpy(ref_ri).to(DEV)
+    out2, lse2 = irs.sparse_gqa_attn_fwd(t["q"], t["k"], t["v"], route2, wl.scale, **win)
     irs.check_device_errors(DEV)
     same_idx = torch.as_tensor(rows[same], device=DEV)
     assert torch.equal(out[same_idx], out2[same_idx]) and torch.equal(lse[same_idx], lse2[same_idx])
     parity.check_attention(out2, lse2, ref_o, ref_l, rows)
+
+
+@pytest.mark.parametrize("case", ["windowed_small", "multi_doc", "window_wider_than_route"])
+def test_window_in_the_kernel_equals_composed_route(irs, case):
+    """The windowed attention entry point against composing the window into the route and
+    attending that: the same keys in the same order, so the outputs agree bit for bit; and
+    both against the oracle on sampled rows."""
+    if case == "windowed_small":
+        wl = irs_synth.make("windowed", small=True)
+        a = wl.arrays
+        t = irs_synth.as_torch(wl, device=DEV)
+        route = irs.sparse_index_score_topk(t["qI"], t["kI"], t["w"], t["cu_seqlens"], wl.c, wl.budget,
+                                            max_doc_len=wl.max_doc_len)
+        window, cu, scale = wl.window, t["cu_seqlens"], wl.scale
+        q, k, v = t["q"], t["k"], t["v"]
+        cu_h = wl.cu_seqlens
+    else:
+        T = 700
+        lens = [5, 300, 395] if case == "multi_doc" else [T]
+        wl = irs_synth.custom(T, 8, 2, 128, 128, 2, 64, 4, 8, doc_lens=lens, seed=len(lens) + 40)
+        a = wl.arrays
+        rng = np.random.default_rng(5)
+        W = 40 if case == "multi_doc" else 7
+        route = torch.from_numpy(irs_synth.random_routes(rng, T, T, W, wl.cu_seqlens, frac_invalid=0.2)).to(DEV)
+        window = 64 if case == "multi_doc" else 200
+        cu_h = wl.cu_seqlens
+        cu = torch.from_numpy(cu_h).to(DEV)
+        scale = wl.scale
+        q, k, v = (torch.from_numpy(a[x]).view(torch.bfloat16).to(DEV) for x in ("q", "k", "v"))
+    comp = irs.compose_window_routes(route, cu, window)
+    o1, l1 = irs.sparse_gqa_attn_fwd(q, k, v, comp, scale)
+    o2, l2 = irs.sparse_gqa_attn_fwd(q, k, v, route, scale, window=window, cu_seqlens=cu)
+    irs.check_device_errors(DEV)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    rows = parity.sample_rows(wl, 96, seed=9)
+    ref_comp = O.compose_window(route.cpu().numpy(), cu_h, wl.T, window)
+    ref_o, ref_l = O.attention(a["q"], a["k"], a["v"], ref_comp, scale, rows=rows)
+    parity.check_attention(o2, l2, ref_o, ref_l, rows)
