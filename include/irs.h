@@ -255,8 +255,9 @@ irs_status irs_sparse_gqa_attn_fwd_windowed(const void* q, int64_t q_stride_t, i
  * dq    fp32 [T, Hq, Dqk] contiguous, overwritten
  * dk    fp32 [Tk, Hkv, Dqk] contiguous, 16-byte aligned, ACCUMULATED (zero it first)
  * dv    fp32 [Tk, Hkv, Dv] contiguous, 16-byte aligned, accumulated; dv may equal dk
- *       (Dv <= Dqk): the value gradient is then added into the first Dv dims of each dk
- *       row, which is the gradient of latent rows used as keys and values
+ *       only when v is a view of k's first Dv dims (same pointer and strides, Dv <= Dqk;
+ *       IRS_ERR_VALUE otherwise): the value gradient is then added into the first Dv dims
+ *       of each dk row, which is the gradient of latent rows used as keys and values
  * The accumulation uses FP32 atomics, so dk and dv are not bit-reproducible across runs.
  * CUDA-core kernel (no tensor cores yet): one CTA per (query, KV head, block of up to
  * 16 query heads); it waits on nothing outside itself.

@@ -279,7 +279,8 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
   B.o_empty = B.o_full + 2;
   B.red = B.o_empty + 2;
   B.fin = B.red + 2;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(B.fin + 2);
+  uint64_t* drain = B.fin + 2;   // [2]: the S and O issuers' last products have completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -313,6 +314,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
       mbar_init(&B.o_empty[i], 4);
       mbar_init(&B.red[i], 4);
       mbar_init(&B.fin[i], 4);
+      mbar_init(&drain[i], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -474,6 +476,14 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
       }
     }
     cp_async_wait_pending(0);   // nothing of this CTA's gathers is in flight when it leaves
+    if (RUNS && ptid == 0 && *abort_flag) {
+      // a wait gave up: let the row tiles this thread issued for the last stages land (their
+      // phases may also miss arrivals of threads that stopped, hence the short bound)
+      for (uint32_t x = n > (uint32_t)ST ? n - ST : 0; x < n; ++x) {
+        const unsigned long long t0 = globaltimer_ns();
+        while (!mbar_try_wait(&B.kv_full[x % ST], (x / ST) & 1) && globaltimer_ns() - t0 < 50000000ull) {}
+      }
+    }
   } else if (warp == kSWarp) {
     // =========================== S issuer ===========================
     // The issuing thread runs in step with the tensor pipe, so S and O products come from
@@ -505,6 +515,10 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           }
         }
       }
+      // every S product this thread issued completes before the CTA releases tensor memory
+      umma_commit(&drain[0]);
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(&drain[0], 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
     }
   } else if (warp == kOWarp) {
     // =========================== O issuer ===========================
@@ -533,6 +547,9 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           umma_commit(&B.kv_empty[m % ST]);
         }
       }
+      umma_commit(&drain[1]);
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(&drain[1], 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
     }
   } else {
     // =========================== softmax + correction (warps PW+1 .. PW+4) ===========================

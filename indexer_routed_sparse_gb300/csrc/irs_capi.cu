@@ -382,7 +382,13 @@ irs_status irs_sparse_gqa_attn_bwd(const void* q, int64_t q_stride_t, int64_t q_
     return fail(IRS_ERR_VALUE, "q/k/v strides must be multiples of 8 elements (16 bytes)");
   if (q_stride_t < 0 || q_stride_h < 0 || k_stride_t < 0 || k_stride_h < 0 || v_stride_t < 0 || v_stride_h < 0)
     return fail(IRS_ERR_VALUE, "negative strides are not supported");
-  if (dv == dk && Dv > Dqk) return fail(IRS_ERR_VALUE, "dv may share dk's buffer only when Dv <= Dqk");
+  if (dv == dk) {
+    // one gradient buffer for keys and values is the gradient of latent rows used as both;
+    // for separate value rows it would silently add the value gradient into the key gradient
+    if (Dv > Dqk) return fail(IRS_ERR_VALUE, "dv may share dk's buffer only when Dv <= Dqk");
+    if (!(v == k && v_stride_t == k_stride_t && v_stride_h == k_stride_h))
+      return fail(IRS_ERR_VALUE, "dv may share dk's buffer only when v is a view of k's first Dv dims");
+  }
   if ((long long)T * Hkv * ((Hq / Hkv + irs::bwd_max_heads() - 1) / irs::bwd_max_heads()) > 0x7fffffffLL)
     return fail(IRS_ERR_VALUE, "too many work items");
   DeviceInfo* dev = nullptr;

@@ -67,7 +67,7 @@ __host__ __device__ inline MlaLayout mla_layout(int Dqk, int W) {
   L.misc_off = L.idx_off + (uint32_t)((W + 63) / 64) * 64 * 4;
   // m_run[64] alpha[64] red[2][64] | flagw[2][2] flag[2] nv[2] cnt[kMlaPW]
   L.bar_off = L.misc_off + (64 * 2 + 128) * 4 + (4 + 2 + 2 + 12) * 4;
-  L.total = L.bar_off + 24 * 8 + 16;
+  L.total = L.bar_off + 26 * 8 + 16;
   return L;
 }
 
@@ -207,7 +207,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
   uint64_t* fin_bar = bar + 22;
   uint64_t* o_full = bar + 20;
   uint64_t* o_free = bar + 21;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 24);
+  uint64_t* drain = bar + 24;        // [2]: the S and O issuers' last products have completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 26);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   constexpr uint32_t IDESC_S = idesc_bf16(128, kMH, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16(128, kMH, true, true);
@@ -237,6 +238,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
     mbar_init(fin_bar, 2);
     mbar_init(o_full, 1);
     mbar_init(o_free, 4);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -334,6 +337,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
         }
         if (alive) umma_commit(q_empty);
       }
+      // every S product this thread issued completes before the CTA releases tensor memory
+      umma_commit(&drain[0]);
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(&drain[0], 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
     }
   } else if (warp == kOW) {
     // =========================== O issuer ===========================
@@ -366,6 +373,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1) mla_fwd_kernel(AttnArgs a) {
           umma_commit(&kv_empty[m & 1]);
         }
       }
+      umma_commit(&drain[1]);
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(&drain[1], 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
     }
   } else {
     // =========================== softmax + correction ===========================

@@ -138,6 +138,10 @@ def test_backward_host_checks(lib):
     # a shared dk/dv buffer needs the value rows to fit in the key rows
     assert _bwd_call(lib, p, Dqk=128, Dv=256) == 2 and b"Dv <= Dqk" in lib.irs_last_error()
     assert _bwd_call(lib, p, T=0) == 0          # nothing to do
+    # separate value rows with a shared gradient buffer would mix the two gradients
+    st = lib.irs_sparse_gqa_attn_bwd(p, 512, 128, p, 256, 128, p + 16, 256, 128, p, 8, p, p, p, 4, 16, 4, 2, 128, 128,
+                                     8, 0.1, p, p, p, None, None)
+    assert st == 2 and b"view of k" in lib.irs_last_error()
 
 
 def test_backward_binding_rejects_wrong_inputs_on_cpu():
