@@ -114,6 +114,55 @@ irs_status irs_sparse_index_score_topk(const void* qI, const void* kI, const flo
                                        size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream);
 
 /*
+ * The indexer with its front half: sparse_index_score_topk over normalised and rotated
+ * index queries and keys.
+ *
+ * QSA page, `Qwen3_8_FlashNextQSAIndexer` (the FP32 group means get K RMSNorm and
+ * group-start RoPE; the index queries RMSNorm and RoPE) and `apply_qsa_rope` (per-token
+ * rotary values cat(cos, sin) over the first rope_dims dims, the rest unchanged). Before
+ * scoring:
+ *   pooled key b (FP32 group mean, first token s_b):  k~_b = bf16(rope(rmsnorm(kbar_b, k_weight), rope[s_b]))
+ *   query row (t, h):                                 q~   = bf16(rope(rmsnorm(qI[t,h], q_weight), rope[t]))
+ * with rmsnorm(x, g)_d = (x_d / sqrt(sum_e x_e^2 / Di + eps)) * g_d and rope pairing dims d
+ * and d + rope_dims/2 (rotate-half): (y_d cos_d - y_{d+h} sin_d, y_{d+h} cos_d + y_d sin_d).
+ * Everything is FP32 with each operation rounded on its own (sum of squares in ascending
+ * dim order, IEEE division and square root), then one rounding to bf16, so the transformed
+ * operands are reproducible bit for bit. Scoring, top-k and routes are then those of
+ * irs_sparse_index_score_topk.
+ *
+ * q_weight, k_weight  fp32 [Di] DEVICE
+ * eps                 >= 0
+ * rope                fp32 [T, rope_dims] DEVICE: row t = cat(cos, sin) for token t (the
+ *                     caller composes it for document-local positions); NULL if rope_dims = 0
+ * rope_dims           a multiple of 16 in [0, Di]
+ * workspace           at least irs_index_front_workspace_bytes(...) bytes (the plain
+ *                     indexer's scratch plus the transformed queries [T, Hi, Di] bf16 and the
+ *                     FP32 group means [floor(T/c), Di])
+ * Other arguments as for irs_sparse_index_score_topk.
+ */
+size_t irs_index_front_workspace_bytes(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len,
+                                       int with_score_buffer);
+irs_status irs_sparse_index_score_topk_front(const void* qI, const void* kI, const float* w,
+                                             const int32_t* cu_seqlens, int ndocs, int max_doc_len, int T, int Hi,
+                                             int Di, int c, int budget, const float* q_weight, const float* k_weight,
+                                             float eps, const float* rope, int rope_dims, int32_t* route_ids,
+                                             float* scores_dbg, int64_t ld_scores, void* workspace,
+                                             size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream);
+
+/*
+ * The front half alone, for checking the transformed operands bit for bit: q_out bf16
+ * [T, Hi, Di] receives the transformed queries, k_out bf16 [floor(T/c), Di] the transformed
+ * pooled keys in pooled order (document by document; rows past the last complete block are
+ * zero). Same definitions and arguments as irs_sparse_index_score_topk_front; the
+ * workspace is sized by irs_index_front_workspace_bytes(..., with_score_buffer = 0).
+ */
+irs_status irs_index_front_operands(const void* qI, const void* kI, const int32_t* cu_seqlens, int ndocs,
+                                    int max_doc_len, int T, int Hi, int Di, int c, int budget, const float* q_weight,
+                                    const float* k_weight, float eps, const float* rope, int rope_dims, void* q_out,
+                                    void* k_out, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                    irs_stream_t stream);
+
+/*
  * irs_sparse_index_score_topk without a workspace: the same computation and arguments,
  * minus `workspace` / `workspace_bytes`. The reference pages have no counterpart; this
  * entry point exists for callers that cannot allocate device memory for the library,

@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     compose_window_routes,
     device_error_flag,
     exported_symbols,
+    index_front_operands,
     index_workspace_bytes,
     lib,
     read_device_errors,

@@ -36,6 +36,11 @@ _SIGNATURES = {
     "irs_index_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "irs_sparse_index_score_topk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I64, _P, _SZ, _P, _P]),
     "irs_sparse_index_score_topk_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I64, _P, _P]),
+    "irs_index_front_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
+    "irs_sparse_index_score_topk_front": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _F, _P, _I, _P, _P,
+                                               _I64, _P, _SZ, _P, _P]),
+    "irs_index_front_operands": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _F, _P, _I, _P, _P, _P, _SZ, _P,
+                                      _P]),
     "irs_topk_from_scores": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "irs_compose_window_routes": (_I, [_P, _I, _P, _I, _I, _I, _P, _P, _P]),
     "irs_sparse_gqa_attn_fwd": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I, _I, _I, _I, _I, _I,
@@ -141,15 +146,34 @@ def _doc_stats(cu_seqlens: torch.Tensor, ndocs, max_doc_len, T: int):
     return int(ndocs), int(max_doc_len)
 
 
+def _front_args(front: dict, Di: int):
+    """(q_weight, k_weight, eps, rope, rope_dims) of a front-half dict, checked."""
+    qw, kw, rope = front["q_weight"], front["k_weight"], front.get("rope")
+    _need(qw, "q_weight", torch.float32, 1)
+    _need(kw, "k_weight", torch.float32, 1)
+    if qw.numel() != Di or kw.numel() != Di or not (qw.is_contiguous() and kw.is_contiguous()):
+        raise ValueError("q_weight and k_weight must be contiguous fp32 [Di]")
+    rope_dims = 0
+    if rope is not None:
+        _need(rope, "rope", torch.float32, 2)
+        if not rope.is_contiguous():
+            raise ValueError("rope must be contiguous [T, rope_dims]")
+        rope_dims = rope.shape[1]
+    return qw, kw, float(front["eps"]), rope, rope_dims
+
+
 def sparse_index_score_topk(qI: torch.Tensor, kI: torch.Tensor, w: torch.Tensor, cu_seqlens: torch.Tensor,
                             c: int, budget: int, *, ndocs: int | None = None, max_doc_len: int | None = None,
                             scores_out: torch.Tensor | None = None, out: torch.Tensor | None = None,
-                            workspace: torch.Tensor | None = None, err: torch.Tensor | None = None) -> torch.Tensor:
+                            workspace: torch.Tensor | None = None, err: torch.Tensor | None = None,
+                            front: dict | None = None) -> torch.Tensor:
     """Route IDs int32 [T, budget + c - 1] from the compressed-block indexer.
 
     qI bf16 [T, Hi, Di], kI bf16 [T, Di] (or [T, 1, Di]), w fp32 [T, Hi], cu_seqlens int32
     [ndocs + 1] on the same device. `scores_out` (fp32 [T, ld >= max_doc_len // c]) receives
-    the block scores of every row with more than budget // c visible blocks.
+    the block scores of every row with more than budget // c visible blocks. `front` (a dict
+    of fp32 device tensors q_weight [Di], k_weight [Di], rope [T, rope_dims] and a float eps)
+    adds the indexer's front half: RMSNorm and RoPE of queries and pooled keys.
     """
     _need(qI, "qI", torch.bfloat16, 3)
     _need(kI, "kI", torch.bfloat16)
@@ -173,18 +197,60 @@ def sparse_index_score_topk(qI: torch.Tensor, kI: torch.Tensor, w: torch.Tensor,
         if scores_out.shape[0] != T or scores_out.stride(1) != 1:
             raise ValueError("scores_out must be [T, ld] with unit inner stride")
         ld = scores_out.stride(0)
-    nbytes = index_workspace_bytes(T, Hi, Di, c, budget, ndocs, max_doc_len, scores_out is None)
+    if front is None:
+        nbytes = index_workspace_bytes(T, Hi, Di, c, budget, ndocs, max_doc_len, scores_out is None)
+    else:
+        nbytes = int(lib().irs_index_front_workspace_bytes(T, Hi, Di, c, budget, ndocs, max_doc_len,
+                                                           int(scores_out is None)))
     if nbytes == 0:
         _check(IRS_ERR_VALUE, "sparse_index_score_topk")
     if workspace is None or workspace.numel() < nbytes:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     if err is None:
         err = device_error_flag(dev)
-    st = lib().irs_sparse_index_score_topk(
-        _ptr(qI), _ptr(kI), _ptr(w), _ptr(cu_seqlens), ndocs, max_doc_len, T, Hi, Di, c, budget, _ptr(out),
-        _ptr(scores_out), ld, _ptr(workspace), workspace.numel(), _ptr(err), _stream(dev))
+    if front is None:
+        st = lib().irs_sparse_index_score_topk(
+            _ptr(qI), _ptr(kI), _ptr(w), _ptr(cu_seqlens), ndocs, max_doc_len, T, Hi, Di, c, budget, _ptr(out),
+            _ptr(scores_out), ld, _ptr(workspace), workspace.numel(), _ptr(err), _stream(dev))
+    else:
+        qw, kw, eps, rope, rope_dims = _front_args(front, Di)
+        st = lib().irs_sparse_index_score_topk_front(
+            _ptr(qI), _ptr(kI), _ptr(w), _ptr(cu_seqlens), ndocs, max_doc_len, T, Hi, Di, c, budget, _ptr(qw),
+            _ptr(kw), eps, _ptr(rope), rope_dims, _ptr(out), _ptr(scores_out), ld, _ptr(workspace),
+            workspace.numel(), _ptr(err), _stream(dev))
     _check(st, "sparse_index_score_topk")
     return out
+
+
+def index_front_operands(qI: torch.Tensor, kI: torch.Tensor, cu_seqlens: torch.Tensor, c: int, budget: int,
+                         front: dict, *, ndocs: int | None = None, max_doc_len: int | None = None,
+                         err: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """The indexer front half alone: (transformed queries bf16 [T, Hi, Di], transformed
+    pooled keys bf16 [T // c, Di], pooled order; rows past the last complete block are 0)."""
+    _need(qI, "qI", torch.bfloat16, 3)
+    _need(kI, "kI", torch.bfloat16)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, Hi, Di = qI.shape
+    if kI.dim() == 3:
+        kI = kI.reshape(kI.shape[0], kI.shape[2])
+    if not (qI.is_contiguous() and kI.is_contiguous() and cu_seqlens.is_contiguous()):
+        raise ValueError("qI, kI and cu_seqlens must be contiguous")
+    ndocs, max_doc_len = _doc_stats(cu_seqlens, ndocs, max_doc_len, T)
+    dev = qI.device
+    qw, kw, eps, rope, rope_dims = _front_args(front, Di)
+    q_out = torch.empty_like(qI)
+    k_out = torch.empty((max(1, T // c), Di), dtype=torch.bfloat16, device=dev)
+    nbytes = int(lib().irs_index_front_workspace_bytes(T, Hi, Di, c, budget, ndocs, max_doc_len, 0))
+    if nbytes == 0:
+        _check(IRS_ERR_VALUE, "index_front_operands")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    if err is None:
+        err = device_error_flag(dev)
+    st = lib().irs_index_front_operands(_ptr(qI), _ptr(kI), _ptr(cu_seqlens), ndocs, max_doc_len, T, Hi, Di, c,
+                                        budget, _ptr(qw), _ptr(kw), eps, _ptr(rope), rope_dims, _ptr(q_out),
+                                        _ptr(k_out), _ptr(ws), ws.numel(), _ptr(err), _stream(dev))
+    _check(st, "index_front_operands")
+    return q_out, k_out
 
 
 def topk_from_scores(scores: torch.Tensor, cu_seqlens: torch.Tensor, c: int, budget: int, *,

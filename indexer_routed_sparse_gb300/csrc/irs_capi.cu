@@ -160,10 +160,25 @@ size_t irs_index_workspace_bytes(int T, int Hi, int Di, int c, int budget, int n
   return irs::plan_index(T, Hi, Di, c, budget, ndocs, max_doc_len, with_score_buffer != 0).ws_bytes;
 }
 
-irs_status irs_sparse_index_score_topk(const void* qI, const void* kI, const float* w, const int32_t* cu_seqlens,
-                                       int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
-                                       int32_t* route_ids, float* scores_dbg, int64_t ld_scores, void* workspace,
-                                       size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+irs_status check_front(const float* q_weight, const float* k_weight, float eps, const float* rope, int rope_dims,
+                       int Di) {
+  if (!q_weight || !k_weight) return fail(IRS_ERR_VALUE, "NULL RMSNorm weights");
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(IRS_ERR_VALUE, "eps must be finite and >= 0");
+  if (rope_dims < 0 || rope_dims > Di || rope_dims % 16 != 0)
+    return fail(IRS_ERR_VALUE, "rope_dims must be a multiple of 16 in [0, Di] (got %d)", rope_dims);
+  if (rope_dims > 0 && rope == nullptr) return fail(IRS_ERR_VALUE, "NULL rotary table");
+  return IRS_OK;
+}
+
+// The indexer with or without its front half (front == nullptr).
+irs_status index_impl(const void* qI, const void* kI, const float* w, const int32_t* cu_seqlens, int ndocs,
+                      int max_doc_len, int T, int Hi, int Di, int c, int budget, const irs::FrontHalf* front,
+                      int32_t* route_ids, float* scores_dbg, int64_t ld_scores, void* workspace,
+                      size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream) {
   irs_status s = check_index_sizes(T, Hi, Di, c, budget, ndocs, max_doc_len);
   if (s != IRS_OK) return s;
   if (!qI || !kI || !w || !cu_seqlens || !route_ids || !workspace)
@@ -171,7 +186,8 @@ irs_status irs_sparse_index_score_topk(const void* qI, const void* kI, const flo
   if (!aligned16(qI) || !aligned16(kI)) return fail(IRS_ERR_VALUE, "qI and kI must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(IRS_ERR_VALUE, "workspace must be 256-byte aligned");
-  const irs::IndexPlan p = irs::plan_index(T, Hi, Di, c, budget, ndocs, max_doc_len, scores_dbg == nullptr);
+  const irs::IndexPlan p =
+      irs::plan_index(T, Hi, Di, c, budget, ndocs, max_doc_len, scores_dbg == nullptr, front != nullptr);
   if (scores_dbg != nullptr && ld_scores < p.ldS)
     return fail(IRS_ERR_VALUE, "ld_scores must be >= max_doc_len / c (%lld)", (long long)p.ldS);
   if (workspace_bytes < p.ws_bytes)
@@ -183,13 +199,74 @@ irs_status irs_sparse_index_score_topk(const void* qI, const void* kI, const flo
   float* scores = scores_dbg != nullptr ? scores_dbg : reinterpret_cast<float*>(ws + p.off_scores);
   const int64_t ldS = scores_dbg != nullptr ? ld_scores : p.ldS;
   CUtensorMap tm_q, tm_k;
-  if ((s = make_tmap(&tm_q, qI, (uint64_t)Di, (uint64_t)T * Hi, 256)) != IRS_OK) return s;
+  // with the front half the scores read the transformed queries from the workspace
+  const void* qsrc = front != nullptr ? static_cast<const void*>(ws + p.off_qfront) : qI;
+  if ((s = make_tmap(&tm_q, qsrc, (uint64_t)Di, (uint64_t)T * Hi, 256)) != IRS_OK) return s;
   if ((s = make_tmap(&tm_k, ws + p.off_kbar, (uint64_t)Di, (uint64_t)p.nblk_cap, 128)) != IRS_OK) return s;
   return launch_status(irs::launch_index(p, static_cast<const __nv_bfloat16*>(qI),
                                          static_cast<const __nv_bfloat16*>(kI), w, cu_seqlens, ndocs, max_doc_len, T,
                                          Hi, Di, c, budget, route_ids, scores, ldS, ws, err_flag, tm_q, tm_k,
-                                         dev->num_sms, reinterpret_cast<cudaStream_t>(stream)),
+                                         dev->num_sms, reinterpret_cast<cudaStream_t>(stream), front),
                        "launching the indexer");
+}
+
+}  // namespace
+
+extern "C" {
+
+irs_status irs_sparse_index_score_topk(const void* qI, const void* kI, const float* w, const int32_t* cu_seqlens,
+                                       int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
+                                       int32_t* route_ids, float* scores_dbg, int64_t ld_scores, void* workspace,
+                                       size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream) {
+  return index_impl(qI, kI, w, cu_seqlens, ndocs, max_doc_len, T, Hi, Di, c, budget, nullptr, route_ids, scores_dbg,
+                    ld_scores, workspace, workspace_bytes, err_flag, stream);
+}
+
+size_t irs_index_front_workspace_bytes(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len,
+                                       int with_score_buffer) {
+  if (check_index_sizes(T, Hi, Di, c, budget, ndocs, max_doc_len) != IRS_OK) return 0;
+  return irs::plan_index(T, Hi, Di, c, budget, ndocs, max_doc_len, with_score_buffer != 0, true).ws_bytes;
+}
+
+irs_status irs_sparse_index_score_topk_front(const void* qI, const void* kI, const float* w,
+                                             const int32_t* cu_seqlens, int ndocs, int max_doc_len, int T, int Hi,
+                                             int Di, int c, int budget, const float* q_weight, const float* k_weight,
+                                             float eps, const float* rope, int rope_dims, int32_t* route_ids,
+                                             float* scores_dbg, int64_t ld_scores, void* workspace,
+                                             size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream) {
+  irs_status s = check_front(q_weight, k_weight, eps, rope, rope_dims, Di);
+  if (s != IRS_OK) return s;
+  const irs::FrontHalf f{q_weight, k_weight, eps, rope, rope_dims};
+  return index_impl(qI, kI, w, cu_seqlens, ndocs, max_doc_len, T, Hi, Di, c, budget, &f, route_ids, scores_dbg,
+                    ld_scores, workspace, workspace_bytes, err_flag, stream);
+}
+
+irs_status irs_index_front_operands(const void* qI, const void* kI, const int32_t* cu_seqlens, int ndocs,
+                                    int max_doc_len, int T, int Hi, int Di, int c, int budget, const float* q_weight,
+                                    const float* k_weight, float eps, const float* rope, int rope_dims, void* q_out,
+                                    void* k_out, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                    irs_stream_t stream) {
+  irs_status s = check_index_sizes(T, Hi, Di, c, budget, ndocs, max_doc_len);
+  if (s != IRS_OK) return s;
+  if ((s = check_front(q_weight, k_weight, eps, rope, rope_dims, Di)) != IRS_OK) return s;
+  if (!qI || !kI || !cu_seqlens || !q_out || !k_out || !workspace) return fail(IRS_ERR_VALUE, "NULL tensor pointer");
+  if (!aligned16(qI) || !aligned16(kI) || !aligned16(q_out) || !aligned16(k_out))
+    return fail(IRS_ERR_VALUE, "qI, kI, q_out and k_out must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(IRS_ERR_VALUE, "workspace must be 256-byte aligned");
+  const irs::IndexPlan p = irs::plan_index(T, Hi, Di, c, budget, ndocs, max_doc_len, false, true);
+  if (workspace_bytes < p.ws_bytes)
+    return fail(IRS_ERR_VALUE, "workspace too small: %zu < %zu bytes", workspace_bytes, p.ws_bytes);
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != IRS_OK) return s;
+  const irs::FrontHalf f{q_weight, k_weight, eps, rope, rope_dims};
+  return launch_status(irs::launch_front_operands(p, static_cast<const __nv_bfloat16*>(qI),
+                                                  static_cast<const __nv_bfloat16*>(kI), cu_seqlens, ndocs,
+                                                  max_doc_len, T, Hi, Di, c, static_cast<uint8_t*>(workspace),
+                                                  err_flag, f, static_cast<__nv_bfloat16*>(q_out),
+                                                  static_cast<__nv_bfloat16*>(k_out),
+                                                  reinterpret_cast<cudaStream_t>(stream)),
+                       "launching the indexer front half");
 }
 
 irs_status irs_topk_from_scores(const float* scores, int64_t ld_scores, const int32_t* cu_seqlens, int ndocs,

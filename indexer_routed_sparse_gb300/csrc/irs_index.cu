@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
                                                    const int32_t* __restrict__ cu, int ndocs, int Di, int c,
                                                    int nblk_cap, const int32_t* __restrict__ meta,
                                                    const int32_t* __restrict__ blk_off,
-                                                   __nv_bfloat16* __restrict__ kbar) {
+                                                   __nv_bfloat16* __restrict__ kbar, float* __restrict__ kbar32) {
   if (meta[0] != 1) return;
   const int nblk = meta[1];
   const int chunks = Di >> 3;
@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
   const int ch = (int)(gid % chunks);
   if (gb >= nblk_cap) return;
   if (gb >= nblk) {
-    reinterpret_cast<uint4*>(kbar + (long long)gb * Di)[ch] = make_uint4(0, 0, 0, 0);
+    if (kbar32 == nullptr) reinterpret_cast<uint4*>(kbar + (long long)gb * Di)[ch] = make_uint4(0, 0, 0, 0);
     return;
   }
   const int d = find_le(blk_off, ndocs, gb);
@@ -123,12 +123,126 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
     }
   }
   const float fc = (float)c;
+  if (kbar32 != nullptr) {
+    // the FP32 means themselves, for the front half (normalised and rotated before rounding)
+    float4* o4 = reinterpret_cast<float4*>(kbar32 + (long long)gb * Di + ch * 8);
+    o4[0] = make_float4(__fdiv_rn(acc[0], fc), __fdiv_rn(acc[1], fc), __fdiv_rn(acc[2], fc), __fdiv_rn(acc[3], fc));
+    o4[1] = make_float4(__fdiv_rn(acc[4], fc), __fdiv_rn(acc[5], fc), __fdiv_rn(acc[6], fc), __fdiv_rn(acc[7], fc));
+    return;
+  }
   uint4 o;
   __nv_bfloat162* q = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
     q[i] = __floats2bfloat162_rn(__fdiv_rn(acc[2 * i], fc), __fdiv_rn(acc[2 * i + 1], fc));
   reinterpret_cast<uint4*>(kbar + (long long)gb * Di)[ch] = o;
+}
+
+// =====================================================================================
+// Indexer front half (QSA page, `Qwen3_8_FlashNextQSAIndexer`: the FP32 group means get K
+// RMSNorm and group-start RoPE, the queries RMSNorm and RoPE; `apply_qsa_rope`: per-token
+// rotary values cat(cos, sin) over the first rope_dims dims, the rest unchanged). One
+// thread per row of Di values, all in FP32 with every operation rounded on its own (no
+// fused multiply-add), in the order the oracle uses:
+//   ss = sum_d x_d * x_d (ascending d), r = sqrt(ss / Di + eps), y_d = (x_d / r) * wt_d,
+//   then for d < h = rope_dims / 2: (y_d cos_d - y_{d+h} sin_d, y_{d+h} cos_d + y_d sin_d),
+// and one rounding to bf16 at the end.
+// =====================================================================================
+template <typename In>
+__device__ __forceinline__ void load8(const In* p, float (&f)[8]);
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&f)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 x = __bfloat1622float2(b[i]);
+    f[2 * i] = x.x;
+    f[2 * i + 1] = x.y;
+  }
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&f)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint4 o;
+  __nv_bfloat162* q = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return o;
+}
+
+// One row: x (Di values) -> out (bf16), normalised with wt and rotated with rope (cos | sin).
+template <typename In>
+__device__ __forceinline__ void front_row(const In* __restrict__ x, int Di, const float* __restrict__ wt, float eps,
+                                          const float* __restrict__ rope, int rope_dims,
+                                          __nv_bfloat16* __restrict__ out) {
+  float ss = 0.f;
+  for (int d0 = 0; d0 < Di; d0 += 8) {
+    float f[8];
+    load8<In>(x + d0, f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(f[i], f[i]));
+  }
+  const float r = __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)Di), eps));
+  const int h = rope_dims >> 1;
+  for (int d0 = 0; d0 < h; d0 += 8) {
+    float a[8], b[8], ya[8], yb[8];
+    load8<In>(x + d0, a);
+    load8<In>(x + d0 + h, b);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float y1 = __fmul_rn(__fdiv_rn(a[i], r), __ldg(wt + d0 + i));
+      const float y2 = __fmul_rn(__fdiv_rn(b[i], r), __ldg(wt + d0 + h + i));
+      const float cs = __ldg(rope + d0 + i), sn = __ldg(rope + h + d0 + i);
+      ya[i] = __fsub_rn(__fmul_rn(y1, cs), __fmul_rn(y2, sn));
+      yb[i] = __fadd_rn(__fmul_rn(y2, cs), __fmul_rn(y1, sn));
+    }
+    *reinterpret_cast<uint4*>(out + d0) = pack8(ya);
+    *reinterpret_cast<uint4*>(out + d0 + h) = pack8(yb);
+  }
+  for (int d0 = rope_dims; d0 < Di; d0 += 8) {
+    float a[8];
+    load8<In>(x + d0, a);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = __fmul_rn(__fdiv_rn(a[i], r), __ldg(wt + d0 + i));
+    *reinterpret_cast<uint4*>(out + d0) = pack8(a);
+  }
+}
+
+// Pooled keys: block gb takes the rotary values of its first token; rows past the last
+// complete block are zeroed (as pool_kernel does without the front half).
+__global__ void __launch_bounds__(128) front_keys_kernel(const float* __restrict__ kbar32, int nblk_cap, int Di,
+                                                         const int32_t* __restrict__ meta,
+                                                         const int32_t* __restrict__ blk_off,
+                                                         const int32_t* __restrict__ cu, int ndocs, int c,
+                                                         const float* __restrict__ k_weight, float eps,
+                                                         const float* __restrict__ rope, int rope_dims,
+                                                         __nv_bfloat16* __restrict__ kbar) {
+  if (meta[0] != 1) return;
+  const int gb = blockIdx.x * blockDim.x + threadIdx.x;
+  if (gb >= nblk_cap) return;
+  __nv_bfloat16* out = kbar + (long long)gb * Di;
+  if (gb >= meta[1]) {
+    for (int d0 = 0; d0 < Di; d0 += 8) *reinterpret_cast<uint4*>(out + d0) = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const int d = find_le(blk_off, ndocs, gb);
+  const long long tok = (long long)cu[d] + (long long)(gb - blk_off[d]) * c;
+  front_row<float>(kbar32 + (long long)gb * Di, Di, k_weight, eps, rope + tok * rope_dims, rope_dims, out);
+}
+
+// Queries: row t*Hi + h takes the rotary values of token t.
+__global__ void __launch_bounds__(128) front_queries_kernel(const __nv_bfloat16* __restrict__ qI, long long rows,
+                                                            int Hi, int Di, const float* __restrict__ q_weight,
+                                                            float eps, const float* __restrict__ rope, int rope_dims,
+                                                            __nv_bfloat16* __restrict__ qout) {
+  const long long row = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= rows) return;
+  const long long t = row / Hi;
+  front_row<__nv_bfloat16>(qI + row * Di, Di, q_weight, eps, rope + t * rope_dims, rope_dims, qout + row * Di);
 }
 
 // =====================================================================================
@@ -560,7 +674,8 @@ __global__ void __launch_bounds__(128) compose_window_kernel(const int32_t* __re
 // =====================================================================================
 // host launchers
 // =====================================================================================
-IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len, bool with_scores) {
+IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len, bool with_scores,
+                     bool front) {
   IndexPlan p{};
   p.kb = budget / c;
   p.QT = kIdxN / Hi;
@@ -579,6 +694,8 @@ IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int ma
   p.off_tile = take(sizeof(int32_t) * (size_t)(ndocs + 1), 256);
   p.off_kbar = take((size_t)p.nblk_cap * Di * 2, 1024);
   p.off_scores = with_scores ? take((size_t)T * p.ldS * sizeof(float), 1024) : 0;
+  p.off_qfront = front ? take((size_t)T * Hi * Di * 2, 1024) : 0;
+  p.off_kbar32 = front ? take((size_t)p.nblk_cap * Di * sizeof(float), 1024) : 0;
   p.ws_bytes = (off + 255) / 256 * 256;
   p.stages = Di == 64 ? 8 : 5;
   p.score_smem = Di == 64 ? IdxSmem<64>::total(p.stages) : IdxSmem<128>::total(p.stages);
@@ -591,22 +708,46 @@ size_t topk_smem_bytes(int nvis_cap, int kb) {
   return (size_t)nvis_cap * 4 + nw * 4 * 3 + (size_t)kb * 4 + 16;
 }
 
-cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI, const float* w,
-                         const int32_t* cu, int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
-                         int32_t* route, float* scores, int64_t ldS, uint8_t* ws, int32_t* err,
-                         const CUtensorMap& tm_q, const CUtensorMap& tm_k, int num_sms, cudaStream_t stream) {
+// Layout, pooling and (with `front`) the front half's transforms: pooled bf16 keys into
+// kbar, transformed queries into qfront.
+static void launch_pool(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI, const int32_t* cu,
+                        int ndocs, int max_doc_len, int T, int Hi, int Di, int c, uint8_t* ws, int32_t* err,
+                        const FrontHalf* front, __nv_bfloat16* kbar, __nv_bfloat16* qfront, cudaStream_t stream) {
   int32_t* meta = reinterpret_cast<int32_t*>(ws + p.off_meta);
   int32_t* blk_off = reinterpret_cast<int32_t*>(ws + p.off_blk);
   int32_t* tile_off = reinterpret_cast<int32_t*>(ws + p.off_tile);
-  __nv_bfloat16* kbar = reinterpret_cast<__nv_bfloat16*>(ws + p.off_kbar);
+  float* kbar32 = reinterpret_cast<float*>(ws + p.off_kbar32);
 
   layout_kernel<<<1, 1024, 0, stream>>>(cu, ndocs, T, c, p.tau_sparse, p.QT, max_doc_len, meta, blk_off, tile_off,
                                         err);
   {
     const long long threads = (long long)p.nblk_cap * (Di / 8);
     const int grid = (int)((threads + 255) / 256);
-    pool_kernel<<<grid, 256, 0, stream>>>(kI, cu, ndocs, Di, c, p.nblk_cap, meta, blk_off, kbar);
+    pool_kernel<<<grid, 256, 0, stream>>>(kI, cu, ndocs, Di, c, p.nblk_cap, meta, blk_off, kbar,
+                                          front ? kbar32 : nullptr);
   }
+  if (front) {
+    front_keys_kernel<<<(p.nblk_cap + 127) / 128, 128, 0, stream>>>(kbar32, p.nblk_cap, Di, meta, blk_off, cu, ndocs, c,
+                                                                    front->k_weight, front->eps, front->rope,
+                                                                    front->rope_dims, kbar);
+    const long long rows = (long long)T * Hi;
+    front_queries_kernel<<<(unsigned)((rows + 127) / 128), 128, 0, stream>>>(qI, rows, Hi, Di, front->q_weight,
+                                                                             front->eps, front->rope, front->rope_dims,
+                                                                             qfront);
+  }
+}
+
+cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI, const float* w,
+                         const int32_t* cu, int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
+                         int32_t* route, float* scores, int64_t ldS, uint8_t* ws, int32_t* err,
+                         const CUtensorMap& tm_q, const CUtensorMap& tm_k, int num_sms, cudaStream_t stream,
+                         const FrontHalf* front) {
+  int32_t* meta = reinterpret_cast<int32_t*>(ws + p.off_meta);
+  int32_t* blk_off = reinterpret_cast<int32_t*>(ws + p.off_blk);
+  int32_t* tile_off = reinterpret_cast<int32_t*>(ws + p.off_tile);
+  __nv_bfloat16* kbar = reinterpret_cast<__nv_bfloat16*>(ws + p.off_kbar);
+  launch_pool(p, qI, kI, cu, ndocs, max_doc_len, T, Hi, Di, c, ws, err, front, kbar,
+              reinterpret_cast<__nv_bfloat16*>(ws + p.off_qfront), stream);
   IndexArgs ia{w, cu, blk_off, tile_off, meta, scores, ldS, err, ndocs, T, c, p.QT, p.tau_sparse, p.stages};
   const int grid = num_sms < kMaxIndexCtas ? num_sms : kMaxIndexCtas;
   const cudaError_t le = Di == 64 ? launch_score_64(Hi, grid, p.score_smem, stream, tm_q, tm_k, ia)
@@ -614,6 +755,14 @@ cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv
   if (le != cudaSuccess) return le;
   TopkArgs ta{scores, ldS, cu, meta, route, err, ndocs, T, c, budget, max_doc_len, (int)p.ldS};
   return launch_topk(ta, p.kb, stream, p.topk_smem);
+}
+
+cudaError_t launch_front_operands(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI,
+                                  const int32_t* cu, int ndocs, int max_doc_len, int T, int Hi, int Di, int c,
+                                  uint8_t* ws, int32_t* err, const FrontHalf& front, __nv_bfloat16* q_out,
+                                  __nv_bfloat16* k_out, cudaStream_t stream) {
+  launch_pool(p, qI, kI, cu, ndocs, max_doc_len, T, Hi, Di, c, ws, err, &front, k_out, q_out, stream);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_topk_from_scores(const float* scores, int64_t ldS, const int32_t* cu, int ndocs, int max_doc_len,

@@ -14,6 +14,16 @@ namespace irs {
 // Sizes and scratch offsets of one indexer call.
 constexpr int kMaxIndexCtas = 160;   // persistent CTAs of the score kernel (>= one per SM)
 
+// Indexer front half: RMSNorm weights of queries and keys, eps, and the per-token rotary
+// table [T, rope_dims] = cat(cos, sin) (device pointers).
+struct FrontHalf {
+  const float* q_weight;
+  const float* k_weight;
+  float eps;
+  const float* rope;
+  int rope_dims;
+};
+
 struct IndexPlan {
   int kb;              // blocks kept per query (budget / c)
   int QT;              // queries per score tile (256 / Hi)
@@ -22,18 +32,29 @@ struct IndexPlan {
   int64_t ldS;         // row stride of the score buffer (max_doc_len / c)
   int stages;          // 64-dim key atoms in the score kernel's TMA ring
   size_t off_meta, off_blk, off_tile, off_kbar, off_scores, ws_bytes;
+  size_t off_qfront, off_kbar32;   // front half only: transformed queries, FP32 group means
   size_t score_smem, topk_smem;
 };
 
-IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len, bool with_scores);
+IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len, bool with_scores,
+                     bool front = false);
 size_t topk_smem_bytes(int nvis_cap, int kb);
 
 cudaError_t configure_score_kernels(size_t smem);
 cudaError_t configure_topk_kernel(size_t smem);
+// front == nullptr: the plain indexer. Otherwise the scores use the transformed queries
+// (tm_q must map ws + p.off_qfront) and the transformed pooled keys.
 cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI, const float* w,
                          const int32_t* cu, int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
                          int32_t* route, float* scores, int64_t ldS, uint8_t* ws, int32_t* err,
-                         const CUtensorMap& tm_q, const CUtensorMap& tm_k, int num_sms, cudaStream_t stream);
+                         const CUtensorMap& tm_q, const CUtensorMap& tm_k, int num_sms, cudaStream_t stream,
+                         const FrontHalf* front = nullptr);
+// The front half alone: transformed queries [T*Hi, Di] into q_out, pooled keys [T/c, Di]
+// into k_out (rows past the last complete block zeroed).
+cudaError_t launch_front_operands(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI,
+                                  const int32_t* cu, int ndocs, int max_doc_len, int T, int Hi, int Di, int c,
+                                  uint8_t* ws, int32_t* err, const FrontHalf& front, __nv_bfloat16* q_out,
+                                  __nv_bfloat16* k_out, cudaStream_t stream);
 cudaError_t launch_topk_from_scores(const float* scores, int64_t ldS, const int32_t* cu, int ndocs, int max_doc_len,
                                     int T, int c, int budget, int32_t* route, int32_t* err, cudaStream_t stream);
 cudaError_t launch_compose_window(const int32_t* route, int W, const int32_t* cu, int ndocs, int T, int window,

@@ -156,3 +156,19 @@ def test_backward_binding_rejects_wrong_inputs_on_cpu():
         irs.sparse_gqa_attn_bwd(qb.float(), qb, qb, r, qb, lse, qb)
     with pytest.raises(ValueError):     # not CUDA tensors
         irs.sparse_gqa_attn_bwd(qb, qb, qb, r, qb, lse, qb)
+
+
+def test_front_half_validation_is_value_error(lib):
+    import ctypes as C
+    buf = C.create_string_buffer(256)
+    p = C.addressof(buf) + (16 - C.addressof(buf) % 16) % 16
+    def call(rope_dims=32, qw=p, kw=p, eps=1e-6, rope=p):
+        return lib.irs_sparse_index_score_topk_front(p, p, p, p, 1, 64, 64, 4, 64, 4, 16, qw, kw, eps, rope, rope_dims,
+                                                     p, None, 0, p, 1 << 20, None, None)
+    assert call(rope_dims=24) == 2 and b"rope_dims" in lib.irs_last_error()
+    assert call(rope_dims=80) == 2
+    assert call(qw=None) == 2 and b"RMSNorm" in lib.irs_last_error()
+    assert call(eps=-1.0) == 2 and b"eps" in lib.irs_last_error()
+    assert call(rope=None) == 2 and b"rotary" in lib.irs_last_error()
+    assert lib.irs_index_front_workspace_bytes(64, 4, 64, 4, 16, 1, 64, 1) > lib.irs_index_workspace_bytes(
+        64, 4, 64, 4, 16, 1, 64, 1)
