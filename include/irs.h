@@ -163,6 +163,28 @@ irs_status irs_index_front_operands(const void* qI, const void* kI, const int32_
                                     irs_stream_t stream);
 
 /*
+ * The indexer with a separate selection per KV group.
+ *
+ * Step-5 sparse page, `Step5SparseIndexer.forward` (region IDs per KV group) and
+ * `indexer_score_tile` (one weighted-ReLU score per group, with that group's FP32 head
+ * weights; signed weights allowed). Group g of token t scores the shared pooled keys with
+ * its own Hi query heads and weights and selects its own blocks, each group exactly as
+ * irs_sparse_index_score_topk does for one (same kernels, run once per group).
+ *
+ * qI          bf16 [T, G, Hi, Di] contiguous;  w  fp32 [T, G, Hi] contiguous
+ * route_ids   int32 [T, G, budget + c - 1]
+ * scores_dbg  NULL or fp32 [T, G, ld_scores] (row (t, g) at (t*G + g) * ld_scores)
+ * workspace   irs_index_workspace_bytes(T, Hi, Di, c, budget, ndocs, max_doc_len, ...) bytes:
+ *             the score scratch is reused group after group
+ * Other arguments as for irs_sparse_index_score_topk; G >= 1.
+ */
+irs_status irs_sparse_index_score_topk_grouped(const void* qI, const void* kI, const float* w,
+                                               const int32_t* cu_seqlens, int ndocs, int max_doc_len, int T, int G,
+                                               int Hi, int Di, int c, int budget, int32_t* route_ids,
+                                               float* scores_dbg, int64_t ld_scores, void* workspace,
+                                               size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream);
+
+/*
  * irs_sparse_index_score_topk without a workspace: the same computation and arguments,
  * minus `workspace` / `workspace_bytes`. The reference pages have no counterpart; this
  * entry point exists for callers that cannot allocate device memory for the library,
@@ -255,6 +277,22 @@ irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_
                                    int64_t v_stride_h, const int32_t* route_ids, int64_t route_stride, int T,
                                    int Tk, int Hq, int Hkv, int Dqk, int Dv, int W, float scale, void* out,
                                    float* lse, int32_t* err_flag, irs_stream_t stream);
+
+/*
+ * sparse_gqa_attn_fwd with a route per KV group.
+ *
+ * Step-5 sparse page, `Step5SparseIndexer.forward` (region IDs per KV group); the query
+ * heads of KV head g (h / (Hq/Hkv) == g) attend the entries of route row (t, g) at
+ * route_ids + t*route_stride + g*route_group_stride (W entries, -1 padding), with the
+ * definitions of irs_sparse_gqa_attn_fwd. route_group_stride >= W. Runs the GQA kernel once
+ * per KV head.
+ */
+irs_status irs_sparse_gqa_attn_fwd_grouped(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k,
+                                           int64_t k_stride_t, int64_t k_stride_h, const void* v, int64_t v_stride_t,
+                                           int64_t v_stride_h, const int32_t* route_ids, int64_t route_stride,
+                                           int64_t route_group_stride, int T, int Tk, int Hq, int Hkv, int Dqk,
+                                           int Dv, int W, float scale, void* out, float* lse, int32_t* err_flag,
+                                           irs_stream_t stream);
 
 /*
  * sparse_gqa_attn_fwd with a sliding window in front of every route row.

@@ -25,6 +25,8 @@ from ._binding import (  # noqa: F401
     read_device_errors,
     sparse_gqa_attn_bwd,
     sparse_gqa_attn_fwd,
+    sparse_gqa_attn_fwd_grouped,
     sparse_index_score_topk,
+    sparse_index_score_topk_grouped,
     topk_from_scores,
 )

@@ -41,6 +41,10 @@ _SIGNATURES = {
                                                _I64, _P, _SZ, _P, _P]),
     "irs_index_front_operands": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _F, _P, _I, _P, _P, _P, _SZ, _P,
                                       _P]),
+    "irs_sparse_index_score_topk_grouped": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I64, _P,
+                                                 _SZ, _P, _P]),
+    "irs_sparse_gqa_attn_fwd_grouped": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _I, _I,
+                                             _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "irs_topk_from_scores": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "irs_compose_window_routes": (_I, [_P, _I, _P, _I, _I, _I, _P, _P, _P]),
     "irs_sparse_gqa_attn_fwd": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I, _I, _I, _I, _I, _I,
@@ -427,3 +431,78 @@ def check_bounded_wait(limit_ms: float = 20.0, device=None, err: torch.Tensor | 
     st = lib().irs_check_bounded_wait(int(limit_ms * 1e6), _ptr(err), _stream(dev))
     _check(st, "check_bounded_wait")
     return err
+
+
+def sparse_index_score_topk_grouped(qI: torch.Tensor, kI: torch.Tensor, w: torch.Tensor, cu_seqlens: torch.Tensor,
+                                    c: int, budget: int, *, ndocs: int | None = None, max_doc_len: int | None = None,
+                                    scores_out: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                                    err: torch.Tensor | None = None) -> torch.Tensor:
+    """Per-KV-group routes int32 [T, G, budget + c - 1] (Step-5 selection per group).
+
+    qI bf16 [T, G, Hi, Di], kI bf16 [T, Di], w fp32 [T, G, Hi]; scores_out fp32 [T, G, ld].
+    """
+    _need(qI, "qI", torch.bfloat16, 4)
+    _need(kI, "kI", torch.bfloat16)
+    _need(w, "w", torch.float32, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, G, Hi, Di = qI.shape
+    if kI.dim() == 3:
+        kI = kI.reshape(kI.shape[0], kI.shape[2])
+    if tuple(kI.shape) != (T, Di) or tuple(w.shape) != (T, G, Hi):
+        raise ValueError(f"shape mismatch: qI {tuple(qI.shape)}, kI {tuple(kI.shape)}, w {tuple(w.shape)}")
+    if not (qI.is_contiguous() and kI.is_contiguous() and w.is_contiguous() and cu_seqlens.is_contiguous()):
+        raise ValueError("qI, kI, w and cu_seqlens must be contiguous")
+    ndocs, max_doc_len = _doc_stats(cu_seqlens, ndocs, max_doc_len, T)
+    dev = qI.device
+    W = budget + c - 1
+    if out is None:
+        out = torch.empty((T, G, W), dtype=torch.int32, device=dev)
+    ld = 0
+    if scores_out is not None:
+        _need(scores_out, "scores_out", torch.float32, 3)
+        if tuple(scores_out.shape[:2]) != (T, G) or not scores_out.is_contiguous():
+            raise ValueError("scores_out must be a contiguous fp32 [T, G, ld]")
+        ld = scores_out.shape[2]
+    nbytes = index_workspace_bytes(T, Hi, Di, c, budget, ndocs, max_doc_len, scores_out is None)
+    if nbytes == 0:
+        _check(IRS_ERR_VALUE, "sparse_index_score_topk_grouped")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    if err is None:
+        err = device_error_flag(dev)
+    st = lib().irs_sparse_index_score_topk_grouped(
+        _ptr(qI), _ptr(kI), _ptr(w), _ptr(cu_seqlens), ndocs, max_doc_len, T, G, Hi, Di, c, budget, _ptr(out),
+        _ptr(scores_out), ld, _ptr(ws), ws.numel(), _ptr(err), _stream(dev))
+    _check(st, "sparse_index_score_topk_grouped")
+    return out
+
+
+def sparse_gqa_attn_fwd_grouped(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, route_ids: torch.Tensor,
+                                scale: float | None = None, *, err: torch.Tensor | None = None):
+    """Attention with a route per KV group: route_ids int32 [T, Hkv, W]; the query heads of
+    KV head g attend route_ids[t, g]. Returns (out bf16 [T, Hq, Dv], lse fp32 [T, Hq])."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(route_ids, "route_ids", torch.int32, 3)
+    T, Hq, Dqk = q.shape
+    Tk, Hkv, _ = k.shape
+    Dv = v.shape[2]
+    if route_ids.shape[0] != T or route_ids.shape[1] != Hkv or route_ids.stride(2) != 1:
+        raise ValueError("route_ids must be [T, Hkv, W] with unit inner stride")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.stride(-1) != 1:
+            raise ValueError(f"{name} must have unit inner stride")
+    W = route_ids.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(Dqk)
+    dev = q.device
+    out = torch.empty((T, Hq, Dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+    if err is None:
+        err = device_error_flag(dev)
+    st = lib().irs_sparse_gqa_attn_fwd_grouped(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1), _ptr(v), v.stride(0), v.stride(1),
+        _ptr(route_ids), route_ids.stride(0), route_ids.stride(1), T, Tk, Hq, Hkv, Dqk, Dv, W, float(scale),
+        _ptr(out), _ptr(lse), _ptr(err), _stream(dev))
+    _check(st, "sparse_gqa_attn_fwd_grouped")
+    return out, lse

@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           const int i = base + k * kProducerThreads + ptid;
           const int id = ids[k];
           const bool inrange = id >= 0 && id < a.Tk;
-          if (i < a.W && id != -1 && !inrange && a.g0 == 0) record_error(a.err, IRS_DEVERR_ROUTE_ID);
+          if (i < a.W && id != -1 && !inrange && a.flag_routes) record_error(a.err, IRS_DEVERR_ROUTE_ID);
           const bool okid = inrange && (a.window == 0 || id < lo_w);
           const uint32_t bal = __ballot_sync(0xffffffffu, okid);
           if (lane == 0) sCnt[warp] = __popc(bal);

@@ -108,6 +108,23 @@ irs_status make_row_tile_map(CUtensorMap* m, const void* base, uint64_t inner, u
   return IRS_OK;
 }
 
+// 3-D bf16 map of index queries [T][rows_per_token][Di] (contiguous), box {64, Hi, 256/Hi}:
+// the (query, head) rows of one score tile, for any head group of the token.
+irs_status make_query_tiles_map(CUtensorMap* m, const void* base, uint64_t Di, uint64_t rows_per_token, uint64_t T,
+                                uint32_t Hi) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(IRS_ERR_RUNTIME, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {Di, rows_per_token, T};
+  cuuint64_t strides[2] = {Di * 2, rows_per_token * Di * 2};
+  cuuint32_t box[3] = {64, Hi, 256 / Hi};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(IRS_ERR_RUNTIME, "cuTensorMapEncodeTiled (query tiles) failed (%d)", (int)r);
+  return IRS_OK;
+}
+
 irs_status launch_status(cudaError_t e, const char* what) {
   if (e != cudaSuccess) return fail(IRS_ERR_RUNTIME, "%s: %s", what, cudaGetErrorString(e));
   return IRS_OK;
@@ -178,9 +195,10 @@ irs_status check_front(const float* q_weight, const float* k_weight, float eps, 
 irs_status index_impl(const void* qI, const void* kI, const float* w, const int32_t* cu_seqlens, int ndocs,
                       int max_doc_len, int T, int Hi, int Di, int c, int budget, const irs::FrontHalf* front,
                       int32_t* route_ids, float* scores_dbg, int64_t ld_scores, void* workspace,
-                      size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream) {
+                      size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream, int G = 1) {
   irs_status s = check_index_sizes(T, Hi, Di, c, budget, ndocs, max_doc_len);
   if (s != IRS_OK) return s;
+  if (G < 1 || (long long)T * G * Hi >= (1LL << 31)) return fail(IRS_ERR_VALUE, "bad group count %d", G);
   if (!qI || !kI || !w || !cu_seqlens || !route_ids || !workspace)
     return fail(IRS_ERR_VALUE, "NULL tensor pointer");
   if (!aligned16(qI) || !aligned16(kI)) return fail(IRS_ERR_VALUE, "qI and kI must be 16-byte aligned");
@@ -196,17 +214,22 @@ irs_status index_impl(const void* qI, const void* kI, const float* w, const int3
   if ((s = current_device(&dev)) != IRS_OK) return s;
   if ((s = configure_index(dev, p)) != IRS_OK) return s;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // score rows: the caller's [T, G, ld_scores] (group g of token t at (t*G + g) * ld_scores),
+  // or the workspace's [T, ldS], reused group after group
   float* scores = scores_dbg != nullptr ? scores_dbg : reinterpret_cast<float*>(ws + p.off_scores);
-  const int64_t ldS = scores_dbg != nullptr ? ld_scores : p.ldS;
+  const int64_t ldS = scores_dbg != nullptr ? ld_scores * G : p.ldS;
+  const int64_t group_stride = scores_dbg != nullptr ? ld_scores : 0;
   CUtensorMap tm_q, tm_k;
   // with the front half the scores read the transformed queries from the workspace
   const void* qsrc = front != nullptr ? static_cast<const void*>(ws + p.off_qfront) : qI;
-  if ((s = make_tmap(&tm_q, qsrc, (uint64_t)Di, (uint64_t)T * Hi, 256)) != IRS_OK) return s;
+  if ((s = make_query_tiles_map(&tm_q, qsrc, (uint64_t)Di, (uint64_t)G * Hi, (uint64_t)T, (uint32_t)Hi)) != IRS_OK)
+    return s;
   if ((s = make_tmap(&tm_k, ws + p.off_kbar, (uint64_t)Di, (uint64_t)p.nblk_cap, 128)) != IRS_OK) return s;
   return launch_status(irs::launch_index(p, static_cast<const __nv_bfloat16*>(qI),
                                          static_cast<const __nv_bfloat16*>(kI), w, cu_seqlens, ndocs, max_doc_len, T,
                                          Hi, Di, c, budget, route_ids, scores, ldS, ws, err_flag, tm_q, tm_k,
-                                         dev->num_sms, reinterpret_cast<cudaStream_t>(stream), front),
+                                         dev->num_sms, reinterpret_cast<cudaStream_t>(stream), front, G,
+                                         group_stride),
                        "launching the indexer");
 }
 
@@ -239,6 +262,15 @@ irs_status irs_sparse_index_score_topk_front(const void* qI, const void* kI, con
   const irs::FrontHalf f{q_weight, k_weight, eps, rope, rope_dims};
   return index_impl(qI, kI, w, cu_seqlens, ndocs, max_doc_len, T, Hi, Di, c, budget, &f, route_ids, scores_dbg,
                     ld_scores, workspace, workspace_bytes, err_flag, stream);
+}
+
+irs_status irs_sparse_index_score_topk_grouped(const void* qI, const void* kI, const float* w,
+                                               const int32_t* cu_seqlens, int ndocs, int max_doc_len, int T, int G,
+                                               int Hi, int Di, int c, int budget, int32_t* route_ids,
+                                               float* scores_dbg, int64_t ld_scores, void* workspace,
+                                               size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream) {
+  return index_impl(qI, kI, w, cu_seqlens, ndocs, max_doc_len, T, Hi, Di, c, budget, nullptr, route_ids, scores_dbg,
+                    ld_scores, workspace, workspace_bytes, err_flag, stream, G);
 }
 
 irs_status irs_index_front_operands(const void* qI, const void* kI, const int32_t* cu_seqlens, int ndocs,
@@ -315,7 +347,7 @@ irs_status attn_fwd_impl(const void* q, int64_t q_stride_t, int64_t q_stride_h, 
                          int64_t k_stride_h, const void* v, int64_t v_stride_t, int64_t v_stride_h,
                          const int32_t* route_ids, int64_t route_stride, int T, int Tk, int Hq, int Hkv, int Dqk,
                          int Dv, int W, float scale, const int32_t* cu_seqlens, int ndocs, int window, void* out,
-                         float* lse, int32_t* err_flag, irs_stream_t stream) {
+                         float* lse, int32_t* err_flag, irs_stream_t stream, int64_t route_group_stride = 0) {
   if (T < 0 || Tk < 1 || Hq < 1 || Hkv < 1) return fail(IRS_ERR_VALUE, "bad sizes (T=%d Tk=%d Hq=%d Hkv=%d)", T, Tk, Hq, Hkv);
   if (Hq % Hkv != 0) return fail(IRS_ERR_VALUE, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
   if (Dqk < 64 || Dqk > 576 || Dqk % 64 != 0) return fail(IRS_ERR_VALUE, "Dqk must be a multiple of 64 in [64, 576]");
@@ -356,7 +388,8 @@ irs_status attn_fwd_impl(const void* q, int64_t q_stride_t, int64_t q_stride_h, 
   a.cu = cu_seqlens;
   a.ndocs = ndocs;
   a.window = window;
-  if (window == 0 && irs::mla_supported(a)) {
+  a.flag_routes = 1;
+  if (window == 0 && route_group_stride == 0 && irs::mla_supported(a)) {
     const size_t smem = irs::mla_smem_bytes(a);
     {
       std::lock_guard<std::mutex> lk(g_dev_mu);
@@ -378,8 +411,12 @@ irs_status attn_fwd_impl(const void* q, int64_t q_stride_t, int64_t q_stride_h, 
     }
   }
   // one launch per group of up to kMaxKvMaps KV heads (one row-tile map per head and operand)
-  for (int g0 = 0; g0 < Hkv; g0 += irs::kMaxKvMaps) {
-    const int ng = Hkv - g0 < irs::kMaxKvMaps ? Hkv - g0 : irs::kMaxKvMaps;
+  // per-group routes: one launch per KV head, on that head's route rows
+  const int gstep = route_group_stride != 0 ? 1 : irs::kMaxKvMaps;
+  for (int g0 = 0; g0 < Hkv; g0 += gstep) {
+    const int ng = Hkv - g0 < gstep ? Hkv - g0 : gstep;
+    a.route = route_ids + (int64_t)g0 * route_group_stride;
+    a.flag_routes = (route_group_stride != 0 || g0 == 0) ? 1 : 0;
     irs::AttnMaps maps;
     memset(&maps, 0, sizeof(maps));
     // Runs of 64 consecutive routed rows load as TMA row tiles when the key/value rows cannot
@@ -417,6 +454,18 @@ irs_status irs_sparse_gqa_attn_fwd(const void* q, int64_t q_stride_t, int64_t q_
                                    float* lse, int32_t* err_flag, irs_stream_t stream) {
   return attn_fwd_impl(q, q_stride_t, q_stride_h, k, k_stride_t, k_stride_h, v, v_stride_t, v_stride_h, route_ids,
                        route_stride, T, Tk, Hq, Hkv, Dqk, Dv, W, scale, nullptr, 0, 0, out, lse, err_flag, stream);
+}
+
+irs_status irs_sparse_gqa_attn_fwd_grouped(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k,
+                                           int64_t k_stride_t, int64_t k_stride_h, const void* v, int64_t v_stride_t,
+                                           int64_t v_stride_h, const int32_t* route_ids, int64_t route_stride,
+                                           int64_t route_group_stride, int T, int Tk, int Hq, int Hkv, int Dqk,
+                                           int Dv, int W, float scale, void* out, float* lse, int32_t* err_flag,
+                                           irs_stream_t stream) {
+  if (route_group_stride < W) return fail(IRS_ERR_VALUE, "route_group_stride must be >= W");
+  return attn_fwd_impl(q, q_stride_t, q_stride_h, k, k_stride_t, k_stride_h, v, v_stride_t, v_stride_h, route_ids,
+                       route_stride, T, Tk, Hq, Hkv, Dqk, Dv, W, scale, nullptr, 0, 0, out, lse, err_flag, stream,
+                       route_group_stride);
 }
 
 irs_status irs_sparse_gqa_attn_fwd_windowed(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k,
@@ -565,7 +614,7 @@ extern "C" irs_status irs_sparse_index_score_topk_noalloc(const void* qI, const 
   float* scores = scores_dbg != nullptr ? scores_dbg : reinterpret_cast<float*>(ws + p.off_scores);
   const int64_t ldS = scores_dbg != nullptr ? ld_scores : p.ldS;
   CUtensorMap tm_q, tm_k;
-  if ((s = make_tmap(&tm_q, qI, (uint64_t)Di, (uint64_t)T * Hi, 256)) != IRS_OK) return s;
+  if ((s = make_query_tiles_map(&tm_q, qI, (uint64_t)Di, (uint64_t)Hi, (uint64_t)T, (uint32_t)Hi)) != IRS_OK) return s;
   if ((s = make_tmap(&tm_k, ws + p.off_kbar, (uint64_t)Di, (uint64_t)p.nblk_cap, 128)) != IRS_OK) return s;
   return launch_status(irs::launch_index(p, static_cast<const __nv_bfloat16*>(qI),
                                          static_cast<const __nv_bfloat16*>(kI), w, cu_seqlens, ndocs, max_doc_len, T,

@@ -266,6 +266,7 @@ struct TopkArgs {
   int32_t* err;
   int ndocs, T, c, budget, max_doc_len;
   int nvis_cap;          // shared-memory capacity in blocks
+  int64_t route_ts;      // elements between the route rows of consecutive tokens
 };
 
 __global__ void __launch_bounds__(kTopkThreads) topk_expand_kernel(TopkArgs a) {
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_expand_kernel(TopkArgs a) {
   const int t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int W = a.budget + a.c - 1;
-  int32_t* out = a.route + (long long)t * W;
+  int32_t* out = a.route + (long long)t * a.route_ts;
 
   const int d = find_doc(a.cu, a.ndocs, t);
   const int s = a.cu[d], e = a.cu[d + 1];
@@ -504,7 +505,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_reg_kernel(TopkArgs a) {
   const int t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int W = a.budget + a.c - 1;
-  int32_t* out = a.route + (long long)t * W;
+  int32_t* out = a.route + (long long)t * a.route_ts;
   const int d = find_doc(a.cu, a.ndocs, t);
   const int s = a.cu[d], e = a.cu[d + 1];
   if (!(s <= t && t < e && e <= a.T && e - s <= a.max_doc_len)) {
@@ -741,20 +742,36 @@ cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv
                          const int32_t* cu, int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
                          int32_t* route, float* scores, int64_t ldS, uint8_t* ws, int32_t* err,
                          const CUtensorMap& tm_q, const CUtensorMap& tm_k, int num_sms, cudaStream_t stream,
-                         const FrontHalf* front) {
+                         const FrontHalf* front, int G, int64_t scores_group_stride) {
   int32_t* meta = reinterpret_cast<int32_t*>(ws + p.off_meta);
   int32_t* blk_off = reinterpret_cast<int32_t*>(ws + p.off_blk);
   int32_t* tile_off = reinterpret_cast<int32_t*>(ws + p.off_tile);
   __nv_bfloat16* kbar = reinterpret_cast<__nv_bfloat16*>(ws + p.off_kbar);
   launch_pool(p, qI, kI, cu, ndocs, max_doc_len, T, Hi, Di, c, ws, err, front, kbar,
               reinterpret_cast<__nv_bfloat16*>(ws + p.off_qfront), stream);
-  IndexArgs ia{w, cu, blk_off, tile_off, meta, scores, ldS, err, ndocs, T, c, p.QT, p.tau_sparse, p.stages};
   const int grid = num_sms < kMaxIndexCtas ? num_sms : kMaxIndexCtas;
-  const cudaError_t le = Di == 64 ? launch_score_64(Hi, grid, p.score_smem, stream, tm_q, tm_k, ia)
-                                  : launch_score_128(Hi, grid, p.score_smem, stream, tm_q, tm_k, ia);
-  if (le != cudaSuccess) return le;
-  TopkArgs ta{scores, ldS, cu, meta, route, err, ndocs, T, c, budget, max_doc_len, (int)p.ldS};
-  return launch_topk(ta, p.kb, stream, p.topk_smem);
+  const int W = budget + c - 1;
+  // one score + top-k pass per KV group (Step-5 selects per group), sharing the pooled keys;
+  // passes run in stream order, so they can share the score scratch
+  for (int g = 0; g < G; ++g) {
+    // the score kernel's tile counter (meta[3]) starts at 0 for every pass (the layout
+    // kernel has reset it for the first)
+    if (g > 0) {
+      const cudaError_t me = cudaMemsetAsync(meta + 3, 0, sizeof(int32_t), stream);
+      if (me != cudaSuccess) return me;
+    }
+    float* sg = scores + (int64_t)g * scores_group_stride;
+    IndexArgs ia{w + (int64_t)g * Hi, cu, blk_off, tile_off, meta, sg, ldS, err, ndocs, T, c, p.QT, p.tau_sparse,
+                 p.stages, (int64_t)G * Hi, g * Hi};
+    const cudaError_t le = Di == 64 ? launch_score_64(Hi, grid, p.score_smem, stream, tm_q, tm_k, ia)
+                                    : launch_score_128(Hi, grid, p.score_smem, stream, tm_q, tm_k, ia);
+    if (le != cudaSuccess) return le;
+    TopkArgs ta{sg, ldS, cu, meta, route + (int64_t)g * W, err, ndocs, T, c, budget, max_doc_len, (int)p.ldS,
+                (int64_t)G * W};
+    const cudaError_t te = launch_topk(ta, p.kb, stream, p.topk_smem);
+    if (te != cudaSuccess) return te;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_front_operands(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI,
@@ -768,7 +785,7 @@ cudaError_t launch_front_operands(const IndexPlan& p, const __nv_bfloat16* qI, c
 cudaError_t launch_topk_from_scores(const float* scores, int64_t ldS, const int32_t* cu, int ndocs, int max_doc_len,
                                     int T, int c, int budget, int32_t* route, int32_t* err, cudaStream_t stream) {
   const int nvis_cap = max_doc_len / c > 0 ? max_doc_len / c : 1;
-  TopkArgs ta{scores, ldS, cu, nullptr, route, err, ndocs, T, c, budget, max_doc_len, nvis_cap};
+  TopkArgs ta{scores, ldS, cu, nullptr, route, err, ndocs, T, c, budget, max_doc_len, nvis_cap, budget + c - 1};
   return launch_topk(ta, budget / c, stream, topk_smem_bytes(nvis_cap, budget / c));
 }
 

@@ -73,6 +73,9 @@ struct IndexArgs {
   int64_t ldS;
   int32_t* err;
   int ndocs, T, c, QT, tau_sparse, stages;
+  int64_t w_ts;       // elements between the head weights of consecutive tokens (Hi, or G*Hi
+                      // for per-group weights, w already offset to the group)
+  int q_y0;           // first of the token's query rows in tm_q (g*Hi for group g)
 };
 
 __device__ __forceinline__ int rot_tile(int j, int jrot, int nbt) {
@@ -201,8 +204,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&b_full[bs], L::kBBytes);
+        // tm_q: 3-D [T][rows per token][Di], box {64, Hi, QT}: the tile's (query, head) rows
         for (int ka = 0; ka < KATOMS; ++ka)
-          tma_load_2d(sB + bs * L::kBBytes + ka * L::kBAtom, &tm_q, ka * 64, ti.t0 * HI, &b_full[bs]);
+          tma_load_3d(sB + bs * L::kBBytes + ka * L::kBAtom, &tm_q, ka * 64, a.q_y0, ti.t0, &b_full[bs]);
       }
       // head weights of the tile's (query, head) columns (zero past the last token); all
       // loads are issued before the stores
@@ -210,8 +214,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         float wv[kIdxN / 32];
 #pragma unroll
         for (int k = 0; k < kIdxN / 32; ++k) {
-          const long long gi = (long long)ti.t0 * HI + k * 32 + lane;
-          wv[k] = gi < (long long)a.T * HI ? __ldg(a.w + gi) : 0.f;
+          const int col = k * 32 + lane;
+          const long long tq = (long long)ti.t0 + col / HI;
+          wv[k] = tq < a.T ? __ldg(a.w + tq * a.w_ts + (col % HI)) : 0.f;
         }
 #pragma unroll
         for (int k = 0; k < kIdxN / 32; ++k) sW[bs * kIdxN + k * 32 + lane] = wv[k];

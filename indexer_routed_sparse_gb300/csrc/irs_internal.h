@@ -43,12 +43,14 @@ size_t topk_smem_bytes(int nvis_cap, int kb);
 cudaError_t configure_score_kernels(size_t smem);
 cudaError_t configure_topk_kernel(size_t smem);
 // front == nullptr: the plain indexer. Otherwise the scores use the transformed queries
-// (tm_q must map ws + p.off_qfront) and the transformed pooled keys.
+// (tm_q must map ws + p.off_qfront) and the transformed pooled keys. G > 1: per-group
+// selection; tm_q maps [T][G*Hi][Di], w is [T, G, Hi], route [T, G, W], and group g's score
+// rows start at scores + g * scores_group_stride (row stride ldS).
 cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI, const float* w,
                          const int32_t* cu, int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
                          int32_t* route, float* scores, int64_t ldS, uint8_t* ws, int32_t* err,
                          const CUtensorMap& tm_q, const CUtensorMap& tm_k, int num_sms, cudaStream_t stream,
-                         const FrontHalf* front = nullptr);
+                         const FrontHalf* front = nullptr, int G = 1, int64_t scores_group_stride = 0);
 // The front half alone: transformed queries [T*Hi, Di] into q_out, pooled keys [T/c, Di]
 // into k_out (rows past the last complete block zeroed).
 cudaError_t launch_front_operands(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI,
@@ -93,6 +95,7 @@ struct AttnArgs {
   const int32_t* cu;
   int ndocs;
   int window;
+  int flag_routes;   // 1: this launch reports route IDs out of range (each route row once)
 };
 
 struct AttnPlan {
