@@ -185,6 +185,26 @@ irs_status irs_sparse_index_score_topk_grouped(const void* qI, const void* kI, c
                                                size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream);
 
 /*
+ * The indexer with FP8 E4M3 scoring operands.
+ *
+ * Step-5 sparse page, `indexer_score_tile` (queries and summaries rounded to FP8 E4M3) and
+ * `_summarize_region_payload` (summaries keep both roundings, BF16 then FP8). Queries are
+ * rounded bf16 -> E4M3, pooled keys FP32 mean -> bf16 -> E4M3 (to nearest, ties to even,
+ * saturating at +-448), and the block scores run on the kind::f8f6f4 tensor-core path
+ * (products of E4M3 values accumulated in FP32); top-k and routes as in
+ * irs_sparse_index_score_topk. Di must be 128. The workspace is
+ * irs_index_e4m3_workspace_bytes(...) bytes (the plain scratch plus the byte copies of the
+ * queries [T, Hi, Di] and pooled keys [floor(T/c), Di]). Other arguments as for
+ * irs_sparse_index_score_topk.
+ */
+size_t irs_index_e4m3_workspace_bytes(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len,
+                                      int with_score_buffer);
+irs_status irs_sparse_index_score_topk_e4m3(const void* qI, const void* kI, const float* w, const int32_t* cu_seqlens,
+                                            int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
+                                            int32_t* route_ids, float* scores_dbg, int64_t ld_scores, void* workspace,
+                                            size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream);
+
+/*
  * irs_sparse_index_score_topk without a workspace: the same computation and arguments,
  * minus `workspace` / `workspace_bytes`. The reference pages have no counterpart; this
  * entry point exists for callers that cannot allocate device memory for the library,

@@ -45,6 +45,9 @@ _SIGNATURES = {
                                                  _SZ, _P, _P]),
     "irs_sparse_gqa_attn_fwd_grouped": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _I, _I,
                                              _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
+    "irs_index_e4m3_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
+    "irs_sparse_index_score_topk_e4m3": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I64, _P, _SZ, _P,
+                                              _P]),
     "irs_topk_from_scores": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "irs_compose_window_routes": (_I, [_P, _I, _P, _I, _I, _I, _P, _P, _P]),
     "irs_sparse_gqa_attn_fwd": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I, _I, _I, _I, _I, _I,
@@ -170,7 +173,7 @@ def sparse_index_score_topk(qI: torch.Tensor, kI: torch.Tensor, w: torch.Tensor,
                             c: int, budget: int, *, ndocs: int | None = None, max_doc_len: int | None = None,
                             scores_out: torch.Tensor | None = None, out: torch.Tensor | None = None,
                             workspace: torch.Tensor | None = None, err: torch.Tensor | None = None,
-                            front: dict | None = None) -> torch.Tensor:
+                            front: dict | None = None, operands: str = "bf16") -> torch.Tensor:
     """Route IDs int32 [T, budget + c - 1] from the compressed-block indexer.
 
     qI bf16 [T, Hi, Di], kI bf16 [T, Di] (or [T, 1, Di]), w fp32 [T, Hi], cu_seqlens int32
@@ -178,7 +181,12 @@ def sparse_index_score_topk(qI: torch.Tensor, kI: torch.Tensor, w: torch.Tensor,
     the block scores of every row with more than budget // c visible blocks. `front` (a dict
     of fp32 device tensors q_weight [Di], k_weight [Di], rope [T, rope_dims] and a float eps)
     adds the indexer's front half: RMSNorm and RoPE of queries and pooled keys.
+    operands="e4m3" scores with the Step-5 FP8 E4M3 roundings of queries and pooled keys.
     """
+    if operands not in ("bf16", "e4m3"):
+        raise ValueError("operands must be 'bf16' or 'e4m3'")
+    if operands == "e4m3" and front is not None:
+        raise ValueError("E4M3 operands are not combined with the front half")
     _need(qI, "qI", torch.bfloat16, 3)
     _need(kI, "kI", torch.bfloat16)
     _need(w, "w", torch.float32, 2)
@@ -201,7 +209,10 @@ def sparse_index_score_topk(qI: torch.Tensor, kI: torch.Tensor, w: torch.Tensor,
         if scores_out.shape[0] != T or scores_out.stride(1) != 1:
             raise ValueError("scores_out must be [T, ld] with unit inner stride")
         ld = scores_out.stride(0)
-    if front is None:
+    if operands == "e4m3":
+        nbytes = int(lib().irs_index_e4m3_workspace_bytes(T, Hi, Di, c, budget, ndocs, max_doc_len,
+                                                          int(scores_out is None)))
+    elif front is None:
         nbytes = index_workspace_bytes(T, Hi, Di, c, budget, ndocs, max_doc_len, scores_out is None)
     else:
         nbytes = int(lib().irs_index_front_workspace_bytes(T, Hi, Di, c, budget, ndocs, max_doc_len,
@@ -212,7 +223,11 @@ def sparse_index_score_topk(qI: torch.Tensor, kI: torch.Tensor, w: torch.Tensor,
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     if err is None:
         err = device_error_flag(dev)
-    if front is None:
+    if operands == "e4m3":
+        st = lib().irs_sparse_index_score_topk_e4m3(
+            _ptr(qI), _ptr(kI), _ptr(w), _ptr(cu_seqlens), ndocs, max_doc_len, T, Hi, Di, c, budget, _ptr(out),
+            _ptr(scores_out), ld, _ptr(workspace), workspace.numel(), _ptr(err), _stream(dev))
+    elif front is None:
         st = lib().irs_sparse_index_score_topk(
             _ptr(qI), _ptr(kI), _ptr(w), _ptr(cu_seqlens), ndocs, max_doc_len, T, Hi, Di, c, budget, _ptr(out),
             _ptr(scores_out), ld, _ptr(workspace), workspace.numel(), _ptr(err), _stream(dev))

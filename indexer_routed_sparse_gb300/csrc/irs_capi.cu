@@ -125,6 +125,33 @@ irs_status make_query_tiles_map(CUtensorMap* m, const void* base, uint64_t Di, u
   return IRS_OK;
 }
 
+// Byte maps for E4M3 operands (128-byte SW128 rows of 128 elements): the queries as
+// [T][Hi][Di] with box {128, Hi, 256/Hi}, the pooled keys as [rows][Di] with box {128, 128}.
+irs_status make_e4m3_maps(CUtensorMap* tq, CUtensorMap* tk, const void* q8, const void* k8, uint64_t Di, uint64_t Hi,
+                          uint64_t T, uint64_t krows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(IRS_ERR_RUNTIME, "cuTensorMapEncodeTiled is unavailable");
+  {
+    cuuint64_t dims[3] = {Di, Hi, T};
+    cuuint64_t strides[2] = {Di, Hi * Di};
+    cuuint32_t box[3] = {128, (cuuint32_t)Hi, (cuuint32_t)(256 / Hi)};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q8), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(IRS_ERR_RUNTIME, "cuTensorMapEncodeTiled (E4M3 queries) failed (%d)", (int)r);
+  }
+  cuuint64_t dims[2] = {Di, krows};
+  cuuint64_t strides[1] = {Di};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(k8), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(IRS_ERR_RUNTIME, "cuTensorMapEncodeTiled (E4M3 keys) failed (%d)", (int)r);
+  return IRS_OK;
+}
+
 irs_status launch_status(cudaError_t e, const char* what) {
   if (e != cudaSuccess) return fail(IRS_ERR_RUNTIME, "%s: %s", what, cudaGetErrorString(e));
   return IRS_OK;
@@ -195,9 +222,12 @@ irs_status check_front(const float* q_weight, const float* k_weight, float eps, 
 irs_status index_impl(const void* qI, const void* kI, const float* w, const int32_t* cu_seqlens, int ndocs,
                       int max_doc_len, int T, int Hi, int Di, int c, int budget, const irs::FrontHalf* front,
                       int32_t* route_ids, float* scores_dbg, int64_t ld_scores, void* workspace,
-                      size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream, int G = 1) {
+                      size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream, int G = 1,
+                      bool e4m3 = false) {
   irs_status s = check_index_sizes(T, Hi, Di, c, budget, ndocs, max_doc_len);
   if (s != IRS_OK) return s;
+  if (e4m3 && (Di != 128 || G != 1 || front != nullptr))
+    return fail(IRS_ERR_VALUE, "E4M3 scoring needs Di = 128 (one group, no front half)");
   if (G < 1 || (long long)T * G * Hi >= (1LL << 31)) return fail(IRS_ERR_VALUE, "bad group count %d", G);
   if (!qI || !kI || !w || !cu_seqlens || !route_ids || !workspace)
     return fail(IRS_ERR_VALUE, "NULL tensor pointer");
@@ -205,7 +235,7 @@ irs_status index_impl(const void* qI, const void* kI, const float* w, const int3
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(IRS_ERR_VALUE, "workspace must be 256-byte aligned");
   const irs::IndexPlan p =
-      irs::plan_index(T, Hi, Di, c, budget, ndocs, max_doc_len, scores_dbg == nullptr, front != nullptr);
+      irs::plan_index(T, Hi, Di, c, budget, ndocs, max_doc_len, scores_dbg == nullptr, front != nullptr, e4m3);
   if (scores_dbg != nullptr && ld_scores < p.ldS)
     return fail(IRS_ERR_VALUE, "ld_scores must be >= max_doc_len / c (%lld)", (long long)p.ldS);
   if (workspace_bytes < p.ws_bytes)
@@ -222,14 +252,20 @@ irs_status index_impl(const void* qI, const void* kI, const float* w, const int3
   CUtensorMap tm_q, tm_k;
   // with the front half the scores read the transformed queries from the workspace
   const void* qsrc = front != nullptr ? static_cast<const void*>(ws + p.off_qfront) : qI;
-  if ((s = make_query_tiles_map(&tm_q, qsrc, (uint64_t)Di, (uint64_t)G * Hi, (uint64_t)T, (uint32_t)Hi)) != IRS_OK)
-    return s;
-  if ((s = make_tmap(&tm_k, ws + p.off_kbar, (uint64_t)Di, (uint64_t)p.nblk_cap, 128)) != IRS_OK) return s;
+  if (e4m3) {
+    if ((s = make_e4m3_maps(&tm_q, &tm_k, ws + p.off_q8, ws + p.off_k8, (uint64_t)Di, (uint64_t)Hi, (uint64_t)T,
+                            (uint64_t)p.nblk_cap)) != IRS_OK)
+      return s;
+  } else {
+    if ((s = make_query_tiles_map(&tm_q, qsrc, (uint64_t)Di, (uint64_t)G * Hi, (uint64_t)T, (uint32_t)Hi)) != IRS_OK)
+      return s;
+    if ((s = make_tmap(&tm_k, ws + p.off_kbar, (uint64_t)Di, (uint64_t)p.nblk_cap, 128)) != IRS_OK) return s;
+  }
   return launch_status(irs::launch_index(p, static_cast<const __nv_bfloat16*>(qI),
                                          static_cast<const __nv_bfloat16*>(kI), w, cu_seqlens, ndocs, max_doc_len, T,
                                          Hi, Di, c, budget, route_ids, scores, ldS, ws, err_flag, tm_q, tm_k,
                                          dev->num_sms, reinterpret_cast<cudaStream_t>(stream), front, G,
-                                         group_stride),
+                                         group_stride, e4m3),
                        "launching the indexer");
 }
 
@@ -271,6 +307,20 @@ irs_status irs_sparse_index_score_topk_grouped(const void* qI, const void* kI, c
                                                size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream) {
   return index_impl(qI, kI, w, cu_seqlens, ndocs, max_doc_len, T, Hi, Di, c, budget, nullptr, route_ids, scores_dbg,
                     ld_scores, workspace, workspace_bytes, err_flag, stream, G);
+}
+
+size_t irs_index_e4m3_workspace_bytes(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len,
+                                      int with_score_buffer) {
+  if (check_index_sizes(T, Hi, Di, c, budget, ndocs, max_doc_len) != IRS_OK || Di != 128) return 0;
+  return irs::plan_index(T, Hi, Di, c, budget, ndocs, max_doc_len, with_score_buffer != 0, false, true).ws_bytes;
+}
+
+irs_status irs_sparse_index_score_topk_e4m3(const void* qI, const void* kI, const float* w, const int32_t* cu_seqlens,
+                                            int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
+                                            int32_t* route_ids, float* scores_dbg, int64_t ld_scores, void* workspace,
+                                            size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream) {
+  return index_impl(qI, kI, w, cu_seqlens, ndocs, max_doc_len, T, Hi, Di, c, budget, nullptr, route_ids, scores_dbg,
+                    ld_scores, workspace, workspace_bytes, err_flag, stream, 1, true);
 }
 
 irs_status irs_index_front_operands(const void* qI, const void* kI, const int32_t* cu_seqlens, int ndocs,

@@ -6,6 +6,8 @@
 // `select_qsa_token_ids`, `Qwen3_8_FlashNextQSAIndexer`, `_forward_packed`) and the Step-5
 // sparse page (nemo_automodel.components.models.step5.sparse: `indexer_score_tile`,
 // `pack_region_bitmap`).
+#include <cuda_fp8.h>
+
 #include "irs_index_score.cuh"
 
 namespace irs {
@@ -93,7 +95,8 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
                                                    const int32_t* __restrict__ cu, int ndocs, int Di, int c,
                                                    int nblk_cap, const int32_t* __restrict__ meta,
                                                    const int32_t* __restrict__ blk_off,
-                                                   __nv_bfloat16* __restrict__ kbar, float* __restrict__ kbar32) {
+                                                   __nv_bfloat16* __restrict__ kbar, float* __restrict__ kbar32,
+                                                   uint8_t* __restrict__ kbar8) {
   if (meta[0] != 1) return;
   const int nblk = meta[1];
   const int chunks = Di >> 3;
@@ -102,7 +105,8 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
   const int ch = (int)(gid % chunks);
   if (gb >= nblk_cap) return;
   if (gb >= nblk) {
-    if (kbar32 == nullptr) reinterpret_cast<uint4*>(kbar + (long long)gb * Di)[ch] = make_uint4(0, 0, 0, 0);
+    if (kbar8 != nullptr) reinterpret_cast<uint2*>(kbar8 + (long long)gb * Di)[ch] = make_uint2(0, 0);
+    else if (kbar32 == nullptr) reinterpret_cast<uint4*>(kbar + (long long)gb * Di)[ch] = make_uint4(0, 0, 0, 0);
     return;
   }
   const int d = find_le(blk_off, ndocs, gb);
@@ -130,12 +134,49 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
     o4[1] = make_float4(__fdiv_rn(acc[4], fc), __fdiv_rn(acc[5], fc), __fdiv_rn(acc[6], fc), __fdiv_rn(acc[7], fc));
     return;
   }
+  if (kbar8 != nullptr) {
+    // Step-5 E4M3 summaries: the FP32 mean rounded to bf16, then to E4M3 (nearest even,
+    // saturating at 448)
+    uint8_t b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float m = __bfloat162float(__float2bfloat16_rn(__fdiv_rn(acc[i], fc)));
+      b[i] = (uint8_t)__nv_cvt_float_to_fp8(m, __NV_SATFINITE, __NV_E4M3);
+    }
+    reinterpret_cast<uint2*>(kbar8 + (long long)gb * Di)[ch] = *reinterpret_cast<const uint2*>(b);
+    return;
+  }
   uint4 o;
   __nv_bfloat162* q = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
     q[i] = __floats2bfloat162_rn(__fdiv_rn(acc[2 * i], fc), __fdiv_rn(acc[2 * i + 1], fc));
   reinterpret_cast<uint4*>(kbar + (long long)gb * Di)[ch] = o;
+}
+
+// Step-5 E4M3 queries: every bf16 index query value rounded to E4M3 (nearest even,
+// saturating at 448). Thread = 16 consecutive values.
+__global__ void __launch_bounds__(256) quantize_e4m3_kernel(const __nv_bfloat16* __restrict__ x, long long n16,
+                                                            uint8_t* __restrict__ y) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n16) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x) + 2 * i;
+  uint8_t b[16];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float f[8];
+    const uint4 u = __ldg(src + h);
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 v = __bfloat1622float2(p[k]);
+      f[2 * k] = v.x;
+      f[2 * k + 1] = v.y;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) b[8 * h + k] = (uint8_t)__nv_cvt_float_to_fp8(f[k], __NV_SATFINITE, __NV_E4M3);
+  }
+  reinterpret_cast<uint4*>(y)[i] = *reinterpret_cast<const uint4*>(b);
 }
 
 // =====================================================================================
@@ -676,7 +717,7 @@ __global__ void __launch_bounds__(128) compose_window_kernel(const int32_t* __re
 // host launchers
 // =====================================================================================
 IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len, bool with_scores,
-                     bool front) {
+                     bool front, bool e4m3) {
   IndexPlan p{};
   p.kb = budget / c;
   p.QT = kIdxN / Hi;
@@ -697,9 +738,16 @@ IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int ma
   p.off_scores = with_scores ? take((size_t)T * p.ldS * sizeof(float), 1024) : 0;
   p.off_qfront = front ? take((size_t)T * Hi * Di * 2, 1024) : 0;
   p.off_kbar32 = front ? take((size_t)p.nblk_cap * Di * sizeof(float), 1024) : 0;
+  p.off_q8 = e4m3 ? take((size_t)T * Hi * Di, 1024) : 0;
+  p.off_k8 = e4m3 ? take((size_t)p.nblk_cap * Di, 1024) : 0;
   p.ws_bytes = (off + 255) / 256 * 256;
-  p.stages = Di == 64 ? 8 : 5;
-  p.score_smem = Di == 64 ? IdxSmem<64>::total(p.stages) : IdxSmem<128>::total(p.stages);
+  if (e4m3) {   // one 128-byte atom per key tile
+    p.stages = 8;
+    p.score_smem = IdxSmem<128, true>::total(p.stages);
+  } else {
+    p.stages = Di == 64 ? 8 : 5;
+    p.score_smem = Di == 64 ? IdxSmem<64>::total(p.stages) : IdxSmem<128>::total(p.stages);
+  }
   p.topk_smem = topk_smem_bytes(p.ldS, p.kb);
   return p;
 }
@@ -713,7 +761,8 @@ size_t topk_smem_bytes(int nvis_cap, int kb) {
 // kbar, transformed queries into qfront.
 static void launch_pool(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI, const int32_t* cu,
                         int ndocs, int max_doc_len, int T, int Hi, int Di, int c, uint8_t* ws, int32_t* err,
-                        const FrontHalf* front, __nv_bfloat16* kbar, __nv_bfloat16* qfront, cudaStream_t stream) {
+                        const FrontHalf* front, __nv_bfloat16* kbar, __nv_bfloat16* qfront, cudaStream_t stream,
+                        bool e4m3 = false) {
   int32_t* meta = reinterpret_cast<int32_t*>(ws + p.off_meta);
   int32_t* blk_off = reinterpret_cast<int32_t*>(ws + p.off_blk);
   int32_t* tile_off = reinterpret_cast<int32_t*>(ws + p.off_tile);
@@ -725,7 +774,11 @@ static void launch_pool(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_
     const long long threads = (long long)p.nblk_cap * (Di / 8);
     const int grid = (int)((threads + 255) / 256);
     pool_kernel<<<grid, 256, 0, stream>>>(kI, cu, ndocs, Di, c, p.nblk_cap, meta, blk_off, kbar,
-                                          front ? kbar32 : nullptr);
+                                          front ? kbar32 : nullptr, e4m3 ? ws + p.off_k8 : nullptr);
+  }
+  if (e4m3) {
+    const long long n16 = (long long)T * Hi * Di / 16;
+    quantize_e4m3_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, stream>>>(qI, n16, ws + p.off_q8);
   }
   if (front) {
     front_keys_kernel<<<(p.nblk_cap + 127) / 128, 128, 0, stream>>>(kbar32, p.nblk_cap, Di, meta, blk_off, cu, ndocs, c,
@@ -742,13 +795,13 @@ cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv
                          const int32_t* cu, int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
                          int32_t* route, float* scores, int64_t ldS, uint8_t* ws, int32_t* err,
                          const CUtensorMap& tm_q, const CUtensorMap& tm_k, int num_sms, cudaStream_t stream,
-                         const FrontHalf* front, int G, int64_t scores_group_stride) {
+                         const FrontHalf* front, int G, int64_t scores_group_stride, bool e4m3) {
   int32_t* meta = reinterpret_cast<int32_t*>(ws + p.off_meta);
   int32_t* blk_off = reinterpret_cast<int32_t*>(ws + p.off_blk);
   int32_t* tile_off = reinterpret_cast<int32_t*>(ws + p.off_tile);
   __nv_bfloat16* kbar = reinterpret_cast<__nv_bfloat16*>(ws + p.off_kbar);
   launch_pool(p, qI, kI, cu, ndocs, max_doc_len, T, Hi, Di, c, ws, err, front, kbar,
-              reinterpret_cast<__nv_bfloat16*>(ws + p.off_qfront), stream);
+              reinterpret_cast<__nv_bfloat16*>(ws + p.off_qfront), stream, e4m3);
   const int grid = num_sms < kMaxIndexCtas ? num_sms : kMaxIndexCtas;
   const int W = budget + c - 1;
   // one score + top-k pass per KV group (Step-5 selects per group), sharing the pooled keys;
@@ -763,8 +816,9 @@ cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv
     float* sg = scores + (int64_t)g * scores_group_stride;
     IndexArgs ia{w + (int64_t)g * Hi, cu, blk_off, tile_off, meta, sg, ldS, err, ndocs, T, c, p.QT, p.tau_sparse,
                  p.stages, (int64_t)G * Hi, g * Hi};
-    const cudaError_t le = Di == 64 ? launch_score_64(Hi, grid, p.score_smem, stream, tm_q, tm_k, ia)
-                                    : launch_score_128(Hi, grid, p.score_smem, stream, tm_q, tm_k, ia);
+    const cudaError_t le = e4m3 ? launch_score_e4m3(Hi, grid, p.score_smem, stream, tm_q, tm_k, ia)
+                           : (Di == 64 ? launch_score_64(Hi, grid, p.score_smem, stream, tm_q, tm_k, ia)
+                                       : launch_score_128(Hi, grid, p.score_smem, stream, tm_q, tm_k, ia));
     if (le != cudaSuccess) return le;
     TopkArgs ta{sg, ldS, cu, meta, route + (int64_t)g * W, err, ndocs, T, c, budget, max_doc_len, (int)p.ldS,
                 (int64_t)G * W};
@@ -798,7 +852,8 @@ cudaError_t launch_compose_window(const int32_t* route, int W, const int32_t* cu
 cudaError_t configure_score_kernels(size_t smem) {
   cudaError_t e = configure_score_64(smem);
   if (e != cudaSuccess) return e;
-  return configure_score_128(smem);
+  if ((e = configure_score_128(smem)) != cudaSuccess) return e;
+  return configure_score_e4m3(smem);
 }
 
 cudaError_t configure_topk_kernel(size_t smem) {

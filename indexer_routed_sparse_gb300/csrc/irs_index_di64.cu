@@ -5,9 +5,9 @@ namespace irs {
 
 cudaError_t launch_score_64(int Hi, int grid, size_t smem, cudaStream_t st, const CUtensorMap& tq,
                              const CUtensorMap& tk, const IndexArgs& ia) {
-  return launch_score_di<64>(Hi, grid, smem, st, tq, tk, ia);
+  return launch_score_di<64, false>(Hi, grid, smem, st, tq, tk, ia);
 }
 
-cudaError_t configure_score_64(size_t smem) { return score_attr_all<64>(smem); }
+cudaError_t configure_score_64(size_t smem) { return score_attr_all<64, false>(smem); }
 
 }  // namespace irs

@@ -109,10 +109,13 @@ __device__ __forceinline__ float w4f(const float4* w4, int k) {
   return (k & 3) == 0 ? v.x : ((k & 3) == 1 ? v.y : ((k & 3) == 2 ? v.z : v.w));
 }
 
-template <int DI>
+// Shared-memory layout of the score kernel for Di of bf16 (F8 = false: 64 elements per
+// 128-byte atom row) or of E4M3 (F8 = true: 128 elements per row) operands.
+template <int DI, bool F8 = false>
 struct IdxSmem {
+  static constexpr int kAtomElems = F8 ? 128 : 64;
   static constexpr uint32_t kBAtom = kIdxN * 128;
-  static constexpr uint32_t kBBytes = (DI / 64) * kBAtom;
+  static constexpr uint32_t kBBytes = (DI / kAtomElems) * kBAtom;
   static constexpr uint32_t b_off = 0;                                   // [2] query tiles
   static constexpr uint32_t a_off = 2 * kBBytes;                         // [stages] key atoms
   __host__ __device__ static uint32_t w_off(int st) { return a_off + (uint32_t)st * kIdxAtom; }   // [2][256] fp32
@@ -122,13 +125,20 @@ struct IdxSmem {
   __host__ __device__ static uint32_t total(int st) { return bar_off(st) + (2 * st + 17) * 8 + 16 + 1024; }
 };
 
-template <int DI, int HI>
+template <bool F8>
+__device__ __forceinline__ void umma_op(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if constexpr (F8) umma_f8(d, a, b, idesc, acc);
+  else umma_bf16(d, a, b, idesc, acc);
+}
+
+template <int DI, int HI, bool F8>
 __global__ void __launch_bounds__(kIdxThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        IndexArgs a) {
-  constexpr int KATOMS = DI / 64;
-  using L = IdxSmem<DI>;
-  constexpr uint32_t IDESC = idesc_bf16(kIdxM, kIdxN, false, false);
+  using L = IdxSmem<DI, F8>;
+  constexpr int AE = L::kAtomElems;   // elements per 128-byte row of an atom
+  constexpr int KATOMS = DI / AE;
+  constexpr uint32_t IDESC = F8 ? idesc_e4m3(kIdxM, kIdxN) : idesc_bf16(kIdxM, kIdxN, false, false);
   constexpr int kColsPerWarp = kIdxN / 2;
 
   extern __shared__ uint8_t smem_raw[];
@@ -206,7 +216,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         mbar_arrive_expect_tx(&b_full[bs], L::kBBytes);
         // tm_q: 3-D [T][rows per token][Di], box {64, Hi, QT}: the tile's (query, head) rows
         for (int ka = 0; ka < KATOMS; ++ka)
-          tma_load_3d(sB + bs * L::kBBytes + ka * L::kBAtom, &tm_q, ka * 64, a.q_y0, ti.t0, &b_full[bs]);
+          tma_load_3d(sB + bs * L::kBBytes + ka * L::kBAtom, &tm_q, ka * AE, a.q_y0, ti.t0, &b_full[bs]);
       }
       // head weights of the tile's (query, head) columns (zero past the last token); all
       // loads are issued before the stores
@@ -234,7 +244,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
               break;
             }
             mbar_arrive_expect_tx(&a_full[st], kIdxAtom);
-            tma_load_2d(sA + (size_t)st * kIdxAtom, &tm_k, ka * 64, ti.blk0 + bt * kIdxM, &a_full[st]);
+            tma_load_2d(sA + (size_t)st * kIdxAtom, &tm_k, ka * AE, ti.blk0 + bt * kIdxM, &a_full[st]);
           }
         }
       }
@@ -278,7 +288,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             const uint64_t bd = sdesc_sw128(b_base + ka * L::kBAtom, 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              umma_bf16(tbase + buf * kIdxN, ad + (uint64_t)((ks * 32) >> 4), bd + (uint64_t)((ks * 32) >> 4), IDESC,
+              umma_op<F8>(tbase + buf * kIdxN, ad + (uint64_t)((ks * 32) >> 4), bd + (uint64_t)((ks * 32) >> 4), IDESC,
                         (ka > 0 || ks > 0) ? 1u : 0u);
             umma_commit(&a_empty[st]);
           }
@@ -404,39 +414,38 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   }
 }
 
-// Host side of the Di-specific translation units.
-template <int DI>
+// Host side of the translation units that instantiate the kernel.
+template <int DI, bool F8>
 static cudaError_t launch_score_di(int Hi, int grid, size_t smem, cudaStream_t st, const CUtensorMap& tq,
                                    const CUtensorMap& tk, const IndexArgs& ia) {
   switch (Hi) {
-    case 1: score_kernel<DI, 1><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
-    case 2: score_kernel<DI, 2><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
-    case 4: score_kernel<DI, 4><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
-    case 8: score_kernel<DI, 8><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
-    case 16: score_kernel<DI, 16><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
-    case 32: score_kernel<DI, 32><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
-    case 64: score_kernel<DI, 64><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
-    case 128: score_kernel<DI, 128><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
-    default: score_kernel<DI, 256><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 1: score_kernel<DI, 1, F8><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 2: score_kernel<DI, 2, F8><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 4: score_kernel<DI, 4, F8><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 8: score_kernel<DI, 8, F8><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 16: score_kernel<DI, 16, F8><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 32: score_kernel<DI, 32, F8><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 64: score_kernel<DI, 64, F8><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    case 128: score_kernel<DI, 128, F8><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
+    default: score_kernel<DI, 256, F8><<<grid, kIdxThreads, smem, st>>>(tq, tk, ia); break;
   }
   return cudaGetLastError();
 }
 
-template <int DI, int HI>
+template <int DI, int HI, bool F8>
 static cudaError_t score_attr(size_t smem) {
-  return cudaFuncSetAttribute(score_kernel<DI, HI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return cudaFuncSetAttribute(score_kernel<DI, HI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
-template <int DI>
+template <int DI, bool F8>
 static cudaError_t score_attr_all(size_t smem) {
   cudaError_t e = cudaSuccess;
-  for (cudaError_t x : {score_attr<DI, 1>(smem), score_attr<DI, 2>(smem), score_attr<DI, 4>(smem),
-                        score_attr<DI, 8>(smem), score_attr<DI, 16>(smem), score_attr<DI, 32>(smem),
-                        score_attr<DI, 64>(smem), score_attr<DI, 128>(smem), score_attr<DI, 256>(smem)})
+  for (cudaError_t x : {score_attr<DI, 1, F8>(smem), score_attr<DI, 2, F8>(smem), score_attr<DI, 4, F8>(smem),
+                        score_attr<DI, 8, F8>(smem), score_attr<DI, 16, F8>(smem), score_attr<DI, 32, F8>(smem),
+                        score_attr<DI, 64, F8>(smem), score_attr<DI, 128, F8>(smem), score_attr<DI, 256, F8>(smem)})
     if (x != cudaSuccess) e = x;
   return e;
 }
-
 
 cudaError_t launch_score_64(int Hi, int grid, size_t smem, cudaStream_t st, const CUtensorMap& tq, const CUtensorMap& tk,
                             const IndexArgs& ia);
@@ -444,5 +453,9 @@ cudaError_t launch_score_128(int Hi, int grid, size_t smem, cudaStream_t st, con
                              const CUtensorMap& tk, const IndexArgs& ia);
 cudaError_t configure_score_64(size_t smem);
 cudaError_t configure_score_128(size_t smem);
+// E4M3 operands (Di = 128 only)
+cudaError_t launch_score_e4m3(int Hi, int grid, size_t smem, cudaStream_t st, const CUtensorMap& tq,
+                              const CUtensorMap& tk, const IndexArgs& ia);
+cudaError_t configure_score_e4m3(size_t smem);
 
 }  // namespace irs

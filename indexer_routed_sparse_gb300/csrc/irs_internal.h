@@ -33,11 +33,12 @@ struct IndexPlan {
   int stages;          // 64-dim key atoms in the score kernel's TMA ring
   size_t off_meta, off_blk, off_tile, off_kbar, off_scores, ws_bytes;
   size_t off_qfront, off_kbar32;   // front half only: transformed queries, FP32 group means
+  size_t off_q8, off_k8;           // E4M3 operands only: queries and pooled keys, one byte each
   size_t score_smem, topk_smem;
 };
 
 IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len, bool with_scores,
-                     bool front = false);
+                     bool front = false, bool e4m3 = false);
 size_t topk_smem_bytes(int nvis_cap, int kb);
 
 cudaError_t configure_score_kernels(size_t smem);
@@ -45,12 +46,15 @@ cudaError_t configure_topk_kernel(size_t smem);
 // front == nullptr: the plain indexer. Otherwise the scores use the transformed queries
 // (tm_q must map ws + p.off_qfront) and the transformed pooled keys. G > 1: per-group
 // selection; tm_q maps [T][G*Hi][Di], w is [T, G, Hi], route [T, G, W], and group g's score
-// rows start at scores + g * scores_group_stride (row stride ldS).
+// rows start at scores + g * scores_group_stride (row stride ldS). e4m3: queries and pooled
+// keys are rounded to FP8 E4M3 and scored with kind::f8f6f4 (tm_q / tm_k map the byte copies
+// at ws + p.off_q8 / p.off_k8; Di = 128).
 cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI, const float* w,
                          const int32_t* cu, int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
                          int32_t* route, float* scores, int64_t ldS, uint8_t* ws, int32_t* err,
                          const CUtensorMap& tm_q, const CUtensorMap& tm_k, int num_sms, cudaStream_t stream,
-                         const FrontHalf* front = nullptr, int G = 1, int64_t scores_group_stride = 0);
+                         const FrontHalf* front = nullptr, int G = 1, int64_t scores_group_stride = 0,
+                         bool e4m3 = false);
 // The front half alone: transformed queries [T*Hi, Di] into q_out, pooled keys [T/c, Di]
 // into k_out (rows past the last complete block zeroed).
 cudaError_t launch_front_operands(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI,
