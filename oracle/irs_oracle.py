@@ -65,6 +65,13 @@ notes of the repository):
       fused multiply-add) and rounded once to bf16.
 * R16 E4M3 operands (Step-5): queries are rounded bf16 -> E4M3 and pooled keys
       FP32 -> bf16 -> E4M3, ties to even, saturating past 448.
+* R17 Learned-logit summaries (Step-5): the page gives the inputs (keys and
+      per-dimension compression logits shaped like them), FP32 arithmetic and the
+      two roundings, not the formula. Read plainly: per region and dim, the
+      softmax of the logits over the region's c tokens weights the keys, in FP32
+      (max subtracted, sequential sums in token order, one division), then bf16,
+      then E4M3. The exponential is `exp_f32`, a stated FP32 evaluation, so that
+      the codes it decides are reproducible.
 * The FP32 mean is a sequential FP32 sum over the c rows of the block in
   ascending token order, followed by one IEEE division by c.
 * Route entries outside [0, Tk) are padding.
@@ -318,7 +325,7 @@ def route_row(doc_start: int, tau: int, c: int, budget: int, scores_f32) -> np.n
 
 def index_routes(qI_bits, kI_bits, w, cu_seqlens, c: int, budget: int, rows=None,
                  want_scores: bool = False, ldS: int | None = None, front: dict | None = None,
-                 operands: str = "bf16"):
+                 operands: str = "bf16", logits=None):
     """Indexer routes (and optionally FP32 block scores) for the requested rows.
 
     qI_bits [T, Hi, Di] bf16 bits, kI_bits [T, Di] bf16 bits, w [T, Hi] float32,
@@ -330,7 +337,12 @@ def index_routes(qI_bits, kI_bits, w, cu_seqlens, c: int, budget: int, rows=None
     normalised and rotated before scoring (`front_query_row`, `front_keys`).
     operands: "bf16", or "e4m3" for the Step-5 scoring operands: the bf16 queries and
     bf16 pooled keys are further rounded to FP8 E4M3 values (`round_to_e4m3`).
+    logits: optional Step-5 compression logits, bf16 bits shaped like kI_bits; the block
+    keys are then the learned-logit summaries (`region_summaries_e4m3`) instead of the
+    means, and `operands` decides only whether the queries are rounded to E4M3.
     """
+    if logits is not None and front is not None:
+        raise ValueError("learned-logit summaries take the keys as given (no front half)")
     if operands not in ("bf16", "e4m3"):
         raise ValueError("operands must be 'bf16' or 'e4m3'")
     if budget % c != 0 or budget <= 0 or c <= 0:
@@ -340,7 +352,9 @@ def index_routes(qI_bits, kI_bits, w, cu_seqlens, c: int, budget: int, rows=None
     rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
     kb = budget // c
     W = budget + c - 1
-    if front is None:
+    if logits is not None:
+        ktilde, blk_off = region_summaries_e4m3(kI_bits, logits, cu_seqlens, c)
+    elif front is None:
         kbar, blk_off = pool_keys(kI_bits, cu_seqlens, c)
         ktilde = round_to_bf16(kbar).astype(np.float64)
     else:
@@ -408,8 +422,89 @@ def round_to_e4m3(x: np.ndarray) -> np.ndarray:
     return np.copysign(q, x)
 
 
+# --------------------------------------------------------------------------------------
+# Step-5 learned-logit region summaries (Step-5 sparse page: `project_keys` returns the
+# index keys and per-dimension compression logits shaped like them; `gather_region_payload`
+# takes both; `_summarize_region_payload` turns them into region summaries in FP32 and
+# keeps both roundings, BF16 then FP8 E4M3; `indexer_score_tile` scores the
+# "E4M3-rounded BF16 region summaries [batch, regions, dim]"; `region_metadata` resets the
+# regions at every document boundary). Reading R17.
+# --------------------------------------------------------------------------------------
+
+# Natural-log constants as the float32 nearest to their exact values, and the Taylor
+# coefficients (ln 2)^k / k! of 2^f = e^(f ln 2), k = 0..7, each the float32 nearest to it.
+_LOG2E_F32 = np.float32(1.0 / math.log(2.0))
+_EXP2_TAYLOR_F32 = [np.float32(math.log(2.0) ** k / math.factorial(k)) for k in range(8)]
+
+
+def exp_f32(x: np.ndarray) -> np.ndarray:
+    """e^x for float32 x <= 0 in float32 arithmetic, every operation rounded to nearest
+    (reading R17). Cody and Waite's range reduction (Software Manual for the Elementary
+    Functions, 1980) to base 2: t = x * log2(e), n = rint(t) (ties to even), f = t - n
+    (exact, |f| <= 1/2); 2^f from its degree-7 Taylor polynomial in Horner form, no fused
+    multiply-add; the result p * 2^n (exact). For t < -125 the result is 0: e^x < 2^-125
+    there, and the scaled result stays a normal float32 otherwise."""
+    x = np.asarray(x, dtype=np.float32)
+    with np.errstate(over="ignore"):                  # x * log2(e) may round to -inf: flushed below
+        t = (x * _LOG2E_F32).astype(np.float32)
+    under = t < np.float32(-125.0)
+    t = np.where(under, np.float32(0.0), t).astype(np.float32)
+    n = np.rint(t).astype(np.float32)
+    f = (t - n).astype(np.float32)
+    p = np.full_like(f, _EXP2_TAYLOR_F32[7])
+    for k in range(6, -1, -1):
+        p = ((p * f).astype(np.float32) + _EXP2_TAYLOR_F32[k]).astype(np.float32)
+    y = np.ldexp(p, n.astype(np.int32)).astype(np.float32)
+    return np.where(under, np.float32(0.0), y).astype(np.float32)
+
+
+def summarize_doc(k_doc_bits: np.ndarray, z_doc_bits: np.ndarray, c: int) -> np.ndarray:
+    """FP32 learned-logit summaries of the complete runs of c tokens of one document
+    (reading R17): per region and dim d, the softmax over the region's tokens of the
+    compression logits z[., d] weights the keys k[., d].
+
+    m_d = max_j z[j,d]; e_j = exp_f32(z[j,d] - m_d) (the difference rounded to float32);
+    s_d and n_d are sequential float32 sums over j in token order of e_j and of
+    e_j * k[j,d] (the product rounded first); summary_d = n_d / s_d (one float32 division).
+    Returns float32 [floor(L/c), Di].
+    """
+    L, Di = k_doc_bits.shape
+    nb = L // c
+    k = bf16_to_f32(k_doc_bits)[: nb * c].reshape(nb, c, Di)
+    z = bf16_to_f32(z_doc_bits)[: nb * c].reshape(nb, c, Di)
+    m = z.max(axis=1)
+    s = np.zeros((nb, Di), dtype=np.float32)
+    num = np.zeros((nb, Di), dtype=np.float32)
+    for j in range(c):
+        e = exp_f32((z[:, j] - m).astype(np.float32))
+        s = (s + e).astype(np.float32)
+        num = (num + (e * k[:, j]).astype(np.float32)).astype(np.float32)
+    return (num / s).astype(np.float32)
+
+
+def region_summaries(kI_bits, z_bits, cu_seqlens, c: int) -> tuple[np.ndarray, np.ndarray]:
+    """Summaries of every document's regions, concatenated (float32, before rounding), and
+    the per-document region offsets. Regions start over at each document."""
+    T = kI_bits.shape[0]
+    starts, ends = doc_bounds(cu_seqlens, T)
+    parts, offs = [], [0]
+    for s, e in zip(starts, ends):
+        sm = summarize_doc(kI_bits[s:e], z_bits[s:e], c)
+        parts.append(sm)
+        offs.append(offs[-1] + sm.shape[0])
+    Di = kI_bits.shape[1]
+    out = np.concatenate(parts, axis=0) if parts else np.zeros((0, Di), np.float32)
+    return out, np.asarray(offs, dtype=np.int64)
+
+
+def region_summaries_e4m3(kI_bits, z_bits, cu_seqlens, c: int) -> tuple[np.ndarray, np.ndarray]:
+    """The summaries as the scorer sees them: FP32 -> bf16 -> E4M3 (float64 values)."""
+    sm, offs = region_summaries(kI_bits, z_bits, cu_seqlens, c)
+    return round_to_e4m3(round_to_bf16(sm).astype(np.float64)), offs
+
+
 def index_routes_grouped(qI_bits, kI_bits, w, cu_seqlens, c: int, budget: int, rows=None,
-                         operands: str = "bf16") -> np.ndarray:
+                         operands: str = "bf16", logits=None) -> np.ndarray:
     """Per-KV-group routes int32 [len(rows), G, budget + c - 1].
 
     qI_bits [T, G, Hi, Di], w [T, G, Hi] (signed allowed): the heads and weights of group g
@@ -418,7 +513,7 @@ def index_routes_grouped(qI_bits, kI_bits, w, cu_seqlens, c: int, budget: int, r
     """
     G = qI_bits.shape[1]
     return np.stack([index_routes(qI_bits[:, g], kI_bits, np.asarray(w)[:, g], cu_seqlens, c, budget, rows=rows,
-                                  operands=operands) for g in range(G)], axis=1)
+                                  operands=operands, logits=logits) for g in range(G)], axis=1)
 
 
 def attention_grouped(q_bits, k_bits, v_bits, routes_g, scale: float, rows=None):

@@ -864,6 +864,180 @@ def pin_window_compose(O):
     del rng
 
 
+def pin_exp_f32(O):
+    """exp_f32 against the library exponential: e^0 = 1 exactly; relative error within the
+    range reduction's rounding (|t| * 2^-24 twice, scaled by ln 2) plus 8 float32 ulps for the
+    polynomial; 0 where e^x < 2^-125 (the stated flush)."""
+    assert O.exp_f32(np.float32(0.0)) == np.float32(1.0)
+    x = np.concatenate([np.linspace(-86.0, 0.0, 40001), -np.geomspace(1e-7, 1.0, 2001)]).astype(np.float32)
+    got = O.exp_f32(x).astype(np.float64)
+    ref = np.asarray([math.exp(float(v)) for v in x])
+    t = np.abs(x.astype(np.float64)) / math.log(2.0)
+    bound = (2.0 * t * 2.0 ** -24 * math.log(2.0) + 8.0 * 2.0 ** -24) * ref
+    assert np.all(np.abs(got - ref) <= bound), float(np.max(np.abs(got - ref) / bound))
+    far = np.asarray([-88.0, -90.0, -200.0, -3.0e38], np.float32)
+    np.testing.assert_array_equal(O.exp_f32(far), np.zeros(4, np.float32))
+    assert math.exp(-87.0) < 2.0 ** -125
+
+
+def _regions_fixture(rng, lens, Di):
+    T = sum(lens)
+    cu = np.asarray([0] + list(np.cumsum(lens)), np.int32)
+    k = torch_bf16_bits(rng.standard_normal((T, Di)).astype(np.float32))
+    return T, cu, k
+
+
+def pin_summaries_uniform_logits(O):
+    """Logits equal across a region's tokens give equal softmax weights: the summary is the
+    mean of the region's keys (exact rational mean, one rounding; keys on a 2^-4 grid so that
+    every FP32 partial sum is exact), then torch's bf16 and E4M3 casts. The pair
+    (1.0625, 1.0703125) averages to a bf16 tie that rounds down onto an E4M3 tie: rounding
+    twice gives 1.0 where one rounding would give 1.125."""
+    rng = np.random.default_rng(40)
+    lens, Di = [9, 6, 11], 5
+    T = sum(lens)
+    cu = np.asarray([0] + list(np.cumsum(lens)), np.int32)
+    kv = (np.round(rng.uniform(-6, 6, (T, Di)) * 16) / 16).astype(np.float32)
+    kv[0, 0], kv[1, 0] = 1.0625, 1.0703125
+    k = exact_bf16_bits(kv)
+    for c in (2, 3, 4):
+        zr = rng.standard_normal((T // c + len(lens), Di)).astype(np.float32)
+        z = np.zeros((T, Di), np.float32)
+        starts = [int(v) for v in cu[:-1]]
+        ridx = 0
+        for s, L in zip(starts, lens):
+            for b in range(L // c):
+                z[s + b * c: s + b * c + c] = zr[ridx]
+                ridx += 1
+            z[s + (L // c) * c: s + L] = rng.standard_normal((L % c, Di))   # tails take no part
+        sm, offs = O.region_summaries(k, torch_bf16_bits(z), cu, c)
+        assert offs.tolist() == [0] + list(np.cumsum([L // c for L in lens]))
+        want = []
+        for s, L in zip(starts, lens):
+            for b in range(L // c):
+                want.append([np.float32(sum(Fraction(float(kv[s + b * c + j, i])) for j in range(c)) / c)
+                             for i in range(Di)])
+        want = np.asarray(want, np.float32)
+        np.testing.assert_array_equal(sm, want)
+        q, _ = O.region_summaries_e4m3(k, torch_bf16_bits(z), cu, c)
+        np.testing.assert_array_equal(q, torch_e4m3(bits_to_f64(torch_bf16_bits(want))))
+        if c == 2:
+            assert q[0, 0] == 1.0
+
+
+def pin_summaries_one_hot_logits(O):
+    """One token per (region, dim) has logit 0 and the others -200: its softmax weight is 1
+    and the others' e^-200 flush to 0, so the summary is that token's key in that dim,
+    exactly; E4M3 rounding as torch's cast."""
+    rng = np.random.default_rng(41)
+    lens, Di, c = [13, 10], 7, 4
+    T, cu, k = _regions_fixture(rng, lens, Di)
+    kf = bits_to_f64(k)
+    z = np.full((T, Di), -200.0, np.float32)
+    want = []
+    for s, L in zip(cu[:-1], lens):
+        for b in range(L // c):
+            pick = rng.integers(0, c, Di)
+            z[s + b * c + pick, np.arange(Di)] = 0.0
+            want.append(kf[s + b * c + pick, np.arange(Di)])
+    sm, _ = O.region_summaries(k, exact_bf16_bits(z), cu, c)
+    np.testing.assert_array_equal(sm.astype(np.float64), np.asarray(want))
+    q, _ = O.region_summaries_e4m3(k, exact_bf16_bits(z), cu, c)
+    np.testing.assert_array_equal(q, torch_e4m3(np.asarray(want, np.float32)))
+
+
+def pin_summaries_softmax_fp64(O):
+    """Random logits against the softmax-weighted sum in float64 (library exp): agreement
+    within the FP32 evaluation's error, |x| * 2^-22 relative for the weights plus c + 2 ulps
+    of the sums; tokens of a document's last incomplete region change nothing."""
+    rng = np.random.default_rng(42)
+    lens, Di = [11, 5, 14], 6
+    T, cu, k = _regions_fixture(rng, lens, Di)
+    kf = bits_to_f64(k)
+    z = torch_bf16_bits((rng.standard_normal((T, Di)) * 3).astype(np.float32))
+    zf = bits_to_f64(z)
+    for c in (2, 5):
+        sm, offs = O.region_summaries(k, z, cu, c)
+        r = 0
+        for s, L in zip(cu[:-1], lens):
+            for b in range(L // c):
+                zz = zf[s + b * c: s + b * c + c]
+                kk = kf[s + b * c: s + b * c + c]
+                x = zz - zz.max(axis=0)
+                p = np.exp(x) / np.exp(x).sum(axis=0)
+                ref = (p * kk).sum(axis=0)
+                mag = (p * np.abs(kk)).sum(axis=0)
+                tol = mag * (np.abs(x).max(axis=0) * 2.0 ** -22 + (c + 2) * 2.0 ** -23) + 1e-30
+                assert np.all(np.abs(sm[r].astype(np.float64) - ref) <= tol), (c, r)
+                r += 1
+        assert r == sm.shape[0]
+        # the incomplete tail of every document takes no part
+        k2, z2 = k.copy(), z.copy()
+        for s, L in zip(cu[:-1], lens):
+            tail = slice(int(s) + (L // c) * c, int(s) + L)
+            k2[tail] ^= np.uint16(0x1234)
+            z2[tail] ^= np.uint16(0x0101)
+        np.testing.assert_array_equal(O.region_summaries(k2, z2, cu, c)[0], sm)
+
+
+def pin_summaries_two_tokens(O):
+    """c = 2 with logits (0, -a): the summary is (k0 + e^-a k1) / (1 + e^-a)."""
+    rng = np.random.default_rng(43)
+    T, Di, c = 16, 8, 2
+    cu = np.asarray([0, T], np.int32)
+    k = torch_bf16_bits(rng.standard_normal((T, Di)).astype(np.float32))
+    kf = bits_to_f64(k)
+    a = bits_to_f64(torch_bf16_bits(rng.uniform(0.0, 4.0, (T // 2, Di)).astype(np.float32)))
+    z = np.zeros((T, Di), np.float32)
+    z[1::2] = -a
+    sm, _ = O.region_summaries(k, exact_bf16_bits(z), cu, c)
+    e = np.exp(-a)
+    ref = (kf[0::2] + e * kf[1::2]) / (1.0 + e)
+    tol = (np.abs(kf[0::2]) + np.abs(kf[1::2])) * 2.0 ** -20
+    assert np.all(np.abs(sm.astype(np.float64) - ref) <= tol)
+
+
+def pin_summary_scores(O):
+    """One-hot queries read dim d of the summaries; one-hot logits make the summary of block
+    b in dim d the key of one chosen token: each score is then sum_h w_h ReLU(b_h e4m3(k)) with
+    torch's casts, rounded once to FP32 (bf16 queries; E4M3 queries round b_h too)."""
+    rng = np.random.default_rng(44)
+    lens, Hi, Di, c, budget = [14, 18], 2, 8, 2, 2
+    T, cu, k = _regions_fixture(rng, lens, Di)
+    kf = bits_to_f64(k)
+    z = np.full((T, Di), -200.0, np.float32)
+    pick = rng.integers(0, c, (T // c + 2, Di))
+    chosen = {}
+    r = 0
+    for s, L in zip(cu[:-1], lens):
+        for b in range(L // c):
+            z[s + b * c + pick[r], np.arange(Di)] = 0.0
+            chosen[(int(s), b)] = kf[s + b * c + pick[r], np.arange(Di)]
+            r += 1
+    bvals = np.asarray([0.71875, -1.3125], np.float32)
+    qv = np.zeros((T, Hi, Di), np.float32)
+    dims = rng.integers(0, Di, (T, Hi))
+    for t in range(T):
+        for h in range(Hi):
+            qv[t, h, dims[t, h]] = bvals[h]
+    qI = exact_bf16_bits(qv)
+    w = rng.standard_normal((T, Hi)).astype(np.float32)
+    for operands in ("bf16", "e4m3"):
+        bq = torch_e4m3(bvals) if operands == "e4m3" else bvals.astype(np.float64)
+        _, sc = O.index_routes(qI, k, w, cu, c, budget, want_scores=True, operands=operands,
+                               logits=exact_bf16_bits(z))
+        for t in range(T):
+            d = int(np.searchsorted(cu, t, side="right") - 1)
+            s = int(cu[d])
+            nv = (t - s + 1) // c
+            if nv <= budget // c:
+                continue
+            for b in range(nv):
+                kk = torch_e4m3(chosen[(s, b)].astype(np.float32))
+                want = np.float32(sum(float(w[t, h]) * max(bq[h] * kk[dims[t, h]], 0.0) for h in range(Hi)))
+                assert sc[t, b] == want, (operands, t, b)
+
+
 ALL_PINS = [
     pin_golden_two_docs,
     pin_golden_head_weights,
@@ -894,4 +1068,10 @@ ALL_PINS = [
     pin_e4m3_scores,
     pin_grouped_routes,
     pin_grouped_attention,
+    pin_exp_f32,
+    pin_summaries_uniform_logits,
+    pin_summaries_one_hot_logits,
+    pin_summaries_softmax_fp64,
+    pin_summaries_two_tokens,
+    pin_summary_scores,
 ]

@@ -248,6 +248,53 @@ def _grouped_attention_group0(q_bits, k_bits, v_bits, routes_g, scale, rows=None
                               rows)
 
 
+def _exp_variant(coef3_div=6, log2e=True):
+    def ex(x):
+        x = np.asarray(x, dtype=np.float32)
+        with np.errstate(over="ignore"):
+            t = (x * np.float32(1.0 / math.log(2.0) if log2e else math.log(2.0))).astype(np.float32)
+        under = t < -125
+        t = np.where(under, np.float32(0.0), t).astype(np.float32)
+        n = np.rint(t).astype(np.float32)
+        f = (t - n).astype(np.float32)
+        cf = [np.float32(math.log(2.0) ** k / math.factorial(k)) for k in range(8)]
+        cf[3] = np.float32(math.log(2.0) ** 3 / coef3_div)
+        p = np.full_like(f, cf[7])
+        for k in range(6, -1, -1):
+            p = ((p * f).astype(np.float32) + cf[k]).astype(np.float32)
+        return np.where(under, np.float32(0.0), np.ldexp(p, n.astype(np.int32))).astype(np.float32)
+    return ex
+
+
+def _summary_variant(weights="softmax", normalise=True, sign=1.0):
+    def summ(k_doc_bits, z_doc_bits, c):
+        L, Di = k_doc_bits.shape
+        nb = L // c
+        k = O.bf16_to_f32(k_doc_bits)[: nb * c].reshape(nb, c, Di).astype(np.float64)
+        z = sign * O.bf16_to_f32(z_doc_bits)[: nb * c].reshape(nb, c, Di).astype(np.float64)
+        if weights == "mean":
+            e = np.ones_like(z)
+        elif weights == "over_dims":
+            e = np.exp(z - z.max(axis=2, keepdims=True))
+            e = e / e.sum(axis=2, keepdims=True) * e.sum(axis=1, keepdims=True)
+        else:
+            e = np.exp(z - z.max(axis=1, keepdims=True))
+        num = (e * k).sum(axis=1)
+        return (num / e.sum(axis=1) if normalise else num).astype(np.float32)
+    return summ
+
+
+def _summaries_ignore_docs(kI_bits, z_bits, cu_seqlens, c):
+    sm = O.summarize_doc(kI_bits, z_bits, c)
+    offs = [0] + [int(v) // c for v in np.asarray(cu_seqlens, np.int64)[1:]]
+    return sm, np.asarray(offs, np.int64)
+
+
+def _summaries_one_rounding(kI_bits, z_bits, cu_seqlens, c):
+    sm, offs = O.region_summaries(kI_bits, z_bits, cu_seqlens, c)
+    return O.round_to_e4m3(sm.astype(np.float64)), offs
+
+
 _REAL_ATTEND = O.attend_row
 _REAL_GROUPED_ATTN = O.attention_grouped
 _REAL_COMPOSE = O.compose_window
@@ -294,6 +341,14 @@ MUTATIONS = {
     "grouped_routes_shared_weights": ("index_routes_grouped", _grouped_routes_shared_weights),
     "grouped_routes_first_group_only": ("index_routes_grouped", _grouped_routes_first_group),
     "grouped_attention_first_group_routes": ("attention_grouped", _grouped_attention_group0),
+    "exp_wrong_cubic_term": ("exp_f32", _exp_variant(coef3_div=3)),
+    "exp_ln2_for_log2e": ("exp_f32", _exp_variant(log2e=False)),
+    "summary_mean_weights": ("summarize_doc", _summary_variant(weights="mean")),
+    "summary_softmax_over_dims": ("summarize_doc", _summary_variant(weights="over_dims")),
+    "summary_unnormalised": ("summarize_doc", _summary_variant(normalise=False)),
+    "summary_negated_logits": ("summarize_doc", _summary_variant(sign=-1.0)),
+    "summaries_ignore_documents": ("region_summaries", _summaries_ignore_docs),
+    "summaries_one_rounding": ("region_summaries_e4m3", _summaries_one_rounding),
 }
 
 
