@@ -205,6 +205,59 @@ irs_status irs_sparse_index_score_topk_e4m3(const void* qI, const void* kI, cons
                                             size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream);
 
 /*
+ * Step-5 learned-logit region summaries.
+ *
+ * Step-5 sparse page: `Step5SparseIndexer.project_keys` returns the index keys and
+ * per-dimension compression logits shaped like them; `_summarize_region_payload` turns
+ * them into region summaries in FP32 and keeps both roundings (bf16, then FP8 E4M3);
+ * `indexer_score_tile` scores E4M3-rounded bf16 region summaries; `region_metadata` resets
+ * the regions at every document boundary. A region is a run of c consecutive tokens of
+ * one document (as the pooled blocks of irs_sparse_index_score_topk). Per region and dim d:
+ *   m_d = max_j z[j, d]
+ *   e_j = exp(z[j, d] - m_d)
+ *   summary_d = e4m3(bf16((sum_j e_j k[j, d]) / (sum_j e_j)))
+ * The sums run over the region's tokens in order, in FP32, without fused multiply-add.
+ * exp is evaluated in FP32 as follows, each operation rounded to nearest:
+ *   t = x * log2(e),  n = rint(t),  f = t - n;
+ *   2^f by its degree-7 Taylor polynomial in Horner form;
+ *   the result times 2^n, and 0 where t < -125.
+ * E4M3 rounding is to nearest, ties to even, saturating at +-448.
+ *
+ * irs_region_summaries writes the summaries alone:
+ *   kI, z      bf16 [T, Di] contiguous (keys and compression logits), 16-byte aligned
+ *   out        bf16 [floor(T/c), Di]: row blk_off[d] + b is region b of document d (blk_off
+ *              the running count of floor(len/c) over documents); rows past the last region
+ *              are zeroed
+ *   workspace  irs_region_summaries_workspace_bytes(T, Di, c, ndocs, max_doc_len) bytes,
+ *              256-byte aligned
+ *   Di 64 or 128; other arguments as for irs_sparse_index_score_topk.
+ *
+ * irs_sparse_index_score_topk_summaries is the per-group indexer of
+ * irs_sparse_index_score_topk_grouped with these summaries as the block keys instead of
+ * the means:
+ *   - e4m3_queries = 0: bf16 queries, Di 64 or 128;
+ *   - e4m3_queries = 1: queries rounded bf16 -> E4M3 and the scores on the kind::f8f6f4
+ *     path, as in irs_sparse_index_score_topk_e4m3; Di must be 128.
+ * qI [T, G, Hi, Di], w [T, G, Hi], route_ids [T, G, budget + c - 1] and scores_dbg as in
+ * irs_sparse_index_score_topk_grouped (G = 1 is the ungrouped indexer). The workspace is
+ * irs_index_summaries_workspace_bytes(...) bytes.
+ * Errors: IRS_ERR_VALUE for NULL or unaligned pointers and unsupported sizes, before any
+ * work is queued; IRS_ERR_RUNTIME when a launch fails.
+ */
+size_t irs_region_summaries_workspace_bytes(int T, int Di, int c, int ndocs, int max_doc_len);
+irs_status irs_region_summaries(const void* kI, const void* z, const int32_t* cu_seqlens, int ndocs, int max_doc_len,
+                                int T, int Di, int c, void* out, void* workspace, size_t workspace_bytes,
+                                int32_t* err_flag, irs_stream_t stream);
+size_t irs_index_summaries_workspace_bytes(int T, int G, int Hi, int Di, int c, int budget, int ndocs,
+                                           int max_doc_len, int e4m3_queries, int with_score_buffer);
+irs_status irs_sparse_index_score_topk_summaries(const void* qI, const void* kI, const void* z, const float* w,
+                                                 const int32_t* cu_seqlens, int ndocs, int max_doc_len, int T, int G,
+                                                 int Hi, int Di, int c, int budget, int e4m3_queries,
+                                                 int32_t* route_ids, float* scores_dbg, int64_t ld_scores,
+                                                 void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                                 irs_stream_t stream);
+
+/*
  * irs_sparse_index_score_topk without a workspace: the same computation and arguments,
  * minus `workspace` / `workspace_bytes`. The reference pages have no counterpart; this
  * entry point exists for callers that cannot allocate device memory for the library,

@@ -8,6 +8,9 @@ this package is its thin Python binding. Names follow the C entry points:
 * ``sparse_gqa_attn_bwd(q, k, v, route_ids, out, lse, dout, scale) -> (dq, dk, dv)``
 * ``topk_from_scores(scores, cu_seqlens, c, budget) -> route_ids``
 * ``compose_window_routes(route_ids, cu_seqlens, window) -> route_ids``
+* ``sparse_index_score_topk_grouped`` / ``sparse_gqa_attn_fwd_grouped``: per-KV-group routes
+* ``region_summaries(kI, z, cu_seqlens, c)`` and ``sparse_index_score_topk_summaries``:
+  Step-5 learned-logit region summaries and the indexer that scores them
 """
 from ._binding import (  # noqa: F401
     DEVERR_CU_SEQLENS,
@@ -23,10 +26,12 @@ from ._binding import (  # noqa: F401
     index_workspace_bytes,
     lib,
     read_device_errors,
+    region_summaries,
     sparse_gqa_attn_bwd,
     sparse_gqa_attn_fwd,
     sparse_gqa_attn_fwd_grouped,
     sparse_index_score_topk,
     sparse_index_score_topk_grouped,
+    sparse_index_score_topk_summaries,
     topk_from_scores,
 )

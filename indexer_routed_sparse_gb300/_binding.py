@@ -48,6 +48,11 @@ _SIGNATURES = {
     "irs_index_e4m3_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "irs_sparse_index_score_topk_e4m3": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I64, _P, _SZ, _P,
                                               _P]),
+    "irs_region_summaries_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "irs_region_summaries": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
+    "irs_index_summaries_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I]),
+    "irs_sparse_index_score_topk_summaries": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P,
+                                                   _I64, _P, _SZ, _P, _P]),
     "irs_topk_from_scores": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "irs_compose_window_routes": (_I, [_P, _I, _P, _I, _I, _I, _P, _P, _P]),
     "irs_sparse_gqa_attn_fwd": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I, _I, _I, _I, _I, _I,
@@ -488,6 +493,104 @@ def sparse_index_score_topk_grouped(qI: torch.Tensor, kI: torch.Tensor, w: torch
         _ptr(qI), _ptr(kI), _ptr(w), _ptr(cu_seqlens), ndocs, max_doc_len, T, G, Hi, Di, c, budget, _ptr(out),
         _ptr(scores_out), ld, _ptr(ws), ws.numel(), _ptr(err), _stream(dev))
     _check(st, "sparse_index_score_topk_grouped")
+    return out
+
+
+def region_summaries(kI: torch.Tensor, z: torch.Tensor, cu_seqlens: torch.Tensor, c: int, *,
+                     ndocs: int | None = None, max_doc_len: int | None = None, out: torch.Tensor | None = None,
+                     err: torch.Tensor | None = None) -> torch.Tensor:
+    """Step-5 learned-logit region summaries, bf16 [T // c, Di] holding E4M3 values.
+
+    kI and z (the compression logits) bf16 [T, Di]. Row blk_off[d] + b is region b of
+    document d; rows past the last region are zero.
+    """
+    _need(kI, "kI", torch.bfloat16, 2)
+    _need(z, "z", torch.bfloat16, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, Di = kI.shape
+    if tuple(z.shape) != (T, Di) or not (kI.is_contiguous() and z.is_contiguous() and cu_seqlens.is_contiguous()):
+        raise ValueError("kI and z must be contiguous bf16 [T, Di] of one shape")
+    ndocs, max_doc_len = _doc_stats(cu_seqlens, ndocs, max_doc_len, T)
+    dev = kI.device
+    rows = max(T // c, 1)
+    if out is None:
+        out = torch.empty((rows, Di), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, 2)
+    if tuple(out.shape) != (rows, Di) or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous bf16 [{rows}, {Di}]")
+    nbytes = int(lib().irs_region_summaries_workspace_bytes(T, Di, c, ndocs, max_doc_len))
+    if nbytes == 0:
+        _check(IRS_ERR_VALUE, "region_summaries")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    if err is None:
+        err = device_error_flag(dev)
+    st = lib().irs_region_summaries(_ptr(kI), _ptr(z), _ptr(cu_seqlens), ndocs, max_doc_len, T, Di, c, _ptr(out),
+                                    _ptr(ws), ws.numel(), _ptr(err), _stream(dev))
+    _check(st, "region_summaries")
+    return out
+
+
+def sparse_index_score_topk_summaries(qI: torch.Tensor, kI: torch.Tensor, z: torch.Tensor, w: torch.Tensor,
+                                      cu_seqlens: torch.Tensor, c: int, budget: int, *, operands: str = "e4m3",
+                                      ndocs: int | None = None, max_doc_len: int | None = None,
+                                      scores_out: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                                      workspace: torch.Tensor | None = None,
+                                      err: torch.Tensor | None = None) -> torch.Tensor:
+    """Step-5 indexer: routes scored against the learned-logit region summaries of kI under
+    the compression logits z, per KV group.
+
+    qI bf16 [T, G, Hi, Di] (or [T, Hi, Di] for one group), kI and z bf16 [T, Di], w fp32
+    [T, G, Hi] (or [T, Hi]). operands "e4m3" rounds the queries to E4M3 too (Di 128),
+    "bf16" keeps them. Returns int32 [T, G, budget + c - 1] ([T, budget + c - 1] for 3-D qI);
+    scores_out fp32 [T, G, ld] (or [T, ld]).
+    """
+    if operands not in ("bf16", "e4m3"):
+        raise ValueError("operands must be 'bf16' or 'e4m3'")
+    _need(qI, "qI", torch.bfloat16)
+    _need(kI, "kI", torch.bfloat16)
+    _need(z, "z", torch.bfloat16)
+    _need(w, "w", torch.float32)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    flat = qI.dim() == 3
+    q4 = qI.unsqueeze(1) if flat else qI
+    w3 = w.unsqueeze(1) if flat else w
+    if q4.dim() != 4:
+        raise ValueError("qI must be [T, Hi, Di] or [T, G, Hi, Di]")
+    T, G, Hi, Di = q4.shape
+    if kI.dim() == 3:
+        kI = kI.reshape(kI.shape[0], kI.shape[2])
+    if z.dim() == 3:
+        z = z.reshape(z.shape[0], z.shape[2])
+    if tuple(kI.shape) != (T, Di) or tuple(z.shape) != (T, Di) or tuple(w3.shape) != (T, G, Hi):
+        raise ValueError(f"shape mismatch: qI {tuple(qI.shape)}, kI {tuple(kI.shape)}, z {tuple(z.shape)}, "
+                         f"w {tuple(w.shape)}")
+    if not all(t.is_contiguous() for t in (q4, kI, z, w3, cu_seqlens)):
+        raise ValueError("qI, kI, z, w and cu_seqlens must be contiguous")
+    ndocs, max_doc_len = _doc_stats(cu_seqlens, ndocs, max_doc_len, T)
+    dev = qI.device
+    W = budget + c - 1
+    if out is None:
+        out = torch.empty((T, W) if flat else (T, G, W), dtype=torch.int32, device=dev)
+    ld = 0
+    if scores_out is not None:
+        _need(scores_out, "scores_out", torch.float32)
+        s3 = scores_out.unsqueeze(1) if flat else scores_out
+        if s3.dim() != 3 or tuple(s3.shape[:2]) != (T, G) or not s3.is_contiguous():
+            raise ValueError("scores_out must be a contiguous fp32 [T, G, ld] ([T, ld] for one group)")
+        ld = s3.shape[2]
+    e4 = int(operands == "e4m3")
+    nbytes = int(lib().irs_index_summaries_workspace_bytes(T, G, Hi, Di, c, budget, ndocs, max_doc_len, e4,
+                                                            int(scores_out is None)))
+    if nbytes == 0:
+        _check(IRS_ERR_VALUE, "sparse_index_score_topk_summaries")
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    if err is None:
+        err = device_error_flag(dev)
+    st = lib().irs_sparse_index_score_topk_summaries(
+        _ptr(q4), _ptr(kI), _ptr(z), _ptr(w3), _ptr(cu_seqlens), ndocs, max_doc_len, T, G, Hi, Di, c, budget, e4,
+        _ptr(out), _ptr(scores_out), ld, _ptr(workspace), workspace.numel(), _ptr(err), _stream(dev))
+    _check(st, "sparse_index_score_topk_summaries")
     return out
 
 

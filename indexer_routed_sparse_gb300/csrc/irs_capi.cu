@@ -126,14 +126,15 @@ irs_status make_query_tiles_map(CUtensorMap* m, const void* base, uint64_t Di, u
 }
 
 // Byte maps for E4M3 operands (128-byte SW128 rows of 128 elements): the queries as
-// [T][Hi][Di] with box {128, Hi, 256/Hi}, the pooled keys as [rows][Di] with box {128, 128}.
+// [T][rows_per_token][Di] with box {128, Hi, 256/Hi} (rows_per_token = G*Hi), the pooled keys
+// as [krows][Di] with box {128, 128}.
 irs_status make_e4m3_maps(CUtensorMap* tq, CUtensorMap* tk, const void* q8, const void* k8, uint64_t Di, uint64_t Hi,
-                          uint64_t T, uint64_t krows) {
+                          uint64_t rows_per_token, uint64_t T, uint64_t krows) {
   auto fn = encode_fn();
   if (fn == nullptr) return fail(IRS_ERR_RUNTIME, "cuTensorMapEncodeTiled is unavailable");
   {
-    cuuint64_t dims[3] = {Di, Hi, T};
-    cuuint64_t strides[2] = {Di, Hi * Di};
+    cuuint64_t dims[3] = {Di, rows_per_token, T};
+    cuuint64_t strides[2] = {Di, rows_per_token * Di};
     cuuint32_t box[3] = {128, (cuuint32_t)Hi, (cuuint32_t)(256 / Hi)};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = fn(tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q8), dims, strides, box, es,
@@ -223,11 +224,12 @@ irs_status index_impl(const void* qI, const void* kI, const float* w, const int3
                       int max_doc_len, int T, int Hi, int Di, int c, int budget, const irs::FrontHalf* front,
                       int32_t* route_ids, float* scores_dbg, int64_t ld_scores, void* workspace,
                       size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream, int G = 1,
-                      bool e4m3 = false) {
+                      bool e4m3 = false, const void* z = nullptr) {
   irs_status s = check_index_sizes(T, Hi, Di, c, budget, ndocs, max_doc_len);
   if (s != IRS_OK) return s;
-  if (e4m3 && (Di != 128 || G != 1 || front != nullptr))
-    return fail(IRS_ERR_VALUE, "E4M3 scoring needs Di = 128 (one group, no front half)");
+  if (e4m3 && (Di != 128 || front != nullptr))
+    return fail(IRS_ERR_VALUE, "E4M3 scoring needs Di = 128 (no front half)");
+  if (z != nullptr && !aligned16(z)) return fail(IRS_ERR_VALUE, "the compression logits must be 16-byte aligned");
   if (G < 1 || (long long)T * G * Hi >= (1LL << 31)) return fail(IRS_ERR_VALUE, "bad group count %d", G);
   if (!qI || !kI || !w || !cu_seqlens || !route_ids || !workspace)
     return fail(IRS_ERR_VALUE, "NULL tensor pointer");
@@ -235,7 +237,7 @@ irs_status index_impl(const void* qI, const void* kI, const float* w, const int3
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(IRS_ERR_VALUE, "workspace must be 256-byte aligned");
   const irs::IndexPlan p =
-      irs::plan_index(T, Hi, Di, c, budget, ndocs, max_doc_len, scores_dbg == nullptr, front != nullptr, e4m3);
+      irs::plan_index(T, Hi, Di, c, budget, ndocs, max_doc_len, scores_dbg == nullptr, front != nullptr, e4m3, G);
   if (scores_dbg != nullptr && ld_scores < p.ldS)
     return fail(IRS_ERR_VALUE, "ld_scores must be >= max_doc_len / c (%lld)", (long long)p.ldS);
   if (workspace_bytes < p.ws_bytes)
@@ -253,8 +255,8 @@ irs_status index_impl(const void* qI, const void* kI, const float* w, const int3
   // with the front half the scores read the transformed queries from the workspace
   const void* qsrc = front != nullptr ? static_cast<const void*>(ws + p.off_qfront) : qI;
   if (e4m3) {
-    if ((s = make_e4m3_maps(&tm_q, &tm_k, ws + p.off_q8, ws + p.off_k8, (uint64_t)Di, (uint64_t)Hi, (uint64_t)T,
-                            (uint64_t)p.nblk_cap)) != IRS_OK)
+    if ((s = make_e4m3_maps(&tm_q, &tm_k, ws + p.off_q8, ws + p.off_k8, (uint64_t)Di, (uint64_t)Hi,
+                            (uint64_t)G * Hi, (uint64_t)T, (uint64_t)p.nblk_cap)) != IRS_OK)
       return s;
   } else {
     if ((s = make_query_tiles_map(&tm_q, qsrc, (uint64_t)Di, (uint64_t)G * Hi, (uint64_t)T, (uint32_t)Hi)) != IRS_OK)
@@ -265,7 +267,7 @@ irs_status index_impl(const void* qI, const void* kI, const float* w, const int3
                                          static_cast<const __nv_bfloat16*>(kI), w, cu_seqlens, ndocs, max_doc_len, T,
                                          Hi, Di, c, budget, route_ids, scores, ldS, ws, err_flag, tm_q, tm_k,
                                          dev->num_sms, reinterpret_cast<cudaStream_t>(stream), front, G,
-                                         group_stride, e4m3),
+                                         group_stride, e4m3, static_cast<const __nv_bfloat16*>(z)),
                        "launching the indexer");
 }
 
@@ -321,6 +323,53 @@ irs_status irs_sparse_index_score_topk_e4m3(const void* qI, const void* kI, cons
                                             size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream) {
   return index_impl(qI, kI, w, cu_seqlens, ndocs, max_doc_len, T, Hi, Di, c, budget, nullptr, route_ids, scores_dbg,
                     ld_scores, workspace, workspace_bytes, err_flag, stream, 1, true);
+}
+
+size_t irs_index_summaries_workspace_bytes(int T, int G, int Hi, int Di, int c, int budget, int ndocs,
+                                           int max_doc_len, int e4m3_queries, int with_score_buffer) {
+  if (check_index_sizes(T, Hi, Di, c, budget, ndocs, max_doc_len) != IRS_OK || G < 1) return 0;
+  if (e4m3_queries != 0 && Di != 128) return 0;
+  return irs::plan_index(T, Hi, Di, c, budget, ndocs, max_doc_len, with_score_buffer != 0, false, e4m3_queries != 0,
+                         G)
+      .ws_bytes;
+}
+
+irs_status irs_sparse_index_score_topk_summaries(const void* qI, const void* kI, const void* z, const float* w,
+                                                 const int32_t* cu_seqlens, int ndocs, int max_doc_len, int T, int G,
+                                                 int Hi, int Di, int c, int budget, int e4m3_queries,
+                                                 int32_t* route_ids, float* scores_dbg, int64_t ld_scores,
+                                                 void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                                 irs_stream_t stream) {
+  if (z == nullptr) return fail(IRS_ERR_VALUE, "NULL compression logits");
+  return index_impl(qI, kI, w, cu_seqlens, ndocs, max_doc_len, T, Hi, Di, c, budget, nullptr, route_ids, scores_dbg,
+                    ld_scores, workspace, workspace_bytes, err_flag, stream, G, e4m3_queries != 0, z);
+}
+
+size_t irs_region_summaries_workspace_bytes(int T, int Di, int c, int ndocs, int max_doc_len) {
+  if (check_index_sizes(T, 1, Di, c, c, ndocs, max_doc_len) != IRS_OK) return 0;
+  return irs::plan_index(T, 1, Di, c, c, ndocs, max_doc_len, false).ws_bytes;
+}
+
+irs_status irs_region_summaries(const void* kI, const void* z, const int32_t* cu_seqlens, int ndocs, int max_doc_len,
+                                int T, int Di, int c, void* out, void* workspace, size_t workspace_bytes,
+                                int32_t* err_flag, irs_stream_t stream) {
+  irs_status s = check_index_sizes(T, 1, Di, c, c, ndocs, max_doc_len);
+  if (s != IRS_OK) return s;
+  if (!kI || !z || !cu_seqlens || !out || !workspace) return fail(IRS_ERR_VALUE, "NULL tensor pointer");
+  if (!aligned16(kI) || !aligned16(z) || !aligned16(out))
+    return fail(IRS_ERR_VALUE, "kI, z and out must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(IRS_ERR_VALUE, "workspace must be 256-byte aligned");
+  const irs::IndexPlan p = irs::plan_index(T, 1, Di, c, c, ndocs, max_doc_len, false);
+  if (workspace_bytes < p.ws_bytes)
+    return fail(IRS_ERR_VALUE, "workspace too small: %zu < %zu bytes", workspace_bytes, p.ws_bytes);
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != IRS_OK) return s;
+  return launch_status(irs::launch_summaries(p, static_cast<const __nv_bfloat16*>(kI),
+                                             static_cast<const __nv_bfloat16*>(z), cu_seqlens, ndocs, max_doc_len, T,
+                                             Di, c, static_cast<uint8_t*>(workspace), err_flag,
+                                             static_cast<__nv_bfloat16*>(out), reinterpret_cast<cudaStream_t>(stream)),
+                       "launching the region summaries");
 }
 
 irs_status irs_index_front_operands(const void* qI, const void* kI, const int32_t* cu_seqlens, int ndocs,

@@ -180,6 +180,93 @@ __global__ void __launch_bounds__(256) quantize_e4m3_kernel(const __nv_bfloat16*
 }
 
 // =====================================================================================
+// Step-5 learned-logit region summaries (Step-5 sparse page: `project_keys` gives per-dim
+// compression logits shaped like the keys; `_summarize_region_payload` makes the region
+// summaries in FP32 and keeps the bf16 and E4M3 roundings; regions reset at document
+// boundaries). Per region and dim, the softmax of the logits over the region's c tokens
+// weights the keys: m = max_j z_j, e_j = exp(z_j - m), summary = (sum_j e_j k_j) / (sum_j e_j)
+// with both sums sequential in token order, then bf16, then E4M3.
+// =====================================================================================
+
+// e^x for x <= 0, evaluated in FP32 with every operation rounded to nearest and no fused
+// multiply-add, so that its value is a fixed function of x: Cody and Waite's reduction to
+// base 2 (t = x log2(e), n = rint(t), f = t - n, exact), 2^f from its degree-7 Taylor
+// polynomial (coefficients (ln 2)^k / k! rounded to FP32) in Horner form, times 2^n (exact,
+// the result stays normal). Where t < -125 the value is 0.
+__device__ __forceinline__ float exp_stated(float x) {
+  const float t = __fmul_rn(x, 0x1.715476p+0f);
+  if (t < -125.f) return 0.f;
+  const float n = rintf(t);
+  const float f = __fsub_rn(t, n);
+  float p = 0x1.ffcbfcp-17f;
+  p = __fadd_rn(__fmul_rn(p, f), 0x1.430912p-13f);
+  p = __fadd_rn(__fmul_rn(p, f), 0x1.5d87fep-10f);
+  p = __fadd_rn(__fmul_rn(p, f), 0x1.3b2ab6p-7f);
+  p = __fadd_rn(__fmul_rn(p, f), 0x1.c6b08ep-5f);
+  p = __fadd_rn(__fmul_rn(p, f), 0x1.ebfbe0p-3f);
+  p = __fadd_rn(__fmul_rn(p, f), 0x1.62e430p-1f);
+  p = __fadd_rn(__fmul_rn(p, f), 1.0f);
+  return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
+}
+
+// Thread = (region, pair of dims): pass 1 takes the logits' max, pass 2 the two sums.
+// Output: E4M3 bytes into kbar8, or (kbar8 == nullptr) the E4M3 values as bf16 into kbar.
+// Rows from the region count up to nblk_cap are zeroed.
+__global__ void __launch_bounds__(256) summary_kernel(const __nv_bfloat16* __restrict__ kI,
+                                                      const __nv_bfloat16* __restrict__ z,
+                                                      const int32_t* __restrict__ cu, int ndocs, int Di, int c,
+                                                      int nblk_cap, const int32_t* __restrict__ meta,
+                                                      const int32_t* __restrict__ blk_off,
+                                                      __nv_bfloat16* __restrict__ kbar, uint8_t* __restrict__ kbar8) {
+  if (meta[0] != 1) return;
+  const int nblk = meta[1];
+  const int pairs = Di >> 1;
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int gb = (int)(gid / pairs);
+  const int pr = (int)(gid % pairs);
+  if (gb >= nblk_cap) return;
+  if (gb >= nblk) {
+    if (kbar8 != nullptr) reinterpret_cast<uint16_t*>(kbar8 + (long long)gb * Di)[pr] = 0;
+    else reinterpret_cast<uint32_t*>(kbar + (long long)gb * Di)[pr] = 0u;
+    return;
+  }
+  const int d = find_le(blk_off, ndocs, gb);
+  const long long row0 = (long long)cu[d] + (long long)(gb - blk_off[d]) * c;
+  const __nv_bfloat162* zs = reinterpret_cast<const __nv_bfloat162*>(z + row0 * Di) + pr;
+  const __nv_bfloat162* ks = reinterpret_cast<const __nv_bfloat162*>(kI + row0 * Di) + pr;
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll 8
+  for (int j = 0; j < c; ++j) {
+    const float2 v = __bfloat1622float2(zs[(long long)j * pairs]);
+    m0 = fmaxf(m0, v.x);
+    m1 = fmaxf(m1, v.y);
+  }
+  float s0 = 0.f, s1 = 0.f, n0 = 0.f, n1 = 0.f;
+#pragma unroll 8
+  for (int j = 0; j < c; ++j) {
+    const float2 v = __bfloat1622float2(zs[(long long)j * pairs]);
+    const float2 k = __bfloat1622float2(ks[(long long)j * pairs]);
+    const float e0 = exp_stated(__fsub_rn(v.x, m0));
+    const float e1 = exp_stated(__fsub_rn(v.y, m1));
+    s0 = __fadd_rn(s0, e0);
+    s1 = __fadd_rn(s1, e1);
+    n0 = __fadd_rn(n0, __fmul_rn(e0, k.x));
+    n1 = __fadd_rn(n1, __fmul_rn(e1, k.y));
+  }
+  const __nv_fp8_storage_t b0 = __nv_cvt_float_to_fp8(
+      __bfloat162float(__float2bfloat16_rn(__fdiv_rn(n0, s0))), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8_storage_t b1 = __nv_cvt_float_to_fp8(
+      __bfloat162float(__float2bfloat16_rn(__fdiv_rn(n1, s1))), __NV_SATFINITE, __NV_E4M3);
+  if (kbar8 != nullptr) {
+    reinterpret_cast<uint16_t*>(kbar8 + (long long)gb * Di)[pr] = (uint16_t)(b0 | ((uint16_t)b1 << 8));
+    return;
+  }
+  const float f0 = __half2float(__half(__nv_cvt_fp8_to_halfraw(b0, __NV_E4M3)));
+  const float f1 = __half2float(__half(__nv_cvt_fp8_to_halfraw(b1, __NV_E4M3)));
+  reinterpret_cast<__nv_bfloat162*>(kbar + (long long)gb * Di)[pr] = __floats2bfloat162_rn(f0, f1);
+}
+
+// =====================================================================================
 // Indexer front half (QSA page, `Qwen3_8_FlashNextQSAIndexer`: the FP32 group means get K
 // RMSNorm and group-start RoPE, the queries RMSNorm and RoPE; `apply_qsa_rope`: per-token
 // rotary values cat(cos, sin) over the first rope_dims dims, the rest unchanged). One
@@ -717,7 +804,7 @@ __global__ void __launch_bounds__(128) compose_window_kernel(const int32_t* __re
 // host launchers
 // =====================================================================================
 IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len, bool with_scores,
-                     bool front, bool e4m3) {
+                     bool front, bool e4m3, int G) {
   IndexPlan p{};
   p.kb = budget / c;
   p.QT = kIdxN / Hi;
@@ -738,7 +825,7 @@ IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int ma
   p.off_scores = with_scores ? take((size_t)T * p.ldS * sizeof(float), 1024) : 0;
   p.off_qfront = front ? take((size_t)T * Hi * Di * 2, 1024) : 0;
   p.off_kbar32 = front ? take((size_t)p.nblk_cap * Di * sizeof(float), 1024) : 0;
-  p.off_q8 = e4m3 ? take((size_t)T * Hi * Di, 1024) : 0;
+  p.off_q8 = e4m3 ? take((size_t)T * G * Hi * Di, 1024) : 0;
   p.off_k8 = e4m3 ? take((size_t)p.nblk_cap * Di, 1024) : 0;
   p.ws_bytes = (off + 255) / 256 * 256;
   if (e4m3) {   // one 128-byte atom per key tile
@@ -762,7 +849,7 @@ size_t topk_smem_bytes(int nvis_cap, int kb) {
 static void launch_pool(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI, const int32_t* cu,
                         int ndocs, int max_doc_len, int T, int Hi, int Di, int c, uint8_t* ws, int32_t* err,
                         const FrontHalf* front, __nv_bfloat16* kbar, __nv_bfloat16* qfront, cudaStream_t stream,
-                        bool e4m3 = false) {
+                        bool e4m3 = false, const __nv_bfloat16* z = nullptr, int G = 1) {
   int32_t* meta = reinterpret_cast<int32_t*>(ws + p.off_meta);
   int32_t* blk_off = reinterpret_cast<int32_t*>(ws + p.off_blk);
   int32_t* tile_off = reinterpret_cast<int32_t*>(ws + p.off_tile);
@@ -770,14 +857,19 @@ static void launch_pool(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_
 
   layout_kernel<<<1, 1024, 0, stream>>>(cu, ndocs, T, c, p.tau_sparse, p.QT, max_doc_len, meta, blk_off, tile_off,
                                         err);
-  {
+  if (z != nullptr) {
+    const long long threads = (long long)p.nblk_cap * (Di / 2);
+    summary_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(kI, z, cu, ndocs, Di, c, p.nblk_cap, meta,
+                                                                          blk_off, kbar,
+                                                                          e4m3 ? ws + p.off_k8 : nullptr);
+  } else {
     const long long threads = (long long)p.nblk_cap * (Di / 8);
     const int grid = (int)((threads + 255) / 256);
     pool_kernel<<<grid, 256, 0, stream>>>(kI, cu, ndocs, Di, c, p.nblk_cap, meta, blk_off, kbar,
                                           front ? kbar32 : nullptr, e4m3 ? ws + p.off_k8 : nullptr);
   }
   if (e4m3) {
-    const long long n16 = (long long)T * Hi * Di / 16;
+    const long long n16 = (long long)T * G * Hi * Di / 16;
     quantize_e4m3_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, stream>>>(qI, n16, ws + p.off_q8);
   }
   if (front) {
@@ -795,13 +887,14 @@ cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv
                          const int32_t* cu, int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
                          int32_t* route, float* scores, int64_t ldS, uint8_t* ws, int32_t* err,
                          const CUtensorMap& tm_q, const CUtensorMap& tm_k, int num_sms, cudaStream_t stream,
-                         const FrontHalf* front, int G, int64_t scores_group_stride, bool e4m3) {
+                         const FrontHalf* front, int G, int64_t scores_group_stride, bool e4m3,
+                         const __nv_bfloat16* z) {
   int32_t* meta = reinterpret_cast<int32_t*>(ws + p.off_meta);
   int32_t* blk_off = reinterpret_cast<int32_t*>(ws + p.off_blk);
   int32_t* tile_off = reinterpret_cast<int32_t*>(ws + p.off_tile);
   __nv_bfloat16* kbar = reinterpret_cast<__nv_bfloat16*>(ws + p.off_kbar);
   launch_pool(p, qI, kI, cu, ndocs, max_doc_len, T, Hi, Di, c, ws, err, front, kbar,
-              reinterpret_cast<__nv_bfloat16*>(ws + p.off_qfront), stream, e4m3);
+              reinterpret_cast<__nv_bfloat16*>(ws + p.off_qfront), stream, e4m3, z, G);
   const int grid = num_sms < kMaxIndexCtas ? num_sms : kMaxIndexCtas;
   const int W = budget + c - 1;
   // one score + top-k pass per KV group (Step-5 selects per group), sharing the pooled keys;
@@ -833,6 +926,20 @@ cudaError_t launch_front_operands(const IndexPlan& p, const __nv_bfloat16* qI, c
                                   uint8_t* ws, int32_t* err, const FrontHalf& front, __nv_bfloat16* q_out,
                                   __nv_bfloat16* k_out, cudaStream_t stream) {
   launch_pool(p, qI, kI, cu, ndocs, max_doc_len, T, Hi, Di, c, ws, err, &front, k_out, q_out, stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_summaries(const IndexPlan& p, const __nv_bfloat16* kI, const __nv_bfloat16* z, const int32_t* cu,
+                             int ndocs, int max_doc_len, int T, int Di, int c, uint8_t* ws, int32_t* err,
+                             __nv_bfloat16* out, cudaStream_t stream) {
+  int32_t* meta = reinterpret_cast<int32_t*>(ws + p.off_meta);
+  int32_t* blk_off = reinterpret_cast<int32_t*>(ws + p.off_blk);
+  int32_t* tile_off = reinterpret_cast<int32_t*>(ws + p.off_tile);
+  layout_kernel<<<1, 1024, 0, stream>>>(cu, ndocs, T, c, p.tau_sparse, p.QT, max_doc_len, meta, blk_off, tile_off,
+                                        err);
+  const long long threads = (long long)p.nblk_cap * (Di / 2);
+  summary_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(kI, z, cu, ndocs, Di, c, p.nblk_cap, meta,
+                                                                        blk_off, out, nullptr);
   return cudaGetLastError();
 }
 

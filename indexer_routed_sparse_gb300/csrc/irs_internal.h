@@ -38,7 +38,7 @@ struct IndexPlan {
 };
 
 IndexPlan plan_index(int T, int Hi, int Di, int c, int budget, int ndocs, int max_doc_len, bool with_scores,
-                     bool front = false, bool e4m3 = false);
+                     bool front = false, bool e4m3 = false, int G = 1);
 size_t topk_smem_bytes(int nvis_cap, int kb);
 
 cudaError_t configure_score_kernels(size_t smem);
@@ -48,13 +48,20 @@ cudaError_t configure_topk_kernel(size_t smem);
 // selection; tm_q maps [T][G*Hi][Di], w is [T, G, Hi], route [T, G, W], and group g's score
 // rows start at scores + g * scores_group_stride (row stride ldS). e4m3: queries and pooled
 // keys are rounded to FP8 E4M3 and scored with kind::f8f6f4 (tm_q / tm_k map the byte copies
-// at ws + p.off_q8 / p.off_k8; Di = 128).
+// at ws + p.off_q8 / p.off_k8; Di = 128). z != nullptr: the block keys are the Step-5
+// learned-logit summaries of kI under the compression logits z [T, Di] (E4M3 values; as bytes
+// for e4m3, else as bf16) instead of the means.
 cudaError_t launch_index(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI, const float* w,
                          const int32_t* cu, int ndocs, int max_doc_len, int T, int Hi, int Di, int c, int budget,
                          int32_t* route, float* scores, int64_t ldS, uint8_t* ws, int32_t* err,
                          const CUtensorMap& tm_q, const CUtensorMap& tm_k, int num_sms, cudaStream_t stream,
                          const FrontHalf* front = nullptr, int G = 1, int64_t scores_group_stride = 0,
-                         bool e4m3 = false);
+                         bool e4m3 = false, const __nv_bfloat16* z = nullptr);
+// The learned-logit summaries alone, as E4M3-valued bf16 [nblk_cap, Di] into out (rows past
+// the region count zeroed); uses the plan's layout scratch.
+cudaError_t launch_summaries(const IndexPlan& p, const __nv_bfloat16* kI, const __nv_bfloat16* z, const int32_t* cu,
+                             int ndocs, int max_doc_len, int T, int Di, int c, uint8_t* ws, int32_t* err,
+                             __nv_bfloat16* out, cudaStream_t stream);
 // The front half alone: transformed queries [T*Hi, Di] into q_out, pooled keys [T/c, Di]
 // into k_out (rows past the last complete block zeroed).
 cudaError_t launch_front_operands(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_bfloat16* kI,

@@ -255,6 +255,19 @@ def front_half_inputs(T: int, Di: int, rope_dims: int, cu_seqlens: np.ndarray, s
     return dict(q_weight=q_weight, k_weight=k_weight, eps=eps, rope=rope)
 
 
+def compression_logits(T: int, Di: int, seed: int = 0, scale: float = 2.0) -> np.ndarray:
+    """Step-5 compression logits shaped like the index keys: bf16 bits [T, Di] of
+    scale * N(0, 1). scale 2 gives softmax weights that are neither flat nor one-hot over a
+    region; 0 gives equal logits; a large scale gives near one-hot weights with underflow."""
+    rng = np.random.default_rng(seed)
+    out = np.empty((T, Di), dtype=np.uint16)
+    for r0 in range(0, T, _DRAW_ROWS):
+        r1 = min(T, r0 + _DRAW_ROWS)
+        x = rng.standard_normal((r1 - r0, Di), dtype=np.float32) * np.float32(scale)
+        out[r0:r1] = f32_to_bf16_bits(x.astype(np.float32))
+    return out
+
+
 def random_routes(rng: np.random.Generator, T: int, Tk: int, width: int, cu_seqlens: np.ndarray,
                   frac_invalid: float = 0.25) -> np.ndarray:
     """Arbitrary causal, document-confined routes with -1 holes at random slots.

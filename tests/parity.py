@@ -30,11 +30,12 @@ def doc_starts(cu, rows):
     return cu[d]
 
 
-def check_scores(gpu_scores: np.ndarray, ref_scores: np.ndarray, wl, rows) -> None:
-    """gpu_scores / ref_scores: [len(rows), ld]; entries [0, nvis) of sparse rows compared."""
+def check_scores(gpu_scores: np.ndarray, ref_scores: np.ndarray, wl, rows, ktilde=None) -> None:
+    """gpu_scores / ref_scores: [len(rows), ld]; entries [0, nvis) of sparse rows compared.
+    ktilde: the scored block keys (float64 values) when they are not the bf16 means."""
     a = wl.arrays
     kbar, blk_off = O.pool_keys(a["kI"], wl.cu_seqlens, wl.c)
-    kt_abs = np.abs(O.round_to_bf16(kbar).astype(np.float64))
+    kt_abs = np.abs(O.round_to_bf16(kbar).astype(np.float64) if ktilde is None else np.asarray(ktilde, np.float64))
     cu = np.asarray(wl.cu_seqlens, np.int64)
     kb = wl.budget // wl.c
     worst = 0.0

@@ -172,3 +172,31 @@ def test_front_half_validation_is_value_error(lib):
     assert call(rope=None) == 2 and b"rotary" in lib.irs_last_error()
     assert lib.irs_index_front_workspace_bytes(64, 4, 64, 4, 16, 1, 64, 1) > lib.irs_index_workspace_bytes(
         64, 4, 64, 4, 16, 1, 64, 1)
+
+
+def test_summaries_validation_is_value_error(lib):
+    import ctypes as C
+    buf = C.create_string_buffer(512)
+    p = C.addressof(buf) + (256 - C.addressof(buf) % 256) % 256
+
+    def call(z=p, Di=128, e4=1, G=1):
+        return lib.irs_sparse_index_score_topk_summaries(p, p, z, p, p, 1, 64, 64, G, 4, Di, 4, 16, e4, p, None, 0,
+                                                         p, 1 << 30, None, None)
+    assert call(z=None) == 2 and b"compression logits" in lib.irs_last_error()
+    assert call(Di=64, e4=1) == 2 and b"Di = 128" in lib.irs_last_error()
+    assert call(z=p + 2) == 2 and b"16-byte" in lib.irs_last_error()
+    assert call(G=0) == 2
+    one = lib.irs_index_summaries_workspace_bytes(64, 1, 4, 128, 4, 16, 1, 64, 1, 1)
+    two = lib.irs_index_summaries_workspace_bytes(64, 2, 4, 128, 4, 16, 1, 64, 1, 1)
+    assert 0 < one < two                       # the E4M3 query copy holds every group
+    assert lib.irs_index_summaries_workspace_bytes(64, 1, 4, 64, 4, 16, 1, 64, 1, 1) == 0
+    assert lib.irs_index_summaries_workspace_bytes(64, 1, 4, 64, 4, 16, 1, 64, 0, 1) > 0
+    # the summaries alone
+    assert lib.irs_region_summaries_workspace_bytes(64, 96, 4, 1, 64) == 0
+    assert lib.irs_region_summaries_workspace_bytes(64, 128, 4, 1, 64) > 0
+    st = lib.irs_region_summaries(p, None, p, 1, 64, 64, 128, 4, p, p, 1 << 20, None, None)
+    assert st == 2 and b"NULL" in lib.irs_last_error()
+    st = lib.irs_region_summaries(p, p + 8, p, 1, 64, 64, 128, 4, p, p, 1 << 20, None, None)
+    assert st == 2 and b"aligned" in lib.irs_last_error()
+    st = lib.irs_region_summaries(p, p, p, 1, 64, 64, 128, 4, p, p, 16, None, None)
+    assert st == 2 and b"workspace too small" in lib.irs_last_error()
