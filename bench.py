@@ -437,6 +437,73 @@ def measure_other_workload(irs, name, args, dev, stream, flush, peaks, l2_gbs) -
     return rep
 
 
+def measure_indexer_variants(irs, wl, d, dev, stream, flush, peaks, steps: int) -> dict:
+    """The indexer rows beyond the plain one, on the headline workload's indexer shape
+    (T, Hi, Di, c, budget, documents), each timed cold (L2 flushed before every call):
+    the QSA front half (RMSNorm + RoPE, 64 rotary dims), FP8 E4M3 operands, per-KV-group
+    selection (G = Hkv groups of Hi heads), and the Step-5 configuration (learned-logit
+    summaries, E4M3 queries, per group). Grouped queries, weights and the compression logits
+    come from a seeded device generator. Roofline: the score FLOPs at the tensor peak of the
+    operand type (E4M3 at twice the measured bf16 rate, the nominal ratio) or the
+    algorithmic bytes at the HBM rate, whichever is slower."""
+    import torch
+
+    T, Hi, Di, c, budget, G = wl.T, wl.Hi, wl.Di, wl.c, wl.budget, max(wl.Hkv, 1)
+    W = budget + c - 1
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    qg = torch.randn((T, G, Hi, Di), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    wg = torch.rand((T, G, Hi), generator=gen, device=dev, dtype=torch.float32)
+    z = (2.0 * torch.randn((T, Di), generator=gen, device=dev, dtype=torch.float32)).to(torch.bfloat16)
+    fr = irs_synth.front_half_inputs(T, Di, 64, wl.cu_seqlens, seed=5)
+    front = {k: (torch.from_numpy(v).to(dev) if isinstance(v, np.ndarray) else v) for k, v in fr.items()}
+    err = irs.device_error_flag(dev)
+    kw = dict(ndocs=wl.ndocs, max_doc_len=wl.max_doc_len, err=err)
+    score_pairs = counts(wl)["score_pairs"]
+    base_bytes = T * Hi * Di * 2 + T * Di * 2 + T * Hi * 4 + T * W * 4
+    variants = {
+        "front_half": (lambda: irs.sparse_index_score_topk(d["qI"], d["kI"], d["w"], d["cu_seqlens"], c, budget,
+                                                           front=front, **kw),
+                       1, "bf16", base_bytes + T * 64 * 4 + 2 * Di * 4),
+        "e4m3": (lambda: irs.sparse_index_score_topk(d["qI"], d["kI"], d["w"], d["cu_seqlens"], c, budget,
+                                                     operands="e4m3", **kw), 1, "e4m3", base_bytes),
+        f"grouped_g{G}": (lambda: irs.sparse_index_score_topk_grouped(qg, d["kI"], wg, d["cu_seqlens"], c, budget,
+                                                                      **kw),
+                          G, "bf16", G * (T * Hi * Di * 2 + T * Hi * 4 + T * W * 4) + T * Di * 2),
+        f"step5_summaries_e4m3_g{G}": (lambda: irs.sparse_index_score_topk_summaries(
+            qg, d["kI"], z, wg, d["cu_seqlens"], c, budget, operands="e4m3", **kw),
+            G, "e4m3", G * (T * Hi * Di * 2 + T * Hi * 4 + T * W * 4) + 2 * T * Di * 2),
+    }
+    out = {}
+    for name, (fn, groups, dtype, nbytes) in variants.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        irs.check_device_errors(dev)
+        ms = np.asarray([e[0].elapsed_time(e[1]) for e in ev])
+        sec = float(np.mean(ms)) * 1e-3
+        flops = 2.0 * Hi * Di * score_pairs * groups
+        tc_peak = peaks["bf16_tflops"] * (2.0 if dtype == "e4m3" else 1.0)
+        t_tc = flops / (tc_peak * 1e12)
+        t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+        roof = max(t_tc, t_hbm)
+        out[name] = {"ms": round(sec * 1e3, 4), "ms_median": round(float(np.median(ms)), 4),
+                     "queries_per_s": round(T / sec, 1), "groups": groups, "operands": dtype,
+                     "tflops": round(flops / sec / 1e12, 3), "roofline_bound": "tensor" if t_tc >= t_hbm else "hbm",
+                     "roofline_frac": round(roof / sec, 4),
+                     "tensor_peak_tflops": round(tc_peak, 1) if dtype == "bf16" else
+                     f"{2 * peaks['bf16_tflops']:.1f} (2x measured bf16, nominal E4M3 ratio)"}
+    del qg, wg, z
+    return out
+
+
 def run_gpu(args) -> dict | None:
     import torch
 
@@ -510,6 +577,9 @@ def run_gpu(args) -> dict | None:
         ee[i][1].synchronize()
     barrier(world)
     e2e_ms = reduce_max(float(np.mean([ee[i][0].elapsed_time(ee[i][1]) for i in range(e2e_steps)])), world, dev)
+    variants = None
+    if not args.no_per_workload and not args.small and args.workload == WORKLOAD and not wl.latent:
+        variants = measure_indexer_variants(irs, wl, path.d, dev, stream, flush, peaks, max(3, min(args.steps, 20)))
     bwd = time_backward(args, wl, irs, path.d, path.route, path.kv_v, path.out, path.lse, flush, path.err, stream,
                         dev) if args.with_backward else None
     clk = clocks.stop() if rank == 0 else None
@@ -575,6 +645,8 @@ def run_gpu(args) -> dict | None:
     }
     if not wl.latent:
         res["indexer"] = indexer_report(wl, cnt, idx_ms, idx_w, peaks)
+    if variants is not None:
+        res["indexer_variants"] = variants
     if bwd is not None:
         res["backward"] = backward_report(wl, cnt, bwd, peaks)
     if per_workload:

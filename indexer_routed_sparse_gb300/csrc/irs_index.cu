@@ -303,10 +303,11 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 }
 
 // One row: x (Di values) -> out (bf16), normalised with wt and rotated with rope (cos | sin).
+// out may be x itself (bf16 rows staged in shared memory): every 8-value chunk is read
+// before it is written, and later chunks are read before their own writes.
 template <typename In>
-__device__ __forceinline__ void front_row(const In* __restrict__ x, int Di, const float* __restrict__ wt, float eps,
-                                          const float* __restrict__ rope, int rope_dims,
-                                          __nv_bfloat16* __restrict__ out) {
+__device__ __forceinline__ void front_row(const In* x, int Di, const float* __restrict__ wt, float eps,
+                                          const float* __restrict__ rope, int rope_dims, __nv_bfloat16* out) {
   float ss = 0.f;
   for (int d0 = 0; d0 < Di; d0 += 8) {
     float f[8];
@@ -362,15 +363,33 @@ __global__ void __launch_bounds__(128) front_keys_kernel(const float* __restrict
   front_row<float>(kbar32 + (long long)gb * Di, Di, k_weight, eps, rope + tok * rope_dims, rope_dims, out);
 }
 
-// Queries: row t*Hi + h takes the rotary values of token t.
-__global__ void __launch_bounds__(128) front_queries_kernel(const __nv_bfloat16* __restrict__ qI, long long rows,
-                                                            int Hi, int Di, const float* __restrict__ q_weight,
-                                                            float eps, const float* __restrict__ rope, int rope_dims,
-                                                            __nv_bfloat16* __restrict__ qout) {
-  const long long row = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= rows) return;
-  const long long t = row / Hi;
-  front_row<__nv_bfloat16>(qI + row * Di, Di, q_weight, eps, rope + t * rope_dims, rope_dims, qout + row * Di);
+// Queries: row t*Hi + h takes the rotary values of token t. A CTA stages 128 rows in
+// shared memory with coalesced 16-byte loads (rows padded by one 16-byte chunk, so the
+// per-thread row reads of 8 consecutive threads fall in distinct banks), each thread
+// transforms its row in place, and the CTA stores the rows back coalesced.
+constexpr int kFrontRows = 128;
+
+__global__ void __launch_bounds__(kFrontRows) front_queries_kernel(const __nv_bfloat16* __restrict__ qI,
+                                                                   long long rows, int Hi, int Di,
+                                                                   const float* __restrict__ q_weight, float eps,
+                                                                   const float* __restrict__ rope, int rope_dims,
+                                                                   __nv_bfloat16* __restrict__ qout) {
+  extern __shared__ uint4 stage[];
+  const int cpr = Di >> 3;        // 16-byte chunks per row
+  const int pitch = cpr + 1;
+  const long long row0 = (long long)blockIdx.x * kFrontRows;
+  const int nrows = rows - row0 < kFrontRows ? (int)(rows - row0) : kFrontRows;
+  const uint4* src = reinterpret_cast<const uint4*>(qI + row0 * Di);
+  for (int i = threadIdx.x; i < nrows * cpr; i += kFrontRows) stage[(i / cpr) * pitch + i % cpr] = __ldg(src + i);
+  __syncthreads();
+  if (threadIdx.x < nrows) {
+    __nv_bfloat16* r = reinterpret_cast<__nv_bfloat16*>(stage + threadIdx.x * pitch);
+    const long long t = (row0 + threadIdx.x) / Hi;
+    front_row<__nv_bfloat16>(r, Di, q_weight, eps, rope + t * rope_dims, rope_dims, r);
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(qout + row0 * Di);
+  for (int i = threadIdx.x; i < nrows * cpr; i += kFrontRows) dst[i] = stage[(i / cpr) * pitch + i % cpr];
 }
 
 // =====================================================================================
@@ -754,10 +773,224 @@ __global__ void __launch_bounds__(kTopkThreads) topk_reg_kernel(TopkArgs a) {
   }
 }
 
-// Launch the top-k + expansion for every row: the register variant when the longest row
-// has at most 2048 visible blocks, else the shared-memory variant.
+// Warp-per-row variant for small selections (kb <= 32) of rows of at most 32*KPL visible
+// blocks; eight rows per CTA, no block barriers. Lane l holds blocks l, l+32, ... of its row.
+// The threshold (the kb-th largest key) is found in two steps. The kb-th largest of the 32
+// lane maxima, L, is a lower bound for it: the kb lanes whose maxima are >= L hold kb keys
+// >= L. So every key >= the threshold is >= L, and only those candidates (about 32 ln 2 + kb
+// of them on continuous scores) need ranking. With at most 32 candidates, one per lane,
+// three 32-lane bitonic sorts in registers give L, the threshold and the ascending list of
+// selected blocks. More candidates (many keys tied near the top) take a general path: an
+// exact rank count over up to kTopkCand candidates in shared memory, else a bit-serial
+// radix select over all keys, and the selection from bitmap words (ballots of the lanes'
+// j-th keys). Both paths select the keys above the threshold plus the lowest-index keys
+// equal to it, as the other variants do.
+constexpr int kTopkWarpRows = 8;
+constexpr int kTopkCand = 128;
+
+// 32-lane bitonic sort of one value per lane: descending (lane 0 the largest) or ascending.
+template <bool kDescending>
+__device__ __forceinline__ uint32_t warp_bitonic_sort(uint32_t v, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint32_t o = __shfl_xor_sync(0xffffffffu, v, j);
+      // within a run of k lanes sorted in direction `dir`, the lower lane of each pair keeps
+      // the value that comes first in that direction
+      const bool dir = ((lane & k) == 0) == kDescending;
+      const bool lower = (lane & j) == 0;
+      const uint32_t hi = v > o ? v : o, lo = v > o ? o : v;
+      v = (lower == dir) ? hi : lo;
+    }
+  }
+  return v;
+}
+
+template <int KPL>
+__global__ void __launch_bounds__(kTopkWarpRows * 32) topk_warp_kernel(TopkArgs a) {
+  static_assert(KPL % 8 == 0, "keys are handled in chunks of 8 words");
+  extern __shared__ uint8_t smem_raw[];
+  const int kb = a.budget / a.c;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t lt = (1u << lane) - 1u;   // lanes below this one
+  uint32_t* cand = reinterpret_cast<uint32_t*>(smem_raw) + warp * 2 * kTopkCand;   // keys
+  uint32_t* cidx = cand + kTopkCand;                                              // their blocks
+  if (a.meta != nullptr && a.meta[0] != 1) return;
+  const int t = blockIdx.x * kTopkWarpRows + warp;
+  if (t >= a.T) return;
+  const int W = a.budget + a.c - 1;
+  int32_t* out = a.route + (long long)t * a.route_ts;
+  const int d = find_doc(a.cu, a.ndocs, t);
+  const int s = a.cu[d], e = a.cu[d + 1];
+  if (!(s <= t && t < e && e <= a.T && e - s <= a.max_doc_len)) {
+    if (lane == 0) record_error(a.err, IRS_DEVERR_CU_SEQLENS);
+    return;
+  }
+  const int tau = t - s;
+  const int nvis = (tau + 1) / a.c;
+  const int ntail = (tau + 1) % a.c;
+  const bool sparse = nvis > kb;
+  const int nsel = sparse ? kb : nvis;
+  // lane r < nsel ends up holding the r-th selected block (ascending)
+  uint32_t selv = (uint32_t)lane;
+  if (sparse) {
+    const float* row = a.scores + (long long)t * a.ldS;
+    const int nw = (nvis + 31) >> 5;   // words with at least one visible block (uniform)
+    uint32_t key[KPL];
+    // per-key work runs on chunks of 8 words, skipped past the row's last visible block;
+    // every load is issued before any key is used
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) {
+      key[j] = 0u;
+      if (8 * (j >> 3) < nw) {
+        const int i = lane + 32 * j;
+        if (i < nvis) key[j] = __float_as_uint(__ldg(row + i));
+      }
+    }
+    uint32_t mx = 0;   // 0 is below every key of a real score (order_key(-inf) > 0)
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) {
+      if (8 * (j >> 3) < nw) {
+        const int i = lane + 32 * j;
+        key[j] = i < nvis ? order_key(__uint_as_float(key[j])) : 0u;
+        mx = key[j] > mx ? key[j] : mx;
+      }
+    }
+    const uint32_t L = __shfl_sync(0xffffffffu, warp_bitonic_sort<true>(mx, lane), kb - 1);
+    // candidates (keys >= L) compacted by ballots in ascending block order
+    int C = 0;
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) {
+      if (8 * (j >> 3) < nw) {
+        const bool p = key[j] >= L;
+        const uint32_t bal = __ballot_sync(0xffffffffu, p);
+        const int o = C + __popc(bal & lt);
+        if (p && o < kTopkCand) { cand[o] = key[j]; cidx[o] = (uint32_t)(lane + 32 * j); }
+        C += __popc(bal);
+      }
+    }
+    __syncwarp();
+    if (C <= 32) {
+      // ---- common path: one candidate per lane, lanes in ascending block order ----
+      const uint32_t ck = lane < C ? cand[lane] : 0u;
+      const uint32_t ci = lane < C ? cidx[lane] : 0u;
+      const uint32_t thr = __shfl_sync(0xffffffffu, warp_bitonic_sort<true>(ck, lane), kb - 1);
+      const uint32_t gt = __ballot_sync(0xffffffffu, ck > thr);
+      const uint32_t eq = __ballot_sync(0xffffffffu, ck == thr);
+      const int rem = kb - __popc(gt);
+      // keys above the threshold, and the rem lowest blocks (= lowest lanes) equal to it
+      const bool take = ck > thr || (ck == thr && __popc(eq & lt) < rem);
+      const uint32_t tk = __ballot_sync(0xffffffffu, take);
+      __syncwarp();
+      if (take) cidx[__popc(tk & lt)] = ci;
+      __syncwarp();
+      selv = lane < kb ? cidx[lane] : 0u;
+    } else {
+      // ---- general path ----
+      uint32_t thr;
+      int rem;
+      if (C <= kTopkCand) {
+        bool found = false;
+        uint32_t my_thr = 0;
+        int my_rem = 0;
+        for (int i = lane; i < C; i += 32) {
+          const uint32_t v = cand[i];
+          int gt = 0, ge = 0;
+          for (int q = 0; q < C; ++q) {
+            const uint32_t u = cand[q];
+            gt += u > v ? 1 : 0;
+            ge += u >= v ? 1 : 0;
+          }
+          if (gt < kb && kb <= ge) { found = true; my_thr = v; my_rem = kb - gt; }
+        }
+        const int src = __ffs(__ballot_sync(0xffffffffu, found)) - 1;
+        thr = __shfl_sync(0xffffffffu, my_thr, src);
+        rem = __shfl_sync(0xffffffffu, my_rem, src);
+      } else {
+        // bit-serial radix select: the rem-th largest among the keys that match the prefix
+        uint32_t prefix = 0, mask = 0;
+        rem = kb;
+        for (int bit = 31; bit >= 0; --bit) {
+          const uint32_t m2 = mask | (1u << bit), want = prefix | (1u << bit);
+          int c1 = 0;
+#pragma unroll
+          for (int j = 0; j < KPL; ++j) c1 += (key[j] & m2) == want ? 1 : 0;
+          const int tot = __reduce_add_sync(0xffffffffu, c1);
+          if (tot >= rem) prefix = want;
+          else rem -= tot;
+          mask = m2;
+        }
+        thr = prefix;
+      }
+      // bitmap word j = ballot of the lanes' j-th keys; selected blocks in ascending order
+      int eq_before = 0, sel_before = 0;
+#pragma unroll
+      for (int j = 0; j < KPL; ++j) {
+        if (j >= nw) break;
+        const uint32_t g = __ballot_sync(0xffffffffu, key[j] > thr);
+        const uint32_t q = __ballot_sync(0xffffffffu, key[j] == thr);
+        uint32_t tk = 0;
+        if (eq_before < rem) {
+          const int want = rem - eq_before;
+          if (want >= __popc(q)) tk = q;
+          else {
+            uint32_t x = q;
+            for (int r = 0; r < want; ++r) { tk |= x & (~x + 1u); x &= x - 1u; }
+          }
+        }
+        eq_before += __popc(q);
+        const uint32_t bits = g | tk;
+        // the n-th set bit of this word goes to lane sel_before + n
+        const int n_here = __popc(bits);
+        const int r = lane - sel_before;
+        if (r >= 0 && r < n_here) {
+          uint32_t x = bits;
+          for (int q2 = 0; q2 < r; ++q2) x &= x - 1u;
+          selv = 32u * j + (uint32_t)(__ffs(x) - 1);
+        }
+        sel_before += n_here;
+      }
+    }
+  }
+  // ---- route row: [selected blocks x c tokens | -1 ...][tail tokens | -1 ...] ----
+  const int c = a.c;
+  const int nblk_slots = nsel * c;
+  if ((c & 31) == 0) {
+    for (int r = 0; r < nsel; ++r) {
+      const int base = s + (int)__shfl_sync(0xffffffffu, selv, r) * c;
+      for (int j = lane; j < c; j += 32) out[r * c + j] = base + j;
+    }
+  } else {
+    const bool pow2 = (c & (c - 1)) == 0;
+    const int cs = __ffs(c) - 1;
+    for (int slot0 = 0; slot0 < nblk_slots; slot0 += 32) {
+      const int slot = slot0 + lane;
+      const int rr = slot < nblk_slots ? (pow2 ? slot >> cs : slot / c) : 0;
+      const int b = (int)__shfl_sync(0xffffffffu, selv, rr);
+      if (slot < nblk_slots) out[slot] = s + b * c + (slot - rr * c);
+    }
+  }
+  for (int slot = nblk_slots + lane; slot < W; slot += 32) {
+    const int j = slot - a.budget;
+    out[slot] = (j >= 0 && j < ntail) ? s + nvis * c + j : -1;
+  }
+}
+
+// Launch the top-k + expansion for every row: the warp-per-row variant for kb <= 32 and
+// rows of at most 2048 visible blocks, the register variant for larger kb on such rows,
+// else the shared-memory variant.
 static cudaError_t launch_topk(const TopkArgs& ta, int kb, cudaStream_t stream, size_t cta_smem) {
   const int nv = ta.nvis_cap;
+  if (kb <= 32 && nv <= 2048) {
+    const size_t wsmem = (size_t)kTopkWarpRows * 2 * kTopkCand * 4;
+    const unsigned grid = (unsigned)((ta.T + kTopkWarpRows - 1) / kTopkWarpRows);
+    if (nv <= 256) topk_warp_kernel<8><<<grid, kTopkWarpRows * 32, wsmem, stream>>>(ta);
+    else if (nv <= 512) topk_warp_kernel<16><<<grid, kTopkWarpRows * 32, wsmem, stream>>>(ta);
+    else if (nv <= 1024) topk_warp_kernel<32><<<grid, kTopkWarpRows * 32, wsmem, stream>>>(ta);
+    else topk_warp_kernel<64><<<grid, kTopkWarpRows * 32, wsmem, stream>>>(ta);
+    return cudaGetLastError();
+  }
   const size_t smem = (size_t)kb * 4;
   if (nv <= 2048 && smem <= 48 * 1024) {
     if (nv <= 256) topk_reg_kernel<2><<<ta.T, kTopkThreads, smem, stream>>>(ta);
@@ -877,9 +1110,9 @@ static void launch_pool(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_
                                                                     front->k_weight, front->eps, front->rope,
                                                                     front->rope_dims, kbar);
     const long long rows = (long long)T * Hi;
-    front_queries_kernel<<<(unsigned)((rows + 127) / 128), 128, 0, stream>>>(qI, rows, Hi, Di, front->q_weight,
-                                                                             front->eps, front->rope, front->rope_dims,
-                                                                             qfront);
+    const size_t stage_bytes = (size_t)kFrontRows * (Di / 8 + 1) * 16;
+    front_queries_kernel<<<(unsigned)((rows + kFrontRows - 1) / kFrontRows), kFrontRows, stage_bytes, stream>>>(
+        qI, rows, Hi, Di, front->q_weight, front->eps, front->rope, front->rope_dims, qfront);
   }
 }
 

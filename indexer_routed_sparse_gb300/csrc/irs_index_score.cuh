@@ -46,15 +46,17 @@ __device__ __forceinline__ int find_le(const int32_t* __restrict__ off, int n, i
 // next. The epilogue thread of lane b reduces each query's heads in order,
 // s = sum_h w[t,h] * max(acc, 0) (FP32 FMA chains), and writes row t of the FP32 scores.
 //
-// Warps: 0 scheduler + TMA producer (+ head weights), 1 TMEM owner + MMA issuer,
-// 2..9 epilogue (two per TMEM lane quarter, 128 columns each). Every cross-warp wait is a
-// bounded mbarrier wait.
+// Warps: 0 scheduler + TMA producer, 1 TMEM owner + MMA issuer, 2..17 epilogue (four per
+// TMEM lane quarter, 64 columns each). The producer only issues copies (it fetches the
+// next tile's id one tile ahead); each epilogue warp loads the head weights of its own
+// columns, so no global-load latency sits between two tiles' key copies. Every cross-warp
+// wait is a bounded mbarrier wait.
 // =====================================================================================
-constexpr int kIdxThreads = 320;      // producer, MMA issuer, 8 epilogue warps
+constexpr int kIdxThreads = 576;      // producer, MMA issuer, 16 epilogue warps
 constexpr int kIdxN = 256;           // (query, head) columns per tile
 constexpr int kIdxM = 128;           // key blocks per key tile
 constexpr int kEpiWarp0 = 2;
-constexpr int kNumEpi = 8;
+constexpr int kNumEpi = 16;
 constexpr int kTileSlots = 4;
 constexpr int kIdxAtom = kIdxM * 128;   // bytes of one 64-dim atom of a key tile
 enum { kTileSparse = 0, kTileStop = 2 };
@@ -118,9 +120,11 @@ struct IdxSmem {
   static constexpr uint32_t kBBytes = (DI / kAtomElems) * kBAtom;
   static constexpr uint32_t b_off = 0;                                   // [2] query tiles
   static constexpr uint32_t a_off = 2 * kBBytes;                         // [stages] key atoms
-  __host__ __device__ static uint32_t w_off(int st) { return a_off + (uint32_t)st * kIdxAtom; }   // [2][256] fp32
-  __host__ __device__ static uint32_t part_off(int st) { return w_off(st) + 2 * kIdxN * 4; }      // [2][128] fp32
-  __host__ __device__ static uint32_t tile_off(int st) { return part_off(st) + 2 * 128 * 4; }
+  // [16 epilogue warps][64] fp32: each warp's copy of its columns' head weights
+  __host__ __device__ static uint32_t w_off(int st) { return a_off + (uint32_t)st * kIdxAtom; }
+  // [2 buffers][4 lane quarters][4 column blocks][32 lanes] fp32 partial sums
+  __host__ __device__ static uint32_t part_off(int st) { return w_off(st) + kNumEpi * 64 * 4; }
+  __host__ __device__ static uint32_t tile_off(int st) { return part_off(st) + 2 * 512 * 4; }
   __host__ __device__ static uint32_t bar_off(int st) { return tile_off(st) + kTileSlots * sizeof(TileInfo); }
   __host__ __device__ static uint32_t total(int st) { return bar_off(st) + (2 * st + 17) * 8 + 16 + 1024; }
 };
@@ -139,7 +143,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   constexpr int AE = L::kAtomElems;   // elements per 128-byte row of an atom
   constexpr int KATOMS = DI / AE;
   constexpr uint32_t IDESC = F8 ? idesc_e4m3(kIdxM, kIdxN) : idesc_bf16(kIdxM, kIdxN, false, false);
-  constexpr int kColsPerWarp = kIdxN / 2;
+  constexpr int kColsPerWarp = kIdxN / 4;
 
   extern __shared__ uint8_t smem_raw[];
   // aligned by pointer arithmetic on the __shared__ array, so that accesses through these
@@ -168,8 +172,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < S; ++s) { mbar_init(&a_full[s], 1); mbar_init(&a_empty[s], 1); }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&b_full[i], 1 + 32);           // the TMA issuer's arrival + every producer lane (weights)
-      mbar_init(&b_empty[i], 1 + kNumEpi);     // the last MMA of the tile + every epilogue warp
+      mbar_init(&b_full[i], 1);                // the query tile's TMA
+      mbar_init(&b_empty[i], 1);               // the last MMA of the tile
       mbar_init(&t_full[i], 1);
       mbar_init(&t_empty[i], kNumEpi);
     }
@@ -195,20 +199,23 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     const int nsparse = a.meta[2];
     if (lane == 0) { tma_prefetch_map(&tm_q); tma_prefetch_map(&tm_k); }
     uint32_t i = 0, nb = 0, at = 0;
+    // the next tile's id is fetched one tile ahead, so the counter's round trip overlaps
+    // the current tile's loads
+    int next_id = 0;
+    if (lane == 0) next_id = atomicAdd(&a.meta[3], 1);
     while (true) {
       const int slot = i & (kTileSlots - 1);
       if (i >= kTileSlots &&
           !__all_sync(0xffffffffu, mbar_wait(&tile_empty[slot], ((i / kTileSlots) - 1) & 1, abort_flag, a.err)))
         break;
-      int id = 0;
-      if (lane == 0) id = atomicAdd(&a.meta[3], 1);
-      id = __shfl_sync(0xffffffffu, id, 0);
+      const int id = __shfl_sync(0xffffffffu, next_id, 0);
       const TileInfo ti = decode_tile(a, id, nsparse);
       if (lane == 0) sTile[slot] = ti;
       __syncwarp();
       if (lane == 0) mbar_arrive(&tile_full[slot]);
       ++i;
       if (ti.kind == kTileStop) break;
+      if (lane == 0) next_id = atomicAdd(&a.meta[3], 1);
       const int bs = nb & 1;
       if (nb >= 2 && !__all_sync(0xffffffffu, mbar_wait(&b_empty[bs], ((nb >> 1) - 1) & 1, abort_flag, a.err)))
         break;
@@ -218,20 +225,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         for (int ka = 0; ka < KATOMS; ++ka)
           tma_load_3d(sB + bs * L::kBBytes + ka * L::kBAtom, &tm_q, ka * AE, a.q_y0, ti.t0, &b_full[bs]);
       }
-      // head weights of the tile's (query, head) columns (zero past the last token); all
-      // loads are issued before the stores
-      {
-        float wv[kIdxN / 32];
-#pragma unroll
-        for (int k = 0; k < kIdxN / 32; ++k) {
-          const int col = k * 32 + lane;
-          const long long tq = (long long)ti.t0 + col / HI;
-          wv[k] = tq < a.T ? __ldg(a.w + tq * a.w_ts + (col % HI)) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < kIdxN / 32; ++k) sW[bs * kIdxN + k * 32 + lane] = wv[k];
-      }
-      mbar_arrive(&b_full[bs]);
       ++nb;
       bool ok = true;
       if (lane == 0) {
@@ -305,12 +298,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
     }
   } else {
-    // ---------------- epilogue: warps 2..9 ----------------
+    // ---------------- epilogue: warps 2..17 ----------------
     const int e = warp - kEpiWarp0;
     const int quarter = warp & 3;
     const int col0 = (e >> 2) * kColsPerWarp;
     const uint32_t lane_addr = tmem_lane_base(warp);
-    uint32_t i = 0, nb = 0, kt = 0;
+    uint32_t i = 0, kt = 0;
     bool alive = true;
     while (alive) {
       const int slot = i & (kTileSlots - 1);
@@ -321,9 +314,22 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       ++i;
       if (ti.kind == kTileStop) break;
       {
-        const int bs = nb & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&b_full[bs], (nb >> 1) & 1, abort_flag, a.err))) break;
-        const float* wt = sW + bs * kIdxN;
+        // this warp's head weights (its 64 columns; zero past the last token), loaded before
+        // the first wait on the MMA so that their latency overlaps it
+        float* wt = sW + e * kColsPerWarp;
+        {
+          float wv[kColsPerWarp / 32];
+#pragma unroll
+          for (int k = 0; k < kColsPerWarp / 32; ++k) {
+            const int col = col0 + k * 32 + lane;
+            const long long tq = (long long)ti.t0 + col / HI;
+            wv[k] = tq < a.T ? __ldg(a.w + tq * a.w_ts + (col % HI)) : 0.f;
+          }
+          __syncwarp();   // the previous tile's reads of wt are done
+#pragma unroll
+          for (int k = 0; k < kColsPerWarp / 32; ++k) wt[k * 32 + lane] = wv[k];
+          __syncwarp();
+        }
         for (int j = 0; j < ti.nbt; ++j, ++kt) {
           const int buf = kt & 1;
           // one decision per warp, taken after every lane's wait: tcgen05.ld is warp-aligned
@@ -336,22 +342,15 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           // query q of the tile sees block blk iff (blk+1)*c - 1 <= tau0 + q
           const int qmin = (blk + 1) * a.c - 1 - ti.tau0;
           float carry = 0.f;
-          // the second 64 columns are read from TMEM while the first 64 are reduced
-          float v[4][32];
+          float v[2][32];
           tmem_ld32(tbase + lane_addr + buf * kIdxN + col0, v[0]);
           tmem_ld32(tbase + lane_addr + buf * kIdxN + col0 + 32, v[1]);
           tmem_ld_wait_regs(v[0]);
           tmem_ld_wait_regs(v[1]);
-          tmem_ld32(tbase + lane_addr + buf * kIdxN + col0 + 64, v[2]);
-          tmem_ld32(tbase + lane_addr + buf * kIdxN + col0 + 96, v[3]);
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            if (c4 == 2) {
-              tmem_ld_wait_regs(v[2]);
-              tmem_ld_wait_regs(v[3]);
-            }
+          for (int c4 = 0; c4 < 2; ++c4) {
             const int ccx = col0 + 32 * c4;
-            const float4* w4 = reinterpret_cast<const float4*>(wt + ccx);
+            const float4* w4 = reinterpret_cast<const float4*>(wt + 32 * c4);
             // per query: 4 interleaved FMA chains over its heads (h mod 4), then combined;
             // prod[q0] holds the sum of the group of columns starting at q0
             float prod[32];
@@ -388,21 +387,26 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             }
           }
           if constexpr (HI > kColsPerWarp) {
-            // one query spans both column halves: the upper half's warp hands its partial
-            // sum to the lower half's warp of the same lane quarter (fixed order)
-            float* part = sPart + (kt & 1) * 128 + quarter * 32;
-            if (col0 != 0) part[lane] = carry;
-            named_bar_sync(1 + quarter, 64);
-            if (col0 == 0 && 0 >= qmin && ti.n > 0) a.scores[(int64_t)ti.t0 * a.ldS + blk] = carry + part[lane];
+            // a query spans HI/64 warps of this lane quarter: each leaves its partial sum, and
+            // the warp holding the query's first columns adds them in column order
+            constexpr int WPQ = HI / kColsPerWarp;
+            float* part = sPart + (kt & 1) * 512 + quarter * 128;
+            const int cb = col0 / kColsPerWarp;
+            part[cb * 32 + lane] = carry;
+            named_bar_sync(1 + quarter, 128);
+            if (cb % WPQ == 0) {
+              float sum = part[cb * 32 + lane];
+#pragma unroll
+              for (int x = 1; x < WPQ; ++x) sum += part[(cb + x) * 32 + lane];
+              const int qi = col0 / HI;
+              if (qi >= qmin && qi < ti.n) a.scores[(int64_t)(ti.t0 + qi) * a.ldS + blk] = sum;
+            }
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&t_empty[buf]);
         }
         if (!alive) break;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&b_empty[bs]);   // this warp no longer reads the tile's weights
-        ++nb;
       }
     }
   }

@@ -148,3 +148,50 @@ def test_single_key_empty_rows_and_bad_ids(irs):
     assert torch.all(dq[::3] == 0)
     for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
         check_grad(name, got, want)
+
+
+def test_mid_backward_full_size(irs):
+    """The mid workload at full size (T 8192, Hq 32, Hkv 8, D 128, routes of 2051 IDs from the
+    GPU indexer, forward outputs from the GPU forward), in the launch configuration the
+    backward timing uses. Checked against the oracle on sampled outputs it can compute one by
+    one: dq of 24 query rows, and the complete dk / dv rows of 6 key rows, each summed by the
+    oracle over every query row that routes that key. Every dk / dv row is also checked by
+    two invariants: per KV group the value gradients sum to the group's sum of dO (the
+    weights of each row sum to one), and the key gradients sum to zero (the softmax is
+    invariant to a shift of the logits)."""
+    wl = irs_synth.make("mid")
+    a = wl.arrays
+    t = irs_synth.as_torch(wl, device=DEV)
+    route = irs.sparse_index_score_topk(t["qI"], t["kI"], t["w"], t["cu_seqlens"], wl.c, wl.budget,
+                                        max_doc_len=wl.max_doc_len)
+    out, lse = irs.sparse_gqa_attn_fwd(t["q"], t["k"], t["v"], route, wl.scale)
+    rng = np.random.default_rng(31)
+    dout = irs_synth.f32_to_bf16_bits(rng.standard_normal((wl.T, wl.Hq, wl.Dv)).astype(np.float32))
+    dq, dk, dv = irs.sparse_gqa_attn_bwd(t["q"], t["k"], t["v"], route, out, lse, bf16_dev(dout), wl.scale)
+    irs.check_device_errors(DEV)
+    routes = route.cpu().numpy()
+    q, k, v = a["q"], a["k"], a["v"]
+    # sampled query rows: dq against the oracle
+    rows = np.unique(np.concatenate([[0, 1, 3, 2047, 2048, wl.T - 1], rng.integers(0, wl.T, 18)]))
+    ref_dq, _, _ = O.attention_bwd(q, k, v, routes, wl.scale, dout, rows=rows)
+    check_grad("dq", dq[torch.as_tensor(rows, device=DEV)], ref_dq)
+    # sampled key rows: all of their query rows, so the oracle's dk / dv rows are complete
+    ids = routes[routes >= 0]
+    fan_in = np.bincount(ids, minlength=wl.T)
+    cand = np.flatnonzero((fan_in >= 2) & (fan_in <= 12))
+    keys = np.unique(cand[np.linspace(0, cand.shape[0] - 1, 6).astype(np.int64)])
+    users = np.flatnonzero(np.isin(routes, keys).any(axis=1))
+    _, ref_dk, ref_dv = O.attention_bwd(q, k, v, routes, wl.scale, dout, rows=users)
+    kidx = torch.as_tensor(keys, device=DEV)
+    check_grad("dk", dk[kidx], ref_dk[keys])
+    check_grad("dv", dv[kidx], ref_dv[keys])
+    # invariants over every key row (float64 sums of the FP32 gradients)
+    G = wl.Hq // wl.Hkv
+    dO = O.bf16_to_f64(dout).reshape(wl.T, wl.Hkv, G, wl.Dv).sum(axis=(0, 2))       # [Hkv, Dv]
+    dv_sum = dv.double().sum(dim=0).cpu().numpy()
+    assert np.abs(dv_sum - dO).max() <= 1e-2, np.abs(dv_sum - dO).max()
+    dk_abs = dk.double().abs().sum(dim=0).cpu().numpy()
+    dk_sum = dk.double().sum(dim=0).cpu().numpy()
+    # the kernel's D = dO . out uses the bf16 output, so each row's ds sums to about 2^-9 |out||dO|
+    # instead of 0; over 32768 (row, head) pairs that leaves about 4e-4 of sum |dk|
+    assert np.all(np.abs(dk_sum) <= 2e-3 * dk_abs + 1e-3), float(np.max(np.abs(dk_sum) / (dk_abs + 1e-30)))

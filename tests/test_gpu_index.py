@@ -138,12 +138,15 @@ def test_malformed_cu_seqlens_sets_the_device_flag(irs):
     run_index(irs, wl)
 
 
+@pytest.mark.parametrize("budget", [64, 256])
 @pytest.mark.parametrize("kind", ["constant", "two_values", "signed_zero", "negative", "wide_range"])
-def test_topk_degenerate_scores_bit_exact(irs, kind):
-    """Ties everywhere, -0/+0, negative and widely spread scores: routes equal the oracle's."""
+def test_topk_degenerate_scores_bit_exact(irs, kind, budget):
+    """Ties everywhere, -0/+0, negative and widely spread scores: routes equal the oracle's
+    (kb 32: the warp-per-row variant, its bit-serial path where many keys tie; kb 128: the
+    register variant)."""
     rng = np.random.default_rng(len(kind))
     cu = np.asarray([0, 700, 2000], np.int32)
-    T, c, budget = 2000, 2, 64
+    T, c = 2000, 2
     ld = 1300 // c
     if kind == "constant":
         sc = np.full((T, ld), 0.75, np.float32)
@@ -155,6 +158,32 @@ def test_topk_degenerate_scores_bit_exact(irs, kind):
         sc = -rng.random((T, ld), dtype=np.float32)
     else:
         sc = (rng.standard_normal((T, ld)) * np.exp(rng.uniform(-30, 30, (T, ld)))).astype(np.float32)
+    dev = torch.device("cuda", 0)
+    r = irs.topk_from_scores(torch.from_numpy(sc).to(dev), torch.from_numpy(cu).to(dev), c, budget)
+    irs.check_device_errors(dev)
+    np.testing.assert_array_equal(r.cpu().numpy(), O.routes_from_scores(sc, cu, T, c, budget))
+
+
+@pytest.mark.parametrize("c, budget, lens", [
+    (64, 1024, [2048]),                          # kb 16, rows up to 32 blocks (lanes without keys)
+    (4, 64, [1000, 24, 3000]),                   # kb 16, up to 750 blocks (KPL 32), a short document
+    (2, 2, [4100]),                              # kb 1, up to 2050 blocks (KPL 64)
+    (8, 256, [2048, 777]),                       # kb 32, up to 256 blocks (KPL 8)
+    (1, 20, [400, 1700]),                        # kb 20, up to 1700 blocks, c = 1
+    (3, 48, [1500]),                             # kb 16, c not a power of two
+])
+def test_topk_warp_variant_bit_exact(irs, c, budget, lens):
+    """The warp-per-row top-k (kb <= 32) on continuous scores, where the candidate ranking
+    decides, with a few rows of tied top scores mixed in (the bit-serial path): routes equal
+    the oracle's selection from the same FP32 scores."""
+    rng = np.random.default_rng(c * 1000 + budget)
+    T = sum(lens)
+    cu = np.zeros(len(lens) + 1, np.int32)
+    cu[1:] = np.cumsum(lens)
+    ld = max(lens) // c
+    sc = rng.standard_normal((T, ld)).astype(np.float32)
+    sc[::7, : ld // 2] = 3.0                      # many keys tied at the top of every 7th row
+    sc[1::11] = np.abs(sc[1::11])                 # some rows of positive scores only
     dev = torch.device("cuda", 0)
     r = irs.topk_from_scores(torch.from_numpy(sc).to(dev), torch.from_numpy(cu).to(dev), c, budget)
     irs.check_device_errors(dev)
