@@ -199,6 +199,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     const int nsparse = a.meta[2];
     if (lane == 0) { tma_prefetch_map(&tm_q); tma_prefetch_map(&tm_k); }
     uint32_t i = 0, nb = 0, at = 0;
+    int pst = 0;          // ring stage of atom `at`
+    uint32_t pph = 0;     // (at / S) & 1
     // the next tile's id is fetched one tile ahead, so the counter's round trip overlaps
     // the current tile's loads
     int next_id = 0;
@@ -231,13 +233,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         for (int j = 0; j < ti.nbt && ok; ++j) {
           const int bt = rot_tile(j, ti.jrot, ti.nbt);
           for (int ka = 0; ka < KATOMS; ++ka, ++at) {
-            const int st = at % S;
-            if (at >= (uint32_t)S && !mbar_wait(&a_empty[st], ((at / S) - 1) & 1, abort_flag, a.err)) {
+            if (at >= (uint32_t)S && !mbar_wait(&a_empty[pst], pph ^ 1u, abort_flag, a.err)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&a_full[st], kIdxAtom);
-            tma_load_2d(sA + (size_t)st * kIdxAtom, &tm_k, ka * AE, ti.blk0 + bt * kIdxM, &a_full[st]);
+            mbar_arrive_expect_tx(&a_full[pst], kIdxAtom);
+            tma_load_2d(sA + (size_t)pst * kIdxAtom, &tm_k, ka * AE, ti.blk0 + bt * kIdxM, &a_full[pst]);
+            if (++pst == S) { pst = 0; pph ^= 1u; }
           }
         }
       }
@@ -257,8 +259,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    // tcgen05.mma blocks once the tensor pipe's short queue is full, so whatever this
+    // thread does between two atoms' MMAs shows up as idle pipe time: the ring stage and
+    // its phase advance incrementally (no division by the runtime stage count) and the
+    // descriptors are a base plus an offset.
     if (lane == 0) {
-      uint32_t i = 0, nb = 0, at = 0, kt = 0;
+      uint32_t i = 0, nb = 0, kt = 0;
+      int st = 0;
+      uint32_t aph = 0;   // phase parity of the ring's current pass
+      const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA), 16, 1024);
+      const uint64_t b_desc0 = sdesc_sw128(smem_u32(sB), 16, 1024);
       bool alive = true;
       while (alive) {
         const int slot = i & (kTileSlots - 1);
@@ -269,22 +279,29 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         if (ti.kind == kTileStop) break;
         const int bs = nb & 1;
         if (!mbar_wait(&b_full[bs], (nb >> 1) & 1, abort_flag, a.err)) break;
-        const uint32_t b_base = smem_u32(sB + bs * L::kBBytes);
+        const uint64_t b_desc = b_desc0 + (uint64_t)((bs * L::kBBytes) >> 4);
         for (int j = 0; j < ti.nbt && alive; ++j, ++kt) {
           const int buf = kt & 1;
           if (kt >= 2 && !mbar_wait(&t_empty[buf], ((kt >> 1) - 1) & 1, abort_flag, a.err)) { alive = false; break; }
-          for (int ka = 0; ka < KATOMS; ++ka, ++at) {
-            const int st = at % S;
-            if (!mbar_wait(&a_full[st], (at / S) & 1, abort_flag, a.err)) { alive = false; break; }
+          // each atom's MMAs go out as soon as it has landed; the stages are released
+          // together at the end of the key tile, so no commit sits between two atoms' MMAs
+          int sts[KATOMS];
+#pragma unroll
+          for (int ka = 0; ka < KATOMS; ++ka) {
+            sts[ka] = st;
+            if (!mbar_wait(&a_full[st], aph, abort_flag, a.err)) { alive = false; break; }
+            if (++st == S) { st = 0; aph ^= 1u; }
             tc_fence_after();
-            const uint64_t ad = sdesc_sw128(smem_u32(sA + (size_t)st * kIdxAtom), 16, 1024);
-            const uint64_t bd = sdesc_sw128(b_base + ka * L::kBAtom, 16, 1024);
+            const uint64_t ad = a_desc0 + (uint64_t)((sts[ka] * kIdxAtom) >> 4);
+            const uint64_t bd = b_desc + (uint64_t)((ka * L::kBAtom) >> 4);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
               umma_op<F8>(tbase + buf * kIdxN, ad + (uint64_t)((ks * 32) >> 4), bd + (uint64_t)((ks * 32) >> 4), IDESC,
                         (ka > 0 || ks > 0) ? 1u : 0u);
-            umma_commit(&a_empty[st]);
           }
+          if (!alive) break;
+#pragma unroll
+          for (int ka = 0; ka < KATOMS; ++ka) umma_commit(&a_empty[sts[ka]]);
           if (!alive) break;
           umma_commit(&t_full[buf]);
         }
