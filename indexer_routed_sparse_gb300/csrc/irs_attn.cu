@@ -335,6 +335,8 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
     // wait gave up stops issuing and carries that into the next agreement.
     const int ptid = tid;
     uint32_t n = 0, u = 0, qi = 0;
+    int pst = 0;          // n % ST
+    uint32_t pph = 0;     // (n / ST) & 1
     bool mine = true;
     for (long long t = blockIdx.x; t < a.T; t += gridDim.x, ++qi) {
       const int b = qi & 1;
@@ -415,8 +417,11 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
         const __nv_bfloat16* kbase = a.k + (long long)(a.g0 + g) * a.k_sh;
         const __nv_bfloat16* vbase = a.v + (long long)(a.g0 + g) * a.v_sh;
         for (int c = 0; c < nchunks; ++c, ++n) {
-          const int st = n % ST;
-          if ((int)n >= ST && !mbar_wait(&B.kv_empty[st], ((n / ST) - 1) & 1, abort_flag, a.err)) { mine = false; break; }
+          // stage n % ST and the parity of use n / ST - 1, kept incrementally (no division)
+          const int st = pst;
+          const uint32_t par = pph ^ 1u;
+          if (++pst == ST) { pst = 0; pph ^= 1u; }
+          if ((int)n >= ST && !mbar_wait(&B.kv_empty[st], par, abort_flag, a.err)) { mine = false; break; }
           const int rows = min(kChunk, nv - c * kChunk);
           const int32_t* ids = sIdx + c * kChunk;
           uint8_t* stage = smem + (uint32_t)st * Ly.stage_bytes;
@@ -491,6 +496,8 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
     // chunk never queues behind S of a chunk whose stage has not landed.
     if (lane == 0) {
       uint32_t n = 0, u = 0, qi = 0;
+      int sst = 0;          // n % ST
+      uint32_t sph = 0;     // (n / ST) & 1
       bool alive = true;
       for (long long t = blockIdx.x; t < a.T && alive; t += gridDim.x, ++qi) {
         const int b = qi & 1;
@@ -504,8 +511,10 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           if (!mbar_wait(&B.q_full[qb], (u >> 1) & 1, abort_flag, a.err)) { alive = false; break; }
           const uint32_t qbase = smem_u32(sQ + qb * (kNH * a.Dqk * 2));
           for (int c = 0; c < nchunks; ++c, ++n) {
-            const int st = n % ST, sb = n & 1;
-            if (!mbar_wait(&B.kv_full[st], (n / ST) & 1, abort_flag, a.err)) { alive = false; break; }
+            const int st = sst, sb = n & 1;
+            const uint32_t par = sph;
+            if (++sst == ST) { sst = 0; sph ^= 1u; }
+            if (!mbar_wait(&B.kv_full[st], par, abort_flag, a.err)) { alive = false; break; }
             if (n >= 2 && !mbar_wait(&B.s_empty[sb], ((n >> 1) - 1) & 1, abort_flag, a.err)) { alive = false; break; }
             fence_proxy_async_smem();   // gathered rows (generic-proxy writes) -> UMMA reads
             tc_fence_after();
@@ -526,6 +535,7 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
     // its completion frees the P buffer and the K/V stage.
     if (lane == 0) {
       uint32_t m = 0, qi = 0;
+      int ost = 0;          // m % ST
       bool alive = true;
       for (long long t = blockIdx.x; t < a.T && alive; t += gridDim.x, ++qi) {
         const int b = qi & 1;
@@ -539,12 +549,14 @@ __global__ void __launch_bounds__(attn_threads(PW), 1) attn_fwd_kernel(const __g
           if (!mbar_wait(&B.p_full[pb], (m >> 1) & 1, abort_flag, a.err)) { alive = false; break; }
           if (m >= 2 && !mbar_wait(&B.o_empty[pb], ((m >> 1) - 1) & 1, abort_flag, a.err)) { alive = false; break; }
           tc_fence_after();
-          const uint8_t* stage = smem + (uint32_t)(m % ST) * Ly.stage_bytes;
+          const int ost_m = ost;
+          if (++ost == ST) ost = 0;
+          const uint8_t* stage = smem + (uint32_t)ost_m * Ly.stage_bytes;
           const uint32_t vb = smem_u32(a.v_alias ? stage : stage + Ly.k_bytes);
           issue_output_any(ndvb, tbase + 32 + pb * (kNH * kMaxDvBlocks), vb, smem_u32(sP + pb * (kNH * kChunk * 2)),
                            IDESC_O);
           umma_commit(&B.o_full[pb]);
-          umma_commit(&B.kv_empty[m % ST]);
+          umma_commit(&B.kv_empty[ost_m]);
         }
       }
       umma_commit(&drain[1]);
