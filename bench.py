@@ -456,7 +456,10 @@ def measure_indexer_variants(irs, wl, d, dev, stream, flush, peaks, steps: int) 
     W = budget + c - 1
     gen = torch.Generator(device=dev)
     gen.manual_seed(1234)
-    qg = torch.randn((T, G, Hi, Di), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    qg = torch.empty((T, G, Hi, Di), dtype=torch.bfloat16, device=dev)
+    for r0 in range(0, T, 4096):
+        r1 = min(T, r0 + 4096)
+        qg[r0:r1] = torch.randn((r1 - r0, G, Hi, Di), generator=gen, device=dev, dtype=torch.float32)
     wg = torch.rand((T, G, Hi), generator=gen, device=dev, dtype=torch.float32)
     z = (2.0 * torch.randn((T, Di), generator=gen, device=dev, dtype=torch.float32)).to(torch.bfloat16)
     fr = irs_synth.front_half_inputs(T, Di, 64, wl.cu_seqlens, seed=5)
@@ -553,6 +556,27 @@ def e2e_pipelined(path, steps: int, flush, stream, dev) -> float:
     end.record(s_out)
     end.synchronize()
     return start.elapsed_time(end) / steps
+
+
+def run_variants_only(args) -> dict:
+    """The indexer variants alone on the workload's indexer inputs (qI, kI, w, cu_seqlens)."""
+    import torch
+
+    import indexer_routed_sparse_gb300 as irs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    irs.lib()
+    wl = irs_synth.make(args.workload, small=args.small)
+    if wl.latent:
+        raise SystemExit("the latent workload has no indexer")
+    keys = ("qI", "kI", "w", "cu_seqlens")
+    host = irs_synth.as_torch(wl, device="cpu")
+    d = {k: host[k].to(dev) for k in keys}
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    variants = measure_indexer_variants(irs, wl, d, dev, torch.cuda.current_stream(dev), flush, load_peaks(),
+                                        max(3, min(args.steps, 20)))
+    return {"workload": describe(wl), "indexer_variants": variants}
 
 
 def run_gpu(args) -> dict | None:
@@ -950,12 +974,19 @@ def main(argv=None):
                     help="time only the headline workload (skip the other four)")
     ap.add_argument("--with-backward", action="store_true",
                     help="also time sparse_gqa_attn_bwd on the step's routes (reported under 'backward')")
+    ap.add_argument("--variants-only", action="store_true",
+                    help="time only the indexer rows beyond the plain one (front half, E4M3, per-group, "
+                         "Step-5 summaries) on the workload's indexer shape; a few GB on the device "
+                         "(profiler captures), not a bench line")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=150.0)
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "irs":
         args.warmup = 3
-    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if args.variants_only:
+        res = run_variants_only(args)
+    else:
+        res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 
