@@ -2,7 +2,8 @@
 
 The kernel gets the oracle's forward outputs (out rounded to bf16, as a forward saves
 it, and the FP32 lse) and an arbitrary bf16 output gradient; its dq, dk and dv are
-compared with the oracle's backward, per tensor:
+compared with the oracle's backward element by element, against bounds derived from the
+arithmetic (`grad_bounds`), and per tensor:
     dq, dk:  max |gpu - ref| <= 2e-2 max |ref| + 1e-4,  mean |gpu - ref| <= 5e-3 mean |ref| + 1e-5
     dv:      max |gpu - ref| <= 1e-4 max |ref| + 1e-6,  mean |gpu - ref| <= 2e-5 mean |ref| + 1e-7
 Reading: the kernel takes D = dO . out from the bf16 output, while the oracle sums
@@ -50,6 +51,54 @@ def check_grad(name, got, ref):
     assert err.mean() <= mean_rel * np.abs(ref).mean() + mean_abs, (name, err.mean(), np.abs(ref).mean())
 
 
+def grad_bounds(q, k, v, routes, scale, dout, out_bf16, rows=None, c=1e-4):
+    """Element-wise bounds on |kernel - oracle| for dq (the given rows), dk and dv, from the
+    arithmetic (reading R13). The kernel takes D = dO . out from the bf16 output, so a row's
+    ds_r = p_r (dp_r - D) is off by p_r dD with dD = dO . (out - bf16(out)): dq[h, d] moves by
+    scale dD sum_r p_r |K[r, d]| and dk[r, d] by scale p_r dD |q[h, d]|, both computed exactly
+    here. Everything else is FP32 rounding (probabilities from the FP32 lse and FP32 scores,
+    sums over at most a few thousand terms): c times the sums of the terms' magnitudes,
+    c = 1e-4, 10 to 100 times the FP32 worst case at these lengths. Empty rows bound to 0."""
+    T, Hq, Dqk = q.shape
+    Tk, Hkv, _ = k.shape
+    Dv = v.shape[2]
+    G = Hq // Hkv
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    qf, kf, vf, dO = O.bf16_to_f64(q), O.bf16_to_f64(k), O.bf16_to_f64(v), O.bf16_to_f64(dout)
+    ob = np.asarray(out_bf16, np.float64)
+    dq_b = np.zeros((rows.shape[0], Hq, Dqk))
+    dk_b = np.zeros((Tk, Hkv, Dqk))
+    dv_b = np.zeros((Tk, Hkv, Dv))
+    for i, t in enumerate(rows):
+        ids = np.asarray(routes[t], np.int64)
+        ids = ids[(ids >= 0) & (ids < Tk)]
+        if ids.shape[0] == 0:
+            continue
+        for h in range(Hq):
+            g = h // G
+            K, V = kf[ids, g], vf[ids, g]
+            sc = scale * (K @ qf[t, h])
+            p = np.exp(sc - sc.max())
+            p /= p.sum()
+            dp = V @ dO[t, h]
+            D = p @ dp
+            dD = abs(dO[t, h] @ (p @ V - ob[t, h]))
+            wgt = p * (np.abs(dp) + abs(D))
+            dq_b[i, h] = scale * (dD * (p @ np.abs(K)) + c * (wgt @ np.abs(K)))
+            np.add.at(dk_b[:, g], ids, scale * np.outer(p * dD + c * wgt, np.abs(qf[t, h])))
+            np.add.at(dv_b[:, g], ids, c * np.outer(p, np.abs(dO[t, h])))
+    return dq_b, dk_b, dv_b
+
+
+def check_grad_elementwise(name, got, ref, bound):
+    """|got - ref| <= 2 bound + 1e-7 in every element (bound from grad_bounds)."""
+    got = got.double().cpu().numpy() if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
+    err = np.abs(got - np.asarray(ref, np.float64))
+    lim = 2.0 * bound + 1e-7
+    bad = err > lim
+    assert not bad.any(), (name, int(bad.sum()), float((err / lim).max()), np.unravel_index(int(np.argmax(err / lim)), err.shape))
+
+
 def forward_outputs(q, k, v, routes, scale):
     out, lse = O.attention(q, k, v, routes, scale)
     return torch.from_numpy(out).to(torch.bfloat16).to(DEV), torch.from_numpy(lse).to(DEV)
@@ -88,6 +137,12 @@ def test_gqa_backward_matches_oracle(irs, T, Hq, Hkv, Dqk, Dv, W, lens, seed):
     check_grad("dq", dq, ref_dq)
     check_grad("dk", dk, ref_dk)
     check_grad("dv", dv, ref_dv)
+    # element by element, against bounds derived from the arithmetic
+    out_bf16 = torch.from_numpy(O.attention(q, k, v, routes, scale)[0]).to(torch.bfloat16).double().numpy()
+    bq, bk, bv = grad_bounds(q, k, v, routes, scale, dout, out_bf16)
+    check_grad_elementwise("dq", dq, ref_dq, bq)
+    check_grad_elementwise("dk", dk, ref_dk, bk)
+    check_grad_elementwise("dv", dv, ref_dv, bv)
 
 
 def test_gradients_are_added_to_the_given_buffers(irs):
@@ -122,6 +177,11 @@ def test_latent_backward_matches_oracle(irs):
     ref_dq, ref_dkv = O.latent_attention_bwd(q, kv, routes, scale, dout, Dv=Dv)
     check_grad("dq", dq, ref_dq)
     check_grad("dkv", dkv, ref_dkv)
+    out_bf16 = torch.from_numpy(out).to(torch.bfloat16).double().numpy()
+    bq, bk, bv = grad_bounds(q, kv, kv[:, :, :Dv], routes, scale, dout, out_bf16)
+    bk[:, :, :Dv] += bv
+    check_grad_elementwise("dq", dq, ref_dq, bq)
+    check_grad_elementwise("dkv", dkv, ref_dkv, bk)
 
 
 def test_single_key_empty_rows_and_bad_ids(irs):
@@ -137,6 +197,9 @@ def test_single_key_empty_rows_and_bad_ids(irs):
     ref = O.attention_bwd(q, k, v, r1, 0.2, dout)
     for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
         check_grad(name, got, want)
+    ob = torch.from_numpy(O.attention(q, k, v, r1, 0.2)[0]).to(torch.bfloat16).double().numpy()
+    for name, got, want, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, grad_bounds(q, k, v, r1, 0.2, dout, ob)):
+        check_grad_elementwise(name, got, want, b)
     # rows without keys give no gradient; an ID outside [-1, Tk) is padding and is reported
     r2 = irs_synth.random_routes(rng, T, Tk, 12, wl.cu_seqlens)
     r2[::3] = -1
@@ -148,6 +211,9 @@ def test_single_key_empty_rows_and_bad_ids(irs):
     assert torch.all(dq[::3] == 0)
     for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
         check_grad(name, got, want)
+    ob = torch.from_numpy(O.attention(q, k, v, r2, 0.2)[0]).to(torch.bfloat16).double().numpy()
+    for name, got, want, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, grad_bounds(q, k, v, r2, 0.2, dout, ob)):
+        check_grad_elementwise(name, got, want, b)
 
 
 def test_mid_backward_full_size(irs):
@@ -175,6 +241,9 @@ def test_mid_backward_full_size(irs):
     rows = np.unique(np.concatenate([[0, 1, 3, 2047, 2048, wl.T - 1], rng.integers(0, wl.T, 18)]))
     ref_dq, _, _ = O.attention_bwd(q, k, v, routes, wl.scale, dout, rows=rows)
     check_grad("dq", dq[torch.as_tensor(rows, device=DEV)], ref_dq)
+    out_np = out.double().cpu().numpy()
+    bq, _, _ = grad_bounds(q, k, v, routes, wl.scale, dout, out_np, rows=rows)
+    check_grad_elementwise("dq", dq[torch.as_tensor(rows, device=DEV)], ref_dq, bq)
     # sampled key rows: all of their query rows, so the oracle's dk / dv rows are complete
     ids = routes[routes >= 0]
     fan_in = np.bincount(ids, minlength=wl.T)
@@ -185,6 +254,9 @@ def test_mid_backward_full_size(irs):
     kidx = torch.as_tensor(keys, device=DEV)
     check_grad("dk", dk[kidx], ref_dk[keys])
     check_grad("dv", dv[kidx], ref_dv[keys])
+    _, bk, bv = grad_bounds(q, k, v, routes, wl.scale, dout, out_np, rows=users)
+    check_grad_elementwise("dk", dk[kidx], ref_dk[keys], bk[keys])
+    check_grad_elementwise("dv", dv[kidx], ref_dv[keys], bv[keys])
     # invariants over every key row (float64 sums of the FP32 gradients)
     G = wl.Hq // wl.Hkv
     dO = O.bf16_to_f64(dout).reshape(wl.T, wl.Hkv, G, wl.Dv).sum(axis=(0, 2))       # [Hkv, Dv]
