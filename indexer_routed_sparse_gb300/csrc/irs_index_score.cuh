@@ -106,6 +106,24 @@ static __device__ TileInfo decode_tile(const IndexArgs& a, int id, int nsparse) 
   return ti;
 }
 
+// Packed FP32 pairs (sm_100+ f32x2 arithmetic): x in the low half, y in the high half.
+__device__ __forceinline__ uint64_t pack2(float x, float y) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+// a * b + c on both halves, each rounded to nearest
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
 __device__ __forceinline__ float w4f(const float4* w4, int k) {
   const float4 v = w4[k >> 2];
   return (k & 3) == 0 ? v.x : ((k & 3) == 1 ? v.y : ((k & 3) == 2 ? v.z : v.w));
@@ -375,16 +393,32 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             constexpr int CH = G < 4 ? G : 4;      // independent chains per query
 #pragma unroll
             for (int q0 = 0; q0 < 32; q0 += G) {
-              float acc4[CH];
+              if constexpr (G >= 4) {
+                // two packed chains (heads 4j, 4j+1 and 4j+2, 4j+3): one f32x2 FMA per two
+                // columns after the scalar ReLU
+                uint64_t acc2[2] = {0ull, 0ull};
 #pragma unroll
-              for (int x = 0; x < CH; ++x) acc4[x] = 0.f;
+                for (int k = 0; k < G; k += 4) {
+                  const float4 wq = w4[(q0 + k) >> 2];
+                  acc2[0] = ffma2(pack2(wq.x, wq.y), pack2(fmaxf(v[c4][q0 + k], 0.f), fmaxf(v[c4][q0 + k + 1], 0.f)),
+                                  acc2[0]);
+                  acc2[1] = ffma2(pack2(wq.z, wq.w),
+                                  pack2(fmaxf(v[c4][q0 + k + 2], 0.f), fmaxf(v[c4][q0 + k + 3], 0.f)), acc2[1]);
+                }
+                const float2 a0 = unpack2(acc2[0]), a1 = unpack2(acc2[1]);
+                prod[q0] = (a0.x + a1.x) + (a0.y + a1.y);
+              } else {
+                float acc4[CH];
 #pragma unroll
-              for (int k = 0; k < G; ++k)
-                acc4[k % CH] = fmaf(w4f(w4, q0 + k), fmaxf(v[c4][q0 + k], 0.f), acc4[k % CH]);
-              float sum = acc4[0];
+                for (int x = 0; x < CH; ++x) acc4[x] = 0.f;
 #pragma unroll
-              for (int x = 1; x < CH; ++x) sum += acc4[x];
-              prod[q0] = sum;
+                for (int k = 0; k < G; ++k)
+                  acc4[k % CH] = fmaf(w4f(w4, q0 + k), fmaxf(v[c4][q0 + k], 0.f), acc4[k % CH]);
+                float sum = acc4[0];
+#pragma unroll
+                for (int x = 1; x < CH; ++x) sum += acc4[x];
+                prod[q0] = sum;
+              }
             }
             if constexpr (HI <= 32) {
 #pragma unroll
