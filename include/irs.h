@@ -130,10 +130,11 @@ irs_status irs_sparse_index_score_topk(const void* qI, const void* kI, const flo
  * operands are reproducible bit for bit. Scoring, top-k and routes are then those of
  * irs_sparse_index_score_topk.
  *
- * q_weight, k_weight  fp32 [Di] DEVICE
+ * q_weight, k_weight  fp32 [Di] DEVICE, 16-byte aligned
  * eps                 >= 0
- * rope                fp32 [T, rope_dims] DEVICE: row t = cat(cos, sin) for token t (the
- *                     caller composes it for document-local positions); NULL if rope_dims = 0
+ * rope                fp32 [T, rope_dims] DEVICE, 16-byte aligned: row t = cat(cos, sin) for
+ *                     token t (the caller composes it for document-local positions); NULL if
+ *                     rope_dims = 0
  * rope_dims           a multiple of 16 in [0, Di]
  * workspace           at least irs_index_front_workspace_bytes(...) bytes (the plain
  *                     indexer's scratch plus the transformed queries [T, Hi, Di] bf16 and the

@@ -212,6 +212,8 @@ namespace {
 irs_status check_front(const float* q_weight, const float* k_weight, float eps, const float* rope, int rope_dims,
                        int Di) {
   if (!q_weight || !k_weight) return fail(IRS_ERR_VALUE, "NULL RMSNorm weights");
+  if (!aligned16(q_weight) || !aligned16(k_weight) || (rope != nullptr && !aligned16(rope)))
+    return fail(IRS_ERR_VALUE, "RMSNorm weights and the rotary table must be 16-byte aligned");
   if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(IRS_ERR_VALUE, "eps must be finite and >= 0");
   if (rope_dims < 0 || rope_dims > Di || rope_dims % 16 != 0)
     return fail(IRS_ERR_VALUE, "rope_dims must be a multiple of 16 in [0, Di] (got %d)", rope_dims);

@@ -317,26 +317,32 @@ __device__ __forceinline__ void front_row(const In* x, int Di, const float* __re
   }
   const float r = __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)Di), eps));
   const int h = rope_dims >> 1;
+  // weights and rotary values by 16-byte loads (the C ABI requires 16-byte alignment of
+  // both tables; every offset below is a multiple of 8 floats)
   for (int d0 = 0; d0 < h; d0 += 8) {
-    float a[8], b[8], ya[8], yb[8];
+    float a[8], b[8], ya[8], yb[8], wa[8], wb[8], cs[8], sn[8];
     load8<In>(x + d0, a);
     load8<In>(x + d0 + h, b);
+    load8<float>(wt + d0, wa);
+    load8<float>(wt + d0 + h, wb);
+    load8<float>(rope + d0, cs);
+    load8<float>(rope + h + d0, sn);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float y1 = __fmul_rn(__fdiv_rn(a[i], r), __ldg(wt + d0 + i));
-      const float y2 = __fmul_rn(__fdiv_rn(b[i], r), __ldg(wt + d0 + h + i));
-      const float cs = __ldg(rope + d0 + i), sn = __ldg(rope + h + d0 + i);
-      ya[i] = __fsub_rn(__fmul_rn(y1, cs), __fmul_rn(y2, sn));
-      yb[i] = __fadd_rn(__fmul_rn(y2, cs), __fmul_rn(y1, sn));
+      const float y1 = __fmul_rn(__fdiv_rn(a[i], r), wa[i]);
+      const float y2 = __fmul_rn(__fdiv_rn(b[i], r), wb[i]);
+      ya[i] = __fsub_rn(__fmul_rn(y1, cs[i]), __fmul_rn(y2, sn[i]));
+      yb[i] = __fadd_rn(__fmul_rn(y2, cs[i]), __fmul_rn(y1, sn[i]));
     }
     *reinterpret_cast<uint4*>(out + d0) = pack8(ya);
     *reinterpret_cast<uint4*>(out + d0 + h) = pack8(yb);
   }
   for (int d0 = rope_dims; d0 < Di; d0 += 8) {
-    float a[8];
+    float a[8], wa[8];
     load8<In>(x + d0, a);
+    load8<float>(wt + d0, wa);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = __fmul_rn(__fdiv_rn(a[i], r), __ldg(wt + d0 + i));
+    for (int i = 0; i < 8; ++i) a[i] = __fmul_rn(__fdiv_rn(a[i], r), wa[i]);
     *reinterpret_cast<uint4*>(out + d0) = pack8(a);
   }
 }

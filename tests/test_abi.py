@@ -170,6 +170,8 @@ def test_front_half_validation_is_value_error(lib):
     assert call(qw=None) == 2 and b"RMSNorm" in lib.irs_last_error()
     assert call(eps=-1.0) == 2 and b"eps" in lib.irs_last_error()
     assert call(rope=None) == 2 and b"rotary" in lib.irs_last_error()
+    assert call(qw=p + 4) == 2 and b"16-byte aligned" in lib.irs_last_error()
+    assert call(rope=p + 8) == 2 and b"16-byte aligned" in lib.irs_last_error()
     assert lib.irs_index_front_workspace_bytes(64, 4, 64, 4, 16, 1, 64, 1) > lib.irs_index_workspace_bytes(
         64, 4, 64, 4, 16, 1, 64, 1)
 
