@@ -511,13 +511,14 @@ def measure_indexer_variants(irs, wl, d, dev, stream, flush, peaks, steps: int) 
     return out
 
 
-def e2e_pipelined(path, steps: int, flush, stream, dev) -> float:
+def e2e_pipelined(path, steps: int, flush, stream, dev, warmup: int = 2) -> float:
     """Mean ms per step end to end through the public API with host buffers, copies
     overlapped with compute: inputs and outputs are double-buffered on the device; step
     i+1's host-to-device copies (pinned memory, their own stream) and step i-1's
     device-to-host copies (another stream) run while step i computes. Every step copies
     all of its inputs in and its outputs (out, lse) back; L2 is flushed before each step's
-    compute. Timed from the first copy's start to the last copy's end."""
+    compute. The first `warmup` steps (which touch every buffer once) run untimed; the
+    timed region runs from the first timed step's first copy to the last copy's end."""
     import torch
 
     host = path.host
@@ -530,9 +531,12 @@ def e2e_pipelined(path, steps: int, flush, stream, dev) -> float:
     in_ready, in_free, done, out_free = [ev(), ev()], [ev(), ev()], [ev(), ev()], [ev(), ev()]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
-    start.record(s_in)
-    for i in range(steps):
+    for i in range(warmup + steps):
         b = i & 1
+        if i == warmup:
+            s_in.wait_stream(s_out)                # the warm-up steps have left the device
+            s_in.wait_stream(stream)
+            start.record(s_in)
         with torch.cuda.stream(s_in):
             if i >= 2:
                 s_in.wait_event(in_free[b])        # step i-2 no longer reads this input set
@@ -637,6 +641,15 @@ def run_gpu(args) -> dict | None:
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
     e2e_steps = max(3, args.steps // 2)
     ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(e2e_steps)]
+    # untimed warm-up steps: the first copies into freshly pinned buffers pay for the
+    # buffers' first use, which is not a per-step cost
+    for _ in range(2):
+        for k_, v_ in host.items():
+            path.d[k_].copy_(v_, non_blocking=True)
+        path.index()
+        path.attend()
+        out_h.copy_(path.out, non_blocking=True)
+        lse_h.copy_(path.lse, non_blocking=True)
     barrier(world)
     torch.cuda.synchronize(dev)
     for i in range(e2e_steps):
