@@ -72,6 +72,10 @@ notes of the repository):
       (max subtracted, sequential sums in token order, one division), then bf16,
       then E4M3. The exponential is `exp_f32`, a stated FP32 evaluation, so that
       the codes it decides are reproducible.
+* R18 Indexer projections: one bf16 weight matrix W [(Hi+1)*Di + Hi, H]; output
+      columns [0, Hi*Di) are the queries (head-major), then the raw keys, then the
+      Hi signed head weights; exact dot products rounded once, to bf16 (queries,
+      keys) or FP32 (head weights).
 * The FP32 mean is a sequential FP32 sum over the c rows of the block in
   ascending token order, followed by one IEEE division by c.
 * Route entries outside [0, Tk) are padding.
@@ -174,6 +178,51 @@ def pool_keys(kI_bits: np.ndarray, cu_seqlens: np.ndarray, c: int) -> tuple[np.n
     Di = kI_bits.shape[1]
     kbar = np.concatenate(blocks, axis=0) if blocks else np.zeros((0, Di), np.float32)
     return kbar, np.asarray(blk_off, dtype=np.int64)
+
+
+# --------------------------------------------------------------------------------------
+# a0: the indexer's projections (QSA page, indexer class: one fused projection gives the
+# raw query/key layout [B, S, (H_index + 1) * D_index], split into queries
+# [B, S, H_index, D_index] and raw keys [B, S, 1, D_index]; Step-5 sparse page,
+# `Step5IndexerWeightProjection`: FP32 source weights, a BF16 projection, signed FP32 head
+# weights). Reading R18: one bf16 weight matrix W [(Hi+1)*Di + Hi, H], row n giving output
+# column n; columns [0, Hi*Di) are the queries (head-major), [Hi*Di, (Hi+1)*Di) the raw
+# keys, the last Hi the head weights. Each output is the exact dot product of the bf16
+# operands, rounded once: to bf16 for queries and keys, to FP32 for the head weights.
+# --------------------------------------------------------------------------------------
+
+
+def round_f64_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Nearest bf16 value of each float64, ties to even, in one rounding (no detour through
+    float32). bf16 keeps 8 significant bits: with |x| = m * 2^e, 0.5 <= m < 1, its spacing
+    is 2^(e-8). Returns float64 (normal magnitudes; the projection's outputs are)."""
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(np.abs(x))
+    q = np.ldexp(1.0, e - 8)
+    return np.copysign(np.round(np.abs(x) / q) * q, x)
+
+
+def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of float64 values that are exact in bf16."""
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float32))
+    return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def project_indexer(hidden_bits: np.ndarray, W_bits: np.ndarray, Hi: int, Di: int):
+    """Indexer inputs from hidden states (reading R18): hidden [T, H] and W
+    [(Hi+1)*Di + Hi, H] bf16 bits. Returns qI bits [T, Hi, Di], kI bits [T, Di] (bf16) and
+    w float32 [T, Hi]. The dot products are taken in float64 (a library matmul of exact
+    bf16 values; its rounding error is below 2^-40 of the terms' magnitude here)."""
+    T, H = hidden_bits.shape
+    N = W_bits.shape[0]
+    if N != (Hi + 1) * Di + Hi or W_bits.shape[1] != H:
+        raise ValueError("W must be [(Hi+1)*Di + Hi, H]")
+    y = bf16_to_f64(hidden_bits) @ bf16_to_f64(W_bits).T
+    qk = f64_to_bf16_bits(round_f64_to_bf16(y[:, :(Hi + 1) * Di]))
+    qI = np.ascontiguousarray(qk[:, :Hi * Di].reshape(T, Hi, Di))
+    kI = np.ascontiguousarray(qk[:, Hi * Di:])
+    w = y[:, (Hi + 1) * Di:].astype(np.float32)
+    return qI, kI, w
 
 
 # --------------------------------------------------------------------------------------

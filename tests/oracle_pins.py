@@ -1038,6 +1038,71 @@ def pin_summary_scores(O):
                 assert sc[t, b] == want, (operands, t, b)
 
 
+def pin_round_f64_to_bf16(O):
+    """Direct float64 -> bf16 rounding: equals torch's cast on values exact in float32 (where
+    no double rounding can occur), and the hand-worked cases where float64 bits below float32
+    precision decide a tie (1 + 2^-8 is a tie, rounded to even 1.0; 1 + 2^-8 + 2^-40 is
+    above it, 1 + 2^-7)."""
+    rng = np.random.default_rng(50)
+    x = (rng.standard_normal(20000) * np.exp2(rng.uniform(-20, 20, 20000))).astype(np.float32).astype(np.float64)
+    ties = (np.arange(0, 128, dtype=np.float64) * 2.0 + 1.0) * 2.0 ** -8 + 1.0   # 1 + odd * 2^-8: halfway cases
+    for v in (x, ties[ties < 2.0], -ties[ties < 2.0]):
+        want = torch.from_numpy(v).to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+        np.testing.assert_array_equal(O.round_f64_to_bf16(v), want)
+    cases = {1.0 + 2.0 ** -8: 1.0, 1.0 + 2.0 ** -8 + 2.0 ** -40: 1.0 + 2.0 ** -7,
+             1.0 + 3 * 2.0 ** -8 - 2.0 ** -40: 1.0 + 2.0 ** -7, -(2.0 + 2.0 ** -7 + 2.0 ** -45): -(2.0 + 2.0 ** -6)}
+    for v, want in cases.items():
+        assert O.round_f64_to_bf16(np.asarray([v]))[0] == want, (v, want)
+
+
+def _projection_fixture(Hi=3, Di=8, H=16, T=12, seed=51):
+    rng = np.random.default_rng(seed)
+    N = (Hi + 1) * Di + Hi
+    # weights: small integers times 2^-3 (exact in bf16); row n gets a value that encodes n
+    Wv = (rng.integers(-8, 9, (N, H)) / 8.0).astype(np.float32)
+    return rng, T, H, Hi, Di, N, Wv
+
+
+def pin_projection_one_hot(O):
+    """One-hot hidden rows pick one column of W: qI[t, h, d] = W[h*Di + d, j], kI[t, d] =
+    W[Hi*Di + d, j], w[t, h] = W[(Hi+1)*Di + h, j], all exact (head-major queries, then keys,
+    then head weights)."""
+    rng, T, H, Hi, Di, N, Wv = _projection_fixture()
+    j = rng.integers(0, H, T)
+    hid = np.zeros((T, H), np.float32)
+    hid[np.arange(T), j] = 1.0
+    qI, kI, w = O.project_indexer(exact_bf16_bits(hid), exact_bf16_bits(Wv), Hi, Di)
+    for t in range(T):
+        col = Wv[:, j[t]]
+        np.testing.assert_array_equal(bits_to_f64(qI[t]), col[:Hi * Di].reshape(Hi, Di).astype(np.float64))
+        np.testing.assert_array_equal(bits_to_f64(kI[t]), col[Hi * Di:(Hi + 1) * Di].astype(np.float64))
+        np.testing.assert_array_equal(w[t], col[(Hi + 1) * Di:])
+
+
+def pin_projection_sums(O):
+    """Two-hot hidden rows (a at column i, b at column j, exact in bf16): every output is
+    a*W[n, i] + b*W[n, j], computed here in exact rationals; queries and keys are that sum
+    rounded once to bf16 (torch's cast of the exact value, which these sums keep exact in
+    float32), head weights the sum itself."""
+    rng, T, H, Hi, Di, N, Wv = _projection_fixture(seed=52)
+    hid = np.zeros((T, H), np.float32)
+    ii = rng.integers(0, H // 2, T)
+    jj = rng.integers(H // 2, H, T)
+    av = np.asarray([1.0, -1.5, 0.375, 3.0], np.float32)[rng.integers(0, 4, T)]
+    bv = np.asarray([1.0, 2.5, -0.75, 0.0078125], np.float32)[rng.integers(0, 4, T)]
+    hid[np.arange(T), ii] = av
+    hid[np.arange(T), jj] = bv
+    qI, kI, w = O.project_indexer(exact_bf16_bits(hid), exact_bf16_bits(Wv), Hi, Di)
+    for t in range(T):
+        exact = [Fraction(float(av[t])) * Fraction(float(Wv[n, ii[t]])) + Fraction(float(bv[t])) * Fraction(float(Wv[n, jj[t]]))
+                 for n in range(N)]
+        ex = np.asarray([float(e) for e in exact])
+        qk = torch.from_numpy(ex[:(Hi + 1) * Di].astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+        np.testing.assert_array_equal(bits_to_f64(qI[t]).ravel(), qk[:Hi * Di])
+        np.testing.assert_array_equal(bits_to_f64(kI[t]), qk[Hi * Di:])
+        np.testing.assert_array_equal(w[t].astype(np.float64), ex[(Hi + 1) * Di:])
+
+
 ALL_PINS = [
     pin_golden_two_docs,
     pin_golden_head_weights,
@@ -1074,4 +1139,7 @@ ALL_PINS = [
     pin_summaries_softmax_fp64,
     pin_summaries_two_tokens,
     pin_summary_scores,
+    pin_round_f64_to_bf16,
+    pin_projection_one_hot,
+    pin_projection_sums,
 ]

@@ -295,6 +295,25 @@ def _summaries_one_rounding(kI_bits, z_bits, cu_seqlens, c):
     return O.round_to_e4m3(sm.astype(np.float64)), offs
 
 
+def _round_via_f32(x):
+    return O.round_to_bf16(np.asarray(x, np.float64).astype(np.float32)).astype(np.float64)
+
+
+def _project_variant(keys_first=False, weights_bf16=False):
+    def proj(hidden_bits, W_bits, Hi, Di):
+        T = hidden_bits.shape[0]
+        y = O.bf16_to_f64(hidden_bits) @ O.bf16_to_f64(W_bits).T
+        qk = O.f64_to_bf16_bits(O.round_f64_to_bf16(y[:, :(Hi + 1) * Di]))
+        if keys_first:
+            kI, qI = qk[:, :Di], qk[:, Di:].reshape(T, Hi, Di)
+        else:
+            qI, kI = qk[:, :Hi * Di].reshape(T, Hi, Di), qk[:, Hi * Di:]
+        w = y[:, (Hi + 1) * Di:]
+        w = (O.round_f64_to_bf16(w) if weights_bf16 else w).astype(np.float32)
+        return np.ascontiguousarray(qI), np.ascontiguousarray(kI), w
+    return proj
+
+
 _REAL_ATTEND = O.attend_row
 _REAL_GROUPED_ATTN = O.attention_grouped
 _REAL_COMPOSE = O.compose_window
@@ -349,6 +368,9 @@ MUTATIONS = {
     "summary_negated_logits": ("summarize_doc", _summary_variant(sign=-1.0)),
     "summaries_ignore_documents": ("region_summaries", _summaries_ignore_docs),
     "summaries_one_rounding": ("region_summaries_e4m3", _summaries_one_rounding),
+    "bf16_rounding_via_float32": ("round_f64_to_bf16", _round_via_f32),
+    "projection_keys_first": ("project_indexer", _project_variant(keys_first=True)),
+    "projection_weights_rounded_to_bf16": ("project_indexer", _project_variant(weights_bf16=True)),
 }
 
 
