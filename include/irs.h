@@ -206,6 +206,32 @@ irs_status irs_sparse_index_score_topk_e4m3(const void* qI, const void* kI, cons
                                             size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream);
 
 /*
+ * The indexer's projections: queries, raw keys and signed head weights from hidden states.
+ *
+ * QSA page, the indexer class (`Qwen3_8_FlashNextQSAIndexer`): one fused projection gives
+ * the raw query/key layout [B, S, (H_index + 1) * D_index], split into queries
+ * [B, S, H_index, D_index] and raw keys [B, S, 1, D_index]. Step-5 sparse page,
+ * `Step5IndexerWeightProjection`: FP32 source weights matched by a BF16 projection give
+ * signed FP32 head weights. Here one weight matrix holds all three (N = (Hi+1)*Di + Hi):
+ *   out[t, n] = sum_k hidden[t, k] * weight[n, k]   (products of bf16 values, FP32 sums)
+ *   qI[t, h, d] = bf16(out[t, h*Di + d])             (round to nearest even)
+ *   kI[t, d]    = bf16(out[t, Hi*Di + d])
+ *   w[t, h]     = out[t, (Hi+1)*Di + h]              (FP32)
+ * It runs as one tcgen05 GEMM (128 tokens x 256 columns per tile, K in 64-wide steps).
+ *
+ * hidden  bf16 [T, H] contiguous, 16-byte aligned; H a positive multiple of 8
+ * weight  bf16 [N, H] contiguous, 16-byte aligned (row n gives output column n)
+ * qI      bf16 [T, Hi, Di] out, 16-byte aligned; Di a positive multiple of 8
+ * kI      bf16 [T, Di] out, 16-byte aligned
+ * w       fp32 [T, Hi] out
+ * Errors: IRS_ERR_VALUE for NULL or unaligned pointers and unsupported sizes, before any
+ * work is queued; IRS_ERR_RUNTIME when a launch fails. err_flag as elsewhere (a bounded
+ * wait that gave up).
+ */
+irs_status irs_indexer_projection(const void* hidden, const void* weight, int T, int H, int Hi, int Di, void* qI,
+                                  void* kI, float* w, int32_t* err_flag, irs_stream_t stream);
+
+/*
  * Step-5 learned-logit region summaries.
  *
  * Step-5 sparse page: `Step5SparseIndexer.project_keys` returns the index keys and

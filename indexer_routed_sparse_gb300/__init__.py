@@ -9,6 +9,7 @@ this package is its thin Python binding. Names follow the C entry points:
 * ``topk_from_scores(scores, cu_seqlens, c, budget) -> route_ids``
 * ``compose_window_routes(route_ids, cu_seqlens, window) -> route_ids``
 * ``sparse_index_score_topk_grouped`` / ``sparse_gqa_attn_fwd_grouped``: per-KV-group routes
+* ``indexer_projection(hidden, weight, Hi, Di) -> (qI, kI, w)``: the indexer's projections
 * ``region_summaries(kI, z, cu_seqlens, c)`` and ``sparse_index_score_topk_summaries``:
   Step-5 learned-logit region summaries and the indexer that scores them
 """
@@ -24,6 +25,7 @@ from ._binding import (  # noqa: F401
     exported_symbols,
     index_front_operands,
     index_workspace_bytes,
+    indexer_projection,
     lib,
     read_device_errors,
     region_summaries,

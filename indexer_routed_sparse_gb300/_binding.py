@@ -53,6 +53,7 @@ _SIGNATURES = {
     "irs_index_summaries_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I]),
     "irs_sparse_index_score_topk_summaries": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P,
                                                    _I64, _P, _SZ, _P, _P]),
+    "irs_indexer_projection": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "irs_topk_from_scores": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "irs_compose_window_routes": (_I, [_P, _I, _P, _I, _I, _I, _P, _P, _P]),
     "irs_sparse_gqa_attn_fwd": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I, _I, _I, _I, _I, _I,
@@ -494,6 +495,36 @@ def sparse_index_score_topk_grouped(qI: torch.Tensor, kI: torch.Tensor, w: torch
         _ptr(scores_out), ld, _ptr(ws), ws.numel(), _ptr(err), _stream(dev))
     _check(st, "sparse_index_score_topk_grouped")
     return out
+
+
+def indexer_projection(hidden: torch.Tensor, weight: torch.Tensor, Hi: int, Di: int, *,
+                       out: tuple | None = None, err: torch.Tensor | None = None):
+    """The indexer's queries, raw keys and signed head weights from hidden states:
+    (qI bf16 [T, Hi, Di], kI bf16 [T, Di], w fp32 [T, Hi]).
+
+    hidden bf16 [T, H]; weight bf16 [(Hi+1)*Di + Hi, H] (row n gives output column n:
+    queries head-major, then keys, then head weights).
+    """
+    _need(hidden, "hidden", torch.bfloat16, 2)
+    _need(weight, "weight", torch.bfloat16, 2)
+    T, H = hidden.shape
+    N = (Hi + 1) * Di + Hi
+    if tuple(weight.shape) != (N, H):
+        raise ValueError(f"weight must be [(Hi+1)*Di + Hi, H] = [{N}, {H}], got {tuple(weight.shape)}")
+    if not (hidden.is_contiguous() and weight.is_contiguous()):
+        raise ValueError("hidden and weight must be contiguous")
+    dev = hidden.device
+    if out is None:
+        out = (torch.empty((T, Hi, Di), dtype=torch.bfloat16, device=dev),
+               torch.empty((T, Di), dtype=torch.bfloat16, device=dev),
+               torch.empty((T, Hi), dtype=torch.float32, device=dev))
+    qI, kI, w = out
+    if err is None:
+        err = device_error_flag(dev)
+    st = lib().irs_indexer_projection(_ptr(hidden), _ptr(weight), T, H, Hi, Di, _ptr(qI), _ptr(kI), _ptr(w),
+                                      _ptr(err), _stream(dev))
+    _check(st, "indexer_projection")
+    return qI, kI, w
 
 
 def region_summaries(kI: torch.Tensor, z: torch.Tensor, cu_seqlens: torch.Tensor, c: int, *,

@@ -33,6 +33,7 @@ struct DeviceInfo {
   int num_sms = 0;
   size_t l2_bytes = 0;
   size_t score_smem = 0, topk_smem = 0, attn_smem = 0, mla_smem = 0, bwd_smem = 0;   // largest configured so far
+  bool proj_configured = false;
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -372,6 +373,35 @@ irs_status irs_region_summaries(const void* kI, const void* z, const int32_t* cu
                                              Di, c, static_cast<uint8_t*>(workspace), err_flag,
                                              static_cast<__nv_bfloat16*>(out), reinterpret_cast<cudaStream_t>(stream)),
                        "launching the region summaries");
+}
+
+irs_status irs_indexer_projection(const void* hidden, const void* weight, int T, int H, int Hi, int Di, void* qI,
+                                  void* kI, float* w, int32_t* err_flag, irs_stream_t stream) {
+  if (T < 1 || H < 8 || H % 8 != 0) return fail(IRS_ERR_VALUE, "need T >= 1 and H a positive multiple of 8");
+  if (Hi < 1 || Di < 8 || Di % 8 != 0) return fail(IRS_ERR_VALUE, "need Hi >= 1 and Di a positive multiple of 8");
+  const long long N = (long long)(Hi + 1) * Di + Hi;
+  if (N >= (1LL << 24) || (long long)T * N >= (1LL << 40)) return fail(IRS_ERR_VALUE, "projection too large");
+  if (!hidden || !weight || !qI || !kI || !w) return fail(IRS_ERR_VALUE, "NULL tensor pointer");
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(qI) || !aligned16(kI))
+    return fail(IRS_ERR_VALUE, "hidden, weight, qI and kI must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(w) & 3u) != 0) return fail(IRS_ERR_VALUE, "w must be 4-byte aligned");
+  DeviceInfo* dev = nullptr;
+  irs_status s = current_device(&dev);
+  if (s != IRS_OK) return s;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!dev->proj_configured) {
+      if ((s = launch_status(irs::configure_proj_kernel(), "configuring the projection")) != IRS_OK) return s;
+      dev->proj_configured = true;
+    }
+  }
+  CUtensorMap tm_x, tm_w;
+  if ((s = make_tmap(&tm_x, hidden, (uint64_t)H, (uint64_t)T, 128)) != IRS_OK) return s;
+  if ((s = make_tmap(&tm_w, weight, (uint64_t)H, (uint64_t)N, 256)) != IRS_OK) return s;
+  irs::ProjArgs a{T, H, (int)N, Hi, Di, static_cast<__nv_bfloat16*>(qI), static_cast<__nv_bfloat16*>(kI), w,
+                  err_flag, (T + 127) / 128, (int)((N + 255) / 256)};
+  return launch_status(irs::launch_proj(tm_x, tm_w, a, dev->num_sms, reinterpret_cast<cudaStream_t>(stream)),
+                       "launching the projection");
 }
 
 irs_status irs_index_front_operands(const void* qI, const void* kI, const int32_t* cu_seqlens, int ndocs,

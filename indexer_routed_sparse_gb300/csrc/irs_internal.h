@@ -73,6 +73,22 @@ cudaError_t launch_topk_from_scores(const float* scores, int64_t ldS, const int3
 cudaError_t launch_compose_window(const int32_t* route, int W, const int32_t* cu, int ndocs, int T, int window,
                                   int32_t* out, int32_t* err, cudaStream_t stream);
 
+// The indexer's projections (one GEMM): out[T, N] = X[T, H] . W[N, H]^T with N =
+// (Hi+1)*Di + Hi; columns [0, Hi*Di) -> qI (bf16), the next Di -> kI (bf16), the last Hi
+// -> w (fp32).
+struct ProjArgs {
+  int T, H, N, Hi, Di;
+  __nv_bfloat16* qI;
+  __nv_bfloat16* kI;
+  float* w;
+  int32_t* err;
+  int tiles_m, tiles_n;
+};
+size_t proj_smem_bytes();
+cudaError_t configure_proj_kernel();
+cudaError_t launch_proj(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const ProjArgs& a, int num_sms,
+                        cudaStream_t stream);
+
 // Gathered sparse attention.
 constexpr int kMaxKvMaps = 8;   // KV heads handled by one launch (one row-tile map per head)
 

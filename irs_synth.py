@@ -255,6 +255,21 @@ def front_half_inputs(T: int, Di: int, rope_dims: int, cu_seqlens: np.ndarray, s
     return dict(q_weight=q_weight, k_weight=k_weight, eps=eps, rope=rope)
 
 
+def projection_inputs(T: int, H: int, Hi: int, Di: int, seed: int = 0) -> tuple[np.ndarray, np.ndarray]:
+    """Hidden states and the indexer's projection weights, bf16 bits: hidden [T, H] ~ N(0, 1)
+    and weight [(Hi+1)*Di + Hi, H] ~ N(0, 1/H), so every projected value is about N(0, 1).
+    Synthetic stand-ins for a model's activations and trained weights."""
+    rng = np.random.default_rng(seed)
+    hidden = np.empty((T, H), dtype=np.uint16)
+    for r0 in range(0, T, _DRAW_ROWS):
+        r1 = min(T, r0 + _DRAW_ROWS)
+        hidden[r0:r1] = f32_to_bf16_bits(rng.standard_normal((r1 - r0, H), dtype=np.float32))
+    N = (Hi + 1) * Di + Hi
+    weight = f32_to_bf16_bits((rng.standard_normal((N, H), dtype=np.float32) * np.float32(1.0 / np.sqrt(H)))
+                              .astype(np.float32))
+    return hidden, weight
+
+
 def compression_logits(T: int, Di: int, seed: int = 0, scale: float = 2.0) -> np.ndarray:
     """Step-5 compression logits shaped like the index keys: bf16 bits [T, Di] of
     scale * N(0, 1). scale 2 gives softmax weights that are neither flat nor one-hot over a

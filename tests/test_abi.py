@@ -202,3 +202,19 @@ def test_summaries_validation_is_value_error(lib):
     assert st == 2 and b"aligned" in lib.irs_last_error()
     st = lib.irs_region_summaries(p, p, p, 1, 64, 64, 128, 4, p, p, 16, None, None)
     assert st == 2 and b"workspace too small" in lib.irs_last_error()
+
+
+def test_projection_validation_is_value_error(lib):
+    import ctypes as C
+    buf = C.create_string_buffer(512)
+    p = C.addressof(buf) + (256 - C.addressof(buf) % 256) % 256
+
+    def call(T=64, H=128, Hi=4, Di=64, hid=p, wt=p, q=p, k=p, w=p):
+        return lib.irs_indexer_projection(hid, wt, T, H, Hi, Di, q, k, w, None, None)
+    assert call(H=100) == 2 and b"multiple of 8" in lib.irs_last_error()
+    assert call(Di=12) == 2 and b"multiple of 8" in lib.irs_last_error()
+    assert call(T=0) == 2
+    assert call(Hi=0) == 2
+    assert call(wt=None) == 2 and b"NULL" in lib.irs_last_error()
+    assert call(q=p + 8) == 2 and b"16-byte aligned" in lib.irs_last_error()
+    assert call(w=p + 2) == 2 and b"4-byte aligned" in lib.irs_last_error()
