@@ -444,7 +444,7 @@ def measure_other_workload(irs, name, args, dev, stream, flush, peaks, l2_gbs) -
 def measure_indexer_variants(irs, wl, d, dev, stream, flush, peaks, steps: int) -> dict:
     """The indexer rows beyond the plain one, on the headline workload's indexer shape
     (T, Hi, Di, c, budget, documents), each timed cold (L2 flushed before every call):
-    the QSA front half (RMSNorm + RoPE, 64 rotary dims), FP8 E4M3 operands, per-KV-group
+    the projections from hidden states (one GEMM, synthetic hidden size 4096), the QSA front half (RMSNorm + RoPE, 64 rotary dims), FP8 E4M3 operands, per-KV-group
     selection (G = Hkv groups of Hi heads), and the Step-5 configuration (learned-logit
     summaries, E4M3 queries, per group). Grouped queries, weights and the compression logits
     come from a seeded device generator. Roofline: the score FLOPs at the tensor peak of the
@@ -482,6 +482,41 @@ def measure_indexer_variants(irs, wl, d, dev, stream, flush, peaks, steps: int) 
             G, "e4m3", G * (T * Hi * Di * 2 + T * Hi * 4 + T * W * 4) + 2 * T * Di * 2),
     }
     out = {}
+    # the indexer's projections from hidden states (synthetic hidden size 4096): one GEMM
+    H = 4096
+    N = (Hi + 1) * Di + Hi
+    hid = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    for r0 in range(0, T, 8192):
+        r1 = min(T, r0 + 8192)
+        hid[r0:r1] = torch.randn((r1 - r0, H), generator=gen, device=dev, dtype=torch.float32)
+    wproj = (torch.randn((N, H), generator=gen, device=dev, dtype=torch.float32) / H ** 0.5).to(torch.bfloat16)
+    proj_out = (torch.empty((T, Hi, Di), dtype=torch.bfloat16, device=dev),
+                torch.empty((T, Di), dtype=torch.bfloat16, device=dev),
+                torch.empty((T, Hi), dtype=torch.float32, device=dev))
+    proj = lambda: irs.indexer_projection(hid, wproj, Hi, Di, out=proj_out, err=err)
+    for _ in range(3):
+        proj()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        proj()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    irs.check_device_errors(dev)
+    ms = np.asarray([e[0].elapsed_time(e[1]) for e in ev])
+    sec = float(np.mean(ms)) * 1e-3
+    flops = 2.0 * T * H * N
+    pbytes = T * H * 2 + N * H * 2 + T * (Hi + 1) * Di * 2 + T * Hi * 4
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = pbytes / (peaks["hbm_gbs"] * 1e9)
+    out["projection_h4096"] = {"ms": round(sec * 1e3, 4), "ms_median": round(float(np.median(ms)), 4),
+                               "tflops": round(flops / sec / 1e12, 1), "hidden_size": H, "output_columns": N,
+                               "roofline_bound": "tensor" if t_tc >= t_hbm else "hbm",
+                               "roofline_frac": round(max(t_tc, t_hbm) / sec, 4),
+                               "tensor_peak_tflops": round(peaks["bf16_tflops"], 1)}
+    del hid, wproj, proj_out
     for name, (fn, groups, dtype, nbytes) in variants.items():
         for _ in range(3):
             fn()
