@@ -232,6 +232,34 @@ irs_status irs_indexer_projection(const void* hidden, const void* weight, int T,
                                   void* kI, float* w, int32_t* err_flag, irs_stream_t stream);
 
 /*
+ * The projection with the query side of the indexer front half fused into its epilogue
+ * (QSA page, the indexer class: RMSNorm and RoPE of the queries; `apply_qsa_rope`). qI
+ * receives the transformed queries, equal bit for bit to
+ * irs_index_front_operands' queries computed from irs_indexer_projection's qI: each head
+ * row is rounded to bf16, normalised with q_weight and rotated with the token's rotary
+ * row, in the FP32 order documented for irs_sparse_index_score_topk_front, then rounded to
+ * bf16. kI stays raw (the keys get their front half after pooling) and w is unchanged.
+ * Di must be 64 or 128; q_weight fp32 [Di] and rope fp32 [T, rope_dims] as for
+ * irs_sparse_index_score_topk_front (16-byte aligned).
+ */
+irs_status irs_indexer_projection_front(const void* hidden, const void* weight, int T, int H, int Hi, int Di,
+                                        const float* q_weight, float eps, const float* rope, int rope_dims, void* qI,
+                                        void* kI, float* w, int32_t* err_flag, irs_stream_t stream);
+
+/*
+ * irs_sparse_index_score_topk_front for queries that arrive already transformed (from
+ * irs_indexer_projection_front): the pooled keys get K RMSNorm and group-start RoPE with
+ * k_weight, the queries are scored as given. Workspace, arguments and errors as for
+ * irs_sparse_index_score_topk_front (without q_weight).
+ */
+irs_status irs_sparse_index_score_topk_front_keys(const void* qI, const void* kI, const float* w,
+                                                  const int32_t* cu_seqlens, int ndocs, int max_doc_len, int T, int Hi,
+                                                  int Di, int c, int budget, const float* k_weight, float eps,
+                                                  const float* rope, int rope_dims, int32_t* route_ids,
+                                                  float* scores_dbg, int64_t ld_scores, void* workspace,
+                                                  size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream);
+
+/*
  * Step-5 learned-logit region summaries.
  *
  * Step-5 sparse page: `Step5SparseIndexer.project_keys` returns the index keys and

@@ -54,6 +54,9 @@ _SIGNATURES = {
     "irs_sparse_index_score_topk_summaries": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P,
                                                    _I64, _P, _SZ, _P, _P]),
     "irs_indexer_projection": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "irs_indexer_projection_front": (_I, [_P, _P, _I, _I, _I, _I, _P, _F, _P, _I, _P, _P, _P, _P, _P]),
+    "irs_sparse_index_score_topk_front_keys": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _F, _P, _I, _P,
+                                                    _P, _I64, _P, _SZ, _P, _P]),
     "irs_topk_from_scores": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "irs_compose_window_routes": (_I, [_P, _I, _P, _I, _I, _I, _P, _P, _P]),
     "irs_sparse_gqa_attn_fwd": (_I, [_P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I64, _P, _I64, _I, _I, _I, _I, _I, _I,
@@ -179,7 +182,8 @@ def sparse_index_score_topk(qI: torch.Tensor, kI: torch.Tensor, w: torch.Tensor,
                             c: int, budget: int, *, ndocs: int | None = None, max_doc_len: int | None = None,
                             scores_out: torch.Tensor | None = None, out: torch.Tensor | None = None,
                             workspace: torch.Tensor | None = None, err: torch.Tensor | None = None,
-                            front: dict | None = None, operands: str = "bf16") -> torch.Tensor:
+                            front: dict | None = None, operands: str = "bf16",
+                            queries_ready: bool = False) -> torch.Tensor:
     """Route IDs int32 [T, budget + c - 1] from the compressed-block indexer.
 
     qI bf16 [T, Hi, Di], kI bf16 [T, Di] (or [T, 1, Di]), w fp32 [T, Hi], cu_seqlens int32
@@ -188,11 +192,15 @@ def sparse_index_score_topk(qI: torch.Tensor, kI: torch.Tensor, w: torch.Tensor,
     of fp32 device tensors q_weight [Di], k_weight [Di], rope [T, rope_dims] and a float eps)
     adds the indexer's front half: RMSNorm and RoPE of queries and pooled keys.
     operands="e4m3" scores with the Step-5 FP8 E4M3 roundings of queries and pooled keys.
+    queries_ready (with `front`): qI already holds transformed queries (from
+    indexer_projection(front=...)); only the pooled keys get the front half.
     """
     if operands not in ("bf16", "e4m3"):
         raise ValueError("operands must be 'bf16' or 'e4m3'")
     if operands == "e4m3" and front is not None:
         raise ValueError("E4M3 operands are not combined with the front half")
+    if queries_ready and front is None:
+        raise ValueError("queries_ready needs the front half's key weights (front=...)")
     _need(qI, "qI", torch.bfloat16, 3)
     _need(kI, "kI", torch.bfloat16)
     _need(w, "w", torch.float32, 2)
@@ -237,6 +245,12 @@ def sparse_index_score_topk(qI: torch.Tensor, kI: torch.Tensor, w: torch.Tensor,
         st = lib().irs_sparse_index_score_topk(
             _ptr(qI), _ptr(kI), _ptr(w), _ptr(cu_seqlens), ndocs, max_doc_len, T, Hi, Di, c, budget, _ptr(out),
             _ptr(scores_out), ld, _ptr(workspace), workspace.numel(), _ptr(err), _stream(dev))
+    elif queries_ready:
+        _, kw, eps, rope, rope_dims = _front_args(dict(front, q_weight=front["k_weight"]), Di)
+        st = lib().irs_sparse_index_score_topk_front_keys(
+            _ptr(qI), _ptr(kI), _ptr(w), _ptr(cu_seqlens), ndocs, max_doc_len, T, Hi, Di, c, budget, _ptr(kw), eps,
+            _ptr(rope), rope_dims, _ptr(out), _ptr(scores_out), ld, _ptr(workspace), workspace.numel(), _ptr(err),
+            _stream(dev))
     else:
         qw, kw, eps, rope, rope_dims = _front_args(front, Di)
         st = lib().irs_sparse_index_score_topk_front(
@@ -498,12 +512,14 @@ def sparse_index_score_topk_grouped(qI: torch.Tensor, kI: torch.Tensor, w: torch
 
 
 def indexer_projection(hidden: torch.Tensor, weight: torch.Tensor, Hi: int, Di: int, *,
-                       out: tuple | None = None, err: torch.Tensor | None = None):
+                       front: dict | None = None, out: tuple | None = None, err: torch.Tensor | None = None):
     """The indexer's queries, raw keys and signed head weights from hidden states:
     (qI bf16 [T, Hi, Di], kI bf16 [T, Di], w fp32 [T, Hi]).
 
     hidden bf16 [T, H]; weight bf16 [(Hi+1)*Di + Hi, H] (row n gives output column n:
-    queries head-major, then keys, then head weights).
+    queries head-major, then keys, then head weights). `front` (q_weight, eps, rope as for
+    sparse_index_score_topk) fuses the queries' RMSNorm and RoPE into the projection: qI
+    then holds the transformed queries, for sparse_index_score_topk(queries_ready=True).
     """
     _need(hidden, "hidden", torch.bfloat16, 2)
     _need(weight, "weight", torch.bfloat16, 2)
@@ -521,8 +537,13 @@ def indexer_projection(hidden: torch.Tensor, weight: torch.Tensor, Hi: int, Di: 
     qI, kI, w = out
     if err is None:
         err = device_error_flag(dev)
-    st = lib().irs_indexer_projection(_ptr(hidden), _ptr(weight), T, H, Hi, Di, _ptr(qI), _ptr(kI), _ptr(w),
-                                      _ptr(err), _stream(dev))
+    if front is None:
+        st = lib().irs_indexer_projection(_ptr(hidden), _ptr(weight), T, H, Hi, Di, _ptr(qI), _ptr(kI), _ptr(w),
+                                          _ptr(err), _stream(dev))
+    else:
+        qw, _, eps, rope, rope_dims = _front_args(dict(front, k_weight=front["q_weight"]), Di)
+        st = lib().irs_indexer_projection_front(_ptr(hidden), _ptr(weight), T, H, Hi, Di, _ptr(qw), eps, _ptr(rope),
+                                                rope_dims, _ptr(qI), _ptr(kI), _ptr(w), _ptr(err), _stream(dev))
     _check(st, "indexer_projection")
     return qI, kI, w
 

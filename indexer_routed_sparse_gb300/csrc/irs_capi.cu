@@ -255,8 +255,10 @@ irs_status index_impl(const void* qI, const void* kI, const float* w, const int3
   const int64_t ldS = scores_dbg != nullptr ? ld_scores * G : p.ldS;
   const int64_t group_stride = scores_dbg != nullptr ? ld_scores : 0;
   CUtensorMap tm_q, tm_k;
-  // with the front half the scores read the transformed queries from the workspace
-  const void* qsrc = front != nullptr ? static_cast<const void*>(ws + p.off_qfront) : qI;
+  // with the front half the scores read the transformed queries from the workspace (unless
+  // the caller's queries are already transformed)
+  const void* qsrc =
+      (front != nullptr && front->q_weight != nullptr) ? static_cast<const void*>(ws + p.off_qfront) : qI;
   if (e4m3) {
     if ((s = make_e4m3_maps(&tm_q, &tm_k, ws + p.off_q8, ws + p.off_k8, (uint64_t)Di, (uint64_t)Hi,
                             (uint64_t)G * Hi, (uint64_t)T, (uint64_t)p.nblk_cap)) != IRS_OK)
@@ -375,8 +377,13 @@ irs_status irs_region_summaries(const void* kI, const void* z, const int32_t* cu
                        "launching the region summaries");
 }
 
-irs_status irs_indexer_projection(const void* hidden, const void* weight, int T, int H, int Hi, int Di, void* qI,
-                                  void* kI, float* w, int32_t* err_flag, irs_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+irs_status projection_impl(const void* hidden, const void* weight, int T, int H, int Hi, int Di, void* qI, void* kI,
+                           float* w, int32_t* err_flag, irs_stream_t stream, const float* q_weight, float eps,
+                           const float* rope, int rope_dims) {
   if (T < 1 || H < 8 || H % 8 != 0) return fail(IRS_ERR_VALUE, "need T >= 1 and H a positive multiple of 8");
   if (Hi < 1 || Di < 8 || Di % 8 != 0) return fail(IRS_ERR_VALUE, "need Hi >= 1 and Di a positive multiple of 8");
   const long long N = (long long)(Hi + 1) * Di + Hi;
@@ -399,9 +406,40 @@ irs_status irs_indexer_projection(const void* hidden, const void* weight, int T,
   if ((s = make_tmap(&tm_x, hidden, (uint64_t)H, (uint64_t)T, 128)) != IRS_OK) return s;
   if ((s = make_tmap(&tm_w, weight, (uint64_t)H, (uint64_t)N, 256)) != IRS_OK) return s;
   irs::ProjArgs a{T, H, (int)N, Hi, Di, static_cast<__nv_bfloat16*>(qI), static_cast<__nv_bfloat16*>(kI), w,
-                  err_flag, (T + 127) / 128, (int)((N + 255) / 256)};
+                  err_flag, (T + 127) / 128, (int)((N + 255) / 256), q_weight, eps, rope, rope_dims};
   return launch_status(irs::launch_proj(tm_x, tm_w, a, dev->num_sms, reinterpret_cast<cudaStream_t>(stream)),
                        "launching the projection");
+}
+
+}  // namespace
+
+extern "C" {
+
+irs_status irs_indexer_projection(const void* hidden, const void* weight, int T, int H, int Hi, int Di, void* qI,
+                                  void* kI, float* w, int32_t* err_flag, irs_stream_t stream) {
+  return projection_impl(hidden, weight, T, H, Hi, Di, qI, kI, w, err_flag, stream, nullptr, 0.f, nullptr, 0);
+}
+
+irs_status irs_sparse_index_score_topk_front_keys(const void* qI, const void* kI, const float* w,
+                                                  const int32_t* cu_seqlens, int ndocs, int max_doc_len, int T, int Hi,
+                                                  int Di, int c, int budget, const float* k_weight, float eps,
+                                                  const float* rope, int rope_dims, int32_t* route_ids,
+                                                  float* scores_dbg, int64_t ld_scores, void* workspace,
+                                                  size_t workspace_bytes, int32_t* err_flag, irs_stream_t stream) {
+  irs_status s = check_front(k_weight, k_weight, eps, rope, rope_dims, Di);
+  if (s != IRS_OK) return s;
+  const irs::FrontHalf f{nullptr, k_weight, eps, rope, rope_dims};
+  return index_impl(qI, kI, w, cu_seqlens, ndocs, max_doc_len, T, Hi, Di, c, budget, &f, route_ids, scores_dbg,
+                    ld_scores, workspace, workspace_bytes, err_flag, stream);
+}
+
+irs_status irs_indexer_projection_front(const void* hidden, const void* weight, int T, int H, int Hi, int Di,
+                                        const float* q_weight, float eps, const float* rope, int rope_dims, void* qI,
+                                        void* kI, float* w, int32_t* err_flag, irs_stream_t stream) {
+  if (Di != 64 && Di != 128) return fail(IRS_ERR_VALUE, "the fused front half needs Di = 64 or 128 (got %d)", Di);
+  irs_status s = check_front(q_weight, q_weight, eps, rope, rope_dims, Di);
+  if (s != IRS_OK) return s;
+  return projection_impl(hidden, weight, T, H, Hi, Di, qI, kI, w, err_flag, stream, q_weight, eps, rope, rope_dims);
 }
 
 irs_status irs_index_front_operands(const void* qI, const void* kI, const int32_t* cu_seqlens, int ndocs,

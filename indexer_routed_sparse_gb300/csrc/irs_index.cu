@@ -1115,6 +1115,8 @@ static void launch_pool(const IndexPlan& p, const __nv_bfloat16* qI, const __nv_
     front_keys_kernel<<<(p.nblk_cap + 127) / 128, 128, 0, stream>>>(kbar32, p.nblk_cap, Di, meta, blk_off, cu, ndocs, c,
                                                                     front->k_weight, front->eps, front->rope,
                                                                     front->rope_dims, kbar);
+  }
+  if (front && front->q_weight != nullptr) {   // (no q_weight: the queries arrive transformed)
     const long long rows = (long long)T * Hi;
     const size_t stage_bytes = (size_t)kFrontRows * (Di / 8 + 1) * 16;
     front_queries_kernel<<<(unsigned)((rows + kFrontRows - 1) / kFrontRows), kFrontRows, stage_bytes, stream>>>(

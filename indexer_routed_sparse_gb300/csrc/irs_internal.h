@@ -17,7 +17,7 @@ constexpr int kMaxIndexCtas = 160;   // persistent CTAs of the score kernel (>= 
 // Indexer front half: RMSNorm weights of queries and keys, eps, and the per-token rotary
 // table [T, rope_dims] = cat(cos, sin) (device pointers).
 struct FrontHalf {
-  const float* q_weight;
+  const float* q_weight;   // nullptr: the queries are already transformed (keys only)
   const float* k_weight;
   float eps;
   const float* rope;
@@ -83,6 +83,11 @@ struct ProjArgs {
   float* w;
   int32_t* err;
   int tiles_m, tiles_n;
+  // query front half fused into the epilogue (q_weight == nullptr: off; Di 64 or 128)
+  const float* q_weight;
+  float eps;
+  const float* rope;   // [T, rope_dims] = cat(cos, sin)
+  int rope_dims;
 };
 size_t proj_smem_bytes();
 cudaError_t configure_proj_kernel();

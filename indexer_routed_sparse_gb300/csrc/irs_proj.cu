@@ -43,6 +43,75 @@ struct ProjSmem {
   static constexpr uint32_t total = bar_off + (2 * kPStages + 5) * 8 + 16 + 1024;
 };
 
+// Query front half on one head row of the accumulator, read from tensor memory (the
+// values rounded to bf16 first, as the unfused path's qI): RMSNorm then rotate-half RoPE,
+// in FP32 with every operation rounded on its own, in the order of the indexer's
+// front-half kernels (sum of squares in ascending dim order; IEEE division and square
+// root; the rotation as separate products then a difference or sum), then one rounding to
+// bf16. tcgen05.ld takes a run-time column, so the rotation pairs (d, d + rope_dims/2) are
+// loaded where they lie. Warp-collective: every lane calls it; only rows < T store.
+__device__ __forceinline__ float bf16r(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+template <int DI>
+__device__ __forceinline__ void front_head(uint32_t taddr, const float* __restrict__ wt, float eps,
+                                           const float* __restrict__ rope, int rope_dims, bool store,
+                                           __nv_bfloat16* __restrict__ out) {
+  float ss = 0.f;
+#pragma unroll
+  for (int c = 0; c < DI / 32; ++c) {
+    float v[32];
+    tmem_ld32(taddr + 32 * c, v);
+    tmem_ld_wait_regs(v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float x = bf16r(v[i]);
+      ss = __fadd_rn(ss, __fmul_rn(x, x));
+    }
+  }
+  const float r = __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)DI), eps));
+  const int h = rope_dims >> 1;
+  for (int d0 = 0; d0 < h; d0 += 8) {
+    float a[8], b[8];
+    tmem_ld8(taddr + d0, a);
+    tmem_ld8(taddr + d0 + h, b);
+    tmem_ld_wait_regs(a);   // waits, and keeps every use of a and b behind the wait
+    tmem_ld_wait_regs(b);
+    if (store) {
+      __nv_bfloat162 p1[4], p2[4];
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        float o1[2], o2[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int d = d0 + i + k;
+          const float y1 = __fmul_rn(__fdiv_rn(bf16r(a[i + k]), r), __ldg(wt + d));
+          const float y2 = __fmul_rn(__fdiv_rn(bf16r(b[i + k]), r), __ldg(wt + d + h));
+          const float cs = __ldg(rope + d), sn = __ldg(rope + h + d);
+          o1[k] = __fsub_rn(__fmul_rn(y1, cs), __fmul_rn(y2, sn));
+          o2[k] = __fadd_rn(__fmul_rn(y2, cs), __fmul_rn(y1, sn));
+        }
+        p1[i >> 1] = __floats2bfloat162_rn(o1[0], o1[1]);
+        p2[i >> 1] = __floats2bfloat162_rn(o2[0], o2[1]);
+      }
+      *reinterpret_cast<uint4*>(out + d0) = *reinterpret_cast<const uint4*>(p1);
+      *reinterpret_cast<uint4*>(out + d0 + h) = *reinterpret_cast<const uint4*>(p2);
+    }
+  }
+  for (int d0 = rope_dims; d0 < DI; d0 += 8) {
+    float a[8];
+    tmem_ld8(taddr + d0, a);
+    tmem_ld_wait_regs(a);
+    if (store) {
+      __nv_bfloat162 p[4];
+#pragma unroll
+      for (int i = 0; i < 8; i += 2)
+        p[i >> 1] = __floats2bfloat162_rn(__fmul_rn(__fdiv_rn(bf16r(a[i]), r), __ldg(wt + d0 + i)),
+                                          __fmul_rn(__fdiv_rn(bf16r(a[i + 1]), r), __ldg(wt + d0 + i + 1)));
+      *reinterpret_cast<uint4*>(out + d0) = *reinterpret_cast<const uint4*>(p);
+    }
+  }
+}
+
 // Store one 8-column chunk of row `row` (global columns gcol .. gcol+7) where it belongs.
 __device__ __forceinline__ void proj_store8(const ProjArgs& a, int row, int gcol, const float* v) {
   const int qd = a.Hi * a.Di;
@@ -66,6 +135,7 @@ __device__ __forceinline__ void proj_store8(const ProjArgs& a, int row, int gcol
   }
 }
 
+template <int FRONT_DI>   // 0: plain; 64 or 128: queries leave with the front half applied
 __global__ void __launch_bounds__(kPThreads, 1)
     proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, ProjArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -170,6 +240,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&t_full[buf], (tc >> 1) & 1, abort_flag, a.err))) break;
       tc_fence_after();
       const int row = m * kPM + quarter * 32 + lane;
+      if constexpr (FRONT_DI > 0) {
+        const int gbase = n * kPN + col0;
+        if (gbase + kPN / 2 <= a.Hi * a.Di) {
+          // 128 query columns = 128 / Di whole heads of this token
+          const bool live = row < a.T;
+#pragma unroll 1
+          for (int hd = 0; hd < (kPN / 2) / FRONT_DI; ++hd) {
+            const int head = gbase / FRONT_DI + hd;
+            front_head<FRONT_DI>(tbase + lane_addr + buf * kPN + col0 + hd * FRONT_DI, a.q_weight, a.eps,
+                                 a.rope + (int64_t)(live ? row : 0) * a.rope_dims, a.rope_dims, live,
+                                 a.qI + ((int64_t)(live ? row : 0) * a.Hi + head) * FRONT_DI);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&t_empty[buf]);
+          continue;
+        }
+      }
 #pragma unroll 1
       for (int c32 = 0; c32 < kPN / 2; c32 += 32) {
         float v[32];
@@ -199,14 +287,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
 size_t proj_smem_bytes() { return ProjSmem::total; }
 
 cudaError_t configure_proj_kernel() {
-  return cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ProjSmem::total);
+  cudaError_t e = cudaFuncSetAttribute(proj_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)ProjSmem::total);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(proj_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)ProjSmem::total)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(proj_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ProjSmem::total);
 }
 
 cudaError_t launch_proj(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const ProjArgs& a, int num_sms,
                         cudaStream_t stream) {
   const int ntiles = a.tiles_m * a.tiles_n;
   const int grid = ntiles < num_sms ? ntiles : num_sms;
-  proj_kernel<<<grid, kPThreads, ProjSmem::total, stream>>>(tm_x, tm_w, a);
+  if (a.q_weight == nullptr) proj_kernel<0><<<grid, kPThreads, ProjSmem::total, stream>>>(tm_x, tm_w, a);
+  else if (a.Di == 64) proj_kernel<64><<<grid, kPThreads, ProjSmem::total, stream>>>(tm_x, tm_w, a);
+  else proj_kernel<128><<<grid, kPThreads, ProjSmem::total, stream>>>(tm_x, tm_w, a);
   return cudaGetLastError();
 }
 

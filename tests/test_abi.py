@@ -218,3 +218,16 @@ def test_projection_validation_is_value_error(lib):
     assert call(wt=None) == 2 and b"NULL" in lib.irs_last_error()
     assert call(q=p + 8) == 2 and b"16-byte aligned" in lib.irs_last_error()
     assert call(w=p + 2) == 2 and b"4-byte aligned" in lib.irs_last_error()
+
+
+def test_fused_projection_and_keys_only_validation(lib):
+    import ctypes as C
+    buf = C.create_string_buffer(512)
+    p = C.addressof(buf) + (256 - C.addressof(buf) % 256) % 256
+    st = lib.irs_indexer_projection_front(p, p, 64, 128, 4, 96, p, 1e-6, p, 32, p, p, p, None, None)
+    assert st == 2 and b"Di = 64 or 128" in lib.irs_last_error()
+    st = lib.irs_indexer_projection_front(p, p, 64, 128, 4, 64, None, 1e-6, p, 32, p, p, p, None, None)
+    assert st == 2 and b"RMSNorm" in lib.irs_last_error()
+    st = lib.irs_sparse_index_score_topk_front_keys(p, p, p, p, 1, 64, 64, 4, 64, 4, 16, p, 1e-6, p, 24, p, None, 0,
+                                                    p, 1 << 20, None, None)
+    assert st == 2 and b"rope_dims" in lib.irs_last_error()

@@ -93,3 +93,50 @@ def test_projection_feeds_the_indexer(irs):
     ref_r, ref_s = O.index_routes(qb, kb, wf, wl.cu_seqlens, c, budget, want_scores=True, ldS=ld)
     parity.check_scores(scores.cpu().numpy(), ref_s, wl, rows)
     parity.check_routes_e2e(route.cpu().numpy(), ref_r, ref_s, wl, rows)
+
+
+def _front_dev(T, Di, rope_dims, seed):
+    fr = irs_synth.front_half_inputs(T, Di, rope_dims, np.asarray([0, T], np.int32), seed=seed)
+    front = {"q_weight": torch.from_numpy(fr["q_weight"]).to(DEV), "k_weight": torch.from_numpy(fr["k_weight"]).to(DEV),
+             "eps": fr["eps"], "rope": torch.from_numpy(np.ascontiguousarray(fr["rope"])).to(DEV) if rope_dims else None}
+    return fr, front
+
+
+@pytest.mark.parametrize("Di, rope_dims, Hi", [(128, 64, 8), (128, 128, 4), (64, 32, 8), (64, 0, 2)])
+def test_fused_query_front_half_is_bit_exact(irs, Di, rope_dims, Hi):
+    """The projection with the queries' RMSNorm + RoPE in its epilogue: its queries equal
+    the oracle's front transform of the unfused projection's bf16 queries bit for bit; the
+    raw keys and head weights equal the unfused call's."""
+    T, H = 777, 320
+    hidden, weight = irs_synth.projection_inputs(T, H, Hi, Di, seed=Di + rope_dims)
+    fr, front = _front_dev(T, Di, rope_dims, seed=3)
+    raw = irs.indexer_projection(_dev(hidden), _dev(weight), Hi, Di)
+    fused = irs.indexer_projection(_dev(hidden), _dev(weight), Hi, Di, front=front)
+    irs.check_device_errors(DEV)
+    assert torch.equal(fused[1], raw[1]) and torch.equal(fused[2], raw[2])
+    raw_q = _bits(raw[0])
+    rope = np.asarray(fr["rope"])
+    want = np.stack([O.f64_to_bf16_bits(O.front_query_row(raw_q[t], fr["q_weight"], fr["eps"], rope[t]))
+                     for t in range(T)])
+    np.testing.assert_array_equal(_bits(fused[0]), want)
+
+
+def test_fused_pipeline_equals_the_unfused_one(irs):
+    """Projection with the fused query front half, then the indexer with the keys' front half
+    only, gives the same scores and routes, bit for bit, as the plain projection followed by
+    the indexer's full front half."""
+    T, H, Hi, Di, c, budget = 2048, 256, 16, 128, 4, 256
+    hidden, weight = irs_synth.projection_inputs(T, H, Hi, Di, seed=11)
+    _, front = _front_dev(T, Di, 64, seed=12)
+    cu = torch.tensor([0, 1000, T], dtype=torch.int32, device=DEV)
+    ld = 1048 // c
+    qI, kI, w = irs.indexer_projection(_dev(hidden), _dev(weight), Hi, Di)
+    s_u = torch.full((T, ld), float("nan"), dtype=torch.float32, device=DEV)
+    r_u = irs.sparse_index_score_topk(qI, kI, w, cu, c, budget, max_doc_len=1048, scores_out=s_u, front=front)
+    qf, kf, wf = irs.indexer_projection(_dev(hidden), _dev(weight), Hi, Di, front=front)
+    s_f = torch.full((T, ld), float("nan"), dtype=torch.float32, device=DEV)
+    r_f = irs.sparse_index_score_topk(qf, kf, wf, cu, c, budget, max_doc_len=1048, scores_out=s_f, front=front,
+                                      queries_ready=True)
+    irs.check_device_errors(DEV)
+    assert torch.equal(r_f, r_u)
+    assert torch.equal(torch.nan_to_num(s_f, nan=-7.0), torch.nan_to_num(s_u, nan=-7.0))
