@@ -516,6 +516,31 @@ def measure_indexer_variants(irs, wl, d, dev, stream, flush, peaks, steps: int) 
                                "roofline_bound": "tensor" if t_tc >= t_hbm else "hbm",
                                "roofline_frac": round(max(t_tc, t_hbm) / sec, 4),
                                "tensor_peak_tflops": round(peaks["bf16_tflops"], 1)}
+    # projection then the front-half indexer: the queries' front half as its own pass, or
+    # fused into the projection's epilogue
+    def pipeline(fused: bool):
+        if fused:
+            q, k, wv = irs.indexer_projection(hid, wproj, Hi, Di, front=front, out=proj_out, err=err)
+            return irs.sparse_index_score_topk(q, k, wv, d["cu_seqlens"], c, budget, front=front, queries_ready=True,
+                                               **kw)
+        q, k, wv = irs.indexer_projection(hid, wproj, Hi, Di, out=proj_out, err=err)
+        return irs.sparse_index_score_topk(q, k, wv, d["cu_seqlens"], c, budget, front=front, **kw)
+    for fused in (False, True):
+        for _ in range(3):
+            pipeline(fused)
+        torch.cuda.synchronize(dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            pipeline(fused)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        irs.check_device_errors(dev)
+        ms = np.asarray([e[0].elapsed_time(e[1]) for e in ev])
+        key = "projection_front_fused_then_indexer_h4096" if fused else "projection_then_front_half_indexer_h4096"
+        out[key] = {"ms": round(float(np.mean(ms)), 4), "ms_median": round(float(np.median(ms)), 4),
+                    "queries_per_s": round(T / (float(np.mean(ms)) * 1e-3), 1)}
     del hid, wproj, proj_out
     for name, (fn, groups, dtype, nbytes) in variants.items():
         for _ in range(3):
