@@ -856,6 +856,15 @@ def time_backward(args, wl, irs, d, route, kv_v, out, lse, flush, err, stream, d
     return float(np.mean([e[0].elapsed_time(e[1]) for e in ev])) * 1e-3
 
 
+def backward_kernel_name(wl) -> str:
+    """The kernel sparse_gqa_attn_bwd launches for this shape: the warp-per-row kernel for
+    separate K and V of the listed head dims, the staged kernel otherwise (latent rows)."""
+    fast_dims = {(64, 64), (64, 128), (128, 128), (128, 256), (192, 128)}
+    if not wl.latent and (wl.Dqk, wl.Dv) in fast_dims:
+        return "attn_bwd_fast_kernel"
+    return "attn_bwd_kernel"
+
+
 def backward_report(wl, cnt, bwd_s: float, peaks: dict) -> dict:
     """Backward rate against the forward's roofline definition.
 
@@ -876,7 +885,7 @@ def backward_report(wl, cnt, bwd_s: float, peaks: dict) -> dict:
     return {"ms": round(bwd_s * 1e3, 4), "tflops": round(flops / bwd_s / 1e12, 3),
             "gbs": round(nbytes / bwd_s / 1e9, 1), "bound": "hbm" if t_hbm >= t_tc else "tensor",
             "roofline_ms": round(roof_s * 1e3, 4), "roofline_frac": round(roof_s / bwd_s, 4),
-            "algorithmic_bytes": int(nbytes), "flops": flops, "kernel": "attn_bwd_kernel",
+            "algorithmic_bytes": int(nbytes), "flops": flops, "kernel": backward_kernel_name(wl),
             "launches_per_call": 1,
             "note": "FP32 CUDA-core kernel; timed separately, not part of the step or of value"}
 

@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_kernel(BwdArgs a) {
 // instructions, where the general kernel above spends several hundred on predicated
 // 18-wide arrays and shared-memory read-modify-writes.
 // ---------------------------------------------------------------------------------------
-constexpr int kFastRows = 32;   // routed rows staged per chunk (8 per warp)
+constexpr int kFastRows = 16;   // routed rows per staged chunk; two chunk buffers
 
 struct FastLayout {
   uint32_t ids, q, dO, dq, misc, k, v, total;
@@ -243,30 +243,62 @@ __host__ __device__ inline FastLayout fast_layout(int Dqk, int Dv, int W, int HB
   L.dO = off; off += (uint32_t)(HB * Dv) * 4u;
   L.dq = off; off += (uint32_t)(HB * Dqk) * 4u;
   L.misc = off; off += (16 + 16 + 4) * 4u;
-  L.k = off; off += (uint32_t)(kFastRows * Dqk) * 2u;
-  L.v = off; off += (uint32_t)(kFastRows * Dv) * 2u;
+  L.k = off; off += (uint32_t)(2 * kFastRows * Dqk) * 2u;
+  L.v = off; off += (uint32_t)(2 * kFastRows * Dv) * 2u;
   L.total = round16(off);
   return L;
 }
 
 template <int N>
 __device__ __forceinline__ void ld_bf16n(const __nv_bfloat16* p, float (&x)[N]) {
+  if constexpr (N % 8 == 0) {
 #pragma unroll
-  for (int i = 0; i < N; i += 2) {
-    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p + i));
-    x[i] = f.x;
-    x[i + 1] = f.y;
+    for (int i = 0; i < N; i += 8) {
+      const uint4 u = *reinterpret_cast<const uint4*>(p + i);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+        x[i + 2 * k] = f.x;
+        x[i + 2 * k + 1] = f.y;
+      }
+    }
+  } else if constexpr (N % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(p + i);
+      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+      x[i] = f0.x;
+      x[i + 1] = f0.y;
+      x[i + 2] = f1.x;
+      x[i + 3] = f1.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p + i));
+      x[i] = f.x;
+      x[i + 1] = f.y;
+    }
   }
 }
-template <int N>
-__device__ __forceinline__ void ld_f32n(const float* p, float (&x)[N]) {
+// The 2H dims of one lane, as H packed FP32 pairs, from a pair-interleaved row (pair i of
+// lane l at float2 index i * 32 + l): each load of the warp reads 256 contiguous bytes.
+template <int H>
+__device__ __forceinline__ void ld_pairs(const float* p, int lane, uint64_t (&x)[H]) {
 #pragma unroll
-  for (int i = 0; i < N; i += 2) {
-    const float2 f = *reinterpret_cast<const float2*>(p + i);
-    x[i] = f.x;
-    x[i + 1] = f.y;
-  }
+  for (int i = 0; i < H; ++i) x[i] = *reinterpret_cast<const uint64_t*>(p + (i * 32 + lane) * 2);
 }
+// 2H bf16 values as H packed FP32 pairs
+template <int H>
+__device__ __forceinline__ void ld_bf16_pairs(const __nv_bfloat16* p, uint64_t (&x)[H]) {
+  float f[2 * H];
+  ld_bf16n<2 * H>(p, f);
+#pragma unroll
+  for (int i = 0; i < H; ++i) x[i] = pack2(f[2 * i], f[2 * i + 1]);
+}
+
 // x[0..N) added to p[0..N) (p 16-byte aligned when N % 4 == 0, else 8-byte aligned)
 template <int N>
 __device__ __forceinline__ void red_add_n(float* p, const float (&x)[N]) {
@@ -279,10 +311,58 @@ __device__ __forceinline__ void red_add_n(float* p, const float (&x)[N]) {
     for (int i = 0; i < N; i += 2) atomicAdd(reinterpret_cast<float2*>(p + i), make_float2(x[i], x[i + 1]));
   }
 }
+// H packed pairs added to p[0..2H)
+template <int H>
+__device__ __forceinline__ void red_add_pairs(float* p, const uint64_t (&x)[H]) {
+  float f[2 * H];
+#pragma unroll
+  for (int i = 0; i < H; ++i) {
+    const float2 v = unpack2(x[i]);
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+  red_add_n<2 * H>(p, f);
+}
 
-template <int NQ, int NV, int NHB>
+// Per-lane sizes of the fast kernel: a routed row spreads over the 32 lanes of one warp.
+template <int DQ, int DV, int NHB>
+struct FastShape {
+  static constexpr int NQ = DQ / 32, NV = DV / 32;   // dims per lane
+  static constexpr int HQ = NQ / 2, HV = NV / 2;     // ... as packed FP32 pairs
+  // small head blocks keep q and dO in registers for the whole CTA (they are the same for
+  // every routed row); larger ones re-read them from shared memory per row
+  static constexpr bool kQReg = NHB * (NQ + NV) <= 64;
+  static constexpr int V = 2 * NHB;   // partial sums per row: s and dp of each head
+  static constexpr int LV = NHB == 4 ? 3 : (NHB == 8 ? 4 : 5);   // log2(V)
+};
+
+// Head j's q and dO dims of this lane: from registers, or from the lane-interleaved rows.
+template <bool kQReg, int RH, int HQ, int HV>
+__device__ __forceinline__ void head_vectors(const uint64_t (&qr)[RH][HQ], const uint64_t (&dr)[RH][HV],
+                                             const float* qs, const float* dos, int j, int lane, uint64_t (&q)[HQ],
+                                             uint64_t (&d)[HV]) {
+  if constexpr (kQReg) {
+#pragma unroll
+    for (int i = 0; i < HQ; ++i) q[i] = qr[j][i];
+#pragma unroll
+    for (int i = 0; i < HV; ++i) d[i] = dr[j][i];
+  } else {
+    ld_pairs<HQ>(qs + j * 64 * HQ, lane, q);
+    ld_pairs<HV>(dos + j * 64 * HV, lane, d);
+  }
+}
+
+// One CTA per (query, KV head, head block), 4 warps. The routed rows of the query are staged
+// in chunks of kFastRows; each row goes to one warp, whose lane l holds the row's K and V dims
+// [l*N, (l+1)*N) and, for every head, the matching q and dO dims. Per row and
+// head: s = q.k and dp = dO.v (lane partial sums, reduced together), p = exp2(s*scale*log2e
+// - lse*log2e), ds = p*(dp - D)*scale, then dq += ds*k in registers and ds*q, p*dO summed
+// over the heads into the row's dk and dv with one vector atomic per 4 dims.
+template <int DQ, int DV, int NHB>
 __global__ void __launch_bounds__(kBwdThreads) attn_bwd_fast_kernel(BwdArgs a) {
-  constexpr int DQ = 32 * NQ, DV = 32 * NV;
+  using Sh = FastShape<DQ, DV, NHB>;
+  constexpr int NQ = Sh::NQ, NV = Sh::NV, HQ = Sh::HQ, HV = Sh::HV, V = Sh::V, LV = Sh::LV;
+  constexpr bool kQReg = Sh::kQReg;
   extern __shared__ __align__(16) uint8_t smem[];
   const FastLayout L = fast_layout(DQ, DV, a.W, a.HB);
   int32_t* ids = reinterpret_cast<int32_t*>(smem + L.ids);
@@ -303,14 +383,20 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_fast_kernel(BwdArgs a) {
   const int h0 = g * a.G + hb * a.HB;
   const int nh = min(a.HB, a.G - hb * a.HB);
 
+  // q and dO as FP32, pair-interleaved: dims (2i, 2i+1) of lane l's range [l*N, (l+1)*N) of
+  // head j at float2 [j][i][l], so a warp reads each pair of all its lanes as 256 bytes
   for (int i = tid; i < nh * DQ; i += kBwdThreads) {
     const int j = i / DQ, d = i - j * DQ;
-    qs[i] = __bfloat162float(a.q[(int64_t)t * a.q_st + (int64_t)(h0 + j) * a.q_sh + d]);
+    qs[j * DQ + (((d % NQ) >> 1) * 32 + d / NQ) * 2 + (d & 1)] =
+        __bfloat162float(a.q[(int64_t)t * a.q_st + (int64_t)(h0 + j) * a.q_sh + d]);
     dqr[i] = 0.f;
   }
   const __nv_bfloat16* dO_t = a.dout + ((int64_t)t * a.Hq + h0) * DV;
   const __nv_bfloat16* o_t = a.out + ((int64_t)t * a.Hq + h0) * DV;
-  for (int i = tid; i < nh * DV; i += kBwdThreads) dos[i] = __bfloat162float(dO_t[i]);
+  for (int i = tid; i < nh * DV; i += kBwdThreads) {
+    const int j = i / DV, d = i - j * DV;
+    dos[j * DV + (((d % NV) >> 1) * 32 + d / NV) * 2 + (d & 1)] = __bfloat162float(dO_t[i]);
+  }
   for (int j = warp; j < nh; j += 4) {
     float s = 0.f;
     for (int d = lane; d < DV; d += 32)
@@ -342,82 +428,150 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_fast_kernel(BwdArgs a) {
     n += wcnt[0] + wcnt[1] + wcnt[2] + wcnt[3];
     __syncthreads();
   }
+  __syncthreads();   // qs, dos, Dh and l2h complete even when the route row is empty
 
-  float dqa[NHB][NQ];
+  // all arithmetic on packed FP32 pairs (fma.rn.f32x2: two FMAs per instruction); a zero
+  // pair is the all-zero bit pattern
+  uint64_t dqa[NHB][HQ];
 #pragma unroll
   for (int j = 0; j < NHB; ++j)
 #pragma unroll
-    for (int i = 0; i < NQ; ++i) dqa[j][i] = 0.f;
+    for (int i = 0; i < HQ; ++i) dqa[j][i] = 0ull;
+  constexpr int RH = kQReg ? NHB : 1;
+  uint64_t qr[RH][HQ], dr[RH][HV];
+  if constexpr (kQReg) {
+#pragma unroll
+    for (int j = 0; j < NHB; ++j) {
+#pragma unroll
+      for (int i = 0; i < HQ; ++i) qr[j][i] = 0ull;
+#pragma unroll
+      for (int i = 0; i < HV; ++i) dr[j][i] = 0ull;
+      if (j < nh) {
+        ld_pairs<HQ>(qs + j * DQ, lane, qr[j]);
+        ld_pairs<HV>(dos + j * DV, lane, dr[j]);
+      }
+    }
+  }
 
   constexpr int kp = DQ / 8, vp = DV / 8;   // 16-byte pieces per staged row
-  for (int c0 = 0; c0 < n; c0 += kFastRows) {
+  constexpr int SH = 5 - LV;                // after the reduction, 2^SH lanes share one sum
+  const int vi = lane >> SH;                // ... namely s_vi (vi < NHB) or dp_(vi-NHB)
+  // chunk c's K and V rows land in buffer c & 1 by cp.async, issued one chunk ahead
+  auto stage = [&](int c0, int buf) {
     const int nc = min(kFastRows, n - c0);
+    const uint32_t kb = smem_u32(ks + buf * kFastRows * DQ), vb = smem_u32(vs + buf * kFastRows * DV);
     for (int i = tid; i < nc * kp; i += kBwdThreads) {
       const int r = i / kp, pc = i - r * kp;
       const uint4* src = reinterpret_cast<const uint4*>(a.k + (int64_t)ids[c0 + r] * a.k_st + (int64_t)g * a.k_sh);
-      reinterpret_cast<uint4*>(ks + r * DQ)[pc] = __ldg(src + pc);
+      cp_async_16(kb + (uint32_t)(r * DQ + pc * 8) * 2u, src + pc, 16);
     }
     for (int i = tid; i < nc * vp; i += kBwdThreads) {
       const int r = i / vp, pc = i - r * vp;
       const uint4* src = reinterpret_cast<const uint4*>(a.v + (int64_t)ids[c0 + r] * a.v_st + (int64_t)g * a.v_sh);
-      reinterpret_cast<uint4*>(vs + r * DV)[pc] = __ldg(src + pc);
+      cp_async_16(vb + (uint32_t)(r * DV + pc * 8) * 2u, src + pc, 16);
+    }
+    cp_async_commit();
+  };
+  if (n > 0) stage(0, 0);
+  for (int c0 = 0, buf = 0; c0 < n; c0 += kFastRows, buf ^= 1) {
+    const int nc = min(kFastRows, n - c0);
+    if (c0 + kFastRows < n) {
+      stage(c0 + kFastRows, buf ^ 1);   // buffer buf^1 was released by the last chunk's barrier
+      cp_async_wait_pending(1);
+    } else {
+      cp_async_wait_pending(0);
     }
     __syncthreads();
+    const __nv_bfloat16* kc = ks + buf * kFastRows * DQ;
+    const __nv_bfloat16* vc = vs + buf * kFastRows * DV;
     for (int r = warp; r < nc; r += 4) {
-      float kr[NQ], vr[NV], ak[NQ], av[NV];
-      ld_bf16n<NQ>(ks + r * DQ + lane * NQ, kr);
-      ld_bf16n<NV>(vs + r * DV + lane * NV, vr);
+      uint64_t kr[HQ], vr[HV], ak[HQ], av[HV];
+      ld_bf16_pairs<HQ>(kc + r * DQ + lane * NQ, kr);
+      ld_bf16_pairs<HV>(vc + r * DV + lane * NV, vr);
 #pragma unroll
-      for (int i = 0; i < NQ; ++i) ak[i] = 0.f;
+      for (int i = 0; i < HQ; ++i) ak[i] = 0ull;
 #pragma unroll
-      for (int i = 0; i < NV; ++i) av[i] = 0.f;
+      for (int i = 0; i < HV; ++i) av[i] = 0ull;
+      // s_j and dp_j of every head as lane partial sums, then one transposed butterfly over
+      // all V = 2*NHB values: at each of the first log2(V) steps a lane keeps half of its
+      // values and swaps the other half with its partner, so it ends with one sum and 2^SH
+      // lanes share it: V - 1 + SH shuffles for the row instead of 5 per value
+      float x[V];
+#pragma unroll
+      for (int j = 0; j < NHB; ++j) {
+        uint64_t s2 = 0ull, dp2 = 0ull;
+        if (j < nh) {   // warp-uniform
+          uint64_t q[HQ], d[HV];
+          head_vectors<kQReg>(qr, dr, qs, dos, j, lane, q, d);
+#pragma unroll
+          for (int i = 0; i < HQ; ++i) s2 = ffma2(q[i], kr[i], s2);
+#pragma unroll
+          for (int i = 0; i < HV; ++i) dp2 = ffma2(d[i], vr[i], dp2);
+        }
+        const float2 sp = unpack2(s2), dpp = unpack2(dp2);
+        x[j] = sp.x + sp.y;
+        x[NHB + j] = dpp.x + dpp.y;
+      }
+#pragma unroll
+      for (int k = 0; k < LV; ++k) {
+        const int o = 16 >> k, m = V >> k;
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < m / 2; ++i) {
+          const float send = upper ? x[i] : x[i + m / 2];
+          const float keep = upper ? x[i + m / 2] : x[i];
+          x[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+#pragma unroll
+      for (int o = 16 >> LV; o > 0; o >>= 1) x[0] += __shfl_xor_sync(0xffffffffu, x[0], o);
+      const float dp_mine = __shfl_sync(0xffffffffu, x[0], ((vi + NHB) << SH) | (lane & ((1 << SH) - 1)));
+      float p_mine = 0.f, ds_mine = 0.f;
+      if (vi < nh) {
+        p_mine = ex2_approx(fmaf(x[0], a.scale_log2, -l2h[vi]));
+        ds_mine = p_mine * (dp_mine - Dh[vi]) * a.scale;
+      }
 #pragma unroll
       for (int j = 0; j < NHB; ++j) {
         if (j < nh) {   // warp-uniform
-          float q[NQ], d[NV];
-          ld_f32n<NQ>(qs + j * DQ + lane * NQ, q);
-          ld_f32n<NV>(dos + j * DV + lane * NV, d);
-          float s = 0.f, dp = 0.f;
+          const float p = __shfl_sync(0xffffffffu, p_mine, j << SH);
+          const float dsk = __shfl_sync(0xffffffffu, ds_mine, j << SH);
+          const uint64_t p2 = pack2(p, p), ds2 = pack2(dsk, dsk);
+          uint64_t q[HQ], d[HV];
+          head_vectors<kQReg>(qr, dr, qs, dos, j, lane, q, d);
 #pragma unroll
-          for (int i = 0; i < NQ; ++i) s = fmaf(q[i], kr[i], s);
-#pragma unroll
-          for (int i = 0; i < NV; ++i) dp = fmaf(d[i], vr[i], dp);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            s += __shfl_xor_sync(0xffffffffu, s, o);
-            dp += __shfl_xor_sync(0xffffffffu, dp, o);
-          }
-          const float p = ex2_approx(fmaf(s, a.scale_log2, -l2h[j]));
-          const float dsk = p * (dp - Dh[j]) * a.scale;
-#pragma unroll
-          for (int i = 0; i < NQ; ++i) {
-            dqa[j][i] = fmaf(dsk, kr[i], dqa[j][i]);
-            ak[i] = fmaf(dsk, q[i], ak[i]);
+          for (int i = 0; i < HQ; ++i) {
+            dqa[j][i] = ffma2(ds2, kr[i], dqa[j][i]);
+            ak[i] = ffma2(ds2, q[i], ak[i]);
           }
 #pragma unroll
-          for (int i = 0; i < NV; ++i) av[i] = fmaf(p, d[i], av[i]);
+          for (int i = 0; i < HV; ++i) av[i] = ffma2(p2, d[i], av[i]);
         }
       }
       const int64_t row = (int64_t)ids[c0 + r] * a.Hkv + g;
-      red_add_n<NQ>(a.dk + row * DQ + lane * NQ, ak);
-      red_add_n<NV>(a.dv + row * DV + lane * NV, av);
+      red_add_pairs<HQ>(a.dk + row * DQ + lane * NQ, ak);
+      red_add_pairs<HV>(a.dv + row * DV + lane * NV, av);
     }
-    __syncthreads();   // the staged rows are reused by the next chunk
+    __syncthreads();   // buffer buf is refilled by the next iteration's prefetch
   }
   // the four warps' dq partials, then dq out
 #pragma unroll
   for (int j = 0; j < NHB; ++j)
     if (j < nh)
 #pragma unroll
-      for (int i = 0; i < NQ; ++i) atomicAdd(&dqr[j * DQ + lane * NQ + i], dqa[j][i]);
+      for (int i = 0; i < HQ; ++i) {
+        const float2 v = unpack2(dqa[j][i]);
+        atomicAdd(&dqr[j * DQ + lane * NQ + 2 * i], v.x);
+        atomicAdd(&dqr[j * DQ + lane * NQ + 2 * i + 1], v.y);
+      }
   __syncthreads();
   float* dq_t = a.dq + ((int64_t)t * a.Hq + h0) * DQ;
   for (int i = tid; i < nh * DQ; i += kBwdThreads) dq_t[i] = dqr[i];
 }
 
-template <int NQ, int NV>
-static bool launch_fast_nq(const BwdArgs& a, unsigned items, cudaStream_t stream, cudaError_t* e) {
-  const size_t smem = fast_layout(32 * NQ, 32 * NV, a.W, a.HB).total;
+template <int DQ, int DV>
+static bool launch_fast_dims(const BwdArgs& a, unsigned items, cudaStream_t stream, cudaError_t* e) {
+  const size_t smem = fast_layout(DQ, DV, a.W, a.HB).total;
   auto go = [&](auto kernel) {
     *e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (*e == cudaSuccess) {
@@ -426,9 +580,9 @@ static bool launch_fast_nq(const BwdArgs& a, unsigned items, cudaStream_t stream
     }
     return true;
   };
-  if (a.HB <= 4) return go(attn_bwd_fast_kernel<NQ, NV, 4>);
-  if (a.HB <= 8) return go(attn_bwd_fast_kernel<NQ, NV, 8>);
-  return go(attn_bwd_fast_kernel<NQ, NV, 16>);
+  if (a.HB <= 4) return go(attn_bwd_fast_kernel<DQ, DV, 4>);
+  if (a.HB <= 8) return go(attn_bwd_fast_kernel<DQ, DV, 8>);
+  return go(attn_bwd_fast_kernel<DQ, DV, 16>);
 }
 
 // The fast kernel when the shape has an instantiation; false otherwise.
@@ -436,11 +590,11 @@ static bool launch_fast(const BwdArgs& a, unsigned items, cudaStream_t stream, c
   if (a.v_alias || a.dv_alias || a.HB > 16) return false;
   if (fast_layout(a.Dqk, a.Dv, a.W, a.HB).total > 227u * 1024u) return false;
   switch (a.Dqk * 1000 + a.Dv) {
-    case 64064: return launch_fast_nq<2, 2>(a, items, stream, e);
-    case 64128: return launch_fast_nq<2, 4>(a, items, stream, e);
-    case 128128: return launch_fast_nq<4, 4>(a, items, stream, e);
-    case 128256: return launch_fast_nq<4, 8>(a, items, stream, e);
-    case 192128: return launch_fast_nq<6, 4>(a, items, stream, e);
+    case 64064: return launch_fast_dims<64, 64>(a, items, stream, e);
+    case 64128: return launch_fast_dims<64, 128>(a, items, stream, e);
+    case 128128: return launch_fast_dims<128, 128>(a, items, stream, e);
+    case 128256: return launch_fast_dims<128, 256>(a, items, stream, e);
+    case 192128: return launch_fast_dims<192, 128>(a, items, stream, e);
     default: return false;
   }
 }

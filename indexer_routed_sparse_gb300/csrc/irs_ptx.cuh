@@ -151,6 +151,25 @@ __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
 }
 
 // ---------------------------------------------------------------------------------
+// Packed FP32 pairs (sm_100+ f32x2 arithmetic): x in the low half, y in the high half.
+__device__ __forceinline__ uint64_t pack2(float x, float y) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+// a * b + c on both halves, each rounded to nearest
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// ---------------------------------------------------------------------------------
 // 16-byte cp.async (zero-fills the destination when src_bytes == 0)
 // ---------------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
