@@ -267,11 +267,14 @@ def test_end_to_end(irs, name, nrows):
     parity.check_attention(out2, lse2, ref_o, ref_l, rows)
 
 
-@pytest.mark.parametrize("case", ["windowed_small", "multi_doc", "window_wider_than_route"])
+@pytest.mark.parametrize("case", ["windowed_small", "multi_doc", "window_wider_than_route", "g1_dv256",
+                                  "g16_d192_docs"])
 def test_window_in_the_kernel_equals_composed_route(irs, case):
     """The windowed attention entry point against composing the window into the route and
     attending that: the same keys in the same order, so the outputs agree bit for bit; and
-    both against the oracle on sampled rows."""
+    both against the oracle on sampled rows. The shapes cover ragged tails, windows that
+    start at document starts (a one-token document included), G = 1, 4 and 16, Dqk 64 to
+    192, Dv = 256 and a window wider than the route."""
     if case == "windowed_small":
         wl = irs_synth.make("windowed", small=True)
         a = wl.arrays
@@ -282,14 +285,17 @@ def test_window_in_the_kernel_equals_composed_route(irs, case):
         q, k, v = t["q"], t["k"], t["v"]
         cu_h = wl.cu_seqlens
     else:
-        T = 700
-        lens = [5, 300, 395] if case == "multi_doc" else [T]
-        wl = irs_synth.custom(T, 8, 2, 128, 128, 2, 64, 4, 8, doc_lens=lens, seed=len(lens) + 40)
+        shapes = {  # T, Hq, Hkv, Dqk, Dv, doc lengths, route width, window
+            "multi_doc": (700, 8, 2, 128, 128, [5, 300, 395], 40, 64),
+            "window_wider_than_route": (700, 8, 2, 128, 128, [700], 7, 200),
+            "g1_dv256": (300, 2, 2, 64, 256, [170, 130], 24, 100),
+            "g16_d192_docs": (400, 32, 2, 192, 128, [90, 1, 309], 30, 130),
+        }
+        T, Hq, Hkv, Dqk, Dv, lens, W, window = shapes[case]
+        wl = irs_synth.custom(T, Hq, Hkv, Dqk, Dv, 2, 64, 4, 8, doc_lens=lens, seed=len(lens) + 40)
         a = wl.arrays
         rng = np.random.default_rng(5)
-        W = 40 if case == "multi_doc" else 7
         route = torch.from_numpy(irs_synth.random_routes(rng, T, T, W, wl.cu_seqlens, frac_invalid=0.2)).to(DEV)
-        window = 64 if case == "multi_doc" else 200
         cu_h = wl.cu_seqlens
         cu = torch.from_numpy(cu_h).to(DEV)
         scale = wl.scale
