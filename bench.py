@@ -831,6 +831,10 @@ def time_backward(args, wl, irs, d, route, kv_v, out, lse, flush, err, stream, d
     gen = torch.Generator(device=dev)
     gen.manual_seed(wl.seed + 1000)
     dout = torch.randn(out.shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    if wl.window:
+        # the forward attended the window in front of each route: its backward takes the
+        # composed route (window + route), built once outside the timed region
+        route = irs.compose_window_routes(route, d["cu_seqlens"], wl.window)
     k, v = (d["kv"], kv_v) if wl.latent else (d["k"], d["v"])
     dq = torch.empty((wl.T, wl.Hq, wl.Dqk), dtype=torch.float32, device=dev)
     dk = torch.empty((wl.Tk, wl.Hkv, wl.Dqk), dtype=torch.float32, device=dev)
@@ -857,12 +861,24 @@ def time_backward(args, wl, irs, d, route, kv_v, out, lse, flush, err, stream, d
 
 
 def backward_kernel_name(wl) -> str:
-    """The kernel sparse_gqa_attn_bwd launches for this shape: the warp-per-row kernel for
-    separate K and V of the listed head dims, the staged kernel otherwise (latent rows)."""
+    """The kernel sparse_gqa_attn_bwd launches for this shape: the tensor-core kernel for
+    separate K and V whose tiles fit (dims multiples of 64 up to 256, TMEM and shared-memory
+    budgets) with 8 or more query heads per KV head; else the CUDA-core warp-per-row kernel
+    for the listed dims; else the tensor-core kernel if it fits, else the staged CUDA-core
+    kernel (latent rows)."""
+    if wl.latent:
+        return "attn_bwd_kernel"
+    W = wl.route_width
+    smem = (512 * (wl.Dqk + wl.Dv) + 32 * (wl.Dqk + wl.Dv) + 2 * 128 * 128 + 2 * 16 * 128 + ((4 * W + 15) & ~15)
+            + 4 * 16 * 36 * 4 + 1392)
+    tc = (wl.Dqk % 64 == 0 and wl.Dv % 64 == 0 and max(wl.Dqk, wl.Dv) <= 256 and 96 + wl.Dqk + wl.Dv <= 512
+          and smem <= 227 * 1024)
+    if tc and min(wl.Hq // wl.Hkv, 16) >= 8:
+        return "attn_bwd_tc_kernel"
     fast_dims = {(64, 64), (64, 128), (128, 128), (128, 256), (192, 128)}
-    if not wl.latent and (wl.Dqk, wl.Dv) in fast_dims:
+    if (wl.Dqk, wl.Dv) in fast_dims:
         return "attn_bwd_fast_kernel"
-    return "attn_bwd_kernel"
+    return "attn_bwd_tc_kernel" if tc else "attn_bwd_kernel"
 
 
 def backward_report(wl, cnt, bwd_s: float, peaks: dict) -> dict:
@@ -887,7 +903,7 @@ def backward_report(wl, cnt, bwd_s: float, peaks: dict) -> dict:
             "roofline_ms": round(roof_s * 1e3, 4), "roofline_frac": round(roof_s / bwd_s, 4),
             "algorithmic_bytes": int(nbytes), "flops": flops, "kernel": backward_kernel_name(wl),
             "launches_per_call": 1,
-            "note": "FP32 CUDA-core kernel; timed separately, not part of the step or of value"}
+            "note": "timed separately, not part of the step or of value"}
 
 
 # --------------------------------------------------------------------------------------

@@ -10,7 +10,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(os.path.dirname(HERE), "_build", "irs")
 LIB = os.path.join(HERE, "libirs.so")
 SOURCES = ["irs_capi.cu", "irs_index.cu", "irs_index_di64.cu", "irs_index_di128.cu", "irs_index_e4m3.cu",
-           "irs_attn.cu", "irs_mla.cu", "irs_bwd.cu", "irs_proj.cu"]
+           "irs_attn.cu", "irs_mla.cu", "irs_bwd.cu", "irs_bwd_tc.cu", "irs_proj.cu"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",

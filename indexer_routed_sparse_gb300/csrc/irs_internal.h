@@ -177,5 +177,8 @@ int bwd_pick_rows(const BwdArgs& a, size_t max_smem);
 int bwd_max_heads();
 cudaError_t configure_bwd_kernel(size_t smem);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+// The tensor-core backward (separate K and V, Dqk and Dv multiples of 64 up to 256).
+bool bwd_tc_supported(const BwdArgs& a);
+cudaError_t launch_bwd_tc(const BwdArgs& a, unsigned items, cudaStream_t stream);
 
 }  // namespace irs
