@@ -474,8 +474,10 @@ irs_status irs_sparse_gqa_attn_fwd_windowed(const void* q, int64_t q_stride_t, i
  *       IRS_ERR_VALUE otherwise): the value gradient is then added into the first Dv dims
  *       of each dk row, which is the gradient of latent rows used as keys and values
  * The accumulation uses FP32 atomics, so dk and dv are not bit-reproducible across runs.
- * CUDA-core kernel (no tensor cores yet): one CTA per (query, KV head, block of up to
- * 16 query heads); it waits on nothing outside itself.
+ * One CTA per (query, KV head, block of up to 16 query heads), waiting on nothing outside
+ * itself. Blocks of 8 or more heads with separate K and V (dims multiples of 64 up to 256)
+ * run on the tensor cores, where P and ds are rounded once to bf16 as product operands (as
+ * the forward rounds P); smaller blocks and latent rows run in FP32 on the CUDA cores.
  */
 irs_status irs_sparse_gqa_attn_bwd(const void* q, int64_t q_stride_t, int64_t q_stride_h, const void* k,
                                    int64_t k_stride_t, int64_t k_stride_h, const void* v, int64_t v_stride_t,

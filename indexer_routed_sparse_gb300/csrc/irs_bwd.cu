@@ -10,13 +10,16 @@
 //   ds_r = p_r (dO.v_r - D)
 //   dq   = scale * sum_r ds_r k_r,   dk_r += scale * ds_r q,   dv_r += p_r dO
 //
-// This is the first, plain version: the contractions are per (key, head) vector
-// products on the CUDA cores. A work item is (query, KV head, block of <= 16 query heads),
-// one CTA of 4 warps; warp w owns the heads j = w (mod 4) of the block, so its dq rows
-// are private (shared memory, no atomics). Routed rows are staged 16 at a time; for each
-// row a warp sums its heads' dk/dv contributions in registers (lane l holds dims
-// l, l+32, ...), the four warps meet in a shared-memory row, and the staged rows are
-// flushed to the FP32 global accumulators with float4 atomics. No waits on other CTAs.
+// The FP32 CUDA-core kernels, and the dispatch (launch_bwd) among them and the tensor-core
+// kernel of irs_bwd_tc.cu. A work item is (query, KV head, block of <= 16 query heads), one
+// CTA of 4 warps; no kernel waits on other CTAs.
+//   attn_bwd_kernel       the general kernel (latent rows, any shape): warp w owns the heads
+//                         j = w (mod 4) of the block, so its dq rows are private; routed rows
+//                         are staged 16 at a time, each warp sums its heads' dk/dv
+//                         contributions in registers, the four warps meet in a shared row,
+//                         and staged rows go to the FP32 accumulators by float4 atomics.
+//   attn_bwd_fast_kernel  separate K and V of the common head dims: one routed row per warp,
+//                         all heads reduced at once (see its own comment).
 #include "irs_internal.h"
 #include "irs_ptx.cuh"
 
