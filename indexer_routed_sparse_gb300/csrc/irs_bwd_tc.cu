@@ -19,9 +19,9 @@
 // as operands, as the forward rounds P. Each chunk's dK and dV rows are added to the FP32
 // global accumulators with float4 reductions by their own warps while the next chunk's
 // scores are computed; dQ leaves TMEM once, at the end.
-// S^T and dP^T are double-buffered in TMEM and the scores of chunk c+1 are issued before the
-// gradient products of chunk c, so P and dS of the next chunk are formed while the current
-// chunk's dK/dV rows drain.
+// S^T and dP^T are double-buffered in TMEM; the scores of chunk c+1 are issued before the
+// gradient products of chunk c when its rows have landed, so P and dS of the next chunk
+// are formed while the current chunk's dK/dV rows drain.
 // Warps: 0-5 gather, 6 issues the products (TMEM owner), 7..10 form P and dS (one key per
 // thread), 11..14 drain dK/dV (one key per thread) and then dQ (one dim per thread); each
 // group of four covers the four TMEM lane quarters. Waits are bounded; after one gives up,
@@ -327,7 +327,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_bwd_tc_kernel(BwdArgs a) {
       bool alive = mbar_wait(qd_full, 0, abort_flag, a.err) && scores(0);
       for (int c = 0; c < nchunks && alive; ++c) {
         const int st = c & 1;
-        if (c + 1 < nchunks && !scores(c + 1)) break;   // the next chunk's scores first
+        // the next chunk's scores go first only when its rows have already landed: waiting
+        // for them here would hold back this chunk's products, whose completion frees the
+        // stage the chunk after next is gathered into
+        const bool early = c + 1 < nchunks && mbar_test(&kv_full[(c + 1) & 1], ((c + 1) >> 1) & 1);
+        if (early && !scores(c + 1)) break;
         // P / dS set pb of chunk c (use c / npb of that set)
         const int pb = c % L.npb, pu = c / L.npb;
         const uint32_t ptb = ptb0 + (uint32_t)pb * L.pbuf_bytes, dstb = dstb0 + (uint32_t)pb * L.pbuf_bytes;
@@ -349,6 +353,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_bwd_tc_kernel(BwdArgs a) {
         umma_commit(&kv_empty[st]);
         umma_commit(&p_empty[pb]);
         if (c == nchunks - 1) umma_commit(dq_full);
+        if (c + 1 < nchunks && !early && !scores(c + 1)) break;
       }
       // every product this thread issued completes before the CTA releases tensor memory
       umma_commit(drain);
